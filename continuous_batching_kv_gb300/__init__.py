@@ -1,0 +1,313 @@
+"""Python binding of libkvattn: ubatch attention over a cell-indexed KV cache.
+
+Argument marshalling only.  Every step of the path runs in the native library
+(host C++ for splitting and cell reservation, CUDA kernels for the K/V
+scatter, the mask and attention); this module converts Python lists, numpy
+arrays and torch tensors to the C interface declared in include/kvattn.h and
+raises ``KvError`` for negative return codes.  There is no fallback: if the
+library is missing, importing this package fails.
+
+The functions keep the C names:
+
+    kv_init, kv_free, kv_n_batch, kv_n_ubatch, kv_kv_size, kv_last_error,
+    kv_split_ubatches, kv_split_count, kv_split_ubatch, kv_split_free,
+    kv_prepare_cells, kv_seq_rm, kv_seq_pos_max, kv_cells_read,
+    kv_stream_n_kv, kv_store, ubatch_attention, kv_device_error,
+    kv_device_bytes
+"""
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvattn.so")
+
+KV_OK, KV_NO_SLOT = 0, 1
+KV_E_INVAL, KV_E_BATCH_TOO_LARGE, KV_E_SEQ_RANGE, KV_E_CROSS_STREAM = -1, -2, -3, -4
+KV_E_ORDER, KV_E_STALE, KV_E_CUDA, KV_E_NOMEM, KV_E_NO_DEVICE = -5, -6, -7, -8, -9
+KV_SPLIT_AUTO, KV_SPLIT_SIMPLE, KV_SPLIT_EQUAL, KV_SPLIT_SEQ = 0, 1, 2, 3
+KV_MAX_SEQ, KV_HEAD_DIM = 256, 128
+
+EXPORTS = [
+    "kv_init", "kv_free", "kv_n_batch", "kv_n_ubatch", "kv_kv_size", "kv_last_error",
+    "kv_split_ubatches", "kv_split_count", "kv_split_ubatch", "kv_split_free",
+    "kv_prepare_cells", "kv_seq_rm", "kv_seq_pos_max", "kv_cells_read", "kv_stream_n_kv",
+    "kv_store", "ubatch_attention", "kv_device_error", "kv_device_bytes",
+]
+
+
+class KvError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("kvattn error %d: %s" % (code, msg))
+        self.code = code
+
+
+class kv_params(C.Structure):
+    _fields_ = [("n_ctx", C.c_int32), ("n_batch", C.c_int32), ("n_ubatch", C.c_int32),
+                ("n_seq_max", C.c_int32), ("n_stream", C.c_int32), ("n_layer", C.c_int32),
+                ("n_head", C.c_int32), ("n_head_kv", C.c_int32), ("head_dim", C.c_int32),
+                ("causal", C.c_int32), ("seq_to_stream", C.POINTER(C.c_int32)),
+                ("k_layers", C.POINTER(C.c_void_p)), ("v_layers", C.POINTER(C.c_void_p))]
+
+
+class kv_batch(C.Structure):
+    _fields_ = [("n_tokens", C.c_int32), ("pos", C.POINTER(C.c_int32)),
+                ("n_seq_id", C.POINTER(C.c_int32)),
+                ("seq_id", C.POINTER(C.POINTER(C.c_int32)))]
+
+
+class kv_ubatch_info(C.Structure):
+    _fields_ = [("n_tokens", C.c_int32), ("n_seq_tokens", C.c_int32), ("n_seqs", C.c_int32),
+                ("n_seqs_unq", C.c_int32), ("n_kv", C.c_int32),
+                ("rows", C.POINTER(C.c_int32)), ("pos", C.POINTER(C.c_int32)),
+                ("seq0", C.POINTER(C.c_int32)), ("seq_id_unq", C.POINTER(C.c_int32)),
+                ("streams", C.POINTER(C.c_int32)), ("cells", C.POINTER(C.c_int32))]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libkvattn.so is not built; run "
+                          "`python -m continuous_batching_kv_gb300.build` (needs nvcc)")
+    lib = C.CDLL(LIB_PATH)
+    P = C.c_void_p
+    sig = {
+        "kv_init": (C.c_int, [C.POINTER(kv_params), C.POINTER(P)]),
+        "kv_free": (None, [P]),
+        "kv_n_batch": (C.c_int32, [P]),
+        "kv_n_ubatch": (C.c_int32, [P]),
+        "kv_kv_size": (C.c_int32, [P]),
+        "kv_last_error": (C.c_char_p, [P]),
+        "kv_split_ubatches": (C.c_int, [P, C.POINTER(kv_batch), C.c_int32, C.POINTER(P)]),
+        "kv_split_count": (C.c_int32, [P]),
+        "kv_split_ubatch": (C.c_int, [P, C.c_int32, C.POINTER(kv_ubatch_info)]),
+        "kv_split_free": (None, [P]),
+        "kv_prepare_cells": (C.c_int, [P, P]),
+        "kv_seq_rm": (C.c_int, [P, C.c_int32, C.c_int32, C.c_int32]),
+        "kv_seq_pos_max": (C.c_int32, [P, C.c_int32]),
+        "kv_cells_read": (C.c_int, [P, C.c_int32, C.POINTER(C.c_int32), C.POINTER(C.c_uint64)]),
+        "kv_stream_n_kv": (C.c_int32, [P, C.c_int32]),
+        "kv_store": (C.c_int, [P, P, C.c_int32, C.c_int32, P, P, P]),
+        "ubatch_attention": (C.c_int, [P, P, C.c_int32, C.c_int32, P, P, P, P]),
+        "kv_device_error": (C.c_int, [P]),
+        "kv_device_bytes": (C.c_size_t, [P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def _ptr(x):
+    """Device (or host) address of a torch tensor, or an int address, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(c, rc):
+    if rc < 0:
+        msg = lib.kv_last_error(c).decode() if c else ""
+        raise KvError(rc, msg)
+    return rc
+
+
+class Cache:
+    """Handle returned by kv_init (keeps the marshalled arrays alive)."""
+
+    def __init__(self, ptr, keep):
+        self.ptr = ptr
+        self._keep = keep
+
+    @property
+    def _as_parameter_(self):
+        return self.ptr
+
+
+class Split:
+    """Handle returned by kv_split_ubatches."""
+
+    def __init__(self, ptr, cache):
+        self.ptr = ptr
+        self.cache = cache
+
+    @property
+    def _as_parameter_(self):
+        return self.ptr
+
+
+# ---- lifetime -----------------------------------------------------------------
+
+def kv_init(n_ctx, n_batch=2048, n_ubatch=512, n_seq_max=1, n_stream=1, n_layer=1,
+            n_head=16, n_head_kv=8, head_dim=128, causal=True, seq_to_stream=None,
+            k_layers=None, v_layers=None):
+    """Create a cache.  k_layers / v_layers: lists of device tensors (or
+    addresses), one per layer, each [n_stream * kv_size, n_head_kv * head_dim]
+    fp16; None for a host-only cache."""
+    p = kv_params()
+    p.n_ctx, p.n_batch, p.n_ubatch = n_ctx, n_batch, n_ubatch
+    p.n_seq_max, p.n_stream, p.n_layer = n_seq_max, n_stream, n_layer
+    p.n_head, p.n_head_kv, p.head_dim, p.causal = n_head, n_head_kv, head_dim, int(bool(causal))
+    keep = []
+    if seq_to_stream is not None:
+        arr = (C.c_int32 * len(seq_to_stream))(*seq_to_stream)
+        keep.append(arr)
+        p.seq_to_stream = C.cast(arr, C.POINTER(C.c_int32))
+    if k_layers is not None:
+        ka = (C.c_void_p * len(k_layers))(*[_ptr(t) for t in k_layers])
+        va = (C.c_void_p * len(v_layers))(*[_ptr(t) for t in v_layers])
+        keep += [ka, va, list(k_layers), list(v_layers)]
+        p.k_layers = C.cast(ka, C.POINTER(C.c_void_p))
+        p.v_layers = C.cast(va, C.POINTER(C.c_void_p))
+    out = C.c_void_p()
+    rc = lib.kv_init(C.byref(p), C.byref(out))
+    if rc != 0:
+        raise KvError(rc, "kv_init failed")
+    return Cache(out.value, keep)
+
+
+def kv_free(c):
+    if c.ptr:
+        lib.kv_free(c.ptr)
+        c.ptr = None
+
+
+def kv_n_batch(c):
+    return lib.kv_n_batch(c)
+
+
+def kv_n_ubatch(c):
+    return lib.kv_n_ubatch(c)
+
+
+def kv_kv_size(c):
+    return lib.kv_kv_size(c)
+
+
+def kv_last_error(c):
+    return lib.kv_last_error(c).decode()
+
+
+# ---- host side -------------------------------------------------------------------
+
+def kv_split_ubatches(c, pos, seq_id=None, n_seq_id=None, mode=KV_SPLIT_AUTO, n_tokens=None):
+    """Split a batch.  pos: list / array of positions or None (auto-fill);
+    seq_id: list of id lists (first id first) or None (all sequence 0);
+    n_seq_id: counts, default the lists' lengths (pass False for the C NULL:
+    one id per slot)."""
+    if n_tokens is None:
+        n_tokens = len(pos) if pos is not None else len(seq_id)
+    b = kv_batch()
+    b.n_tokens = n_tokens
+    keep = []
+    if pos is not None:
+        pa = np.ascontiguousarray(np.asarray(pos, dtype=np.int32))
+        keep.append(pa)
+        b.pos = pa.ctypes.data_as(C.POINTER(C.c_int32))
+    if seq_id is not None:
+        rows = []
+        for ids in seq_id:
+            a = (C.c_int32 * max(1, len(ids)))(*ids)
+            rows.append(a)
+        ptrs = (C.POINTER(C.c_int32) * len(rows))(*[C.cast(a, C.POINTER(C.c_int32)) for a in rows])
+        keep += [rows, ptrs]
+        b.seq_id = C.cast(ptrs, C.POINTER(C.POINTER(C.c_int32)))
+        if n_seq_id is None:
+            n_seq_id = [len(ids) for ids in seq_id]
+    if n_seq_id is not None and n_seq_id is not False:
+        na = np.ascontiguousarray(np.asarray(n_seq_id, dtype=np.int32))
+        keep.append(na)
+        b.n_seq_id = na.ctypes.data_as(C.POINTER(C.c_int32))
+    out = C.c_void_p()
+    _check(c, lib.kv_split_ubatches(c, C.byref(b), mode, C.byref(out)))
+    return Split(out.value, c)
+
+
+def kv_split_count(s):
+    return lib.kv_split_count(s)
+
+
+def kv_split_ubatch(s, k):
+    """Ubatch k as a dict of Python ints and numpy arrays (copies)."""
+    info = kv_ubatch_info()
+    rc = lib.kv_split_ubatch(s, k, C.byref(info))
+    if rc != 0:
+        raise KvError(rc, "bad ubatch index")
+    n = info.n_tokens
+
+    def arr(p, m):
+        return np.ctypeslib.as_array(p, shape=(m,)).copy() if p and m else np.zeros(0, np.int32)
+
+    return {"n_tokens": n, "n_seq_tokens": info.n_seq_tokens, "n_seqs": info.n_seqs,
+            "n_seqs_unq": info.n_seqs_unq, "n_kv": info.n_kv,
+            "rows": arr(info.rows, n), "pos": arr(info.pos, n), "seq0": arr(info.seq0, n),
+            "seq_id_unq": arr(info.seq_id_unq, info.n_seqs_unq),
+            "streams": arr(info.streams, n),
+            "cells": arr(info.cells, n) if info.cells else None}
+
+
+def kv_split_free(s):
+    if s.ptr:
+        lib.kv_split_free(s.ptr)
+        s.ptr = None
+
+
+def kv_prepare_cells(c, s):
+    """0 on success, KV_NO_SLOT (1) if the cache is full (cache unchanged)."""
+    return _check(c, lib.kv_prepare_cells(c, s))
+
+
+def kv_seq_rm(c, seq, p0=0, p1=-1):
+    return _check(c, lib.kv_seq_rm(c, seq, p0, p1))
+
+
+def kv_seq_pos_max(c, seq):
+    return lib.kv_seq_pos_max(c, seq)
+
+
+def kv_cells_read(c, stream, n_seq_max):
+    kv_size = lib.kv_kv_size(c)
+    nw = (n_seq_max + 63) // 64
+    pos = np.zeros(kv_size, np.int32)
+    bits = np.zeros(kv_size * nw, np.uint64)
+    _check(c, lib.kv_cells_read(c, stream, pos.ctypes.data_as(C.POINTER(C.c_int32)),
+                                bits.ctypes.data_as(C.POINTER(C.c_uint64))))
+    return pos, bits.reshape(kv_size, nw)
+
+
+def kv_stream_n_kv(c, stream):
+    return _check(c, lib.kv_stream_n_kv(c, stream))
+
+
+# ---- device side ---------------------------------------------------------------------
+
+def kv_store(c, s, ub, layer, k_cur, v_cur, stream=None):
+    return _check(c, lib.kv_store(c, s, ub, layer, _ptr(k_cur), _ptr(v_cur), _stream(stream)))
+
+
+def ubatch_attention(c, s, ub, layer, q, o, mask_out=None, stream=None):
+    return _check(c, lib.ubatch_attention(c, s, ub, layer, _ptr(q), _ptr(o), _ptr(mask_out),
+                                          _stream(stream)))
+
+
+def kv_device_error(c):
+    return _check(c, lib.kv_device_error(c))
+
+
+def kv_device_bytes(c):
+    return lib.kv_device_bytes(c)

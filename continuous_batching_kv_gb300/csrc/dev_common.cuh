@@ -1,0 +1,125 @@
+// Device helpers shared by the kvattn kernels: the visibility rule, mbarrier
+// and TMA wrappers (inline PTX for sm_103a), bounded waits, error reporting.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace kvd {
+
+// Device error codes written to the cache's error word.
+enum : int32_t {
+    DERR_NONE = 0,
+    DERR_TMA_TIMEOUT = 1,     // an mbarrier wait for a TMA load gave up
+    DERR_MMA_TIMEOUT = 2,     // an mbarrier wait for a tensor-core commit gave up
+    DERR_BOUNDS = 3,          // an index check failed
+    DERR_TMEM = 4,            // TMEM allocation returned an unusable address
+};
+
+// A bounded wait gives up after this many SM clock cycles (~1 s at 2 GHz).
+constexpr long long WAIT_LIMIT_CYCLES = 2000000000ll;
+
+__device__ __forceinline__ void report(int32_t *err, int32_t code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// Everything a kernel needs to decide whether row i sees cell j.
+// "llama.cpp and the ubatch", "The mask is doing the work": the cell must be
+// occupied, hold the row's first sequence id, and (causal) not be later than
+// the row.  Cells reserved by later ubatches of the same batch carry a larger
+// epoch and are not visible yet ("Batch、Ubatch 与解码主循环", Part D).
+struct CellView {
+    const int32_t *pos;       // [n_cells]
+    const uint32_t *epoch;    // [n_cells]
+    const uint64_t *bits;     // [n_cells * n_words]
+    int32_t n_words;
+    uint32_t ub_epoch;
+    int32_t causal;
+};
+
+// Sequence-membership and epoch part of the rule (same for every row of a
+// block, since a block shares its first sequence id).
+__device__ __forceinline__ bool cell_has_seq(const CellView &cv, int64_t g, int32_t seq0) {
+    uint64_t w = cv.bits[g * cv.n_words + (seq0 >> 6)];
+    return ((w >> (seq0 & 63)) & 1ull) && cv.epoch[g] <= cv.ub_epoch;
+}
+
+__device__ __forceinline__ bool row_sees(const CellView &cv, int32_t cell_pos, int32_t row_pos) {
+    return !cv.causal || cell_pos <= row_pos;
+}
+
+// ---- shared-memory addresses ---------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier -----------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete; false if the wait gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > WAIT_LIMIT_CYCLES) return false;
+    }
+    return true;
+}
+
+// ---- TMA ------------------------------------------------------------------------
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+// 2-D tiled load of box (x, y) into shared memory, completing on `bar`.
+// x (the innermost coordinate) must be a multiple of 8 for 16-bit data.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, int32_t x, int32_t y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y),
+          "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a tile
+// written by TMA with 128-byte swizzling (rows of 128 bytes, 1024-byte atoms).
+__device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk) {
+    return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+}  // namespace kvd

@@ -1,0 +1,383 @@
+// Device half of libkvattn: workspace, TMA descriptors, the cell-mirror
+// upload, and the two device entry points kv_store and ubatch_attention.
+//
+// "Batch、Ubatch 与解码主循环", Part F: after the batch is split and cells are
+// reserved, each ubatch runs in order; inside it every layer stores its K/V
+// rows and attends.  The host owns the cell metadata; the device keeps a
+// mirror (position, sequence bitset, reserving-ubatch serial per cell) that
+// is brought up to date, from a list of changed cells, at the first device
+// call after each reservation or removal.
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+
+#include <cudaTypedefs.h>
+
+#include "dev_common.cuh"
+#include "kernels.h"
+
+namespace kvi {
+
+struct DeviceState {
+    int device = 0;
+    int n_sm = 148;
+    // cell mirror
+    int32_t *d_pos = nullptr;
+    uint32_t *d_epoch = nullptr;
+    uint64_t *d_bits = nullptr;
+    // uploads
+    Delta *d_delta = nullptr;
+    int32_t delta_cap = 0;
+    uint8_t *d_tables = nullptr;
+    size_t tables_cap = 0;
+    uint8_t *h_stage = nullptr;
+    size_t stage_cap = 0;
+    cudaEvent_t stage_ev = nullptr;
+    bool stage_pending = false;
+    // attention plan and split-K scratch
+    kvk::Plan plan{};
+    int32_t max_blocks = 0;
+    int32_t gx_dec = 1, gx_pf = 1, dec_target = 1, pf_target = 1;
+    float *d_part_dec = nullptr;
+    float *d_part_pf = nullptr;
+    int32_t *d_err = nullptr;
+    // one TMA descriptor per K / V tensor
+    std::vector<CUtensorMap> tm_k, tm_v;
+    uint64_t plan_split = 0;
+    int32_t plan_ub = -1;
+    size_t bytes = 0;
+    std::vector<void *> allocs;
+};
+
+}  // namespace kvi
+
+using namespace kvi;
+
+namespace {
+
+constexpr int32_t DEC_PART_FLOATS = DEC_QMAX * 132;
+constexpr int32_t PF_PART_FLOATS = PF_M * 132;
+
+int cuda_fail(kv_cache *c, cudaError_t e, const char *what) {
+    char buf[256];
+    std::snprintf(buf, sizeof buf, "%s: %s", what, cudaGetErrorString(e));
+    return c->set_err(KV_E_CUDA, buf);
+}
+
+template <class T>
+cudaError_t dev_alloc(DeviceState *d, T **p, size_t n) {
+    void *v = nullptr;
+    size_t bytes = std::max<size_t>(n * sizeof(T), 16);
+    cudaError_t e = cudaMalloc(&v, bytes);
+    if (e != cudaSuccess) return e;
+    d->allocs.push_back(v);
+    d->bytes += bytes;
+    *p = static_cast<T *>(v);
+    return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// A K or V tensor as a 2-D fp16 matrix: n_stream*kv_size rows of
+// n_head_kv*128 values; boxes of 64 rows x 64 values, 128-byte swizzle.
+bool make_kv_map(CUtensorMap *m, void *base, int32_t n_head_kv, int64_t n_rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)n_head_kv * 128, (cuuint64_t)n_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)n_head_kv * 128 * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)TILE};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+size_t tables_bound(const kv_cache *c) {
+    const size_t n = (size_t)c->n_batch;
+    const size_t per_ub = 4 * ((size_t)c->prm.n_seq_max + 1) + 6 * 16;
+    return 56 * n + n * per_ub + 4096;
+}
+
+kvk::UbView make_view(const kv_cache *c, const kv_split *sp, int32_t ub) {
+    const DeviceState *d = c->dev;
+    const UbatchHost &u = sp->ub[ub];
+    kvk::UbView v{};
+    v.cell_pos = d->d_pos;
+    v.cell_epoch = d->d_epoch;
+    v.cell_bits = d->d_bits;
+    v.n_words = c->n_words;
+    v.ub_epoch = u.epoch;
+    v.causal = c->prm.causal;
+    v.kv_size = c->kv_size;
+    v.n_kv = u.n_kv;
+    v.n_tokens = u.n_tokens;
+    v.n_blocks = (int32_t)u.blocks.size();
+    v.n_dec_blocks = u.n_dec_blocks;
+    v.rows = reinterpret_cast<const DevRow *>(d->d_tables + sp->off_rows[ub]);
+    v.perm = reinterpret_cast<const int32_t *>(d->d_tables + sp->off_perm[ub]);
+    v.blocks = reinterpret_cast<const DevBlock *>(d->d_tables + sp->off_blocks[ub]);
+    v.seq_blk_off = reinterpret_cast<const int32_t *>(d->d_tables + sp->off_seq_off[ub]);
+    v.seq_blk = reinterpret_cast<const int32_t *>(d->d_tables + sp->off_seq_blk[ub]);
+    return v;
+}
+
+// Bring the device mirror and this split's tables up to date (stream-ordered).
+int sync_device(kv_cache *c, const kv_split *sp, cudaStream_t st) {
+    DeviceState *d = c->dev;
+    const bool need_tables = c->dev_tables_split != sp->id;
+    if (!c->pending_reset && c->pending.empty() && !need_tables) return KV_OK;
+    cudaError_t e;
+    if (d->stage_pending) {   // the staging buffer is reused: wait for its last copy
+        e = cudaEventSynchronize(d->stage_ev);
+        if (e != cudaSuccess) return cuda_fail(c, e, "stage event");
+        d->stage_pending = false;
+    }
+    if (c->pending_reset) {
+        const size_t n = (size_t)c->prm.n_ctx;
+        if ((e = cudaMemsetAsync(d->d_pos, 0xff, n * sizeof(int32_t), st)) != cudaSuccess ||
+            (e = cudaMemsetAsync(d->d_epoch, 0, n * sizeof(uint32_t), st)) != cudaSuccess ||
+            (e = cudaMemsetAsync(d->d_bits, 0, n * c->n_words * sizeof(uint64_t), st)) != cudaSuccess)
+            return cuda_fail(c, e, "mirror reset");
+        c->pending_reset = false;
+    }
+    const size_t nd = c->pending.size();
+    const size_t dbytes = nd * sizeof(Delta);
+    const size_t tbytes = need_tables ? sp->image.size() : 0;
+    if (tbytes > d->tables_cap) return c->set_err(KV_E_INVAL, "split tables exceed bound");
+    if (nd > (size_t)d->delta_cap) {   // rare (large removals): grow
+        Delta *nd_buf = nullptr;
+        if ((e = dev_alloc(d, &nd_buf, nd)) != cudaSuccess) return cuda_fail(c, e, "delta grow");
+        d->d_delta = nd_buf;
+        d->delta_cap = (int32_t)nd;
+    }
+    if (dbytes + tbytes > d->stage_cap) {
+        if (d->h_stage) cudaFreeHost(d->h_stage);
+        d->h_stage = nullptr;
+        size_t cap = dbytes + tbytes;
+        if ((e = cudaHostAlloc((void **)&d->h_stage, cap, cudaHostAllocDefault)) != cudaSuccess)
+            return cuda_fail(c, e, "stage grow");
+        d->stage_cap = cap;
+    }
+    if (nd) std::memcpy(d->h_stage, c->pending.data(), dbytes);
+    if (tbytes) std::memcpy(d->h_stage + dbytes, sp->image.data(), tbytes);
+    if (nd) {
+        if ((e = cudaMemcpyAsync(d->d_delta, d->h_stage, dbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+            return cuda_fail(c, e, "delta upload");
+        if ((e = kvk::launch_apply_deltas(d->d_delta, (int32_t)nd, c->n_words, d->d_pos, d->d_epoch,
+                                          d->d_bits, st)) != cudaSuccess)
+            return cuda_fail(c, e, "apply deltas");
+    }
+    if (tbytes) {
+        if ((e = cudaMemcpyAsync(d->d_tables, d->h_stage + dbytes, tbytes, cudaMemcpyHostToDevice, st)) !=
+            cudaSuccess)
+            return cuda_fail(c, e, "table upload");
+        c->dev_tables_split = sp->id;
+        d->plan_split = 0;
+        d->plan_ub = -1;
+    }
+    if ((e = cudaEventRecord(d->stage_ev, st)) != cudaSuccess) return cuda_fail(c, e, "stage record");
+    d->stage_pending = true;
+    c->pending.clear();
+    return KV_OK;
+}
+
+int check_call(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer) {
+    if (!c || !sp || sp->owner != c) return KV_E_INVAL;
+    if (!c->has_device) return c->set_err(KV_E_NO_DEVICE, "host-only cache");
+    if (!sp->prepared) return c->set_err(KV_E_ORDER, "split not prepared");
+    if (sp->rm_gen != c->rm_gen) return c->set_err(KV_E_STALE, "split prepared before a removal");
+    if (ub < 0 || ub >= (int32_t)sp->ub.size()) return c->set_err(KV_E_INVAL, "ubatch index");
+    if (layer < 0 || layer >= c->prm.n_layer) return c->set_err(KV_E_INVAL, "layer index");
+    return KV_OK;
+}
+
+}  // namespace
+
+namespace kvi {
+
+int device_init(kv_cache *c) {
+    DeviceState *d = new (std::nothrow) DeviceState();
+    if (!d) return c->set_err(KV_E_NOMEM, "device state");
+    c->dev = d;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&d->device)) != cudaSuccess) return cuda_fail(c, e, "cudaGetDevice");
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d->device) == cudaSuccess && sms > 0)
+        d->n_sm = sms;
+    const int64_t n_cells = c->prm.n_ctx;
+    if ((e = dev_alloc(d, &d->d_pos, n_cells)) != cudaSuccess ||
+        (e = dev_alloc(d, &d->d_epoch, n_cells)) != cudaSuccess ||
+        (e = dev_alloc(d, &d->d_bits, n_cells * c->n_words)) != cudaSuccess)
+        return cuda_fail(c, e, "mirror alloc");
+    if ((e = cudaMemset(d->d_pos, 0xff, n_cells * sizeof(int32_t))) != cudaSuccess ||
+        (e = cudaMemset(d->d_epoch, 0, n_cells * sizeof(uint32_t))) != cudaSuccess ||
+        (e = cudaMemset(d->d_bits, 0, n_cells * c->n_words * sizeof(uint64_t))) != cudaSuccess)
+        return cuda_fail(c, e, "mirror clear");
+    d->delta_cap = std::max<int32_t>(c->n_batch, 4096);
+    if ((e = dev_alloc(d, &d->d_delta, d->delta_cap)) != cudaSuccess) return cuda_fail(c, e, "delta alloc");
+    d->tables_cap = tables_bound(c);
+    if ((e = dev_alloc(d, &d->d_tables, d->tables_cap)) != cudaSuccess) return cuda_fail(c, e, "table alloc");
+    d->stage_cap = d->tables_cap + (size_t)d->delta_cap * sizeof(Delta);
+    if ((e = cudaHostAlloc((void **)&d->h_stage, d->stage_cap, cudaHostAllocDefault)) != cudaSuccess)
+        return cuda_fail(c, e, "stage alloc");
+    if ((e = cudaEventCreateWithFlags(&d->stage_ev, cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(c, e, "event");
+
+    // plan and split-K scratch
+    const int32_t hkv = c->prm.n_head_kv;
+    d->max_blocks = c->n_ubatch;
+    const int32_t max_pf_blocks = std::max<int32_t>(1, (c->n_ubatch * c->gqa + PF_MIN_QV - 1) / PF_MIN_QV);
+    d->gx_dec = std::max<int32_t>(1, d->n_sm * kvk::decode_ctas_per_sm() / hkv);
+    d->gx_pf = std::max<int32_t>(1, d->n_sm / hkv);
+    d->dec_target = 4 * d->gx_dec;
+    d->pf_target = 4 * d->gx_pf;
+    kvk::Plan &p = d->plan;
+    p.tile_stride = (c->kv_size + TILE - 1) / TILE;
+    p.cap_dec = d->dec_target + d->max_blocks;
+    p.cap_pf = d->pf_target + max_pf_blocks;
+    const size_t fl = (size_t)d->max_blocks * p.tile_stride;
+    if ((e = dev_alloc(d, &p.flags, fl)) != cudaSuccess || (e = dev_alloc(d, &p.tiles, fl)) != cudaSuccess ||
+        (e = dev_alloc(d, &p.counts, d->max_blocks)) != cudaSuccess ||
+        (e = dev_alloc(d, &p.work, (size_t)p.cap_dec + p.cap_pf)) != cudaSuccess ||
+        (e = dev_alloc(d, &p.n_work, 2)) != cudaSuccess ||
+        (e = dev_alloc(d, &p.blk_item0, d->max_blocks)) != cudaSuccess ||
+        (e = dev_alloc(d, &p.blk_nitems, d->max_blocks)) != cudaSuccess ||
+        (e = dev_alloc(d, &p.counters, (size_t)d->max_blocks * hkv)) != cudaSuccess ||
+        (e = dev_alloc(d, &d->d_part_dec, (size_t)p.cap_dec * hkv * DEC_PART_FLOATS)) != cudaSuccess ||
+        (e = dev_alloc(d, &d->d_part_pf, (size_t)p.cap_pf * hkv * PF_PART_FLOATS)) != cudaSuccess ||
+        (e = dev_alloc(d, &d->d_err, 1)) != cudaSuccess)
+        return cuda_fail(c, e, "plan alloc");
+    if ((e = cudaMemset(p.counters, 0, (size_t)d->max_blocks * hkv * sizeof(int32_t))) != cudaSuccess ||
+        (e = cudaMemset(d->d_err, 0, sizeof(int32_t))) != cudaSuccess)
+        return cuda_fail(c, e, "plan clear");
+
+    d->tm_k.resize(c->prm.n_layer);
+    d->tm_v.resize(c->prm.n_layer);
+    const int64_t rows = (int64_t)c->prm.n_stream * c->kv_size;
+    for (int32_t l = 0; l < c->prm.n_layer; ++l) {
+        if (!make_kv_map(&d->tm_k[l], c->k_layers[l], hkv, rows) ||
+            !make_kv_map(&d->tm_v[l], c->v_layers[l], hkv, rows))
+            return c->set_err(KV_E_CUDA, "cuTensorMapEncodeTiled failed");
+    }
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(c, e, "init sync");
+    return KV_OK;
+}
+
+void device_free(kv_cache *c) {
+    DeviceState *d = c->dev;
+    if (!d) return;
+    if (d->stage_pending && d->stage_ev) cudaEventSynchronize(d->stage_ev);
+    for (void *p : d->allocs) cudaFree(p);
+    if (d->h_stage) cudaFreeHost(d->h_stage);
+    if (d->stage_ev) cudaEventDestroy(d->stage_ev);
+    delete d;
+    c->dev = nullptr;
+}
+
+}  // namespace kvi
+
+extern "C" {
+
+int kv_store(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer, const void *k_cur,
+             const void *v_cur, void *stream) {
+    int rc = check_call(c, sp, ub, layer);
+    if (rc != KV_OK) return rc;
+    if (!k_cur || !v_cur || ((uintptr_t)k_cur & 15) || ((uintptr_t)v_cur & 15))
+        return c->set_err(KV_E_INVAL, "k_cur / v_cur must be 16-byte aligned device pointers");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((rc = sync_device(c, sp, st)) != KV_OK) return rc;
+    const UbatchHost &u = sp->ub[ub];
+    DeviceState *d = c->dev;
+    const DevRow *rows = reinterpret_cast<const DevRow *>(d->d_tables + sp->off_rows[ub]);
+    cudaError_t e = kvk::launch_store(c->k_layers[layer], c->v_layers[layer], k_cur, v_cur, rows, u.n_tokens,
+                                      c->prm.n_head_kv * c->prm.head_dim * 2, (int64_t)c->prm.n_ctx, d->d_err, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "store launch");
+    const_cast<kv_split *>(sp)->stored[layer][ub] = 1;
+    return KV_OK;
+}
+
+int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer, const void *q, float *o,
+                     void *mask_out, void *stream) {
+    int rc = check_call(c, sp, ub, layer);
+    if (rc != KV_OK) return rc;
+    if (!q || !o || ((uintptr_t)q & 15) || ((uintptr_t)o & 15))
+        return c->set_err(KV_E_INVAL, "q / o must be 16-byte aligned device pointers");
+    for (int32_t k = 0; k <= ub; ++k)
+        if (!sp->stored[layer][k]) return c->set_err(KV_E_ORDER, "attention before its K/V were stored");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((rc = sync_device(c, sp, st)) != KV_OK) return rc;
+    DeviceState *d = c->dev;
+    const UbatchHost &u = sp->ub[ub];
+    kvk::UbView v = make_view(c, sp, ub);
+    cudaError_t e;
+    if (d->plan_split != sp->id || d->plan_ub != ub) {
+        kvk::Plan p = d->plan;
+        if ((e = kvk::launch_plan(v, p, c->prm.n_stream, d->dec_target, d->pf_target, st)) != cudaSuccess)
+            return cuda_fail(c, e, "plan launch");
+        d->plan_split = sp->id;
+        d->plan_ub = ub;
+    }
+    if (mask_out) {
+        if ((e = kvk::launch_mask(v, static_cast<uint16_t *>(mask_out), st)) != cudaSuccess)
+            return cuda_fail(c, e, "mask launch");
+    }
+    const float scale_log2 = 1.4426950408889634f / sqrtf((float)c->prm.head_dim);
+    if (u.n_dec_blocks > 0) {
+        kvk::DecodeArgs a{};
+        a.u = v;
+        a.p = d->plan;
+        a.q = static_cast<const __half *>(q);
+        a.o = o;
+        a.part = d->d_part_dec;
+        a.n_head = c->prm.n_head;
+        a.n_head_kv = c->prm.n_head_kv;
+        a.gqa = c->gqa;
+        a.scale_log2 = scale_log2;
+        a.err = d->d_err;
+        if ((e = kvk::launch_decode(&d->tm_k[layer], &d->tm_v[layer], a, d->gx_dec, st)) != cudaSuccess)
+            return cuda_fail(c, e, "decode launch");
+    }
+    if (u.n_pf_blocks > 0) {
+        kvk::PrefillArgs a{};
+        a.u = v;
+        a.p = d->plan;
+        a.q = static_cast<const __half *>(q);
+        a.o = o;
+        a.part = d->d_part_pf;
+        a.n_head = c->prm.n_head;
+        a.n_head_kv = c->prm.n_head_kv;
+        a.gqa = c->gqa;
+        a.scale_log2 = scale_log2;
+        a.err = d->d_err;
+        if ((e = kvk::launch_prefill(&d->tm_k[layer], &d->tm_v[layer], a, d->gx_pf, st)) != cudaSuccess)
+            return cuda_fail(c, e, "prefill launch");
+    }
+    return KV_OK;
+}
+
+int kv_device_error(kv_cache *c) {
+    if (!c || !c->has_device) return KV_E_INVAL;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(c, e, "sync");
+    int32_t v = 0;
+    if ((e = cudaMemcpy(&v, c->dev->d_err, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(c, e, "error word read");
+    if (v) cudaMemset(c->dev->d_err, 0, sizeof(int32_t));
+    return v;
+}
+
+size_t kv_device_bytes(const kv_cache *c) { return (c && c->dev) ? c->dev->bytes : 0; }
+
+}  // extern "C"

@@ -1,0 +1,216 @@
+// K2: the KQ-mask builder.
+//
+// "llama.cpp and the ubatch", "The mask is doing the work": row i sees cell j
+// iff the cell is occupied, holds seq_id[i][0], and (causal) pos_j <= pos_i;
+// everything else is -inf before the softmax.  The mask is built on the
+// device from the cell mirror (position, sequence bitset, and the serial of
+// the ubatch that reserved the cell), once per ubatch, and reused by every
+// layer.  Two products:
+//   * the attention plan -- for every block of rows (rows sharing a stream and
+//     a first sequence id) and every 64-cell tile: how many (row, cell) pairs
+//     are visible and which 8-cell groups hold one; then each block's list of
+//     tiles with anything visible, and the split-K work items over those
+//     lists.  Attention reads K/V only for listed tiles and skips the per-cell
+//     test on tiles that are fully visible.
+//   * on request, the dense additive F16 mask [n_tokens][n_kv]: 0x0000
+//     visible, 0xFC00 (-inf) masked, column j = cell j of the row's stream.
+
+#include "dev_common.cuh"
+#include "kernels.h"
+
+namespace {
+
+using kvi::TILE;
+using kvi::SUB;
+
+// Rows of block b that see a cell at position cpos (sequence and epoch
+// already checked).
+__device__ __forceinline__ int32_t rows_seeing(const kvk::UbView &u, const kvi::DevBlock &b,
+                                               int32_t cpos) {
+    if (!u.causal || cpos <= b.pos_min) return b.n_rows;
+    if (cpos > b.pos_max) return 0;
+    int32_t n = 0;
+    for (int32_t k = 0; k < b.n_rows; ++k) n += (cpos <= u.rows[u.perm[b.row0 + k]].pos) ? 1 : 0;
+    return n;
+}
+
+// One CTA per (64-cell tile, stream).  Shared counters per block, then one
+// plain store per (block of this stream, tile): no global atomics and no
+// separate clearing pass.
+__global__ void __launch_bounds__(TILE) k_plan_tiles(kvk::UbView u, kvk::Plan p) {
+    extern __shared__ uint32_t sh[];
+    uint32_t *cnt = sh;                 // [n_blocks]
+    uint32_t *sub = sh + u.n_blocks;    // [n_blocks]
+    const int32_t t = blockIdx.x;
+    const int32_t s = blockIdx.y;
+    for (int32_t b = threadIdx.x; b < u.n_blocks; b += blockDim.x) { cnt[b] = 0; sub[b] = 0; }
+    __syncthreads();
+    const int32_t j = t * TILE + threadIdx.x;
+    if (j < u.n_kv) {
+        const int64_t g = (int64_t)s * u.kv_size + j;
+        if (u.cell_epoch[g] <= u.ub_epoch) {
+            const int32_t cpos = u.cell_pos[g];
+            for (int32_t w = 0; w < u.n_words; ++w) {
+                uint64_t bits = u.cell_bits[g * u.n_words + w];
+                while (bits) {
+                    const int32_t q = w * 64 + __ffsll((long long)bits) - 1;
+                    bits &= bits - 1;
+                    for (int32_t k = u.seq_blk_off[q]; k < u.seq_blk_off[q + 1]; ++k) {
+                        const int32_t bi = u.seq_blk[k];
+                        const int32_t n = rows_seeing(u, u.blocks[bi], cpos);
+                        if (n) {
+                            atomicAdd(&cnt[bi], (uint32_t)n);
+                            atomicOr(&sub[bi], 1u << (threadIdx.x / SUB));
+                        }
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    for (int32_t b = threadIdx.x; b < u.n_blocks; b += blockDim.x) {
+        if (u.blocks[b].stream == s)
+            p.flags[(int64_t)b * p.tile_stride + t] = cnt[b] | (sub[b] << 16);
+    }
+}
+
+// One CTA per block: ordered list of the tiles with any visible pair.
+__global__ void __launch_bounds__(256) k_plan_compact(kvk::UbView u, kvk::Plan p, int32_t n_tiles) {
+    __shared__ int32_t warp_sum[8];
+    __shared__ int32_t base;
+    const int32_t b = blockIdx.x;
+    const uint32_t *f = p.flags + (int64_t)b * p.tile_stride;
+    int32_t *out = p.tiles + (int64_t)b * p.tile_stride;
+    if (threadIdx.x == 0) base = 0;
+    __syncthreads();
+    const int32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int32_t a = 0; a < n_tiles; a += blockDim.x) {
+        const int32_t t = a + threadIdx.x;
+        const bool nz = t < n_tiles && f[t] != 0;
+        const uint32_t bal = __ballot_sync(0xffffffffu, nz);
+        const int32_t before = __popc(bal & ((1u << lane) - 1u));
+        if (lane == 0) warp_sum[warp] = __popc(bal);
+        __syncthreads();
+        int32_t off = base;
+        for (int32_t w = 0; w < warp; ++w) off += warp_sum[w];
+        if (nz) out[off + before] = t;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int32_t tot = 0;
+            for (int32_t w = 0; w < (int32_t)(blockDim.x >> 5); ++w) tot += warp_sum[w];
+            base += tot;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) p.counts[b] = base;
+}
+
+// One CTA: cut the tile lists into split-K work items.  Decode lists are cut
+// into chunks of cdec entries, prefill lists into chunks of 2*cpf entries
+// (the prefill kernel consumes entries in pairs).  A block with an empty list
+// still gets one item, which writes zeros.
+__global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, int32_t dec_target,
+                                                     int32_t pf_target) {
+    __shared__ unsigned long long tot[2];
+    __shared__ int32_t csz[2];
+    __shared__ int32_t run[2];
+    __shared__ int32_t scan[1024];
+    if (threadIdx.x < 2) { tot[threadIdx.x] = 0; run[threadIdx.x] = 0; }
+    __syncthreads();
+    for (int32_t b = threadIdx.x; b < u.n_blocks; b += blockDim.x) {
+        const bool pf = b >= u.n_dec_blocks;
+        const int32_t c = p.counts[b];
+        atomicAdd(&tot[pf ? 1 : 0], (unsigned long long)(pf ? (c + 1) / 2 : c));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const long long td = (long long)tot[0], tp = (long long)tot[1];
+        csz[0] = (int32_t)max(1ll, (td + dec_target - 1) / max(1, dec_target));
+        csz[1] = (int32_t)max(1ll, (tp + pf_target - 1) / max(1, pf_target));
+    }
+    __syncthreads();
+    // two passes: decode blocks [0, n_dec), prefill blocks [n_dec, n_blocks)
+    for (int32_t pass = 0; pass < 2; ++pass) {
+        const int32_t lo = pass == 0 ? 0 : u.n_dec_blocks;
+        const int32_t hi = pass == 0 ? u.n_dec_blocks : u.n_blocks;
+        const int32_t step = pass == 0 ? csz[0] : 2 * csz[1];
+        const int32_t item_base = pass == 0 ? 0 : p.cap_dec;
+        const int32_t cap = pass == 0 ? p.cap_dec : p.cap_pf;
+        for (int32_t a = lo; a < hi; a += blockDim.x) {
+            const int32_t b = a + threadIdx.x;
+            int32_t n = 0;
+            if (b < hi) n = max(1, (p.counts[b] + step - 1) / step);
+            scan[threadIdx.x] = n;
+            __syncthreads();
+            for (int32_t d = 1; d < (int32_t)blockDim.x; d <<= 1) {   // inclusive scan
+                int32_t v = threadIdx.x >= d ? scan[threadIdx.x - d] : 0;
+                __syncthreads();
+                scan[threadIdx.x] += v;
+                __syncthreads();
+            }
+            const int32_t first = run[pass] + scan[threadIdx.x] - n;
+            if (b < hi) {
+                p.blk_item0[b] = item_base + first;
+                p.blk_nitems[b] = n;
+                const int32_t cnt = p.counts[b];
+                for (int32_t k = 0; k < n; ++k) {
+                    const int32_t idx = first + k;
+                    if (idx < cap) {
+                        kvk::WorkItem w;
+                        w.block = b;
+                        w.t0 = min(cnt, k * step);
+                        w.t1 = min(cnt, (k + 1) * step);
+                        w.chunk = k;
+                        p.work[item_base + idx] = w;
+                    }
+                }
+            }
+            __syncthreads();
+            if (threadIdx.x == blockDim.x - 1) run[pass] += scan[threadIdx.x];
+            __syncthreads();
+        }
+        if (threadIdx.x == 0) p.n_work[pass] = min(run[pass], cap);
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(256) k_mask(kvk::UbView u, uint16_t *mask) {
+    const int32_t i = blockIdx.y;
+    const int32_t j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= u.n_kv) return;
+    const kvi::DevRow r = u.rows[i];
+    const int64_t g = (int64_t)r.stream * u.kv_size + j;
+    bool vis = u.cell_epoch[g] <= u.ub_epoch;
+    if (vis) {
+        const uint64_t w = u.cell_bits[g * u.n_words + (r.seq0 >> 6)];
+        vis = (w >> (r.seq0 & 63)) & 1ull;
+    }
+    if (vis && u.causal) vis = u.cell_pos[g] <= r.pos;
+    mask[(int64_t)i * u.n_kv + j] = vis ? (uint16_t)0x0000 : (uint16_t)0xFC00;
+}
+
+}  // namespace
+
+namespace kvk {
+
+cudaError_t launch_plan(const UbView &u, const Plan &p, int32_t n_stream, int32_t dec_target,
+                        int32_t pf_target, cudaStream_t st) {
+    const int32_t n_tiles = (u.n_kv + TILE - 1) / TILE;
+    const size_t sh = (size_t)u.n_blocks * 2 * sizeof(uint32_t);
+    if (sh > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k_plan_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)sh);
+        if (e != cudaSuccess) return e;
+    }
+    k_plan_tiles<<<dim3(n_tiles, n_stream), TILE, sh, st>>>(u, p);
+    k_plan_compact<<<u.n_blocks, 256, 0, st>>>(u, p, n_tiles);
+    k_plan_work<<<1, 1024, 0, st>>>(u, p, dec_target, pf_target);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mask(const UbView &u, uint16_t *mask, cudaStream_t st) {
+    k_mask<<<dim3((u.n_kv + 255) / 256, u.n_tokens), 256, 0, st>>>(u, mask);
+    return cudaGetLastError();
+}
+
+}  // namespace kvk

@@ -1,0 +1,73 @@
+// K1: the K/V scatter (set_rows) and the cell-mirror delta apply.
+//
+// "What does llama.cpp's KV cache actually look like in memory?", sections
+// "One row, one token's keys" and "The tensor's three dimensions": a layer's
+// K tensor is rows of n_head_kv * head_dim fp16 values, one row per cell,
+// streams stacked as slabs of kv_size rows; V has the same layout.  Each
+// ubatch row's K (V) values go to the row of its reserved cell.
+
+#include "dev_common.cuh"
+#include "kernels.h"
+
+namespace {
+
+// One 16-byte chunk per thread; consecutive threads cover consecutive chunks
+// of one row, so loads and stores are fully coalesced 16-byte vectors.
+__global__ void __launch_bounds__(256) k_store(uint4 *__restrict__ kc, uint4 *__restrict__ vc,
+                                               const uint4 *__restrict__ kin,
+                                               const uint4 *__restrict__ vin,
+                                               const kvi::DevRow *__restrict__ rows, int32_t n_tokens,
+                                               int32_t chunks_per_row, int64_t n_cells,
+                                               int32_t *err) {
+    const int64_t total = (int64_t)n_tokens * chunks_per_row;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t r = (int32_t)(t / chunks_per_row);
+        const int32_t c = (int32_t)(t - (int64_t)r * chunks_per_row);
+        const int64_t cell = rows[r].cell;
+        if (cell < 0 || cell >= n_cells) {
+            kvd::report(err, kvd::DERR_BOUNDS);
+            continue;
+        }
+        const int64_t dst = cell * chunks_per_row + c;
+        const uint4 kv = __ldg(kin + t);
+        const uint4 vv = __ldg(vin + t);
+        kc[dst] = kv;
+        vc[dst] = vv;
+    }
+}
+
+__global__ void k_apply_deltas(const kvi::Delta *__restrict__ d, int32_t n, int32_t n_words,
+                               int32_t *pos, uint32_t *epoch, uint64_t *bits) {
+    int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const kvi::Delta r = d[i];
+    pos[r.cell] = r.pos;
+    epoch[r.cell] = r.epoch;
+    for (int32_t w = 0; w < n_words; ++w) bits[(int64_t)r.cell * n_words + w] = r.bits[w];
+}
+
+}  // namespace
+
+namespace kvk {
+
+cudaError_t launch_store(void *k_cache, void *v_cache, const void *k_cur, const void *v_cur,
+                         const kvi::DevRow *rows, int32_t n_tokens, int32_t row_bytes,
+                         int64_t n_cells, int32_t *err, cudaStream_t st) {
+    const int32_t cpr = row_bytes / 16;
+    const int64_t total = (int64_t)n_tokens * cpr;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    k_store<<<(unsigned)blocks, 256, 0, st>>>((uint4 *)k_cache, (uint4 *)v_cache, (const uint4 *)k_cur,
+                                              (const uint4 *)v_cur, rows, n_tokens, cpr, n_cells, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_apply_deltas(const kvi::Delta *d, int32_t n, int32_t n_words, int32_t *pos,
+                                uint32_t *epoch, uint64_t *bits, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    k_apply_deltas<<<(n + 255) / 256, 256, 0, st>>>(d, n, n_words, pos, epoch, bits);
+    return cudaGetLastError();
+}
+
+}  // namespace kvk

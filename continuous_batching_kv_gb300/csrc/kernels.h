@@ -1,0 +1,99 @@
+// Launch interfaces of the kvattn kernels (host side of each .cu file).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace kvk {
+
+// One unit of attention work: tile-list entries [t0, t1) of one block.  The
+// items of a block are consecutive; `chunk` is the item's index among them
+// and also names its split-K partial slot (the item's own index).
+struct WorkItem {
+    int32_t block;
+    int32_t t0;
+    int32_t t1;
+    int32_t chunk;
+};
+
+// Read-only view of one ubatch's planning inputs and the cell mirror.
+struct UbView {
+    const int32_t *cell_pos;      // mirror
+    const uint32_t *cell_epoch;
+    const uint64_t *cell_bits;
+    int32_t n_words;
+    uint32_t ub_epoch;
+    int32_t causal;
+    int32_t kv_size;
+    int32_t n_kv;
+    int32_t n_tokens;
+    int32_t n_blocks;
+    int32_t n_dec_blocks;
+    const kvi::DevRow *rows;      // [n_tokens]
+    const int32_t *perm;          // [n_tokens]
+    const kvi::DevBlock *blocks;  // [n_blocks]
+    const int32_t *seq_blk_off;   // [n_seq_max + 1]
+    const int32_t *seq_blk;       // [n_blocks]
+};
+
+// Attention plan buffers (library-owned device memory).
+struct Plan {
+    uint32_t *flags;        // [max_blocks][tile_stride]: bits 0..15 visible (row, cell)
+                            // pairs in the 64-cell tile, bits 16..23 which 8-cell groups
+                            // hold a visible pair
+    int32_t *tiles;         // [max_blocks][tile_stride] compacted tile lists
+    int32_t *counts;        // [max_blocks]
+    WorkItem *work;         // decode items [0, cap_dec), prefill items [cap_dec, +cap_pf)
+    int32_t *n_work;        // [2] decode / prefill item counts
+    int32_t *blk_item0;     // [max_blocks] first item of each block
+    int32_t *blk_nitems;    // [max_blocks]
+    int32_t *counters;      // [max_blocks * n_head_kv] split-K completion counters
+    int32_t tile_stride;
+    int32_t cap_dec, cap_pf;
+};
+
+// k_store.cu
+cudaError_t launch_store(void *k_cache, void *v_cache, const void *k_cur, const void *v_cur,
+                         const kvi::DevRow *rows, int32_t n_tokens, int32_t row_bytes,
+                         int64_t n_cells, int32_t *err, cudaStream_t st);
+cudaError_t launch_apply_deltas(const kvi::Delta *d, int32_t n, int32_t n_words, int32_t *pos,
+                                uint32_t *epoch, uint64_t *bits, cudaStream_t st);
+
+// k_plan.cu
+cudaError_t launch_plan(const UbView &u, const Plan &p, int32_t n_stream, int32_t dec_target,
+                        int32_t pf_target, cudaStream_t st);
+cudaError_t launch_mask(const UbView &u, uint16_t *mask, cudaStream_t st);
+
+// k_decode.cu
+struct DecodeArgs {
+    UbView u;
+    Plan p;
+    const __half *q;        // [n_tokens][n_head][128]
+    float *o;               // [n_tokens][n_head][128]
+    float *part;            // split-K partials [cap_dec][n_head_kv][DEC_QMAX][2 + 128]
+    int32_t n_head, n_head_kv, gqa;
+    float scale_log2;       // log2(e) / sqrt(head_dim)
+    int32_t *err;
+};
+cudaError_t launch_decode(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const DecodeArgs &a,
+                          int32_t grid_x, cudaStream_t st);
+int32_t decode_ctas_per_sm();
+
+// k_prefill.cu
+struct PrefillArgs {
+    UbView u;
+    Plan p;
+    const __half *q;
+    float *o;
+    float *part;            // [cap_pf][n_head_kv][128][2 + 128]
+    int32_t n_head, n_head_kv, gqa;
+    float scale_log2;
+    int32_t *err;
+};
+cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const PrefillArgs &a,
+                           int32_t grid_x, cudaStream_t st);
+
+}  // namespace kvk
