@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Benchmark: ubatch attention over a cell-indexed KV cache on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+host splitting and cell reservation, then for every ubatch and every layer the
+K/V store and the attention (the mask / attention plan is built once per
+ubatch).  Default workload (configuration 2): a 5000-token single-sequence
+prefill with a Qwen3-0.6B attention shape (16 query heads, 8 KV heads,
+head_dim 128, 28 layers), n_batch 2048, n_ubatch 512 -> 3 decode calls, 10
+ubatches; the step starts from an empty cache.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2|3|4|5]
+                    [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path has no cross-GPU exchange); value = all ranks' tokens / the slowest
+rank's time.  `--impl reference` times the CPU oracle (plain NumPy float64)
+on a bounded sample of the same workload; rank 0 only.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+if "reference" in sys.argv:
+    # the oracle runs single-threaded; BLAS reads these when NumPy loads
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = "1"
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import configs  # noqa: E402
+
+METRIC = "ubatch tokens/s"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# workload bookkeeping (no attention arithmetic: counts only)
+# ---------------------------------------------------------------------------
+
+def measured_tokens(cfg):
+    return sum(len(c["pos"]) for c in cfg["measured"])
+
+
+def row_visible_cells(pos):
+    """Every workload stores positions 0..p of a row's sequence before the
+    row attends, so a causal row at position p sees p + 1 cells."""
+    return np.asarray(pos, dtype=np.int64) + 1
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu):
+        self.proc = None
+        self.gpu = gpu
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class OursArm:
+    def __init__(self, cfg, device):
+        import torch
+        import continuous_batching_kv_gb300 as kv
+        self.torch, self.kv, self.cfg = torch, kv, cfg
+        sh, prm = cfg["shape"], cfg["params"]
+        self.H, self.Hk, self.d, self.L = sh["n_head"], sh["n_head_kv"], sh["head_dim"], sh["n_layer"]
+        self.dev = device
+        width = self.Hk * self.d
+        self.kc = [torch.zeros((prm["n_ctx"], width), dtype=torch.float16, device=device) for _ in range(self.L)]
+        self.vc = [torch.zeros((prm["n_ctx"], width), dtype=torch.float16, device=device) for _ in range(self.L)]
+        self.c = kv.kv_init(n_ctx=prm["n_ctx"], n_batch=prm["n_batch"], n_ubatch=prm["n_ubatch"],
+                            n_seq_max=prm["n_seq_max"], n_stream=prm["n_stream"], n_layer=self.L,
+                            n_head=self.H, n_head_kv=self.Hk, head_dim=self.d,
+                            seq_to_stream=prm.get("seq_to_stream"), k_layers=self.kc, v_layers=self.vc)
+        self.stream = torch.cuda.current_stream(device)
+        self.gen = torch.Generator(device=device)
+        self.gen.manual_seed(1234)
+        self._setup()
+        self._prepare_inputs()
+
+    def _randn(self, *shape):
+        return self.torch.randn(*shape, generator=self.gen, device=self.dev, dtype=self.torch.float32).half()
+
+    def _setup(self):
+        """Fill the cache with the workload's setup calls (untimed)."""
+        kv = self.kv
+        width = self.Hk * self.d
+        for call in self.cfg["setup"]:
+            s = kv.kv_split_ubatches(self.c, call["pos"], call["seq"])
+            assert kv.kv_prepare_cells(self.c, s) == 0
+            for k in range(kv.kv_split_count(s)):
+                n = kv.kv_split_ubatch(s, k)["n_tokens"]
+                for layer in range(self.L):
+                    kk = self._randn(n, width)
+                    vv = self._randn(n, width)
+                    kv.kv_store(self.c, s, k, layer, kk, vv, self.stream)
+            kv.kv_split_free(s)
+        self.torch.cuda.synchronize()
+        self.base_pos_max = {}
+        for call in self.cfg["measured"]:
+            for seqs in call["seq"]:
+                q = seqs[0]
+                self.base_pos_max[q] = kv.kv_seq_pos_max(self.c, q)
+
+    def _prepare_inputs(self):
+        """Per measured call: the marshalled batch, its ubatch shapes, and
+        resident per-(ubatch, layer) Q/K/V/O device tensors."""
+        kv = self.kv
+        self.calls = []
+        self.flops_per_ub = []
+        for call in self.cfg["measured"]:
+            s = kv.kv_split_ubatches(self.c, call["pos"], call["seq"])
+            ubs = []
+            for k in range(kv.kv_split_count(s)):
+                u = kv.kv_split_ubatch(s, k)
+                rows = list(u["rows"])
+                n = len(rows)
+                t = {"n": n,
+                     "q": [self._randn(n, self.H, self.d) for _ in range(self.L)],
+                     "k": [self._randn(n, self.Hk * self.d) for _ in range(self.L)],
+                     "v": [self._randn(n, self.Hk * self.d) for _ in range(self.L)],
+                     "o": self.torch.empty((n, self.H, self.d), dtype=self.torch.float32, device=self.dev),
+                     "pairs": int(row_visible_cells([call["pos"][r] for r in rows]).sum())}
+                ubs.append(t)
+            kv.kv_split_free(s)
+            # the batch is marshalled once; each step re-splits it in the library
+            self.calls.append((call, ubs))
+        self.torch.cuda.synchronize()
+
+    def input_bytes(self):
+        tot = 0
+        for _, ubs in self.calls:
+            for t in ubs:
+                tot += sum(x.numel() * 2 for x in t["q"] + t["k"] + t["v"])
+        return tot
+
+    def reset(self):
+        """Return the cache to its post-setup state."""
+        kv = self.kv
+        if not self.cfg["setup"]:
+            kv.kv_seq_rm(self.c, -1, 0, -1)
+        else:
+            for q, pmax in self.base_pos_max.items():
+                kv.kv_seq_rm(self.c, q, pmax + 1, -1)
+
+    def step(self, timers=None, host=None):
+        """One pass of the whole path.  timers: list to append (start, end)
+        events around attention calls that launch no planning kernels.
+        host: pinned host copies of the inputs (end-to-end mode)."""
+        kv, torch = self.kv, self.torch
+        self.reset()
+        last = []
+        for ci, (call, ubs) in enumerate(self.calls):
+            s = kv.kv_split_ubatches(self.c, call["pos"], call["seq"])
+            assert kv.kv_prepare_cells(self.c, s) == 0
+            for k, t in enumerate(ubs):
+                for layer in range(self.L):
+                    if host is not None:
+                        hq, hk_, hv = host[ci][k][layer]
+                        t["q"][layer].copy_(hq, non_blocking=True)
+                        t["k"][layer].copy_(hk_, non_blocking=True)
+                        t["v"][layer].copy_(hv, non_blocking=True)
+                    kv.kv_store(self.c, s, k, layer, t["k"][layer], t["v"][layer], self.stream)
+                    if timers is not None and layer > 0:
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record(self.stream)
+                        kv.ubatch_attention(self.c, s, k, layer, t["q"][layer], t["o"], None, self.stream)
+                        e1.record(self.stream)
+                        timers.append((e0, e1, t["pairs"]))
+                    else:
+                        kv.ubatch_attention(self.c, s, k, layer, t["q"][layer], t["o"], None, self.stream)
+                if host is not None:
+                    last.append(t["o"].to("cpu", non_blocking=True))
+            kv.kv_split_free(s)
+        return last
+
+
+def run_ours(args, rank, world, device):
+    import torch
+    import continuous_batching_kv_gb300 as kv
+    torch.cuda.set_device(device)
+    cfg = configs.config(args.config)
+    arm = OursArm(cfg, device)
+    hbm, tflops, peak_src = load_peaks()
+    dist = world > 1
+
+    def barrier():
+        if dist:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        arm.step()
+    barrier()
+    clocks = Clocks(device if isinstance(device, int) else torch.cuda.current_device())
+    timers = []
+    launches0 = kv.kv_launch_count(arm.c)
+    clocks.start()
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(arm.stream)
+    for _ in range(args.steps):
+        arm.step(timers=timers)
+    t1.record(arm.stream)
+    barrier()
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    launches = kv.kv_launch_count(arm.c) - launches0
+    assert kv.kv_device_error(arm.c) == 0
+    ms_max = ms_total
+    if dist:
+        tt = torch.tensor([ms_total], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(tt.item())
+    tokens = measured_tokens(cfg) * args.steps * world
+    value = tokens / (ms_max / 1e3)
+
+    # roofline of the dominant kernel (attention), timed live above
+    durs = [a.elapsed_time(b) for a, b, _ in timers]
+    pairs = [p for _, _, p in timers]
+    per_pair_flops = 4 * arm.d * arm.H
+    achieved = (sum(pairs) * per_pair_flops) / (sum(durs) / 1e3) / 1e12 if durs else 0.0
+    roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tflops, "unit": "TFLOP/s",
+            "frac": round(achieved / tflops, 4), "traffic": None,
+            "kernel": "ubatch_attention (k_decode / k_prefill)", "peak_source": peak_src,
+            "launches_timed": len(durs), "avg_launch_us": round(1e3 * sum(durs) / max(1, len(durs)), 2)}
+
+    e2e = None
+    if not args.no_e2e:
+        host = []
+        for ci, (call, ubs) in enumerate(arm.calls):
+            hc = []
+            for t in ubs:
+                hc.append([(t["q"][l].cpu().pin_memory(), t["k"][l].cpu().pin_memory(),
+                            t["v"][l].cpu().pin_memory()) for l in range(arm.L)])
+            host.append(hc)
+        arm.step(host=host)
+        barrier()
+        t0.record(arm.stream)
+        out = None
+        for _ in range(args.steps):
+            out = arm.step(host=host)
+        t1.record(arm.stream)
+        barrier()
+        ms_e2e = t0.elapsed_time(t1)
+        if dist:
+            tt = torch.tensor([ms_e2e], device=device)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            ms_e2e = float(tt.item())
+        e2e = {"value": round(tokens / (ms_e2e / 1e3), 1), "unit": UNIT,
+               "h2d_bytes_per_step": arm.input_bytes(),
+               "d2h_bytes_per_step": int(sum(x.numel() * 4 for x in out))}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16 in, f32 accumulate/out",
+            "data": "synthetic N(0,1) fp16 Q/K/V (seeded); no weights",
+            "config": {"workload": cfg["name"], "config_id": cfg["id"],
+                       "n_layer": arm.L, "n_head": arm.H, "n_head_kv": arm.Hk, "head_dim": arm.d,
+                       "tokens_per_step": measured_tokens(cfg), **{k: v for k, v in cfg["params"].items()
+                                                                    if k != "seq_to_stream"},
+                       "parallelism": "replicas" if world > 1 else "single-gpu",
+                       "l2": "inputs larger than L2 (%.2f GB resident per step)" % (arm.input_bytes() / 1e9)},
+            "roofline": roof, "gpu_launches": int(launches), "clocks": clk, "e2e": e2e}
+    return line, arm
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(cfg, rows_per_ub):
+    """Run the oracle's whole path for one layer on a bounded sample; return
+    (seconds, extrapolated tokens/s, description)."""
+    from oracle.session import OracleKV
+    from workloads import gen
+    sh, prm = cfg["shape"], cfg["params"]
+    H, Hk, d, L = sh["n_head"], sh["n_head_kv"], sh["head_dim"], sh["n_layer"]
+    o = OracleKV(n_ctx=prm["n_ctx"], n_batch=prm["n_batch"], n_ubatch=prm["n_ubatch"],
+                 n_seq_max=prm["n_seq_max"], n_stream=prm["n_stream"], n_layer=1, n_head=H,
+                 n_head_kv=Hk, head_dim=d, seq_to_stream=prm.get("seq_to_stream"))
+    for call in cfg["setup"]:
+        code, sp = o.split(call["pos"], call["seq"], keep_snapshots=False)
+        for k, ub in enumerate(sp.ubatches):
+            pos = [call["pos"][r] for r in ub["rows"]]
+            con = [call["content"][r] for r in ub["rows"]]
+            o.store(sp, k, 0, gen.batch_rows(cfg["id"], 0, 1, pos, con, Hk * d),
+                    gen.batch_rows(cfg["id"], 0, 2, pos, con, Hk * d))
+    t_split = t_store = t_attn = 0.0
+    n_att = 0
+    for call in cfg["measured"]:
+        t = time.perf_counter()
+        code, sp = o.split(call["pos"], call["seq"])
+        t_split += time.perf_counter() - t
+        for k, ub in enumerate(sp.ubatches):
+            rows = ub["rows"]
+            pos = [call["pos"][r] for r in rows]
+            con = [call["content"][r] for r in rows]
+            kk = gen.batch_rows(cfg["id"], 0, 1, pos, con, Hk * d)
+            vv = gen.batch_rows(cfg["id"], 0, 2, pos, con, Hk * d)
+            t = time.perf_counter()
+            o.store(sp, k, 0, kk, vv)
+            t_store += time.perf_counter() - t
+            n = len(rows)
+            sel = list(range(n)) if n <= rows_per_ub else \
+                sorted(set(np.linspace(0, n - 1, rows_per_ub).astype(int).tolist()))
+            q = gen.batch_rows(cfg["id"], 0, 0, pos, con, H * d).reshape(n, H, d)
+            t = time.perf_counter()
+            o.attention(sp, k, 0, q, rows=sel)
+            t_attn += time.perf_counter() - t
+            n_att += len(sel)
+    ntok = measured_tokens(cfg)
+    per_step = t_split + L * (t_store + t_attn * ntok / max(1, n_att))
+    desc = ("oracle (NumPy float64, 1 thread): split+prepare of all %d tokens, 1 of %d layers stored, "
+            "attention for %d of %d rows (<= %d per ubatch); extrapolated to %d layers x %d rows"
+            % (ntok, L, n_att, ntok, rows_per_ub, L, ntok))
+    return t_split + t_store + t_attn, ntok / per_step, desc
+
+
+def cpu_baseline(cfg):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; from workloads import configs; "
+            "s, v, d = bench.oracle_sample(configs.config(%d), %d); print(json.dumps([s, v, d]))"
+            % (ROOT, cfg["id"], 48 if cfg["id"] == 2 else 64))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": "failed: " + r.stderr.strip().splitlines()[-1][:200] if r.stderr else "failed"}
+    secs, val, desc = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": round(val, 2), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
+            "cpu_seconds": round(secs, 2), "host_cores_available": os.cpu_count()}
+
+
+def run_reference(args, cfg):
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    rows = 8
+    for _ in range(args.warmup):
+        oracle_sample(cfg, rows)
+    vals, secs = [], 0.0
+    desc = ""
+    for _ in range(args.steps):
+        s, v, desc = oracle_sample(cfg, rows)
+        vals.append(v)
+        secs += s
+    value = statistics.mean(vals)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic N(0,1) fp16 Q/K/V (seeded); no weights",
+            "config": {"workload": cfg["name"], "config_id": cfg["id"]},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = configs.config(args.config)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, cfg)), flush=True)
+        return
+    import torch
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line, _ = run_ours(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu:
+            line["cpu_baseline"] = cpu_baseline(cfg)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

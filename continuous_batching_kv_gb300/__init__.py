@@ -13,7 +13,7 @@ The functions keep the C names:
     kv_split_ubatches, kv_split_count, kv_split_ubatch, kv_split_free,
     kv_prepare_cells, kv_seq_rm, kv_seq_pos_max, kv_cells_read,
     kv_stream_n_kv, kv_store, ubatch_attention, kv_device_error,
-    kv_device_bytes
+    kv_device_bytes, kv_launch_count
 """
 
 import ctypes as C
@@ -34,7 +34,7 @@ EXPORTS = [
     "kv_init", "kv_free", "kv_n_batch", "kv_n_ubatch", "kv_kv_size", "kv_last_error",
     "kv_split_ubatches", "kv_split_count", "kv_split_ubatch", "kv_split_free",
     "kv_prepare_cells", "kv_seq_rm", "kv_seq_pos_max", "kv_cells_read", "kv_stream_n_kv",
-    "kv_store", "ubatch_attention", "kv_device_error", "kv_device_bytes",
+    "kv_store", "ubatch_attention", "kv_device_error", "kv_device_bytes", "kv_launch_count",
 ]
 
 
@@ -92,6 +92,7 @@ def _load():
         "ubatch_attention": (C.c_int, [P, P, C.c_int32, C.c_int32, P, P, P, P]),
         "kv_device_error": (C.c_int, [P]),
         "kv_device_bytes": (C.c_size_t, [P]),
+        "kv_launch_count": (C.c_uint64, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -311,3 +312,7 @@ def kv_device_error(c):
 
 def kv_device_bytes(c):
     return lib.kv_device_bytes(c)
+
+
+def kv_launch_count(c):
+    return lib.kv_launch_count(c)

@@ -178,6 +178,7 @@ int sync_device(kv_cache *c, const kv_split *sp, cudaStream_t st) {
         if ((e = kvk::launch_apply_deltas(d->d_delta, (int32_t)nd, c->n_words, d->d_pos, d->d_epoch,
                                           d->d_bits, st)) != cudaSuccess)
             return cuda_fail(c, e, "apply deltas");
+        c->launches += 1;
     }
     if (tbytes) {
         if ((e = cudaMemcpyAsync(d->d_tables, d->h_stage + dbytes, tbytes, cudaMemcpyHostToDevice, st)) !=
@@ -304,6 +305,7 @@ int kv_store(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer, const v
     cudaError_t e = kvk::launch_store(c->k_layers[layer], c->v_layers[layer], k_cur, v_cur, rows, u.n_tokens,
                                       c->prm.n_head_kv * c->prm.head_dim * 2, (int64_t)c->prm.n_ctx, d->d_err, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "store launch");
+    c->launches += 1;
     const_cast<kv_split *>(sp)->stored[layer][ub] = 1;
     return KV_OK;
 }
@@ -326,12 +328,14 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
         kvk::Plan p = d->plan;
         if ((e = kvk::launch_plan(v, p, c->prm.n_stream, d->dec_target, d->pf_target, st)) != cudaSuccess)
             return cuda_fail(c, e, "plan launch");
+        c->launches += 3;
         d->plan_split = sp->id;
         d->plan_ub = ub;
     }
     if (mask_out) {
         if ((e = kvk::launch_mask(v, static_cast<uint16_t *>(mask_out), st)) != cudaSuccess)
             return cuda_fail(c, e, "mask launch");
+        c->launches += 1;
     }
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)c->prm.head_dim);
     if (u.n_dec_blocks > 0) {
@@ -348,6 +352,7 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
         a.err = d->d_err;
         if ((e = kvk::launch_decode(&d->tm_k[layer], &d->tm_v[layer], a, d->gx_dec, st)) != cudaSuccess)
             return cuda_fail(c, e, "decode launch");
+        c->launches += 1;
     }
     if (u.n_pf_blocks > 0) {
         kvk::PrefillArgs a{};
@@ -363,6 +368,7 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
         a.err = d->d_err;
         if ((e = kvk::launch_prefill(&d->tm_k[layer], &d->tm_v[layer], a, d->gx_pf, st)) != cudaSuccess)
             return cuda_fail(c, e, "prefill launch");
+        c->launches += 1;
     }
     return KV_OK;
 }
@@ -379,5 +385,7 @@ int kv_device_error(kv_cache *c) {
 }
 
 size_t kv_device_bytes(const kv_cache *c) { return (c && c->dev) ? c->dev->bytes : 0; }
+
+uint64_t kv_launch_count(const kv_cache *c) { return c ? c->launches : 0; }
 
 }  // extern "C"

@@ -118,6 +118,7 @@ struct kv_cache {
     bool pending_reset = false;
     uint64_t dev_tables_split = 0;      // split whose tables are on the device
     kvi::DeviceState *dev = nullptr;
+    uint64_t launches = 0;          // kernels launched (all entry points)
 
     std::string err;
     int set_err(int code, const std::string &msg) { err = msg; return code; }

@@ -289,6 +289,9 @@ int kv_device_error(kv_cache *c);
 /* Bytes of device memory the library allocated for this cache. */
 size_t kv_device_bytes(const kv_cache *c);
 
+/* Number of CUDA kernels this cache has launched so far (all entry points). */
+uint64_t kv_launch_count(const kv_cache *c);
+
 #ifdef __cplusplus
 }
 #endif

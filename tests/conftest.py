@@ -13,6 +13,14 @@ GOLDEN = os.path.join(ROOT, "tests", "golden")
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+    # (re)build libkvattn.so if any source is newer than it; a no-op otherwise.
+    # build.py is loaded by path: importing the package would load the library.
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_kvattn_build", os.path.join(ROOT, "continuous_batching_kv_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
 
 
 def golden(name):

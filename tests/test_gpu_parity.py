@@ -1,0 +1,164 @@
+"""GPU parity: the CUDA path (through the C interface) against the CPU oracle.
+
+Splits, cells and masks bit-exact; attention within max-abs 2e-3 and
+relative L2 1e-2 (fp16 inputs, fp32 accumulation and output).
+"""
+
+import numpy as np
+import pytest
+
+from workloads import configs
+from tests.gpu_util import Pair, sample_rows, check_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import continuous_batching_kv_gb300  # noqa: F401  (fails loudly if the library is missing)
+
+
+def _run(cfg, rows_sample=None, check_mask=False, poison=False, layers=None):
+    p = Pair(cfg, poison=poison)
+    try:
+        for call in cfg["setup"]:
+            p.run_call(call, attend=False)
+        stats = []
+        outs = {}
+        for call in cfg["measured"]:
+            st, o = p.run_call(call, attend=True, rows_sample=rows_sample, check_mask=check_mask,
+                               layers=layers)
+            stats += st
+            outs.update(o)
+        return stats, outs
+    finally:
+        p.close()
+
+
+def test_config1_prompt_then_decode_all_rows_and_masks():
+    stats, _ = _run(configs.config(1), check_mask=True)
+    assert len(stats) == 5
+
+
+def test_config1_nan_poisoned_cache():
+    # unused cells hold NaN: masked cells must contribute nothing at all
+    stats, outs = _run(configs.config(1), check_mask=True, poison=True)
+    assert all(np.isfinite(v).all() for v in outs.values())
+
+
+def test_config2_prefill_5000_sampled_rows():
+    cfg = configs.config(2, n_layer=2)
+    stats, _ = _run(cfg, rows_sample=lambda n: sample_rows(n, 24), check_mask=True, layers=[1])
+    assert len(stats) == 10
+
+
+def test_config3_decode_unified_all_rows():
+    stats, _ = _run(configs.config(3, n_layer=2), check_mask=True)
+    assert len(stats) == 2
+
+
+def test_config4_mixed_prefix_streams_and_twins():
+    cfg = configs.config(4, n_layer=1)
+    stats, outs = _run(cfg, rows_sample=lambda n: sample_rows(n, 40), check_mask=True)
+    assert len(stats) == 7
+    # prefix cells shared by 16 sequences give the same output as duplicated copies
+    for s in range(16):
+        a = outs[((s,), 1280, 0)]
+        b = outs[((s + 16,), 1280, 0)]
+        check_close(a, b.astype(np.float64), "twin %d" % s)
+
+
+def test_config5_full_size_one_layer_sampled():
+    cfg = configs.config(5, n_layer=1)
+    stats, _ = _run(cfg, rows_sample=lambda n: sample_rows(n, 32))
+    assert len(stats) == 1
+
+
+def test_ragged_kv_size_and_streams():
+    # kv_size not a multiple of the 64-cell tile, two streams, prefix sharing
+    cfg = {"id": 7, "name": "ragged", "shape": dict(configs.QWEN, n_layer=1),
+           "params": dict(n_ctx=2 * 100, n_batch=200, n_ubatch=37, n_seq_max=4, n_stream=2,
+                          seq_to_stream=[0, 1, 0, 1]),
+           "setup": [],
+           "measured": [
+               {"pos": list(range(30)), "seq": [[0, 2]] * 30, "content": [0] * 30},
+               {"pos": list(range(30, 97)) + list(range(40)),
+                "seq": [[0]] * 67 + [[1, 3]] * 40, "content": [0] * 67 + [1] * 40},
+               {"pos": [97, 30, 40, 40], "seq": [[0], [2], [1], [3]], "content": [0, 2, 1, 3]},
+           ]}
+    stats, _ = _run(cfg, check_mask=True)
+    assert len(stats) >= 5
+
+
+def test_random_small_batches():
+    rng = np.random.default_rng(5)
+    calls = []
+    nxt = [0, 0, 0]
+    for _ in range(6):
+        n = int(rng.integers(1, 60))
+        pos, seq, con = [], [], []
+        for _ in range(n):
+            q = int(rng.integers(0, 3))
+            pos.append(nxt[q]); seq.append([q]); con.append(q)
+            nxt[q] += 1
+        calls.append({"pos": pos, "seq": seq, "content": con})
+    cfg = {"id": 8, "name": "random", "shape": dict(configs.LLAMA, n_layer=1),
+           "params": dict(n_ctx=512, n_batch=64, n_ubatch=24, n_seq_max=3, n_stream=1),
+           "setup": [], "measured": calls}
+    stats, _ = _run(cfg, check_mask=True)
+    assert stats
+
+
+def test_retire_and_reuse_cells():
+    import torch
+    import continuous_batching_kv_gb300 as kv
+    cfg = {"id": 9, "name": "retire", "shape": dict(configs.QWEN, n_layer=1),
+           "params": dict(n_ctx=256, n_batch=256, n_ubatch=64, n_seq_max=4, n_stream=1),
+           "setup": [], "measured": []}
+    p = Pair(cfg)
+    try:
+        p.run_call({"pos": list(range(40)), "seq": [[0]] * 40, "content": [0] * 40})
+        p.run_call({"pos": list(range(30)), "seq": [[1]] * 30, "content": [1] * 30})
+        # retire sequence 0 (ITER: finished sequences release their cache)
+        kv.kv_seq_rm(p.c, 0, 0, -1)
+        p.o.seq_rm(0, 0, -1)
+        st, _ = p.run_call({"pos": list(range(50)), "seq": [[2]] * 50, "content": [2] * 50})
+        assert st
+        st, _ = p.run_call({"pos": [30, 50], "seq": [[1], [2]], "content": [1, 2]})
+        assert st
+    finally:
+        p.close()
+
+
+def test_device_call_errors():
+    import torch
+    import continuous_batching_kv_gb300 as kv
+    k = [torch.zeros((64, 1024), dtype=torch.float16, device="cuda")]
+    v = [torch.zeros((64, 1024), dtype=torch.float16, device="cuda")]
+    c = kv.kv_init(n_ctx=64, n_batch=64, n_ubatch=8, n_layer=1, k_layers=k, v_layers=v)
+    q = torch.zeros((8, 16, 128), dtype=torch.float16, device="cuda")
+    o = torch.zeros((8, 16, 128), dtype=torch.float32, device="cuda")
+    kc = torch.zeros((8, 1024), dtype=torch.float16, device="cuda")
+    s = kv.kv_split_ubatches(c, list(range(16)), [[0]] * 16)
+    with pytest.raises(kv.KvError) as e:
+        kv.kv_store(c, s, 0, 0, kc, kc)
+    assert e.value.code == kv.KV_E_ORDER            # not prepared
+    kv.kv_prepare_cells(c, s)
+    with pytest.raises(kv.KvError) as e:
+        kv.ubatch_attention(c, s, 1, 0, q, o)
+    assert e.value.code == kv.KV_E_ORDER            # ubatches 0..1 not stored
+    kv.kv_store(c, s, 0, 0, kc, kc)
+    kv.kv_store(c, s, 1, 0, kc, kc)
+    kv.ubatch_attention(c, s, 1, 0, q, o)
+    with pytest.raises(kv.KvError) as e:
+        kv.kv_store(c, s, 0, 1, kc, kc)
+    assert e.value.code == kv.KV_E_INVAL            # layer out of range
+    kv.kv_seq_rm(c, 0, 3, -1)
+    with pytest.raises(kv.KvError) as e:
+        kv.ubatch_attention(c, s, 1, 0, q, o)
+    assert e.value.code == kv.KV_E_STALE
+    assert kv.kv_device_error(c) == 0
+    kv.kv_free(c)

@@ -22,7 +22,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def test_library_exports_every_declared_symbol():
     hdr = open(os.path.join(ROOT, "include", "kvattn.h")).read()
-    decl = re.findall(r"^\s*(?:int|void|int32_t|size_t|const char \*)\s*\*?\s*(\w+)\s*\(", hdr, re.M)
+    decl = re.findall(r"^\s*(?:int|void|int32_t|uint64_t|size_t|const char \*)\s*\*?\s*(\w+)\s*\(", hdr, re.M)
     assert len(decl) >= 19
     for name in decl:
         assert hasattr(kv.lib, name), name
