@@ -190,6 +190,7 @@ int sync_device(kv_cache *c, const kv_split *sp, cudaStream_t st) {
     }
     if ((e = cudaEventRecord(d->stage_ev, st)) != cudaSuccess) return cuda_fail(c, e, "stage record");
     d->stage_pending = true;
+    for (const Delta &r : c->pending) c->pending_idx[r.cell] = -1;
     c->pending.clear();
     return KV_OK;
 }

@@ -332,7 +332,15 @@ void push_delta(kv_cache *c, size_t g) {
     d.epoch = cs.epoch[g];
     d.nseq = cs.nseq[g];
     for (int32_t w = 0; w < cs.n_words; ++w) d.bits[w] = cs.bits[g * cs.n_words + w];
-    c->pending.push_back(d);
+    // The device applies all records of one upload in parallel, so a cell
+    // changed twice (freed, then reserved again) keeps only its latest record.
+    int32_t &slot = c->pending_idx[g];
+    if (slot >= 0) {
+        c->pending[slot] = d;
+    } else {
+        slot = (int32_t)c->pending.size();
+        c->pending.push_back(d);
+    }
 }
 
 }  // namespace
@@ -374,6 +382,7 @@ int kv_init(const kv_params *p, kv_cache **out) {
     c->prm.k_layers = c->prm.v_layers = nullptr;
     cells_init(c->cells, p->n_stream, c->kv_size, c->n_words);
     if (p->k_layers) {
+        c->pending_idx.assign((size_t)p->n_ctx, -1);
         c->k_layers.assign(p->k_layers, p->k_layers + p->n_layer);
         c->v_layers.assign(p->v_layers, p->v_layers + p->n_layer);
         for (int32_t l = 0; l < p->n_layer; ++l) {
@@ -601,6 +610,7 @@ int kv_seq_rm(kv_cache *c, int32_t seq, int32_t p0, int32_t p1) {
         c->rm_gen++;
         if (c->has_device && all) {
             // the whole mirror is cleared on the device instead of cell by cell
+            for (const Delta &d : c->pending) c->pending_idx[d.cell] = -1;
             c->pending.clear();
             c->pending_reset = true;
         }

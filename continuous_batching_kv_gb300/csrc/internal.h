@@ -114,7 +114,8 @@ struct kv_cache {
     uint64_t rm_gen = 0;
 
     // device mirror bookkeeping
-    std::vector<kvi::Delta> pending;
+    std::vector<kvi::Delta> pending;     // at most one record per cell (the latest)
+    std::vector<int32_t> pending_idx;    // [n_cells] index into pending, or -1
     bool pending_reset = false;
     uint64_t dev_tables_split = 0;      // split whose tables are on the device
     kvi::DeviceState *dev = nullptr;
