@@ -1,12 +1,526 @@
-// K3b: GQA flash attention, prefill / mixed path on tcgen05 (in progress).
+// K3b: GQA flash attention, prefill / mixed path, on tcgen05 tensor cores.
+//
+// "llama.cpp and the ubatch", "Chunked prefill is the same mechanism": a
+// chunk of U rows against C cached cells is a [U, C+U] score matrix; with the
+// mask of "The mask is doing the work" (occupied, same first sequence id,
+// not later) it is the same softmax(q K^T / sqrt(d) + mask) V as decode, but
+// now a dense contraction worth putting on the tensor cores.
+//
+// Design (sm_103a, one CTA of 192 threads per SM):
+//  * a block = up to 128 query vectors (rows sharing a stream and first
+//    sequence id, times the GQA group) = the 128 TMEM lanes of one MMA tile;
+//    a work item = one block, one KV head, a chunk of the block's list of
+//    visible 64-cell tiles, consumed two at a time (N = 128 cells);
+//  * warp 4 (one thread) streams K and V tiles with TMA (128-byte swizzle)
+//    into a 2-stage ring; warp 5 allocates TMEM and one thread issues
+//    tcgen05.mma: S = Q K^T (M 128, N 128, K 128) into one of two TMEM score
+//    buffers, then O += P V (K = 128 cells, V read MN-major) into a TMEM
+//    accumulator; tcgen05.commit signals the mbarriers;
+//  * warps 0-3 (thread = TMEM lane = query vector) read S with tcgen05.ld,
+//    apply the mask per cell on tiles that are not fully visible, run the
+//    online softmax in base 2, write P (fp16) to shared memory in the
+//    swizzled K-major layout, and rescale O in TMEM only when the running
+//    maximum grew by more than 2^8 (otherwise the stale maximum is kept; the
+//    final normalisation uses the same one);
+//  * cells nobody in the block may see get their V rows zeroed in shared
+//    memory before the PV product (P is 0 there, but 0 * NaN would not be);
+//  * split-K chunks of one block are merged by the last CTA to finish, as in
+//    the decode path; every mbarrier wait is bounded.
+
 #include "dev_common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
+
+namespace {
+
+using kvi::TILE;
+
+constexpr int NT = 192;
+constexpr int M = 128;
+constexpr int HALF = 128 * 128;          // [128 rows][64 fp16], 128-byte rows
+constexpr int TILEB = 2 * HALF;          // 32 KiB
+constexpr int BOX = 64 * 128;            // one TMA box: 64 rows x 64 fp16
+constexpr int STAGES = 2;
+constexpr int OFF_Q = 0;
+constexpr int OFF_P = OFF_Q + TILEB;
+constexpr int OFF_K = OFF_P + TILEB;
+constexpr int OFF_V = OFF_K + STAGES * TILEB;
+constexpr int OFF_AUX = OFF_V + STAGES * TILEB;
+constexpr int PART_STRIDE = 132;
+constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128), S1 [128,256), O [256,384)
+constexpr uint32_t COL_O = 256;
+constexpr float RESCALE_LOG2 = 8.0f;
+
+constexpr uint32_t IDESC_S = tc::idesc_f16(128, 128, 0, 0);
+constexpr uint32_t IDESC_PV = tc::idesc_f16(128, 128, 0, 1);
+
+struct __align__(16) Aux {
+    uint64_t k_full[STAGES], v_full[STAGES], kv_empty[STAGES];
+    uint64_t s_full[2], p_full, pv_done, q_full, spare;
+    uint32_t tmem_base;
+    int32_t fail;
+    int32_t flag;
+    int32_t pad;
+    int32_t cpos[2][128];
+    uint8_t chas[2][128];
+    uint8_t anyvis[2][128];
+};
+
+constexpr size_t SMEM_BYTES = OFF_AUX + sizeof(Aux);
+
+__device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, volatile int32_t *fail) {
+    if (kvd::mbar_try_wait(bar, parity)) return true;
+    long long t0 = clock64();
+    while (!kvd::mbar_try_wait(bar, parity)) {
+        if (*fail) return false;
+        if (clock64() - t0 > kvd::WAIT_LIMIT_CYCLES) {
+            *fail = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+struct ItemInfo {
+    int32_t block, t0, t1, pairs, nitems;
+};
+
+__device__ __forceinline__ ItemInfo item_info(const kvk::PrefillArgs &a, int32_t wi) {
+    const kvk::WorkItem w = a.p.work[a.p.cap_dec + wi];
+    ItemInfo r;
+    r.block = w.block;
+    r.t0 = w.t0;
+    r.t1 = w.t1;
+    r.pairs = (w.t1 - w.t0 + 1) / 2;
+    r.nitems = a.p.blk_nitems[w.block];
+    return r;
+}
+
+__device__ __forceinline__ bool entry_full(const kvk::PrefillArgs &a, const kvi::DevBlock &b, int32_t blk,
+                                           int32_t e, int32_t t1) {
+    if (e >= t1) return false;
+    const int32_t t = a.p.tiles[(int64_t)blk * a.p.tile_stride + e];
+    const uint32_t f = a.p.flags[(int64_t)blk * a.p.tile_stride + t];
+    return (int32_t)(f & 0xffffu) == b.n_rows * TILE;
+}
+
+__global__ void __launch_bounds__(NT, 1)
+k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+          const kvk::PrefillArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    Aux &x = *reinterpret_cast<Aux *>(smem + OFF_AUX);
+    volatile int32_t *fail = &x.fail;
+    const int32_t tid = threadIdx.x;
+    const int32_t warp = tid >> 5;
+    const int32_t hk = blockIdx.y;
+    const int32_t n_work = a.p.n_work[1];
+    const int32_t G = a.gqa;
+    const uint32_t sbase = kvd::smem_u32(smem);
+
+    if ((sbase & 1023u) != 0) {
+        if (tid == 0) kvd::report(a.err, kvd::DERR_BOUNDS);
+        return;
+    }
+    if (tid == 0) {
+        kvd::prefetch_tmap(&tm_k);
+        kvd::prefetch_tmap(&tm_v);
+        for (int s = 0; s < STAGES; ++s) {
+            kvd::mbar_init(&x.k_full[s], 1);
+            kvd::mbar_init(&x.v_full[s], 1);
+            kvd::mbar_init(&x.kv_empty[s], 1);
+        }
+        kvd::mbar_init(&x.s_full[0], 1);
+        kvd::mbar_init(&x.s_full[1], 1);
+        kvd::mbar_init(&x.p_full, 128);
+        kvd::mbar_init(&x.pv_done, 1);
+        kvd::mbar_init(&x.q_full, 128);
+        kvd::mbar_init(&x.spare, 1);
+        x.fail = 0;
+        kvd::fence_mbar_init();
+    }
+    if (warp == 5) {
+        tc::alloc(&x.tmem_base, TMEM_COLS);
+        tc::relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = x.tmem_base;
+
+    if (warp == 4) {
+        // ===================== TMA producer =====================
+        if ((tid & 31) == 0) {
+            int32_t issued = 0;
+            for (int32_t wi = blockIdx.x; wi < n_work && !*fail; wi += gridDim.x) {
+                const ItemInfo it = item_info(a, wi);
+                const kvi::DevBlock b = a.u.blocks[it.block];
+                for (int32_t j = 0; j < it.pairs; ++j) {
+                    const int32_t st = issued % STAGES;
+                    if (issued >= STAGES &&
+                        !wait_or_fail(&x.kv_empty[st], (uint32_t)((issued / STAGES) - 1) & 1u, fail))
+                        break;
+                    int32_t ys[2];
+                    for (int h = 0; h < 2; ++h) {
+                        const int32_t e = it.t0 + 2 * j + h;
+                        if (e < it.t1) {
+                            const int32_t t = a.p.tiles[(int64_t)it.block * a.p.tile_stride + e];
+                            ys[h] = b.stream * a.u.kv_size + t * TILE;
+                        } else {
+                            ys[h] = -TILE;   // entirely out of bounds: TMA writes zeros
+                        }
+                    }
+                    uint8_t *ks = smem + OFF_K + st * TILEB;
+                    uint8_t *vs = smem + OFF_V + st * TILEB;
+                    const int32_t xk = hk * 128;
+                    kvd::fence_proxy_async_smem();
+                    kvd::mbar_arrive_expect_tx(&x.k_full[st], TILEB);
+                    for (int h = 0; h < 2; ++h) {
+                        kvd::tma_load_2d(ks + h * BOX, &tm_k, xk, ys[h], &x.k_full[st]);
+                        kvd::tma_load_2d(ks + HALF + h * BOX, &tm_k, xk + 64, ys[h], &x.k_full[st]);
+                    }
+                    kvd::mbar_arrive_expect_tx(&x.v_full[st], TILEB);
+                    for (int h = 0; h < 2; ++h) {
+                        kvd::tma_load_2d(vs + h * BOX, &tm_v, xk, ys[h], &x.v_full[st]);
+                        kvd::tma_load_2d(vs + HALF + h * BOX, &tm_v, xk + 64, ys[h], &x.v_full[st]);
+                    }
+                    ++issued;
+                }
+            }
+            if (*fail) {
+                // let loads already issued land before the CTA exits
+                for (int32_t k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k) {
+                    (void)kvd::mbar_wait_bounded(&x.k_full[k % STAGES], (uint32_t)(k / STAGES) & 1u);
+                    (void)kvd::mbar_wait_bounded(&x.v_full[k % STAGES], (uint32_t)(k / STAGES) & 1u);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ===================== MMA issuer =====================
+        if ((tid & 31) == 0) {
+            int32_t gidx = 0;          // global pair-tile counter (stage ring)
+            uint32_t n_q = 0, n_p = 0;
+            uint32_t n_s[2] = {0, 0};
+            const uint32_t q_addr = sbase + OFF_Q;
+            const uint32_t p_addr = sbase + OFF_P;
+            auto issue_s = [&](int32_t gi, int32_t buf) {
+                const uint32_t k_addr = sbase + OFF_K + (gi % STAGES) * TILEB;
+                const uint32_t d = tmem + (uint32_t)buf * 128u;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * HALF + (uint32_t)(kk & 3) * 32u;
+                    tc::mma_ss(d, tc::sdesc_sw128(q_addr + off, 16, 1024), tc::sdesc_sw128(k_addr + off, 16, 1024),
+                               IDESC_S, kk > 0 ? 1u : 0u);
+                }
+                tc::commit(&x.s_full[buf]);
+            };
+            for (int32_t wi = blockIdx.x; wi < n_work && !*fail; wi += gridDim.x) {
+                const ItemInfo it = item_info(a, wi);
+                if (it.pairs == 0) continue;
+                if (!wait_or_fail(&x.q_full, n_q & 1u, fail)) break;
+                ++n_q;
+                tc::fence_after();
+                bool ok = true;
+                for (int32_t j = 0; j < 2 && j < it.pairs && ok; ++j) {
+                    const int32_t gi = gidx + j;
+                    ok = wait_or_fail(&x.k_full[gi % STAGES], (uint32_t)(gi / STAGES) & 1u, fail);
+                    if (ok) { tc::fence_after(); issue_s(gi, j & 1); ++n_s[j & 1]; }
+                }
+                for (int32_t j = 0; j < it.pairs && ok; ++j) {
+                    const int32_t gi = gidx + j;
+                    ok = wait_or_fail(&x.p_full, n_p & 1u, fail);
+                    if (!ok) break;
+                    ++n_p;
+                    ok = wait_or_fail(&x.v_full[gi % STAGES], (uint32_t)(gi / STAGES) & 1u, fail);
+                    if (!ok) break;
+                    tc::fence_after();
+                    const uint32_t v_addr = sbase + OFF_V + (gi % STAGES) * TILEB;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t aoff = (uint32_t)(kk >> 2) * HALF + (uint32_t)(kk & 3) * 32u;
+                        const uint32_t boff = (uint32_t)kk * 2048u;
+                        tc::mma_ss(tmem + COL_O, tc::sdesc_sw128(p_addr + aoff, 16, 1024),
+                                   tc::sdesc_sw128(v_addr + boff, HALF, 1024), IDESC_PV,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::commit(&x.pv_done);
+                    tc::commit(&x.kv_empty[gi % STAGES]);
+                    if (j + 2 < it.pairs) {
+                        const int32_t g2 = gi + 2;
+                        ok = wait_or_fail(&x.k_full[g2 % STAGES], (uint32_t)(g2 / STAGES) & 1u, fail);
+                        if (ok) { tc::fence_after(); issue_s(g2, j & 1); ++n_s[j & 1]; }
+                    }
+                }
+                gidx += it.pairs;
+                if (!ok) break;
+            }
+            // all issued MMAs complete before TMEM is released
+            tc::commit(&x.spare);
+            (void)kvd::mbar_wait_bounded(&x.spare, 0);
+        }
+    } else {
+        // ===================== softmax / correction / epilogue (warps 0-3) =====================
+        const int32_t n = tid;                 // TMEM lane = query vector
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        uint32_t n_s[2] = {0, 0};
+        uint32_t n_pv = 0, n_q = 0;
+        int32_t gidx = 0;
+        int32_t mb = 0;                        // metadata double-buffer index
+        for (int32_t wi = blockIdx.x; wi < n_work && !*fail; wi += gridDim.x) {
+            const ItemInfo it = item_info(a, wi);
+            const kvi::DevBlock b = a.u.blocks[it.block];
+            const int32_t nqv = b.n_rows * G;
+            const bool live = n < nqv;
+            int32_t row = 0, h = 0, rpos = 0;
+            if (live) {
+                row = a.u.perm[b.row0 + n / G];
+                h = hk * G + (n % G);
+                rpos = a.u.rows[row].pos;
+            }
+            float *orow = a.o + ((int64_t)row * a.n_head + h) * 128;
+            if (it.pairs == 0) {   // nothing visible: zeros (only item of its block)
+                if (live)
+                    for (int c = 0; c < 128; c += 4) *reinterpret_cast<float4 *>(orow + c) = make_float4(0, 0, 0, 0);
+                continue;
+            }
+            // ---- Q tile: row n, 128-byte swizzle, two d-halves ----
+            {
+                uint8_t *qs = smem + OFF_Q;
+                const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((int64_t)row * a.n_head + h) * 128);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    uint4 v = live ? src[c] : make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(qs + (c >> 3) * HALF + kvd::swz128(n, c & 7)) = v;
+                }
+                kvd::fence_proxy_async_smem();
+                kvd::mbar_arrive(&x.q_full);
+                ++n_q;
+            }
+            float m_run = -INFINITY, l_run = 0.f;
+            bool ok = true;
+            for (int32_t j = 0; j < it.pairs; ++j) {
+                const int32_t gi = gidx + j;
+                const int32_t st = gi % STAGES;
+                const int32_t ea = it.t0 + 2 * j;
+                const bool full = entry_full(a, b, it.block, ea, it.t1) && entry_full(a, b, it.block, ea + 1, it.t1);
+                if (!full) {
+                    // cell metadata: thread t -> cell t of the pair tile
+                    const int32_t e = ea + (n >> 6);
+                    bool has = false;
+                    int32_t cp = 0;
+                    if (e < it.t1) {
+                        const int32_t t = a.p.tiles[(int64_t)it.block * a.p.tile_stride + e];
+                        const int32_t jc = t * TILE + (n & 63);
+                        if (jc < a.u.n_kv) {
+                            const int64_t g = (int64_t)b.stream * a.u.kv_size + jc;
+                            const uint64_t w = a.u.cell_bits[g * a.u.n_words + (b.seq0 >> 6)];
+                            has = ((w >> (b.seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
+                            cp = a.u.cell_pos[g];
+                        }
+                    }
+                    x.chas[mb][n] = has ? 1 : 0;
+                    x.cpos[mb][n] = cp;
+                    x.anyvis[mb][n] = (has && (!a.u.causal || cp <= b.pos_max)) ? 1 : 0;
+                    tc::named_bar(1, 128);
+                }
+                ok = wait_or_fail(&x.s_full[j & 1], n_s[j & 1] & 1u, fail);
+                if (!ok) break;
+                ++n_s[j & 1];
+                tc::fence_after();
+                // ---- S row -> registers, scaled to log2 units, masked ----
+                float s[128];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t r[32];
+                    tc::ld32(lane_base + (uint32_t)(j & 1) * 128u + (uint32_t)q4 * 32u, r);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) s[q4 * 32 + c] = __uint_as_float(r[c]) * a.scale_log2;
+                }
+                float tmax = -INFINITY;
+                if (full) {
+                    if (!live) {
+#pragma unroll
+                        for (int c = 0; c < 128; ++c) s[c] = -INFINITY;
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) {
+                        const bool vis = live && x.chas[mb][c] && (!a.u.causal || x.cpos[mb][c] <= rpos);
+                        s[c] = vis ? s[c] : -INFINITY;
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 128; ++c) tmax = fmaxf(tmax, s[c]);
+                const float m_new = fmaxf(m_run, tmax);
+                const bool grow = m_new > m_run + RESCALE_LOG2 || (m_run == -INFINITY && m_new != -INFINITY);
+                float alpha = 1.f;
+                if (grow) {
+                    alpha = exp2f(m_run - m_new);
+                    m_run = m_new;
+                    l_run *= alpha;
+                }
+                // ---- P = 2^(s - m), row sum ----
+                uint32_t pk[64];
+                float lsum = 0.f;
+#pragma unroll
+                for (int c = 0; c < 128; c += 2) {
+                    float p0 = 0.f, p1 = 0.f;
+                    if (m_run != -INFINITY) {
+                        p0 = exp2f(s[c] - m_run);
+                        p1 = exp2f(s[c + 1] - m_run);
+                    }
+                    lsum += p0 + p1;
+                    __half2 hv = __floats2half2_rn(p0, p1);
+                    pk[c >> 1] = *reinterpret_cast<uint32_t *>(&hv);
+                }
+                l_run += lsum;
+                // ---- P buffer free and O stable once the previous PV finished ----
+                if (j > 0) {
+                    ok = wait_or_fail(&x.pv_done, n_pv & 1u, fail);
+                    if (!ok) break;
+                    ++n_pv;
+                    tc::fence_after();
+                    if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint32_t r[32];
+                            const uint32_t ta = lane_base + COL_O + (uint32_t)q4 * 32u;
+                            tc::ld32(ta, r);
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+                            tc::st32(ta, r);
+                        }
+                        tc::wait_st();
+                    }
+                }
+                // ---- P (fp16) to shared memory, 128-byte swizzled K-major ----
+                {
+                    uint8_t *ps = smem + OFF_P;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                        *reinterpret_cast<uint4 *>(ps + (c >> 3) * HALF + kvd::swz128(n, c & 7)) = v;
+                    }
+                }
+                if (!full) {
+                    // V rows of cells nobody in the block sees: zero (P is 0 there; V may be garbage)
+                    ok = wait_or_fail(&x.v_full[st], (uint32_t)(gi / STAGES) & 1u, fail);
+                    if (!ok) break;
+                    if (!x.anyvis[mb][n]) {
+                        uint8_t *vs = smem + OFF_V + st * TILEB;
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                *reinterpret_cast<uint4 *>(vs + hh * HALF + n * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    mb ^= 1;
+                }
+                kvd::fence_proxy_async_smem();
+                tc::fence_before();
+                kvd::mbar_arrive(&x.p_full);
+            }
+            if (!ok) break;
+            gidx += it.pairs;
+            // ---- epilogue: wait for the last PV, read O ----
+            if (!wait_or_fail(&x.pv_done, n_pv & 1u, fail)) break;
+            ++n_pv;
+            tc::fence_after();
+            float ov[128];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t r[32];
+                tc::ld32(lane_base + COL_O + (uint32_t)q4 * 32u, r);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) ov[q4 * 32 + c] = __uint_as_float(r[c]);
+            }
+            tc::fence_before();
+            if (it.nitems == 1) {
+                if (live) {
+                    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+                    for (int c = 0; c < 128; c += 4)
+                        *reinterpret_cast<float4 *>(orow + c) =
+                            make_float4(ov[c] * inv, ov[c + 1] * inv, ov[c + 2] * inv, ov[c + 3] * inv);
+                }
+            } else {
+                // this item's partial slot is its index among the prefill items
+                float *pp = a.part + (((int64_t)wi * a.n_head_kv + hk) * M + n) * PART_STRIDE;
+                pp[0] = m_run;
+                pp[1] = l_run;
+#pragma unroll
+                for (int c = 0; c < 128; c += 4)
+                    *reinterpret_cast<float4 *>(pp + 4 + c) = make_float4(ov[c], ov[c + 1], ov[c + 2], ov[c + 3]);
+                __threadfence();
+                tc::named_bar(1, 128);
+                if (n == 0) {
+                    const int32_t prev = atomicAdd(&a.p.counters[it.block * a.n_head_kv + hk], 1);
+                    x.flag = (prev == it.nitems - 1) ? 1 : 0;
+                }
+                tc::named_bar(1, 128);
+                if (x.flag) {
+                    __threadfence();
+                    const int32_t first = a.p.blk_item0[it.block] - a.p.cap_dec;
+                    float M_ = -INFINITY;
+                    for (int32_t k = 0; k < it.nitems; ++k)
+                        M_ = fmaxf(M_, __ldcg(a.part + (((int64_t)(first + k) * a.n_head_kv + hk) * M + n) * PART_STRIDE));
+                    float L = 0.f;
+                    float acc[128];
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) acc[c] = 0.f;
+                    if (M_ != -INFINITY) {
+                        for (int32_t k = 0; k < it.nitems; ++k) {
+                            const float *pk2 = a.part + (((int64_t)(first + k) * a.n_head_kv + hk) * M + n) * PART_STRIDE;
+                            const float mk = __ldcg(pk2);
+                            if (mk == -INFINITY) continue;
+                            const float sc = exp2f(mk - M_);
+                            L = fmaf(__ldcg(pk2 + 1), sc, L);
+#pragma unroll
+                            for (int c = 0; c < 128; c += 4) {
+                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(pk2 + 4 + c));
+                                acc[c] = fmaf(v.x, sc, acc[c]);
+                                acc[c + 1] = fmaf(v.y, sc, acc[c + 1]);
+                                acc[c + 2] = fmaf(v.z, sc, acc[c + 2]);
+                                acc[c + 3] = fmaf(v.w, sc, acc[c + 3]);
+                            }
+                        }
+                    }
+                    if (live) {
+                        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+                        for (int c = 0; c < 128; c += 4)
+                            *reinterpret_cast<float4 *>(orow + c) =
+                                make_float4(acc[c] * inv, acc[c + 1] * inv, acc[c + 2] * inv, acc[c + 3] * inv);
+                    }
+                    if (n == 0) a.p.counters[it.block * a.n_head_kv + hk] = 0;
+                }
+            }
+        }
+    }
+
+    tc::fence_before();
+    __syncthreads();
+    if (*fail && tid == 0) kvd::report(a.err, kvd::DERR_MMA_TIMEOUT);
+    if (warp == 5) {
+        tc::fence_after();
+        tc::dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace
 
 namespace kvk {
 
-cudaError_t launch_prefill(const CUtensorMap *, const CUtensorMap *, const PrefillArgs &, int32_t,
-                           cudaStream_t) {
-    return cudaErrorNotSupported;
+cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const PrefillArgs &a,
+                           int32_t grid_x, cudaStream_t st) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    k_prefill<<<dim3(grid_x, a.n_head_kv), NT, SMEM_BYTES, st>>>(*tm_k, *tm_v, a);
+    return cudaGetLastError();
 }
 
 }  // namespace kvk
