@@ -372,6 +372,7 @@ int kv_init(const kv_params *p, kv_cache **out) {
     c->kv_size = p->n_ctx / p->n_stream;
     c->n_words = (p->n_seq_max + 63) / 64;
     c->gqa = p->n_head / p->n_head_kv;
+    c->pf_min_qv = PF_MIN_QV;
     c->seq_to_stream.resize(p->n_seq_max);
     for (int32_t q = 0; q < p->n_seq_max; ++q) {
         int32_t s = p->seq_to_stream ? p->seq_to_stream[q] : q % p->n_stream;

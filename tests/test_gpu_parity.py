@@ -55,6 +55,16 @@ def test_config2_prefill_5000_sampled_rows():
     assert len(stats) == 10
 
 
+def test_config2_nan_poisoned_cache_prefill_path():
+    # the tensor-core path multiplies whole tiles: unused cells (NaN) must
+    # have their V rows cleared before the PV product
+    cfg = configs.config(2, n_layer=1)
+    cfg["measured"] = cfg["measured"][:1]
+    stats, outs = _run(cfg, rows_sample=lambda n: sample_rows(n, 32), poison=True)
+    assert len(stats) == 4
+    assert all(np.isfinite(v).all() for v in outs.values())
+
+
 def test_config3_decode_unified_all_rows():
     stats, _ = _run(configs.config(3, n_layer=2), check_mask=True)
     assert len(stats) == 2
