@@ -38,7 +38,7 @@ struct DeviceState {
     // attention plan and split-K scratch
     kvk::Plan plan{};
     int32_t max_blocks = 0;
-    int32_t gx_dec = 1, gx_pf = 1, dec_target = 1, pf_target = 1;
+    int32_t gx_dec = 1, gx_pf = 1;          // CTA columns of the decode / prefill grids
     float *d_part_dec = nullptr;
     float *d_part_pf = nullptr;
     int32_t *d_err = nullptr;
@@ -243,12 +243,10 @@ int device_init(kv_cache *c) {
     const int32_t max_pf_blocks = std::max<int32_t>(1, (c->n_ubatch * c->gqa + PF_MIN_QV - 1) / PF_MIN_QV);
     d->gx_dec = std::max<int32_t>(1, d->n_sm * kvk::decode_ctas_per_sm() / hkv);
     d->gx_pf = std::max<int32_t>(1, d->n_sm / hkv);
-    d->dec_target = 4 * d->gx_dec;
-    d->pf_target = 4 * d->gx_pf;
     kvk::Plan &p = d->plan;
     p.tile_stride = (c->kv_size + TILE - 1) / TILE;
-    p.cap_dec = d->dec_target + d->max_blocks;
-    p.cap_pf = d->pf_target + max_pf_blocks;
+    p.cap_dec = d->gx_dec + d->max_blocks;
+    p.cap_pf = d->gx_pf + max_pf_blocks;
     const size_t fl = (size_t)d->max_blocks * p.tile_stride;
     if ((e = dev_alloc(d, &p.flags, fl)) != cudaSuccess || (e = dev_alloc(d, &p.tiles, fl)) != cudaSuccess ||
         (e = dev_alloc(d, &p.counts, d->max_blocks)) != cudaSuccess ||
@@ -257,10 +255,12 @@ int device_init(kv_cache *c) {
         (e = dev_alloc(d, &p.blk_item0, d->max_blocks)) != cudaSuccess ||
         (e = dev_alloc(d, &p.blk_nitems, d->max_blocks)) != cudaSuccess ||
         (e = dev_alloc(d, &p.counters, (size_t)d->max_blocks * hkv)) != cudaSuccess ||
+        (e = dev_alloc(d, &p.cta_item0, (size_t)d->gx_dec + d->gx_pf + 2)) != cudaSuccess ||
         (e = dev_alloc(d, &d->d_part_dec, (size_t)p.cap_dec * hkv * DEC_PART_FLOATS)) != cudaSuccess ||
         (e = dev_alloc(d, &d->d_part_pf, (size_t)p.cap_pf * hkv * PF_PART_FLOATS)) != cudaSuccess ||
         (e = dev_alloc(d, &d->d_err, 1)) != cudaSuccess)
         return cuda_fail(c, e, "plan alloc");
+    p.err = d->d_err;
     if ((e = cudaMemset(p.counters, 0, (size_t)d->max_blocks * hkv * sizeof(int32_t))) != cudaSuccess ||
         (e = cudaMemset(d->d_err, 0, sizeof(int32_t))) != cudaSuccess)
         return cuda_fail(c, e, "plan clear");
@@ -327,7 +327,7 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
     cudaError_t e;
     if (d->plan_split != sp->id || d->plan_ub != ub) {
         kvk::Plan p = d->plan;
-        if ((e = kvk::launch_plan(v, p, c->prm.n_stream, d->dec_target, d->pf_target, st)) != cudaSuccess)
+        if ((e = kvk::launch_plan(v, p, c->prm.n_stream, d->gx_dec, d->gx_pf, st)) != cudaSuccess)
             return cuda_fail(c, e, "plan launch");
         c->launches += 3;
         d->plan_split = sp->id;
@@ -362,6 +362,7 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
         a.q = static_cast<const __half *>(q);
         a.o = o;
         a.part = d->d_part_pf;
+        a.gx_dec = d->gx_dec;
         a.n_head = c->prm.n_head;
         a.n_head_kv = c->prm.n_head_kv;
         a.gqa = c->gqa;

@@ -105,71 +105,113 @@ __global__ void __launch_bounds__(256) k_plan_compact(kvk::UbView u, kvk::Plan p
     if (threadIdx.x == 0) p.counts[b] = base;
 }
 
-// One CTA: cut the tile lists into split-K work items.  Decode lists are cut
-// into chunks of cdec entries, prefill lists into chunks of 2*cpf entries
-// (the prefill kernel consumes entries in pairs).  A block with an empty list
-// still gets one item, which writes zeros.
-__global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, int32_t dec_target,
-                                                     int32_t pf_target) {
-    __shared__ unsigned long long tot[2];
-    __shared__ int32_t csz[2];
-    __shared__ int32_t run[2];
-    __shared__ int32_t scan[1024];
-    if (threadIdx.x < 2) { tot[threadIdx.x] = 0; run[threadIdx.x] = 0; }
-    __syncthreads();
-    for (int32_t b = threadIdx.x; b < u.n_blocks; b += blockDim.x) {
-        const bool pf = b >= u.n_dec_blocks;
-        const int32_t c = p.counts[b];
-        atomicAdd(&tot[pf ? 1 : 0], (unsigned long long)(pf ? (c + 1) / 2 : c));
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const long long td = (long long)tot[0], tp = (long long)tot[1];
-        csz[0] = (int32_t)max(1ll, (td + dec_target - 1) / max(1, dec_target));
-        csz[1] = (int32_t)max(1ll, (tp + pf_target - 1) / max(1, pf_target));
-    }
-    __syncthreads();
-    // two passes: decode blocks [0, n_dec), prefill blocks [n_dec, n_blocks)
+// One CTA: cut the tile lists into split-K work items, stream-K style.  Per
+// path (decode blocks first, then prefill blocks) the blocks' lists are laid
+// end to end (decode in tiles, prefill in pairs of tiles) and cut into gx
+// equal slices, one per CTA column of the attention grid; a slice is split at
+// block boundaries into items.  So every CTA gets the same amount of work, a
+// block's items are consecutive, and a block is covered by as few items as
+// the slices allow.  A block with an empty list gets one empty item (its rows
+// see nothing and get zeros).
+__device__ __forceinline__ int64_t slice_start(int64_t x, int64_t U, int64_t gx) { return (x * U) / gx; }
+
+// Largest x with slice_start(x) <= q (U > 0).
+__device__ __forceinline__ int32_t slice_of(int64_t q, int64_t U, int64_t gx) {
+    return (int32_t)(((q + 1) * gx + U - 1) / U - 1);
+}
+
+__global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, int32_t gx_dec, int32_t gx_pf) {
+    __shared__ long long tot;
+    __shared__ long long run_u;
+    __shared__ int32_t run_i;
+    __shared__ long long scan_u[1024];
+    __shared__ int32_t scan_i[1024];
+    const int32_t tid = threadIdx.x;
     for (int32_t pass = 0; pass < 2; ++pass) {
         const int32_t lo = pass == 0 ? 0 : u.n_dec_blocks;
         const int32_t hi = pass == 0 ? u.n_dec_blocks : u.n_blocks;
-        const int32_t step = pass == 0 ? csz[0] : 2 * csz[1];
+        const int64_t gx = pass == 0 ? gx_dec : gx_pf;
         const int32_t item_base = pass == 0 ? 0 : p.cap_dec;
         const int32_t cap = pass == 0 ? p.cap_dec : p.cap_pf;
+        int32_t *cta0 = p.cta_item0 + (pass == 0 ? 0 : gx_dec + 1);
+        if (tid == 0) { tot = 0; run_u = 0; run_i = 0; }
+        __syncthreads();
+        for (int32_t b = lo + tid; b < hi; b += blockDim.x) {
+            const int32_t c = p.counts[b];
+            atomicAdd((unsigned long long *)&tot, (unsigned long long)(pass ? (c + 1) / 2 : c));
+        }
+        __syncthreads();
+        const int64_t U = tot;
         for (int32_t a = lo; a < hi; a += blockDim.x) {
-            const int32_t b = a + threadIdx.x;
-            int32_t n = 0;
-            if (b < hi) n = max(1, (p.counts[b] + step - 1) / step);
-            scan[threadIdx.x] = n;
+            const int32_t b = a + tid;
+            int64_t ub = 0;
+            if (b < hi) ub = pass ? (p.counts[b] + 1) / 2 : p.counts[b];
+            scan_u[tid] = ub;
             __syncthreads();
-            for (int32_t d = 1; d < (int32_t)blockDim.x; d <<= 1) {   // inclusive scan
-                int32_t v = threadIdx.x >= d ? scan[threadIdx.x - d] : 0;
+            for (int32_t d = 1; d < (int32_t)blockDim.x; d <<= 1) {
+                const long long v = tid >= d ? scan_u[tid - d] : 0;
                 __syncthreads();
-                scan[threadIdx.x] += v;
+                scan_u[tid] += v;
                 __syncthreads();
             }
-            const int32_t first = run[pass] + scan[threadIdx.x] - n;
+            const int64_t P = run_u + scan_u[tid] - ub;   // first unit of block b
+            int32_t first = 0, nseg = 0;
             if (b < hi) {
-                p.blk_item0[b] = item_base + first;
-                p.blk_nitems[b] = n;
+                if (ub == 0) {
+                    first = P < U ? slice_of(P, U, gx) : (int32_t)gx - 1;
+                    nseg = 1;
+                } else {
+                    first = slice_of(P, U, gx);
+                    nseg = slice_of(P + ub - 1, U, gx) - first + 1;
+                }
+            }
+            scan_i[tid] = nseg;
+            __syncthreads();
+            for (int32_t d = 1; d < (int32_t)blockDim.x; d <<= 1) {
+                const int32_t v = tid >= d ? scan_i[tid - d] : 0;
+                __syncthreads();
+                scan_i[tid] += v;
+                __syncthreads();
+            }
+            const int32_t ibase = run_i + scan_i[tid] - nseg;
+            if (b < hi) {
+                p.blk_item0[b] = item_base + ibase;
+                p.blk_nitems[b] = nseg;
                 const int32_t cnt = p.counts[b];
-                for (int32_t k = 0; k < n; ++k) {
-                    const int32_t idx = first + k;
-                    if (idx < cap) {
-                        kvk::WorkItem w;
-                        w.block = b;
-                        w.t0 = min(cnt, k * step);
-                        w.t1 = min(cnt, (k + 1) * step);
-                        w.chunk = k;
-                        p.work[item_base + idx] = w;
+                for (int32_t k = 0; k < nseg; ++k) {
+                    const int32_t x = first + k;
+                    int64_t lo_u = 0, hi_u = 0;
+                    if (ub > 0) {
+                        lo_u = max(P, slice_start(x, U, gx)) - P;
+                        hi_u = min(P + ub, slice_start(x + 1, U, gx)) - P;
                     }
+                    kvk::WorkItem w;
+                    w.block = b;
+                    w.t0 = pass ? (int32_t)(2 * lo_u) : (int32_t)lo_u;
+                    w.t1 = pass ? (int32_t)min((int64_t)cnt, 2 * hi_u) : (int32_t)hi_u;
+                    w.cta = x;
+                    const int32_t idx = ibase + k;
+                    if (idx < cap) p.work[item_base + idx] = w;
+                    else kvd::report(p.err, kvd::DERR_BOUNDS);
                 }
             }
             __syncthreads();
-            if (threadIdx.x == blockDim.x - 1) run[pass] += scan[threadIdx.x];
+            if (tid == blockDim.x - 1) { run_u += scan_u[tid]; run_i += scan_i[tid]; }
             __syncthreads();
         }
-        if (threadIdx.x == 0) p.n_work[pass] = min(run[pass], cap);
+        const int32_t n_items = min(run_i, cap);
+        if (tid == 0) p.n_work[pass] = n_items;
+        __syncthreads();   // items written by other threads are visible below
+        // cta0[x] = first item whose slice is >= x; cta0[gx] = n_items
+        for (int32_t i = tid; i < n_items; i += blockDim.x) {
+            const int32_t c = p.work[item_base + i].cta;
+            const int32_t cp = i > 0 ? p.work[item_base + i - 1].cta : -1;
+            for (int32_t x = cp + 1; x <= c; ++x) cta0[x] = i;
+        }
+        if (tid == 0) {
+            const int32_t clast = n_items > 0 ? p.work[item_base + n_items - 1].cta : -1;
+            for (int32_t x = clast + 1; x <= (int32_t)gx; ++x) cta0[x] = n_items;
+        }
         __syncthreads();
     }
 }
@@ -193,8 +235,8 @@ __global__ void __launch_bounds__(256) k_mask(kvk::UbView u, uint16_t *mask) {
 
 namespace kvk {
 
-cudaError_t launch_plan(const UbView &u, const Plan &p, int32_t n_stream, int32_t dec_target,
-                        int32_t pf_target, cudaStream_t st) {
+cudaError_t launch_plan(const UbView &u, const Plan &p, int32_t n_stream, int32_t gx_dec, int32_t gx_pf,
+                        cudaStream_t st) {
     const int32_t n_tiles = (u.n_kv + TILE - 1) / TILE;
     const size_t sh = (size_t)u.n_blocks * 2 * sizeof(uint32_t);
     if (sh > 48 * 1024) {
@@ -204,7 +246,7 @@ cudaError_t launch_plan(const UbView &u, const Plan &p, int32_t n_stream, int32_
     }
     k_plan_tiles<<<dim3(n_tiles, n_stream), TILE, sh, st>>>(u, p);
     k_plan_compact<<<u.n_blocks, 256, 0, st>>>(u, p, n_tiles);
-    k_plan_work<<<1, 1024, 0, st>>>(u, p, dec_target, pf_target);
+    k_plan_work<<<1, 1024, 0, st>>>(u, p, gx_dec, gx_pf);
     return cudaGetLastError();
 }
 

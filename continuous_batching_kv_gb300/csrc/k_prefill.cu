@@ -54,6 +54,19 @@ constexpr float RESCALE_LOG2 = 8.0f;
 constexpr uint32_t IDESC_S = tc::idesc_f16(128, 128, 0, 0);
 constexpr uint32_t IDESC_PV = tc::idesc_f16(128, 128, 0, 1);
 
+struct Meta {                 // per stage: what the producer learned about the pair tile
+    int32_t full;
+    int32_t pad[3];
+    int32_t cpos[128];
+    uint8_t has[128];         // cell holds the block's sequence and is not from a later ubatch
+    uint8_t anyvis[128];      // ... and some row of the block may see it
+};
+
+struct ItemSlot {             // per work item: the query vector behind each TMEM lane
+    int32_t row[M];           // ubatch row, -1 for lanes past the block's query vectors
+    int32_t rpos[M];
+};
+
 struct __align__(16) Aux {
     uint64_t k_full[STAGES], v_full[STAGES], kv_empty[STAGES];
     uint64_t s_full[2], p_full, pv_done, q_full, spare;
@@ -61,9 +74,8 @@ struct __align__(16) Aux {
     int32_t fail;
     int32_t flag;
     int32_t pad;
-    int32_t cpos[2][128];
-    uint8_t chas[2][128];
-    uint8_t anyvis[2][128];
+    Meta meta[STAGES];
+    ItemSlot islot[2];
 };
 
 constexpr size_t SMEM_BYTES = OFF_AUX + sizeof(Aux);
@@ -96,14 +108,6 @@ __device__ __forceinline__ ItemInfo item_info(const kvk::PrefillArgs &a, int32_t
     return r;
 }
 
-__device__ __forceinline__ bool entry_full(const kvk::PrefillArgs &a, const kvi::DevBlock &b, int32_t blk,
-                                           int32_t e, int32_t t1) {
-    if (e >= t1) return false;
-    const int32_t t = a.p.tiles[(int64_t)blk * a.p.tile_stride + e];
-    const uint32_t f = a.p.flags[(int64_t)blk * a.p.tile_stride + t];
-    return (int32_t)(f & 0xffffu) == b.n_rows * TILE;
-}
-
 __global__ void __launch_bounds__(NT, 1)
 k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
           const kvk::PrefillArgs a) {
@@ -113,8 +117,10 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     const int32_t tid = threadIdx.x;
     const int32_t warp = tid >> 5;
     const int32_t hk = blockIdx.y;
-    const int32_t n_work = a.p.n_work[1];
     const int32_t G = a.gqa;
+    const int32_t* c0 = a.p.cta_item0 + a.gx_dec + 1;
+    const int32_t i0 = c0[blockIdx.x];
+    const int32_t i1 = c0[blockIdx.x + 1];
     const uint32_t sbase = kvd::smem_u32(smem);
 
     if ((sbase & 1023u) != 0) {
@@ -125,7 +131,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         kvd::prefetch_tmap(&tm_k);
         kvd::prefetch_tmap(&tm_v);
         for (int s = 0; s < STAGES; ++s) {
-            kvd::mbar_init(&x.k_full[s], 1);
+            kvd::mbar_init(&x.k_full[s], 33);   // lane 0's expect_tx + 32 producer lanes
             kvd::mbar_init(&x.v_full[s], 1);
             kvd::mbar_init(&x.kv_empty[s], 1);
         }
@@ -148,27 +154,49 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     const uint32_t tmem = x.tmem_base;
 
     if (warp == 4) {
-        // ===================== TMA producer =====================
-        if ((tid & 31) == 0) {
-            int32_t issued = 0;
-            for (int32_t wi = blockIdx.x; wi < n_work && !*fail; wi += gridDim.x) {
-                const ItemInfo it = item_info(a, wi);
-                const kvi::DevBlock b = a.u.blocks[it.block];
-                for (int32_t j = 0; j < it.pairs; ++j) {
-                    const int32_t st = issued % STAGES;
-                    if (issued >= STAGES &&
-                        !wait_or_fail(&x.kv_empty[st], (uint32_t)((issued / STAGES) - 1) & 1u, fail))
-                        break;
-                    int32_t ys[2];
-                    for (int h = 0; h < 2; ++h) {
-                        const int32_t e = it.t0 + 2 * j + h;
-                        if (e < it.t1) {
-                            const int32_t t = a.p.tiles[(int64_t)it.block * a.p.tile_stride + e];
-                            ys[h] = b.stream * a.u.kv_size + t * TILE;
-                        } else {
-                            ys[h] = -TILE;   // entirely out of bounds: TMA writes zeros
+        // ===================== producer (whole warp) =====================
+        const int32_t lane = tid & 31;
+        int32_t issued = 0, nonempty = 0;
+        for (int32_t wi = i0; wi < i1 && !*fail; ++wi) {
+            const ItemInfo it = item_info(a, wi);
+            if (it.pairs == 0) continue;
+            const kvi::DevBlock b = a.u.blocks[it.block];
+            const int32_t nqv = b.n_rows * G;
+            ItemSlot &is = x.islot[nonempty & 1];
+            ++nonempty;
+            const int32_t *list = a.p.tiles + (int64_t)it.block * a.p.tile_stride;
+            const uint32_t *flg = a.p.flags + (int64_t)it.block * a.p.tile_stride;
+            for (int32_t j = 0; j < it.pairs; ++j) {
+                const int32_t st = issued % STAGES;
+                if (issued >= STAGES &&
+                    !wait_or_fail(&x.kv_empty[st], (uint32_t)((issued / STAGES) - 1) & 1u, fail))
+                    break;
+                if (j == 0) {
+                    // the item's lane table; the slot's previous reader started two or more
+                    // loads ago, and this load's stage was just released, so it is done with it
+                    for (int32_t n = lane; n < M; n += 32) {
+                        int32_t row = -1, rp = 0;
+                        if (n < nqv) {
+                            row = a.u.perm[b.row0 + n / G];
+                            rp = a.u.rows[row].pos;
                         }
+                        is.row[n] = row;
+                        is.rpos[n] = rp;
                     }
+                }
+                int32_t tt[2];
+                bool fullh[2];
+                for (int h = 0; h < 2; ++h) {
+                    const int32_t e = it.t0 + 2 * j + h;
+                    tt[h] = e < it.t1 ? list[e] : -1;
+                    fullh[h] = tt[h] >= 0 && (int32_t)(flg[tt[h]] & 0xffffu) == b.n_rows * TILE;
+                }
+                const bool full = fullh[0] && fullh[1];
+                Meta &mt = x.meta[st];
+                if (lane == 0) {
+                    int32_t ys[2];
+                    for (int h = 0; h < 2; ++h)   // a missing second tile: out of bounds, TMA writes zeros
+                        ys[h] = tt[h] >= 0 ? b.stream * a.u.kv_size + tt[h] * TILE : -TILE;
                     uint8_t *ks = smem + OFF_K + st * TILEB;
                     uint8_t *vs = smem + OFF_V + st * TILEB;
                     const int32_t xk = hk * 128;
@@ -183,15 +211,39 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         kvd::tma_load_2d(vs + h * BOX, &tm_v, xk, ys[h], &x.v_full[st]);
                         kvd::tma_load_2d(vs + HALF + h * BOX, &tm_v, xk + 64, ys[h], &x.v_full[st]);
                     }
-                    ++issued;
+                    mt.full = full ? 1 : 0;
                 }
+                if (!full) {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int32_t c = lane + 32 * r;
+                        const int32_t t = tt[c >> 6];
+                        bool has = false;
+                        int32_t cp = 0;
+                        if (t >= 0) {
+                            const int32_t jc = t * TILE + (c & 63);
+                            if (jc < a.u.n_kv) {
+                                const int64_t g = (int64_t)b.stream * a.u.kv_size + jc;
+                                const uint64_t w = a.u.cell_bits[g * a.u.n_words + (b.seq0 >> 6)];
+                                has = ((w >> (b.seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
+                                cp = a.u.cell_pos[g];
+                            }
+                        }
+                        mt.has[c] = has ? 1 : 0;
+                        mt.cpos[c] = cp;
+                        mt.anyvis[c] = (has && (!a.u.causal || cp <= b.pos_max)) ? 1 : 0;
+                    }
+                }
+                __syncwarp();
+                kvd::mbar_arrive(&x.k_full[st]);
+                ++issued;
             }
-            if (*fail) {
-                // let loads already issued land before the CTA exits
-                for (int32_t k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k) {
-                    (void)kvd::mbar_wait_bounded(&x.k_full[k % STAGES], (uint32_t)(k / STAGES) & 1u);
-                    (void)kvd::mbar_wait_bounded(&x.v_full[k % STAGES], (uint32_t)(k / STAGES) & 1u);
-                }
+        }
+        if (*fail && lane == 0) {
+            // let loads already issued land before the CTA exits
+            for (int32_t q = issued > STAGES ? issued - STAGES : 0; q < issued; ++q) {
+                (void)kvd::mbar_wait_bounded(&x.k_full[q % STAGES], (uint32_t)(q / STAGES) & 1u);
+                (void)kvd::mbar_wait_bounded(&x.v_full[q % STAGES], (uint32_t)(q / STAGES) & 1u);
             }
         }
     } else if (warp == 5) {
@@ -213,7 +265,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 }
                 tc::commit(&x.s_full[buf]);
             };
-            for (int32_t wi = blockIdx.x; wi < n_work && !*fail; wi += gridDim.x) {
+            for (int32_t wi = i0; wi < i1 && !*fail; ++wi) {
                 const ItemInfo it = item_info(a, wi);
                 if (it.pairs == 0) continue;
                 if (!wait_or_fail(&x.q_full, n_q & 1u, fail)) break;
@@ -262,68 +314,51 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         const int32_t n = tid;                 // TMEM lane = query vector
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         uint32_t n_s[2] = {0, 0};
-        uint32_t n_pv = 0, n_q = 0;
-        int32_t gidx = 0;
-        int32_t mb = 0;                        // metadata double-buffer index
-        for (int32_t wi = blockIdx.x; wi < n_work && !*fail; wi += gridDim.x) {
+        uint32_t n_pv = 0;
+        int32_t k = 0;                         // pair tiles consumed (stage ring position)
+        int32_t nonempty = 0;
+        bool ok = true;
+        for (int32_t wi = i0; wi < i1 && ok && !*fail; ++wi) {
             const ItemInfo it = item_info(a, wi);
-            const kvi::DevBlock b = a.u.blocks[it.block];
-            const int32_t nqv = b.n_rows * G;
-            const bool live = n < nqv;
-            int32_t row = 0, h = 0, rpos = 0;
-            if (live) {
-                row = a.u.perm[b.row0 + n / G];
-                h = hk * G + (n % G);
-                rpos = a.u.rows[row].pos;
-            }
-            float *orow = a.o + ((int64_t)row * a.n_head + h) * 128;
-            if (it.pairs == 0) {   // nothing visible: zeros (only item of its block)
-                if (live)
+            if (it.pairs == 0) {
+                // the block sees no cell at all: zeros (the only item of its block)
+                const kvi::DevBlock b = a.u.blocks[it.block];
+                if (n < b.n_rows * G) {
+                    const int32_t row = a.u.perm[b.row0 + n / G];
+                    float *orow = a.o + ((int64_t)row * a.n_head + hk * G + (n % G)) * 128;
                     for (int c = 0; c < 128; c += 4) *reinterpret_cast<float4 *>(orow + c) = make_float4(0, 0, 0, 0);
+                }
                 continue;
             }
+            // the first pair's arrival also publishes this item's lane table
+            if (!(ok = wait_or_fail(&x.k_full[k % STAGES], (uint32_t)(k / STAGES) & 1u, fail))) break;
+            const ItemSlot &is = x.islot[nonempty & 1];
+            ++nonempty;
+            const int32_t row = is.row[n];
+            const int32_t rpos = is.rpos[n];
+            const bool live = row >= 0;
+            const int32_t h = hk * G + (n % G);
+            float *orow = a.o + ((int64_t)(live ? row : 0) * a.n_head + h) * 128;
             // ---- Q tile: row n, 128-byte swizzle, two d-halves ----
             {
                 uint8_t *qs = smem + OFF_Q;
-                const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((int64_t)row * a.n_head + h) * 128);
+                const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((int64_t)(live ? row : 0) * a.n_head + h) * 128);
+                uint4 qv[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    uint4 v = live ? src[c] : make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4 *>(qs + (c >> 3) * HALF + kvd::swz128(n, c & 7)) = v;
-                }
+                for (int c = 0; c < 16; ++c) qv[c] = live ? src[c] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    *reinterpret_cast<uint4 *>(qs + (c >> 3) * HALF + kvd::swz128(n, c & 7)) = qv[c];
                 kvd::fence_proxy_async_smem();
                 kvd::mbar_arrive(&x.q_full);
-                ++n_q;
             }
             float m_run = -INFINITY, l_run = 0.f;
-            bool ok = true;
-            for (int32_t j = 0; j < it.pairs; ++j) {
-                const int32_t gi = gidx + j;
-                const int32_t st = gi % STAGES;
-                const int32_t ea = it.t0 + 2 * j;
-                const bool full = entry_full(a, b, it.block, ea, it.t1) && entry_full(a, b, it.block, ea + 1, it.t1);
-                if (!full) {
-                    // cell metadata: thread t -> cell t of the pair tile
-                    const int32_t e = ea + (n >> 6);
-                    bool has = false;
-                    int32_t cp = 0;
-                    if (e < it.t1) {
-                        const int32_t t = a.p.tiles[(int64_t)it.block * a.p.tile_stride + e];
-                        const int32_t jc = t * TILE + (n & 63);
-                        if (jc < a.u.n_kv) {
-                            const int64_t g = (int64_t)b.stream * a.u.kv_size + jc;
-                            const uint64_t w = a.u.cell_bits[g * a.u.n_words + (b.seq0 >> 6)];
-                            has = ((w >> (b.seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
-                            cp = a.u.cell_pos[g];
-                        }
-                    }
-                    x.chas[mb][n] = has ? 1 : 0;
-                    x.cpos[mb][n] = cp;
-                    x.anyvis[mb][n] = (has && (!a.u.causal || cp <= b.pos_max)) ? 1 : 0;
-                    tc::named_bar(1, 128);
-                }
-                ok = wait_or_fail(&x.s_full[j & 1], n_s[j & 1] & 1u, fail);
-                if (!ok) break;
+            for (int32_t j = 0; j < it.pairs; ++j, ++k) {
+                const int32_t st = k % STAGES;
+                if (!(ok = wait_or_fail(&x.k_full[st], (uint32_t)(k / STAGES) & 1u, fail))) break;
+                const Meta &mt = x.meta[st];
+                const bool full = mt.full != 0;
+                if (!(ok = wait_or_fail(&x.s_full[j & 1], n_s[j & 1] & 1u, fail))) break;
                 ++n_s[j & 1];
                 tc::fence_after();
                 // ---- S row -> registers, scaled to log2 units, masked ----
@@ -335,7 +370,6 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
 #pragma unroll
                     for (int c = 0; c < 32; ++c) s[q4 * 32 + c] = __uint_as_float(r[c]) * a.scale_log2;
                 }
-                float tmax = -INFINITY;
                 if (full) {
                     if (!live) {
 #pragma unroll
@@ -344,10 +378,11 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 } else {
 #pragma unroll
                     for (int c = 0; c < 128; ++c) {
-                        const bool vis = live && x.chas[mb][c] && (!a.u.causal || x.cpos[mb][c] <= rpos);
+                        const bool vis = live && mt.has[c] && (!a.u.causal || mt.cpos[c] <= rpos);
                         s[c] = vis ? s[c] : -INFINITY;
                     }
                 }
+                float tmax = -INFINITY;
 #pragma unroll
                 for (int c = 0; c < 128; ++c) tmax = fmaxf(tmax, s[c]);
                 const float m_new = fmaxf(m_run, tmax);
@@ -375,8 +410,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 l_run += lsum;
                 // ---- P buffer free and O stable once the previous PV finished ----
                 if (j > 0) {
-                    ok = wait_or_fail(&x.pv_done, n_pv & 1u, fail);
-                    if (!ok) break;
+                    if (!(ok = wait_or_fail(&x.pv_done, n_pv & 1u, fail))) break;
                     ++n_pv;
                     tc::fence_after();
                     if (__any_sync(0xffffffffu, grow)) {
@@ -403,9 +437,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 }
                 if (!full) {
                     // V rows of cells nobody in the block sees: zero (P is 0 there; V may be garbage)
-                    ok = wait_or_fail(&x.v_full[st], (uint32_t)(gi / STAGES) & 1u, fail);
-                    if (!ok) break;
-                    if (!x.anyvis[mb][n]) {
+                    if (!(ok = wait_or_fail(&x.v_full[st], (uint32_t)(k / STAGES) & 1u, fail))) break;
+                    if (!mt.anyvis[n]) {
                         uint8_t *vs = smem + OFF_V + st * TILEB;
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh)
@@ -413,16 +446,14 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                             for (int c = 0; c < 8; ++c)
                                 *reinterpret_cast<uint4 *>(vs + hh * HALF + n * 128 + c * 16) = make_uint4(0, 0, 0, 0);
                     }
-                    mb ^= 1;
                 }
                 kvd::fence_proxy_async_smem();
                 tc::fence_before();
                 kvd::mbar_arrive(&x.p_full);
             }
             if (!ok) break;
-            gidx += it.pairs;
             // ---- epilogue: wait for the last PV, read O ----
-            if (!wait_or_fail(&x.pv_done, n_pv & 1u, fail)) break;
+            if (!(ok = wait_or_fail(&x.pv_done, n_pv & 1u, fail))) break;
             ++n_pv;
             tc::fence_after();
             float ov[128];
@@ -460,16 +491,16 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 if (x.flag) {
                     __threadfence();
                     const int32_t first = a.p.blk_item0[it.block] - a.p.cap_dec;
+                    const float *base = a.part + ((int64_t)hk * M + n) * PART_STRIDE;
+                    const int64_t istride = (int64_t)a.n_head_kv * M * PART_STRIDE;
                     float M_ = -INFINITY;
-                    for (int32_t k = 0; k < it.nitems; ++k)
-                        M_ = fmaxf(M_, __ldcg(a.part + (((int64_t)(first + k) * a.n_head_kv + hk) * M + n) * PART_STRIDE));
+                    for (int32_t q = 0; q < it.nitems; ++q) M_ = fmaxf(M_, __ldcg(base + (first + q) * istride));
                     float L = 0.f;
-                    float acc[128];
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) acc[c] = 0.f;
+                    for (int c = 0; c < 128; ++c) ov[c] = 0.f;
                     if (M_ != -INFINITY) {
-                        for (int32_t k = 0; k < it.nitems; ++k) {
-                            const float *pk2 = a.part + (((int64_t)(first + k) * a.n_head_kv + hk) * M + n) * PART_STRIDE;
+                        for (int32_t q = 0; q < it.nitems; ++q) {
+                            const float *pk2 = base + (first + q) * istride;
                             const float mk = __ldcg(pk2);
                             if (mk == -INFINITY) continue;
                             const float sc = exp2f(mk - M_);
@@ -477,10 +508,10 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
 #pragma unroll
                             for (int c = 0; c < 128; c += 4) {
                                 const float4 v = __ldcg(reinterpret_cast<const float4 *>(pk2 + 4 + c));
-                                acc[c] = fmaf(v.x, sc, acc[c]);
-                                acc[c + 1] = fmaf(v.y, sc, acc[c + 1]);
-                                acc[c + 2] = fmaf(v.z, sc, acc[c + 2]);
-                                acc[c + 3] = fmaf(v.w, sc, acc[c + 3]);
+                                ov[c] = fmaf(v.x, sc, ov[c]);
+                                ov[c + 1] = fmaf(v.y, sc, ov[c + 1]);
+                                ov[c + 2] = fmaf(v.z, sc, ov[c + 2]);
+                                ov[c + 3] = fmaf(v.w, sc, ov[c + 3]);
                             }
                         }
                     }
@@ -489,7 +520,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
 #pragma unroll
                         for (int c = 0; c < 128; c += 4)
                             *reinterpret_cast<float4 *>(orow + c) =
-                                make_float4(acc[c] * inv, acc[c + 1] * inv, acc[c + 2] * inv, acc[c + 3] * inv);
+                                make_float4(ov[c] * inv, ov[c + 1] * inv, ov[c + 2] * inv, ov[c + 3] * inv);
                     }
                     if (n == 0) a.p.counters[it.block * a.n_head_kv + hk] = 0;
                 }

@@ -9,14 +9,14 @@
 
 namespace kvk {
 
-// One unit of attention work: tile-list entries [t0, t1) of one block.  The
-// items of a block are consecutive; `chunk` is the item's index among them
-// and also names its split-K partial slot (the item's own index).
+// One unit of attention work: tile-list entries [t0, t1) of one block, run
+// by CTA column `cta`.  A block's items are consecutive; an item's index
+// (within its path) names its split-K partial slot.
 struct WorkItem {
     int32_t block;
     int32_t t0;
     int32_t t1;
-    int32_t chunk;
+    int32_t cta;
 };
 
 // Read-only view of one ubatch's planning inputs and the cell mirror.
@@ -51,6 +51,8 @@ struct Plan {
     int32_t *blk_item0;     // [max_blocks] first item of each block
     int32_t *blk_nitems;    // [max_blocks]
     int32_t *counters;      // [max_blocks * n_head_kv] split-K completion counters
+    int32_t *cta_item0;     // decode [gx_dec + 1], then prefill [gx_pf + 1]: each CTA column's items
+    int32_t *err;
     int32_t tile_stride;
     int32_t cap_dec, cap_pf;
 };
@@ -63,8 +65,8 @@ cudaError_t launch_apply_deltas(const kvi::Delta *d, int32_t n, int32_t n_words,
                                 uint32_t *epoch, uint64_t *bits, cudaStream_t st);
 
 // k_plan.cu
-cudaError_t launch_plan(const UbView &u, const Plan &p, int32_t n_stream, int32_t dec_target,
-                        int32_t pf_target, cudaStream_t st);
+cudaError_t launch_plan(const UbView &u, const Plan &p, int32_t n_stream, int32_t gx_dec, int32_t gx_pf,
+                        cudaStream_t st);
 cudaError_t launch_mask(const UbView &u, uint16_t *mask, cudaStream_t st);
 
 // k_decode.cu
@@ -90,6 +92,7 @@ struct PrefillArgs {
     float *o;
     float *part;            // [cap_pf][n_head_kv][128][2 + 128]
     int32_t n_head, n_head_kv, gqa;
+    int32_t gx_dec;         // decode grid columns (offset of the prefill cta_item0 table)
     float scale_log2;
     int32_t *err;
 };
