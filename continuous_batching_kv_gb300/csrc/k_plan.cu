@@ -111,8 +111,9 @@ __global__ void __launch_bounds__(256) k_plan_compact(kvk::UbView u, kvk::Plan p
 // equal slices, one per CTA column of the attention grid; a slice is split at
 // block boundaries into items.  So every CTA gets the same amount of work, a
 // block's items are consecutive, and a block is covered by as few items as
-// the slices allow.  A block with an empty list gets one empty item (its rows
-// see nothing and get zeros).
+// the slices allow.  Only a block with an empty list gets an empty item (its
+// rows see nothing and get zeros); empty slices (more CTA columns than units)
+// get no item.
 __device__ __forceinline__ int64_t slice_start(int64_t x, int64_t U, int64_t gx) { return (x * U) / gx; }
 
 // Largest x with slice_start(x) <= q (U > 0).
@@ -161,8 +162,11 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                     first = P < U ? slice_of(P, U, gx) : (int32_t)gx - 1;
                     nseg = 1;
                 } else {
+                    // the slices overlapping [P, P + ub), skipping empty (zero-length) slices
                     first = slice_of(P, U, gx);
-                    nseg = slice_of(P + ub - 1, U, gx) - first + 1;
+                    const int32_t last = slice_of(P + ub - 1, U, gx);
+                    for (int32_t x = first; x <= last; ++x)
+                        if (slice_start(x + 1, U, gx) > slice_start(x, U, gx)) ++nseg;
                 }
             }
             scan_i[tid] = nseg;
@@ -178,10 +182,11 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                 p.blk_item0[b] = item_base + ibase;
                 p.blk_nitems[b] = nseg;
                 const int32_t cnt = p.counts[b];
-                for (int32_t k = 0; k < nseg; ++k) {
-                    const int32_t x = first + k;
+                int32_t x = first;
+                for (int32_t k = 0; k < nseg; ++k, ++x) {
                     int64_t lo_u = 0, hi_u = 0;
                     if (ub > 0) {
+                        while (slice_start(x + 1, U, gx) == slice_start(x, U, gx)) ++x;
                         lo_u = max(P, slice_start(x, U, gx)) - P;
                         hi_u = min(P + ub, slice_start(x + 1, U, gx)) - P;
                     }

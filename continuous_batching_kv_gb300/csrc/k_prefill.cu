@@ -320,25 +320,27 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         bool ok = true;
         for (int32_t wi = i0; wi < i1 && ok && !*fail; ++wi) {
             const ItemInfo it = item_info(a, wi);
+            int32_t row = -1, rpos = 0;
             if (it.pairs == 0) {
-                // the block sees no cell at all: zeros (the only item of its block)
+                // an empty item (its block sees no cell): zeros, or an empty partial
                 const kvi::DevBlock b = a.u.blocks[it.block];
-                if (n < b.n_rows * G) {
-                    const int32_t row = a.u.perm[b.row0 + n / G];
-                    float *orow = a.o + ((int64_t)row * a.n_head + hk * G + (n % G)) * 128;
-                    for (int c = 0; c < 128; c += 4) *reinterpret_cast<float4 *>(orow + c) = make_float4(0, 0, 0, 0);
-                }
-                continue;
+                if (n < b.n_rows * G) row = a.u.perm[b.row0 + n / G];
+            } else {
+                // the first pair's arrival also publishes this item's lane table
+                if (!(ok = wait_or_fail(&x.k_full[k % STAGES], (uint32_t)(k / STAGES) & 1u, fail))) break;
+                const ItemSlot &is = x.islot[nonempty & 1];
+                ++nonempty;
+                row = is.row[n];
+                rpos = is.rpos[n];
             }
-            // the first pair's arrival also publishes this item's lane table
-            if (!(ok = wait_or_fail(&x.k_full[k % STAGES], (uint32_t)(k / STAGES) & 1u, fail))) break;
-            const ItemSlot &is = x.islot[nonempty & 1];
-            ++nonempty;
-            const int32_t row = is.row[n];
-            const int32_t rpos = is.rpos[n];
             const bool live = row >= 0;
             const int32_t h = hk * G + (n % G);
             float *orow = a.o + ((int64_t)(live ? row : 0) * a.n_head + h) * 128;
+            float m_run = -INFINITY, l_run = 0.f;
+            float ov[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) ov[c] = 0.f;
+            if (it.pairs > 0) {
             // ---- Q tile: row n, 128-byte swizzle, two d-halves ----
             {
                 uint8_t *qs = smem + OFF_Q;
@@ -352,7 +354,6 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 kvd::fence_proxy_async_smem();
                 kvd::mbar_arrive(&x.q_full);
             }
-            float m_run = -INFINITY, l_run = 0.f;
             for (int32_t j = 0; j < it.pairs; ++j, ++k) {
                 const int32_t st = k % STAGES;
                 if (!(ok = wait_or_fail(&x.k_full[st], (uint32_t)(k / STAGES) & 1u, fail))) break;
@@ -456,7 +457,6 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             if (!(ok = wait_or_fail(&x.pv_done, n_pv & 1u, fail))) break;
             ++n_pv;
             tc::fence_after();
-            float ov[128];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t r[32];
@@ -465,6 +465,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 for (int c = 0; c < 32; ++c) ov[q4 * 32 + c] = __uint_as_float(r[c]);
             }
             tc::fence_before();
+            }   // it.pairs > 0
             if (it.nitems == 1) {
                 if (live) {
                     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
