@@ -93,6 +93,14 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, vol
     return true;
 }
 
+// 2^x with the hardware's approximate base-2 exponential (ex2.approx.ftz:
+// flushes subnormals, 2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 struct ItemInfo {
     int32_t block, t0, t1, pairs, nitems;
 };
@@ -362,53 +370,35 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 if (!(ok = wait_or_fail(&x.s_full[j & 1], n_s[j & 1] & 1u, fail))) break;
                 ++n_s[j & 1];
                 tc::fence_after();
-                // ---- S row -> registers, scaled to log2 units, masked ----
-                float s[128];
+                // ---- pass 1: raw scores -> registers, masked; row max (4 chains) ----
+                float sr[128];
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint32_t r[32];
                     tc::ld32(lane_base + (uint32_t)(j & 1) * 128u + (uint32_t)q4 * 32u, r);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) s[q4 * 32 + c] = __uint_as_float(r[c]) * a.scale_log2;
-                }
-                if (full) {
-                    if (!live) {
-#pragma unroll
-                        for (int c = 0; c < 128; ++c) s[c] = -INFINITY;
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        const bool vis = live && mt.has[c] && (!a.u.causal || mt.cpos[c] <= rpos);
-                        s[c] = vis ? s[c] : -INFINITY;
+                    for (int c = 0; c < 32; ++c) {
+                        const int cc = q4 * 32 + c;
+                        float v = __uint_as_float(r[c]);
+                        if (!full) {
+                            const bool vis = mt.has[cc] && (!a.u.causal || mt.cpos[cc] <= rpos);
+                            v = vis ? v : -INFINITY;
+                        }
+                        v = live ? v : -INFINITY;
+                        sr[cc] = v;
+                        mx[c & 3] = fmaxf(mx[c & 3], v);
                     }
                 }
-                float tmax = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < 128; ++c) tmax = fmaxf(tmax, s[c]);
+                const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
                 const float m_new = fmaxf(m_run, tmax);
                 const bool grow = m_new > m_run + RESCALE_LOG2 || (m_run == -INFINITY && m_new != -INFINITY);
                 float alpha = 1.f;
                 if (grow) {
-                    alpha = exp2f(m_run - m_new);
+                    alpha = ex2_approx(m_run - m_new);
                     m_run = m_new;
                     l_run *= alpha;
                 }
-                // ---- P = 2^(s - m), row sum ----
-                uint32_t pk[64];
-                float lsum = 0.f;
-#pragma unroll
-                for (int c = 0; c < 128; c += 2) {
-                    float p0 = 0.f, p1 = 0.f;
-                    if (m_run != -INFINITY) {
-                        p0 = exp2f(s[c] - m_run);
-                        p1 = exp2f(s[c + 1] - m_run);
-                    }
-                    lsum += p0 + p1;
-                    __half2 hv = __floats2half2_rn(p0, p1);
-                    pk[c >> 1] = *reinterpret_cast<uint32_t *>(&hv);
-                }
-                l_run += lsum;
                 // ---- P buffer free and O stable once the previous PV finished ----
                 if (j > 0) {
                     if (!(ok = wait_or_fail(&x.pv_done, n_pv & 1u, fail))) break;
@@ -427,14 +417,32 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         tc::wait_st();
                     }
                 }
-                // ---- P (fp16) to shared memory, 128-byte swizzled K-major ----
+                // ---- pass 2: P = 2^(s*scale - m) as fp16, straight to shared memory
+                //      (128-byte swizzled K-major); row sum in 4 chains ----
                 {
                     uint8_t *ps = smem + OFF_P;
+                    const bool any = m_run != -INFINITY;
+                    const float nm = -m_run;
+                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                        *reinterpret_cast<uint4 *>(ps + (c >> 3) * HALF + kvd::swz128(n, c & 7)) = v;
+                    for (int c8 = 0; c8 < 16; ++c8) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int cc = c8 * 8 + 2 * e;
+                            float p0 = 0.f, p1 = 0.f;
+                            if (any) {
+                                p0 = ex2_approx(fmaf(sr[cc], a.scale_log2, nm));
+                                p1 = ex2_approx(fmaf(sr[cc + 1], a.scale_log2, nm));
+                            }
+                            ls[e] += p0 + p1;
+                            __half2 hv = __floats2half2_rn(p0, p1);
+                            w[e] = *reinterpret_cast<uint32_t *>(&hv);
+                        }
+                        *reinterpret_cast<uint4 *>(ps + (c8 >> 3) * HALF + kvd::swz128(n, c8 & 7)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
                     }
+                    l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 }
                 if (!full) {
                     // V rows of cells nobody in the block sees: zero (P is 0 there; V may be garbage)
@@ -504,7 +512,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                             const float *pk2 = base + (first + q) * istride;
                             const float mk = __ldcg(pk2);
                             if (mk == -INFINITY) continue;
-                            const float sc = exp2f(mk - M_);
+                            const float sc = ex2_approx(mk - M_);
                             L = fmaf(__ldcg(pk2 + 1), sc, L);
 #pragma unroll
                             for (int c = 0; c < 128; c += 4) {
