@@ -176,22 +176,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             const uint32_t *flg = a.p.flags + (int64_t)it.block * a.p.tile_stride;
             for (int32_t j = 0; j < it.pairs; ++j) {
                 const int32_t st = issued % STAGES;
-                if (issued >= STAGES &&
-                    !wait_or_fail(&x.kv_empty[st], (uint32_t)((issued / STAGES) - 1) & 1u, fail))
-                    break;
-                if (j == 0) {
-                    // the item's lane table; the slot's previous reader started two or more
-                    // loads ago, and this load's stage was just released, so it is done with it
-                    for (int32_t n = lane; n < M; n += 32) {
-                        int32_t row = -1, rp = 0;
-                        if (n < nqv) {
-                            row = a.u.perm[b.row0 + n / G];
-                            rp = a.u.rows[row].pos;
-                        }
-                        is.row[n] = row;
-                        is.rpos[n] = rp;
-                    }
-                }
+                // everything this pair needs from global memory, fetched before the
+                // stage is free so that only the TMA issue waits for it
                 int32_t tt[2];
                 bool fullh[2];
                 for (int h = 0; h < 2; ++h) {
@@ -200,6 +186,52 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     fullh[h] = tt[h] >= 0 && (int32_t)(flg[tt[h]] & 0xffffu) == b.n_rows * TILE;
                 }
                 const bool full = fullh[0] && fullh[1];
+                bool mhas[4], many[4];
+                int32_t mpos[4];
+                if (!full) {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int32_t c = lane + 32 * r;
+                        const int32_t t = tt[c >> 6];
+                        bool has = false;
+                        int32_t cp = 0;
+                        if (t >= 0) {
+                            const int32_t jc = t * TILE + (c & 63);
+                            if (jc < a.u.n_kv) {
+                                const int64_t g = (int64_t)b.stream * a.u.kv_size + jc;
+                                const uint64_t w = a.u.cell_bits[g * a.u.n_words + (b.seq0 >> 6)];
+                                has = ((w >> (b.seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
+                                cp = a.u.cell_pos[g];
+                            }
+                        }
+                        mhas[r] = has;
+                        mpos[r] = cp;
+                        many[r] = has && (!a.u.causal || cp <= b.pos_max);
+                    }
+                }
+                int32_t lrow[4], lpos[4];
+                if (j == 0) {
+                    for (int r = 0; r < 4; ++r) {
+                        const int32_t n = lane + 32 * r;
+                        lrow[r] = -1;
+                        lpos[r] = 0;
+                        if (n < nqv) {
+                            lrow[r] = a.u.perm[b.row0 + n / G];
+                            lpos[r] = a.u.rows[lrow[r]].pos;
+                        }
+                    }
+                }
+                if (issued >= STAGES &&
+                    !wait_or_fail(&x.kv_empty[st], (uint32_t)((issued / STAGES) - 1) & 1u, fail))
+                    break;
+                if (j == 0) {
+                    // the item's lane table; the slot's previous reader started two or more
+                    // loads ago, and this load's stage was just released, so it is done with it
+                    for (int r = 0; r < 4; ++r) {
+                        is.row[lane + 32 * r] = lrow[r];
+                        is.rpos[lane + 32 * r] = lpos[r];
+                    }
+                }
                 Meta &mt = x.meta[st];
                 if (lane == 0) {
                     int32_t ys[2];
@@ -225,21 +257,9 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
                         const int32_t c = lane + 32 * r;
-                        const int32_t t = tt[c >> 6];
-                        bool has = false;
-                        int32_t cp = 0;
-                        if (t >= 0) {
-                            const int32_t jc = t * TILE + (c & 63);
-                            if (jc < a.u.n_kv) {
-                                const int64_t g = (int64_t)b.stream * a.u.kv_size + jc;
-                                const uint64_t w = a.u.cell_bits[g * a.u.n_words + (b.seq0 >> 6)];
-                                has = ((w >> (b.seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
-                                cp = a.u.cell_pos[g];
-                            }
-                        }
-                        mt.has[c] = has ? 1 : 0;
-                        mt.cpos[c] = cp;
-                        mt.anyvis[c] = (has && (!a.u.causal || cp <= b.pos_max)) ? 1 : 0;
+                        mt.has[c] = mhas[r] ? 1 : 0;
+                        mt.cpos[c] = mpos[r];
+                        mt.anyvis[c] = many[r] ? 1 : 0;
                     }
                 }
                 __syncwarp();
@@ -498,38 +518,40 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 }
                 tc::named_bar(1, 128);
                 if (x.flag) {
+                    // merge: warp w takes rows 32w..32w+31 one at a time, lane l holds
+                    // d = 4l..4l+3, so every load and store is a coalesced 512-byte row
                     __threadfence();
                     const int32_t first = a.p.blk_item0[it.block] - a.p.cap_dec;
-                    const float *base = a.part + ((int64_t)hk * M + n) * PART_STRIDE;
                     const int64_t istride = (int64_t)a.n_head_kv * M * PART_STRIDE;
-                    float M_ = -INFINITY;
-                    for (int32_t q = 0; q < it.nitems; ++q) M_ = fmaxf(M_, __ldcg(base + (first + q) * istride));
-                    float L = 0.f;
-#pragma unroll
-                    for (int c = 0; c < 128; ++c) ov[c] = 0.f;
-                    if (M_ != -INFINITY) {
-                        for (int32_t q = 0; q < it.nitems; ++q) {
-                            const float *pk2 = base + (first + q) * istride;
-                            const float mk = __ldcg(pk2);
-                            if (mk == -INFINITY) continue;
-                            const float sc = ex2_approx(mk - M_);
-                            L = fmaf(__ldcg(pk2 + 1), sc, L);
-#pragma unroll
-                            for (int c = 0; c < 128; c += 4) {
-                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(pk2 + 4 + c));
-                                ov[c] = fmaf(v.x, sc, ov[c]);
-                                ov[c + 1] = fmaf(v.y, sc, ov[c + 1]);
-                                ov[c + 2] = fmaf(v.z, sc, ov[c + 2]);
-                                ov[c + 3] = fmaf(v.w, sc, ov[c + 3]);
+                    const float *base = a.part + ((int64_t)first * a.n_head_kv + hk) * M * PART_STRIDE;
+                    const int32_t lane = n & 31;
+                    for (int32_t i = 0; i < 32; ++i) {
+                        const int32_t r = warp * 32 + i;
+                        const int32_t rrow = __shfl_sync(0xffffffffu, row, i);
+                        if (rrow < 0) continue;
+                        const float *pr = base + (int64_t)r * PART_STRIDE;
+                        float M_ = -INFINITY;
+                        for (int32_t q = 0; q < it.nitems; ++q) M_ = fmaxf(M_, __ldcg(pr + q * istride));
+                        float L = 0.f;
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (M_ != -INFINITY) {
+                            for (int32_t q = 0; q < it.nitems; ++q) {
+                                const float *pq = pr + q * istride;
+                                const float mk = __ldcg(pq);
+                                const float lk = __ldcg(pq + 1);
+                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(pq + 4) + lane);
+                                const float sc = mk == -INFINITY ? 0.f : ex2_approx(mk - M_);
+                                L = fmaf(lk, sc, L);
+                                acc.x = fmaf(v.x, sc, acc.x);
+                                acc.y = fmaf(v.y, sc, acc.y);
+                                acc.z = fmaf(v.z, sc, acc.z);
+                                acc.w = fmaf(v.w, sc, acc.w);
                             }
                         }
-                    }
-                    if (live) {
                         const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-                        for (int c = 0; c < 128; c += 4)
-                            *reinterpret_cast<float4 *>(orow + c) =
-                                make_float4(ov[c] * inv, ov[c + 1] * inv, ov[c + 2] * inv, ov[c + 3] * inv);
+                        const int32_t hr = hk * G + (r % G);
+                        reinterpret_cast<float4 *>(a.o + ((int64_t)rrow * a.n_head + hr) * 128)[lane] =
+                            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
                     }
                     if (n == 0) a.p.counters[it.block * a.n_head_kv + hk] = 0;
                 }
