@@ -518,41 +518,69 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 }
                 tc::named_bar(1, 128);
                 if (x.flag) {
-                    // merge: warp w takes rows 32w..32w+31 one at a time, lane l holds
-                    // d = 4l..4l+3, so every load and store is a coalesced 512-byte row
+                    // merge.  Step 1: each thread reduces its own row's maxima and sums;
+                    // step 2: four threads per row, 32 values each, all loads independent.
+                    // The P buffer is free here and holds the per-row results.
                     __threadfence();
                     const int32_t first = a.p.blk_item0[it.block] - a.p.cap_dec;
                     const int64_t istride = (int64_t)a.n_head_kv * M * PART_STRIDE;
                     const float *base = a.part + ((int64_t)first * a.n_head_kv + hk) * M * PART_STRIDE;
-                    const int32_t lane = n & 31;
-                    for (int32_t i = 0; i < 32; ++i) {
-                        const int32_t r = warp * 32 + i;
-                        const int32_t rrow = __shfl_sync(0xffffffffu, row, i);
-                        if (rrow < 0) continue;
-                        const float *pr = base + (int64_t)r * PART_STRIDE;
+                    float *mrow = reinterpret_cast<float *>(smem + OFF_P);
+                    float *irow = mrow + M;
+                    int32_t *rrow = reinterpret_cast<int32_t *>(irow + M);
+                    {
+                        const float *pr = base + (int64_t)n * PART_STRIDE;
                         float M_ = -INFINITY;
                         for (int32_t q = 0; q < it.nitems; ++q) M_ = fmaxf(M_, __ldcg(pr + q * istride));
                         float L = 0.f;
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (M_ != -INFINITY) {
+                        if (M_ != -INFINITY)
+                            for (int32_t q = 0; q < it.nitems; ++q) {
+                                const float mk = __ldcg(pr + q * istride);
+                                if (mk != -INFINITY) L = fmaf(__ldcg(pr + q * istride + 1), ex2_approx(mk - M_), L);
+                            }
+                        mrow[n] = M_;
+                        irow[n] = L > 0.f ? 1.f / L : 0.f;
+                        rrow[n] = row;
+                    }
+                    tc::named_bar(1, 128);
+                    const int32_t qd = n & 3;            // which 32 values of the row
+#pragma unroll 1
+                    for (int32_t pass = 0; pass < 4; ++pass) {
+                        const int32_t r = pass * 32 + (n >> 2);
+                        const int32_t orow_id = rrow[r];
+                        const float Mr = mrow[r];
+                        const float inv = irow[r];
+                        float acc[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) acc[c] = 0.f;
+                        if (orow_id >= 0 && Mr != -INFINITY) {
+                            const float *pr = base + (int64_t)r * PART_STRIDE;
                             for (int32_t q = 0; q < it.nitems; ++q) {
                                 const float *pq = pr + q * istride;
                                 const float mk = __ldcg(pq);
-                                const float lk = __ldcg(pq + 1);
-                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(pq + 4) + lane);
-                                const float sc = mk == -INFINITY ? 0.f : ex2_approx(mk - M_);
-                                L = fmaf(lk, sc, L);
-                                acc.x = fmaf(v.x, sc, acc.x);
-                                acc.y = fmaf(v.y, sc, acc.y);
-                                acc.z = fmaf(v.z, sc, acc.z);
-                                acc.w = fmaf(v.w, sc, acc.w);
+                                float4 v[8];
+#pragma unroll
+                                for (int c = 0; c < 8; ++c)
+                                    v[c] = __ldcg(reinterpret_cast<const float4 *>(pq + 4 + 32 * qd) + c);
+                                const float sc = mk == -INFINITY ? 0.f : ex2_approx(mk - Mr);
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) {
+                                    acc[4 * c + 0] = fmaf(v[c].x, sc, acc[4 * c + 0]);
+                                    acc[4 * c + 1] = fmaf(v[c].y, sc, acc[4 * c + 1]);
+                                    acc[4 * c + 2] = fmaf(v[c].z, sc, acc[4 * c + 2]);
+                                    acc[4 * c + 3] = fmaf(v[c].w, sc, acc[4 * c + 3]);
+                                }
                             }
                         }
-                        const float inv = L > 0.f ? 1.f / L : 0.f;
-                        const int32_t hr = hk * G + (r % G);
-                        reinterpret_cast<float4 *>(a.o + ((int64_t)rrow * a.n_head + hr) * 128)[lane] =
-                            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                        if (orow_id >= 0) {
+                            float *dst = a.o + ((int64_t)orow_id * a.n_head + hk * G + (r % G)) * 128 + 32 * qd;
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                reinterpret_cast<float4 *>(dst)[c] = make_float4(acc[4 * c] * inv, acc[4 * c + 1] * inv,
+                                                                                 acc[4 * c + 2] * inv, acc[4 * c + 3] * inv);
+                        }
                     }
+                    tc::named_bar(1, 128);   // the P buffer is written again by the next item
                     if (n == 0) a.p.counters[it.block * a.n_head_kv + hk] = 0;
                 }
             }
