@@ -101,6 +101,24 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// 2^x on the FMA pipe.  Range reduction: x = n + f with n = round(x) taken by
+// adding 1.5 * 2^23 (the integer lands in the low mantissa bits), f in
+// [-1/2, 1/2]; 2^f by a cubic 1 + f (c1 + f (c2 + f c3)) whose coefficients
+// were fitted here to minimise the maximum relative error on [-1/2, 1/2]
+// (about 1.0e-4, below the 4.9e-4 half-ulp of the fp16 P it feeds); 2^n is
+// added to the exponent field with one integer multiply-add.  x is clamped to
+// -127, where the result is exactly +0 (so is 2^-inf).
+__device__ __forceinline__ float ex2_poly(float x) {
+    constexpr float MAGIC = 12582912.0f;    // 1.5 * 2^23
+    constexpr float C1 = 6.932828051e-01f, C2 = 2.422090319e-01f, C3 = 5.500809860e-02f;
+    x = fmaxf(x, -127.0f);
+    const float t = x + MAGIC;
+    const float nf = t - MAGIC;
+    const float f = x - nf;
+    const float p = fmaf(f, fmaf(f, fmaf(f, C3, C2), C1), 1.0f);
+    return __uint_as_float(__float_as_uint(p) + (__float_as_uint(t) << 23));
+}
+
 struct ItemInfo {
     int32_t block, t0, t1, pairs, nitems;
 };
@@ -390,25 +408,25 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 if (!(ok = wait_or_fail(&x.s_full[j & 1], n_s[j & 1] & 1u, fail))) break;
                 ++n_s[j & 1];
                 tc::fence_after();
-                // ---- pass 1: raw scores -> registers, masked; row max (4 chains) ----
-                float sr[128];
+                // ---- pass 1: masked row maximum (one TMEM round trip, 4 chains) ----
+                const uint32_t s_addr = lane_base + (uint32_t)(j & 1) * 128u;
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (live) {
+                    uint32_t r[128];
+                    tc::ld128(s_addr, r);
+                    if (full) {
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t r[32];
-                    tc::ld32(lane_base + (uint32_t)(j & 1) * 128u + (uint32_t)q4 * 32u, r);
+                        for (int c = 0; c < 128; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(r[c]));
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const int cc = q4 * 32 + c;
-                        float v = __uint_as_float(r[c]);
-                        if (!full) {
-                            const bool vis = mt.has[cc] && (!a.u.causal || mt.cpos[cc] <= rpos);
-                            v = vis ? v : -INFINITY;
+                        for (int c = 0; c < 128; ++c) {
+                            const bool vis = mt.has[c] && (!a.u.causal || mt.cpos[c] <= rpos);
+                            mx[c & 3] = fmaxf(mx[c & 3], vis ? __uint_as_float(r[c]) : -INFINITY);
                         }
-                        v = live ? v : -INFINITY;
-                        sr[cc] = v;
-                        mx[c & 3] = fmaxf(mx[c & 3], v);
                     }
+                } else {
+                    uint32_t r[128];          // the load is warp-collective: every lane takes part
+                    tc::ld128(s_addr, r);
                 }
                 const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
                 const float m_new = fmaxf(m_run, tmax);
@@ -438,29 +456,42 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     }
                 }
                 // ---- pass 2: P = 2^(s*scale - m) as fp16, straight to shared memory
-                //      (128-byte swizzled K-major); row sum in 4 chains ----
+                //      (128-byte swizzled K-major), S re-read in two halves; half of the
+                //      exponentials on the MUFU unit, half on the FMA pipe; row sum in
+                //      4 chains ----
                 {
                     uint8_t *ps = smem + OFF_P;
-                    const bool any = m_run != -INFINITY;
+                    const bool any = live && m_run != -INFINITY;
                     const float nm = -m_run;
                     float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int c8 = 0; c8 < 16; ++c8) {
-                        uint32_t w[4];
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t r[64];
+                        tc::ld64(s_addr + (uint32_t)hh * 64u, r);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int cc = c8 * 8 + 2 * e;
-                            float p0 = 0.f, p1 = 0.f;
-                            if (any) {
-                                p0 = ex2_approx(fmaf(sr[cc], a.scale_log2, nm));
-                                p1 = ex2_approx(fmaf(sr[cc + 1], a.scale_log2, nm));
+                        for (int c8 = 0; c8 < 8; ++c8) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int cl = c8 * 8 + 2 * e;     // column within the half
+                                const int cc = hh * 64 + cl;       // column within the tile
+                                float p0 = 0.f, p1 = 0.f;
+                                if (any) {
+                                    float s0 = __uint_as_float(r[cl]), s1 = __uint_as_float(r[cl + 1]);
+                                    if (!full) {
+                                        if (!(mt.has[cc] && (!a.u.causal || mt.cpos[cc] <= rpos))) s0 = -INFINITY;
+                                        if (!(mt.has[cc + 1] && (!a.u.causal || mt.cpos[cc + 1] <= rpos))) s1 = -INFINITY;
+                                    }
+                                    p0 = ex2_approx(fmaf(s0, a.scale_log2, nm));
+                                    p1 = ex2_poly(fmaf(s1, a.scale_log2, nm));
+                                }
+                                ls[e] += p0 + p1;
+                                __half2 hv = __floats2half2_rn(p0, p1);
+                                w[e] = *reinterpret_cast<uint32_t *>(&hv);
                             }
-                            ls[e] += p0 + p1;
-                            __half2 hv = __floats2half2_rn(p0, p1);
-                            w[e] = *reinterpret_cast<uint32_t *>(&hv);
+                            *reinterpret_cast<uint4 *>(ps + hh * HALF + kvd::swz128(n, c8)) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
                         }
-                        *reinterpret_cast<uint4 *>(ps + (c8 >> 3) * HALF + kvd::swz128(n, c8 & 7)) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
                     }
                     l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 }
