@@ -124,14 +124,18 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     if (warp == 4) {
         // ======================= producer =======================
         int32_t k = 0;
-        for (int32_t wi = i0; wi < i1 && !*fail; ++wi) {
+        // wait outcomes and the loop condition are agreed by the whole warp, so a
+        // failure never splits it in front of __syncwarp
+        for (int32_t wi = i0; wi < i1 && __all_sync(0xffffffffu, *fail == 0); ++wi) {
             const kvk::WorkItem w = a.p.work[wi];
             const kvi::DevBlock b = a.u.blocks[w.block];
             const int32_t *list = a.p.tiles + (int64_t)w.block * a.p.tile_stride;
             const uint32_t *flg = a.p.flags + (int64_t)w.block * a.p.tile_stride;
             for (int32_t li = w.t0; li < w.t1; ++li) {
                 const int32_t st = k % STAGES;
-                if (k >= STAGES && !wait_or_fail(&x.empty[st], (uint32_t)((k / STAGES) - 1) & 1u, fail)) break;
+                if (k >= STAGES &&
+                    !__all_sync(0xffffffffu, wait_or_fail(&x.empty[st], (uint32_t)((k / STAGES) - 1) & 1u, fail)))
+                    break;
                 const int32_t t = list[li];
                 const bool full = (int32_t)(flg[t] & 0xffffu) == b.n_rows * TILE;
                 if (lane == 0) {

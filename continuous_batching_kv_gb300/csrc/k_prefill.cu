@@ -119,6 +119,10 @@ __device__ __forceinline__ float ex2_poly(float x) {
     return __uint_as_float(__float_as_uint(p) + (__float_as_uint(t) << 23));
 }
 
+// True while no wait has given up, agreed by all 32 lanes of the warp (so a
+// failure never splits a warp in front of a warp-collective instruction).
+__device__ __forceinline__ bool warp_ok(volatile int32_t *fail) { return __all_sync(0xffffffffu, *fail == 0); }
+
 struct ItemInfo {
     int32_t block, t0, t1, pairs, nitems;
 };
@@ -183,7 +187,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         // ===================== producer (whole warp) =====================
         const int32_t lane = tid & 31;
         int32_t issued = 0, nonempty = 0;
-        for (int32_t wi = i0; wi < i1 && !*fail; ++wi) {
+        for (int32_t wi = i0; wi < i1 && warp_ok(fail); ++wi) {
             const ItemInfo it = item_info(a, wi);
             if (it.pairs == 0) continue;
             const kvi::DevBlock b = a.u.blocks[it.block];
@@ -240,7 +244,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     }
                 }
                 if (issued >= STAGES &&
-                    !wait_or_fail(&x.kv_empty[st], (uint32_t)((issued / STAGES) - 1) & 1u, fail))
+                    !__all_sync(0xffffffffu,
+                                wait_or_fail(&x.kv_empty[st], (uint32_t)((issued / STAGES) - 1) & 1u, fail)))
                     break;
                 if (j == 0) {
                     // the item's lane table; the slot's previous reader started two or more
@@ -364,7 +369,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         int32_t k = 0;                         // pair tiles consumed (stage ring position)
         int32_t nonempty = 0;
         bool ok = true;
-        for (int32_t wi = i0; wi < i1 && ok && !*fail; ++wi) {
+        for (int32_t wi = i0; wi < i1 && ok && warp_ok(fail); ++wi) {
             const ItemInfo it = item_info(a, wi);
             int32_t row = -1, rpos = 0;
             if (it.pairs == 0) {
@@ -373,7 +378,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 if (n < b.n_rows * G) row = a.u.perm[b.row0 + n / G];
             } else {
                 // the first pair's arrival also publishes this item's lane table
-                if (!(ok = wait_or_fail(&x.k_full[k % STAGES], (uint32_t)(k / STAGES) & 1u, fail))) break;
+                ok = __all_sync(0xffffffffu, wait_or_fail(&x.k_full[k % STAGES], (uint32_t)(k / STAGES) & 1u, fail));
+                if (!ok) break;
                 const ItemSlot &is = x.islot[nonempty & 1];
                 ++nonempty;
                 row = is.row[n];
@@ -402,31 +408,34 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             }
             for (int32_t j = 0; j < it.pairs; ++j, ++k) {
                 const int32_t st = k % STAGES;
-                if (!(ok = wait_or_fail(&x.k_full[st], (uint32_t)(k / STAGES) & 1u, fail))) break;
+                ok = __all_sync(0xffffffffu, wait_or_fail(&x.k_full[st], (uint32_t)(k / STAGES) & 1u, fail));
+                if (!ok) break;
                 const Meta &mt = x.meta[st];
                 const bool full = mt.full != 0;
-                if (!(ok = wait_or_fail(&x.s_full[j & 1], n_s[j & 1] & 1u, fail))) break;
+                ok = __all_sync(0xffffffffu, wait_or_fail(&x.s_full[j & 1], n_s[j & 1] & 1u, fail));
+                if (!ok) break;
                 ++n_s[j & 1];
                 tc::fence_after();
                 // ---- pass 1: masked row maximum (one TMEM round trip, 4 chains) ----
                 const uint32_t s_addr = lane_base + (uint32_t)(j & 1) * 128u;
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                if (live) {
+                {
+                    // tcgen05.ld is a .sync.aligned warp collective: it is issued by all 32
+                    // lanes together, outside any lane-dependent branch
                     uint32_t r[128];
                     tc::ld128(s_addr, r);
-                    if (full) {
+                    if (live) {
+                        if (full) {
 #pragma unroll
-                        for (int c = 0; c < 128; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(r[c]));
-                    } else {
+                            for (int c = 0; c < 128; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(r[c]));
+                        } else {
 #pragma unroll
-                        for (int c = 0; c < 128; ++c) {
-                            const bool vis = mt.has[c] && (!a.u.causal || mt.cpos[c] <= rpos);
-                            mx[c & 3] = fmaxf(mx[c & 3], vis ? __uint_as_float(r[c]) : -INFINITY);
+                            for (int c = 0; c < 128; ++c) {
+                                const bool vis = mt.has[c] && (!a.u.causal || mt.cpos[c] <= rpos);
+                                mx[c & 3] = fmaxf(mx[c & 3], vis ? __uint_as_float(r[c]) : -INFINITY);
+                            }
                         }
                     }
-                } else {
-                    uint32_t r[128];          // the load is warp-collective: every lane takes part
-                    tc::ld128(s_addr, r);
                 }
                 const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
                 const float m_new = fmaxf(m_run, tmax);
@@ -439,7 +448,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 }
                 // ---- P buffer free and O stable once the previous PV finished ----
                 if (j > 0) {
-                    if (!(ok = wait_or_fail(&x.pv_done, n_pv & 1u, fail))) break;
+                    ok = __all_sync(0xffffffffu, wait_or_fail(&x.pv_done, n_pv & 1u, fail));
+                    if (!ok) break;
                     ++n_pv;
                     tc::fence_after();
                     if (__any_sync(0xffffffffu, grow)) {
@@ -497,7 +507,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 }
                 if (!full) {
                     // V rows of cells nobody in the block sees: zero (P is 0 there; V may be garbage)
-                    if (!(ok = wait_or_fail(&x.v_full[st], (uint32_t)(k / STAGES) & 1u, fail))) break;
+                    ok = __all_sync(0xffffffffu, wait_or_fail(&x.v_full[st], (uint32_t)(k / STAGES) & 1u, fail));
+                    if (!ok) break;
                     if (!mt.anyvis[n]) {
                         uint8_t *vs = smem + OFF_V + st * TILEB;
 #pragma unroll
@@ -513,7 +524,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             }
             if (!ok) break;
             // ---- epilogue: wait for the last PV, read O ----
-            if (!(ok = wait_or_fail(&x.pv_done, n_pv & 1u, fail))) break;
+            ok = __all_sync(0xffffffffu, wait_or_fail(&x.pv_done, n_pv & 1u, fail));
+            if (!ok) break;
             ++n_pv;
             tc::fence_after();
 #pragma unroll
