@@ -416,27 +416,28 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 if (!ok) break;
                 ++n_s[j & 1];
                 tc::fence_after();
-                // ---- pass 1: masked row maximum (one TMEM round trip, 4 chains) ----
+                // ---- pass 1: masked row maximum.  A runtime loop over four 32-column
+                //      chunks keeps the hot code small; each chunk is one TMEM load
+                //      (issued by the whole warp) and 32 independent max chains ----
                 const uint32_t s_addr = lane_base + (uint32_t)(j & 1) * 128u;
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                {
-                    // tcgen05.ld is a .sync.aligned warp collective: it is issued by all 32
-                    // lanes together, outside any lane-dependent branch
-                    uint32_t r[128];
-                    tc::ld128(s_addr, r);
-                    if (live) {
-                        if (full) {
+#pragma unroll 1
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t r[32];
+                    tc::ld32(s_addr + (uint32_t)q4 * 32u, r);
+                    if (full) {
 #pragma unroll
-                            for (int c = 0; c < 128; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(r[c]));
-                        } else {
+                        for (int c = 0; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(r[c]));
+                    } else {
 #pragma unroll
-                            for (int c = 0; c < 128; ++c) {
-                                const bool vis = mt.has[c] && (!a.u.causal || mt.cpos[c] <= rpos);
-                                mx[c & 3] = fmaxf(mx[c & 3], vis ? __uint_as_float(r[c]) : -INFINITY);
-                            }
+                        for (int c = 0; c < 32; ++c) {
+                            const int cc = q4 * 32 + c;
+                            const bool vis = mt.has[cc] && (!a.u.causal || mt.cpos[cc] <= rpos);
+                            mx[c & 3] = fmaxf(mx[c & 3], vis ? __uint_as_float(r[c]) : -INFINITY);
                         }
                     }
                 }
+                if (!live) mx[0] = mx[1] = mx[2] = mx[3] = -INFINITY;
                 const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
                 const float m_new = fmaxf(m_run, tmax);
                 const bool grow = m_new > m_run + RESCALE_LOG2 || (m_run == -INFINITY && m_new != -INFINITY);
@@ -466,40 +467,42 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     }
                 }
                 // ---- pass 2: P = 2^(s*scale - m) as fp16, straight to shared memory
-                //      (128-byte swizzled K-major), S re-read in two halves; half of the
-                //      exponentials on the MUFU unit, half on the FMA pipe; row sum in
-                //      4 chains ----
+                //      (128-byte swizzled K-major); S re-read chunk by chunk; one
+                //      exponential in four on the FMA pipe, the rest on the MUFU unit;
+                //      row sum in 4 chains ----
                 {
                     uint8_t *ps = smem + OFF_P;
                     const bool any = live && m_run != -INFINITY;
                     const float nm = -m_run;
+                    const float sc = a.scale_log2;
                     float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t r[32];
+                        tc::ld32(s_addr + (uint32_t)q4 * 32u, r);
+                        float p[32];
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        uint32_t r[64];
-                        tc::ld64(s_addr + (uint32_t)hh * 64u, r);
+                        for (int c = 0; c < 32; ++c) {
+                            float v = __uint_as_float(r[c]);
+                            if (!full) {
+                                const int cc = q4 * 32 + c;
+                                if (!(mt.has[cc] && (!a.u.causal || mt.cpos[cc] <= rpos))) v = -INFINITY;
+                            }
+                            const float xx = fmaf(v, sc, nm);
+                            p[c] = (c & 3) == 3 ? ex2_poly(xx) : ex2_approx(xx);
+                            p[c] = any ? p[c] : 0.f;
+                            ls[c & 3] += p[c];
+                        }
+                        uint8_t *dst = ps + (q4 >> 1) * HALF;
 #pragma unroll
-                        for (int c8 = 0; c8 < 8; ++c8) {
+                        for (int c8 = 0; c8 < 4; ++c8) {
                             uint32_t w[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const int cl = c8 * 8 + 2 * e;     // column within the half
-                                const int cc = hh * 64 + cl;       // column within the tile
-                                float p0 = 0.f, p1 = 0.f;
-                                if (any) {
-                                    float s0 = __uint_as_float(r[cl]), s1 = __uint_as_float(r[cl + 1]);
-                                    if (!full) {
-                                        if (!(mt.has[cc] && (!a.u.causal || mt.cpos[cc] <= rpos))) s0 = -INFINITY;
-                                        if (!(mt.has[cc + 1] && (!a.u.causal || mt.cpos[cc + 1] <= rpos))) s1 = -INFINITY;
-                                    }
-                                    p0 = ex2_approx(fmaf(s0, a.scale_log2, nm));
-                                    p1 = ex2_poly(fmaf(s1, a.scale_log2, nm));
-                                }
-                                ls[e] += p0 + p1;
-                                __half2 hv = __floats2half2_rn(p0, p1);
+                                __half2 hv = __floats2half2_rn(p[c8 * 8 + 2 * e], p[c8 * 8 + 2 * e + 1]);
                                 w[e] = *reinterpret_cast<uint32_t *>(&hv);
                             }
-                            *reinterpret_cast<uint4 *>(ps + hh * HALF + kvd::swz128(n, c8)) =
+                            *reinterpret_cast<uint4 *>(dst + kvd::swz128(n, (q4 & 1) * 4 + c8)) =
                                 make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     }
