@@ -416,28 +416,24 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 if (!ok) break;
                 ++n_s[j & 1];
                 tc::fence_after();
-                // ---- pass 1: masked row maximum.  A runtime loop over four 32-column
-                //      chunks keeps the hot code small; each chunk is one TMEM load
-                //      (issued by the whole warp) and 32 independent max chains ----
-                const uint32_t s_addr = lane_base + (uint32_t)(j & 1) * 128u;
+                // ---- S row -> 128 registers, read from TMEM once, right when it is ready
+                //      (TMEM reads stall while the next MMA runs, so pass 2 must not go
+                //      back to TMEM); masked cells become -inf; row max in 4 chains ----
+                uint32_t sb[128];
+                tc::ld128(lane_base + (uint32_t)(j & 1) * 128u, sb);   // warp collective
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t r[32];
-                    tc::ld32(s_addr + (uint32_t)q4 * 32u, r);
-                    if (full) {
+                if (!live) {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(r[c]));
-                    } else {
+                    for (int c = 0; c < 128; ++c) sb[c] = __float_as_uint(-INFINITY);
+                } else if (!full) {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            const int cc = q4 * 32 + c;
-                            const bool vis = mt.has[cc] && (!a.u.causal || mt.cpos[cc] <= rpos);
-                            mx[c & 3] = fmaxf(mx[c & 3], vis ? __uint_as_float(r[c]) : -INFINITY);
-                        }
+                    for (int c = 0; c < 128; ++c) {
+                        const bool vis = mt.has[c] && (!a.u.causal || mt.cpos[c] <= rpos);
+                        if (!vis) sb[c] = __float_as_uint(-INFINITY);
                     }
                 }
-                if (!live) mx[0] = mx[1] = mx[2] = mx[3] = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 128; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sb[c]));
                 const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
                 const float m_new = fmaxf(m_run, tmax);
                 const bool grow = m_new > m_run + RESCALE_LOG2 || (m_run == -INFINITY && m_new != -INFINITY);
@@ -453,60 +449,50 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     if (!ok) break;
                     ++n_pv;
                     tc::fence_after();
-                    if (__any_sync(0xffffffffu, grow)) {
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint32_t r[32];
-                            const uint32_t ta = lane_base + COL_O + (uint32_t)q4 * 32u;
-                            tc::ld32(ta, r);
-#pragma unroll
-                            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-                            tc::st32(ta, r);
-                        }
-                        tc::wait_st();
-                    }
                 }
-                // ---- pass 2: P = 2^(s*scale - m) as fp16, straight to shared memory
-                //      (128-byte swizzled K-major); S re-read chunk by chunk; one
-                //      exponential in four on the FMA pipe, the rest on the MUFU unit;
-                //      row sum in 4 chains ----
+                // ---- pass 2 (from registers): P = 2^(s*scale - m) as fp16, straight to
+                //      shared memory (128-byte swizzled K-major); one exponential in four
+                //      on the FMA pipe, the rest on the MUFU unit; row sum in 4 chains ----
                 {
                     uint8_t *ps = smem + OFF_P;
-                    const bool any = live && m_run != -INFINITY;
+                    const bool any = m_run != -INFINITY;   // false for lanes past the block
                     const float nm = -m_run;
                     const float sc = a.scale_log2;
                     float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int c8 = 0; c8 < 16; ++c8) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = c8 * 8 + 2 * e;
+                            const float x0 = fmaf(__uint_as_float(sb[c]), sc, nm);
+                            const float x1 = fmaf(__uint_as_float(sb[c + 1]), sc, nm);
+                            float p0 = ex2_approx(x0);
+                            float p1 = (e & 1) ? ex2_poly(x1) : ex2_approx(x1);
+                            p0 = any ? p0 : 0.f;
+                            p1 = any ? p1 : 0.f;
+                            ls[e] += p0 + p1;
+                            __half2 hv = __floats2half2_rn(p0, p1);
+                            w[e] = *reinterpret_cast<uint32_t *>(&hv);
+                        }
+                        *reinterpret_cast<uint4 *>(ps + (c8 >> 3) * HALF + kvd::swz128(n, c8 & 7)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                }
+                // ---- O *= alpha where the running maximum moved (rare); O is stable
+                //      since the previous PV finished, and this pair's PV waits for us ----
+                if (j > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint32_t r[32];
-                        tc::ld32(s_addr + (uint32_t)q4 * 32u, r);
-                        float p[32];
+                        const uint32_t ta = lane_base + COL_O + (uint32_t)q4 * 32u;
+                        tc::ld32(ta, r);
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            float v = __uint_as_float(r[c]);
-                            if (!full) {
-                                const int cc = q4 * 32 + c;
-                                if (!(mt.has[cc] && (!a.u.causal || mt.cpos[cc] <= rpos))) v = -INFINITY;
-                            }
-                            const float xx = fmaf(v, sc, nm);
-                            p[c] = (c & 3) == 3 ? ex2_poly(xx) : ex2_approx(xx);
-                            p[c] = any ? p[c] : 0.f;
-                            ls[c & 3] += p[c];
-                        }
-                        uint8_t *dst = ps + (q4 >> 1) * HALF;
-#pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                __half2 hv = __floats2half2_rn(p[c8 * 8 + 2 * e], p[c8 * 8 + 2 * e + 1]);
-                                w[e] = *reinterpret_cast<uint32_t *>(&hv);
-                            }
-                            *reinterpret_cast<uint4 *>(dst + kvd::swz128(n, (q4 & 1) * 4 + c8)) =
-                                make_uint4(w[0], w[1], w[2], w[3]);
-                        }
+                        for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+                        tc::st32(ta, r);
                     }
-                    l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                    tc::wait_st();
                 }
                 if (!full) {
                     // V rows of cells nobody in the block sees: zero (P is 0 there; V may be garbage)
