@@ -370,7 +370,7 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
         a.err = d->d_err;
         if ((e = kvk::launch_prefill(&d->tm_k[layer], &d->tm_v[layer], a, d->gx_pf, st)) != cudaSuccess)
             return cuda_fail(c, e, "prefill launch");
-        c->launches += 1;
+        c->launches += 2;   // attention + split-K merge
     }
     return KV_OK;
 }

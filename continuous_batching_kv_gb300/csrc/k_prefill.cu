@@ -6,26 +6,30 @@
 // not later) it is the same softmax(q K^T / sqrt(d) + mask) V as decode, but
 // now a dense contraction worth putting on the tensor cores.
 //
-// Design (sm_103a, one CTA of 192 threads per SM):
+// Design (sm_103a, one CTA of 320 threads per SM):
 //  * a block = up to 128 query vectors (rows sharing a stream and first
 //    sequence id, times the GQA group) = the 128 TMEM lanes of one MMA tile;
 //    a work item = one block, one KV head, a chunk of the block's list of
 //    visible 64-cell tiles, consumed two at a time (N = 128 cells);
-//  * warp 4 (one thread) streams K and V tiles with TMA (128-byte swizzle)
-//    into a 2-stage ring; warp 5 allocates TMEM and one thread issues
+//  * warp 8 streams K and V tiles with TMA (128-byte swizzle) into a 2-stage
+//    ring, with each tile's list entry, flags and per-cell visibility
+//    fetched ahead into the same slot; warp 9 allocates TMEM and one thread issues
 //    tcgen05.mma: S = Q K^T (M 128, N 128, K 128) into one of two TMEM score
 //    buffers, then O += P V (K = 128 cells, V read MN-major) into a TMEM
 //    accumulator; tcgen05.commit signals the mbarriers;
-//  * warps 0-3 (thread = TMEM lane = query vector) read S with tcgen05.ld,
-//    apply the mask per cell on tiles that are not fully visible, run the
-//    online softmax in base 2, write P (fp16) to shared memory in the
-//    swizzled K-major layout, and rescale O in TMEM only when the running
-//    maximum grew by more than 2^8 (otherwise the stale maximum is kept; the
-//    final normalisation uses the same one);
+//  * warps 0-7 (two threads per TMEM lane = query vector, 64 columns each)
+//    read S with one tcgen05.ld as soon as it lands (TMEM reads stall behind
+//    running MMAs), apply the mask per cell on tiles that are not fully
+//    visible, run the online softmax in base 2 (a quarter of the exponentials
+//    on the FMA pipe), write P (fp16) to shared memory in the swizzled K-major
+//    layout, and rescale O in TMEM only when the running maximum grew by more
+//    than 2^8 (otherwise the stale maximum is kept; the final normalisation
+//    uses the same one);
 //  * cells nobody in the block may see get their V rows zeroed in shared
 //    memory before the PV product (P is 0 there, but 0 * NaN would not be);
-//  * split-K chunks of one block are merged by the last CTA to finish, as in
-//    the decode path; every mbarrier wait is bounded.
+//  * a block split over several CTAs leaves one partial (m, l, O) per piece,
+//    merged by a small second kernel, so no CTA stalls its own pipeline to
+//    merge; every mbarrier wait is bounded.
 
 #include "dev_common.cuh"
 #include "kernels.h"
@@ -35,7 +39,8 @@ namespace {
 
 using kvi::TILE;
 
-constexpr int NT = 192;
+constexpr int NSM = 256;                 // softmax threads: two per TMEM lane
+constexpr int NT = NSM + 64;             // + producer warp + MMA warp
 constexpr int M = 128;
 constexpr int HALF = 128 * 128;          // [128 rows][64 fp16], 128-byte rows
 constexpr int TILEB = 2 * HALF;          // 32 KiB
@@ -70,12 +75,15 @@ struct ItemSlot {             // per work item: the query vector behind each TME
 struct __align__(16) Aux {
     uint64_t k_full[STAGES], v_full[STAGES], kv_empty[STAGES];
     uint64_t s_full[2], p_full, pv_done, q_full, spare;
+    uint64_t rbar, lbar;      // softmax-group exchanges (row maxima, row sums), all 256 threads
     uint32_t tmem_base;
     int32_t fail;
     int32_t flag;
     int32_t pad;
     Meta meta[STAGES];
     ItemSlot islot[2];
+    float red[2][2][M];       // [pair parity][column half][row]: partial row maxima
+    float lex[2][2][M];       // [item parity][column half][row]: partial row sums
 };
 
 constexpr size_t SMEM_BYTES = OFF_AUX + sizeof(Aux);
@@ -167,14 +175,16 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         }
         kvd::mbar_init(&x.s_full[0], 1);
         kvd::mbar_init(&x.s_full[1], 1);
-        kvd::mbar_init(&x.p_full, 128);
+        kvd::mbar_init(&x.p_full, NSM);
         kvd::mbar_init(&x.pv_done, 1);
-        kvd::mbar_init(&x.q_full, 128);
+        kvd::mbar_init(&x.q_full, NSM);
         kvd::mbar_init(&x.spare, 1);
+        kvd::mbar_init(&x.rbar, NSM);
+        kvd::mbar_init(&x.lbar, NSM);
         x.fail = 0;
         kvd::fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tc::alloc(&x.tmem_base, TMEM_COLS);
         tc::relinquish();
     }
@@ -183,7 +193,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     tc::fence_after();
     const uint32_t tmem = x.tmem_base;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ===================== producer (whole warp) =====================
         const int32_t lane = tid & 31;
         int32_t issued = 0, nonempty = 0;
@@ -297,7 +307,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 (void)kvd::mbar_wait_bounded(&x.v_full[q % STAGES], (uint32_t)(q / STAGES) & 1u);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ===================== MMA issuer =====================
         if ((tid & 31) == 0) {
             int32_t gidx = 0;          // global pair-tile counter (stage ring)
@@ -361,14 +371,21 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             (void)kvd::mbar_wait_bounded(&x.spare, 0);
         }
     } else {
-        // ===================== softmax / correction / epilogue (warps 0-3) =====================
-        const int32_t n = tid;                 // TMEM lane = query vector
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        // ============ softmax / correction / epilogue (warps 0-7, two threads per row) ============
+        // Warps w and w + 4 share TMEM lane quarter w: thread (n, ch) owns row n's
+        // columns 64ch .. 64ch + 63 of S, P and O.  Row maxima and row sums are
+        // combined through shared memory.
+        const int32_t n = tid & 127;           // TMEM lane = query vector
+        const int32_t ch = tid >> 7;           // column half
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(64 * ch);
         uint32_t n_s[2] = {0, 0};
-        uint32_t n_pv = 0;
+        uint32_t n_pv = 0, n_r = 0, n_l = 0;
         int32_t k = 0;                         // pair tiles consumed (stage ring position)
         int32_t nonempty = 0;
         bool ok = true;
+        // The two halves of a row meet through mbarriers (arrive, then a bounded
+        // wait), never bar.sync: if a wait elsewhere gives up, the others time out
+        // instead of waiting for threads that left.
         for (int32_t wi = i0; wi < i1 && ok && warp_ok(fail); ++wi) {
             const ItemInfo it = item_info(a, wi);
             int32_t row = -1, rpos = 0;
@@ -387,22 +404,22 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             }
             const bool live = row >= 0;
             const int32_t h = hk * G + (n % G);
-            float *orow = a.o + ((int64_t)(live ? row : 0) * a.n_head + h) * 128;
-            float m_run = -INFINITY, l_run = 0.f;
-            float ov[128];
+            float *orow = a.o + ((int64_t)(live ? row : 0) * a.n_head + h) * 128 + 64 * ch;
+            float m_run = -INFINITY, l_run = 0.f;   // l_run: this thread's half of the row sum
+            float ov[64];
 #pragma unroll
-            for (int c = 0; c < 128; ++c) ov[c] = 0.f;
+            for (int c = 0; c < 64; ++c) ov[c] = 0.f;
             if (it.pairs > 0) {
-            // ---- Q tile: row n, 128-byte swizzle, two d-halves ----
+            // ---- Q tile: row n, d-half ch, 128-byte swizzle ----
             {
-                uint8_t *qs = smem + OFF_Q;
-                const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((int64_t)(live ? row : 0) * a.n_head + h) * 128);
-                uint4 qv[16];
+                uint8_t *qs = smem + OFF_Q + ch * HALF;
+                const uint4 *src =
+                    reinterpret_cast<const uint4 *>(a.q + ((int64_t)(live ? row : 0) * a.n_head + h) * 128 + 64 * ch);
+                uint4 qv[8];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) qv[c] = live ? src[c] : make_uint4(0, 0, 0, 0);
+                for (int c = 0; c < 8; ++c) qv[c] = live ? src[c] : make_uint4(0, 0, 0, 0);
 #pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    *reinterpret_cast<uint4 *>(qs + (c >> 3) * HALF + kvd::swz128(n, c & 7)) = qv[c];
+                for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qs + kvd::swz128(n, c)) = qv[c];
                 kvd::fence_proxy_async_smem();
                 kvd::mbar_arrive(&x.q_full);
             }
@@ -416,25 +433,31 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 if (!ok) break;
                 ++n_s[j & 1];
                 tc::fence_after();
-                // ---- S row -> 128 registers, read from TMEM once, right when it is ready
-                //      (TMEM reads stall while the next MMA runs, so pass 2 must not go
-                //      back to TMEM); masked cells become -inf; row max in 4 chains ----
-                uint32_t sb[128];
-                tc::ld128(lane_base + (uint32_t)(j & 1) * 128u, sb);   // warp collective
+                // ---- my 64 columns of S -> registers, read from TMEM once, right when
+                //      ready (TMEM reads stall behind running MMAs); masked -> -inf ----
+                uint32_t sb[64];
+                tc::ld64(lane_base + (uint32_t)(j & 1) * 128u, sb);   // warp collective
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                 if (!live) {
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) sb[c] = __float_as_uint(-INFINITY);
+                    for (int c = 0; c < 64; ++c) sb[c] = __float_as_uint(-INFINITY);
                 } else if (!full) {
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        const bool vis = mt.has[c] && (!a.u.causal || mt.cpos[c] <= rpos);
+                    for (int c = 0; c < 64; ++c) {
+                        const int cc = 64 * ch + c;
+                        const bool vis = mt.has[cc] && (!a.u.causal || mt.cpos[cc] <= rpos);
                         if (!vis) sb[c] = __float_as_uint(-INFINITY);
                     }
                 }
 #pragma unroll
-                for (int c = 0; c < 128; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sb[c]));
-                const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+                for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sb[c]));
+                // ---- row maximum over both halves (double-buffered by pair parity) ----
+                x.red[j & 1][ch][n] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                kvd::mbar_arrive(&x.rbar);
+                ok = __all_sync(0xffffffffu, wait_or_fail(&x.rbar, n_r & 1u, fail));
+                ++n_r;
+                if (!ok) break;
+                const float tmax = fmaxf(x.red[j & 1][0][n], x.red[j & 1][1][n]) * a.scale_log2;
                 const float m_new = fmaxf(m_run, tmax);
                 const bool grow = m_new > m_run + RESCALE_LOG2 || (m_run == -INFINITY && m_new != -INFINITY);
                 float alpha = 1.f;
@@ -450,17 +473,16 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     ++n_pv;
                     tc::fence_after();
                 }
-                // ---- pass 2 (from registers): P = 2^(s*scale - m) as fp16, straight to
-                //      shared memory (128-byte swizzled K-major); one exponential in four
-                //      on the FMA pipe, the rest on the MUFU unit; row sum in 4 chains ----
+                // ---- P = 2^(s*scale - m) as fp16 into P half ch (128-byte swizzled
+                //      K-major); one exponential in four on the FMA pipe ----
                 {
-                    uint8_t *ps = smem + OFF_P;
+                    uint8_t *ps = smem + OFF_P + ch * HALF;
                     const bool any = m_run != -INFINITY;   // false for lanes past the block
                     const float nm = -m_run;
                     const float sc = a.scale_log2;
                     float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int c8 = 0; c8 < 16; ++c8) {
+                    for (int c8 = 0; c8 < 8; ++c8) {
                         uint32_t w[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -475,18 +497,16 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                             __half2 hv = __floats2half2_rn(p0, p1);
                             w[e] = *reinterpret_cast<uint32_t *>(&hv);
                         }
-                        *reinterpret_cast<uint4 *>(ps + (c8 >> 3) * HALF + kvd::swz128(n, c8 & 7)) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4 *>(ps + kvd::swz128(n, c8)) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                     l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 }
-                // ---- O *= alpha where the running maximum moved (rare); O is stable
-                //      since the previous PV finished, and this pair's PV waits for us ----
+                // ---- O *= alpha where the running maximum moved (rare), my 64 columns ----
                 if (j > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
-                    for (int q4 = 0; q4 < 4; ++q4) {
+                    for (int q2 = 0; q2 < 2; ++q2) {
                         uint32_t r[32];
-                        const uint32_t ta = lane_base + COL_O + (uint32_t)q4 * 32u;
+                        const uint32_t ta = lane_base + COL_O + (uint32_t)q2 * 32u;
                         tc::ld32(ta, r);
 #pragma unroll
                         for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
@@ -495,16 +515,14 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     tc::wait_st();
                 }
                 if (!full) {
-                    // V rows of cells nobody in the block sees: zero (P is 0 there; V may be garbage)
+                    // V rows of cells nobody in the block sees: zero (P is 0 there; V may
+                    // be garbage); thread (n, ch) clears d-half ch of cell n
                     ok = __all_sync(0xffffffffu, wait_or_fail(&x.v_full[st], (uint32_t)(k / STAGES) & 1u, fail));
                     if (!ok) break;
                     if (!mt.anyvis[n]) {
-                        uint8_t *vs = smem + OFF_V + st * TILEB;
+                        uint8_t *vs = smem + OFF_V + st * TILEB + ch * HALF + n * 128;
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                            for (int c = 0; c < 8; ++c)
-                                *reinterpret_cast<uint4 *>(vs + hh * HALF + n * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(vs + c * 16) = make_uint4(0, 0, 0, 0);
                     }
                 }
                 kvd::fence_proxy_async_smem();
@@ -512,109 +530,45 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 kvd::mbar_arrive(&x.p_full);
             }
             if (!ok) break;
-            // ---- epilogue: wait for the last PV, read O ----
+            // ---- epilogue: wait for the last PV, read my 64 columns of O ----
             ok = __all_sync(0xffffffffu, wait_or_fail(&x.pv_done, n_pv & 1u, fail));
             if (!ok) break;
             ++n_pv;
             tc::fence_after();
+            {
+                uint32_t r[64];
+                tc::ld64(lane_base + COL_O, r);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t r[32];
-                tc::ld32(lane_base + COL_O + (uint32_t)q4 * 32u, r);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) ov[q4 * 32 + c] = __uint_as_float(r[c]);
+                for (int c = 0; c < 64; ++c) ov[c] = __uint_as_float(r[c]);
             }
             tc::fence_before();
             }   // it.pairs > 0
+            // ---- the row sum over both halves (double-buffered by item parity) ----
+            x.lex[n_l & 1][ch][n] = l_run;
+            kvd::mbar_arrive(&x.lbar);
+            ok = __all_sync(0xffffffffu, wait_or_fail(&x.lbar, n_l & 1u, fail));
+            if (!ok) break;
+            const float l_tot = x.lex[n_l & 1][0][n] + x.lex[n_l & 1][1][n];
+            ++n_l;
             if (it.nitems == 1) {
                 if (live) {
-                    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                    const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
 #pragma unroll
-                    for (int c = 0; c < 128; c += 4)
+                    for (int c = 0; c < 64; c += 4)
                         *reinterpret_cast<float4 *>(orow + c) =
                             make_float4(ov[c] * inv, ov[c + 1] * inv, ov[c + 2] * inv, ov[c + 3] * inv);
                 }
             } else {
-                // this item's partial slot is its index among the prefill items
+                // a split block: this item's partial (its slot is its index among the
+                // prefill items); k_merge_pf combines the partials after the kernel
                 float *pp = a.part + (((int64_t)wi * a.n_head_kv + hk) * M + n) * PART_STRIDE;
-                pp[0] = m_run;
-                pp[1] = l_run;
-#pragma unroll
-                for (int c = 0; c < 128; c += 4)
-                    *reinterpret_cast<float4 *>(pp + 4 + c) = make_float4(ov[c], ov[c + 1], ov[c + 2], ov[c + 3]);
-                __threadfence();
-                tc::named_bar(1, 128);
-                if (n == 0) {
-                    const int32_t prev = atomicAdd(&a.p.counters[it.block * a.n_head_kv + hk], 1);
-                    x.flag = (prev == it.nitems - 1) ? 1 : 0;
+                if (ch == 0) {
+                    pp[0] = m_run;
+                    pp[1] = l_tot;
                 }
-                tc::named_bar(1, 128);
-                if (x.flag) {
-                    // merge.  Step 1: each thread reduces its own row's maxima and sums;
-                    // step 2: four threads per row, 32 values each, all loads independent.
-                    // The P buffer is free here and holds the per-row results.
-                    __threadfence();
-                    const int32_t first = a.p.blk_item0[it.block] - a.p.cap_dec;
-                    const int64_t istride = (int64_t)a.n_head_kv * M * PART_STRIDE;
-                    const float *base = a.part + ((int64_t)first * a.n_head_kv + hk) * M * PART_STRIDE;
-                    float *mrow = reinterpret_cast<float *>(smem + OFF_P);
-                    float *irow = mrow + M;
-                    int32_t *rrow = reinterpret_cast<int32_t *>(irow + M);
-                    {
-                        const float *pr = base + (int64_t)n * PART_STRIDE;
-                        float M_ = -INFINITY;
-                        for (int32_t q = 0; q < it.nitems; ++q) M_ = fmaxf(M_, __ldcg(pr + q * istride));
-                        float L = 0.f;
-                        if (M_ != -INFINITY)
-                            for (int32_t q = 0; q < it.nitems; ++q) {
-                                const float mk = __ldcg(pr + q * istride);
-                                if (mk != -INFINITY) L = fmaf(__ldcg(pr + q * istride + 1), ex2_approx(mk - M_), L);
-                            }
-                        mrow[n] = M_;
-                        irow[n] = L > 0.f ? 1.f / L : 0.f;
-                        rrow[n] = row;
-                    }
-                    tc::named_bar(1, 128);
-                    const int32_t qd = n & 3;            // which 32 values of the row
-#pragma unroll 1
-                    for (int32_t pass = 0; pass < 4; ++pass) {
-                        const int32_t r = pass * 32 + (n >> 2);
-                        const int32_t orow_id = rrow[r];
-                        const float Mr = mrow[r];
-                        const float inv = irow[r];
-                        float acc[32];
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) acc[c] = 0.f;
-                        if (orow_id >= 0 && Mr != -INFINITY) {
-                            const float *pr = base + (int64_t)r * PART_STRIDE;
-                            for (int32_t q = 0; q < it.nitems; ++q) {
-                                const float *pq = pr + q * istride;
-                                const float mk = __ldcg(pq);
-                                float4 v[8];
-#pragma unroll
-                                for (int c = 0; c < 8; ++c)
-                                    v[c] = __ldcg(reinterpret_cast<const float4 *>(pq + 4 + 32 * qd) + c);
-                                const float sc = mk == -INFINITY ? 0.f : ex2_approx(mk - Mr);
-#pragma unroll
-                                for (int c = 0; c < 8; ++c) {
-                                    acc[4 * c + 0] = fmaf(v[c].x, sc, acc[4 * c + 0]);
-                                    acc[4 * c + 1] = fmaf(v[c].y, sc, acc[4 * c + 1]);
-                                    acc[4 * c + 2] = fmaf(v[c].z, sc, acc[4 * c + 2]);
-                                    acc[4 * c + 3] = fmaf(v[c].w, sc, acc[4 * c + 3]);
-                                }
-                            }
-                        }
-                        if (orow_id >= 0) {
-                            float *dst = a.o + ((int64_t)orow_id * a.n_head + hk * G + (r % G)) * 128 + 32 * qd;
-#pragma unroll
-                            for (int c = 0; c < 8; ++c)
-                                reinterpret_cast<float4 *>(dst)[c] = make_float4(acc[4 * c] * inv, acc[4 * c + 1] * inv,
-                                                                                 acc[4 * c + 2] * inv, acc[4 * c + 3] * inv);
-                        }
-                    }
-                    tc::named_bar(1, 128);   // the P buffer is written again by the next item
-                    if (n == 0) a.p.counters[it.block * a.n_head_kv + hk] = 0;
-                }
+                for (int c = 0; c < 64; c += 4)
+                    *reinterpret_cast<float4 *>(pp + 4 + 64 * ch + c) = make_float4(ov[c], ov[c + 1], ov[c + 2], ov[c + 3]);
             }
         }
     }
@@ -622,10 +576,62 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     tc::fence_before();
     __syncthreads();
     if (*fail && tid == 0) kvd::report(a.err, kvd::DERR_MMA_TIMEOUT);
-    if (warp == 5) {
+    if (warp == 9) {
         tc::fence_after();
         tc::dealloc(tmem, TMEM_COLS);
     }
+}
+
+
+// Split-K merge of the prefill path: one CTA per (prefill block, KV head);
+// blocks covered by a single item were written directly and return at once.
+// Thread t takes row t / 2 and half of its 128 values, so every load is
+// independent of the others:  O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
+__global__ void __launch_bounds__(256) k_merge_pf(const kvk::PrefillArgs a) {
+    const int32_t b = a.u.n_dec_blocks + blockIdx.x;
+    const int32_t hk = blockIdx.y;
+    const int32_t nitems = a.p.blk_nitems[b];
+    if (nitems <= 1) return;
+    const kvi::DevBlock blk = a.u.blocks[b];
+    const int32_t n = threadIdx.x >> 1, half = threadIdx.x & 1;
+    const int32_t G = a.gqa;
+    if (n >= blk.n_rows * G) return;
+    const int32_t row = a.u.perm[blk.row0 + n / G];
+    const int32_t h = hk * G + (n % G);
+    const int32_t first = a.p.blk_item0[b] - a.p.cap_dec;
+    const int64_t istride = (int64_t)a.n_head_kv * M * PART_STRIDE;
+    const float *pr = a.part + (((int64_t)first * a.n_head_kv + hk) * M + n) * PART_STRIDE;
+    float Mx = -INFINITY;
+    for (int32_t q = 0; q < nitems; ++q) Mx = fmaxf(Mx, __ldcg(pr + q * istride));
+    float acc[64];
+#pragma unroll
+    for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+    float L = 0.f;
+    if (Mx != -INFINITY) {
+        for (int32_t q = 0; q < nitems; ++q) {
+            const float *pq = pr + q * istride;
+            const float mk = __ldcg(pq);
+            const float lk = __ldcg(pq + 1);
+            float4 v[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = __ldcg(reinterpret_cast<const float4 *>(pq + 4 + 64 * half) + c);
+            const float sc = mk == -INFINITY ? 0.f : ex2_approx(mk - Mx);
+            L = fmaf(lk, sc, L);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                acc[4 * c + 0] = fmaf(v[c].x, sc, acc[4 * c + 0]);
+                acc[4 * c + 1] = fmaf(v[c].y, sc, acc[4 * c + 1]);
+                acc[4 * c + 2] = fmaf(v[c].z, sc, acc[4 * c + 2]);
+                acc[4 * c + 3] = fmaf(v[c].w, sc, acc[4 * c + 3]);
+            }
+        }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    float *dst = a.o + ((int64_t)row * a.n_head + h) * 128 + 64 * half;
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+        reinterpret_cast<float4 *>(dst)[c] =
+            make_float4(acc[4 * c] * inv, acc[4 * c + 1] * inv, acc[4 * c + 2] * inv, acc[4 * c + 3] * inv);
 }
 
 }  // namespace
@@ -642,6 +648,9 @@ cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, con
         attr = true;
     }
     k_prefill<<<dim3(grid_x, a.n_head_kv), NT, SMEM_BYTES, st>>>(*tm_k, *tm_v, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_merge_pf<<<dim3(a.u.n_blocks - a.u.n_dec_blocks, a.n_head_kv), 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 
