@@ -326,6 +326,10 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 }
                 tc::commit(&x.s_full[buf]);
             };
+            // Per item, a non-blocking scheduler: PV of the oldest ready P first (the
+            // softmax waits on it), then S of the next pair once its K tile has
+            // landed and its score buffer is free (the P two pairs back was taken).
+            // Nothing blocks on one condition while the other is ready.
             for (int32_t wi = i0; wi < i1 && !*fail; ++wi) {
                 const ItemInfo it = item_info(a, wi);
                 if (it.pairs == 0) continue;
@@ -333,34 +337,46 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 ++n_q;
                 tc::fence_after();
                 bool ok = true;
-                for (int32_t j = 0; j < 2 && j < it.pairs && ok; ++j) {
-                    const int32_t gi = gidx + j;
-                    ok = wait_or_fail(&x.k_full[gi % STAGES], (uint32_t)(gi / STAGES) & 1u, fail);
-                    if (ok) { tc::fence_after(); issue_s(gi, j & 1); ++n_s[j & 1]; }
-                }
-                for (int32_t j = 0; j < it.pairs && ok; ++j) {
-                    const int32_t gi = gidx + j;
-                    ok = wait_or_fail(&x.p_full, n_p & 1u, fail);
-                    if (!ok) break;
-                    ++n_p;
-                    ok = wait_or_fail(&x.v_full[gi % STAGES], (uint32_t)(gi / STAGES) & 1u, fail);
-                    if (!ok) break;
-                    tc::fence_after();
-                    const uint32_t v_addr = sbase + OFF_V + (gi % STAGES) * TILEB;
+                int32_t s_done = 0, pv_done = 0;
+                long long t_last = clock64();
+                while (pv_done < it.pairs) {
+                    bool progressed = false;
+                    if (pv_done < s_done && kvd::mbar_test_wait(&x.p_full, n_p & 1u)) {
+                        const int32_t gi = gidx + pv_done;
+                        ok = wait_or_fail(&x.v_full[gi % STAGES], (uint32_t)(gi / STAGES) & 1u, fail);
+                        if (!ok) break;
+                        ++n_p;
+                        tc::fence_after();
+                        const uint32_t v_addr = sbase + OFF_V + (gi % STAGES) * TILEB;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t aoff = (uint32_t)(kk >> 2) * HALF + (uint32_t)(kk & 3) * 32u;
-                        const uint32_t boff = (uint32_t)kk * 2048u;
-                        tc::mma_ss(tmem + COL_O, tc::sdesc_sw128(p_addr + aoff, 16, 1024),
-                                   tc::sdesc_sw128(v_addr + boff, HALF, 1024), IDESC_PV,
-                                   (j > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t aoff = (uint32_t)(kk >> 2) * HALF + (uint32_t)(kk & 3) * 32u;
+                            const uint32_t boff = (uint32_t)kk * 2048u;
+                            tc::mma_ss(tmem + COL_O, tc::sdesc_sw128(p_addr + aoff, 16, 1024),
+                                       tc::sdesc_sw128(v_addr + boff, HALF, 1024), IDESC_PV,
+                                       (pv_done > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc::commit(&x.pv_done);
+                        tc::commit(&x.kv_empty[gi % STAGES]);
+                        ++pv_done;
+                        progressed = true;
                     }
-                    tc::commit(&x.pv_done);
-                    tc::commit(&x.kv_empty[gi % STAGES]);
-                    if (j + 2 < it.pairs) {
-                        const int32_t g2 = gi + 2;
-                        ok = wait_or_fail(&x.k_full[g2 % STAGES], (uint32_t)(g2 / STAGES) & 1u, fail);
-                        if (ok) { tc::fence_after(); issue_s(g2, j & 1); ++n_s[j & 1]; }
+                    if (s_done < it.pairs && s_done <= pv_done + 1) {
+                        const int32_t gi = gidx + s_done;
+                        if (kvd::mbar_test_wait(&x.k_full[gi % STAGES], (uint32_t)(gi / STAGES) & 1u)) {
+                            tc::fence_after();
+                            issue_s(gi, s_done & 1);
+                            ++n_s[s_done & 1];
+                            ++s_done;
+                            progressed = true;
+                        }
+                    }
+                    if (progressed) {
+                        t_last = clock64();
+                    } else if (*fail || clock64() - t_last > kvd::WAIT_LIMIT_CYCLES) {
+                        *fail = 1;
+                        ok = false;
+                        break;
                     }
                 }
                 gidx += it.pairs;
