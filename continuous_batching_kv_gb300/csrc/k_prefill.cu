@@ -59,9 +59,12 @@ constexpr float RESCALE_LOG2 = 8.0f;
 constexpr uint32_t IDESC_S = tc::idesc_f16(128, 128, 0, 0);
 constexpr uint32_t IDESC_PV = tc::idesc_f16(128, 128, 0, 1);
 
-struct Meta {                 // per stage: what the producer learned about the pair tile
+constexpr int MSLOTS = 4;     // metadata ring: a slot outlives its K slot until the softmax is done
+
+struct Meta {                 // per pair tile: what the producer learned about it
     int32_t full;
-    int32_t pad[3];
+    int32_t ys[2];            // TMA row coordinates of the two 64-cell halves
+    int32_t pad;
     int32_t cpos[128];
     uint8_t has[128];         // cell holds the block's sequence and is not from a later ubatch
     uint8_t anyvis[128];      // ... and some row of the block may see it
@@ -73,14 +76,15 @@ struct ItemSlot {             // per work item: the query vector behind each TME
 };
 
 struct __align__(16) Aux {
-    uint64_t k_full[STAGES], v_full[STAGES], kv_empty[STAGES];
+    uint64_t k_full[STAGES], v_full[STAGES], k_empty[STAGES], v_empty[STAGES];
+    uint64_t meta_full[MSLOTS];
     uint64_t s_full[2], p_full, pv_done, q_full, spare;
     uint64_t rbar, lbar;      // softmax-group exchanges (row maxima, row sums), all 256 threads
     uint32_t tmem_base;
     int32_t fail;
     int32_t flag;
     int32_t pad;
-    Meta meta[STAGES];
+    Meta meta[MSLOTS];
     ItemSlot islot[2];
     float red[2][2][M];       // [pair parity][column half][row]: partial row maxima
     float lex[2][2][M];       // [item parity][column half][row]: partial row sums
@@ -169,10 +173,12 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         kvd::prefetch_tmap(&tm_k);
         kvd::prefetch_tmap(&tm_v);
         for (int s = 0; s < STAGES; ++s) {
-            kvd::mbar_init(&x.k_full[s], 33);   // lane 0's expect_tx + 32 producer lanes
+            kvd::mbar_init(&x.k_full[s], 1);
             kvd::mbar_init(&x.v_full[s], 1);
-            kvd::mbar_init(&x.kv_empty[s], 1);
+            kvd::mbar_init(&x.k_empty[s], 1);
+            kvd::mbar_init(&x.v_empty[s], 1);
         }
+        for (int s = 0; s < MSLOTS; ++s) kvd::mbar_init(&x.meta_full[s], 32);
         kvd::mbar_init(&x.s_full[0], 1);
         kvd::mbar_init(&x.s_full[1], 1);
         kvd::mbar_init(&x.p_full, NSM);
@@ -195,117 +201,164 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
 
     if (warp == 8) {
         // ===================== producer (whole warp) =====================
+        // K and V tiles live in separate 2-slot rings: K of pair g + 2 loads as soon
+        // as S of pair g has consumed K of g; V of g + 2 as soon as PV of g is done.
+        // Two cursors walk the CTA's pair sequence; whichever load may go is issued
+        // (decisions by lane 0, broadcast), nothing waits on one while the other is
+        // ready.  The K load also publishes the pair's metadata (and, for an item's
+        // first pair, its lane table) through meta_full.
         const int32_t lane = tid & 31;
-        int32_t issued = 0, nonempty = 0;
-        for (int32_t wi = i0; wi < i1 && warp_ok(fail); ++wi) {
-            const ItemInfo it = item_info(a, wi);
-            if (it.pairs == 0) continue;
-            const kvi::DevBlock b = a.u.blocks[it.block];
-            const int32_t nqv = b.n_rows * G;
-            ItemSlot &is = x.islot[nonempty & 1];
-            ++nonempty;
-            const int32_t *list = a.p.tiles + (int64_t)it.block * a.p.tile_stride;
-            const uint32_t *flg = a.p.flags + (int64_t)it.block * a.p.tile_stride;
-            for (int32_t j = 0; j < it.pairs; ++j) {
-                const int32_t st = issued % STAGES;
-                // everything this pair needs from global memory, fetched before the
-                // stage is free so that only the TMA issue waits for it
-                int32_t tt[2];
-                bool fullh[2];
-                for (int h = 0; h < 2; ++h) {
-                    const int32_t e = it.t0 + 2 * j + h;
-                    tt[h] = e < it.t1 ? list[e] : -1;
-                    fullh[h] = tt[h] >= 0 && (int32_t)(flg[tt[h]] & 0xffffu) == b.n_rows * TILE;
-                }
-                const bool full = fullh[0] && fullh[1];
-                bool mhas[4], many[4];
-                int32_t mpos[4];
-                if (!full) {
+        int32_t total = 0;
+        for (int32_t wi = i0; wi < i1; ++wi) total += item_info(a, wi).pairs;
+        int32_t kc = 0, vc = 0, nonempty = 0;
+        int32_t kwi = i0, kj = 0;              // K cursor: item and pair within it
+        ItemInfo kit{};
+        kvi::DevBlock kb{};
+        bool have_k = false;
+        int32_t tt[2] = {-1, -1};
+        bool full = false;
+        bool mhas[4] = {false, false, false, false}, many[4] = {false, false, false, false};
+        int32_t mpos[4] = {0, 0, 0, 0}, lrow[4] = {-1, -1, -1, -1}, lpos[4] = {0, 0, 0, 0};
+        long long t_last = clock64();
+        while (vc < total) {
+            if (!warp_ok(fail)) break;
+            bool prog = false;
+            if (kc < total) {
+                if (!have_k) {
+                    // the next K load's global reads, done before its slot is free
+                    while (true) {
+                        kit = item_info(a, kwi);
+                        if (kj < kit.pairs) break;
+                        ++kwi;
+                        kj = 0;
+                    }
+                    kb = a.u.blocks[kit.block];
+                    const int32_t *list = a.p.tiles + (int64_t)kit.block * a.p.tile_stride;
+                    const uint32_t *flg = a.p.flags + (int64_t)kit.block * a.p.tile_stride;
+                    bool fullh[2];
+                    for (int h = 0; h < 2; ++h) {
+                        const int32_t e = kit.t0 + 2 * kj + h;
+                        tt[h] = e < kit.t1 ? list[e] : -1;
+                        fullh[h] = tt[h] >= 0 && (int32_t)(flg[tt[h]] & 0xffffu) == kb.n_rows * TILE;
+                    }
+                    full = fullh[0] && fullh[1];
+                    if (!full) {
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int32_t c = lane + 32 * r;
-                        const int32_t t = tt[c >> 6];
-                        bool has = false;
-                        int32_t cp = 0;
-                        if (t >= 0) {
-                            const int32_t jc = t * TILE + (c & 63);
-                            if (jc < a.u.n_kv) {
-                                const int64_t g = (int64_t)b.stream * a.u.kv_size + jc;
-                                const uint64_t w = a.u.cell_bits[g * a.u.n_words + (b.seq0 >> 6)];
-                                has = ((w >> (b.seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
-                                cp = a.u.cell_pos[g];
+                        for (int r = 0; r < 4; ++r) {
+                            const int32_t c = lane + 32 * r;
+                            const int32_t t = tt[c >> 6];
+                            bool has = false;
+                            int32_t cp = 0;
+                            if (t >= 0) {
+                                const int32_t jc = t * TILE + (c & 63);
+                                if (jc < a.u.n_kv) {
+                                    const int64_t g = (int64_t)kb.stream * a.u.kv_size + jc;
+                                    const uint64_t w = a.u.cell_bits[g * a.u.n_words + (kb.seq0 >> 6)];
+                                    has = ((w >> (kb.seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
+                                    cp = a.u.cell_pos[g];
+                                }
+                            }
+                            mhas[r] = has;
+                            mpos[r] = cp;
+                            many[r] = has && (!a.u.causal || cp <= kb.pos_max);
+                        }
+                    }
+                    if (kj == 0) {
+                        const int32_t nqv = kb.n_rows * G;
+                        for (int r = 0; r < 4; ++r) {
+                            const int32_t n = lane + 32 * r;
+                            lrow[r] = -1;
+                            lpos[r] = 0;
+                            if (n < nqv) {
+                                lrow[r] = a.u.perm[kb.row0 + n / G];
+                                lpos[r] = a.u.rows[lrow[r]].pos;
                             }
                         }
-                        mhas[r] = has;
-                        mpos[r] = cp;
-                        many[r] = has && (!a.u.causal || cp <= b.pos_max);
                     }
+                    have_k = true;
                 }
-                int32_t lrow[4], lpos[4];
-                if (j == 0) {
-                    for (int r = 0; r < 4; ++r) {
-                        const int32_t n = lane + 32 * r;
-                        lrow[r] = -1;
-                        lpos[r] = 0;
-                        if (n < nqv) {
-                            lrow[r] = a.u.perm[b.row0 + n / G];
-                            lpos[r] = a.u.rows[lrow[r]].pos;
+                const int32_t st = kc % STAGES;
+                bool ready = kc < STAGES ||
+                             kvd::mbar_test_wait(&x.k_empty[st], (uint32_t)((kc / STAGES) - 1) & 1u);
+                ready = __shfl_sync(0xffffffffu, ready, 0);
+                if (ready) {
+                    Meta &mt = x.meta[kc % MSLOTS];
+                    if (kj == 0) {
+                        // the item's lane table; its previous reader (two non-empty items
+                        // back) read it before any of its S products, and this K slot
+                        // was just freed by such an S product
+                        ItemSlot &is = x.islot[nonempty & 1];
+                        for (int r = 0; r < 4; ++r) {
+                            is.row[lane + 32 * r] = lrow[r];
+                            is.rpos[lane + 32 * r] = lpos[r];
+                        }
+                        ++nonempty;
+                    }
+                    if (lane == 0) {
+                        for (int h = 0; h < 2; ++h)   // a missing second tile: out of bounds, TMA writes zeros
+                            mt.ys[h] = tt[h] >= 0 ? kb.stream * a.u.kv_size + tt[h] * TILE : -TILE;
+                        mt.full = full ? 1 : 0;
+                        uint8_t *ks = smem + OFF_K + st * TILEB;
+                        const int32_t xk = hk * 128;
+                        kvd::fence_proxy_async_smem();
+                        kvd::mbar_arrive_expect_tx(&x.k_full[st], TILEB);
+                        for (int h = 0; h < 2; ++h) {
+                            kvd::tma_load_2d(ks + h * BOX, &tm_k, xk, mt.ys[h], &x.k_full[st]);
+                            kvd::tma_load_2d(ks + HALF + h * BOX, &tm_k, xk + 64, mt.ys[h], &x.k_full[st]);
                         }
                     }
-                }
-                if (issued >= STAGES &&
-                    !__all_sync(0xffffffffu,
-                                wait_or_fail(&x.kv_empty[st], (uint32_t)((issued / STAGES) - 1) & 1u, fail)))
-                    break;
-                if (j == 0) {
-                    // the item's lane table; the slot's previous reader started two or more
-                    // loads ago, and this load's stage was just released, so it is done with it
-                    for (int r = 0; r < 4; ++r) {
-                        is.row[lane + 32 * r] = lrow[r];
-                        is.rpos[lane + 32 * r] = lpos[r];
-                    }
-                }
-                Meta &mt = x.meta[st];
-                if (lane == 0) {
-                    int32_t ys[2];
-                    for (int h = 0; h < 2; ++h)   // a missing second tile: out of bounds, TMA writes zeros
-                        ys[h] = tt[h] >= 0 ? b.stream * a.u.kv_size + tt[h] * TILE : -TILE;
-                    uint8_t *ks = smem + OFF_K + st * TILEB;
-                    uint8_t *vs = smem + OFF_V + st * TILEB;
-                    const int32_t xk = hk * 128;
-                    kvd::fence_proxy_async_smem();
-                    kvd::mbar_arrive_expect_tx(&x.k_full[st], TILEB);
-                    for (int h = 0; h < 2; ++h) {
-                        kvd::tma_load_2d(ks + h * BOX, &tm_k, xk, ys[h], &x.k_full[st]);
-                        kvd::tma_load_2d(ks + HALF + h * BOX, &tm_k, xk + 64, ys[h], &x.k_full[st]);
-                    }
-                    kvd::mbar_arrive_expect_tx(&x.v_full[st], TILEB);
-                    for (int h = 0; h < 2; ++h) {
-                        kvd::tma_load_2d(vs + h * BOX, &tm_v, xk, ys[h], &x.v_full[st]);
-                        kvd::tma_load_2d(vs + HALF + h * BOX, &tm_v, xk + 64, ys[h], &x.v_full[st]);
-                    }
-                    mt.full = full ? 1 : 0;
-                }
-                if (!full) {
+                    if (!full) {
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int32_t c = lane + 32 * r;
-                        mt.has[c] = mhas[r] ? 1 : 0;
-                        mt.cpos[c] = mpos[r];
-                        mt.anyvis[c] = many[r] ? 1 : 0;
+                        for (int r = 0; r < 4; ++r) {
+                            const int32_t c = lane + 32 * r;
+                            mt.has[c] = mhas[r] ? 1 : 0;
+                            mt.cpos[c] = mpos[r];
+                            mt.anyvis[c] = many[r] ? 1 : 0;
+                        }
                     }
+                    __syncwarp();
+                    kvd::mbar_arrive(&x.meta_full[kc % MSLOTS]);
+                    ++kc;
+                    ++kj;
+                    have_k = false;
+                    prog = true;
                 }
-                __syncwarp();
-                kvd::mbar_arrive(&x.k_full[st]);
-                ++issued;
+            }
+            if (vc < kc) {
+                const int32_t st = vc % STAGES;
+                bool ready = vc < STAGES ||
+                             kvd::mbar_test_wait(&x.v_empty[st], (uint32_t)((vc / STAGES) - 1) & 1u);
+                ready = __shfl_sync(0xffffffffu, ready, 0);
+                if (ready) {
+                    if (lane == 0) {
+                        const Meta &mt = x.meta[vc % MSLOTS];   // still intact: K of vc + 4 needs PV of vc
+                        uint8_t *vs = smem + OFF_V + st * TILEB;
+                        const int32_t xk = hk * 128;
+                        kvd::fence_proxy_async_smem();
+                        kvd::mbar_arrive_expect_tx(&x.v_full[st], TILEB);
+                        for (int h = 0; h < 2; ++h) {
+                            kvd::tma_load_2d(vs + h * BOX, &tm_v, xk, mt.ys[h], &x.v_full[st]);
+                            kvd::tma_load_2d(vs + HALF + h * BOX, &tm_v, xk + 64, mt.ys[h], &x.v_full[st]);
+                        }
+                    }
+                    __syncwarp();
+                    ++vc;
+                    prog = true;
+                }
+            }
+            if (prog) {
+                t_last = clock64();
+            } else if (__shfl_sync(0xffffffffu, clock64() - t_last > kvd::WAIT_LIMIT_CYCLES ? 1 : 0, 0)) {
+                if (lane == 0) *fail = 1;
+                break;
             }
         }
         if (*fail && lane == 0) {
             // let loads already issued land before the CTA exits
-            for (int32_t q = issued > STAGES ? issued - STAGES : 0; q < issued; ++q) {
+            for (int32_t q = kc > STAGES ? kc - STAGES : 0; q < kc; ++q)
                 (void)kvd::mbar_wait_bounded(&x.k_full[q % STAGES], (uint32_t)(q / STAGES) & 1u);
+            for (int32_t q = vc > STAGES ? vc - STAGES : 0; q < vc; ++q)
                 (void)kvd::mbar_wait_bounded(&x.v_full[q % STAGES], (uint32_t)(q / STAGES) & 1u);
-            }
         }
     } else if (warp == 9) {
         // ===================== MMA issuer =====================
@@ -325,6 +378,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                                IDESC_S, kk > 0 ? 1u : 0u);
                 }
                 tc::commit(&x.s_full[buf]);
+                tc::commit(&x.k_empty[gi % STAGES]);   // this K tile is consumed
             };
             // Per item, a non-blocking scheduler: PV of the oldest ready P first (the
             // softmax waits on it), then S of the next pair once its K tile has
@@ -357,7 +411,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                                        (pv_done > 0 || kk > 0) ? 1u : 0u);
                         }
                         tc::commit(&x.pv_done);
-                        tc::commit(&x.kv_empty[gi % STAGES]);
+                        tc::commit(&x.v_empty[gi % STAGES]);
                         ++pv_done;
                         progressed = true;
                     }
@@ -410,8 +464,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 const kvi::DevBlock b = a.u.blocks[it.block];
                 if (n < b.n_rows * G) row = a.u.perm[b.row0 + n / G];
             } else {
-                // the first pair's arrival also publishes this item's lane table
-                ok = __all_sync(0xffffffffu, wait_or_fail(&x.k_full[k % STAGES], (uint32_t)(k / STAGES) & 1u, fail));
+                // the first pair's metadata also publishes this item's lane table
+                ok = __all_sync(0xffffffffu, wait_or_fail(&x.meta_full[k % MSLOTS], (uint32_t)(k / MSLOTS) & 1u, fail));
                 if (!ok) break;
                 const ItemSlot &is = x.islot[nonempty & 1];
                 ++nonempty;
@@ -441,9 +495,9 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             }
             for (int32_t j = 0; j < it.pairs; ++j, ++k) {
                 const int32_t st = k % STAGES;
-                ok = __all_sync(0xffffffffu, wait_or_fail(&x.k_full[st], (uint32_t)(k / STAGES) & 1u, fail));
+                ok = __all_sync(0xffffffffu, wait_or_fail(&x.meta_full[k % MSLOTS], (uint32_t)(k / MSLOTS) & 1u, fail));
                 if (!ok) break;
-                const Meta &mt = x.meta[st];
+                const Meta &mt = x.meta[k % MSLOTS];
                 const bool full = mt.full != 0;
                 ok = __all_sync(0xffffffffu, wait_or_fail(&x.s_full[j & 1], n_s[j & 1] & 1u, fail));
                 if (!ok) break;
