@@ -55,6 +55,7 @@ constexpr int PART_STRIDE = 132;
 constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128), S1 [128,256), O [256,384)
 constexpr uint32_t COL_O = 256;
 constexpr float RESCALE_LOG2 = 8.0f;
+constexpr unsigned POLL_NS = 32;         // back-off of the polling producer / MMA loops
 
 constexpr uint32_t IDESC_S = tc::idesc_f16(128, 128, 0, 0);
 constexpr uint32_t IDESC_PV = tc::idesc_f16(128, 128, 0, 1);
@@ -351,6 +352,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             } else if (__shfl_sync(0xffffffffu, clock64() - t_last > kvd::WAIT_LIMIT_CYCLES ? 1 : 0, 0)) {
                 if (lane == 0) *fail = 1;
                 break;
+            } else {
+                __nanosleep(POLL_NS);   // leave the issue slots to the softmax warps
             }
         }
         if (*fail && lane == 0) {
@@ -431,6 +434,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         *fail = 1;
                         ok = false;
                         break;
+                    } else {
+                        __nanosleep(POLL_NS);   // leave the issue slots to the softmax warps
                     }
                 }
                 gidx += it.pairs;
