@@ -47,13 +47,13 @@ constexpr int TILEB = 2 * HALF;          // 32 KiB
 constexpr int BOX = 64 * 128;            // one TMA box: 64 rows x 64 fp16
 constexpr int STAGES = 2;
 constexpr int OFF_Q = 0;
-constexpr int OFF_P = OFF_Q + TILEB;
-constexpr int OFF_K = OFF_P + TILEB;
+constexpr int OFF_K = OFF_Q + TILEB;
 constexpr int OFF_V = OFF_K + STAGES * TILEB;
 constexpr int OFF_AUX = OFF_V + STAGES * TILEB;
 constexpr int PART_STRIDE = 132;
-constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128), S1 [128,256), O [256,384)
+constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128), S1 [128,256), O [256,384), P0, P1 [384,512)
 constexpr uint32_t COL_O = 256;
+constexpr uint32_t COL_P = 384;          // P of pair g: fp16, 64 columns at COL_P + 64 (g & 1)
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr unsigned POLL_NS = 32;         // back-off of the polling producer / MMA loops
 
@@ -79,7 +79,7 @@ struct ItemSlot {             // per work item: the query vector behind each TME
 struct __align__(16) Aux {
     uint64_t k_full[STAGES], v_full[STAGES], k_empty[STAGES], v_empty[STAGES];
     uint64_t meta_full[MSLOTS];
-    uint64_t s_full[2], p_full, pv_done, q_full, spare;
+    uint64_t s_full[2], p_full, pv_done[2], q_full, spare;   // pv_done[g & 1]: PV of pair g
     uint64_t rbar, lbar;      // softmax-group exchanges (row maxima, row sums), all 256 threads
     uint32_t tmem_base;
     int32_t fail;
@@ -183,7 +183,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         kvd::mbar_init(&x.s_full[0], 1);
         kvd::mbar_init(&x.s_full[1], 1);
         kvd::mbar_init(&x.p_full, NSM);
-        kvd::mbar_init(&x.pv_done, 1);
+        kvd::mbar_init(&x.pv_done[0], 1);
+        kvd::mbar_init(&x.pv_done[1], 1);
         kvd::mbar_init(&x.q_full, NSM);
         kvd::mbar_init(&x.spare, 1);
         kvd::mbar_init(&x.rbar, NSM);
@@ -370,7 +371,6 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             uint32_t n_q = 0, n_p = 0;
             uint32_t n_s[2] = {0, 0};
             const uint32_t q_addr = sbase + OFF_Q;
-            const uint32_t p_addr = sbase + OFF_P;
             auto issue_s = [&](int32_t gi, int32_t buf) {
                 const uint32_t k_addr = sbase + OFF_K + (gi % STAGES) * TILEB;
                 const uint32_t d = tmem + (uint32_t)buf * 128u;
@@ -405,15 +405,15 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         ++n_p;
                         tc::fence_after();
                         const uint32_t v_addr = sbase + OFF_V + (gi % STAGES) * TILEB;
+                        const uint32_t p_tmem = tmem + COL_P + 64u * (uint32_t)(gi & 1);
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t aoff = (uint32_t)(kk >> 2) * HALF + (uint32_t)(kk & 3) * 32u;
+                        for (int kk = 0; kk < 8; ++kk) {   // K = 16 cells = 8 TMEM columns of P
                             const uint32_t boff = (uint32_t)kk * 2048u;
-                            tc::mma_ss(tmem + COL_O, tc::sdesc_sw128(p_addr + aoff, 16, 1024),
+                            tc::mma_ts(tmem + COL_O, p_tmem + 8u * (uint32_t)kk,
                                        tc::sdesc_sw128(v_addr + boff, HALF, 1024), IDESC_PV,
                                        (pv_done > 0 || kk > 0) ? 1u : 0u);
                         }
-                        tc::commit(&x.pv_done);
+                        tc::commit(&x.pv_done[gi & 1]);
                         tc::commit(&x.v_empty[gi % STAGES]);
                         ++pv_done;
                         progressed = true;
@@ -454,7 +454,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         const int32_t ch = tid >> 7;           // column half
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(64 * ch);
         uint32_t n_s[2] = {0, 0};
-        uint32_t n_pv = 0, n_r = 0, n_l = 0;
+        uint32_t n_r = 0, n_l = 0;
         int32_t k = 0;                         // pair tiles consumed (stage ring position)
         int32_t nonempty = 0;
         bool ok = true;
@@ -541,43 +541,47 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     m_run = m_new;
                     l_run *= alpha;
                 }
-                // ---- P buffer free and O stable once the previous PV finished ----
-                if (j > 0) {
-                    ok = __all_sync(0xffffffffu, wait_or_fail(&x.pv_done, n_pv & 1u, fail));
+                // ---- P buffer k & 1 is free once PV of pair k - 2 finished (it read it);
+                //      that wait is nearly always already satisfied ----
+                if (k >= 2) {
+                    ok = __all_sync(0xffffffffu,
+                                    wait_or_fail(&x.pv_done[k & 1], (uint32_t)((k - 2) >> 1) & 1u, fail));
                     if (!ok) break;
-                    ++n_pv;
                     tc::fence_after();
                 }
-                // ---- P = 2^(s*scale - m) as fp16 into P half ch (128-byte swizzled
-                //      K-major); one exponential in four on the FMA pipe ----
+                // ---- P = 2^(s*scale - m) as fp16 into TMEM P buffer k & 1: my 64 cells
+                //      are 32 columns (two fp16 per column, lower cell in the low half);
+                //      one exponential in four on the FMA pipe ----
                 {
-                    uint8_t *ps = smem + OFF_P + ch * HALF;
                     const bool any = m_run != -INFINITY;   // false for lanes past the block
                     const float nm = -m_run;
                     const float sc = a.scale_log2;
                     float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                    uint32_t pw[32];
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c = c8 * 8 + 2 * e;
-                            const float x0 = fmaf(__uint_as_float(sb[c]), sc, nm);
-                            const float x1 = fmaf(__uint_as_float(sb[c + 1]), sc, nm);
-                            float p0 = ex2_approx(x0);
-                            float p1 = (e & 1) ? ex2_poly(x1) : ex2_approx(x1);
-                            p0 = any ? p0 : 0.f;
-                            p1 = any ? p1 : 0.f;
-                            ls[e] += p0 + p1;
-                            __half2 hv = __floats2half2_rn(p0, p1);
-                            w[e] = *reinterpret_cast<uint32_t *>(&hv);
-                        }
-                        *reinterpret_cast<uint4 *>(ps + kvd::swz128(n, c8)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int c2 = 0; c2 < 32; ++c2) {
+                        const int c = 2 * c2;
+                        const float x0 = fmaf(__uint_as_float(sb[c]), sc, nm);
+                        const float x1 = fmaf(__uint_as_float(sb[c + 1]), sc, nm);
+                        float p0 = ex2_approx(x0);
+                        float p1 = (c2 & 1) ? ex2_poly(x1) : ex2_approx(x1);
+                        p0 = any ? p0 : 0.f;
+                        p1 = any ? p1 : 0.f;
+                        ls[c2 & 3] += p0 + p1;
+                        __half2 hv = __floats2half2_rn(p0, p1);
+                        pw[c2] = *reinterpret_cast<uint32_t *>(&hv);
                     }
                     l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                    tc::st32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + COL_P + 64u * (uint32_t)(k & 1) +
+                                 32u * (uint32_t)ch, pw);
                 }
-                // ---- O *= alpha where the running maximum moved (rare), my 64 columns ----
+                // ---- O *= alpha where the running maximum moved (rare), my 64 columns;
+                //      O is stable once PV of pair k - 1 finished ----
                 if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                    ok = __all_sync(0xffffffffu,
+                                    wait_or_fail(&x.pv_done[(k - 1) & 1], (uint32_t)((k - 1) >> 1) & 1u, fail));
+                    if (!ok) break;
+                    tc::fence_after();
 #pragma unroll 1
                     for (int q2 = 0; q2 < 2; ++q2) {
                         uint32_t r[32];
@@ -600,15 +604,16 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(vs + c * 16) = make_uint4(0, 0, 0, 0);
                     }
                 }
-                kvd::fence_proxy_async_smem();
+                tc::wait_st();                     // P (and a rescaled O) are in TMEM
+                kvd::fence_proxy_async_smem();     // zeroed V rows are visible to the MMA
                 tc::fence_before();
                 kvd::mbar_arrive(&x.p_full);
             }
             if (!ok) break;
-            // ---- epilogue: wait for the last PV, read my 64 columns of O ----
-            ok = __all_sync(0xffffffffu, wait_or_fail(&x.pv_done, n_pv & 1u, fail));
+            // ---- epilogue: wait for the last PV (pair k - 1), read my 64 columns of O ----
+            ok = __all_sync(0xffffffffu,
+                            wait_or_fail(&x.pv_done[(k - 1) & 1], (uint32_t)((k - 1) >> 1) & 1u, fail));
             if (!ok) break;
-            ++n_pv;
             tc::fence_after();
             {
                 uint32_t r[64];
