@@ -15,8 +15,9 @@
 //    ring, with each tile's list entry, flags and per-cell visibility
 //    fetched ahead into the same slot; warp 9 allocates TMEM and one thread issues
 //    tcgen05.mma: S = Q K^T (M 128, N 128, K 128) into one of two TMEM score
-//    buffers, then O += P V (K = 128 cells, V read MN-major) into a TMEM
-//    accumulator; tcgen05.commit signals the mbarriers;
+//    buffers as soon as the softmax has read that buffer, and O += P V with P
+//    read from TMEM (double-buffered, fp16) and V MN-major from shared memory
+//    into a TMEM accumulator; tcgen05.commit signals the mbarriers;
 //  * warps 0-7 (two threads per TMEM lane = query vector, 64 columns each)
 //    read S with one tcgen05.ld as soon as it lands (TMEM reads stall behind
 //    running MMAs), apply the mask per cell on tiles that are not fully
@@ -60,7 +61,11 @@ constexpr unsigned POLL_NS = 32;         // back-off of the polling producer / M
 constexpr uint32_t IDESC_S = tc::idesc_f16(128, 128, 0, 0);
 constexpr uint32_t IDESC_PV = tc::idesc_f16(128, 128, 0, 1);
 
-constexpr int MSLOTS = 4;     // metadata ring: a slot outlives its K slot until the softmax is done
+// Metadata ring.  Pair g's slot is rewritten by the K load of pair g + 8, which
+// needs S of g + 6, which needs the softmax to have read S of g + 4: by then the
+// softmax is done with pair g, and PV of g (hence the V load of g, which reads
+// the slot) was issued before the softmax of g + 2 wrote its P.
+constexpr int MSLOTS = 8;
 
 struct Meta {                 // per pair tile: what the producer learned about it
     int32_t full;
@@ -79,7 +84,8 @@ struct ItemSlot {             // per work item: the query vector behind each TME
 struct __align__(16) Aux {
     uint64_t k_full[STAGES], v_full[STAGES], k_empty[STAGES], v_empty[STAGES];
     uint64_t meta_full[MSLOTS];
-    uint64_t s_full[2], p_full, pv_done[2], q_full, spare;   // pv_done[g & 1]: PV of pair g
+    uint64_t s_full[2], p_full[2], pv_done[2], q_full, spare;   // p_full, pv_done [g & 1]: pair g
+    uint64_t s_free[2];       // a score buffer was read into registers by all 256 softmax threads
     uint64_t rbar, lbar;      // softmax-group exchanges (row maxima, row sums), all 256 threads
     uint32_t tmem_base;
     int32_t fail;
@@ -182,7 +188,10 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         for (int s = 0; s < MSLOTS; ++s) kvd::mbar_init(&x.meta_full[s], 32);
         kvd::mbar_init(&x.s_full[0], 1);
         kvd::mbar_init(&x.s_full[1], 1);
-        kvd::mbar_init(&x.p_full, NSM);
+        kvd::mbar_init(&x.s_free[0], NSM);
+        kvd::mbar_init(&x.s_free[1], NSM);
+        kvd::mbar_init(&x.p_full[0], NSM);
+        kvd::mbar_init(&x.p_full[1], NSM);
         kvd::mbar_init(&x.pv_done[0], 1);
         kvd::mbar_init(&x.pv_done[1], 1);
         kvd::mbar_init(&x.q_full, NSM);
@@ -333,7 +342,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 ready = __shfl_sync(0xffffffffu, ready, 0);
                 if (ready) {
                     if (lane == 0) {
-                        const Meta &mt = x.meta[vc % MSLOTS];   // still intact: K of vc + 4 needs PV of vc
+                        const Meta &mt = x.meta[vc % MSLOTS];   // still intact (see MSLOTS)
                         uint8_t *vs = smem + OFF_V + st * TILEB;
                         const int32_t xk = hk * 128;
                         kvd::fence_proxy_async_smem();
@@ -368,7 +377,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         // ===================== MMA issuer =====================
         if ((tid & 31) == 0) {
             int32_t gidx = 0;          // global pair-tile counter (stage ring)
-            uint32_t n_q = 0, n_p = 0;
+            uint32_t s_uses[2] = {0, 0};   // S products written into each score buffer so far
+            uint32_t n_q = 0;
             uint32_t n_s[2] = {0, 0};
             const uint32_t q_addr = sbase + OFF_Q;
             auto issue_s = [&](int32_t gi, int32_t buf) {
@@ -398,11 +408,13 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 long long t_last = clock64();
                 while (pv_done < it.pairs) {
                     bool progressed = false;
-                    if (pv_done < s_done && kvd::mbar_test_wait(&x.p_full, n_p & 1u)) {
-                        const int32_t gi = gidx + pv_done;
+                    // P of pair gi in buffer gi & 1 (a single barrier could be lapped: the
+                    // softmax may finish two pairs before this thread looks)
+                    const int32_t gp = gidx + pv_done;
+                    if (pv_done < s_done && kvd::mbar_test_wait(&x.p_full[gp & 1], (uint32_t)(gp >> 1) & 1u)) {
+                        const int32_t gi = gp;
                         ok = wait_or_fail(&x.v_full[gi % STAGES], (uint32_t)(gi / STAGES) & 1u, fail);
                         if (!ok) break;
-                        ++n_p;
                         tc::fence_after();
                         const uint32_t v_addr = sbase + OFF_V + (gi % STAGES) * TILEB;
                         const uint32_t p_tmem = tmem + COL_P + 64u * (uint32_t)(gi & 1);
@@ -418,12 +430,17 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         ++pv_done;
                         progressed = true;
                     }
-                    if (s_done < it.pairs && s_done <= pv_done + 1) {
+                    if (s_done < it.pairs) {
+                        // S of the next pair: its K tile has landed and its score buffer's
+                        // previous contents were read by the softmax
                         const int32_t gi = gidx + s_done;
-                        if (kvd::mbar_test_wait(&x.k_full[gi % STAGES], (uint32_t)(gi / STAGES) & 1u)) {
+                        const int32_t buf = s_done & 1;
+                        if (kvd::mbar_test_wait(&x.k_full[gi % STAGES], (uint32_t)(gi / STAGES) & 1u) &&
+                            (s_uses[buf] == 0 || kvd::mbar_test_wait(&x.s_free[buf], (s_uses[buf] - 1) & 1u))) {
                             tc::fence_after();
-                            issue_s(gi, s_done & 1);
-                            ++n_s[s_done & 1];
+                            issue_s(gi, buf);
+                            ++n_s[buf];
+                            ++s_uses[buf];
                             ++s_done;
                             progressed = true;
                         }
@@ -512,6 +529,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 //      ready (TMEM reads stall behind running MMAs); masked -> -inf ----
                 uint32_t sb[64];
                 tc::ld64(lane_base + (uint32_t)(j & 1) * 128u, sb);   // warp collective
+                tc::fence_before();
+                kvd::mbar_arrive(&x.s_free[j & 1]);                   // the next S may overwrite it
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                 if (!live) {
 #pragma unroll
@@ -607,7 +626,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 tc::wait_st();                     // P (and a rescaled O) are in TMEM
                 kvd::fence_proxy_async_smem();     // zeroed V rows are visible to the MMA
                 tc::fence_before();
-                kvd::mbar_arrive(&x.p_full);
+                kvd::mbar_arrive(&x.p_full[k & 1]);
             }
             if (!ok) break;
             // ---- epilogue: wait for the last PV (pair k - 1), read my 64 columns of O ----

@@ -98,6 +98,7 @@ class Pair:
                     md = torch.empty((n, u["n_kv"]), dtype=torch.int16, device="cuda")
                 kv.ubatch_attention(self.c, s, k, layer, qd, od, md)
                 torch.cuda.synchronize()
+                assert kv.kv_device_error(self.c) == 0, "device error ubatch %d layer %d" % (k, layer)
                 got = od.cpu().numpy()
                 for n_, r in enumerate(rows):
                     outs[(tuple(call["seq"][r]), call["pos"][r], layer)] = got[n_]
