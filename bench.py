@@ -129,6 +129,15 @@ class Clocks:
                 "reasons": sorted(reasons)}
 
 
+def max_over_ranks(ms, device):
+    """The slowest replica's time (every rank gets it).  Replicas share no
+    data: this reduction of one timing value is the only collective."""
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -296,11 +305,7 @@ def run_ours(args, rank, world, device):
     ms_total = t0.elapsed_time(t1)
     launches = kv.kv_launch_count(arm.c) - launches0
     assert kv.kv_device_error(arm.c) == 0
-    ms_max = ms_total
-    if dist:
-        tt = torch.tensor([ms_total], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(tt.item())
+    ms_max = max_over_ranks(ms_total, device) if dist else ms_total
     tokens = measured_tokens(cfg) * args.steps * world
     value = tokens / (ms_max / 1e3)
 
@@ -342,9 +347,7 @@ def run_ours(args, rank, world, device):
         barrier()
         ms_e2e = t0.elapsed_time(t1)
         if dist:
-            tt = torch.tensor([ms_e2e], device=device)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            ms_e2e = float(tt.item())
+            ms_e2e = max_over_ranks(ms_e2e, device)
         e2e = {"value": round(tokens / (ms_e2e / 1e3), 1), "unit": UNIT,
                "h2d_bytes_per_step": arm.input_bytes(),
                "d2h_bytes_per_step": int(sum(x.numel() * 4 for x in out))}

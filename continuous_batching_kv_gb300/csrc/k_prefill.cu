@@ -11,9 +11,10 @@
 //    sequence id, times the GQA group) = the 128 TMEM lanes of one MMA tile;
 //    a work item = one block, one KV head, a chunk of the block's list of
 //    visible 64-cell tiles, consumed two at a time (N = 128 cells);
-//  * warp 8 streams K and V tiles with TMA (128-byte swizzle) into a 2-stage
-//    ring, with each tile's list entry, flags and per-cell visibility
-//    fetched ahead into the same slot; warp 9 allocates TMEM and one thread issues
+//  * warp 8 streams K and V tiles with TMA (128-byte swizzle) into separate
+//    2-slot K and V rings, with each pair's list entries, flags and per-cell
+//    visibility fetched ahead into a metadata ring; warp 9 allocates TMEM and
+//    one thread issues
 //    tcgen05.mma: S = Q K^T (M 128, N 128, K 128) into one of two TMEM score
 //    buffers as soon as the softmax has read that buffer, and O += P V with P
 //    read from TMEM (double-buffered, fp16) and V MN-major from shared memory
@@ -22,8 +23,9 @@
 //    read S with one tcgen05.ld as soon as it lands (TMEM reads stall behind
 //    running MMAs), apply the mask per cell on tiles that are not fully
 //    visible, run the online softmax in base 2 (a quarter of the exponentials
-//    on the FMA pipe), write P (fp16) to shared memory in the swizzled K-major
-//    layout, and rescale O in TMEM only when the running maximum grew by more
+//    on the FMA pipe), write P (fp16, two cells per 32-bit column) into the
+//    TMEM P buffer of the pair's parity, and rescale O in TMEM only when the
+//    running maximum grew by more
 //    than 2^8 (otherwise the stale maximum is kept; the final normalisation
 //    uses the same one);
 //  * cells nobody in the block may see get their V rows zeroed in shared

@@ -14,6 +14,16 @@ A ubatch (BATCH-ZH, Part B) is represented as a dict with
 * ``seq_id_unq``    sorted distinct sequence ids of the ubatch.
 
 Error codes mirror the C interface: 0 ok, negative = error.
+
+Pins: the page's worked splits (5000 tokens at n_batch 2048 give calls of
+2048/2048/904 and 10 ubatches; 1000 tokens give 512 + 488, 1500 give
+512/512/476), the clamps, and brute-forced invariants on every small batch
+(each row once, per-sequence order kept, rectangular ubatches, disjoint
+sequence sets).  split_equal's choice among overlapping sequence sets and its
+"sequential" order, and split_seq's exact rows, follow a written reading of
+the pages that nothing on them fixes further: parity unpinned for those
+tie-breaks (the library must match this reading bit for bit, but no page
+value confirms the reading itself).
 """
 
 E_INVAL = -1

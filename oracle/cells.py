@@ -11,6 +11,13 @@ State per stream s and cell j:
 * ``nseq[s, j]``  how many sequences the cell belongs to (0 = empty);
 * ``bits[s, j, w]`` a plain bitset of those sequences: sequence q is bit
   q % 64 of word q // 64.
+
+Pins: the n_kv examples (700 cells used -> 768; the kv_size clamp), first-fit
+on an empty cache giving cells 0..n-1, the all-or-nothing failure (state
+unchanged, return 1) and the prefix-sharing example of BATCH-ZH, Part E.  The
+slot-finder policy beyond that (first fit from cell 0, cells not necessarily
+contiguous, rows in ubatch order) is not stated by the pages: parity
+unpinned for that policy.
 """
 
 import numpy as np
