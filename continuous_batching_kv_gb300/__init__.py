@@ -12,8 +12,8 @@ The functions keep the C names:
     kv_init, kv_free, kv_n_batch, kv_n_ubatch, kv_kv_size, kv_last_error,
     kv_split_ubatches, kv_split_count, kv_split_ubatch, kv_split_free,
     kv_prepare_cells, kv_seq_rm, kv_seq_pos_max, kv_cells_read,
-    kv_stream_n_kv, kv_store, ubatch_attention, kv_device_error,
-    kv_device_bytes, kv_launch_count
+    kv_stream_n_kv, kv_store, ubatch_attention, ubatch_attention_static_scratch,
+    kv_device_error, kv_device_bytes, kv_launch_count
 """
 
 import ctypes as C
@@ -29,12 +29,14 @@ KV_E_INVAL, KV_E_BATCH_TOO_LARGE, KV_E_SEQ_RANGE, KV_E_CROSS_STREAM = -1, -2, -3
 KV_E_ORDER, KV_E_STALE, KV_E_CUDA, KV_E_NOMEM, KV_E_NO_DEVICE = -5, -6, -7, -8, -9
 KV_SPLIT_AUTO, KV_SPLIT_SIMPLE, KV_SPLIT_EQUAL, KV_SPLIT_SEQ = 0, 1, 2, 3
 KV_MAX_SEQ, KV_HEAD_DIM = 256, 128
+KV_STATIC_SCRATCH_BYTES = 24 << 20
 
 EXPORTS = [
     "kv_init", "kv_free", "kv_n_batch", "kv_n_ubatch", "kv_kv_size", "kv_last_error",
     "kv_split_ubatches", "kv_split_count", "kv_split_ubatch", "kv_split_free",
     "kv_prepare_cells", "kv_seq_rm", "kv_seq_pos_max", "kv_cells_read", "kv_stream_n_kv",
-    "kv_store", "ubatch_attention", "kv_device_error", "kv_device_bytes", "kv_launch_count",
+    "kv_store", "ubatch_attention", "ubatch_attention_static_scratch", "kv_device_error",
+    "kv_device_bytes", "kv_launch_count",
 ]
 
 
@@ -90,6 +92,7 @@ def _load():
         "kv_stream_n_kv": (C.c_int32, [P, C.c_int32]),
         "kv_store": (C.c_int, [P, P, C.c_int32, C.c_int32, P, P, P]),
         "ubatch_attention": (C.c_int, [P, P, C.c_int32, C.c_int32, P, P, P, P]),
+        "ubatch_attention_static_scratch": (C.c_int, [P, P, C.c_int32, C.c_int32, P, P, P, P]),
         "kv_device_error": (C.c_int, [P]),
         "kv_device_bytes": (C.c_size_t, [P]),
         "kv_launch_count": (C.c_uint64, [P]),
@@ -304,6 +307,14 @@ def kv_store(c, s, ub, layer, k_cur, v_cur, stream=None):
 def ubatch_attention(c, s, ub, layer, q, o, mask_out=None, stream=None):
     return _check(c, lib.ubatch_attention(c, s, ub, layer, _ptr(q), _ptr(o), _ptr(mask_out),
                                           _stream(stream)))
+
+
+def ubatch_attention_static_scratch(c, s, ub, layer, q, o, mask_out=None, stream=None):
+    """ubatch_attention for an all-decode ubatch, obtaining no memory during the
+    call: its split-K scratch is a fixed array in the library's device image,
+    shared by every call on the device (order such calls on one stream)."""
+    return _check(c, lib.ubatch_attention_static_scratch(c, s, ub, layer, _ptr(q), _ptr(o),
+                                                         _ptr(mask_out), _stream(stream)))
 
 
 def kv_device_error(c):

@@ -11,6 +11,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include <cudaTypedefs.h>
 
@@ -391,3 +392,112 @@ size_t kv_device_bytes(const kv_cache *c) { return (c && c->dev) ? c->dev->bytes
 uint64_t kv_launch_count(const kv_cache *c) { return c ? c->launches : 0; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Attention without allocation: the decode path with its split-K scratch in a
+// fixed array of the library's device image instead of memory obtained at
+// kv_init.  The array is shared by every call on a device; each call clears
+// the completion counters (which must start at zero) on its own stream.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+constexpr size_t STATIC_SCRATCH_BYTES = KV_STATIC_SCRATCH_BYTES;
+constexpr int MAX_DEVICES = 64;
+
+static __device__ __align__(256) unsigned char g_static_scratch[STATIC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mu;
+void *g_scratch_addr[MAX_DEVICES] = {};
+
+// The array's device address on `dev`, looked up once per device; `dev` must
+// be the current device.
+cudaError_t static_scratch(int dev, unsigned char **out) {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = p;
+    }
+    *out = static_cast<unsigned char *>(g_scratch_addr[dev]);
+    return cudaSuccess;
+}
+
+// True when sync_device would have to grow its delta or staging buffer.
+bool sync_would_allocate(const kv_cache *c, const kv_split *sp) {
+    const DeviceState *d = c->dev;
+    const size_t nd = c->pending.size();
+    const size_t tbytes = c->dev_tables_split != sp->id ? sp->image.size() : 0;
+    return nd > (size_t)d->delta_cap || nd * sizeof(Delta) + tbytes > d->stage_cap || tbytes > d->tables_cap;
+}
+
+}  // namespace
+
+extern "C" int ubatch_attention_static_scratch(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
+                                               const void *q, float *o, void *mask_out, void *stream) {
+    int rc = check_call(c, sp, ub, layer);
+    if (rc != KV_OK) return rc;
+    if (!q || !o || ((uintptr_t)q & 15) || ((uintptr_t)o & 15))
+        return c->set_err(KV_E_INVAL, "q / o must be 16-byte aligned device pointers");
+    for (int32_t k = 0; k <= ub; ++k)
+        if (!sp->stored[layer][k]) return c->set_err(KV_E_ORDER, "attention before its K/V were stored");
+    DeviceState *d = c->dev;
+    const UbatchHost &u = sp->ub[ub];
+    if (u.n_pf_blocks > 0)
+        return c->set_err(KV_E_INVAL, "static-scratch attention runs the decode path only; this ubatch has "
+                                      "prefill blocks (use ubatch_attention)");
+    const int32_t hkv = c->prm.n_head_kv;
+    const size_t cnt_bytes = ((size_t)u.n_dec_blocks * hkv * sizeof(int32_t) + 255) & ~(size_t)255;
+    const size_t part_bytes = ((size_t)d->gx_dec + u.n_dec_blocks) * hkv * DEC_PART_FLOATS * sizeof(float);
+    if (cnt_bytes + part_bytes > STATIC_SCRATCH_BYTES) {
+        char buf[200];
+        std::snprintf(buf, sizeof buf, "static-scratch attention needs %zu bytes of scratch for %d decode blocks, "
+                      "more than the %zu available", cnt_bytes + part_bytes, u.n_dec_blocks, STATIC_SCRATCH_BYTES);
+        return c->set_err(KV_E_INVAL, buf);
+    }
+    int cur = -1;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaGetDevice");
+    if (cur != d->device || cur < 0 || cur >= MAX_DEVICES)
+        return c->set_err(KV_E_INVAL, "static-scratch attention: make the cache's device current");
+    if (sync_would_allocate(c, sp))
+        return c->set_err(KV_E_INVAL, "static-scratch attention: device tables need a larger upload buffer "
+                                      "(call kv_store for this split first)");
+    unsigned char *scratch = nullptr;
+    if ((e = static_scratch(cur, &scratch)) != cudaSuccess) return cuda_fail(c, e, "scratch address");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((rc = sync_device(c, sp, st)) != KV_OK) return rc;
+    kvk::UbView v = make_view(c, sp, ub);
+    if (d->plan_split != sp->id || d->plan_ub != ub) {
+        if ((e = kvk::launch_plan(v, d->plan, c->prm.n_stream, d->gx_dec, d->gx_pf, st)) != cudaSuccess)
+            return cuda_fail(c, e, "plan launch");
+        c->launches += 3;
+        d->plan_split = sp->id;
+        d->plan_ub = ub;
+    }
+    if (mask_out) {
+        if ((e = kvk::launch_mask(v, static_cast<uint16_t *>(mask_out), st)) != cudaSuccess)
+            return cuda_fail(c, e, "mask launch");
+        c->launches += 1;
+    }
+    if (u.n_dec_blocks == 0) return KV_OK;
+    int32_t *counters = reinterpret_cast<int32_t *>(scratch);
+    if ((e = cudaMemsetAsync(counters, 0, cnt_bytes, st)) != cudaSuccess) return cuda_fail(c, e, "counter clear");
+    kvk::DecodeArgs a{};
+    a.u = v;
+    a.p = d->plan;
+    a.p.counters = counters;
+    a.q = static_cast<const __half *>(q);
+    a.o = o;
+    a.part = reinterpret_cast<float *>(scratch + cnt_bytes);
+    a.n_head = c->prm.n_head;
+    a.n_head_kv = hkv;
+    a.gqa = c->gqa;
+    a.scale_log2 = 1.4426950408889634f / sqrtf((float)c->prm.head_dim);
+    a.err = d->d_err;
+    if ((e = kvk::launch_decode(&d->tm_k[layer], &d->tm_v[layer], a, d->gx_dec, st)) != cudaSuccess)
+        return cuda_fail(c, e, "decode launch");
+    c->launches += 1;
+    return KV_OK;
+}

@@ -280,6 +280,40 @@ int ubatch_attention(kv_cache *c, const kv_split *s, int32_t ub, int32_t layer,
                      const void *q, float *o, void *mask_out, void *stream);
 
 /*
+ * ubatch_attention_static_scratch -- the same result as ubatch_attention for
+ * a ubatch whose query blocks all take the decode path (the rows that share
+ * a first sequence id number fewer than 64 * n_head_kv / n_head, as in a
+ * decode iteration), computed without obtaining any device or host memory
+ * during the call.  The pages have no counterpart of this call: it exists
+ * for callers that cannot allocate while a step runs -- a server that has
+ * handed all free device memory to its own pool at start-up, or a decode
+ * loop that must not stall on the device-wide synchronisation cudaMalloc /
+ * cudaFree may imply, or fail half-way on an out-of-memory.
+ *
+ * The split-K partial results and the per-block completion counters live in
+ * one fixed array of KV_STATIC_SCRATCH_BYTES in the library's device image.
+ * Needed: 256-byte-rounded (decode blocks x n_head_kv x 4) bytes of counters
+ * plus (decode CTA columns + decode blocks) x n_head_kv x 8448 bytes of
+ * partials, where decode CTA columns = 2 x SMs / n_head_kv; with 8 KV heads
+ * on 152 SMs that is about 300 single-row sequences.
+ *   Arguments, layout and ownership: as ubatch_attention.
+ *   Errors: as ubatch_attention, and KV_E_INVAL (no work done) when a block
+ *   of the ubatch takes the tensor-core prefill path, when the scratch would
+ *   exceed KV_STATIC_SCRATCH_BYTES, when the current device is not the
+ *   cache's, or when bringing the device tables up to date would need a
+ *   larger upload buffer (call kv_store for this split first).
+ * Every call on a device, for any cache, shares the one array: calls whose
+ * device work overlaps in time (other streams, other threads) race on it and
+ * give wrong results; order them on one stream.  Each call clears the
+ * counters on its stream before its kernel.  The first call on each device,
+ * made with that device current, looks up the array's device address once;
+ * make that first call before any stream capture begins.
+ */
+#define KV_STATIC_SCRATCH_BYTES (24u << 20)
+int ubatch_attention_static_scratch(kv_cache *c, const kv_split *s, int32_t ub, int32_t layer,
+                                    const void *q, float *o, void *mask_out, void *stream);
+
+/*
  * kv_device_error -- synchronise the cache's device work and return the
  * device error word: 0 if no kernel reported a fault, else a nonzero code
  * (a bounded wait gave up or an index check failed); clears it.
