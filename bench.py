@@ -45,12 +45,14 @@ UNIT = "tokens/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run fewer layers than the workload has (small cases for profiling only)")
     return ap.parse_args()
 
 
@@ -127,6 +129,26 @@ class Clocks:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
                 "reasons": sorted(reasons)}
+
+
+class EventPool:
+    """Start/end CUDA events created before the timed region (creating them
+    inside it would put host work between the launches)."""
+
+    def __init__(self, n):
+        import torch
+        self.ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n)]
+        self.meta = []
+
+    def take(self, pairs, nbytes):
+        i = len(self.meta)
+        self.meta.append((pairs, nbytes))
+        return self.ev[i]
+
+    def results(self):
+        """(ms, pairs, bytes) per recorded launch."""
+        return [(self.ev[i][0].elapsed_time(self.ev[i][1]), p, b) for i, (p, b) in enumerate(self.meta)]
 
 
 def max_over_ranks(ms, device):
@@ -209,8 +231,12 @@ class OursArm:
                      "bytes": self._kv_bytes(call, rows, n)}
                 ubs.append(t)
             kv.kv_split_free(s)
-            # the batch is marshalled once; each step re-splits it in the library
-            self.calls.append((call, ubs))
+            # the batch is marshalled once (numpy arrays, ids as a flat list plus
+            # counts); each step re-splits it in the library
+            marsh = (np.asarray(call["pos"], dtype=np.int32),
+                     (np.fromiter((q for ids in call["seq"] for q in ids), dtype=np.int32),
+                      np.asarray([len(ids) for ids in call["seq"]], dtype=np.int32)))
+            self.calls.append((call, ubs, marsh))
         self.torch.cuda.synchronize()
 
     def _kv_bytes(self, call, rows, n):
@@ -225,7 +251,7 @@ class OursArm:
 
     def input_bytes(self):
         tot = 0
-        for _, ubs in self.calls:
+        for _, ubs, _ in self.calls:
             for t in ubs:
                 tot += sum(x.numel() * 2 for x in t["q"] + t["k"] + t["v"])
         return tot
@@ -239,15 +265,18 @@ class OursArm:
             for q, pmax in self.base_pos_max.items():
                 kv.kv_seq_rm(self.c, q, pmax + 1, -1)
 
+    def timed_calls_per_step(self):
+        return sum(len(ubs) for _, ubs, _ in self.calls) * max(0, self.L - 1)
+
     def step(self, timers=None, host=None):
-        """One pass of the whole path.  timers: list to append (start, end)
-        events around attention calls that launch no planning kernels.
+        """One pass of the whole path.  timers: an EventPool that brackets the
+        attention calls that launch no planning kernels (layers >= 1).
         host: pinned host copies of the inputs (end-to-end mode)."""
         kv, torch = self.kv, self.torch
         self.reset()
         last = []
-        for ci, (call, ubs) in enumerate(self.calls):
-            s = kv.kv_split_ubatches(self.c, call["pos"], call["seq"])
+        for ci, (call, ubs, marsh) in enumerate(self.calls):
+            s = kv.kv_split_ubatches(self.c, marsh[0], marsh[1])
             assert kv.kv_prepare_cells(self.c, s) == 0
             for k, t in enumerate(ubs):
                 for layer in range(self.L):
@@ -258,12 +287,10 @@ class OursArm:
                         t["v"][layer].copy_(hv, non_blocking=True)
                     kv.kv_store(self.c, s, k, layer, t["k"][layer], t["v"][layer], self.stream)
                     if timers is not None and layer > 0:
-                        e0 = torch.cuda.Event(enable_timing=True)
-                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0, e1 = timers.take(t["pairs"], t["bytes"])
                         e0.record(self.stream)
                         kv.ubatch_attention(self.c, s, k, layer, t["q"][layer], t["o"], None, self.stream)
                         e1.record(self.stream)
-                        timers.append((e0, e1, t["pairs"], t["bytes"]))
                     else:
                         kv.ubatch_attention(self.c, s, k, layer, t["q"][layer], t["o"], None, self.stream)
                 if host is not None:
@@ -276,7 +303,7 @@ def run_ours(args, rank, world, device):
     import torch
     import continuous_batching_kv_gb300 as kv
     torch.cuda.set_device(device)
-    cfg = configs.config(args.config)
+    cfg = configs.config(args.config, n_layer=args.layers)
     arm = OursArm(cfg, device)
     hbm, tflops, peak_src = load_peaks()
     dist = world > 1
@@ -290,7 +317,7 @@ def run_ours(args, rank, world, device):
         arm.step()
     barrier()
     clocks = Clocks(device if isinstance(device, int) else torch.cuda.current_device())
-    timers = []
+    timers = EventPool(arm.timed_calls_per_step() * args.steps)
     launches0 = kv.kv_launch_count(arm.c)
     clocks.start()
     barrier()
@@ -310,18 +337,19 @@ def run_ours(args, rank, world, device):
     value = tokens / (ms_max / 1e3)
 
     # roofline of the dominant kernel (attention), timed live above
-    durs = [a.elapsed_time(b) for a, b, _, _ in timers]
+    res = timers.results()
+    durs = [ms for ms, _, _ in res]
     secs = sum(durs) / 1e3
     if DECODE_BOUND.get(cfg["id"], False):
         # decode: one query row per sequence, so the launch streams K/V from HBM
-        moved = sum(b for _, _, _, b in timers)
+        moved = sum(b for _, _, b in res)
         achieved = moved / secs / 1e9 if durs else 0.0
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": None, "kernel": "ubatch_attention (k_decode)",
                 "algorithmic_bytes_per_launch": int(moved / max(1, len(durs)))}
     else:
         per_pair_flops = 4 * arm.d * arm.H
-        achieved = (sum(p for _, _, p, _ in timers) * per_pair_flops) / secs / 1e12 if durs else 0.0
+        achieved = (sum(p for _, p, _ in res) * per_pair_flops) / secs / 1e12 if durs else 0.0
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tflops, "unit": "TFLOP/s",
                 "frac": round(achieved / tflops, 4), "traffic": None,
                 "kernel": "ubatch_attention (k_prefill + k_merge_pf)"}
@@ -331,7 +359,7 @@ def run_ours(args, rank, world, device):
     e2e = None
     if not args.no_e2e:
         host = []
-        for ci, (call, ubs) in enumerate(arm.calls):
+        for ci, (call, ubs, _) in enumerate(arm.calls):
             hc = []
             for t in ubs:
                 hc.append([(t["q"][l].cpu().pin_memory(), t["k"][l].cpu().pin_memory(),
@@ -461,7 +489,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    cfg = configs.config(args.config)
+    cfg = configs.config(args.config, n_layer=args.layers)
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, cfg)), flush=True)

@@ -17,6 +17,7 @@ The functions keep the C names:
 """
 
 import ctypes as C
+import itertools
 import os
 
 import numpy as np
@@ -209,13 +210,34 @@ def kv_last_error(c):
 
 # ---- host side -------------------------------------------------------------------
 
+def _seq_arrays(seq_id):
+    """The per-slot id lists as (flat int32 ids, per-slot counts, per-slot
+    offsets).  seq_id: a list of id lists, a 2-D integer array (every slot has
+    the same number of ids), or a (flat ids, counts) pair."""
+    if isinstance(seq_id, tuple):
+        flat = np.ascontiguousarray(seq_id[0], dtype=np.int32)
+        counts = np.ascontiguousarray(seq_id[1], dtype=np.int32)
+    elif isinstance(seq_id, np.ndarray) and seq_id.ndim == 2:
+        flat = np.ascontiguousarray(seq_id, dtype=np.int32).reshape(-1)
+        counts = np.full(seq_id.shape[0], seq_id.shape[1], dtype=np.int32)
+    else:
+        counts = np.fromiter((len(ids) for ids in seq_id), dtype=np.int32, count=len(seq_id))
+        flat = np.fromiter(itertools.chain.from_iterable(seq_id), dtype=np.int32, count=int(counts.sum()))
+    offs = np.zeros(counts.shape[0], dtype=np.int64)
+    if counts.shape[0] > 1:
+        np.cumsum(counts[:-1], out=offs[1:])
+    if flat.size == 0:
+        flat = np.zeros(1, dtype=np.int32)
+    return flat, counts, offs
+
+
 def kv_split_ubatches(c, pos, seq_id=None, n_seq_id=None, mode=KV_SPLIT_AUTO, n_tokens=None):
     """Split a batch.  pos: list / array of positions or None (auto-fill);
-    seq_id: list of id lists (first id first) or None (all sequence 0);
-    n_seq_id: counts, default the lists' lengths (pass False for the C NULL:
-    one id per slot)."""
+    seq_id: list of id lists (first id first), a 2-D id array, a (flat ids,
+    counts) pair, or None (all sequence 0); n_seq_id: counts, default the
+    lists' lengths (pass False for the C NULL: one id per slot)."""
     if n_tokens is None:
-        n_tokens = len(pos) if pos is not None else len(seq_id)
+        n_tokens = len(pos) if pos is not None else (len(seq_id[1]) if isinstance(seq_id, tuple) else len(seq_id))
     b = kv_batch()
     b.n_tokens = n_tokens
     keep = []
@@ -224,15 +246,12 @@ def kv_split_ubatches(c, pos, seq_id=None, n_seq_id=None, mode=KV_SPLIT_AUTO, n_
         keep.append(pa)
         b.pos = pa.ctypes.data_as(C.POINTER(C.c_int32))
     if seq_id is not None:
-        rows = []
-        for ids in seq_id:
-            a = (C.c_int32 * max(1, len(ids)))(*ids)
-            rows.append(a)
-        ptrs = (C.POINTER(C.c_int32) * len(rows))(*[C.cast(a, C.POINTER(C.c_int32)) for a in rows])
-        keep += [rows, ptrs]
-        b.seq_id = C.cast(ptrs, C.POINTER(C.POINTER(C.c_int32)))
+        flat, counts, offs = _seq_arrays(seq_id)
+        ptrs = (offs * 4 + flat.ctypes.data).astype(np.uint64)   # one pointer per slot into flat
+        keep += [flat, ptrs]
+        b.seq_id = C.cast(C.c_void_p(ptrs.ctypes.data), C.POINTER(C.POINTER(C.c_int32)))
         if n_seq_id is None:
-            n_seq_id = [len(ids) for ids in seq_id]
+            n_seq_id = counts
     if n_seq_id is not None and n_seq_id is not False:
         na = np.ascontiguousarray(np.asarray(n_seq_id, dtype=np.int32))
         keep.append(na)

@@ -27,6 +27,15 @@ __device__ __forceinline__ void report(int32_t *err, int32_t code) {
     if (err) atomicCAS(err, 0, code);
 }
 
+// Programmatic dependent launch.  pdl_wait: the calling thread waits until the
+// grids this one depends on have completed and their writes are visible (it
+// returns at once in a grid launched without the programmatic attribute).
+// pdl_trigger: this CTA lets the next grid of the stream, if that grid was
+// launched with the attribute, start now; the next grid still waits for this
+// one in its own pdl_wait before it reads what this one writes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Everything a kernel needs to decide whether row i sees cell j.
 // "llama.cpp and the ubatch", "The mask is doing the work": the cell must be
 // occupied, hold the row's first sequence id, and (causal) not be later than

@@ -32,10 +32,13 @@ struct DeviceState {
     int32_t delta_cap = 0;
     uint8_t *d_tables = nullptr;
     size_t tables_cap = 0;
-    uint8_t *h_stage = nullptr;
-    size_t stage_cap = 0;
-    cudaEvent_t stage_ev = nullptr;
-    bool stage_pending = false;
+    // two pinned staging buffers used in turn, so preparing a split never waits
+    // for the upload of the one before it
+    uint8_t *h_stage[2] = {nullptr, nullptr};
+    size_t stage_cap[2] = {0, 0};
+    cudaEvent_t stage_ev[2] = {nullptr, nullptr};
+    bool stage_pending[2] = {false, false};
+    int stage_slot = 0;
     // attention plan and split-K scratch
     kvk::Plan plan{};
     int32_t max_blocks = 0;
@@ -140,10 +143,11 @@ int sync_device(kv_cache *c, const kv_split *sp, cudaStream_t st) {
     const bool need_tables = c->dev_tables_split != sp->id;
     if (!c->pending_reset && c->pending.empty() && !need_tables) return KV_OK;
     cudaError_t e;
-    if (d->stage_pending) {   // the staging buffer is reused: wait for its last copy
-        e = cudaEventSynchronize(d->stage_ev);
+    const int sl = d->stage_slot;
+    if (d->stage_pending[sl]) {   // this staging buffer is reused: wait for its last copy
+        e = cudaEventSynchronize(d->stage_ev[sl]);
         if (e != cudaSuccess) return cuda_fail(c, e, "stage event");
-        d->stage_pending = false;
+        d->stage_pending[sl] = false;
     }
     if (c->pending_reset) {
         const size_t n = (size_t)c->prm.n_ctx;
@@ -163,18 +167,19 @@ int sync_device(kv_cache *c, const kv_split *sp, cudaStream_t st) {
         d->d_delta = nd_buf;
         d->delta_cap = (int32_t)nd;
     }
-    if (dbytes + tbytes > d->stage_cap) {
-        if (d->h_stage) cudaFreeHost(d->h_stage);
-        d->h_stage = nullptr;
+    if (dbytes + tbytes > d->stage_cap[sl]) {
+        if (d->h_stage[sl]) cudaFreeHost(d->h_stage[sl]);
+        d->h_stage[sl] = nullptr;
         size_t cap = dbytes + tbytes;
-        if ((e = cudaHostAlloc((void **)&d->h_stage, cap, cudaHostAllocDefault)) != cudaSuccess)
+        if ((e = cudaHostAlloc((void **)&d->h_stage[sl], cap, cudaHostAllocDefault)) != cudaSuccess)
             return cuda_fail(c, e, "stage grow");
-        d->stage_cap = cap;
+        d->stage_cap[sl] = cap;
     }
-    if (nd) std::memcpy(d->h_stage, c->pending.data(), dbytes);
-    if (tbytes) std::memcpy(d->h_stage + dbytes, sp->image.data(), tbytes);
+    uint8_t *stage = d->h_stage[sl];
+    if (nd) std::memcpy(stage, c->pending.data(), dbytes);
+    if (tbytes) std::memcpy(stage + dbytes, sp->image.data(), tbytes);
     if (nd) {
-        if ((e = cudaMemcpyAsync(d->d_delta, d->h_stage, dbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+        if ((e = cudaMemcpyAsync(d->d_delta, stage, dbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
             return cuda_fail(c, e, "delta upload");
         if ((e = kvk::launch_apply_deltas(d->d_delta, (int32_t)nd, c->n_words, d->d_pos, d->d_epoch,
                                           d->d_bits, st)) != cudaSuccess)
@@ -182,15 +187,16 @@ int sync_device(kv_cache *c, const kv_split *sp, cudaStream_t st) {
         c->launches += 1;
     }
     if (tbytes) {
-        if ((e = cudaMemcpyAsync(d->d_tables, d->h_stage + dbytes, tbytes, cudaMemcpyHostToDevice, st)) !=
+        if ((e = cudaMemcpyAsync(d->d_tables, stage + dbytes, tbytes, cudaMemcpyHostToDevice, st)) !=
             cudaSuccess)
             return cuda_fail(c, e, "table upload");
         c->dev_tables_split = sp->id;
         d->plan_split = 0;
         d->plan_ub = -1;
     }
-    if ((e = cudaEventRecord(d->stage_ev, st)) != cudaSuccess) return cuda_fail(c, e, "stage record");
-    d->stage_pending = true;
+    if ((e = cudaEventRecord(d->stage_ev[sl], st)) != cudaSuccess) return cuda_fail(c, e, "stage record");
+    d->stage_pending[sl] = true;
+    d->stage_slot = sl ^ 1;
     for (const Delta &r : c->pending) c->pending_idx[r.cell] = -1;
     c->pending.clear();
     return KV_OK;
@@ -232,11 +238,13 @@ int device_init(kv_cache *c) {
     if ((e = dev_alloc(d, &d->d_delta, d->delta_cap)) != cudaSuccess) return cuda_fail(c, e, "delta alloc");
     d->tables_cap = tables_bound(c);
     if ((e = dev_alloc(d, &d->d_tables, d->tables_cap)) != cudaSuccess) return cuda_fail(c, e, "table alloc");
-    d->stage_cap = d->tables_cap + (size_t)d->delta_cap * sizeof(Delta);
-    if ((e = cudaHostAlloc((void **)&d->h_stage, d->stage_cap, cudaHostAllocDefault)) != cudaSuccess)
-        return cuda_fail(c, e, "stage alloc");
-    if ((e = cudaEventCreateWithFlags(&d->stage_ev, cudaEventDisableTiming)) != cudaSuccess)
-        return cuda_fail(c, e, "event");
+    for (int sl = 0; sl < 2; ++sl) {
+        d->stage_cap[sl] = d->tables_cap + (size_t)d->delta_cap * sizeof(Delta);
+        if ((e = cudaHostAlloc((void **)&d->h_stage[sl], d->stage_cap[sl], cudaHostAllocDefault)) != cudaSuccess)
+            return cuda_fail(c, e, "stage alloc");
+        if ((e = cudaEventCreateWithFlags(&d->stage_ev[sl], cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(c, e, "event");
+    }
 
     // plan and split-K scratch
     const int32_t hkv = c->prm.n_head_kv;
@@ -281,10 +289,13 @@ int device_init(kv_cache *c) {
 void device_free(kv_cache *c) {
     DeviceState *d = c->dev;
     if (!d) return;
-    if (d->stage_pending && d->stage_ev) cudaEventSynchronize(d->stage_ev);
+    for (int sl = 0; sl < 2; ++sl)
+        if (d->stage_pending[sl] && d->stage_ev[sl]) cudaEventSynchronize(d->stage_ev[sl]);
     for (void *p : d->allocs) cudaFree(p);
-    if (d->h_stage) cudaFreeHost(d->h_stage);
-    if (d->stage_ev) cudaEventDestroy(d->stage_ev);
+    for (int sl = 0; sl < 2; ++sl) {
+        if (d->h_stage[sl]) cudaFreeHost(d->h_stage[sl]);
+        if (d->stage_ev[sl]) cudaEventDestroy(d->stage_ev[sl]);
+    }
     delete d;
     c->dev = nullptr;
 }
@@ -321,12 +332,17 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
     for (int32_t k = 0; k <= ub; ++k)
         if (!sp->stored[layer][k]) return c->set_err(KV_E_ORDER, "attention before its K/V were stored");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // Nothing of this call precedes the attention kernels when the device is in
+    // sync, the plan is cached and no mask is asked for: then the plan, tables
+    // and mirror were complete before the previous kernel began.
+    bool early_ok = !c->pending_reset && c->pending.empty() && c->dev_tables_split == sp->id && !mask_out;
     if ((rc = sync_device(c, sp, st)) != KV_OK) return rc;
     DeviceState *d = c->dev;
     const UbatchHost &u = sp->ub[ub];
     kvk::UbView v = make_view(c, sp, ub);
     cudaError_t e;
     if (d->plan_split != sp->id || d->plan_ub != ub) {
+        early_ok = false;
         kvk::Plan p = d->plan;
         if ((e = kvk::launch_plan(v, p, c->prm.n_stream, d->gx_dec, d->gx_pf, st)) != cudaSuccess)
             return cuda_fail(c, e, "plan launch");
@@ -369,6 +385,7 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
         a.gqa = c->gqa;
         a.scale_log2 = scale_log2;
         a.err = d->d_err;
+        a.early_ok = early_ok ? 1 : 0;
         if ((e = kvk::launch_prefill(&d->tm_k[layer], &d->tm_v[layer], a, d->gx_pf, st)) != cudaSuccess)
             return cuda_fail(c, e, "prefill launch");
         c->launches += 2;   // attention + split-K merge
@@ -429,7 +446,8 @@ bool sync_would_allocate(const kv_cache *c, const kv_split *sp) {
     const DeviceState *d = c->dev;
     const size_t nd = c->pending.size();
     const size_t tbytes = c->dev_tables_split != sp->id ? sp->image.size() : 0;
-    return nd > (size_t)d->delta_cap || nd * sizeof(Delta) + tbytes > d->stage_cap || tbytes > d->tables_cap;
+    return nd > (size_t)d->delta_cap || nd * sizeof(Delta) + tbytes > d->stage_cap[d->stage_slot] ||
+           tbytes > d->tables_cap;
 }
 
 }  // namespace

@@ -31,8 +31,8 @@
 //  * cells nobody in the block may see get their V rows zeroed in shared
 //    memory before the PV product (P is 0 there, but 0 * NaN would not be);
 //  * a block split over several CTAs leaves one partial (m, l, O) per piece,
-//    merged by a small second kernel, so no CTA stalls its own pipeline to
-//    merge; every mbarrier wait is bounded.
+//    merged by a small second kernel launched as a programmatic dependent (it
+//    reads the plan while this kernel runs); every mbarrier wait is bounded.
 
 #include "dev_common.cuh"
 #include "kernels.h"
@@ -54,20 +54,19 @@ constexpr int OFF_K = OFF_Q + TILEB;
 constexpr int OFF_V = OFF_K + STAGES * TILEB;
 constexpr int OFF_AUX = OFF_V + STAGES * TILEB;
 constexpr int PART_STRIDE = 132;
-constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128), S1 [128,256), O [256,384), P0, P1 [384,512)
-constexpr uint32_t COL_O = 256;
-constexpr uint32_t COL_P = 384;          // P of pair g: fp16, 64 columns at COL_P + 64 (g & 1)
+constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128), S1 [128,256) (P written over S), O_0 [256,384), O_1 [384,512)
+constexpr uint32_t COL_O = 256;          // O_h: accumulator of the cells 64h .. 64h + 63 of each pair tile
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr unsigned POLL_NS = 32;         // back-off of the polling producer / MMA loops
 
 constexpr uint32_t IDESC_S = tc::idesc_f16(128, 128, 0, 0);
 constexpr uint32_t IDESC_PV = tc::idesc_f16(128, 128, 0, 1);
 
-// Metadata ring.  Pair g's slot is rewritten by the K load of pair g + 8, which
-// needs S of g + 6, which needs the softmax to have read S of g + 4: by then the
-// softmax is done with pair g, and PV of g (hence the V load of g, which reads
-// the slot) was issued before the softmax of g + 2 wrote its P.
-constexpr int MSLOTS = 8;
+// Metadata ring.  Pair g's slot is rewritten by the K load of pair g + 4, which
+// needs S of g + 2, which waits for the PV of the pair before it in its score
+// buffer (g or g + 1) to complete: by then the softmax is done with pair g and
+// the V load of g (which reads the slot) was issued.
+constexpr int MSLOTS = 4;
 
 struct Meta {                 // per pair tile: what the producer learned about it
     int32_t full;
@@ -87,16 +86,15 @@ struct __align__(16) Aux {
     uint64_t k_full[STAGES], v_full[STAGES], k_empty[STAGES], v_empty[STAGES];
     uint64_t meta_full[MSLOTS];
     uint64_t s_full[2], p_full[2], pv_done[2], q_full, spare;   // p_full, pv_done [g & 1]: pair g
-    uint64_t s_free[2];       // a score buffer was read into registers by all 256 softmax threads
-    uint64_t rbar, lbar;      // softmax-group exchanges (row maxima, row sums), all 256 threads
+    uint64_t lbar;            // the halves' (m, l) exchange at each item's end, all 256 threads
     uint32_t tmem_base;
     int32_t fail;
     int32_t flag;
     int32_t pad;
     Meta meta[MSLOTS];
     ItemSlot islot[2];
-    float red[2][2][M];       // [pair parity][column half][row]: partial row maxima
-    float lex[2][2][M];       // [item parity][column half][row]: partial row sums
+    float mex[2][2][M];       // [item parity][cell half][row]: running maxima
+    float lex[2][2][M];       // [item parity][cell half][row]: row sums
 };
 
 constexpr size_t SMEM_BYTES = OFF_AUX + sizeof(Aux);
@@ -174,6 +172,11 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     const int32_t i1 = c0[blockIdx.x + 1];
     const uint32_t sbase = kvd::smem_u32(smem);
 
+    // Launched as a programmatic dependent: library state is read before waiting
+    // for the previous kernel only when it was complete before that kernel began;
+    // Q, the K/V cache and the outputs are touched only after the wait.
+    if (!a.early_ok) kvd::pdl_wait();
+    if (tid == 0) kvd::pdl_trigger();   // the split-K merge may be scheduled
     if ((sbase & 1023u) != 0) {
         if (tid == 0) kvd::report(a.err, kvd::DERR_BOUNDS);
         return;
@@ -190,15 +193,12 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         for (int s = 0; s < MSLOTS; ++s) kvd::mbar_init(&x.meta_full[s], 32);
         kvd::mbar_init(&x.s_full[0], 1);
         kvd::mbar_init(&x.s_full[1], 1);
-        kvd::mbar_init(&x.s_free[0], NSM);
-        kvd::mbar_init(&x.s_free[1], NSM);
         kvd::mbar_init(&x.p_full[0], NSM);
         kvd::mbar_init(&x.p_full[1], NSM);
         kvd::mbar_init(&x.pv_done[0], 1);
         kvd::mbar_init(&x.pv_done[1], 1);
         kvd::mbar_init(&x.q_full, NSM);
         kvd::mbar_init(&x.spare, 1);
-        kvd::mbar_init(&x.rbar, NSM);
         kvd::mbar_init(&x.lbar, NSM);
         x.fail = 0;
         kvd::fence_mbar_init();
@@ -311,14 +311,6 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         for (int h = 0; h < 2; ++h)   // a missing second tile: out of bounds, TMA writes zeros
                             mt.ys[h] = tt[h] >= 0 ? kb.stream * a.u.kv_size + tt[h] * TILE : -TILE;
                         mt.full = full ? 1 : 0;
-                        uint8_t *ks = smem + OFF_K + st * TILEB;
-                        const int32_t xk = hk * 128;
-                        kvd::fence_proxy_async_smem();
-                        kvd::mbar_arrive_expect_tx(&x.k_full[st], TILEB);
-                        for (int h = 0; h < 2; ++h) {
-                            kvd::tma_load_2d(ks + h * BOX, &tm_k, xk, mt.ys[h], &x.k_full[st]);
-                            kvd::tma_load_2d(ks + HALF + h * BOX, &tm_k, xk + 64, mt.ys[h], &x.k_full[st]);
-                        }
                     }
                     if (!full) {
 #pragma unroll
@@ -330,7 +322,21 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         }
                     }
                     __syncwarp();
+                    // the metadata (and lane table) go out before the K copy is issued:
+                    // the softmax may fetch its Q rows while the copy is in flight
                     kvd::mbar_arrive(&x.meta_full[kc % MSLOTS]);
+                    if (kc == 0) kvd::pdl_wait();   // the K/V cache rows of this ubatch are written
+                    if (lane == 0) {
+                        uint8_t *ks = smem + OFF_K + st * TILEB;
+                        const int32_t xk = hk * 128;
+                        const int32_t y0 = mt.ys[0], y1 = mt.ys[1];
+                        kvd::fence_proxy_async_smem();
+                        kvd::mbar_arrive_expect_tx(&x.k_full[st], TILEB);
+                        kvd::tma_load_2d(ks, &tm_k, xk, y0, &x.k_full[st]);
+                        kvd::tma_load_2d(ks + HALF, &tm_k, xk + 64, y0, &x.k_full[st]);
+                        kvd::tma_load_2d(ks + BOX, &tm_k, xk, y1, &x.k_full[st]);
+                        kvd::tma_load_2d(ks + HALF + BOX, &tm_k, xk + 64, y1, &x.k_full[st]);
+                    }
                     ++kc;
                     ++kj;
                     have_k = false;
@@ -378,10 +384,9 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     } else if (warp == 9) {
         // ===================== MMA issuer =====================
         if ((tid & 31) == 0) {
-            int32_t gidx = 0;          // global pair-tile counter (stage ring)
-            uint32_t s_uses[2] = {0, 0};   // S products written into each score buffer so far
+            int32_t gidx = 0;                  // global pair-tile counter (stage ring)
+            int32_t last_pair[2] = {-1, -1};   // global pair whose S (then P) last filled each score buffer
             uint32_t n_q = 0;
-            uint32_t n_s[2] = {0, 0};
             const uint32_t q_addr = sbase + OFF_Q;
             auto issue_s = [&](int32_t gi, int32_t buf) {
                 const uint32_t k_addr = sbase + OFF_K + (gi % STAGES) * TILEB;
@@ -395,10 +400,10 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 tc::commit(&x.s_full[buf]);
                 tc::commit(&x.k_empty[gi % STAGES]);   // this K tile is consumed
             };
-            // Per item, a non-blocking scheduler: PV of the oldest ready P first (the
-            // softmax waits on it), then S of the next pair once its K tile has
-            // landed and its score buffer is free (the P two pairs back was taken).
-            // Nothing blocks on one condition while the other is ready.
+            // Per item, a non-blocking scheduler: PV of the oldest ready P first, then S
+            // of the next pair once its K tile has landed and the PV that read the P
+            // held in its score buffer has completed.  Nothing blocks on one condition
+            // while the other is ready.
             for (int32_t wi = i0; wi < i1 && !*fail; ++wi) {
                 const ItemInfo it = item_info(a, wi);
                 if (it.pairs == 0) continue;
@@ -410,39 +415,42 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 long long t_last = clock64();
                 while (pv_done < it.pairs) {
                     bool progressed = false;
-                    // P of pair gi in buffer gi & 1 (a single barrier could be lapped: the
-                    // softmax may finish two pairs before this thread looks)
+                    // P of pair gp is signalled on p_full[gp & 1] (one barrier could be
+                    // lapped: the softmax may finish two pairs before this thread looks)
                     const int32_t gp = gidx + pv_done;
                     if (pv_done < s_done && kvd::mbar_test_wait(&x.p_full[gp & 1], (uint32_t)(gp >> 1) & 1u)) {
-                        const int32_t gi = gp;
-                        ok = wait_or_fail(&x.v_full[gi % STAGES], (uint32_t)(gi / STAGES) & 1u, fail);
+                        ok = wait_or_fail(&x.v_full[gp % STAGES], (uint32_t)(gp / STAGES) & 1u, fail);
                         if (!ok) break;
                         tc::fence_after();
-                        const uint32_t v_addr = sbase + OFF_V + (gi % STAGES) * TILEB;
-                        const uint32_t p_tmem = tmem + COL_P + 64u * (uint32_t)(gi & 1);
+                        const uint32_t v_addr = sbase + OFF_V + (gp % STAGES) * TILEB;
+                        const uint32_t p_tmem = tmem + 128u * (uint32_t)(pv_done & 1);
+                        // O_h += P_h V_h over cells 64h .. 64h + 63 (P_h: 32 TMEM columns at
+                        // 64h of the score buffer, 8 columns per K step of 16 cells)
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {   // K = 16 cells = 8 TMEM columns of P
-                            const uint32_t boff = (uint32_t)kk * 2048u;
-                            tc::mma_ts(tmem + COL_O, p_tmem + 8u * (uint32_t)kk,
-                                       tc::sdesc_sw128(v_addr + boff, HALF, 1024), IDESC_PV,
-                                       (pv_done > 0 || kk > 0) ? 1u : 0u);
+                        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                tc::mma_ts(tmem + COL_O + 128u * (uint32_t)hh, p_tmem + 64u * (uint32_t)hh + 8u * (uint32_t)kk,
+                                           tc::sdesc_sw128(v_addr + (uint32_t)(4 * hh + kk) * 2048u, HALF, 1024), IDESC_PV,
+                                           (pv_done > 0 || kk > 0) ? 1u : 0u);
+                            }
                         }
-                        tc::commit(&x.pv_done[gi & 1]);
-                        tc::commit(&x.v_empty[gi % STAGES]);
+                        tc::commit(&x.pv_done[gp & 1]);
+                        tc::commit(&x.v_empty[gp % STAGES]);
                         ++pv_done;
                         progressed = true;
                     }
                     if (s_done < it.pairs) {
-                        // S of the next pair: its K tile has landed and its score buffer's
-                        // previous contents were read by the softmax
                         const int32_t gi = gidx + s_done;
                         const int32_t buf = s_done & 1;
+                        const int32_t lp = last_pair[buf];
+                        // PVs complete in order and S of lp waited for the PV before it, so
+                        // pv_done[lp & 1] is at most one phase behind: the parity test is exact
                         if (kvd::mbar_test_wait(&x.k_full[gi % STAGES], (uint32_t)(gi / STAGES) & 1u) &&
-                            (s_uses[buf] == 0 || kvd::mbar_test_wait(&x.s_free[buf], (s_uses[buf] - 1) & 1u))) {
+                            (lp < 0 || kvd::mbar_test_wait(&x.pv_done[lp & 1], (uint32_t)(lp >> 1) & 1u))) {
                             tc::fence_after();
                             issue_s(gi, buf);
-                            ++n_s[buf];
-                            ++s_uses[buf];
+                            last_pair[buf] = gi;
                             ++s_done;
                             progressed = true;
                         }
@@ -466,20 +474,25 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         }
     } else {
         // ============ softmax / correction / epilogue (warps 0-7, two threads per row) ============
-        // Warps w and w + 4 share TMEM lane quarter w: thread (n, ch) owns row n's
-        // columns 64ch .. 64ch + 63 of S, P and O.  Row maxima and row sums are
-        // combined through shared memory.
+        // Warps w and w + 4 share TMEM lane quarter w.  Thread (n, ch) owns cells
+        // 64ch .. 64ch + 63 of every pair tile of row n, with its own running maximum,
+        // row sum and accumulator O_ch (all 128 d), so the two halves of a row never
+        // wait for each other inside an item; their (m, l, O) are combined once, at
+        // the item's end.
         const int32_t n = tid & 127;           // TMEM lane = query vector
-        const int32_t ch = tid >> 7;           // column half
-        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(64 * ch);
+        const int32_t ch = tid >> 7;           // cell half
+        const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t s_mine = tmem + lane_q + (uint32_t)(64 * ch);   // + 128 * score buffer
+        const uint32_t o_mine = tmem + lane_q + COL_O + 128u * (uint32_t)ch;
         uint32_t n_s[2] = {0, 0};
-        uint32_t n_r = 0, n_l = 0;
+        uint32_t n_l = 0;
         int32_t k = 0;                         // pair tiles consumed (stage ring position)
         int32_t nonempty = 0;
         bool ok = true;
-        // The two halves of a row meet through mbarriers (arrive, then a bounded
-        // wait), never bar.sync: if a wait elsewhere gives up, the others time out
-        // instead of waiting for threads that left.
+        bool dep_done = false;                 // waited for the previous kernel of the stream
+        // The two halves meet through an mbarrier (arrive, then a bounded wait), never
+        // bar.sync: if a wait elsewhere gives up, the others time out instead of waiting
+        // for threads that left.
         for (int32_t wi = i0; wi < i1 && ok && warp_ok(fail); ++wi) {
             const ItemInfo it = item_info(a, wi);
             int32_t row = -1, rpos = 0;
@@ -496,13 +509,13 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 row = is.row[n];
                 rpos = is.rpos[n];
             }
+            if (!dep_done) {   // before the first read of Q and the first write of an output
+                kvd::pdl_wait();
+                dep_done = true;
+            }
             const bool live = row >= 0;
             const int32_t h = hk * G + (n % G);
-            float *orow = a.o + ((int64_t)(live ? row : 0) * a.n_head + h) * 128 + 64 * ch;
-            float m_run = -INFINITY, l_run = 0.f;   // l_run: this thread's half of the row sum
-            float ov[64];
-#pragma unroll
-            for (int c = 0; c < 64; ++c) ov[c] = 0.f;
+            float m_run = -INFINITY, l_run = 0.f;   // this half's running maximum and row sum
             if (it.pairs > 0) {
             // ---- Q tile: row n, d-half ch, 128-byte swizzle ----
             {
@@ -527,12 +540,11 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 if (!ok) break;
                 ++n_s[j & 1];
                 tc::fence_after();
-                // ---- my 64 columns of S -> registers, read from TMEM once, right when
-                //      ready (TMEM reads stall behind running MMAs); masked -> -inf ----
+                // ---- my 64 columns of S -> registers (one TMEM read, warp collective);
+                //      masked -> -inf ----
+                const uint32_t s_addr = s_mine + (uint32_t)(j & 1) * 128u;
                 uint32_t sb[64];
-                tc::ld64(lane_base + (uint32_t)(j & 1) * 128u, sb);   // warp collective
-                tc::fence_before();
-                kvd::mbar_arrive(&x.s_free[j & 1]);                   // the next S may overwrite it
+                tc::ld64(s_addr, sb);
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                 if (!live) {
 #pragma unroll
@@ -547,13 +559,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 }
 #pragma unroll
                 for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sb[c]));
-                // ---- row maximum over both halves (double-buffered by pair parity) ----
-                x.red[j & 1][ch][n] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                kvd::mbar_arrive(&x.rbar);
-                ok = __all_sync(0xffffffffu, wait_or_fail(&x.rbar, n_r & 1u, fail));
-                ++n_r;
-                if (!ok) break;
-                const float tmax = fmaxf(x.red[j & 1][0][n], x.red[j & 1][1][n]) * a.scale_log2;
+                const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
                 const float m_new = fmaxf(m_run, tmax);
                 const bool grow = m_new > m_run + RESCALE_LOG2 || (m_run == -INFINITY && m_new != -INFINITY);
                 float alpha = 1.f;
@@ -562,17 +568,9 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     m_run = m_new;
                     l_run *= alpha;
                 }
-                // ---- P buffer k & 1 is free once PV of pair k - 2 finished (it read it);
-                //      that wait is nearly always already satisfied ----
-                if (k >= 2) {
-                    ok = __all_sync(0xffffffffu,
-                                    wait_or_fail(&x.pv_done[k & 1], (uint32_t)((k - 2) >> 1) & 1u, fail));
-                    if (!ok) break;
-                    tc::fence_after();
-                }
-                // ---- P = 2^(s*scale - m) as fp16 into TMEM P buffer k & 1: my 64 cells
-                //      are 32 columns (two fp16 per column, lower cell in the low half);
-                //      one exponential in four on the FMA pipe ----
+                // ---- P = 2^(s*scale - m) as fp16 over the S columns just read: my 64
+                //      cells are 32 columns (two fp16 per column, lower cell in the low
+                //      half); one exponential in four on the FMA pipe ----
                 {
                     const bool any = m_run != -INFINITY;   // false for lanes past the block
                     const float nm = -m_run;
@@ -593,26 +591,24 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         pw[c2] = *reinterpret_cast<uint32_t *>(&hv);
                     }
                     l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                    tc::st32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + COL_P + 64u * (uint32_t)(k & 1) +
-                                 32u * (uint32_t)ch, pw);
+                    tc::st32(s_addr, pw);
                 }
-                // ---- O *= alpha where the running maximum moved (rare), my 64 columns;
-                //      O is stable once PV of pair k - 1 finished ----
+                // ---- O_ch *= alpha where this half's running maximum moved (rare);
+                //      O_ch is stable once PV of pair k - 1 finished ----
                 if (j > 0 && __any_sync(0xffffffffu, grow)) {
                     ok = __all_sync(0xffffffffu,
                                     wait_or_fail(&x.pv_done[(k - 1) & 1], (uint32_t)((k - 1) >> 1) & 1u, fail));
                     if (!ok) break;
                     tc::fence_after();
 #pragma unroll 1
-                    for (int q2 = 0; q2 < 2; ++q2) {
+                    for (int q2 = 0; q2 < 4; ++q2) {
                         uint32_t r[32];
-                        const uint32_t ta = lane_base + COL_O + (uint32_t)q2 * 32u;
+                        const uint32_t ta = o_mine + (uint32_t)q2 * 32u;
                         tc::ld32(ta, r);
 #pragma unroll
                         for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
                         tc::st32(ta, r);
                     }
-                    tc::wait_st();
                 }
                 if (!full) {
                     // V rows of cells nobody in the block sees: zero (P is 0 there; V may
@@ -631,46 +627,66 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 kvd::mbar_arrive(&x.p_full[k & 1]);
             }
             if (!ok) break;
-            // ---- epilogue: wait for the last PV (pair k - 1), read my 64 columns of O ----
+            // ---- wait for the item's last PV (pair k - 1) ----
             ok = __all_sync(0xffffffffu,
                             wait_or_fail(&x.pv_done[(k - 1) & 1], (uint32_t)((k - 1) >> 1) & 1u, fail));
             if (!ok) break;
             tc::fence_after();
-            {
-                uint32_t r[64];
-                tc::ld64(lane_base + COL_O, r);
-#pragma unroll
-                for (int c = 0; c < 64; ++c) ov[c] = __uint_as_float(r[c]);
-            }
-            tc::fence_before();
             }   // it.pairs > 0
-            // ---- the row sum over both halves (double-buffered by item parity) ----
+            // ---- combine the halves: O = (2^(m0-M) O_0 + 2^(m1-M) O_1) / (2^(m0-M) l0 + 2^(m1-M) l1);
+            //      thread (n, ch) produces d = 64ch .. 64ch + 63 (exchange double-buffered by item parity) ----
+            x.mex[n_l & 1][ch][n] = m_run;
             x.lex[n_l & 1][ch][n] = l_run;
             kvd::mbar_arrive(&x.lbar);
             ok = __all_sync(0xffffffffu, wait_or_fail(&x.lbar, n_l & 1u, fail));
             if (!ok) break;
-            const float l_tot = x.lex[n_l & 1][0][n] + x.lex[n_l & 1][1][n];
+            const float m0 = x.mex[n_l & 1][0][n], m1 = x.mex[n_l & 1][1][n];
+            const float l0 = x.lex[n_l & 1][0][n], l1 = x.lex[n_l & 1][1][n];
             ++n_l;
+            const float mm = fmaxf(m0, m1);
+            const float s0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - mm);
+            const float s1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mm);
+            const float l_tot = s0 * l0 + s1 * l1;
+            float *dst = nullptr;
+            float sc = 1.f;
             if (it.nitems == 1) {
-                if (live) {
-                    const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-#pragma unroll
-                    for (int c = 0; c < 64; c += 4)
-                        *reinterpret_cast<float4 *>(orow + c) =
-                            make_float4(ov[c] * inv, ov[c + 1] * inv, ov[c + 2] * inv, ov[c + 3] * inv);
-                }
+                if (live) dst = a.o + ((int64_t)row * a.n_head + h) * 128 + 64 * ch;
+                sc = l_tot > 0.f ? 1.f / l_tot : 0.f;
             } else {
                 // a split block: this item's partial (its slot is its index among the
                 // prefill items); k_merge_pf combines the partials after the kernel
                 float *pp = a.part + (((int64_t)wi * a.n_head_kv + hk) * M + n) * PART_STRIDE;
                 if (ch == 0) {
-                    pp[0] = m_run;
+                    pp[0] = mm;
                     pp[1] = l_tot;
                 }
-#pragma unroll
-                for (int c = 0; c < 64; c += 4)
-                    *reinterpret_cast<float4 *>(pp + 4 + 64 * ch + c) = make_float4(ov[c], ov[c + 1], ov[c + 2], ov[c + 3]);
+                dst = pp + 4 + 64 * ch;
             }
+            const float f0 = s0 * sc, f1 = s1 * sc;
+#pragma unroll 1
+            for (int q2 = 0; q2 < 2; ++q2) {
+                uint32_t r0[32], r1[32];
+                if (it.pairs > 0) {              // item-uniform: the TMEM reads stay warp collective
+                    const uint32_t ta = tmem + lane_q + COL_O + (uint32_t)(64 * ch + 32 * q2);
+                    tc::ld32(ta, r0);
+                    tc::ld32(ta + 128u, r1);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) r0[c] = r1[c] = 0u;
+                }
+                if (dst) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        float4 v;
+                        v.x = __uint_as_float(r0[c + 0]) * f0 + __uint_as_float(r1[c + 0]) * f1;
+                        v.y = __uint_as_float(r0[c + 1]) * f0 + __uint_as_float(r1[c + 1]) * f1;
+                        v.z = __uint_as_float(r0[c + 2]) * f0 + __uint_as_float(r1[c + 2]) * f1;
+                        v.w = __uint_as_float(r0[c + 3]) * f0 + __uint_as_float(r1[c + 3]) * f1;
+                        *reinterpret_cast<float4 *>(dst + 32 * q2 + c) = v;
+                    }
+                }
+            }
+            tc::fence_before();
         }
     }
 
@@ -684,17 +700,25 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
 }
 
 
-// Split-K merge of the prefill path: one CTA per (prefill block, KV head);
-// blocks covered by a single item were written directly and return at once.
-// Thread t takes row t / 2 and half of its 128 values, so every load is
-// independent of the others:  O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
+// Split-K merge of the prefill path: eight CTAs per (prefill block, KV head),
+// 16 query vectors each; blocks covered by a single item were written directly
+// and return at once.  Thread t takes query vector 16z + t / 16 and 8 of its
+// 128 values, and loads up to eight partials at once (one round trip to L2
+// for most blocks), folding them into a running (M, L, O):
+//   O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
+// Launched as a programmatic dependent of the attention kernel: the plan is
+// read first, the partials only after the attention grid has finished.
+constexpr int MERGE_SPLIT = 8;
+constexpr int MERGE_QMAX = 8;
+
 __global__ void __launch_bounds__(256) k_merge_pf(const kvk::PrefillArgs a) {
     const int32_t b = a.u.n_dec_blocks + blockIdx.x;
     const int32_t hk = blockIdx.y;
     const int32_t nitems = a.p.blk_nitems[b];
     if (nitems <= 1) return;
     const kvi::DevBlock blk = a.u.blocks[b];
-    const int32_t n = threadIdx.x >> 1, half = threadIdx.x & 1;
+    const int32_t n = (int32_t)blockIdx.z * (M / MERGE_SPLIT) + (int32_t)(threadIdx.x >> 4);
+    const int32_t d0 = (int32_t)(threadIdx.x & 15) * 8;
     const int32_t G = a.gqa;
     if (n >= blk.n_rows * G) return;
     const int32_t row = a.u.perm[blk.row0 + n / G];
@@ -702,37 +726,55 @@ __global__ void __launch_bounds__(256) k_merge_pf(const kvk::PrefillArgs a) {
     const int32_t first = a.p.blk_item0[b] - a.p.cap_dec;
     const int64_t istride = (int64_t)a.n_head_kv * M * PART_STRIDE;
     const float *pr = a.part + (((int64_t)first * a.n_head_kv + hk) * M + n) * PART_STRIDE;
-    float Mx = -INFINITY;
-    for (int32_t q = 0; q < nitems; ++q) Mx = fmaxf(Mx, __ldcg(pr + q * istride));
-    float acc[64];
+    kvd::pdl_wait();
+    float mx = -INFINITY, L = 0.f;
+    float acc[8];
 #pragma unroll
-    for (int c = 0; c < 64; ++c) acc[c] = 0.f;
-    float L = 0.f;
-    if (Mx != -INFINITY) {
-        for (int32_t q = 0; q < nitems; ++q) {
-            const float *pq = pr + q * istride;
-            const float mk = __ldcg(pq);
-            const float lk = __ldcg(pq + 1);
-            float4 v[16];
+    for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+    for (int32_t q0 = 0; q0 < nitems; q0 += MERGE_QMAX) {
+        float mk[MERGE_QMAX], lk[MERGE_QMAX];
+        float4 v0[MERGE_QMAX], v1[MERGE_QMAX];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) v[c] = __ldcg(reinterpret_cast<const float4 *>(pq + 4 + 64 * half) + c);
-            const float sc = mk == -INFINITY ? 0.f : ex2_approx(mk - Mx);
-            L = fmaf(lk, sc, L);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                acc[4 * c + 0] = fmaf(v[c].x, sc, acc[4 * c + 0]);
-                acc[4 * c + 1] = fmaf(v[c].y, sc, acc[4 * c + 1]);
-                acc[4 * c + 2] = fmaf(v[c].z, sc, acc[4 * c + 2]);
-                acc[4 * c + 3] = fmaf(v[c].w, sc, acc[4 * c + 3]);
+        for (int i = 0; i < MERGE_QMAX; ++i) {
+            mk[i] = -INFINITY;
+            lk[i] = 0.f;
+            v0[i] = v1[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (q0 + i < nitems) {
+                const float *pq = pr + (int64_t)(q0 + i) * istride;
+                mk[i] = __ldcg(pq);
+                lk[i] = __ldcg(pq + 1);
+                v0[i] = __ldcg(reinterpret_cast<const float4 *>(pq + 4 + d0));
+                v1[i] = __ldcg(reinterpret_cast<const float4 *>(pq + 4 + d0) + 1);
             }
         }
+        float mr = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < MERGE_QMAX; ++i) mr = fmaxf(mr, mk[i]);
+        const float mn = fmaxf(mx, mr);
+        if (mn == -INFINITY) continue;
+        const float al = mx == -INFINITY ? 0.f : ex2_approx(mx - mn);
+        L *= al;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[c] *= al;
+#pragma unroll
+        for (int i = 0; i < MERGE_QMAX; ++i) {
+            const float sc = mk[i] == -INFINITY ? 0.f : ex2_approx(mk[i] - mn);
+            L = fmaf(lk[i], sc, L);
+            acc[0] = fmaf(v0[i].x, sc, acc[0]);
+            acc[1] = fmaf(v0[i].y, sc, acc[1]);
+            acc[2] = fmaf(v0[i].z, sc, acc[2]);
+            acc[3] = fmaf(v0[i].w, sc, acc[3]);
+            acc[4] = fmaf(v1[i].x, sc, acc[4]);
+            acc[5] = fmaf(v1[i].y, sc, acc[5]);
+            acc[6] = fmaf(v1[i].z, sc, acc[6]);
+            acc[7] = fmaf(v1[i].w, sc, acc[7]);
+        }
+        mx = mn;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    float *dst = a.o + ((int64_t)row * a.n_head + h) * 128 + 64 * half;
-#pragma unroll
-    for (int c = 0; c < 16; ++c)
-        reinterpret_cast<float4 *>(dst)[c] =
-            make_float4(acc[4 * c] * inv, acc[4 * c + 1] * inv, acc[4 * c + 2] * inv, acc[4 * c + 3] * inv);
+    float4 *dst = reinterpret_cast<float4 *>(a.o + ((int64_t)row * a.n_head + h) * 128 + d0);
+    dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
 }
 
 }  // namespace
@@ -741,17 +783,33 @@ namespace kvk {
 
 cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const PrefillArgs &a,
                            int32_t grid_x, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
+    static bool smem_set = false;
+    if (!smem_set) {
         cudaError_t e = cudaFuncSetAttribute(k_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr = true;
+        smem_set = true;
     }
-    k_prefill<<<dim3(grid_x, a.n_head_kv), NT, SMEM_BYTES, st>>>(*tm_k, *tm_v, a);
-    cudaError_t e = cudaGetLastError();
+    // Both kernels are programmatic dependents of the kernel before them: the
+    // attention kernel sets up (and, with early_ok, reads its plan) while the K/V
+    // store finishes; the merge reads the plan while the attention kernel runs.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_x, a.n_head_kv);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_prefill, *tm_k, *tm_v, a);
     if (e != cudaSuccess) return e;
-    k_merge_pf<<<dim3(a.u.n_blocks - a.u.n_dec_blocks, a.n_head_kv), 256, 0, st>>>(a);
+    cfg.gridDim = dim3(a.u.n_blocks - a.u.n_dec_blocks, a.n_head_kv, MERGE_SPLIT);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, k_merge_pf, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

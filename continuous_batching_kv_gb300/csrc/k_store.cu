@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(256) k_store(uint4 *__restrict__ kc, uint4 *__
                                                const kvi::DevRow *__restrict__ rows, int32_t n_tokens,
                                                int32_t chunks_per_row, int64_t n_cells,
                                                int32_t *err) {
+    kvd::pdl_trigger();   // the attention kernel that follows may start its set-up now
     const int64_t total = (int64_t)n_tokens * chunks_per_row;
     for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
          t += (int64_t)gridDim.x * blockDim.x) {

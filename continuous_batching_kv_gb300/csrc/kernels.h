@@ -95,6 +95,9 @@ struct PrefillArgs {
     int32_t gx_dec;         // decode grid columns (offset of the prefill cta_item0 table)
     float scale_log2;
     int32_t *err;
+    int32_t early_ok;       // 1: the plan, tables and cell mirror were complete before the
+                            // previous kernel of the stream began, so they may be read before
+                            // waiting for it (the kernel is launched as a programmatic dependent)
 };
 cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const PrefillArgs &a,
                            int32_t grid_x, cudaStream_t st);
