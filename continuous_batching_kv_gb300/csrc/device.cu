@@ -202,6 +202,13 @@ int sync_device(kv_cache *c, const kv_split *sp, cudaStream_t st) {
     return KV_OK;
 }
 
+// The most query vectors in one decode block of the ubatch (rows x GQA group).
+int32_t decode_nq_max(const kv_cache *c, const UbatchHost &u) {
+    int32_t r = 1;
+    for (int32_t b = 0; b < u.n_dec_blocks; ++b) r = std::max(r, u.blocks[b].n_rows * c->gqa);
+    return r;
+}
+
 int check_call(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer) {
     if (!c || !sp || sp->owner != c) return KV_E_INVAL;
     if (!c->has_device) return c->set_err(KV_E_NO_DEVICE, "host-only cache");
@@ -368,6 +375,8 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
         a.gqa = c->gqa;
         a.scale_log2 = scale_log2;
         a.err = d->d_err;
+        a.nq_max = decode_nq_max(c, u);
+        a.early_ok = early_ok ? 1 : 0;
         if ((e = kvk::launch_decode(&d->tm_k[layer], &d->tm_v[layer], a, d->gx_dec, st)) != cudaSuccess)
             return cuda_fail(c, e, "decode launch");
         c->launches += 1;
@@ -485,9 +494,11 @@ extern "C" int ubatch_attention_static_scratch(kv_cache *c, const kv_split *sp, 
     unsigned char *scratch = nullptr;
     if ((e = static_scratch(cur, &scratch)) != cudaSuccess) return cuda_fail(c, e, "scratch address");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool early_ok = !c->pending_reset && c->pending.empty() && c->dev_tables_split == sp->id && !mask_out;
     if ((rc = sync_device(c, sp, st)) != KV_OK) return rc;
     kvk::UbView v = make_view(c, sp, ub);
     if (d->plan_split != sp->id || d->plan_ub != ub) {
+        early_ok = false;
         if ((e = kvk::launch_plan(v, d->plan, c->prm.n_stream, d->gx_dec, d->gx_pf, st)) != cudaSuccess)
             return cuda_fail(c, e, "plan launch");
         c->launches += 3;
@@ -514,6 +525,9 @@ extern "C" int ubatch_attention_static_scratch(kv_cache *c, const kv_split *sp, 
     a.gqa = c->gqa;
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)c->prm.head_dim);
     a.err = d->d_err;
+    a.nq_max = decode_nq_max(c, u);
+    // the counters were just cleared by a copy engine, not a kernel: wait for it
+    a.early_ok = 0;
     if ((e = kvk::launch_decode(&d->tm_k[layer], &d->tm_v[layer], a, d->gx_dec, st)) != cudaSuccess)
         return cuda_fail(c, e, "decode launch");
     c->launches += 1;

@@ -6,42 +6,50 @@
 // Batching", "The budget that actually binds": the n_head / n_head_kv query
 // heads of a group share one KV head.
 //
-// Design (sm_103a):
-//  * grid = (CTA columns, KV heads); each CTA column owns an equal slice of
-//    the concatenated visible-tile lists of all decode blocks (stream-K),
-//    split at block boundaries into work items; a block is up to 16 query
-//    vectors (rows sharing a first sequence id, times the GQA group), so every
-//    K/V byte read serves all of them;
-//  * warp 4 is the producer: it streams K and V tiles with TMA (2-D tensor
-//    maps, 128-byte swizzle) into a 3-stage ring and, for tiles that are not
-//    fully visible, the cells' visibility and positions into the same slot;
-//    full/empty mbarriers, every wait bounded (a timeout sets the error word);
-//  * warps 0-3 consume: scores with one thread per (cell, query parity), fp32
-//    FMA on fp16 K; online softmax in base 2 with warp-shuffle max/sum; PV
-//    with one thread per (d pair, cell parity);
-//  * cells nobody in the block may see are never multiplied (masked scores
-//    are replaced by -inf and PV skips such cells, so a NaN in an unused cell
-//    cannot leak);
-//  * the items of one block are merged by the last CTA to finish (atomic
-//    counter, no spinning): O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
+// Design (sm_103a), templated on NQ, the query vectors one block may hold
+// (1, 2, 4, 8 or 16; the ubatch's largest decode block picks the instance):
+//  * grid = (CTA columns, KV heads), two CTAs per SM; each CTA column owns an
+//    equal slice of the concatenated visible-tile lists of all decode blocks
+//    (stream-K), split at block boundaries into work items; a block is up to
+//    16 query vectors (rows sharing a first sequence id, times the GQA group),
+//    so every K/V byte read serves all of them;
+//  * warp 8 is the producer: K and V of one 64-cell tile per stage, by TMA
+//    (2-D tensor maps, 128-byte swizzle), into a 2- or 3-stage ring, with the
+//    visibility of the cells of tiles that are not fully visible; its first
+//    copy waits for the previous kernel of the stream (programmatic dependent
+//    launch); every wait is bounded (a timeout sets the error word);
+//  * warps 0-7 consume, each owning 8 cells of every tile and its own online
+//    softmax state, with no barrier between warps inside an item: scores with
+//    four lanes per cell (32 of the 128 d each, fp16 K times fp32 Q in fp32
+//    FMA, summed by two shuffles), softmax in base 2 (the running maximum is
+//    moved only when it grows by more than 2^8), PV with each lane owning 4 of
+//    the 128 d;
+//  * cells outside the block's sequence are skipped in PV, so a NaN in an
+//    unused cell cannot leak (masked cells of the sequence hold finite data);
+//  * at an item's end the 8 warp states are merged in three rounds through
+//    shared memory; a block covered by one item is written at once, the items
+//    of a split block leave partials that the last CTA to finish merges
+//    (atomic count, no spinning):
+//      O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
 
 #include "dev_common.cuh"
 #include "kernels.h"
-#include "tc.cuh"
 
 namespace {
 
 using kvi::TILE;
 using kvi::DEC_QMAX;
 
-constexpr int NCONS = 128;                      // consumer threads (warps 0-3)
+constexpr int NW = 8;                           // consumer warps
+constexpr int NCONS = NW * 32;
 constexpr int NT = NCONS + 32;                  // + producer warp
-constexpr int STAGES = 3;
 constexpr int BOX_BYTES = TILE * 128;           // 64 rows x 64 fp16
 constexpr int STAGE_BYTES = 4 * BOX_BYTES;      // K lo, K hi, V lo, V hi
 constexpr int PART_STRIDE = 132;                // m, l, pad, pad, o[128]
-constexpr int HQ = DEC_QMAX / 2;
-constexpr int PT_STRIDE = DEC_QMAX + 4;         // padded: 4-way instead of 16-way bank conflicts
+constexpr float RESCALE_LOG2 = 8.0f;
+
+template <int NQ>
+constexpr int stages_for() { return NQ <= 4 ? 3 : 2; }
 
 struct Meta {                 // per stage: what the producer learned about the tile
     int32_t full;
@@ -50,20 +58,30 @@ struct Meta {                 // per stage: what the producer learned about the 
     uint8_t has[TILE];        // cell holds the block's sequence and is not from a later ubatch
 };
 
+template <int NQ>
 struct __align__(16) Aux {
-    Meta meta[STAGES];
-    __half q[DEC_QMAX][128];      // queries as given (fp16)
-    float s[DEC_QMAX][TILE];      // scores of the current tile (log2 units)
-    float pt[TILE][PT_STRIDE];    // probabilities, cell-major
-    float m[DEC_QMAX], l[DEC_QMAX], alpha[DEC_QMAX];
-    int32_t rpos[DEC_QMAX];
-    uint64_t full[STAGES], empty[STAGES];
-    uint8_t anyvis[2][TILE];
+    static constexpr int S = stages_for<NQ>();
+    static constexpr int PQ = NQ < 4 ? 4 : NQ;  // padded for 16-byte loads
+    Meta meta[S];
+    float q[NQ][4][36];           // queries in fp32: q[n][dq][j] = Q[n][32 dq + j]
+    float p[NW][8][PQ];           // each warp's probabilities, cell-major
+    float scr_m[4][NQ];           // tree merge: the writing warps' maxima,
+    float scr_l[4][NQ];           //   row sums
+    float scr_o[4][NQ][128];      //   and accumulators
+    int32_t rpos[NQ];
+    uint64_t full[S], empty[S];
+    uint64_t cbar;                // consumer exchanges (all 256 consumer threads)
     int32_t fail;
-    int32_t flag;
 };
 
-constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + sizeof(Aux);
+template <int NQ>
+constexpr size_t smem_bytes() { return (size_t)stages_for<NQ>() * STAGE_BYTES + sizeof(Aux<NQ>); }
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, volatile int32_t *fail) {
     if (kvd::mbar_try_wait(bar, parity)) return true;
@@ -78,30 +96,33 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, vol
     return true;
 }
 
-// Named barrier over the consumer warps that also ORs a predicate.
-__device__ __forceinline__ bool cons_bar_or(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.or.pred p, 1, %2, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r) : "r"((uint32_t)v), "r"(NCONS) : "memory");
-    return r != 0;
+// All 256 consumer threads meet (arrive, then a bounded wait: a thread that
+// gave up elsewhere makes the others time out instead of hanging).
+__device__ __forceinline__ bool cons_sync(uint64_t *bar, uint32_t &phase, volatile int32_t *fail) {
+    kvd::mbar_arrive(bar);
+    const bool ok = __all_sync(0xffffffffu, wait_or_fail(bar, phase & 1u, fail));
+    ++phase;
+    return ok;
 }
-__device__ __forceinline__ void cons_bar() { tc::named_bar(1, NCONS); }
 
-__global__ void __launch_bounds__(NT, 2)
+template <int NQ>
+__global__ void __launch_bounds__(NT, (NQ <= 8 ? 2 : 1))
 k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
          const kvk::DecodeArgs a) {
+    constexpr int S = stages_for<NQ>();
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *stages = smem;
-    Aux &x = *reinterpret_cast<Aux *>(smem + (size_t)STAGES * STAGE_BYTES);
+    Aux<NQ> &x = *reinterpret_cast<Aux<NQ> *>(smem + (size_t)S * STAGE_BYTES);
     volatile int32_t *fail = &x.fail;
     const int32_t tid = threadIdx.x;
     const int32_t lane = tid & 31, warp = tid >> 5;
     const int32_t hk = blockIdx.y;
     const int32_t G = a.gqa;
+    // Launched as a programmatic dependent: the plan, tables and cell mirror are
+    // read before waiting for the previous kernel only when they were complete
+    // before it began; Q, the K/V cache and the outputs only after the wait.
+    if (!a.early_ok) kvd::pdl_wait();
+    if (tid == 0) kvd::pdl_trigger();
     const int32_t i0 = a.p.cta_item0[blockIdx.x];
     const int32_t i1 = a.p.cta_item0[blockIdx.x + 1];
 
@@ -112,18 +133,20 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     if (tid == 0) {
         kvd::prefetch_tmap(&tm_k);
         kvd::prefetch_tmap(&tm_v);
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < S; ++s) {
             kvd::mbar_init(&x.full[s], 33);    // producer lane 0's expect_tx + 32 lanes
-            kvd::mbar_init(&x.empty[s], 4);    // one arrival per consumer warp
+            kvd::mbar_init(&x.empty[s], NW);   // one arrival per consumer warp
         }
+        kvd::mbar_init(&x.cbar, NCONS);
         x.fail = 0;
         kvd::fence_mbar_init();
     }
     __syncthreads();
 
-    if (warp == 4) {
+    if (warp == NW) {
         // ======================= producer =======================
         int32_t k = 0;
+        bool dep_done = false;
         // wait outcomes and the loop condition are agreed by the whole warp, so a
         // failure never splits it in front of __syncwarp
         for (int32_t wi = i0; wi < i1 && __all_sync(0xffffffffu, *fail == 0); ++wi) {
@@ -132,12 +155,31 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             const int32_t *list = a.p.tiles + (int64_t)w.block * a.p.tile_stride;
             const uint32_t *flg = a.p.flags + (int64_t)w.block * a.p.tile_stride;
             for (int32_t li = w.t0; li < w.t1; ++li) {
-                const int32_t st = k % STAGES;
-                if (k >= STAGES &&
-                    !__all_sync(0xffffffffu, wait_or_fail(&x.empty[st], (uint32_t)((k / STAGES) - 1) & 1u, fail)))
-                    break;
+                const int32_t st = k % S;
+                // the tile's list entry and visibility are read before its slot is free
                 const int32_t t = list[li];
                 const bool full = (int32_t)(flg[t] & 0xffffu) == b.n_rows * TILE;
+                bool hs[2] = {false, false};
+                int32_t cp[2] = {0, 0};
+                if (!full) {
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int32_t j = t * TILE + lane + 32 * r;
+                        if (j < a.u.n_kv) {
+                            const int64_t g = (int64_t)b.stream * a.u.kv_size + j;
+                            const uint64_t wb = a.u.cell_bits[g * a.u.n_words + (b.seq0 >> 6)];
+                            hs[r] = ((wb >> (b.seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
+                            cp[r] = a.u.cell_pos[g];
+                        }
+                    }
+                }
+                if (k >= S &&
+                    !__all_sync(0xffffffffu, wait_or_fail(&x.empty[st], (uint32_t)((k / S) - 1) & 1u, fail)))
+                    break;
+                if (!dep_done) {   // the K/V rows of this ubatch are written by the kernel before
+                    kvd::pdl_wait();
+                    dep_done = true;
+                }
                 if (lane == 0) {
                     uint8_t *sp = stages + (size_t)st * STAGE_BYTES;
                     const int32_t y = b.stream * a.u.kv_size + t * TILE;
@@ -153,18 +195,8 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 if (!full) {
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        const int32_t c = lane + 32 * r;
-                        const int32_t j = t * TILE + c;
-                        bool has = false;
-                        int32_t cp = 0;
-                        if (j < a.u.n_kv) {
-                            const int64_t g = (int64_t)b.stream * a.u.kv_size + j;
-                            const uint64_t wb = a.u.cell_bits[g * a.u.n_words + (b.seq0 >> 6)];
-                            has = ((wb >> (b.seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
-                            cp = a.u.cell_pos[g];
-                        }
-                        x.meta[st].has[c] = has ? 1 : 0;
-                        x.meta[st].cpos[c] = cp;
+                        x.meta[st].has[lane + 32 * r] = hs[r] ? 1 : 0;
+                        x.meta[st].cpos[lane + 32 * r] = cp[r];
                     }
                 }
                 __syncwarp();
@@ -174,253 +206,305 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         }
         if (*fail && lane == 0) {
             // let copies already in flight land before the CTA's smem is released
-            for (int32_t q = k > STAGES ? k - STAGES : 0; q < k; ++q)
-                (void)kvd::mbar_wait_bounded(&x.full[q % STAGES], (uint32_t)(q / STAGES) & 1u);
+            for (int32_t q = k > S ? k - S : 0; q < k; ++q)
+                (void)kvd::mbar_wait_bounded(&x.full[q % S], (uint32_t)(q / S) & 1u);
         }
     } else {
         // ======================= consumers =======================
+        const int32_t c = lane >> 2;               // scores: my cell among the warp's 8
+        const int32_t dq = lane & 3;               // scores: my quarter of d
+        const int32_t cw = warp * 8 + c;           // my cell within the tile
+        uint32_t cph = 0;                          // consumer-barrier phase
         int32_t k = 0;
-        const int32_t c_cell = tid & (TILE - 1);   // scores: my cell
-        const int32_t par = tid >> 6;              // scores: query parity / PV: cell parity
-        const int32_t dp = (tid & 63) * 2;         // PV: my d pair
-        bool failed = false;
-        for (int32_t wi = i0; wi < i1 && !failed; ++wi) {
+        bool ok = true;
+        bool dep_done = false;
+        for (int32_t wi = i0; wi < i1 && ok; ++wi) {
             const kvk::WorkItem w = a.p.work[wi];
             const kvi::DevBlock b = a.u.blocks[w.block];
-            const int32_t NQ = b.n_rows * G;
-            for (int32_t e = tid; e < NQ * 16; e += NCONS) {
-                const int32_t n = e >> 4, dd = (e & 15) * 8;
-                const int32_t row = a.u.perm[b.row0 + n / G];
-                const int32_t h = hk * G + (n % G);
-                *reinterpret_cast<uint4 *>(&x.q[n][dd]) = *reinterpret_cast<const uint4 *>(
-                    a.q + ((int64_t)row * a.n_head + h) * 128 + dd);
+            const int32_t nq = b.n_rows * G;
+            if (!dep_done) {   // before the first read of Q and the first write of an output
+                kvd::pdl_wait();
+                dep_done = true;
             }
-            if (tid < DEC_QMAX) {
-                x.m[tid] = -INFINITY;
-                x.l[tid] = 0.f;
-                x.rpos[tid] = tid < b.n_rows ? a.u.rows[a.u.perm[b.row0 + tid]].pos : 0;
-            }
-            float acc[DEC_QMAX][2];
+            // ---- Q (fp32) and the rows' positions ----
+            {
+                const int32_t n = tid >> 4, part = tid & 15;   // 8 values of query vector n
+                if (n < NQ) {
+                    float v[8];
 #pragma unroll
-            for (int n = 0; n < DEC_QMAX; ++n) acc[n][0] = acc[n][1] = 0.f;
-            cons_bar();
-
-            for (int32_t li = w.t0; li < w.t1; ++li) {
-                const int32_t st = k % STAGES;
-                const bool ok = wait_or_fail(&x.full[st], (uint32_t)(k / STAGES) & 1u, fail);
-                if (cons_bar_or(!ok)) { failed = true; break; }
-                const uint8_t *sp = stages + (size_t)st * STAGE_BYTES;
-                const int32_t vb = k & 1;
-                // ---- phase A: visibility and scores ----
-                const bool full = x.meta[st].full != 0;
-                const bool has = full || x.meta[st].has[c_cell];
-                const int32_t cpos = full ? 0 : x.meta[st].cpos[c_cell];
-                float dot[HQ];
-#pragma unroll
-                for (int q = 0; q < HQ; ++q) dot[q] = 0.f;
-                if (has) {
-#pragma unroll 4
-                    for (int ch = 0; ch < 16; ++ch) {
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(
-                            sp + (ch >> 3) * BOX_BYTES + kvd::swz128(c_cell, ch & 7));
+                    for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                    if (n < nq) {
+                        const int32_t row = a.u.perm[b.row0 + n / G];
+                        const int32_t h = hk * G + (n % G);
+                        const uint4 raw =
+                            *reinterpret_cast<const uint4 *>(a.q + ((int64_t)row * a.n_head + h) * 128 + 8 * part);
                         const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
-                        float kf[8];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float2 f = __half22float2(h2[e]);
-                            kf[2 * e] = f.x;
-                            kf[2 * e + 1] = f.y;
+                            v[2 * e] = f.x;
+                            v[2 * e + 1] = f.y;
                         }
+                    }
+                    float *dst = &x.q[n][part >> 2][(part & 3) * 8];
+                    *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+                    *reinterpret_cast<float4 *>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
+                }
+                if (tid < NQ) x.rpos[tid] = tid < nq ? a.u.rows[a.u.perm[b.row0 + tid / G]].pos : 0;
+            }
+            if (!(ok = cons_sync(&x.cbar, cph, fail))) break;
+
+            float m[NQ], lp[NQ], acc[NQ][4];
 #pragma unroll
-                        for (int q = 0; q < HQ; ++q) {
-                            const int n = 2 * q + par;
-                            if (n < NQ) {
-                                const uint4 qr = *reinterpret_cast<const uint4 *>(&x.q[n][ch * 8]);
-                                const __half2 *q2 = reinterpret_cast<const __half2 *>(&qr);
-                                float d0 = dot[q];
+            for (int n = 0; n < NQ; ++n) {
+                m[n] = -INFINITY;
+                lp[n] = 0.f;
+                acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+            }
+            for (int32_t li = w.t0; li < w.t1; ++li, ++k) {
+                const int32_t st = k % S;
+                ok = __all_sync(0xffffffffu, wait_or_fail(&x.full[st], (uint32_t)(k / S) & 1u, fail));
+                if (!ok) break;
+                const uint8_t *sp = stages + (size_t)st * STAGE_BYTES;
+                const bool full = x.meta[st].full != 0;
+                // ---- scores: my cell, my 32 d, all query vectors ----
+                float s[NQ];
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float2 qf = __half22float2(q2[e]);
-                                    d0 = fmaf(qf.x, kf[2 * e], d0);
-                                    d0 = fmaf(qf.y, kf[2 * e + 1], d0);
+                for (int n = 0; n < NQ; ++n) s[n] = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int ch = 4 * dq + i;             // 16-byte chunk of the 256-byte K row
+                    const uint4 raw =
+                        *reinterpret_cast<const uint4 *>(sp + (ch >> 3) * BOX_BYTES + kvd::swz128(cw, ch & 7));
+                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+                    float kf[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __half22float2(h2[e]);
+                        kf[2 * e] = f.x;
+                        kf[2 * e + 1] = f.y;
+                    }
+#pragma unroll
+                    for (int n = 0; n < NQ; ++n) {
+                        const float4 qa = *reinterpret_cast<const float4 *>(&x.q[n][dq][8 * i]);
+                        const float4 qb = *reinterpret_cast<const float4 *>(&x.q[n][dq][8 * i + 4]);
+                        float d0 = s[n];
+                        d0 = fmaf(qa.x, kf[0], d0);
+                        d0 = fmaf(qa.y, kf[1], d0);
+                        d0 = fmaf(qa.z, kf[2], d0);
+                        d0 = fmaf(qa.w, kf[3], d0);
+                        d0 = fmaf(qb.x, kf[4], d0);
+                        d0 = fmaf(qb.y, kf[5], d0);
+                        d0 = fmaf(qb.z, kf[6], d0);
+                        d0 = fmaf(qb.w, kf[7], d0);
+                        s[n] = d0;
+                    }
+                }
+                const bool has = full || x.meta[st].has[cw];
+                const int32_t cpos = full ? 0 : x.meta[st].cpos[cw];
+#pragma unroll
+                for (int n = 0; n < NQ; ++n) {
+                    float v = s[n];
+                    v += __shfl_xor_sync(0xffffffffu, v, 1);
+                    v += __shfl_xor_sync(0xffffffffu, v, 2);
+                    const bool vis = has && n < nq && (full || !a.u.causal || cpos <= x.rpos[n]);
+                    s[n] = vis ? v * a.scale_log2 : -INFINITY;
+                }
+                // ---- online softmax over my warp's 8 cells (warp-uniform decisions) ----
+#pragma unroll
+                for (int n = 0; n < NQ; ++n) {
+                    float t = s[n];
+                    t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 4));
+                    t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 8));
+                    t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 16));
+                    const float mn = fmaxf(m[n], t);
+                    if (mn > m[n] + RESCALE_LOG2 || (m[n] == -INFINITY && mn != -INFINITY)) {
+                        const float al = ex2_approx(m[n] - mn);
+                        lp[n] *= al;
+                        acc[n][0] *= al;
+                        acc[n][1] *= al;
+                        acc[n][2] *= al;
+                        acc[n][3] *= al;
+                        m[n] = mn;
+                    }
+                    const float pv = m[n] == -INFINITY ? 0.f : ex2_approx(s[n] - m[n]);
+                    if (dq == 0) {
+                        lp[n] += pv;
+                        x.p[warp][c][n] = pv;
+                    }
+                }
+                __syncwarp();
+                // ---- O += P V over my warp's 8 cells; lane owns d = 4 lane .. 4 lane + 3 ----
+                {
+                    const uint8_t *vb = sp + 2 * BOX_BYTES + (lane >> 4) * BOX_BYTES;
+                    const uint32_t chunk = (uint32_t)(lane & 15) >> 1, inner = (uint32_t)(lane & 1) * 8u;
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const int32_t cell = warp * 8 + cc;
+                        if (!full && !x.meta[st].has[cell]) continue;   // warp-uniform
+                        const uint2 raw = *reinterpret_cast<const uint2 *>(vb + kvd::swz128(cell, chunk) + inner);
+                        const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+                        const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+#pragma unroll
+                        for (int n4 = 0; n4 < NQ; n4 += 4) {
+                            const float4 pp = *reinterpret_cast<const float4 *>(&x.p[warp][cc][n4]);
+                            const float pq[4] = {pp.x, pp.y, pp.z, pp.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if (n4 + e < NQ) {
+                                    acc[n4 + e][0] = fmaf(pq[e], v01.x, acc[n4 + e][0]);
+                                    acc[n4 + e][1] = fmaf(pq[e], v01.y, acc[n4 + e][1]);
+                                    acc[n4 + e][2] = fmaf(pq[e], v23.x, acc[n4 + e][2]);
+                                    acc[n4 + e][3] = fmaf(pq[e], v23.y, acc[n4 + e][3]);
                                 }
-                                dot[q] = d0;
                             }
                         }
                     }
                 }
-#pragma unroll
-                for (int q = 0; q < HQ; ++q) {
-                    const int n = 2 * q + par;
-                    if (n < NQ) {
-                        const bool vis = has && (full || !a.u.causal || cpos <= x.rpos[n / G]);
-                        x.s[n][c_cell] = vis ? dot[q] * a.scale_log2 : -INFINITY;
-                    }
-                }
-                if (par == 0) {
-                    const bool any = has && (full || !a.u.causal || cpos <= b.pos_max);
-                    x.anyvis[vb][c_cell] = any ? 1 : 0;
-                }
-                cons_bar();
-                // ---- phase B: online softmax, one warp per query (strided) ----
-                for (int n = warp; n < NQ; n += NCONS / 32) {
-                    const float s0 = x.s[n][lane], s1 = x.s[n][lane + 32];
-                    float tmax = fmaxf(s0, s1);
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-                    const float m_old = x.m[n];
-                    const float m_new = fmaxf(m_old, tmax);
-                    float p0 = 0.f, p1 = 0.f, alpha = 1.f;
-                    if (m_new != -INFINITY) {
-                        p0 = exp2f(s0 - m_new);
-                        p1 = exp2f(s1 - m_new);
-                        alpha = exp2f(m_old - m_new);
-                    }
-                    float ls = p0 + p1;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-                    x.pt[lane][n] = p0;
-                    x.pt[lane + 32][n] = p1;
-                    if (lane == 0) {
-                        x.m[n] = m_new;
-                        x.l[n] = x.l[n] * alpha + ls;
-                        x.alpha[n] = alpha;
-                    }
-                }
-                cons_bar();
-                // ---- phase C: O = alpha O + P V, cells of my parity ----
-#pragma unroll
-                for (int n = 0; n < DEC_QMAX; ++n) {
-                    if (n < NQ) {
-                        const float al = x.alpha[n];
-                        acc[n][0] *= al;
-                        acc[n][1] *= al;
-                    }
-                }
-                const int ch = dp >> 3;
-                const uint32_t vin = (uint32_t)(dp & 7) * 2u;
-                const uint8_t *vbase = sp + 2 * BOX_BYTES + (ch >> 3) * BOX_BYTES;
-                for (int c = par; c < TILE; c += 2) {
-                    if (!x.anyvis[vb][c]) continue;
-                    const float2 v = __half22float2(
-                        *reinterpret_cast<const __half2 *>(vbase + kvd::swz128(c, ch & 7) + vin));
-#pragma unroll
-                    for (int n4 = 0; n4 < DEC_QMAX; n4 += 4) {
-                        if (n4 < NQ) {
-                            const float4 p = *reinterpret_cast<const float4 *>(&x.pt[c][n4]);
-                            acc[n4 + 0][0] = fmaf(p.x, v.x, acc[n4 + 0][0]);
-                            acc[n4 + 0][1] = fmaf(p.x, v.y, acc[n4 + 0][1]);
-                            acc[n4 + 1][0] = fmaf(p.y, v.x, acc[n4 + 1][0]);
-                            acc[n4 + 1][1] = fmaf(p.y, v.y, acc[n4 + 1][1]);
-                            acc[n4 + 2][0] = fmaf(p.z, v.x, acc[n4 + 2][0]);
-                            acc[n4 + 2][1] = fmaf(p.z, v.y, acc[n4 + 2][1]);
-                            acc[n4 + 3][0] = fmaf(p.w, v.x, acc[n4 + 3][0]);
-                            acc[n4 + 3][1] = fmaf(p.w, v.y, acc[n4 + 3][1]);
-                        }
-                    }
-                }
-                // release the stage (K, V and its metadata)
                 __syncwarp();
-                if (lane == 0) kvd::mbar_arrive(&x.empty[st]);
-                ++k;
+                if (lane == 0) kvd::mbar_arrive(&x.empty[st]);   // release the stage (K, V, metadata)
             }
-            if (failed) break;
+            if (!ok) break;
 
-            // ---- merge the two cell parities (s and pt hold 16 x 128 floats) ----
-            cons_bar();
-            float *red = &x.s[0][0];
-            if (par == 1) {
+            // ---- the item's result: merge the 8 warps (three rounds) ----
+            float l[NQ];
 #pragma unroll
-                for (int n = 0; n < DEC_QMAX; ++n) {
-                    if (n < NQ) {
-                        red[n * 128 + dp] = acc[n][0];
-                        red[n * 128 + dp + 1] = acc[n][1];
-                    }
-                }
+            for (int n = 0; n < NQ; ++n) {
+                float v = lp[n];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                l[n] = v;
             }
-            cons_bar();
-            const int32_t nitems = a.p.blk_nitems[w.block];
-            if (par == 0) {
+            for (int sd = 4; sd >= 1 && ok; sd >>= 1) {
+                if (warp >= sd && warp < 2 * sd) {
+                    const int slot = warp - sd;
 #pragma unroll
-                for (int n = 0; n < DEC_QMAX; ++n) {
-                    if (n < NQ) {
-                        acc[n][0] += red[n * 128 + dp];
-                        acc[n][1] += red[n * 128 + dp + 1];
+                    for (int n = 0; n < NQ; ++n) {
+                        if (lane == 0) {
+                            x.scr_m[slot][n] = m[n];
+                            x.scr_l[slot][n] = l[n];
+                        }
+                        *reinterpret_cast<float4 *>(&x.scr_o[slot][n][4 * lane]) =
+                            make_float4(acc[n][0], acc[n][1], acc[n][2], acc[n][3]);
                     }
                 }
+                if (!(ok = cons_sync(&x.cbar, cph, fail))) break;
+                if (warp < sd) {
+#pragma unroll
+                    for (int n = 0; n < NQ; ++n) {
+                        const float m2 = x.scr_m[warp][n], l2 = x.scr_l[warp][n];
+                        const float4 o2 = *reinterpret_cast<const float4 *>(&x.scr_o[warp][n][4 * lane]);
+                        const float mn = fmaxf(m[n], m2);
+                        const float a1 = m[n] == -INFINITY ? 0.f : ex2_approx(m[n] - mn);
+                        const float a2 = m2 == -INFINITY ? 0.f : ex2_approx(m2 - mn);
+                        l[n] = l[n] * a1 + l2 * a2;
+                        acc[n][0] = acc[n][0] * a1 + o2.x * a2;
+                        acc[n][1] = acc[n][1] * a1 + o2.y * a2;
+                        acc[n][2] = acc[n][2] * a1 + o2.z * a2;
+                        acc[n][3] = acc[n][3] * a1 + o2.w * a2;
+                        m[n] = mn;
+                    }
+                }
+                ok = cons_sync(&x.cbar, cph, fail);
+            }
+            if (!ok) break;
+            if (warp == 0) {
+                const int32_t nitems = a.p.blk_nitems[w.block];
                 if (nitems == 1) {
 #pragma unroll
-                    for (int n = 0; n < DEC_QMAX; ++n) {
-                        if (n < NQ) {
-                            const float l = x.l[n];
-                            const float inv = l > 0.f ? 1.f / l : 0.f;
+                    for (int n = 0; n < NQ; ++n) {
+                        if (n < nq) {
+                            const float inv = l[n] > 0.f ? 1.f / l[n] : 0.f;
                             const int32_t row = a.u.perm[b.row0 + n / G];
                             const int32_t h = hk * G + (n % G);
-                            *reinterpret_cast<float2 *>(a.o + ((int64_t)row * a.n_head + h) * 128 + dp) =
-                                make_float2(acc[n][0] * inv, acc[n][1] * inv);
+                            *reinterpret_cast<float4 *>(a.o + ((int64_t)row * a.n_head + h) * 128 + 4 * lane) =
+                                make_float4(acc[n][0] * inv, acc[n][1] * inv, acc[n][2] * inv, acc[n][3] * inv);
                         }
                     }
                 } else {
                     float *pp = a.part + ((int64_t)wi * a.n_head_kv + hk) * DEC_QMAX * PART_STRIDE;
 #pragma unroll
-                    for (int n = 0; n < DEC_QMAX; ++n) {
-                        if (n < NQ) {
-                            *reinterpret_cast<float2 *>(pp + n * PART_STRIDE + 4 + dp) = make_float2(acc[n][0], acc[n][1]);
-                            if (dp == 0) {
-                                pp[n * PART_STRIDE + 0] = x.m[n];
-                                pp[n * PART_STRIDE + 1] = x.l[n];
+                    for (int n = 0; n < NQ; ++n) {
+                        if (n < nq) {
+                            if (lane == 0) {
+                                pp[n * PART_STRIDE + 0] = m[n];
+                                pp[n * PART_STRIDE + 1] = l[n];
                             }
+                            *reinterpret_cast<float4 *>(pp + n * PART_STRIDE + 4 + 4 * lane) =
+                                make_float4(acc[n][0], acc[n][1], acc[n][2], acc[n][3]);
                         }
                     }
-                }
-            }
-            if (nitems > 1) {
-                __threadfence();
-                cons_bar();
-                if (tid == 0) {
-                    const int32_t prev = atomicAdd(&a.p.counters[w.block * a.n_head_kv + hk], 1);
-                    x.flag = (prev == nitems - 1) ? 1 : 0;
-                }
-                cons_bar();
-                if (x.flag) {
                     __threadfence();
-                    const int32_t it0 = a.p.blk_item0[w.block];
-                    for (int32_t e = tid; e < NQ * 64; e += NCONS) {
-                        const int32_t n = e >> 6, d2 = (e & 63) * 2;
-                        float M = -INFINITY;
-                        for (int32_t q = 0; q < nitems; ++q) {
-                            const float *pk = a.part + ((int64_t)(it0 + q) * a.n_head_kv + hk) * DEC_QMAX * PART_STRIDE
-                                              + n * PART_STRIDE;
-                            M = fmaxf(M, __ldcg(pk));
-                        }
-                        float L = 0.f, o0 = 0.f, o1 = 0.f;
-                        if (M != -INFINITY) {
-                            for (int32_t q = 0; q < nitems; ++q) {
-                                const float *pk = a.part + ((int64_t)(it0 + q) * a.n_head_kv + hk) * DEC_QMAX * PART_STRIDE
-                                                  + n * PART_STRIDE;
-                                const float mk = __ldcg(pk);
-                                if (mk == -INFINITY) continue;
-                                const float sc = exp2f(mk - M);
-                                L = fmaf(__ldcg(pk + 1), sc, L);
-                                const float2 ov = __ldcg(reinterpret_cast<const float2 *>(pk + 4 + d2));
-                                o0 = fmaf(ov.x, sc, o0);
-                                o1 = fmaf(ov.y, sc, o1);
+                    __syncwarp();
+                    int32_t prev = 0;
+                    if (lane == 0) prev = atomicAdd(&a.p.counters[w.block * a.n_head_kv + hk], 1);
+                    prev = __shfl_sync(0xffffffffu, prev, 0);
+                    if (prev == nitems - 1) {
+                        // the last piece of the block: merge all of its partials
+                        __threadfence();
+                        const int32_t it0 = a.p.blk_item0[w.block];
+                        const int64_t istride = (int64_t)a.n_head_kv * DEC_QMAX * PART_STRIDE;
+                        const float *pb = a.part + ((int64_t)it0 * a.n_head_kv + hk) * DEC_QMAX * PART_STRIDE;
+                        for (int32_t n = 0; n < nq; ++n) {
+                            const float *pn = pb + n * PART_STRIDE;
+                            float M = -INFINITY;
+                            for (int32_t q = 0; q < nitems; ++q) M = fmaxf(M, __ldcg(pn + q * istride));
+                            float L = 0.f;
+                            float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (M != -INFINITY) {
+                                for (int32_t q = 0; q < nitems; ++q) {
+                                    const float *pk = pn + q * istride;
+                                    const float mk = __ldcg(pk);
+                                    const float lk = __ldcg(pk + 1);
+                                    const float4 ov = __ldcg(reinterpret_cast<const float4 *>(pk + 4) + lane);
+                                    const float sc = mk == -INFINITY ? 0.f : ex2_approx(mk - M);
+                                    L = fmaf(lk, sc, L);
+                                    o4.x = fmaf(ov.x, sc, o4.x);
+                                    o4.y = fmaf(ov.y, sc, o4.y);
+                                    o4.z = fmaf(ov.z, sc, o4.z);
+                                    o4.w = fmaf(ov.w, sc, o4.w);
+                                }
                             }
+                            const float inv = L > 0.f ? 1.f / L : 0.f;
+                            const int32_t row = a.u.perm[b.row0 + n / G];
+                            const int32_t h = hk * G + (n % G);
+                            *reinterpret_cast<float4 *>(a.o + ((int64_t)row * a.n_head + h) * 128 + 4 * lane) =
+                                make_float4(o4.x * inv, o4.y * inv, o4.z * inv, o4.w * inv);
                         }
-                        const float inv = L > 0.f ? 1.f / L : 0.f;
-                        const int32_t row = a.u.perm[b.row0 + n / G];
-                        const int32_t h = hk * G + (n % G);
-                        *reinterpret_cast<float2 *>(a.o + ((int64_t)row * a.n_head + h) * 128 + d2) =
-                            make_float2(o0 * inv, o1 * inv);
+                        if (lane == 0) a.p.counters[w.block * a.n_head_kv + hk] = 0;
                     }
-                    if (tid == 0) a.p.counters[w.block * a.n_head_kv + hk] = 0;
                 }
             }
-            cons_bar();
         }
     }
     __syncthreads();
     if (*fail && tid == 0) kvd::report(a.err, kvd::DERR_TMA_TIMEOUT);
+}
+
+template <int NQ>
+cudaError_t launch_nq(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const kvk::DecodeArgs &a, int32_t grid_x,
+                      cudaStream_t st) {
+    static bool smem_set = false;
+    constexpr size_t SMEM = smem_bytes<NQ>();
+    if (!smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_decode<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+        if (e != cudaSuccess) return e;
+        smem_set = true;
+    }
+    // a programmatic dependent of the kernel before it (normally the K/V store)
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_x, a.n_head_kv);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_decode<NQ>, *tm_k, *tm_v, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -431,15 +515,11 @@ int32_t decode_ctas_per_sm() { return 2; }
 
 cudaError_t launch_decode(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const DecodeArgs &a,
                           int32_t grid_x, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_decode, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    k_decode<<<dim3(grid_x, a.n_head_kv), NT, SMEM_BYTES, st>>>(*tm_k, *tm_v, a);
-    return cudaGetLastError();
+    if (a.nq_max <= 1) return launch_nq<1>(tm_k, tm_v, a, grid_x, st);
+    if (a.nq_max <= 2) return launch_nq<2>(tm_k, tm_v, a, grid_x, st);
+    if (a.nq_max <= 4) return launch_nq<4>(tm_k, tm_v, a, grid_x, st);
+    if (a.nq_max <= 8) return launch_nq<8>(tm_k, tm_v, a, grid_x, st);
+    return launch_nq<16>(tm_k, tm_v, a, grid_x, st);
 }
 
 }  // namespace kvk

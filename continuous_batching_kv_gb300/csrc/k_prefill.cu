@@ -167,9 +167,6 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     const int32_t warp = tid >> 5;
     const int32_t hk = blockIdx.y;
     const int32_t G = a.gqa;
-    const int32_t* c0 = a.p.cta_item0 + a.gx_dec + 1;
-    const int32_t i0 = c0[blockIdx.x];
-    const int32_t i1 = c0[blockIdx.x + 1];
     const uint32_t sbase = kvd::smem_u32(smem);
 
     // Launched as a programmatic dependent: library state is read before waiting
@@ -177,6 +174,9 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     // Q, the K/V cache and the outputs are touched only after the wait.
     if (!a.early_ok) kvd::pdl_wait();
     if (tid == 0) kvd::pdl_trigger();   // the split-K merge may be scheduled
+    const int32_t *c0 = a.p.cta_item0 + a.gx_dec + 1;
+    const int32_t i0 = c0[blockIdx.x];
+    const int32_t i1 = c0[blockIdx.x + 1];
     if ((sbase & 1023u) != 0) {
         if (tid == 0) kvd::report(a.err, kvd::DERR_BOUNDS);
         return;
@@ -715,7 +715,10 @@ __global__ void __launch_bounds__(256) k_merge_pf(const kvk::PrefillArgs a) {
     const int32_t b = a.u.n_dec_blocks + blockIdx.x;
     const int32_t hk = blockIdx.y;
     const int32_t nitems = a.p.blk_nitems[b];
-    if (nitems <= 1) return;
+    if (nitems <= 1) {
+        kvd::pdl_trigger();
+        return;
+    }
     const kvi::DevBlock blk = a.u.blocks[b];
     const int32_t n = (int32_t)blockIdx.z * (M / MERGE_SPLIT) + (int32_t)(threadIdx.x >> 4);
     const int32_t d0 = (int32_t)(threadIdx.x & 15) * 8;
@@ -727,6 +730,7 @@ __global__ void __launch_bounds__(256) k_merge_pf(const kvk::PrefillArgs a) {
     const int64_t istride = (int64_t)a.n_head_kv * M * PART_STRIDE;
     const float *pr = a.part + (((int64_t)first * a.n_head_kv + hk) * M + n) * PART_STRIDE;
     kvd::pdl_wait();
+    kvd::pdl_trigger();   // the next kernel (a K/V store) may be scheduled
     float mx = -INFINITY, L = 0.f;
     float acc[8];
 #pragma unroll

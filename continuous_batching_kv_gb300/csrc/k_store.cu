@@ -19,7 +19,11 @@ __global__ void __launch_bounds__(256) k_store(uint4 *__restrict__ kc, uint4 *__
                                                const kvi::DevRow *__restrict__ rows, int32_t n_tokens,
                                                int32_t chunks_per_row, int64_t n_cells,
                                                int32_t *err) {
-    kvd::pdl_trigger();   // the attention kernel that follows may start its set-up now
+    // Launched as a programmatic dependent of the kernel before it: wait for it
+    // before reading the rows (the caller may have just produced them) or
+    // writing the cache; then let the attention kernel that follows set up.
+    kvd::pdl_wait();
+    kvd::pdl_trigger();
     const int64_t total = (int64_t)n_tokens * chunks_per_row;
     for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
          t += (int64_t)gridDim.x * blockDim.x) {
@@ -59,8 +63,18 @@ cudaError_t launch_store(void *k_cache, void *v_cache, const void *k_cur, const 
     const int64_t total = (int64_t)n_tokens * cpr;
     int64_t blocks = (total + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
-    k_store<<<(unsigned)blocks, 256, 0, st>>>((uint4 *)k_cache, (uint4 *)v_cache, (const uint4 *)k_cur,
-                                              (const uint4 *)v_cur, rows, n_tokens, cpr, n_cells, err);
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_store, (uint4 *)k_cache, (uint4 *)v_cache, (const uint4 *)k_cur,
+                                       (const uint4 *)v_cur, rows, n_tokens, cpr, n_cells, err);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -79,6 +79,8 @@ struct DecodeArgs {
     int32_t n_head, n_head_kv, gqa;
     float scale_log2;       // log2(e) / sqrt(head_dim)
     int32_t *err;
+    int32_t nq_max;         // most query vectors in one decode block of this ubatch (1..DEC_QMAX)
+    int32_t early_ok;       // as in PrefillArgs
 };
 cudaError_t launch_decode(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const DecodeArgs &a,
                           int32_t grid_x, cudaStream_t st);
