@@ -180,6 +180,8 @@ class OursArm:
                             n_head=self.H, n_head_kv=self.Hk, head_dim=self.d,
                             seq_to_stream=prm.get("seq_to_stream"), k_layers=self.kc, v_layers=self.vc)
         self.stream = torch.cuda.current_stream(device)
+        self.decode_loop = DECODE_BOUND.get(cfg["id"], False)
+        self.step_no = -1
         self.gen = torch.Generator(device=device)
         self.gen.manual_seed(1234)
         self._setup()
@@ -208,6 +210,16 @@ class OursArm:
             for seqs in call["seq"]:
                 q = seqs[0]
                 self.base_pos_max[q] = kv.kv_seq_pos_max(self.c, q)
+        # decode iterations that fit in the free cells of the fullest stream
+        prm = self.cfg["params"]
+        kv_size = prm["n_ctx"] // prm["n_stream"]
+        per_stream = {}
+        for call in self.cfg["measured"]:
+            for seqs in call["seq"]:
+                st = (prm.get("seq_to_stream") or [i % prm["n_stream"] for i in range(prm["n_seq_max"])])[seqs[0]]
+                per_stream[st] = per_stream.get(st, 0) + 1
+        free = min(kv_size - kv.kv_stream_n_kv(self.c, st) for st in per_stream) if per_stream else 0
+        self.max_steps = max(0, free // max(per_stream.values()) - 1) if per_stream else 0
 
     def _prepare_inputs(self):
         """Per measured call: the marshalled batch, its ubatch shapes, and
@@ -228,7 +240,8 @@ class OursArm:
                      "v": [self._randn(n, self.Hk * self.d) for _ in range(self.L)],
                      "o": self.torch.empty((n, self.H, self.d), dtype=self.torch.float32, device=self.dev),
                      "pairs": int(row_visible_cells([call["pos"][r] for r in rows]).sum()),
-                     "bytes": self._kv_bytes(call, rows, n)}
+                     "bytes": self._kv_bytes(call, rows, n),
+                     "row_kv_bytes": len({call["seq"][r][0] for r in rows}) * 2 * self.Hk * self.d * 2}
                 ubs.append(t)
             kv.kv_split_free(s)
             # the batch is marshalled once (numpy arrays, ids as a flat list plus
@@ -257,8 +270,19 @@ class OursArm:
         return tot
 
     def reset(self):
-        """Return the cache to its post-setup state."""
+        """Before a step: return the cache to its post-setup state, or, for the
+        decode workloads, advance one token (each step is the next decode
+        iteration of the same sequences, as a serving loop runs; the cache is
+        rolled back only when it would run out of cells)."""
         kv = self.kv
+        if self.decode_loop:
+            self.step_no += 1
+            if self.step_no <= self.max_steps:
+                return
+            self.step_no = 0
+            for q, pmax in self.base_pos_max.items():
+                kv.kv_seq_rm(self.c, q, pmax + 1, -1)
+            return
         if not self.cfg["setup"]:
             kv.kv_seq_rm(self.c, -1, 0, -1)
         else:
@@ -275,8 +299,9 @@ class OursArm:
         kv, torch = self.kv, self.torch
         self.reset()
         last = []
+        off = max(0, self.step_no) if self.decode_loop else 0
         for ci, (call, ubs, marsh) in enumerate(self.calls):
-            s = kv.kv_split_ubatches(self.c, marsh[0], marsh[1])
+            s = kv.kv_split_ubatches(self.c, marsh[0] + off if off else marsh[0], marsh[1])
             assert kv.kv_prepare_cells(self.c, s) == 0
             for k, t in enumerate(ubs):
                 for layer in range(self.L):
@@ -287,7 +312,7 @@ class OursArm:
                         t["v"][layer].copy_(hv, non_blocking=True)
                     kv.kv_store(self.c, s, k, layer, t["k"][layer], t["v"][layer], self.stream)
                     if timers is not None and layer > 0:
-                        e0, e1 = timers.take(t["pairs"], t["bytes"])
+                        e0, e1 = timers.take(t["pairs"] + off * t["n"], t["bytes"] + off * t["row_kv_bytes"])
                         e0.record(self.stream)
                         kv.ubatch_attention(self.c, s, k, layer, t["q"][layer], t["o"], None, self.stream)
                         e1.record(self.stream)

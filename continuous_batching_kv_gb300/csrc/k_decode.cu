@@ -64,7 +64,8 @@ struct __align__(16) Aux {
     static constexpr int PQ = NQ < 4 ? 4 : NQ;  // padded for 16-byte loads
     Meta meta[S];
     float q[NQ][4][36];           // queries in fp32: q[n][dq][j] = Q[n][32 dq + j]
-    float p[NW][8][PQ];           // each warp's probabilities, cell-major
+    float p[NW][8][PQ];           // each warp's probabilities, cell-major (NQ > 4)
+    uint16_t ph[NW][8][4];        // ... as fp16 (NQ <= 4)
     float scr_m[4][NQ];           // tree merge: the writing warps' maxima,
     float scr_l[4][NQ];           //   row sums
     float scr_o[4][NQ][128];      //   and accumulators
@@ -81,6 +82,24 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// d0 += a.lo * b.lo and d1 += a.hi * b.hi: a and b hold two fp16 each, the
+// products are exact in fp32 and the sums are fp32 (one mixed-precision FMA each).
+__device__ __forceinline__ void fma2_h(uint32_t a, uint32_t b, float &d0, float &d1) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %0;\n\tfma.rn.f32.f16 %1, ah, bh, %1;\n\t}"
+        : "+f"(d0), "+f"(d1) : "r"(a), "r"(b));
+}
+
+// d[j] += p * v_j for the four fp16 v_j of two words (p fp16, sums fp32).
+__device__ __forceinline__ void fma4_h(uint16_t p, uint32_t v01, uint32_t v23, float (&d)[4]) {
+    asm("{\n\t.reg .b16 a0, a1, a2, a3;\n\t"
+        "mov.b32 {a0, a1}, %5;\n\tmov.b32 {a2, a3}, %6;\n\t"
+        "fma.rn.f32.f16 %0, %4, a0, %0;\n\tfma.rn.f32.f16 %1, %4, a1, %1;\n\t"
+        "fma.rn.f32.f16 %2, %4, a2, %2;\n\tfma.rn.f32.f16 %3, %4, a3, %3;\n\t}"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3]) : "h"(p), "r"(v01), "r"(v23));
 }
 
 __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, volatile int32_t *fail) {
@@ -226,8 +245,29 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 kvd::pdl_wait();
                 dep_done = true;
             }
-            // ---- Q (fp32) and the rows' positions ----
-            {
+            // NQ <= 4: my 16 of the 128 d of every query vector (d = 8e .. 8e + 7 and
+            // 64 + 8e .. 64 + 8e + 7), fp16, stay in registers for the whole item
+            constexpr bool RQ = NQ <= 4;
+            const int32_t g = lane >> 3, e = lane & 7;
+            uint32_t qh[NQ][8];
+            int32_t rp[NQ];
+            if constexpr (RQ) {
+#pragma unroll
+                for (int n = 0; n < NQ; ++n) {
+                    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+                    rp[n] = 0;
+                    if (n < nq) {
+                        const int32_t row = a.u.perm[b.row0 + n / G];
+                        const int32_t h = hk * G + (n % G);
+                        const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((int64_t)row * a.n_head + h) * 128);
+                        lo = src[e];
+                        hi = src[8 + e];
+                        rp[n] = a.u.rows[row].pos;
+                    }
+                    qh[n][0] = lo.x; qh[n][1] = lo.y; qh[n][2] = lo.z; qh[n][3] = lo.w;
+                    qh[n][4] = hi.x; qh[n][5] = hi.y; qh[n][6] = hi.z; qh[n][7] = hi.w;
+                }
+            } else {   // ---- NQ > 4: Q (fp32) and the rows' positions in shared memory ----
                 const int32_t n = tid >> 4, part = tid & 15;   // 8 values of query vector n
                 if (n < NQ) {
                     float v[8];
@@ -251,8 +291,8 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     *reinterpret_cast<float4 *>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
                 }
                 if (tid < NQ) x.rpos[tid] = tid < nq ? a.u.rows[a.u.perm[b.row0 + tid / G]].pos : 0;
+                if (!(ok = cons_sync(&x.cbar, cph, fail))) break;
             }
-            if (!(ok = cons_sync(&x.cbar, cph, fail))) break;
 
             float m[NQ], lp[NQ], acc[NQ][4];
 #pragma unroll
@@ -267,6 +307,78 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 if (!ok) break;
                 const uint8_t *sp = stages + (size_t)st * STAGE_BYTES;
                 const bool full = x.meta[st].full != 0;
+                if constexpr (RQ) {
+                // ---- scores: cells g and g + 4 of my warp's 8, my 16 d, all query vectors
+                //      (fp16 K times fp16 Q, fp32 sums; eight lanes per cell) ----
+                const int32_t c0 = warp * 8 + g, c1 = c0 + 4;
+                float sc[2][NQ];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int32_t cell = r ? c1 : c0;
+                    const uint4 k0 = *reinterpret_cast<const uint4 *>(sp + kvd::swz128(cell, e));
+                    const uint4 k1 = *reinterpret_cast<const uint4 *>(sp + BOX_BYTES + kvd::swz128(cell, e));
+                    const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+                    for (int n = 0; n < NQ; ++n) {
+                        float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) fma2_h(kw[j], qh[n][j], d0, d1);
+                        float v = d0 + d1;
+                        v += __shfl_xor_sync(0xffffffffu, v, 1);
+                        v += __shfl_xor_sync(0xffffffffu, v, 2);
+                        v += __shfl_xor_sync(0xffffffffu, v, 4);
+                        sc[r][n] = v;
+                    }
+                }
+                const bool h0 = full || x.meta[st].has[c0], h1 = full || x.meta[st].has[c1];
+                const int32_t p0 = full ? 0 : x.meta[st].cpos[c0], p1 = full ? 0 : x.meta[st].cpos[c1];
+                // ---- online softmax over my warp's 8 cells (warp-uniform decisions) ----
+#pragma unroll
+                for (int n = 0; n < NQ; ++n) {
+                    const bool v0 = h0 && n < nq && (full || !a.u.causal || p0 <= rp[n]);
+                    const bool v1 = h1 && n < nq && (full || !a.u.causal || p1 <= rp[n]);
+                    const float s0 = v0 ? sc[0][n] * a.scale_log2 : -INFINITY;
+                    const float s1 = v1 ? sc[1][n] * a.scale_log2 : -INFINITY;
+                    float t = fmaxf(s0, s1);
+                    t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 8));
+                    t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 16));
+                    const float mn = fmaxf(m[n], t);
+                    if (mn > m[n] + RESCALE_LOG2 || (m[n] == -INFINITY && mn != -INFINITY)) {
+                        const float al = ex2_approx(m[n] - mn);
+                        lp[n] *= al;
+                        acc[n][0] *= al;
+                        acc[n][1] *= al;
+                        acc[n][2] *= al;
+                        acc[n][3] *= al;
+                        m[n] = mn;
+                    }
+                    const bool live = m[n] != -INFINITY;
+                    const __half q0 = __float2half_rn(live ? ex2_approx(s0 - m[n]) : 0.f);
+                    const __half q1 = __float2half_rn(live ? ex2_approx(s1 - m[n]) : 0.f);
+                    if (e == 0) {   // the row sum counts P as the PV product sees it (fp16)
+                        lp[n] += __half2float(q0) + __half2float(q1);
+                        x.ph[warp][g][n] = __half_as_ushort(q0);
+                        x.ph[warp][g + 4][n] = __half_as_ushort(q1);
+                    }
+                }
+                __syncwarp();
+                // ---- O += P V over my warp's 8 cells; lane owns d = 4 lane .. 4 lane + 3 ----
+                {
+                    const uint8_t *vb = sp + 2 * BOX_BYTES + (lane >> 4) * BOX_BYTES;
+                    const uint32_t chunk = (uint32_t)(lane & 15) >> 1, inner = (uint32_t)(lane & 1) * 8u;
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const int32_t cell = warp * 8 + cc;
+                        if (!full && !x.meta[st].has[cell]) continue;   // warp-uniform
+                        const uint2 raw = *reinterpret_cast<const uint2 *>(vb + kvd::swz128(cell, chunk) + inner);
+                        const uint2 pw = *reinterpret_cast<const uint2 *>(&x.ph[warp][cc][0]);
+                        const uint16_t pq[4] = {(uint16_t)(pw.x & 0xffffu), (uint16_t)(pw.x >> 16),
+                                                (uint16_t)(pw.y & 0xffffu), (uint16_t)(pw.y >> 16)};
+#pragma unroll
+                        for (int n = 0; n < NQ; ++n) fma4_h(pq[n], raw.x, raw.y, acc[n]);
+                    }
+                }
+                } else {
                 // ---- scores: my cell, my 32 d, all query vectors ----
                 float s[NQ];
 #pragma unroll
@@ -361,6 +473,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                         }
                     }
                 }
+                }   // NQ > 4
                 __syncwarp();
                 if (lane == 0) kvd::mbar_arrive(&x.empty[st]);   // release the stage (K, V, metadata)
             }
