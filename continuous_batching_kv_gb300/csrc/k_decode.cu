@@ -301,13 +301,109 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 lp[n] = 0.f;
                 acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
             }
+            // NQ == 4: after the score reduction each lane holds one query vector,
+            // nl = (e >> 1) & 3, with its own running maximum and row-sum part
+            const int32_t nl = (e >> 1) & 3;
+            float m_l = -INFINITY, lp_l = 0.f;
+            int32_t rp_l = 0;
+            if constexpr (NQ == 4) {
+#pragma unroll
+                for (int n = 0; n < NQ; ++n)
+                    if (nl == n) rp_l = rp[n];
+            }
             for (int32_t li = w.t0; li < w.t1; ++li, ++k) {
                 const int32_t st = k % S;
                 ok = __all_sync(0xffffffffu, wait_or_fail(&x.full[st], (uint32_t)(k / S) & 1u, fail));
                 if (!ok) break;
                 const uint8_t *sp = stages + (size_t)st * STAGE_BYTES;
                 const bool full = x.meta[st].full != 0;
-                if constexpr (RQ) {
+                if constexpr (NQ == 4) {
+                // ---- scores: cells g and g + 4 of my warp's 8, my 16 d, the four query
+                //      vectors; the eight lanes of a cell then reduce-scatter the sums so
+                //      that lane e keeps query nl (4 shuffles instead of 12) ----
+                const int32_t c0 = warp * 8 + g, c1 = c0 + 4;
+                float scv[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int32_t cell = r ? c1 : c0;
+                    const uint4 k0 = *reinterpret_cast<const uint4 *>(sp + kvd::swz128(cell, e));
+                    const uint4 k1 = *reinterpret_cast<const uint4 *>(sp + BOX_BYTES + kvd::swz128(cell, e));
+                    const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+                    float dd[4];
+#pragma unroll
+                    for (int n = 0; n < 4; ++n) {
+                        float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) fma2_h(kw[j], qh[n][j], d0, d1);
+                        dd[n] = d0 + d1;
+                    }
+                    const bool up = (e & 4) != 0;       // lanes e >= 4 keep queries 2, 3
+                    float ka = up ? dd[2] : dd[0], kb = up ? dd[3] : dd[1];
+                    const float sa = up ? dd[0] : dd[2], sb = up ? dd[1] : dd[3];
+                    ka += __shfl_xor_sync(0xffffffffu, sa, 4);
+                    kb += __shfl_xor_sync(0xffffffffu, sb, 4);
+                    const bool up2 = (e & 2) != 0;      // then the second of the pair
+                    float kv = up2 ? kb : ka;
+                    kv += __shfl_xor_sync(0xffffffffu, up2 ? ka : kb, 2);
+                    kv += __shfl_xor_sync(0xffffffffu, kv, 1);
+                    scv[r] = kv;
+                }
+                const bool h0 = full || x.meta[st].has[c0], h1 = full || x.meta[st].has[c1];
+                const int32_t p0 = full ? 0 : x.meta[st].cpos[c0], p1 = full ? 0 : x.meta[st].cpos[c1];
+                const bool v0 = h0 && nl < nq && (full || !a.u.causal || p0 <= rp_l);
+                const bool v1 = h1 && nl < nq && (full || !a.u.causal || p1 <= rp_l);
+                const float s0 = v0 ? scv[0] * a.scale_log2 : -INFINITY;
+                const float s1 = v1 ? scv[1] * a.scale_log2 : -INFINITY;
+                // ---- online softmax of query nl over my warp's 8 cells ----
+                float t = fmaxf(s0, s1);
+                t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 8));
+                t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 16));
+                const float mn = fmaxf(m_l, t);
+                const bool grow = mn > m_l + RESCALE_LOG2 || (m_l == -INFINITY && mn != -INFINITY);
+                float al = 1.f;
+                if (grow) {
+                    al = ex2_approx(m_l - mn);
+                    m_l = mn;
+                    lp_l *= al;
+                }
+                if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+                    for (int n = 0; n < 4; ++n) {   // lane 2n holds query n
+                        const float an = __shfl_sync(0xffffffffu, al, 2 * n);
+                        acc[n][0] *= an;
+                        acc[n][1] *= an;
+                        acc[n][2] *= an;
+                        acc[n][3] *= an;
+                    }
+                }
+                {
+                    const bool live = m_l != -INFINITY;
+                    const __half q0 = __float2half_rn(live ? ex2_approx(s0 - m_l) : 0.f);
+                    const __half q1 = __float2half_rn(live ? ex2_approx(s1 - m_l) : 0.f);
+                    if ((e & 1) == 0) {   // the row sum counts P as the PV product sees it (fp16)
+                        lp_l += __half2float(q0) + __half2float(q1);
+                        x.ph[warp][g][nl] = __half_as_ushort(q0);
+                        x.ph[warp][g + 4][nl] = __half_as_ushort(q1);
+                    }
+                }
+                __syncwarp();
+                // ---- O += P V over my warp's 8 cells; lane owns d = 4 lane .. 4 lane + 3 ----
+                {
+                    const uint8_t *vb = sp + 2 * BOX_BYTES + (lane >> 4) * BOX_BYTES;
+                    const uint32_t chunk = (uint32_t)(lane & 15) >> 1, inner = (uint32_t)(lane & 1) * 8u;
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const int32_t cell = warp * 8 + cc;
+                        if (!full && !x.meta[st].has[cell]) continue;   // warp-uniform
+                        const uint2 raw = *reinterpret_cast<const uint2 *>(vb + kvd::swz128(cell, chunk) + inner);
+                        const uint2 pw = *reinterpret_cast<const uint2 *>(&x.ph[warp][cc][0]);
+                        fma4_h((uint16_t)(pw.x & 0xffffu), raw.x, raw.y, acc[0]);
+                        fma4_h((uint16_t)(pw.x >> 16), raw.x, raw.y, acc[1]);
+                        fma4_h((uint16_t)(pw.y & 0xffffu), raw.x, raw.y, acc[2]);
+                        fma4_h((uint16_t)(pw.y >> 16), raw.x, raw.y, acc[3]);
+                    }
+                }
+                } else if constexpr (RQ) {
                 // ---- scores: cells g and g + 4 of my warp's 8, my 16 d, all query vectors
                 //      (fp16 K times fp16 Q, fp32 sums; eight lanes per cell) ----
                 const int32_t c0 = warp * 8 + g, c1 = c0 + 4;
@@ -480,6 +576,13 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             if (!ok) break;
 
             // ---- the item's result: merge the 8 warps (three rounds) ----
+            if constexpr (NQ == 4) {   // back to one (m, l part) per query vector on every lane
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    m[n] = __shfl_sync(0xffffffffu, m_l, 2 * n);
+                    lp[n] = (nl == n && (e & 1) == 0) ? lp_l : 0.f;
+                }
+            }
             float l[NQ];
 #pragma unroll
             for (int n = 0; n < NQ; ++n) {
