@@ -6,28 +6,29 @@
 // not later) it is the same softmax(q K^T / sqrt(d) + mask) V as decode, but
 // now a dense contraction worth putting on the tensor cores.
 //
-// Design (sm_103a, one CTA of 320 threads per SM):
+// Design (sm_103a, one CTA of 352 threads per SM):
 //  * a block = up to 128 query vectors (rows sharing a stream and first
 //    sequence id, times the GQA group) = the 128 TMEM lanes of one MMA tile;
 //    a work item = one block, one KV head, a chunk of the block's list of
 //    visible 64-cell tiles, consumed two at a time (N = 128 cells);
-//  * warp 8 streams K and V tiles with TMA (128-byte swizzle) into separate
-//    2-slot K and V rings, with each pair's list entries, flags and per-cell
-//    visibility fetched ahead into a metadata ring; warp 9 allocates TMEM and
-//    one thread issues
+//  * warp 8 streams K tiles with TMA (128-byte swizzle) into a 2-slot ring,
+//    with each pair's list entries, flags and per-cell visibility fetched ahead
+//    into a metadata ring; warp 10 streams V tiles into a 3-slot ring; warp 9
+//    allocates TMEM and one thread issues
 //    tcgen05.mma: S = Q K^T (M 128, N 128, K 128) into one of two TMEM score
-//    buffers as soon as the softmax has read that buffer, and O += P V with P
-//    read from TMEM (double-buffered, fp16) and V MN-major from shared memory
-//    into a TMEM accumulator; tcgen05.commit signals the mbarriers;
-//  * warps 0-7 (two threads per TMEM lane = query vector, 64 columns each)
-//    read S with one tcgen05.ld as soon as it lands (TMEM reads stall behind
-//    running MMAs), apply the mask per cell on tiles that are not fully
-//    visible, run the online softmax in base 2 (a quarter of the exponentials
-//    on the FMA pipe), write P (fp16, two cells per 32-bit column) into the
-//    TMEM P buffer of the pair's parity, and rescale O in TMEM only when the
-//    running maximum grew by more
-//    than 2^8 (otherwise the stale maximum is kept; the final normalisation
-//    uses the same one);
+//    buffers once the PV that read the P held there has completed, and
+//    O_h += P_h V_h for the two cell halves h, P_h read from TMEM (fp16, written
+//    over S) and V MN-major from shared memory; tcgen05.commit signals the
+//    mbarriers;
+//  * warps 0-7: thread (n, h) owns cells 64h .. 64h + 63 of query vector n
+//    (TMEM lane n) with its own running maximum, row sum and accumulator O_h;
+//    it reads its 64 columns of S with one tcgen05.ld as soon as they land,
+//    applies the mask per cell on tiles that are not fully visible, runs the
+//    online softmax in base 2 (a quarter of the exponentials on the FMA pipe),
+//    writes P (fp16, two cells per 32-bit column) over the S it read, and
+//    rescales O_h in TMEM only when its running maximum grew by more than 2^8
+//    (otherwise the stale maximum is kept; the final normalisation uses the
+//    same one); the two halves of a row combine their (m, l, O) once per item;
 //  * cells nobody in the block may see get their V rows zeroed in shared
 //    memory before the PV product (P is 0 there, but 0 * NaN would not be);
 //  * a block split over several CTAs leaves one partial (m, l, O) per piece,
@@ -43,30 +44,39 @@ namespace {
 using kvi::TILE;
 
 constexpr int NSM = 256;                 // softmax threads: two per TMEM lane
-constexpr int NT = NSM + 64;             // + producer warp + MMA warp
+constexpr int NT = NSM + 96;             // + K producer, MMA and V producer warps
 constexpr int M = 128;
 constexpr int HALF = 128 * 128;          // [128 rows][64 fp16], 128-byte rows
 constexpr int TILEB = 2 * HALF;          // 32 KiB
 constexpr int BOX = 64 * 128;            // one TMA box: 64 rows x 64 fp16
-constexpr int STAGES = 2;
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILEB;
-constexpr int OFF_V = OFF_K + STAGES * TILEB;
-constexpr int OFF_AUX = OFF_V + STAGES * TILEB;
+constexpr int KSTAGES = 3;             // K ring: K of pair g + 3 loads once S of g has read K of g
+constexpr int VSTAGES = 3;             // V ring: V of pair g + 3 loads once PV of g is done
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + KSTAGES * TILEB;
+constexpr int OFF_AUX = OFF_V + VSTAGES * TILEB;
 constexpr int PART_STRIDE = 132;
-constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128), S1 [128,256) (P written over S), O_0 [256,384), O_1 [384,512)
-constexpr uint32_t COL_O = 256;          // O_h: accumulator of the cells 64h .. 64h + 63 of each pair tile
+constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128), S1 [128,256) (P written over S), O [256,384), Q [384,448)
+constexpr uint32_t COL_O = 256;          // O: fp32 accumulator, d = 0 .. 127
+constexpr uint32_t COL_Q = 384;          // Q: fp16, two d per column (the A operand of S = Q K^T)
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr unsigned POLL_NS = 32;         // back-off of the polling producer / MMA loops
 
 constexpr uint32_t IDESC_S = tc::idesc_f16(128, 128, 0, 0);
 constexpr uint32_t IDESC_PV = tc::idesc_f16(128, 128, 0, 1);
 
-// Metadata ring.  Pair g's slot is rewritten by the K load of pair g + 4, which
-// needs S of g + 2, which waits for the PV of the pair before it in its score
-// buffer (g or g + 1) to complete: by then the softmax is done with pair g and
-// the V load of g (which reads the slot) was issued.
-constexpr int MSLOTS = 4;
+// Metadata ring.  Pair g's slot is rewritten by the K load of pair g + MSLOTS,
+// which needs S of g + MSLOTS - KSTAGES to be done, which was issued only after
+// the PV of the pair before it in its score buffer (g + MSLOTS - KSTAGES - 2 or
+// later) was issued, i.e. after the softmax finished that pair: with MSLOTS >=
+// KSTAGES + 2 the softmax is done with pair g, and the V load of g (which reads
+// the slot) went out before that PV.
+constexpr int MSLOTS = 8;
+static_assert(MSLOTS >= KSTAGES + 2, "metadata ring too short for the K ring");
+// Lane tables, one per work item: the K load of an item's first pair g rewrites
+// the slot of the item ISLOTS back; it needs S of g - KSTAGES done, whose item
+// (at most KSTAGES back) had its Q, hence its lane table, taken already.
+constexpr int ISLOTS = 4;
+static_assert(ISLOTS > KSTAGES, "lane-table ring too short for the K ring");
 
 struct Meta {                 // per pair tile: what the producer learned about it
     int32_t full;
@@ -83,17 +93,18 @@ struct ItemSlot {             // per work item: the query vector behind each TME
 };
 
 struct __align__(16) Aux {
-    uint64_t k_full[STAGES], v_full[STAGES], k_empty[STAGES], v_empty[STAGES];
+    uint64_t k_full[KSTAGES], k_empty[KSTAGES], v_full[VSTAGES], v_empty[VSTAGES];
     uint64_t meta_full[MSLOTS];
     uint64_t s_full[2], p_full[2], pv_done[2], q_full, spare;   // p_full, pv_done [g & 1]: pair g
-    uint64_t lbar;            // the halves' (m, l) exchange at each item's end, all 256 threads
+    uint64_t lbar;            // the halves' row-sum exchange at each item's end, all 256 threads
+    uint64_t pbar[4];         // per lane quarter: the two warps of a row exchange maxima per pair
     uint32_t tmem_base;
     int32_t fail;
     int32_t flag;
     int32_t pad;
     Meta meta[MSLOTS];
-    ItemSlot islot[2];
-    float mex[2][2][M];       // [item parity][cell half][row]: running maxima
+    ItemSlot islot[ISLOTS];
+    float red[2][2][M];       // [pair parity][cell half][row]: partial row maxima
     float lex[2][2][M];       // [item parity][cell half][row]: row sums
 };
 
@@ -136,6 +147,31 @@ __device__ __forceinline__ float ex2_poly(float x) {
     const float f = x - nf;
     const float p = fmaf(f, fmaf(f, fmaf(f, C3, C2), C1), 1.0f);
     return __uint_as_float(__float_as_uint(p) + (__float_as_uint(t) << 23));
+}
+
+// Packed fp32 pairs (one 64-bit register) for the two-wide FMA and add.
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 // True while no wait has given up, agreed by all 32 lanes of the warp (so a
@@ -184,10 +220,12 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     if (tid == 0) {
         kvd::prefetch_tmap(&tm_k);
         kvd::prefetch_tmap(&tm_v);
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < KSTAGES; ++s) {
             kvd::mbar_init(&x.k_full[s], 1);
-            kvd::mbar_init(&x.v_full[s], 1);
             kvd::mbar_init(&x.k_empty[s], 1);
+        }
+        for (int s = 0; s < VSTAGES; ++s) {
+            kvd::mbar_init(&x.v_full[s], 1);
             kvd::mbar_init(&x.v_empty[s], 1);
         }
         for (int s = 0; s < MSLOTS; ++s) kvd::mbar_init(&x.meta_full[s], 32);
@@ -200,6 +238,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         kvd::mbar_init(&x.q_full, NSM);
         kvd::mbar_init(&x.spare, 1);
         kvd::mbar_init(&x.lbar, NSM);
+        for (int q = 0; q < 4; ++q) kvd::mbar_init(&x.pbar[q], 64);
         x.fail = 0;
         kvd::fence_mbar_init();
     }
@@ -213,17 +252,16 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     const uint32_t tmem = x.tmem_base;
 
     if (warp == 8) {
-        // ===================== producer (whole warp) =====================
-        // K and V tiles live in separate 2-slot rings: K of pair g + 2 loads as soon
-        // as S of pair g has consumed K of g; V of g + 2 as soon as PV of g is done.
-        // Two cursors walk the CTA's pair sequence; whichever load may go is issued
-        // (decisions by lane 0, broadcast), nothing waits on one while the other is
-        // ready.  The K load also publishes the pair's metadata (and, for an item's
-        // first pair, its lane table) through meta_full.
+        // ===================== K producer (whole warp) =====================
+        // K of pair g + 2 loads as soon as S of pair g has read K of g.  Each pair's
+        // list entries, flags and per-cell visibility (and, for an item's first
+        // pair, its lane table) are fetched while the K slot is still busy and
+        // published through meta_full before the K copy is issued.  V has its own
+        // warp: these dependent global reads never hold up a V copy.
         const int32_t lane = tid & 31;
         int32_t total = 0;
         for (int32_t wi = i0; wi < i1; ++wi) total += item_info(a, wi).pairs;
-        int32_t kc = 0, vc = 0, nonempty = 0;
+        int32_t kc = 0, nonempty = 0;
         int32_t kwi = i0, kj = 0;              // K cursor: item and pair within it
         ItemInfo kit{};
         kvi::DevBlock kb{};
@@ -233,10 +271,10 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         bool mhas[4] = {false, false, false, false}, many[4] = {false, false, false, false};
         int32_t mpos[4] = {0, 0, 0, 0}, lrow[4] = {-1, -1, -1, -1}, lpos[4] = {0, 0, 0, 0};
         long long t_last = clock64();
-        while (vc < total) {
+        while (kc < total) {
             if (!warp_ok(fail)) break;
             bool prog = false;
-            if (kc < total) {
+            {
                 if (!have_k) {
                     // the next K load's global reads, done before its slot is free
                     while (true) {
@@ -290,17 +328,16 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     }
                     have_k = true;
                 }
-                const int32_t st = kc % STAGES;
-                bool ready = kc < STAGES ||
-                             kvd::mbar_test_wait(&x.k_empty[st], (uint32_t)((kc / STAGES) - 1) & 1u);
+                const int32_t st = kc % KSTAGES;
+                bool ready = kc < KSTAGES ||
+                             kvd::mbar_test_wait(&x.k_empty[st], (uint32_t)((kc / KSTAGES) - 1) & 1u);
                 ready = __shfl_sync(0xffffffffu, ready, 0);
                 if (ready) {
                     Meta &mt = x.meta[kc % MSLOTS];
                     if (kj == 0) {
-                        // the item's lane table; its previous reader (two non-empty items
-                        // back) read it before any of its S products, and this K slot
-                        // was just freed by such an S product
-                        ItemSlot &is = x.islot[nonempty & 1];
+                        // the item's lane table (see ISLOTS: its previous reader, ISLOTS
+                        // non-empty items back, has taken it)
+                        ItemSlot &is = x.islot[nonempty % ISLOTS];
                         for (int r = 0; r < 4; ++r) {
                             is.row[lane + 32 * r] = lrow[r];
                             is.rpos[lane + 32 * r] = lpos[r];
@@ -343,28 +380,6 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     prog = true;
                 }
             }
-            if (vc < kc) {
-                const int32_t st = vc % STAGES;
-                bool ready = vc < STAGES ||
-                             kvd::mbar_test_wait(&x.v_empty[st], (uint32_t)((vc / STAGES) - 1) & 1u);
-                ready = __shfl_sync(0xffffffffu, ready, 0);
-                if (ready) {
-                    if (lane == 0) {
-                        const Meta &mt = x.meta[vc % MSLOTS];   // still intact (see MSLOTS)
-                        uint8_t *vs = smem + OFF_V + st * TILEB;
-                        const int32_t xk = hk * 128;
-                        kvd::fence_proxy_async_smem();
-                        kvd::mbar_arrive_expect_tx(&x.v_full[st], TILEB);
-                        for (int h = 0; h < 2; ++h) {
-                            kvd::tma_load_2d(vs + h * BOX, &tm_v, xk, mt.ys[h], &x.v_full[st]);
-                            kvd::tma_load_2d(vs + HALF + h * BOX, &tm_v, xk + 64, mt.ys[h], &x.v_full[st]);
-                        }
-                    }
-                    __syncwarp();
-                    ++vc;
-                    prog = true;
-                }
-            }
             if (prog) {
                 t_last = clock64();
             } else if (__shfl_sync(0xffffffffu, clock64() - t_last > kvd::WAIT_LIMIT_CYCLES ? 1 : 0, 0)) {
@@ -376,10 +391,41 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         }
         if (*fail && lane == 0) {
             // let loads already issued land before the CTA exits
-            for (int32_t q = kc > STAGES ? kc - STAGES : 0; q < kc; ++q)
-                (void)kvd::mbar_wait_bounded(&x.k_full[q % STAGES], (uint32_t)(q / STAGES) & 1u);
-            for (int32_t q = vc > STAGES ? vc - STAGES : 0; q < vc; ++q)
-                (void)kvd::mbar_wait_bounded(&x.v_full[q % STAGES], (uint32_t)(q / STAGES) & 1u);
+            for (int32_t q = kc > KSTAGES ? kc - KSTAGES : 0; q < kc; ++q)
+                (void)kvd::mbar_wait_bounded(&x.k_full[q % KSTAGES], (uint32_t)(q / KSTAGES) & 1u);
+        }
+    } else if (warp == 10) {
+        // ===================== V producer (whole warp) =====================
+        // V of pair g + 3 loads as soon as PV of g is done; the tile coordinates come
+        // from the pair's metadata, published by the K producer before its K copy.
+        const int32_t lane = tid & 31;
+        int32_t total = 0;
+        for (int32_t wi = i0; wi < i1; ++wi) total += item_info(a, wi).pairs;
+        int32_t vc = 0;
+        for (; vc < total; ++vc) {
+            const int32_t st = vc % VSTAGES;
+            bool ok = __all_sync(0xffffffffu, wait_or_fail(&x.meta_full[vc % MSLOTS], (uint32_t)(vc / MSLOTS) & 1u, fail));
+            if (ok && vc >= VSTAGES)
+                ok = __all_sync(0xffffffffu,
+                                wait_or_fail(&x.v_empty[st], (uint32_t)((vc / VSTAGES) - 1) & 1u, fail));
+            if (!ok) break;
+            if (vc == 0) kvd::pdl_wait();   // the K/V cache rows of this ubatch are written
+            if (lane == 0) {
+                const Meta &mt = x.meta[vc % MSLOTS];   // still intact (see MSLOTS)
+                uint8_t *vs = smem + OFF_V + st * TILEB;
+                const int32_t xk = hk * 128;
+                kvd::fence_proxy_async_smem();
+                kvd::mbar_arrive_expect_tx(&x.v_full[st], TILEB);
+                for (int h = 0; h < 2; ++h) {
+                    kvd::tma_load_2d(vs + h * BOX, &tm_v, xk, mt.ys[h], &x.v_full[st]);
+                    kvd::tma_load_2d(vs + HALF + h * BOX, &tm_v, xk + 64, mt.ys[h], &x.v_full[st]);
+                }
+            }
+            __syncwarp();
+        }
+        if (*fail && lane == 0) {
+            for (int32_t q = vc > VSTAGES ? vc - VSTAGES : 0; q < vc; ++q)
+                (void)kvd::mbar_wait_bounded(&x.v_full[q % VSTAGES], (uint32_t)(q / VSTAGES) & 1u);
         }
     } else if (warp == 9) {
         // ===================== MMA issuer =====================
@@ -387,18 +433,17 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             int32_t gidx = 0;                  // global pair-tile counter (stage ring)
             int32_t last_pair[2] = {-1, -1};   // global pair whose S (then P) last filled each score buffer
             uint32_t n_q = 0;
-            const uint32_t q_addr = sbase + OFF_Q;
             auto issue_s = [&](int32_t gi, int32_t buf) {
-                const uint32_t k_addr = sbase + OFF_K + (gi % STAGES) * TILEB;
+                const uint32_t k_addr = sbase + OFF_K + (gi % KSTAGES) * TILEB;
                 const uint32_t d = tmem + (uint32_t)buf * 128u;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 2) * HALF + (uint32_t)(kk & 3) * 32u;
-                    tc::mma_ss(d, tc::sdesc_sw128(q_addr + off, 16, 1024), tc::sdesc_sw128(k_addr + off, 16, 1024),
+                    tc::mma_ts(d, tmem + COL_Q + 8u * (uint32_t)kk, tc::sdesc_sw128(k_addr + off, 16, 1024),
                                IDESC_S, kk > 0 ? 1u : 0u);
                 }
                 tc::commit(&x.s_full[buf]);
-                tc::commit(&x.k_empty[gi % STAGES]);   // this K tile is consumed
+                tc::commit(&x.k_empty[gi % KSTAGES]);   // this K tile is consumed
             };
             // Per item, a non-blocking scheduler: PV of the oldest ready P first, then S
             // of the next pair once its K tile has landed and the PV that read the P
@@ -419,24 +464,21 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     // lapped: the softmax may finish two pairs before this thread looks)
                     const int32_t gp = gidx + pv_done;
                     if (pv_done < s_done && kvd::mbar_test_wait(&x.p_full[gp & 1], (uint32_t)(gp >> 1) & 1u)) {
-                        ok = wait_or_fail(&x.v_full[gp % STAGES], (uint32_t)(gp / STAGES) & 1u, fail);
+                        ok = wait_or_fail(&x.v_full[gp % VSTAGES], (uint32_t)(gp / VSTAGES) & 1u, fail);
                         if (!ok) break;
                         tc::fence_after();
-                        const uint32_t v_addr = sbase + OFF_V + (gp % STAGES) * TILEB;
+                        const uint32_t v_addr = sbase + OFF_V + (gp % VSTAGES) * TILEB;
                         const uint32_t p_tmem = tmem + 128u * (uint32_t)(pv_done & 1);
-                        // O_h += P_h V_h over cells 64h .. 64h + 63 (P_h: 32 TMEM columns at
-                        // 64h of the score buffer, 8 columns per K step of 16 cells)
+                        // O += P V over the 128 cells: P of cells 16kk .. 16kk + 15 is 8 TMEM
+                        // columns at 64 (kk / 4) + 8 (kk % 4) of the score buffer
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                tc::mma_ts(tmem + COL_O + 128u * (uint32_t)hh, p_tmem + 64u * (uint32_t)hh + 8u * (uint32_t)kk,
-                                           tc::sdesc_sw128(v_addr + (uint32_t)(4 * hh + kk) * 2048u, HALF, 1024), IDESC_PV,
-                                           (pv_done > 0 || kk > 0) ? 1u : 0u);
-                            }
+                        for (int kk = 0; kk < 8; ++kk) {
+                            tc::mma_ts(tmem + COL_O, p_tmem + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3),
+                                       tc::sdesc_sw128(v_addr + (uint32_t)kk * 2048u, HALF, 1024), IDESC_PV,
+                                       (pv_done > 0 || kk > 0) ? 1u : 0u);
                         }
                         tc::commit(&x.pv_done[gp & 1]);
-                        tc::commit(&x.v_empty[gp % STAGES]);
+                        tc::commit(&x.v_empty[gp % VSTAGES]);
                         ++pv_done;
                         progressed = true;
                     }
@@ -444,10 +486,11 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         const int32_t gi = gidx + s_done;
                         const int32_t buf = s_done & 1;
                         const int32_t lp = last_pair[buf];
-                        // PVs complete in order and S of lp waited for the PV before it, so
-                        // pv_done[lp & 1] is at most one phase behind: the parity test is exact
-                        if (kvd::mbar_test_wait(&x.k_full[gi % STAGES], (uint32_t)(gi / STAGES) & 1u) &&
-                            (lp < 0 || kvd::mbar_test_wait(&x.pv_done[lp & 1], (uint32_t)(lp >> 1) & 1u))) {
+                        // the S buffer holds the P that PV of pair lp reads: S may follow once
+                        // that PV is issued (the tensor core runs one thread's MMAs in issue
+                        // order, so the PV reads P before this S overwrites it)
+                        if (kvd::mbar_test_wait(&x.k_full[gi % KSTAGES], (uint32_t)(gi / KSTAGES) & 1u) &&
+                            lp < gidx + pv_done) {
                             tc::fence_after();
                             issue_s(gi, buf);
                             last_pair[buf] = gi;
@@ -474,25 +517,23 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         }
     } else {
         // ============ softmax / correction / epilogue (warps 0-7, two threads per row) ============
-        // Warps w and w + 4 share TMEM lane quarter w.  Thread (n, ch) owns cells
-        // 64ch .. 64ch + 63 of every pair tile of row n, with its own running maximum,
-        // row sum and accumulator O_ch (all 128 d), so the two halves of a row never
-        // wait for each other inside an item; their (m, l, O) are combined once, at
-        // the item's end.
+        // Warps w and w + 4 share TMEM lane quarter w: thread (n, ch) owns cells
+        // 64ch .. 64ch + 63 of every pair tile of row n and d = 64ch .. 64ch + 63 of
+        // O.  The two threads of a row exchange their maxima once per pair through
+        // an mbarrier of their two warps (arrive, then a bounded wait, never bar.sync:
+        // if a wait elsewhere gives up, the partner times out instead of hanging).
         const int32_t n = tid & 127;           // TMEM lane = query vector
-        const int32_t ch = tid >> 7;           // cell half
+        const int32_t ch = tid >> 7;           // cell half, and d half of O
         const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t s_mine = tmem + lane_q + (uint32_t)(64 * ch);   // + 128 * score buffer
-        const uint32_t o_mine = tmem + lane_q + COL_O + 128u * (uint32_t)ch;
+        const uint32_t o_mine = tmem + lane_q + COL_O + (uint32_t)(64 * ch);
+        uint64_t *pbar = &x.pbar[warp & 3];
         uint32_t n_s[2] = {0, 0};
-        uint32_t n_l = 0;
+        uint32_t n_l = 0, n_p = 0;
         int32_t k = 0;                         // pair tiles consumed (stage ring position)
         int32_t nonempty = 0;
         bool ok = true;
         bool dep_done = false;                 // waited for the previous kernel of the stream
-        // The two halves meet through an mbarrier (arrive, then a bounded wait), never
-        // bar.sync: if a wait elsewhere gives up, the others time out instead of waiting
-        // for threads that left.
         for (int32_t wi = i0; wi < i1 && ok && warp_ok(fail); ++wi) {
             const ItemInfo it = item_info(a, wi);
             int32_t row = -1, rpos = 0;
@@ -504,7 +545,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 // the first pair's metadata also publishes this item's lane table
                 ok = __all_sync(0xffffffffu, wait_or_fail(&x.meta_full[k % MSLOTS], (uint32_t)(k / MSLOTS) & 1u, fail));
                 if (!ok) break;
-                const ItemSlot &is = x.islot[nonempty & 1];
+                const ItemSlot &is = x.islot[nonempty % ISLOTS];
                 ++nonempty;
                 row = is.row[n];
                 rpos = is.rpos[n];
@@ -515,23 +556,29 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             }
             const bool live = row >= 0;
             const int32_t h = hk * G + (n % G);
-            float m_run = -INFINITY, l_run = 0.f;   // this half's running maximum and row sum
+            float m_run = -INFINITY, l_run = 0.f;   // the row's running maximum, this half's row sum
             if (it.pairs > 0) {
-            // ---- Q tile: row n, d-half ch, 128-byte swizzle ----
+            // ---- Q into TMEM (the A operand of S = Q K^T): row n, d-half ch, fp16,
+            //      two values per 32-bit column ----
             {
-                uint8_t *qs = smem + OFF_Q + ch * HALF;
                 const uint4 *src =
                     reinterpret_cast<const uint4 *>(a.q + ((int64_t)(live ? row : 0) * a.n_head + h) * 128 + 64 * ch);
-                uint4 qv[8];
+                uint32_t qw[32];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) qv[c] = live ? src[c] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qs + kvd::swz128(n, c)) = qv[c];
-                kvd::fence_proxy_async_smem();
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = live ? src[c] : make_uint4(0, 0, 0, 0);
+                    qw[4 * c + 0] = v.x;
+                    qw[4 * c + 1] = v.y;
+                    qw[4 * c + 2] = v.z;
+                    qw[4 * c + 3] = v.w;
+                }
+                tc::st32(tmem + lane_q + COL_Q + 32u * (uint32_t)ch, qw);
+                tc::wait_st();
+                tc::fence_before();
                 kvd::mbar_arrive(&x.q_full);
             }
             for (int32_t j = 0; j < it.pairs; ++j, ++k) {
-                const int32_t st = k % STAGES;
+                const int32_t st = k % VSTAGES;
                 ok = __all_sync(0xffffffffu, wait_or_fail(&x.meta_full[k % MSLOTS], (uint32_t)(k / MSLOTS) & 1u, fail));
                 if (!ok) break;
                 const Meta &mt = x.meta[k % MSLOTS];
@@ -558,8 +605,15 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     }
                 }
 #pragma unroll
-                for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sb[c]));
-                const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+                for (int c = 0; c < 64; c += 2)
+                    mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(sb[c]), __uint_as_float(sb[c + 1]));
+                // ---- the row maximum over both halves (partner: the same lane of warp w ^ 4) ----
+                x.red[j & 1][ch][n] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                kvd::mbar_arrive(pbar);
+                ok = __all_sync(0xffffffffu, wait_or_fail(pbar, n_p & 1u, fail));
+                ++n_p;
+                if (!ok) break;
+                const float tmax = fmaxf(x.red[j & 1][0][n], x.red[j & 1][1][n]) * a.scale_log2;
                 const float m_new = fmaxf(m_run, tmax);
                 const bool grow = m_new > m_run + RESCALE_LOG2 || (m_run == -INFINITY && m_new != -INFINITY);
                 float alpha = 1.f;
@@ -572,36 +626,38 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 //      cells are 32 columns (two fp16 per column, lower cell in the low
                 //      half); one exponential in four on the FMA pipe ----
                 {
-                    const bool any = m_run != -INFINITY;   // false for lanes past the block
-                    const float nm = -m_run;
-                    const float sc = a.scale_log2;
-                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                    // no maximum yet (nothing visible so far, or a lane past the block):
+                    // subtract +inf so that every exponent is -inf and P is 0
+                    const float nm = m_run != -INFINITY ? -m_run : -INFINITY;
+                    const uint64_t sc2 = pk2(a.scale_log2, a.scale_log2), nm2 = pk2(nm, nm);
+                    uint64_t ls2[2] = {pk2(0.f, 0.f), pk2(0.f, 0.f)};
                     uint32_t pw[32];
 #pragma unroll
                     for (int c2 = 0; c2 < 32; ++c2) {
                         const int c = 2 * c2;
-                        const float x0 = fmaf(__uint_as_float(sb[c]), sc, nm);
-                        const float x1 = fmaf(__uint_as_float(sb[c + 1]), sc, nm);
-                        float p0 = ex2_approx(x0);
-                        float p1 = (c2 & 1) ? ex2_poly(x1) : ex2_approx(x1);
-                        p0 = any ? p0 : 0.f;
-                        p1 = any ? p1 : 0.f;
-                        ls[c2 & 3] += p0 + p1;
+                        float x0, x1;
+                        upk2(ffma2(pk2(__uint_as_float(sb[c]), __uint_as_float(sb[c + 1])), sc2, nm2), x0, x1);
+                        const float p0 = ex2_approx(x0);
+                        const float p1 = (c2 & 1) ? ex2_poly(x1) : ex2_approx(x1);
+                        ls2[c2 & 1] = fadd2(ls2[c2 & 1], pk2(p0, p1));
                         __half2 hv = __floats2half2_rn(p0, p1);
                         pw[c2] = *reinterpret_cast<uint32_t *>(&hv);
                     }
-                    l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                    float la, lb, lc, ld;
+                    upk2(ls2[0], la, lb);
+                    upk2(ls2[1], lc, ld);
+                    l_run += (la + lb) + (lc + ld);
                     tc::st32(s_addr, pw);
                 }
-                // ---- O_ch *= alpha where this half's running maximum moved (rare);
-                //      O_ch is stable once PV of pair k - 1 finished ----
+                // ---- O *= alpha where the row's running maximum moved (rare), my 64
+                //      columns; O is stable once PV of pair k - 1 finished ----
                 if (j > 0 && __any_sync(0xffffffffu, grow)) {
                     ok = __all_sync(0xffffffffu,
                                     wait_or_fail(&x.pv_done[(k - 1) & 1], (uint32_t)((k - 1) >> 1) & 1u, fail));
                     if (!ok) break;
                     tc::fence_after();
 #pragma unroll 1
-                    for (int q2 = 0; q2 < 4; ++q2) {
+                    for (int q2 = 0; q2 < 2; ++q2) {
                         uint32_t r[32];
                         const uint32_t ta = o_mine + (uint32_t)q2 * 32u;
                         tc::ld32(ta, r);
@@ -613,7 +669,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 if (!full) {
                     // V rows of cells nobody in the block sees: zero (P is 0 there; V may
                     // be garbage); thread (n, ch) clears d-half ch of cell n
-                    ok = __all_sync(0xffffffffu, wait_or_fail(&x.v_full[st], (uint32_t)(k / STAGES) & 1u, fail));
+                    ok = __all_sync(0xffffffffu, wait_or_fail(&x.v_full[st], (uint32_t)(k / VSTAGES) & 1u, fail));
                     if (!ok) break;
                     if (!mt.anyvis[n]) {
                         uint8_t *vs = smem + OFF_V + st * TILEB + ch * HALF + n * 128;
@@ -633,20 +689,13 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             if (!ok) break;
             tc::fence_after();
             }   // it.pairs > 0
-            // ---- combine the halves: O = (2^(m0-M) O_0 + 2^(m1-M) O_1) / (2^(m0-M) l0 + 2^(m1-M) l1);
-            //      thread (n, ch) produces d = 64ch .. 64ch + 63 (exchange double-buffered by item parity) ----
-            x.mex[n_l & 1][ch][n] = m_run;
+            // ---- the row sum over both halves (double-buffered by item parity) ----
             x.lex[n_l & 1][ch][n] = l_run;
             kvd::mbar_arrive(&x.lbar);
             ok = __all_sync(0xffffffffu, wait_or_fail(&x.lbar, n_l & 1u, fail));
             if (!ok) break;
-            const float m0 = x.mex[n_l & 1][0][n], m1 = x.mex[n_l & 1][1][n];
-            const float l0 = x.lex[n_l & 1][0][n], l1 = x.lex[n_l & 1][1][n];
+            const float l_tot = x.lex[n_l & 1][0][n] + x.lex[n_l & 1][1][n];
             ++n_l;
-            const float mm = fmaxf(m0, m1);
-            const float s0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - mm);
-            const float s1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mm);
-            const float l_tot = s0 * l0 + s1 * l1;
             float *dst = nullptr;
             float sc = 1.f;
             if (it.nitems == 1) {
@@ -657,31 +706,28 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 // prefill items); k_merge_pf combines the partials after the kernel
                 float *pp = a.part + (((int64_t)wi * a.n_head_kv + hk) * M + n) * PART_STRIDE;
                 if (ch == 0) {
-                    pp[0] = mm;
+                    pp[0] = m_run;
                     pp[1] = l_tot;
                 }
                 dst = pp + 4 + 64 * ch;
             }
-            const float f0 = s0 * sc, f1 = s1 * sc;
 #pragma unroll 1
             for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t r0[32], r1[32];
-                if (it.pairs > 0) {              // item-uniform: the TMEM reads stay warp collective
-                    const uint32_t ta = tmem + lane_q + COL_O + (uint32_t)(64 * ch + 32 * q2);
-                    tc::ld32(ta, r0);
-                    tc::ld32(ta + 128u, r1);
+                uint32_t r[32];
+                if (it.pairs > 0) {              // item-uniform: the TMEM read stays warp collective
+                    tc::ld32(o_mine + 32u * (uint32_t)q2, r);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) r0[c] = r1[c] = 0u;
+                    for (int c = 0; c < 32; ++c) r[c] = 0u;
                 }
                 if (dst) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 4) {
                         float4 v;
-                        v.x = __uint_as_float(r0[c + 0]) * f0 + __uint_as_float(r1[c + 0]) * f1;
-                        v.y = __uint_as_float(r0[c + 1]) * f0 + __uint_as_float(r1[c + 1]) * f1;
-                        v.z = __uint_as_float(r0[c + 2]) * f0 + __uint_as_float(r1[c + 2]) * f1;
-                        v.w = __uint_as_float(r0[c + 3]) * f0 + __uint_as_float(r1[c + 3]) * f1;
+                        v.x = __uint_as_float(r[c + 0]) * sc;
+                        v.y = __uint_as_float(r[c + 1]) * sc;
+                        v.z = __uint_as_float(r[c + 2]) * sc;
+                        v.w = __uint_as_float(r[c + 3]) * sc;
                         *reinterpret_cast<float4 *>(dst + 32 * q2 + c) = v;
                     }
                 }
