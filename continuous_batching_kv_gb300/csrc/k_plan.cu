@@ -116,6 +116,10 @@ __global__ void __launch_bounds__(256) k_plan_compact(kvk::UbView u, kvk::Plan p
 // get no item.
 __device__ __forceinline__ int64_t slice_start(int64_t x, int64_t U, int64_t gx) { return (x * U) / gx; }
 
+// Start-up plus epilogue of one prefill work item, in units of one pair of
+// 64-cell tiles of work.
+constexpr int64_t PF_ITEM_COST = 3;
+
 // Largest x with slice_start(x) <= q (U > 0).
 __device__ __forceinline__ int32_t slice_of(int64_t q, int64_t U, int64_t gx) {
     return (int32_t)(((q + 1) * gx + U - 1) / U - 1);
@@ -135,6 +139,73 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
         const int32_t item_base = pass == 0 ? 0 : p.cap_dec;
         const int32_t cap = pass == 0 ? p.cap_dec : p.cap_pf;
         int32_t *cta0 = p.cta_item0 + (pass == 0 ? 0 : gx_dec + 1);
+        if (pass == 1) {
+            // Prefill: every item costs a start-up (Q load, first products) and an
+            // epilogue on top of its pairs, so columns are filled greedily in block
+            // order up to an equal share of pairs + PF_ITEM_COST per item, a block
+            // spilling into the next column only when the column is full.
+            if (tid == 0) {
+                int64_t P = 0;
+                int32_t nne = 0;
+                for (int32_t b = lo; b < hi; ++b) {
+                    const int64_t pr = (p.counts[b] + 1) / 2;
+                    P += pr;
+                    nne += pr > 0 ? 1 : 0;
+                }
+                const int64_t C = PF_ITEM_COST;
+                const int64_t cols = max((int64_t)1, min(gx, (P + C * nne + C - 1) / C));
+                const int64_t T = max(C + 1, (P + C * (nne + cols - 1) + cols - 1) / cols);
+                int32_t x = 0, nitem = 0;
+                int64_t acc = 0;
+                auto emit = [&](int32_t b, int32_t t0, int32_t t1) {
+                    kvk::WorkItem w;
+                    w.block = b;
+                    w.t0 = t0;
+                    w.t1 = t1;
+                    w.cta = x;
+                    if (nitem < cap) p.work[item_base + nitem] = w;
+                    else kvd::report(p.err, kvd::DERR_BOUNDS);
+                    ++nitem;
+                };
+                for (int32_t b = lo; b < hi; ++b) {
+                    const int32_t cnt = p.counts[b];
+                    const int64_t pairs = (cnt + 1) / 2;
+                    p.blk_item0[b] = item_base + nitem;
+                    int32_t nseg = 0;
+                    if (pairs == 0) {
+                        emit(b, 0, 0);
+                        nseg = 1;
+                    } else {
+                        int64_t done = 0;
+                        while (done < pairs) {
+                            if (acc > 0 && acc + C >= T && x < gx - 1) {   // this column is full
+                                ++x;
+                                acc = 0;
+                            }
+                            int64_t take = pairs - done;
+                            if (x < gx - 1) {
+                                take = min(take, max((int64_t)1, T - acc - C));
+                                if (pairs - done - take < C) take = pairs - done;   // no tiny tail item
+                            }
+                            emit(b, (int32_t)(2 * done), (int32_t)min((int64_t)cnt, 2 * (done + take)));
+                            ++nseg;
+                            done += take;
+                            acc += C + take;
+                        }
+                    }
+                    p.blk_nitems[b] = nseg;
+                }
+                const int32_t n_items = min(nitem, cap);
+                p.n_work[1] = n_items;
+                int32_t i = 0;
+                for (int32_t xx = 0; xx <= (int32_t)gx; ++xx) {
+                    while (i < n_items && p.work[item_base + i].cta < xx) ++i;
+                    cta0[xx] = i;
+                }
+            }
+            __syncthreads();
+            continue;
+        }
         if (tid == 0) { tot = 0; run_u = 0; run_i = 0; }
         __syncthreads();
         for (int32_t b = lo + tid; b < hi; b += blockDim.x) {
