@@ -78,7 +78,7 @@ static_assert(MSLOTS >= KSTAGES + 2, "metadata ring too short for the K ring");
 constexpr int ISLOTS = 4;
 static_assert(ISLOTS > KSTAGES, "lane-table ring too short for the K ring");
 
-struct Meta {                 // per pair tile: what the producer learned about it
+struct __align__(16) Meta {     // per pair tile: what the producer learned about it (16-byte loads)
     int32_t full;
     int32_t ys[2];            // TMA row coordinates of the two 64-cell halves
     int32_t pad;
@@ -597,12 +597,32 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
 #pragma unroll
                     for (int c = 0; c < 64; ++c) sb[c] = __float_as_uint(-INFINITY);
                 } else if (!full) {
+                    // which of my 64 cells this row sees, built in a rolled loop (this path
+                    // runs on a few tiles per item: its code is kept small), then applied
+                    // (16-byte loads, all issued before any test)
+                    uint4 hb[4];
+                    int4 cp[16];
+                    const uint4 *hs = reinterpret_cast<const uint4 *>(&mt.has[64 * ch]);
+                    const int4 *cs = reinterpret_cast<const int4 *>(&mt.cpos[64 * ch]);
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        const int cc = 64 * ch + c;
-                        const bool vis = mt.has[cc] && (!a.u.causal || mt.cpos[cc] <= rpos);
-                        if (!vis) sb[c] = __float_as_uint(-INFINITY);
+                    for (int q = 0; q < 4; ++q) hb[q] = hs[q];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) cp[q] = cs[q];
+                    const int32_t lim = a.u.causal ? rpos : INT32_MAX;
+                    uint64_t vm = 0;
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const uint32_t hw = (&hb[q >> 2].x)[q & 3];   // has of cells 4q .. 4q + 3
+                        const int32_t c4[4] = {cp[q].x, cp[q].y, cp[q].z, cp[q].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const bool vis = ((hw >> (8 * e)) & 0xffu) != 0 && c4[e] <= lim;
+                            vm |= (uint64_t)vis << (4 * q + e);
+                        }
                     }
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        sb[c] = ((vm >> c) & 1ull) ? sb[c] : __float_as_uint(-INFINITY);
                 }
 #pragma unroll
                 for (int c = 0; c < 64; c += 2)
