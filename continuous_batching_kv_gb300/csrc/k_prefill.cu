@@ -72,11 +72,6 @@ constexpr uint32_t IDESC_PV = tc::idesc_f16(128, 128, 0, 1);
 // the slot) went out before that PV.
 constexpr int MSLOTS = 8;
 static_assert(MSLOTS >= KSTAGES + 2, "metadata ring too short for the K ring");
-// Lane tables, one per work item: the K load of an item's first pair g rewrites
-// the slot of the item ISLOTS back; it needs S of g - KSTAGES done, whose item
-// (at most KSTAGES back) had its Q, hence its lane table, taken already.
-constexpr int ISLOTS = 4;
-static_assert(ISLOTS > KSTAGES, "lane-table ring too short for the K ring");
 
 struct __align__(16) Meta {     // per pair tile: what the producer learned about it (16-byte loads)
     int32_t full;
@@ -85,11 +80,6 @@ struct __align__(16) Meta {     // per pair tile: what the producer learned abou
     int32_t cpos[128];
     uint8_t has[128];         // cell holds the block's sequence and is not from a later ubatch
     uint8_t anyvis[128];      // ... and some row of the block may see it
-};
-
-struct ItemSlot {             // per work item: the query vector behind each TMEM lane
-    int32_t row[M];           // ubatch row, -1 for lanes past the block's query vectors
-    int32_t rpos[M];
 };
 
 struct __align__(16) Aux {
@@ -103,7 +93,6 @@ struct __align__(16) Aux {
     int32_t flag;
     int32_t pad;
     Meta meta[MSLOTS];
-    ItemSlot islot[ISLOTS];
     float red[2][2][M];       // [pair parity][cell half][row]: partial row maxima
     float lex[2][2][M];       // [item parity][cell half][row]: row sums
 };
@@ -253,15 +242,15 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
 
     if (warp == 8) {
         // ===================== K producer (whole warp) =====================
-        // K of pair g + 2 loads as soon as S of pair g has read K of g.  Each pair's
-        // list entries, flags and per-cell visibility (and, for an item's first
-        // pair, its lane table) are fetched while the K slot is still busy and
-        // published through meta_full before the K copy is issued.  V has its own
-        // warp: these dependent global reads never hold up a V copy.
+        // K of pair g + KSTAGES loads as soon as S of pair g has read K of g.  Each
+        // pair's list entries, flags and per-cell visibility are fetched while the K
+        // slot is still busy and published through meta_full before the K copy is
+        // issued.  V has its own warp: these dependent global reads never hold up a
+        // V copy.
         const int32_t lane = tid & 31;
         int32_t total = 0;
         for (int32_t wi = i0; wi < i1; ++wi) total += item_info(a, wi).pairs;
-        int32_t kc = 0, nonempty = 0;
+        int32_t kc = 0;
         int32_t kwi = i0, kj = 0;              // K cursor: item and pair within it
         ItemInfo kit{};
         kvi::DevBlock kb{};
@@ -269,7 +258,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         int32_t tt[2] = {-1, -1};
         bool full = false;
         bool mhas[4] = {false, false, false, false}, many[4] = {false, false, false, false};
-        int32_t mpos[4] = {0, 0, 0, 0}, lrow[4] = {-1, -1, -1, -1}, lpos[4] = {0, 0, 0, 0};
+        int32_t mpos[4] = {0, 0, 0, 0};
         long long t_last = clock64();
         while (kc < total) {
             if (!warp_ok(fail)) break;
@@ -314,18 +303,6 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                             many[r] = has && (!a.u.causal || cp <= kb.pos_max);
                         }
                     }
-                    if (kj == 0) {
-                        const int32_t nqv = kb.n_rows * G;
-                        for (int r = 0; r < 4; ++r) {
-                            const int32_t n = lane + 32 * r;
-                            lrow[r] = -1;
-                            lpos[r] = 0;
-                            if (n < nqv) {
-                                lrow[r] = a.u.perm[kb.row0 + n / G];
-                                lpos[r] = a.u.rows[lrow[r]].pos;
-                            }
-                        }
-                    }
                     have_k = true;
                 }
                 const int32_t st = kc % KSTAGES;
@@ -334,16 +311,6 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 ready = __shfl_sync(0xffffffffu, ready, 0);
                 if (ready) {
                     Meta &mt = x.meta[kc % MSLOTS];
-                    if (kj == 0) {
-                        // the item's lane table (see ISLOTS: its previous reader, ISLOTS
-                        // non-empty items back, has taken it)
-                        ItemSlot &is = x.islot[nonempty % ISLOTS];
-                        for (int r = 0; r < 4; ++r) {
-                            is.row[lane + 32 * r] = lrow[r];
-                            is.rpos[lane + 32 * r] = lpos[r];
-                        }
-                        ++nonempty;
-                    }
                     if (lane == 0) {
                         for (int h = 0; h < 2; ++h)   // a missing second tile: out of bounds, TMA writes zeros
                             mt.ys[h] = tt[h] >= 0 ? kb.stream * a.u.kv_size + tt[h] * TILE : -TILE;
@@ -359,8 +326,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         }
                     }
                     __syncwarp();
-                    // the metadata (and lane table) go out before the K copy is issued:
-                    // the softmax may fetch its Q rows while the copy is in flight
+                    // the metadata goes out before the K copy is issued
                     kvd::mbar_arrive(&x.meta_full[kc % MSLOTS]);
                     if (kc == 0) kvd::pdl_wait();   // the K/V cache rows of this ubatch are written
                     if (lane == 0) {
@@ -531,24 +497,20 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         uint32_t n_s[2] = {0, 0};
         uint32_t n_l = 0, n_p = 0;
         int32_t k = 0;                         // pair tiles consumed (stage ring position)
-        int32_t nonempty = 0;
         bool ok = true;
         bool dep_done = false;                 // waited for the previous kernel of the stream
         for (int32_t wi = i0; wi < i1 && ok && warp_ok(fail); ++wi) {
             const ItemInfo it = item_info(a, wi);
+            // the query vector behind my TMEM lane (an empty item has a block that sees
+            // no cell: zeros, or an empty partial), fetched here rather than from the
+            // producer so that Q starts loading as early as possible
             int32_t row = -1, rpos = 0;
-            if (it.pairs == 0) {
-                // an empty item (its block sees no cell): zeros, or an empty partial
+            {
                 const kvi::DevBlock b = a.u.blocks[it.block];
-                if (n < b.n_rows * G) row = a.u.perm[b.row0 + n / G];
-            } else {
-                // the first pair's metadata also publishes this item's lane table
-                ok = __all_sync(0xffffffffu, wait_or_fail(&x.meta_full[k % MSLOTS], (uint32_t)(k / MSLOTS) & 1u, fail));
-                if (!ok) break;
-                const ItemSlot &is = x.islot[nonempty % ISLOTS];
-                ++nonempty;
-                row = is.row[n];
-                rpos = is.rpos[n];
+                if (n < b.n_rows * G) {
+                    row = a.u.perm[b.row0 + n / G];
+                    rpos = a.u.rows[row].pos;
+                }
             }
             if (!dep_done) {   // before the first read of Q and the first write of an output
                 kvd::pdl_wait();
