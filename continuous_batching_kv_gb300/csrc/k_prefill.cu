@@ -728,18 +728,20 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
 }
 
 
-// Split-K merge of the prefill path: eight CTAs per (prefill block, KV head),
-// 16 query vectors each; blocks covered by a single item were written directly
-// and return at once.  Thread t takes query vector 16z + t / 16 and 8 of its
-// 128 values, and loads up to eight partials at once (one round trip to L2
-// for most blocks), folding them into a running (M, L, O):
+// Split-K merge of the prefill path: sixteen 128-thread CTAs per (prefill block,
+// KV head), 8 query vectors each; blocks covered by a single item were written
+// directly and return at once.  Thread t takes query vector 8z + t / 16 and 8 of
+// its 128 values, and loads up to four partials at once, folding them into a
+// running (M, L, O):
 //   O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
 // Launched as a programmatic dependent of the attention kernel: the plan is
-// read first, the partials only after the attention grid has finished.
-constexpr int MERGE_SPLIT = 8;
-constexpr int MERGE_QMAX = 8;
+// read first, the partials only after the attention grid has finished.  The
+// CTAs are small (128 threads, at most 64 registers each) so that one fits on
+// an SM beside an attention CTA and waits there, ready, for the grid to end.
+constexpr int MERGE_SPLIT = 16;
+constexpr int MERGE_QMAX = 4;
 
-__global__ void __launch_bounds__(256) k_merge_pf(const kvk::PrefillArgs a) {
+__global__ void __launch_bounds__(128, 8) k_merge_pf(const kvk::PrefillArgs a) {
     const int32_t b = a.u.n_dec_blocks + blockIdx.x;
     const int32_t hk = blockIdx.y;
     const int32_t nitems = a.p.blk_nitems[b];
@@ -748,7 +750,7 @@ __global__ void __launch_bounds__(256) k_merge_pf(const kvk::PrefillArgs a) {
         return;
     }
     const kvi::DevBlock blk = a.u.blocks[b];
-    const int32_t n = (int32_t)blockIdx.z * (M / MERGE_SPLIT) + (int32_t)(threadIdx.x >> 4);
+    const int32_t n = (int32_t)blockIdx.z * (M / MERGE_SPLIT) + (int32_t)(threadIdx.x >> 4);   // 8 per CTA
     const int32_t d0 = (int32_t)(threadIdx.x & 15) * 8;
     const int32_t G = a.gqa;
     if (n >= blk.n_rows * G) return;
@@ -838,7 +840,7 @@ cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, con
     cudaError_t e = cudaLaunchKernelEx(&cfg, k_prefill, *tm_k, *tm_v, a);
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(a.u.n_blocks - a.u.n_dec_blocks, a.n_head_kv, MERGE_SPLIT);
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     e = cudaLaunchKernelEx(&cfg, k_merge_pf, a);
     if (e != cudaSuccess) return e;
