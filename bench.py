@@ -289,6 +289,13 @@ class OursArm:
             for q, pmax in self.base_pos_max.items():
                 kv.kv_seq_rm(self.c, q, pmax + 1, -1)
 
+    def rewind(self):
+        """Return the cache to its post-setup state and the decode loop to its
+        first iteration, so that a second pass replays the same steps."""
+        for q, pmax in self.base_pos_max.items():
+            self.kv.kv_seq_rm(self.c, q, pmax + 1, -1)
+        self.step_no = -1
+
     def timed_calls_per_step(self):
         return sum(len(ubs) for _, ubs, _ in self.calls) * max(0, self.L - 1)
 
@@ -342,7 +349,6 @@ def run_ours(args, rank, world, device):
         arm.step()
     barrier()
     clocks = Clocks(device if isinstance(device, int) else torch.cuda.current_device())
-    timers = EventPool(arm.timed_calls_per_step() * args.steps)
     launches0 = kv.kv_launch_count(arm.c)
     clocks.start()
     barrier()
@@ -350,7 +356,7 @@ def run_ours(args, rank, world, device):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(arm.stream)
     for _ in range(args.steps):
-        arm.step(timers=timers)
+        arm.step()
     t1.record(arm.stream)
     barrier()
     clk = clocks.stop()
@@ -360,6 +366,21 @@ def run_ours(args, rank, world, device):
     ms_max = max_over_ranks(ms_total, device) if dist else ms_total
     tokens = measured_tokens(cfg) * args.steps * world
     value = tokens / (ms_max / 1e3)
+
+    # The attention launches' own durations come from a second pass over the
+    # same steps: an event recorded between kv_store and ubatch_attention sits
+    # between two kernels that otherwise overlap (the attention kernel's
+    # start-up runs under the store's tail), so bracketing every call would
+    # slow the pass whose total is the headline value.
+    arm.rewind()
+    for _ in range(max(args.warmup, 3)):
+        arm.step()
+    timers = EventPool(arm.timed_calls_per_step() * args.steps)
+    barrier()
+    for _ in range(args.steps):
+        arm.step(timers=timers)
+    barrier()
+    assert kv.kv_device_error(arm.c) == 0
 
     # roofline of the dominant kernel (attention), timed live above
     res = timers.results()
@@ -379,6 +400,8 @@ def run_ours(args, rank, world, device):
                 "frac": round(achieved / tflops, 4), "traffic": None,
                 "kernel": "ubatch_attention (k_prefill + k_merge_pf)"}
     roof.update({"peak_source": peak_src, "launches_timed": len(durs),
+                 "timing": "CUDA events around each attention launch of layers >= 1, "
+                           "on a second pass over the same steps",
                  "avg_launch_us": round(1e3 * sum(durs) / max(1, len(durs)), 2)})
 
     e2e = None

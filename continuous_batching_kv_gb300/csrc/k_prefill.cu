@@ -328,7 +328,17 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     __syncwarp();
                     // the metadata goes out before the K copy is issued
                     kvd::mbar_arrive(&x.meta_full[kc % MSLOTS]);
-                    if (kc == 0) kvd::pdl_wait();   // the K/V cache rows of this ubatch are written
+                    if (kc == 0) {
+                        // Warm L2 with the first pair's K and V while the previous kernel
+                        // (normally the store of this ubatch's rows) finishes: a prefetch
+                        // returns nothing, so racing that kernel's writes is harmless.
+                        if (lane < 8) {
+                            const CUtensorMap *tm = lane < 4 ? &tm_k : &tm_v;
+                            const int32_t y = mt.ys[(lane >> 1) & 1];
+                            if (y >= 0) kvd::tma_prefetch_2d(tm, hk * 128 + 64 * (lane & 1), y);
+                        }
+                        kvd::pdl_wait();   // the K/V cache rows of this ubatch are written
+                    }
                     if (lane == 0) {
                         uint8_t *ks = smem + OFF_K + st * TILEB;
                         const int32_t xk = hk * 128;
@@ -512,12 +522,15 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     rpos = a.u.rows[row].pos;
                 }
             }
+            const bool live = row >= 0;
+            const int32_t h = hk * G + (n % G);
             if (!dep_done) {   // before the first read of Q and the first write of an output
+                // warm L2 with my 128 bytes of Q while the previous kernel finishes (a
+                // prefetch returns nothing, so racing its writes is harmless)
+                if (live && it.pairs > 0) kvd::prefetch_l2(a.q + ((int64_t)row * a.n_head + h) * 128 + 64 * ch);
                 kvd::pdl_wait();
                 dep_done = true;
             }
-            const bool live = row >= 0;
-            const int32_t h = hk * G + (n % G);
             float m_run = -INFINITY, l_run = 0.f;   // the row's running maximum, this half's row sum
             if (it.pairs > 0) {
             // ---- Q into TMEM (the A operand of S = Q K^T): row n, d-half ch, fp16,
