@@ -48,6 +48,7 @@ struct DeviceState {
     int32_t *d_err = nullptr;
     // one TMA descriptor per K / V tensor
     std::vector<CUtensorMap> tm_k, tm_v;
+    std::vector<CUtensorMap> tm_dec;   // per layer: K, V with 64-row boxes, K, V with 8-row boxes
     uint64_t plan_split = 0;
     int32_t plan_ub = -1;
     size_t bytes = 0;
@@ -94,13 +95,15 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // A K or V tensor as a 2-D fp16 matrix: n_stream*kv_size rows of
-// n_head_kv*128 values; boxes of 64 rows x 64 values, 128-byte swizzle.
-bool make_kv_map(CUtensorMap *m, void *base, int32_t n_head_kv, int64_t n_rows) {
+// n_head_kv*128 values; boxes of box_rows (64 or 8) rows x 64 values, 128-byte
+// swizzle (an 8-row box lands in shared memory exactly as rows 8g .. 8g + 7 of
+// a 64-row box at the same 1 KiB-aligned offset).
+bool make_kv_map(CUtensorMap *m, void *base, int32_t n_head_kv, int64_t n_rows, uint32_t box_rows = TILE) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)n_head_kv * 128, (cuuint64_t)n_rows};
     cuuint64_t strides[1] = {(cuuint64_t)n_head_kv * 128 * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)TILE};
+    cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -284,10 +287,16 @@ int device_init(kv_cache *c) {
     d->tm_k.resize(c->prm.n_layer);
     d->tm_v.resize(c->prm.n_layer);
     const int64_t rows = (int64_t)c->prm.n_stream * c->kv_size;
+    d->tm_dec.resize(4 * (size_t)c->prm.n_layer);
     for (int32_t l = 0; l < c->prm.n_layer; ++l) {
+        CUtensorMap *td = &d->tm_dec[4 * (size_t)l];
         if (!make_kv_map(&d->tm_k[l], c->k_layers[l], hkv, rows) ||
-            !make_kv_map(&d->tm_v[l], c->v_layers[l], hkv, rows))
+            !make_kv_map(&d->tm_v[l], c->v_layers[l], hkv, rows) ||
+            !make_kv_map(&td[2], c->k_layers[l], hkv, rows, 8) ||
+            !make_kv_map(&td[3], c->v_layers[l], hkv, rows, 8))
             return c->set_err(KV_E_CUDA, "cuTensorMapEncodeTiled failed");
+        td[0] = d->tm_k[l];
+        td[1] = d->tm_v[l];
     }
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(c, e, "init sync");
     return KV_OK;
@@ -377,7 +386,7 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
         a.err = d->d_err;
         a.nq_max = decode_nq_max(c, u);
         a.early_ok = early_ok ? 1 : 0;
-        if ((e = kvk::launch_decode(&d->tm_k[layer], &d->tm_v[layer], a, d->gx_dec, st)) != cudaSuccess)
+        if ((e = kvk::launch_decode(&d->tm_dec[4 * (size_t)layer], a, d->gx_dec, st)) != cudaSuccess)
             return cuda_fail(c, e, "decode launch");
         c->launches += 1;
     }
@@ -528,7 +537,7 @@ extern "C" int ubatch_attention_static_scratch(kv_cache *c, const kv_split *sp, 
     a.nq_max = decode_nq_max(c, u);
     // the counters were just cleared by a copy engine, not a kernel: wait for it
     a.early_ok = 0;
-    if ((e = kvk::launch_decode(&d->tm_k[layer], &d->tm_v[layer], a, d->gx_dec, st)) != cudaSuccess)
+    if ((e = kvk::launch_decode(&d->tm_dec[4 * (size_t)layer], a, d->gx_dec, st)) != cudaSuccess)
         return cuda_fail(c, e, "decode launch");
     c->launches += 1;
     return KV_OK;

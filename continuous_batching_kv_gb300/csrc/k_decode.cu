@@ -51,12 +51,22 @@ constexpr float RESCALE_LOG2 = 8.0f;
 template <int NQ>
 constexpr int stages_for() { return NQ <= 4 ? 3 : 2; }
 
-struct Meta {                 // per stage: what the producer learned about the tile
-    int32_t full;
-    int32_t pad[3];
+// A stage holds either one fully visible tile (64 cells, no per-cell test) or
+// up to 8 packed 8-cell groups taken from the block's partially visible tiles,
+// in the order the tile list gives them; slot w (cells 8w .. 8w + 7) belongs
+// to consumer warp w.  The order of cells does not change the softmax.
+struct Meta {                 // per stage: what the producer learned about its cells
+    int32_t full;             // 1: one fully visible tile
+    int32_t gmask;            // packed: bit w set when slot w holds a group
+    int32_t last;             // the item's last stage
+    int32_t pad;
     int32_t cpos[TILE];
     uint8_t has[TILE];        // cell holds the block's sequence and is not from a later ubatch
 };
+
+constexpr int GROUP_BYTES = 8 * 128;            // one 8-row box
+constexpr int WINDOW = 32;                      // tile-list entries the producer reads at once
+constexpr int GQ = 512;                         // group queue ring (> WINDOW * 8 + 7)
 
 template <int NQ>
 struct __align__(16) Aux {
@@ -70,6 +80,7 @@ struct __align__(16) Aux {
     float scr_l[4][NQ];           //   row sums
     float scr_o[4][NQ][128];      //   and accumulators
     int32_t rpos[NQ];
+    int32_t gq[GQ];               // producer: queued groups' first cells (in the stream)
     uint64_t full[S], empty[S];
     uint64_t cbar;                // consumer exchanges (all 256 consumer threads)
     int32_t fail;
@@ -77,6 +88,10 @@ struct __align__(16) Aux {
 
 template <int NQ>
 constexpr size_t smem_bytes() { return (size_t)stages_for<NQ>() * STAGE_BYTES + sizeof(Aux<NQ>); }
+
+// two CTAs per SM (228 KiB of shared memory, 1 KiB reserved per CTA) up to NQ = 8
+static_assert(2 * (smem_bytes<4>() + 1024) <= 228 * 1024, "two NQ=4 CTAs must fit on an SM");
+static_assert(2 * (smem_bytes<8>() + 1024) <= 228 * 1024, "two NQ=8 CTAs must fit on an SM");
 
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
@@ -127,6 +142,7 @@ __device__ __forceinline__ bool cons_sync(uint64_t *bar, uint32_t &phase, volati
 template <int NQ>
 __global__ void __launch_bounds__(NT, (NQ <= 8 ? 2 : 1))
 k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+         const __grid_constant__ CUtensorMap tm_k8, const __grid_constant__ CUtensorMap tm_v8,
          const kvk::DecodeArgs a) {
     constexpr int S = stages_for<NQ>();
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -152,6 +168,8 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     if (tid == 0) {
         kvd::prefetch_tmap(&tm_k);
         kvd::prefetch_tmap(&tm_v);
+        kvd::prefetch_tmap(&tm_k8);
+        kvd::prefetch_tmap(&tm_v8);
         for (int s = 0; s < S; ++s) {
             kvd::mbar_init(&x.full[s], 33);    // producer lane 0's expect_tx + 32 lanes
             kvd::mbar_init(&x.empty[s], NW);   // one arrival per consumer warp
@@ -164,63 +182,134 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 
     if (warp == NW) {
         // ======================= producer =======================
+        // Per item, the tile list is read WINDOW entries at a time: each fully
+        // visible tile gets a stage of its own (four 64-row boxes); the visible
+        // 8-cell groups of the other tiles are queued and leave in stages of 8
+        // (four 8-row boxes each), the remainder with the item's last window.
         int32_t k = 0;
         bool dep_done = false;
-        // wait outcomes and the loop condition are agreed by the whole warp, so a
+        bool ok = true;
+        uint32_t qh = 0, qt = 0;   // group queue head and tail (ring indices)
+        // wait outcomes and the loop conditions are agreed by the whole warp, so a
         // failure never splits it in front of __syncwarp
-        for (int32_t wi = i0; wi < i1 && __all_sync(0xffffffffu, *fail == 0); ++wi) {
+        auto acquire = [&](int32_t st) -> bool {
+            if (k >= S &&
+                !__all_sync(0xffffffffu, wait_or_fail(&x.empty[st], (uint32_t)((k / S) - 1) & 1u, fail)))
+                return false;
+            if (!dep_done) {   // the K/V rows of this ubatch are written by the kernel before
+                kvd::pdl_wait();
+                dep_done = true;
+            }
+            return true;
+        };
+        for (int32_t wi = i0; wi < i1 && ok; ++wi) {
             const kvk::WorkItem w = a.p.work[wi];
             const kvi::DevBlock b = a.u.blocks[w.block];
             const int32_t *list = a.p.tiles + (int64_t)w.block * a.p.tile_stride;
             const uint32_t *flg = a.p.flags + (int64_t)w.block * a.p.tile_stride;
-            for (int32_t li = w.t0; li < w.t1; ++li) {
-                const int32_t st = k % S;
-                // the tile's list entry and visibility are read before its slot is free
-                const int32_t t = list[li];
-                const bool full = (int32_t)(flg[t] & 0xffffu) == b.n_rows * TILE;
-                bool hs[2] = {false, false};
-                int32_t cp[2] = {0, 0};
-                if (!full) {
+            const int32_t ybase = b.stream * a.u.kv_size;
+            const int32_t xk = hk * 128;
+            for (int32_t base = w.t0; base < w.t1 && ok; base += WINDOW) {
+                const int32_t li = base + lane;
+                int32_t t = 0;
+                uint32_t fl = 0;
+                if (li < w.t1) {
+                    t = list[li];
+                    fl = flg[t];
+                }
+                const bool isfull = li < w.t1 && (int32_t)(fl & 0xffffu) == b.n_rows * TILE;
+                uint32_t fm = __ballot_sync(0xffffffffu, isfull);
+                // queue the visible groups of my tile (flags bits 16..23), in list order
+                uint32_t gm = (li < w.t1 && !isfull) ? ((fl >> 16) & 0xffu) : 0u;
+                const int32_t cnt = __popc(gm);
+                int32_t incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                uint32_t pos = qt + (uint32_t)(incl - cnt);
+                while (gm) {
+                    const int32_t g = __ffs(gm) - 1;
+                    gm &= gm - 1;
+                    x.gq[pos++ & (GQ - 1)] = t * TILE + 8 * g;
+                }
+                qt += (uint32_t)__shfl_sync(0xffffffffu, incl, 31);
+                __syncwarp();
+                const bool final_window = base + WINDOW >= w.t1;
+                // ---- fully visible tiles: one stage each ----
+                while (fm && ok) {
+                    const int32_t src = __ffs(fm) - 1;
+                    fm &= fm - 1;
+                    const int32_t tt = __shfl_sync(0xffffffffu, t, src);
+                    const int32_t st = k % S;
+                    if (!(ok = acquire(st))) break;
+                    if (lane == 0) {
+                        uint8_t *sp = stages + (size_t)st * STAGE_BYTES;
+                        const int32_t y = ybase + tt * TILE;
+                        x.meta[st].full = 1;
+                        x.meta[st].gmask = 0xff;
+                        x.meta[st].last = (final_window && fm == 0 && qt == qh) ? 1 : 0;
+                        kvd::fence_proxy_async_smem();
+                        kvd::mbar_arrive_expect_tx(&x.full[st], STAGE_BYTES);
+                        kvd::tma_load_2d(sp, &tm_k, xk, y, &x.full[st]);
+                        kvd::tma_load_2d(sp + BOX_BYTES, &tm_k, xk + 64, y, &x.full[st]);
+                        kvd::tma_load_2d(sp + 2 * BOX_BYTES, &tm_v, xk, y, &x.full[st]);
+                        kvd::tma_load_2d(sp + 3 * BOX_BYTES, &tm_v, xk + 64, y, &x.full[st]);
+                    }
+                    __syncwarp();
+                    kvd::mbar_arrive(&x.full[st]);
+                    ++k;
+                }
+                // ---- packed stages of 8 groups; the remainder on the item's last window ----
+                while (ok && (qt - qh >= 8u || (final_window && qt != qh))) {
+                    const int32_t n = (int32_t)min(8u, qt - qh);
+                    const bool last = final_window && qt - qh <= 8u;
+                    // the cells' visibility, read before the stage is free
+                    bool hs[2] = {false, false};
+                    int32_t cp[2] = {0, 0};
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        const int32_t j = t * TILE + lane + 32 * r;
-                        if (j < a.u.n_kv) {
-                            const int64_t g = (int64_t)b.stream * a.u.kv_size + j;
-                            const uint64_t wb = a.u.cell_bits[g * a.u.n_words + (b.seq0 >> 6)];
-                            hs[r] = ((wb >> (b.seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
-                            cp[r] = a.u.cell_pos[g];
+                        const int32_t l = lane + 32 * r;
+                        if (l < 8 * n) {
+                            const int32_t j = x.gq[(qh + (uint32_t)(l >> 3)) & (GQ - 1)] + (l & 7);
+                            if (j < a.u.n_kv) {
+                                const int64_t g = (int64_t)ybase + j;
+                                const uint64_t wb = a.u.cell_bits[g * a.u.n_words + (b.seq0 >> 6)];
+                                hs[r] = ((wb >> (b.seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
+                                cp[r] = a.u.cell_pos[g];
+                            }
                         }
                     }
-                }
-                if (k >= S &&
-                    !__all_sync(0xffffffffu, wait_or_fail(&x.empty[st], (uint32_t)((k / S) - 1) & 1u, fail)))
-                    break;
-                if (!dep_done) {   // the K/V rows of this ubatch are written by the kernel before
-                    kvd::pdl_wait();
-                    dep_done = true;
-                }
-                if (lane == 0) {
-                    uint8_t *sp = stages + (size_t)st * STAGE_BYTES;
-                    const int32_t y = b.stream * a.u.kv_size + t * TILE;
-                    const int32_t xk = hk * 128;
-                    kvd::fence_proxy_async_smem();
-                    kvd::mbar_arrive_expect_tx(&x.full[st], STAGE_BYTES);
-                    kvd::tma_load_2d(sp, &tm_k, xk, y, &x.full[st]);
-                    kvd::tma_load_2d(sp + BOX_BYTES, &tm_k, xk + 64, y, &x.full[st]);
-                    kvd::tma_load_2d(sp + 2 * BOX_BYTES, &tm_v, xk, y, &x.full[st]);
-                    kvd::tma_load_2d(sp + 3 * BOX_BYTES, &tm_v, xk + 64, y, &x.full[st]);
-                    x.meta[st].full = full ? 1 : 0;
-                }
-                if (!full) {
+                    const int32_t jg = lane < n ? x.gq[(qh + (uint32_t)lane) & (GQ - 1)] : 0;
+                    const int32_t st = k % S;
+                    if (!(ok = acquire(st))) break;
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
                         x.meta[st].has[lane + 32 * r] = hs[r] ? 1 : 0;
                         x.meta[st].cpos[lane + 32 * r] = cp[r];
                     }
+                    if (lane == 0) {
+                        x.meta[st].full = 0;
+                        x.meta[st].gmask = (1 << n) - 1;
+                        x.meta[st].last = last ? 1 : 0;
+                        kvd::fence_proxy_async_smem();
+                        kvd::mbar_arrive_expect_tx(&x.full[st], (uint32_t)(n * 4 * GROUP_BYTES));
+                    }
+                    __syncwarp();
+                    if (lane < n) {   // slot `lane` of the stage: rows jg .. jg + 7
+                        uint8_t *sp = stages + (size_t)st * STAGE_BYTES + lane * GROUP_BYTES;
+                        const int32_t y = ybase + jg;
+                        kvd::tma_load_2d(sp, &tm_k8, xk, y, &x.full[st]);
+                        kvd::tma_load_2d(sp + BOX_BYTES, &tm_k8, xk + 64, y, &x.full[st]);
+                        kvd::tma_load_2d(sp + 2 * BOX_BYTES, &tm_v8, xk, y, &x.full[st]);
+                        kvd::tma_load_2d(sp + 3 * BOX_BYTES, &tm_v8, xk + 64, y, &x.full[st]);
+                    }
+                    qh += (uint32_t)n;
+                    __syncwarp();
+                    kvd::mbar_arrive(&x.full[st]);
+                    ++k;
                 }
-                __syncwarp();
-                kvd::mbar_arrive(&x.full[st]);
-                ++k;
             }
         }
         if (*fail && lane == 0) {
@@ -311,12 +400,20 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 for (int n = 0; n < NQ; ++n)
                     if (nl == n) rp_l = rp[n];
             }
-            for (int32_t li = w.t0; li < w.t1; ++li, ++k) {
+            // the item's stages, until the one marked last (an item with an empty
+            // list has none)
+            for (bool more = w.t0 < w.t1; more; ++k) {
                 const int32_t st = k % S;
                 ok = __all_sync(0xffffffffu, wait_or_fail(&x.full[st], (uint32_t)(k / S) & 1u, fail));
                 if (!ok) break;
                 const uint8_t *sp = stages + (size_t)st * STAGE_BYTES;
                 const bool full = x.meta[st].full != 0;
+                more = x.meta[st].last == 0;
+                if (!((x.meta[st].gmask >> warp) & 1)) {   // my slot of a packed stage is empty
+                    __syncwarp();
+                    if (lane == 0) kvd::mbar_arrive(&x.empty[st]);
+                    continue;
+                }
                 if constexpr (NQ == 4) {
                 // ---- scores: cells g and g + 4 of my warp's 8, my 16 d, the four query
                 //      vectors; the eight lanes of a cell then reduce-scatter the sums so
@@ -698,8 +795,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 }
 
 template <int NQ>
-cudaError_t launch_nq(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const kvk::DecodeArgs &a, int32_t grid_x,
-                      cudaStream_t st) {
+cudaError_t launch_nq(const CUtensorMap *tm, const kvk::DecodeArgs &a, int32_t grid_x, cudaStream_t st) {
     static bool smem_set = false;
     constexpr size_t SMEM = smem_bytes<NQ>();
     if (!smem_set) {
@@ -718,7 +814,7 @@ cudaError_t launch_nq(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const kv
     cfg.stream = st;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_decode<NQ>, *tm_k, *tm_v, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_decode<NQ>, tm[0], tm[1], tm[2], tm[3], a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -729,13 +825,12 @@ namespace kvk {
 
 int32_t decode_ctas_per_sm() { return 2; }
 
-cudaError_t launch_decode(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const DecodeArgs &a,
-                          int32_t grid_x, cudaStream_t st) {
-    if (a.nq_max <= 1) return launch_nq<1>(tm_k, tm_v, a, grid_x, st);
-    if (a.nq_max <= 2) return launch_nq<2>(tm_k, tm_v, a, grid_x, st);
-    if (a.nq_max <= 4) return launch_nq<4>(tm_k, tm_v, a, grid_x, st);
-    if (a.nq_max <= 8) return launch_nq<8>(tm_k, tm_v, a, grid_x, st);
-    return launch_nq<16>(tm_k, tm_v, a, grid_x, st);
+cudaError_t launch_decode(const CUtensorMap *tm, const DecodeArgs &a, int32_t grid_x, cudaStream_t st) {
+    if (a.nq_max <= 1) return launch_nq<1>(tm, a, grid_x, st);
+    if (a.nq_max <= 2) return launch_nq<2>(tm, a, grid_x, st);
+    if (a.nq_max <= 4) return launch_nq<4>(tm, a, grid_x, st);
+    if (a.nq_max <= 8) return launch_nq<8>(tm, a, grid_x, st);
+    return launch_nq<16>(tm, a, grid_x, st);
 }
 
 }  // namespace kvk

@@ -82,8 +82,8 @@ struct DecodeArgs {
     int32_t nq_max;         // most query vectors in one decode block of this ubatch (1..DEC_QMAX)
     int32_t early_ok;       // as in PrefillArgs
 };
-cudaError_t launch_decode(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const DecodeArgs &a,
-                          int32_t grid_x, cudaStream_t st);
+// tm: the layer's K and V maps with 64-row boxes, then with 8-row boxes
+cudaError_t launch_decode(const CUtensorMap *tm, const DecodeArgs &a, int32_t grid_x, cudaStream_t st);
 int32_t decode_ctas_per_sm();
 
 // k_prefill.cu
