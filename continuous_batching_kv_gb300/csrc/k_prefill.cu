@@ -405,11 +405,18 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         }
     } else if (warp == 9) {
         // ===================== MMA issuer =====================
+        // The tensor core's work per item is a fixed sequence: S_0, S_1, then for
+        // each pair j: PV_j, S_j+2 (S_j+2 goes to the score buffer of pair j, whose P
+        // PV_j reads first: one thread's MMAs run in issue order).  Every step waits
+        // on its mbarrier with a blocking (suspending, bounded) wait, so the thread
+        // wakes as soon as a P or a K tile is ready.
         if ((tid & 31) == 0) {
-            int32_t gidx = 0;                  // global pair-tile counter (stage ring)
-            int32_t last_pair[2] = {-1, -1};   // global pair whose S (then P) last filled each score buffer
+            int32_t gidx = 0;                  // global pair-tile counter (stage rings)
             uint32_t n_q = 0;
-            auto issue_s = [&](int32_t gi, int32_t buf) {
+            bool ok = true;
+            auto issue_s = [&](int32_t gi, int32_t buf) -> bool {
+                if (!wait_or_fail(&x.k_full[gi % KSTAGES], (uint32_t)(gi / KSTAGES) & 1u, fail)) return false;
+                tc::fence_after();
                 const uint32_t k_addr = sbase + OFF_K + (gi % KSTAGES) * TILEB;
                 const uint32_t d = tmem + (uint32_t)buf * 128u;
 #pragma unroll
@@ -420,72 +427,37 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 }
                 tc::commit(&x.s_full[buf]);
                 tc::commit(&x.k_empty[gi % KSTAGES]);   // this K tile is consumed
+                return true;
             };
-            // Per item, a non-blocking scheduler: PV of the oldest ready P first, then S
-            // of the next pair once its K tile has landed and the PV that read the P
-            // held in its score buffer has completed.  Nothing blocks on one condition
-            // while the other is ready.
-            for (int32_t wi = i0; wi < i1 && !*fail; ++wi) {
+            for (int32_t wi = i0; wi < i1 && ok; ++wi) {
                 const ItemInfo it = item_info(a, wi);
                 if (it.pairs == 0) continue;
-                if (!wait_or_fail(&x.q_full, n_q & 1u, fail)) break;
+                if (!(ok = wait_or_fail(&x.q_full, n_q & 1u, fail))) break;
                 ++n_q;
                 tc::fence_after();
-                bool ok = true;
-                int32_t s_done = 0, pv_done = 0;
-                long long t_last = clock64();
-                while (pv_done < it.pairs) {
-                    bool progressed = false;
-                    // P of pair gp is signalled on p_full[gp & 1] (one barrier could be
-                    // lapped: the softmax may finish two pairs before this thread looks)
-                    const int32_t gp = gidx + pv_done;
-                    if (pv_done < s_done && kvd::mbar_test_wait(&x.p_full[gp & 1], (uint32_t)(gp >> 1) & 1u)) {
-                        ok = wait_or_fail(&x.v_full[gp % VSTAGES], (uint32_t)(gp / VSTAGES) & 1u, fail);
-                        if (!ok) break;
-                        tc::fence_after();
-                        const uint32_t v_addr = sbase + OFF_V + (gp % VSTAGES) * TILEB;
-                        const uint32_t p_tmem = tmem + 128u * (uint32_t)(pv_done & 1);
-                        // O += P V over the 128 cells: P of cells 16kk .. 16kk + 15 is 8 TMEM
-                        // columns at 64 (kk / 4) + 8 (kk % 4) of the score buffer
+                ok = issue_s(gidx, 0);
+                if (ok && it.pairs > 1) ok = issue_s(gidx + 1, 1);
+                for (int32_t j = 0; j < it.pairs && ok; ++j) {
+                    // P of pair gp is signalled on p_full[gp & 1]
+                    const int32_t gp = gidx + j;
+                    if (!(ok = wait_or_fail(&x.p_full[gp & 1], (uint32_t)(gp >> 1) & 1u, fail))) break;
+                    if (!(ok = wait_or_fail(&x.v_full[gp % VSTAGES], (uint32_t)(gp / VSTAGES) & 1u, fail))) break;
+                    tc::fence_after();
+                    const uint32_t v_addr = sbase + OFF_V + (gp % VSTAGES) * TILEB;
+                    const uint32_t p_tmem = tmem + 128u * (uint32_t)(j & 1);
+                    // O += P V over the 128 cells: P of cells 16kk .. 16kk + 15 is 8 TMEM
+                    // columns at 64 (kk / 4) + 8 (kk % 4) of the score buffer
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            tc::mma_ts(tmem + COL_O, p_tmem + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3),
-                                       tc::sdesc_sw128(v_addr + (uint32_t)kk * 2048u, HALF, 1024), IDESC_PV,
-                                       (pv_done > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        tc::commit(&x.pv_done[gp & 1]);
-                        tc::commit(&x.v_empty[gp % VSTAGES]);
-                        ++pv_done;
-                        progressed = true;
+                    for (int kk = 0; kk < 8; ++kk) {
+                        tc::mma_ts(tmem + COL_O, p_tmem + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3),
+                                   tc::sdesc_sw128(v_addr + (uint32_t)kk * 2048u, HALF, 1024), IDESC_PV,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
                     }
-                    if (s_done < it.pairs) {
-                        const int32_t gi = gidx + s_done;
-                        const int32_t buf = s_done & 1;
-                        const int32_t lp = last_pair[buf];
-                        // the S buffer holds the P that PV of pair lp reads: S may follow once
-                        // that PV is issued (the tensor core runs one thread's MMAs in issue
-                        // order, so the PV reads P before this S overwrites it)
-                        if (kvd::mbar_test_wait(&x.k_full[gi % KSTAGES], (uint32_t)(gi / KSTAGES) & 1u) &&
-                            lp < gidx + pv_done) {
-                            tc::fence_after();
-                            issue_s(gi, buf);
-                            last_pair[buf] = gi;
-                            ++s_done;
-                            progressed = true;
-                        }
-                    }
-                    if (progressed) {
-                        t_last = clock64();
-                    } else if (*fail || clock64() - t_last > kvd::WAIT_LIMIT_CYCLES) {
-                        *fail = 1;
-                        ok = false;
-                        break;
-                    } else {
-                        __nanosleep(POLL_NS);   // leave the issue slots to the softmax warps
-                    }
+                    tc::commit(&x.pv_done[gp & 1]);
+                    tc::commit(&x.v_empty[gp % VSTAGES]);
+                    if (j + 2 < it.pairs) ok = issue_s(gidx + j + 2, j & 1);
                 }
                 gidx += it.pairs;
-                if (!ok) break;
             }
             // all issued MMAs complete before TMEM is released
             tc::commit(&x.spare);
