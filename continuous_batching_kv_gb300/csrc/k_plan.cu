@@ -118,7 +118,7 @@ __device__ __forceinline__ int64_t slice_start(int64_t x, int64_t U, int64_t gx)
 
 // Start-up plus epilogue of one prefill work item, in units of one pair of
 // 64-cell tiles of work.
-constexpr int64_t PF_ITEM_COST = 3;
+constexpr int64_t PF_ITEM_COST = 5;
 
 // Largest x with slice_start(x) <= q (U > 0).
 __device__ __forceinline__ int32_t slice_of(int64_t q, int64_t U, int64_t gx) {
@@ -141,9 +141,12 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
         int32_t *cta0 = p.cta_item0 + (pass == 0 ? 0 : gx_dec + 1);
         if (pass == 1) {
             // Prefill: every item costs a start-up (Q load, first products) and an
-            // epilogue on top of its pairs, so columns are filled greedily in block
-            // order up to an equal share of pairs + PF_ITEM_COST per item, a block
-            // spilling into the next column only when the column is full.
+            // epilogue on top of its pairs, so a column's cost is its pairs plus
+            // PF_ITEM_COST per item.  Columns are filled greedily in block order up to
+            // a budget T, a block spilling into the next column when the column is
+            // full; T is the smallest budget with which the greedy fill needs at most
+            // gx columns (each thread tries its own T; two rounds narrow the range).
+            const int64_t C = PF_ITEM_COST;
             if (tid == 0) {
                 int64_t P = 0;
                 int32_t nne = 0;
@@ -152,9 +155,58 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                     P += pr;
                     nne += pr > 0 ? 1 : 0;
                 }
-                const int64_t C = PF_ITEM_COST;
-                const int64_t cols = max((int64_t)1, min(gx, (P + C * nne + C - 1) / C));
-                const int64_t T = max(C + 1, (P + C * (nne + cols - 1) + cols - 1) / cols);
+                tot = max(C + 1, (P + C * nne + gx - 1) / gx);   // lower bound on T
+                run_u = P + C * (nne + 1) + 1;                     // feasible with any gx >= 1
+            }
+            __syncthreads();
+            // columns the greedy fill needs with budget T (stops counting past gx)
+            auto columns = [&](int64_t T) -> int64_t {
+                int64_t x = 0, acc = 0;
+                for (int32_t b = lo; b < hi && x < gx; ++b) {
+                    const int64_t pairs = (p.counts[b] + 1) / 2;
+                    int64_t done = 0;
+                    while (done < pairs && x < gx) {
+                        const int64_t room = T - acc - C;
+                        if (room < 1) {
+                            ++x;
+                            acc = 0;
+                            continue;
+                        }
+                        const int64_t take = min(pairs - done, room);
+                        done += take;
+                        acc += C + take;
+                    }
+                }
+                return x + 1;
+            };
+            for (int32_t round = 0; round < 2; ++round) {
+                const int64_t t_lo = tot, t_hi = run_u;            // the answer lies in [t_lo, t_hi]
+                const int64_t step = max((int64_t)1, (t_hi - t_lo + blockDim.x) / (int64_t)blockDim.x);
+                __syncthreads();
+                if (tid == 0) run_i = 0;
+                __syncthreads();
+                const int64_t T = t_lo + (int64_t)tid * step;
+                const bool feas = T <= t_hi && columns(T) <= gx;
+                // the smallest feasible candidate (candidates increase with tid)
+                scan_i[tid] = feas ? tid : (int32_t)blockDim.x;
+                __syncthreads();
+                for (int32_t d = (int32_t)blockDim.x / 2; d > 0; d >>= 1) {
+                    if (tid < d) scan_i[tid] = min(scan_i[tid], scan_i[tid + d]);
+                    __syncthreads();
+                }
+                if (tid == 0) {
+                    const int32_t w = scan_i[0];
+                    if (w < (int32_t)blockDim.x) {
+                        run_u = t_lo + (int64_t)w * step;          // feasible
+                        tot = w > 0 ? t_lo + (int64_t)(w - 1) * step + 1 : t_lo;
+                    } else {
+                        tot = t_lo + (int64_t)(blockDim.x - 1) * step + 1;
+                    }
+                }
+                __syncthreads();
+            }
+            if (tid == 0) {
+                const int64_t T = run_u;
                 int32_t x = 0, nitem = 0;
                 int64_t acc = 0;
                 auto emit = [&](int32_t b, int32_t t0, int32_t t1) {
@@ -178,15 +230,13 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                     } else {
                         int64_t done = 0;
                         while (done < pairs) {
-                            if (acc > 0 && acc + C >= T && x < gx - 1) {   // this column is full
+                            const int64_t room = T - acc - C;
+                            if (room < 1 && x < gx - 1) {   // this column is full
                                 ++x;
                                 acc = 0;
+                                continue;
                             }
-                            int64_t take = pairs - done;
-                            if (x < gx - 1) {
-                                take = min(take, max((int64_t)1, T - acc - C));
-                                if (pairs - done - take < C) take = pairs - done;   // no tiny tail item
-                            }
+                            const int64_t take = x < gx - 1 ? min(pairs - done, room) : pairs - done;
                             emit(b, (int32_t)(2 * done), (int32_t)min((int64_t)cnt, 2 * (done + take)));
                             ++nseg;
                             done += take;
