@@ -99,6 +99,11 @@ struct __align__(16) Aux {
 
 constexpr size_t SMEM_BYTES = OFF_AUX + sizeof(Aux);
 
+// Output staging at the CTA's last item, in the K ring: per softmax warp 32 rows
+// of 64 floats, padded so that the lanes' 16-byte writes fall in distinct banks.
+constexpr int STG_STRIDE = 68;
+static_assert(8 * 32 * STG_STRIDE * 4 <= KSTAGES * TILEB, "output staging exceeds the K ring");
+
 __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, volatile int32_t *fail) {
     if (kvd::mbar_try_wait(bar, parity)) return true;
     long long t0 = clock64();
@@ -168,7 +173,7 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 __device__ __forceinline__ bool warp_ok(volatile int32_t *fail) { return __all_sync(0xffffffffu, *fail == 0); }
 
 struct ItemInfo {
-    int32_t block, t0, t1, pairs, nitems;
+    int32_t block, t0, t1, pairs;
 };
 
 __device__ __forceinline__ ItemInfo item_info(const kvk::PrefillArgs &a, int32_t wi) {
@@ -178,7 +183,6 @@ __device__ __forceinline__ ItemInfo item_info(const kvk::PrefillArgs &a, int32_t
     r.t0 = w.t0;
     r.t1 = w.t1;
     r.pairs = (w.t1 - w.t0 + 1) / 2;
-    r.nitems = a.p.blk_nitems[w.block];
     return r;
 }
 
@@ -248,11 +252,12 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         // issued.  V has its own warp: these dependent global reads never hold up a
         // V copy.
         const int32_t lane = tid & 31;
-        int32_t total = 0;
-        for (int32_t wi = i0; wi < i1; ++wi) total += item_info(a, wi).pairs;
+        // (no pass over the items first: the first K copy waits on as few dependent
+        // global reads as possible -- work item, tile list, flags)
         int32_t kc = 0;
         int32_t kwi = i0, kj = 0;              // K cursor: item and pair within it
         ItemInfo kit{};
+        int32_t kit_wi = -1;                   // the item kit describes
         kvi::DevBlock kb{};
         bool have_k = false;
         int32_t tt[2] = {-1, -1};
@@ -260,18 +265,22 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         bool mhas[4] = {false, false, false, false}, many[4] = {false, false, false, false};
         int32_t mpos[4] = {0, 0, 0, 0};
         long long t_last = clock64();
-        while (kc < total) {
+        while (true) {
             if (!warp_ok(fail)) break;
             bool prog = false;
             {
                 if (!have_k) {
                     // the next K load's global reads, done before its slot is free
-                    while (true) {
-                        kit = item_info(a, kwi);
+                    while (kwi < i1) {
+                        if (kit_wi != kwi) {
+                            kit = item_info(a, kwi);
+                            kit_wi = kwi;
+                        }
                         if (kj < kit.pairs) break;
                         ++kwi;
                         kj = 0;
                     }
+                    if (kwi >= i1) break;      // every pair of every item is loaded
                     kb = a.u.blocks[kit.block];
                     const int32_t *list = a.p.tiles + (int64_t)kit.block * a.p.tile_stride;
                     const uint32_t *flg = a.p.flags + (int64_t)kit.block * a.p.tile_stride;
@@ -483,6 +492,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         bool dep_done = false;                 // waited for the previous kernel of the stream
         for (int32_t wi = i0; wi < i1 && ok && warp_ok(fail); ++wi) {
             const ItemInfo it = item_info(a, wi);
+            const int32_t nitems = a.p.blk_nitems[it.block];   // used at the item's end
             // the query vector behind my TMEM lane (an empty item has a block that sees
             // no cell: zeros, or an empty partial), fetched here rather than from the
             // producer so that Q starts loading as early as possible
@@ -665,7 +675,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             ++n_l;
             float *dst = nullptr;
             float sc = 1.f;
-            if (it.nitems == 1) {
+            if (nitems == 1) {
                 if (live) dst = a.o + ((int64_t)row * a.n_head + h) * 128 + 64 * ch;
                 sc = l_tot > 0.f ? 1.f / l_tot : 0.f;
             } else {
@@ -678,24 +688,57 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 }
                 dst = pp + 4 + 64 * ch;
             }
+            if (wi + 1 == i1) {
+                // The CTA's last item: the K ring is idle (every S has completed), so each
+                // warp stages its 32 rows there and writes them out row by row, 16 lanes
+                // per row (whole 32-byte sectors), instead of one row per lane.
+                float *stg = reinterpret_cast<float *>(smem + OFF_K) + warp * (32 * STG_STRIDE);
 #pragma unroll 1
-            for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t r[32];
-                if (it.pairs > 0) {              // item-uniform: the TMEM read stays warp collective
-                    tc::ld32(o_mine + 32u * (uint32_t)q2, r);
-                } else {
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    uint32_t r[32];
+                    if (it.pairs > 0) {          // item-uniform: the TMEM read stays warp collective
+                        tc::ld32(o_mine + 32u * (uint32_t)q2, r);
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) r[c] = 0u;
+                        for (int c = 0; c < 32; ++c) r[c] = 0u;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        *reinterpret_cast<float4 *>(stg + (tid & 31) * STG_STRIDE + 32 * q2 + c) =
+                            make_float4(__uint_as_float(r[c + 0]) * sc, __uint_as_float(r[c + 1]) * sc,
+                                        __uint_as_float(r[c + 2]) * sc, __uint_as_float(r[c + 3]) * sc);
                 }
-                if (dst) {
+                __syncwarp();
+                const int32_t lane = tid & 31, part = lane & 15;
+#pragma unroll 4
+                for (int i = 0; i < 16; ++i) {
+                    const int32_t rr = 2 * i + (lane >> 4);   // the warp's row (its lane)
+                    float *d = reinterpret_cast<float *>(
+                        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(dst), rr));
+                    if (d)
+                        *reinterpret_cast<float4 *>(d + 4 * part) =
+                            *reinterpret_cast<const float4 *>(stg + rr * STG_STRIDE + 4 * part);
+                }
+            } else {
+#pragma unroll 1
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    uint32_t r[32];
+                    if (it.pairs > 0) {          // item-uniform: the TMEM read stays warp collective
+                        tc::ld32(o_mine + 32u * (uint32_t)q2, r);
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < 32; c += 4) {
-                        float4 v;
-                        v.x = __uint_as_float(r[c + 0]) * sc;
-                        v.y = __uint_as_float(r[c + 1]) * sc;
-                        v.z = __uint_as_float(r[c + 2]) * sc;
-                        v.w = __uint_as_float(r[c + 3]) * sc;
-                        *reinterpret_cast<float4 *>(dst + 32 * q2 + c) = v;
+                        for (int c = 0; c < 32; ++c) r[c] = 0u;
+                    }
+                    if (dst) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 4) {
+                            float4 v;
+                            v.x = __uint_as_float(r[c + 0]) * sc;
+                            v.y = __uint_as_float(r[c + 1]) * sc;
+                            v.z = __uint_as_float(r[c + 2]) * sc;
+                            v.w = __uint_as_float(r[c + 3]) * sc;
+                            *reinterpret_cast<float4 *>(dst + 32 * q2 + c) = v;
+                        }
                     }
                 }
             }
