@@ -70,6 +70,12 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 
 # workloads whose measured calls hold one decode row per sequence
+# DRAM bytes (read + write) of one k_decode launch of the 256-sequence workload,
+# from an ncu capture of the current kernel (profiles/k_decode_llama8b-decode-256seq-
+# lognormal.md; a launch at decode step 2, 3.519 GB algorithmic).  Cleared to nothing
+# whenever the kernel changes until it is captured again.
+DECODE_TRAFFIC = {5: 3556000000}
+
 DECODE_BOUND = {3: True, 5: True}
 
 
@@ -391,7 +397,8 @@ def run_ours(args, rank, world, device):
         moved = sum(b for _, _, b in res)
         achieved = moved / secs / 1e9 if durs else 0.0
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": None, "kernel": "ubatch_attention (k_decode)",
+                "frac": round(achieved / hbm, 4), "traffic": DECODE_TRAFFIC.get(cfg["id"]),
+                "kernel": "ubatch_attention (k_decode)",
                 "algorithmic_bytes_per_launch": int(moved / max(1, len(durs)))}
     else:
         per_pair_flops = 4 * arm.d * arm.H
