@@ -275,11 +275,13 @@ int device_init(kv_cache *c) {
         (e = dev_alloc(d, &p.blk_nitems, d->max_blocks)) != cudaSuccess ||
         (e = dev_alloc(d, &p.counters, (size_t)d->max_blocks * hkv)) != cudaSuccess ||
         (e = dev_alloc(d, &p.cta_item0, (size_t)d->gx_dec + d->gx_pf + 2)) != cudaSuccess ||
+        (e = dev_alloc(d, &p.pf_rows, (size_t)d->gx_pf * 128)) != cudaSuccess ||
         (e = dev_alloc(d, &d->d_part_dec, (size_t)p.cap_dec * hkv * DEC_PART_FLOATS)) != cudaSuccess ||
         (e = dev_alloc(d, &d->d_part_pf, (size_t)p.cap_pf * hkv * PF_PART_FLOATS)) != cudaSuccess ||
         (e = dev_alloc(d, &d->d_err, 1)) != cudaSuccess)
         return cuda_fail(c, e, "plan alloc");
     p.err = d->d_err;
+    p.gqa = c->gqa;
     if ((e = cudaMemset(p.counters, 0, (size_t)d->max_blocks * hkv * sizeof(int32_t))) != cudaSuccess ||
         (e = cudaMemset(d->d_err, 0, sizeof(int32_t))) != cudaSuccess)
         return cuda_fail(c, e, "plan clear");

@@ -253,6 +253,18 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                     cta0[xx] = i;
                 }
             }
+            __syncthreads();   // items and cta0 written by thread 0 are visible below
+            // the rows behind each column's first item, one entry per query vector
+            for (int32_t e = tid; e < (int32_t)gx * 128; e += blockDim.x) {
+                const int32_t x = e >> 7, qv = e & 127;
+                const int32_t i = cta0[x];
+                int32_t r = -1;
+                if (i < cta0[x + 1]) {
+                    const kvi::DevBlock b = u.blocks[p.work[item_base + i].block];
+                    if (qv < b.n_rows * p.gqa) r = u.perm[b.row0 + qv / p.gqa];
+                }
+                p.pf_rows[e] = r;
+            }
             __syncthreads();
             continue;
         }

@@ -43,8 +43,11 @@ namespace {
 
 using kvi::TILE;
 
-constexpr int NSM = 256;                 // softmax threads: two per TMEM lane
+constexpr int NSM = 512;                 // softmax threads: four per TMEM lane
 constexpr int NT = NSM + 96;             // + K producer, MMA and V producer warps
+constexpr int W_K = NSM / 32;            // K producer warp
+constexpr int W_MMA = W_K + 1;           // TMEM allocation and MMA issue
+constexpr int W_V = W_K + 2;             // V producer warp
 constexpr int M = 128;
 constexpr int HALF = 128 * 128;          // [128 rows][64 fp16], 128-byte rows
 constexpr int TILEB = 2 * HALF;          // 32 KiB
@@ -87,22 +90,22 @@ struct __align__(16) Aux {
     uint64_t meta_full[MSLOTS];
     uint64_t s_full[2], p_full[2], pv_done[2], q_full, spare;   // p_full, pv_done [g & 1]: pair g
     uint64_t lbar;            // the halves' row-sum exchange at each item's end, all 256 threads
-    uint64_t pbar[4];         // per lane quarter: the two warps of a row exchange maxima per pair
+    uint64_t pbar[4];         // per lane quarter: the four warps of a row exchange maxima per pair
     uint32_t tmem_base;
     int32_t fail;
     int32_t flag;
     int32_t pad;
     Meta meta[MSLOTS];
-    float red[2][2][M];       // [pair parity][cell half][row]: partial row maxima
-    float lex[2][2][M];       // [item parity][cell half][row]: row sums
+    float red[2][4][M];       // [pair parity][cell quarter][row]: partial row maxima
+    float lex[2][4][M];       // [item parity][cell quarter][row]: row sums
 };
 
 constexpr size_t SMEM_BYTES = OFF_AUX + sizeof(Aux);
 
 // Output staging at the CTA's last item, in the K ring: per softmax warp 32 rows
-// of 64 floats, padded so that the lanes' 16-byte writes fall in distinct banks.
-constexpr int STG_STRIDE = 68;
-static_assert(8 * 32 * STG_STRIDE * 4 <= KSTAGES * TILEB, "output staging exceeds the K ring");
+// of 32 floats, padded so that the lanes' 16-byte writes fall in distinct banks.
+constexpr int STG_STRIDE = 36;
+static_assert((NSM / 32) * 32 * STG_STRIDE * 4 <= KSTAGES * TILEB, "output staging exceeds the K ring");
 
 __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, volatile int32_t *fail) {
     if (kvd::mbar_try_wait(bar, parity)) return true;
@@ -231,11 +234,11 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         kvd::mbar_init(&x.q_full, NSM);
         kvd::mbar_init(&x.spare, 1);
         kvd::mbar_init(&x.lbar, NSM);
-        for (int q = 0; q < 4; ++q) kvd::mbar_init(&x.pbar[q], 64);
+        for (int q = 0; q < 4; ++q) kvd::mbar_init(&x.pbar[q], 128);
         x.fail = 0;
         kvd::fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == W_MMA) {
         tc::alloc(&x.tmem_base, TMEM_COLS);
         tc::relinquish();
     }
@@ -244,7 +247,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     tc::fence_after();
     const uint32_t tmem = x.tmem_base;
 
-    if (warp == 8) {
+    if (warp == W_K) {
         // ===================== K producer (whole warp) =====================
         // K of pair g + KSTAGES loads as soon as S of pair g has read K of g.  Each
         // pair's list entries, flags and per-cell visibility are fetched while the K
@@ -379,7 +382,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             for (int32_t q = kc > KSTAGES ? kc - KSTAGES : 0; q < kc; ++q)
                 (void)kvd::mbar_wait_bounded(&x.k_full[q % KSTAGES], (uint32_t)(q / KSTAGES) & 1u);
         }
-    } else if (warp == 10) {
+    } else if (warp == W_V) {
         // ===================== V producer (whole warp) =====================
         // V of pair g + 3 loads as soon as PV of g is done; the tile coordinates come
         // from the pair's metadata, published by the K producer before its K copy.
@@ -412,7 +415,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             for (int32_t q = vc > VSTAGES ? vc - VSTAGES : 0; q < vc; ++q)
                 (void)kvd::mbar_wait_bounded(&x.v_full[q % VSTAGES], (uint32_t)(q / VSTAGES) & 1u);
         }
-    } else if (warp == 9) {
+    } else if (warp == W_MMA) {
         // ===================== MMA issuer =====================
         // The tensor core's work per item is a fixed sequence: S_0, S_1, then for
         // each pair j: PV_j, S_j+2 (S_j+2 goes to the score buffer of pair j, whose P
@@ -455,10 +458,11 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     const uint32_t v_addr = sbase + OFF_V + (gp % VSTAGES) * TILEB;
                     const uint32_t p_tmem = tmem + 128u * (uint32_t)(j & 1);
                     // O += P V over the 128 cells: P of cells 16kk .. 16kk + 15 is 8 TMEM
-                    // columns at 64 (kk / 4) + 8 (kk % 4) of the score buffer
+                    // columns at 32 (kk / 2) + 8 (kk % 2) of the score buffer (each softmax
+                    // thread writes its 32 cells' P at the start of its own 32 S columns)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        tc::mma_ts(tmem + COL_O, p_tmem + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3),
+                        tc::mma_ts(tmem + COL_O, p_tmem + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1),
                                    tc::sdesc_sw128(v_addr + (uint32_t)kk * 2048u, HALF, 1024), IDESC_PV,
                                    (j > 0 || kk > 0) ? 1u : 0u);
                     }
@@ -473,17 +477,17 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             (void)kvd::mbar_wait_bounded(&x.spare, 0);
         }
     } else {
-        // ============ softmax / correction / epilogue (warps 0-7, two threads per row) ============
-        // Warps w and w + 4 share TMEM lane quarter w: thread (n, ch) owns cells
-        // 64ch .. 64ch + 63 of every pair tile of row n and d = 64ch .. 64ch + 63 of
-        // O.  The two threads of a row exchange their maxima once per pair through
-        // an mbarrier of their two warps (arrive, then a bounded wait, never bar.sync:
-        // if a wait elsewhere gives up, the partner times out instead of hanging).
+        // ============ softmax / correction / epilogue (warps 0-15, four threads per row) ============
+        // Warps w, w + 4, w + 8 and w + 12 share TMEM lane quarter w: thread (n, qd) owns
+        // cells 32qd .. 32qd + 31 of every pair tile of row n and d = 32qd .. 32qd + 31
+        // of O.  The four threads of a row exchange their maxima once per pair through
+        // an mbarrier of their four warps (arrive, then a bounded wait, never bar.sync:
+        // if a wait elsewhere gives up, the partners time out instead of hanging).
         const int32_t n = tid & 127;           // TMEM lane = query vector
-        const int32_t ch = tid >> 7;           // cell half, and d half of O
+        const int32_t qd = tid >> 7;           // cell quarter, and d quarter of O
         const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t s_mine = tmem + lane_q + (uint32_t)(64 * ch);   // + 128 * score buffer
-        const uint32_t o_mine = tmem + lane_q + COL_O + (uint32_t)(64 * ch);
+        const uint32_t s_mine = tmem + lane_q + (uint32_t)(32 * qd);   // + 128 * score buffer
+        const uint32_t o_mine = tmem + lane_q + COL_O + (uint32_t)(32 * qd);
         uint64_t *pbar = &x.pbar[warp & 3];
         uint32_t n_s[2] = {0, 0};
         uint32_t n_l = 0, n_p = 0;
@@ -497,39 +501,39 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             // no cell: zeros, or an empty partial), fetched here rather than from the
             // producer so that Q starts loading as early as possible
             int32_t row = -1, rpos = 0;
-            {
+            if (wi == i0) {
+                row = a.p.pf_rows[blockIdx.x * M + n];   // written by the planner
+            } else {
                 const kvi::DevBlock b = a.u.blocks[it.block];
-                if (n < b.n_rows * G) {
-                    row = a.u.perm[b.row0 + n / G];
-                    rpos = a.u.rows[row].pos;
-                }
+                if (n < b.n_rows * G) row = a.u.perm[b.row0 + n / G];
             }
+            if (row >= 0) rpos = a.u.rows[row].pos;
             const bool live = row >= 0;
             const int32_t h = hk * G + (n % G);
             if (!dep_done) {   // before the first read of Q and the first write of an output
-                // warm L2 with my 128 bytes of Q while the previous kernel finishes (a
+                // warm L2 with my 64 bytes of Q while the previous kernel finishes (a
                 // prefetch returns nothing, so racing its writes is harmless)
-                if (live && it.pairs > 0) kvd::prefetch_l2(a.q + ((int64_t)row * a.n_head + h) * 128 + 64 * ch);
+                if (live && it.pairs > 0) kvd::prefetch_l2(a.q + ((int64_t)row * a.n_head + h) * 128 + 32 * qd);
                 kvd::pdl_wait();
                 dep_done = true;
             }
-            float m_run = -INFINITY, l_run = 0.f;   // the row's running maximum, this half's row sum
+            float m_run = -INFINITY, l_run = 0.f;   // the row's running maximum, this quarter's row sum
             if (it.pairs > 0) {
-            // ---- Q into TMEM (the A operand of S = Q K^T): row n, d-half ch, fp16,
+            // ---- Q into TMEM (the A operand of S = Q K^T): row n, d quarter qd, fp16,
             //      two values per 32-bit column ----
             {
                 const uint4 *src =
-                    reinterpret_cast<const uint4 *>(a.q + ((int64_t)(live ? row : 0) * a.n_head + h) * 128 + 64 * ch);
-                uint32_t qw[32];
+                    reinterpret_cast<const uint4 *>(a.q + ((int64_t)(live ? row : 0) * a.n_head + h) * 128 + 32 * qd);
+                uint32_t qw[16];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     const uint4 v = live ? src[c] : make_uint4(0, 0, 0, 0);
                     qw[4 * c + 0] = v.x;
                     qw[4 * c + 1] = v.y;
                     qw[4 * c + 2] = v.z;
                     qw[4 * c + 3] = v.w;
                 }
-                tc::st32(tmem + lane_q + COL_Q + 32u * (uint32_t)ch, qw);
+                tc::st16(tmem + lane_q + COL_Q + 16u * (uint32_t)qd, qw);
                 tc::wait_st();
                 tc::fence_before();
                 kvd::mbar_arrive(&x.q_full);
@@ -544,53 +548,54 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 if (!ok) break;
                 ++n_s[j & 1];
                 tc::fence_after();
-                // ---- my 64 columns of S -> registers (one TMEM read, warp collective);
+                // ---- my 32 columns of S -> registers (one TMEM read, warp collective);
                 //      masked -> -inf ----
                 const uint32_t s_addr = s_mine + (uint32_t)(j & 1) * 128u;
-                uint32_t sb[64];
-                tc::ld64(s_addr, sb);
-                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                uint32_t sb[32];
+                tc::ld32(s_addr, sb);
                 if (!live) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) sb[c] = __float_as_uint(-INFINITY);
+                    for (int c = 0; c < 32; ++c) sb[c] = __float_as_uint(-INFINITY);
                 } else if (!full) {
-                    // which of my 64 cells this row sees, built in a rolled loop (this path
-                    // runs on a few tiles per item: its code is kept small), then applied
-                    // (16-byte loads, all issued before any test)
-                    uint4 hb[4];
-                    int4 cp[16];
-                    const uint4 *hs = reinterpret_cast<const uint4 *>(&mt.has[64 * ch]);
-                    const int4 *cs = reinterpret_cast<const int4 *>(&mt.cpos[64 * ch]);
+                    // which of my 32 cells this row sees (16-byte loads, all issued before
+                    // any test), applied as a 32-bit mask
+                    uint4 hb[2];
+                    int4 cp[8];
+                    const uint4 *hs = reinterpret_cast<const uint4 *>(&mt.has[32 * qd]);
+                    const int4 *cs = reinterpret_cast<const int4 *>(&mt.cpos[32 * qd]);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) hb[q] = hs[q];
+                    for (int q = 0; q < 2; ++q) hb[q] = hs[q];
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) cp[q] = cs[q];
+                    for (int q = 0; q < 8; ++q) cp[q] = cs[q];
                     const int32_t lim = a.u.causal ? rpos : INT32_MAX;
-                    uint64_t vm = 0;
+                    uint32_t vm = 0;
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
+                    for (int q = 0; q < 8; ++q) {
                         const uint32_t hw = (&hb[q >> 2].x)[q & 3];   // has of cells 4q .. 4q + 3
                         const int32_t c4[4] = {cp[q].x, cp[q].y, cp[q].z, cp[q].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const bool vis = ((hw >> (8 * e)) & 0xffu) != 0 && c4[e] <= lim;
-                            vm |= (uint64_t)vis << (4 * q + e);
+                            vm |= (uint32_t)vis << (4 * q + e);
                         }
                     }
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        sb[c] = ((vm >> c) & 1ull) ? sb[c] : __float_as_uint(-INFINITY);
+                    for (int c = 0; c < 32; ++c)
+                        sb[c] = ((vm >> c) & 1u) ? sb[c] : __float_as_uint(-INFINITY);
                 }
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < 64; c += 2)
+                for (int c = 0; c < 32; c += 2)
                     mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(sb[c]), __uint_as_float(sb[c + 1]));
-                // ---- the row maximum over both halves (partner: the same lane of warp w ^ 4) ----
-                x.red[j & 1][ch][n] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                // ---- the row maximum over the four quarters (partners: the same lane of
+                //      warps w, w + 4, w + 8, w + 12) ----
+                x.red[j & 1][qd][n] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                 kvd::mbar_arrive(pbar);
                 ok = __all_sync(0xffffffffu, wait_or_fail(pbar, n_p & 1u, fail));
                 ++n_p;
                 if (!ok) break;
-                const float tmax = fmaxf(x.red[j & 1][0][n], x.red[j & 1][1][n]) * a.scale_log2;
+                const float tmax = fmaxf(fmaxf(x.red[j & 1][0][n], x.red[j & 1][1][n]),
+                                         fmaxf(x.red[j & 1][2][n], x.red[j & 1][3][n])) * a.scale_log2;
                 const float m_new = fmaxf(m_run, tmax);
                 const bool grow = m_new > m_run + RESCALE_LOG2 || (m_run == -INFINITY && m_new != -INFINITY);
                 float alpha = 1.f;
@@ -599,18 +604,18 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     m_run = m_new;
                     l_run *= alpha;
                 }
-                // ---- P = 2^(s*scale - m) as fp16 over the S columns just read: my 64
-                //      cells are 32 columns (two fp16 per column, lower cell in the low
-                //      half); one exponential in four on the FMA pipe ----
+                // ---- P = 2^(s*scale - m) as fp16 at the start of my S columns: my 32 cells
+                //      are 16 columns (two fp16 per column, lower cell in the low half);
+                //      one exponential in four on the FMA pipe ----
                 {
                     // no maximum yet (nothing visible so far, or a lane past the block):
                     // subtract +inf so that every exponent is -inf and P is 0
                     const float nm = m_run != -INFINITY ? -m_run : -INFINITY;
                     const uint64_t sc2 = pk2(a.scale_log2, a.scale_log2), nm2 = pk2(nm, nm);
                     uint64_t ls2[2] = {pk2(0.f, 0.f), pk2(0.f, 0.f)};
-                    uint32_t pw[32];
+                    uint32_t pw[16];
 #pragma unroll
-                    for (int c2 = 0; c2 < 32; ++c2) {
+                    for (int c2 = 0; c2 < 16; ++c2) {
                         const int c = 2 * c2;
                         float x0, x1;
                         upk2(ffma2(pk2(__uint_as_float(sb[c]), __uint_as_float(sb[c + 1])), sc2, nm2), x0, x1);
@@ -624,32 +629,28 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     upk2(ls2[0], la, lb);
                     upk2(ls2[1], lc, ld);
                     l_run += (la + lb) + (lc + ld);
-                    tc::st32(s_addr, pw);
+                    tc::st16(s_addr, pw);
                 }
-                // ---- O *= alpha where the row's running maximum moved (rare), my 64
+                // ---- O *= alpha where the row's running maximum moved (rare), my 32
                 //      columns; O is stable once PV of pair k - 1 finished ----
                 if (j > 0 && __any_sync(0xffffffffu, grow)) {
                     ok = __all_sync(0xffffffffu,
                                     wait_or_fail(&x.pv_done[(k - 1) & 1], (uint32_t)((k - 1) >> 1) & 1u, fail));
                     if (!ok) break;
                     tc::fence_after();
-#pragma unroll 1
-                    for (int q2 = 0; q2 < 2; ++q2) {
-                        uint32_t r[32];
-                        const uint32_t ta = o_mine + (uint32_t)q2 * 32u;
-                        tc::ld32(ta, r);
+                    uint32_t r[32];
+                    tc::ld32(o_mine, r);
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-                        tc::st32(ta, r);
-                    }
+                    for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+                    tc::st32(o_mine, r);
                 }
-                if (!full) {
+                if (!full && qd < 2) {
                     // V rows of cells nobody in the block sees: zero (P is 0 there; V may
-                    // be garbage); thread (n, ch) clears d-half ch of cell n
+                    // be garbage); thread (n, qd < 2) clears d half qd of cell n
                     ok = __all_sync(0xffffffffu, wait_or_fail(&x.v_full[st], (uint32_t)(k / VSTAGES) & 1u, fail));
                     if (!ok) break;
                     if (!mt.anyvis[n]) {
-                        uint8_t *vs = smem + OFF_V + st * TILEB + ch * HALF + n * 128;
+                        uint8_t *vs = smem + OFF_V + st * TILEB + qd * HALF + n * 128;
 #pragma unroll
                         for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(vs + c * 16) = make_uint4(0, 0, 0, 0);
                     }
@@ -666,80 +667,66 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             if (!ok) break;
             tc::fence_after();
             }   // it.pairs > 0
-            // ---- the row sum over both halves (double-buffered by item parity) ----
-            x.lex[n_l & 1][ch][n] = l_run;
+            // ---- the row sum over the four quarters (double-buffered by item parity) ----
+            x.lex[n_l & 1][qd][n] = l_run;
             kvd::mbar_arrive(&x.lbar);
             ok = __all_sync(0xffffffffu, wait_or_fail(&x.lbar, n_l & 1u, fail));
             if (!ok) break;
-            const float l_tot = x.lex[n_l & 1][0][n] + x.lex[n_l & 1][1][n];
+            const float l_tot = (x.lex[n_l & 1][0][n] + x.lex[n_l & 1][1][n]) +
+                                (x.lex[n_l & 1][2][n] + x.lex[n_l & 1][3][n]);
             ++n_l;
             float *dst = nullptr;
             float sc = 1.f;
             if (nitems == 1) {
-                if (live) dst = a.o + ((int64_t)row * a.n_head + h) * 128 + 64 * ch;
+                if (live) dst = a.o + ((int64_t)row * a.n_head + h) * 128 + 32 * qd;
                 sc = l_tot > 0.f ? 1.f / l_tot : 0.f;
             } else {
                 // a split block: this item's partial (its slot is its index among the
                 // prefill items); k_merge_pf combines the partials after the kernel
                 float *pp = a.part + (((int64_t)wi * a.n_head_kv + hk) * M + n) * PART_STRIDE;
-                if (ch == 0) {
+                if (qd == 0) {
                     pp[0] = m_run;
                     pp[1] = l_tot;
                 }
-                dst = pp + 4 + 64 * ch;
+                dst = pp + 4 + 32 * qd;
+            }
+            uint32_t r[32];
+            if (it.pairs > 0) {                  // item-uniform: the TMEM read stays warp collective
+                tc::ld32(o_mine, r);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) r[c] = 0u;
             }
             if (wi + 1 == i1) {
                 // The CTA's last item: the K ring is idle (every S has completed), so each
-                // warp stages its 32 rows there and writes them out row by row, 16 lanes
-                // per row (whole 32-byte sectors), instead of one row per lane.
+                // warp stages its 32 rows there and writes them out row by row, 8 lanes
+                // per 128-byte row, instead of one row per lane.
                 float *stg = reinterpret_cast<float *>(smem + OFF_K) + warp * (32 * STG_STRIDE);
-#pragma unroll 1
-                for (int q2 = 0; q2 < 2; ++q2) {
-                    uint32_t r[32];
-                    if (it.pairs > 0) {          // item-uniform: the TMEM read stays warp collective
-                        tc::ld32(o_mine + 32u * (uint32_t)q2, r);
-                    } else {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) r[c] = 0u;
-                    }
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4)
-                        *reinterpret_cast<float4 *>(stg + (tid & 31) * STG_STRIDE + 32 * q2 + c) =
-                            make_float4(__uint_as_float(r[c + 0]) * sc, __uint_as_float(r[c + 1]) * sc,
-                                        __uint_as_float(r[c + 2]) * sc, __uint_as_float(r[c + 3]) * sc);
-                }
+                for (int c = 0; c < 32; c += 4)
+                    *reinterpret_cast<float4 *>(stg + (tid & 31) * STG_STRIDE + c) =
+                        make_float4(__uint_as_float(r[c + 0]) * sc, __uint_as_float(r[c + 1]) * sc,
+                                    __uint_as_float(r[c + 2]) * sc, __uint_as_float(r[c + 3]) * sc);
                 __syncwarp();
-                const int32_t lane = tid & 31, part = lane & 15;
+                const int32_t lane = tid & 31, part = lane & 7;
 #pragma unroll 4
-                for (int i = 0; i < 16; ++i) {
-                    const int32_t rr = 2 * i + (lane >> 4);   // the warp's row (its lane)
+                for (int i = 0; i < 8; ++i) {
+                    const int32_t rr = 4 * i + (lane >> 3);   // the warp's row (its lane)
                     float *d = reinterpret_cast<float *>(
                         __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(dst), rr));
                     if (d)
                         *reinterpret_cast<float4 *>(d + 4 * part) =
                             *reinterpret_cast<const float4 *>(stg + rr * STG_STRIDE + 4 * part);
                 }
-            } else {
-#pragma unroll 1
-                for (int q2 = 0; q2 < 2; ++q2) {
-                    uint32_t r[32];
-                    if (it.pairs > 0) {          // item-uniform: the TMEM read stays warp collective
-                        tc::ld32(o_mine + 32u * (uint32_t)q2, r);
-                    } else {
+            } else if (dst) {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) r[c] = 0u;
-                    }
-                    if (dst) {
-#pragma unroll
-                        for (int c = 0; c < 32; c += 4) {
-                            float4 v;
-                            v.x = __uint_as_float(r[c + 0]) * sc;
-                            v.y = __uint_as_float(r[c + 1]) * sc;
-                            v.z = __uint_as_float(r[c + 2]) * sc;
-                            v.w = __uint_as_float(r[c + 3]) * sc;
-                            *reinterpret_cast<float4 *>(dst + 32 * q2 + c) = v;
-                        }
-                    }
+                for (int c = 0; c < 32; c += 4) {
+                    float4 v;
+                    v.x = __uint_as_float(r[c + 0]) * sc;
+                    v.y = __uint_as_float(r[c + 1]) * sc;
+                    v.z = __uint_as_float(r[c + 2]) * sc;
+                    v.w = __uint_as_float(r[c + 3]) * sc;
+                    *reinterpret_cast<float4 *>(dst + c) = v;
                 }
             }
             tc::fence_before();
@@ -749,10 +736,11 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     tc::fence_before();
     __syncthreads();
     if (*fail && tid == 0) kvd::report(a.err, kvd::DERR_MMA_TIMEOUT);
-    if (warp == 9) {
+    if (warp == W_MMA) {
         tc::fence_after();
         tc::dealloc(tmem, TMEM_COLS);
     }
+
 }
 
 

@@ -22,9 +22,18 @@ __global__ void __launch_bounds__(256) k_store(uint4 *__restrict__ kc, uint4 *__
     // Launched as a programmatic dependent of the kernel before it: wait for it
     // before reading the rows (the caller may have just produced them) or
     // writing the cache; then let the attention kernel that follows set up.
+    // Until then, warm L2 with this thread's first 128-byte lines of K and V (a
+    // prefetch returns nothing, so racing the previous kernel's writes is harmless).
+    const int64_t total = (int64_t)n_tokens * chunks_per_row;
+    {
+        const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+        if (t0 < total && (t0 & 7) == 0) {
+            kvd::prefetch_l2(kin + t0);
+            kvd::prefetch_l2(vin + t0);
+        }
+    }
     kvd::pdl_wait();
     kvd::pdl_trigger();
-    const int64_t total = (int64_t)n_tokens * chunks_per_row;
     for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
          t += (int64_t)gridDim.x * blockDim.x) {
         const int32_t r = (int32_t)(t / chunks_per_row);

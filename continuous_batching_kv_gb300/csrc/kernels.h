@@ -52,9 +52,13 @@ struct Plan {
     int32_t *blk_nitems;    // [max_blocks]
     int32_t *counters;      // [max_blocks * n_head_kv] split-K completion counters
     int32_t *cta_item0;     // decode [gx_dec + 1], then prefill [gx_pf + 1]: each CTA column's items
+    int32_t *pf_rows;       // [gx_pf][128]: the ubatch row behind each query vector of each prefill
+                            // CTA column's first item (-1: none), so that Q loads without the
+                            // chain item -> block -> row permutation
     int32_t *err;
     int32_t tile_stride;
     int32_t cap_dec, cap_pf;
+    int32_t gqa;            // query heads per KV head
 };
 
 // k_store.cu

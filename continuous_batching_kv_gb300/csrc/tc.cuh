@@ -94,6 +94,14 @@ __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
         : "memory");
 }
 
+__device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+        ::"r"(taddr), KV_W8(0), KV_W8(8)
+        : "memory");
+}
+
 // 128 consecutive columns: four loads in flight, one wait.
 __device__ __forceinline__ void ld128(uint32_t taddr, uint32_t (&r)[128]) {
     asm volatile(
