@@ -185,13 +185,16 @@ class OursArm:
                             n_seq_max=prm["n_seq_max"], n_stream=prm["n_stream"], n_layer=self.L,
                             n_head=self.H, n_head_kv=self.Hk, head_dim=self.d,
                             seq_to_stream=prm.get("seq_to_stream"), k_layers=self.kc, v_layers=self.vc)
-        self.stream = torch.cuda.current_stream(device)
+        # a stream of its own (not the legacy default stream, which would serialise
+        # with the end-to-end mode's copy stream)
+        self.stream = torch.cuda.Stream(device)
         self.decode_loop = DECODE_BOUND.get(cfg["id"], False)
         self.step_no = -1
         self.gen = torch.Generator(device=device)
         self.gen.manual_seed(1234)
-        self._setup()
-        self._prepare_inputs()
+        with torch.cuda.stream(self.stream):   # inputs are made on the stream that uses them
+            self._setup()
+            self._prepare_inputs()
 
     def _randn(self, *shape):
         return self.torch.randn(*shape, generator=self.gen, device=self.dev, dtype=self.torch.float32).half()
@@ -240,10 +243,15 @@ class OursArm:
                 u = kv.kv_split_ubatch(s, k)
                 rows = list(u["rows"])
                 n = len(rows)
-                t = {"n": n,
-                     "q": [self._randn(n, self.H, self.d) for _ in range(self.L)],
-                     "k": [self._randn(n, self.Hk * self.d) for _ in range(self.L)],
-                     "v": [self._randn(n, self.Hk * self.d) for _ in range(self.L)],
+                # all layers' Q, K and V of the ubatch in one device buffer (the end-to-end
+                # mode copies it from the host in one piece); per layer: Q, K, V
+                lq, lk = n * self.H * self.d, n * self.Hk * self.d
+                per = lq + 2 * lk
+                buf = self._randn(self.L * per)
+                t = {"n": n, "dev": buf,
+                     "q": [buf[l * per:l * per + lq].view(n, self.H, self.d) for l in range(self.L)],
+                     "k": [buf[l * per + lq:l * per + lq + lk].view(n, self.Hk * self.d) for l in range(self.L)],
+                     "v": [buf[l * per + lq + lk:(l + 1) * per].view(n, self.Hk * self.d) for l in range(self.L)],
                      "o": self.torch.empty((n, self.H, self.d), dtype=self.torch.float32, device=self.dev),
                      "pairs": int(row_visible_cells([call["pos"][r] for r in rows]).sum()),
                      "bytes": self._kv_bytes(call, rows, n),
@@ -269,11 +277,19 @@ class OursArm:
         return int(kv_rows * 2 * self.Hk * self.d * 2 + n * self.H * self.d * (2 + 4))
 
     def input_bytes(self):
-        tot = 0
+        return sum(t["dev"].numel() * 2 for _, ubs, _ in self.calls for t in ubs)
+
+    def enable_host_inputs(self):
+        """End-to-end mode: a pinned host copy of every ubatch's input buffer, a
+        copy stream, and one event per ubatch."""
+        torch = self.torch
         for _, ubs, _ in self.calls:
             for t in ubs:
-                tot += sum(x.numel() * 2 for x in t["q"] + t["k"] + t["v"])
-        return tot
+                t["host"] = t["dev"].cpu().pin_memory()
+                t["in_ev"] = torch.cuda.Event()
+        self.copy_stream = torch.cuda.Stream(self.dev)
+        self.step_ev = torch.cuda.Event()
+        self.step_ev.record(self.stream)
 
     def reset(self):
         """Before a step: return the cache to its post-setup state, or, for the
@@ -305,24 +321,32 @@ class OursArm:
     def timed_calls_per_step(self):
         return sum(len(ubs) for _, ubs, _ in self.calls) * max(0, self.L - 1)
 
-    def step(self, timers=None, host=None):
+    def step(self, timers=None, host=False):
         """One pass of the whole path.  timers: an EventPool that brackets the
         attention calls that launch no planning kernels (layers >= 1).
-        host: pinned host copies of the inputs (end-to-end mode)."""
+        host: end-to-end mode -- every ubatch's inputs are copied from pinned host
+        memory on a copy stream (after the previous step's work, so the buffers
+        are free), the attention stream waits for each ubatch's copy, and each
+        ubatch's output is read back to the host."""
         kv, torch = self.kv, self.torch
         self.reset()
         last = []
         off = max(0, self.step_no) if self.decode_loop else 0
+        if host:
+            # the copies of this step overlap the compute of its earlier ubatches
+            self.copy_stream.wait_event(self.step_ev)
+            with torch.cuda.stream(self.copy_stream):
+                for _, ubs, _ in self.calls:
+                    for t in ubs:
+                        t["dev"].copy_(t["host"], non_blocking=True)
+                        t["in_ev"].record(self.copy_stream)
         for ci, (call, ubs, marsh) in enumerate(self.calls):
             s = kv.kv_split_ubatches(self.c, marsh[0] + off if off else marsh[0], marsh[1])
             assert kv.kv_prepare_cells(self.c, s) == 0
             for k, t in enumerate(ubs):
+                if host:
+                    self.stream.wait_event(t["in_ev"])
                 for layer in range(self.L):
-                    if host is not None:
-                        hq, hk_, hv = host[ci][k][layer]
-                        t["q"][layer].copy_(hq, non_blocking=True)
-                        t["k"][layer].copy_(hk_, non_blocking=True)
-                        t["v"][layer].copy_(hv, non_blocking=True)
                     kv.kv_store(self.c, s, k, layer, t["k"][layer], t["v"][layer], self.stream)
                     if timers is not None and layer > 0:
                         e0, e1 = timers.take(t["pairs"] + off * t["n"], t["bytes"] + off * t["row_kv_bytes"])
@@ -331,9 +355,12 @@ class OursArm:
                         e1.record(self.stream)
                     else:
                         kv.ubatch_attention(self.c, s, k, layer, t["q"][layer], t["o"], None, self.stream)
-                if host is not None:
-                    last.append(t["o"].to("cpu", non_blocking=True))
+                if host:
+                    with torch.cuda.stream(self.stream):
+                        last.append(t["o"].to("cpu", non_blocking=True))
             kv.kv_split_free(s)
+        if host:
+            self.step_ev.record(self.stream)
         return last
 
 
@@ -413,19 +440,14 @@ def run_ours(args, rank, world, device):
 
     e2e = None
     if not args.no_e2e:
-        host = []
-        for ci, (call, ubs, _) in enumerate(arm.calls):
-            hc = []
-            for t in ubs:
-                hc.append([(t["q"][l].cpu().pin_memory(), t["k"][l].cpu().pin_memory(),
-                            t["v"][l].cpu().pin_memory()) for l in range(arm.L)])
-            host.append(hc)
-        arm.step(host=host)
+        arm.enable_host_inputs()
+        arm.step(host=True)
         barrier()
         t0.record(arm.stream)
+        arm.step_ev.record(arm.stream)   # the first copies start inside the timed region
         out = None
         for _ in range(args.steps):
-            out = arm.step(host=host)
+            out = arm.step(host=True)
         t1.record(arm.stream)
         barrier()
         ms_e2e = t0.elapsed_time(t1)

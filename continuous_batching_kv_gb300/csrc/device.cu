@@ -28,13 +28,13 @@ struct DeviceState {
     uint32_t *d_epoch = nullptr;
     uint64_t *d_bits = nullptr;
     // uploads
-    Delta *d_delta = nullptr;
-    int32_t delta_cap = 0;
+    int32_t delta_cap = 0;                      // deltas the staging buffers hold without growing
     uint8_t *d_tables = nullptr;
     size_t tables_cap = 0;
     // two pinned staging buffers used in turn, so preparing a split never waits
     // for the upload of the one before it
-    uint8_t *h_stage[2] = {nullptr, nullptr};
+    uint8_t *h_stage[2] = {nullptr, nullptr};   // mapped pinned memory: the host writes, kernels read
+    uint8_t *d_stage[2] = {nullptr, nullptr};   // their device-visible addresses
     size_t stage_cap[2] = {0, 0};
     cudaEvent_t stage_ev[2] = {nullptr, nullptr};
     bool stage_pending[2] = {false, false};
@@ -164,35 +164,30 @@ int sync_device(kv_cache *c, const kv_split *sp, cudaStream_t st) {
     const size_t dbytes = nd * sizeof(Delta);
     const size_t tbytes = need_tables ? sp->image.size() : 0;
     if (tbytes > d->tables_cap) return c->set_err(KV_E_INVAL, "split tables exceed bound");
-    if (nd > (size_t)d->delta_cap) {   // rare (large removals): grow
-        Delta *nd_buf = nullptr;
-        if ((e = dev_alloc(d, &nd_buf, nd)) != cudaSuccess) return cuda_fail(c, e, "delta grow");
-        d->d_delta = nd_buf;
-        d->delta_cap = (int32_t)nd;
-    }
-    if (dbytes + tbytes > d->stage_cap[sl]) {
+    if (dbytes + tbytes > d->stage_cap[sl]) {   // rare (large removals): grow
         if (d->h_stage[sl]) cudaFreeHost(d->h_stage[sl]);
         d->h_stage[sl] = nullptr;
+        d->d_stage[sl] = nullptr;
         size_t cap = dbytes + tbytes;
-        if ((e = cudaHostAlloc((void **)&d->h_stage[sl], cap, cudaHostAllocDefault)) != cudaSuccess)
+        if ((e = cudaHostAlloc((void **)&d->h_stage[sl], cap, cudaHostAllocMapped)) != cudaSuccess ||
+            (e = cudaHostGetDevicePointer((void **)&d->d_stage[sl], d->h_stage[sl], 0)) != cudaSuccess)
             return cuda_fail(c, e, "stage grow");
         d->stage_cap[sl] = cap;
     }
     uint8_t *stage = d->h_stage[sl];
     if (nd) std::memcpy(stage, c->pending.data(), dbytes);
     if (tbytes) std::memcpy(stage + dbytes, sp->image.data(), tbytes);
+    // both uploads are kernels reading the mapped staging buffer (no copy engine)
     if (nd) {
-        if ((e = cudaMemcpyAsync(d->d_delta, stage, dbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
-            return cuda_fail(c, e, "delta upload");
-        if ((e = kvk::launch_apply_deltas(d->d_delta, (int32_t)nd, c->n_words, d->d_pos, d->d_epoch,
-                                          d->d_bits, st)) != cudaSuccess)
+        if ((e = kvk::launch_apply_deltas(reinterpret_cast<const Delta *>(d->d_stage[sl]), (int32_t)nd, c->n_words,
+                                          d->d_pos, d->d_epoch, d->d_bits, st)) != cudaSuccess)
             return cuda_fail(c, e, "apply deltas");
         c->launches += 1;
     }
     if (tbytes) {
-        if ((e = cudaMemcpyAsync(d->d_tables, stage + dbytes, tbytes, cudaMemcpyHostToDevice, st)) !=
-            cudaSuccess)
+        if ((e = kvk::launch_upload(d->d_stage[sl] + dbytes, d->d_tables, tbytes, st)) != cudaSuccess)
             return cuda_fail(c, e, "table upload");
+        c->launches += 1;
         c->dev_tables_split = sp->id;
         d->plan_split = 0;
         d->plan_ub = -1;
@@ -245,12 +240,12 @@ int device_init(kv_cache *c) {
         (e = cudaMemset(d->d_bits, 0, n_cells * c->n_words * sizeof(uint64_t))) != cudaSuccess)
         return cuda_fail(c, e, "mirror clear");
     d->delta_cap = std::max<int32_t>(c->n_batch, 4096);
-    if ((e = dev_alloc(d, &d->d_delta, d->delta_cap)) != cudaSuccess) return cuda_fail(c, e, "delta alloc");
     d->tables_cap = tables_bound(c);
     if ((e = dev_alloc(d, &d->d_tables, d->tables_cap)) != cudaSuccess) return cuda_fail(c, e, "table alloc");
     for (int sl = 0; sl < 2; ++sl) {
         d->stage_cap[sl] = d->tables_cap + (size_t)d->delta_cap * sizeof(Delta);
-        if ((e = cudaHostAlloc((void **)&d->h_stage[sl], d->stage_cap[sl], cudaHostAllocDefault)) != cudaSuccess)
+        if ((e = cudaHostAlloc((void **)&d->h_stage[sl], d->stage_cap[sl], cudaHostAllocMapped)) != cudaSuccess ||
+            (e = cudaHostGetDevicePointer((void **)&d->d_stage[sl], d->h_stage[sl], 0)) != cudaSuccess)
             return cuda_fail(c, e, "stage alloc");
         if ((e = cudaEventCreateWithFlags(&d->stage_ev[sl], cudaEventDisableTiming)) != cudaSuccess)
             return cuda_fail(c, e, "event");
@@ -466,7 +461,7 @@ bool sync_would_allocate(const kv_cache *c, const kv_split *sp) {
     const DeviceState *d = c->dev;
     const size_t nd = c->pending.size();
     const size_t tbytes = c->dev_tables_split != sp->id ? sp->image.size() : 0;
-    return nd > (size_t)d->delta_cap || nd * sizeof(Delta) + tbytes > d->stage_cap[d->stage_slot] ||
+    return nd * sizeof(Delta) + tbytes > d->stage_cap[d->stage_slot] ||
            tbytes > d->tables_cap;
 }
 

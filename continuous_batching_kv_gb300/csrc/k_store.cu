@@ -51,6 +51,17 @@ __global__ void __launch_bounds__(256) k_store(uint4 *__restrict__ kc, uint4 *__
     }
 }
 
+// Host -> device upload through mapped pinned memory: the kernel reads the host
+// buffer directly, so the upload does not queue on a copy engine behind the
+// caller's own transfers.  16-byte chunks, then the remaining bytes.
+__global__ void __launch_bounds__(256) k_upload(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                                int64_t n16, int32_t tail) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+    if (blockIdx.x == 0 && threadIdx.x < (unsigned)tail)
+        reinterpret_cast<uint8_t *>(dst + n16)[threadIdx.x] = reinterpret_cast<const uint8_t *>(src + n16)[threadIdx.x];
+}
+
 __global__ void k_apply_deltas(const kvi::Delta *__restrict__ d, int32_t n, int32_t n_words,
                                int32_t *pos, uint32_t *epoch, uint64_t *bits) {
     int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -84,6 +95,16 @@ cudaError_t launch_store(void *k_cache, void *v_cache, const void *k_cur, const 
     cudaError_t e = cudaLaunchKernelEx(&cfg, k_store, (uint4 *)k_cache, (uint4 *)v_cache, (const uint4 *)k_cur,
                                        (const uint4 *)v_cur, rows, n_tokens, cpr, n_cells, err);
     if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_upload(const void *src, void *dst, size_t bytes, cudaStream_t st) {
+    const int64_t n16 = (int64_t)(bytes / 16);
+    int64_t blocks = (n16 + 255) / 256;
+    if (blocks < 1) blocks = 1;
+    if (blocks > 152 * 4) blocks = 152 * 4;
+    k_upload<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n16,
+                                                (int32_t)(bytes % 16));
     return cudaGetLastError();
 }
 

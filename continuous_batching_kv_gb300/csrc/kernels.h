@@ -65,6 +65,8 @@ struct Plan {
 cudaError_t launch_store(void *k_cache, void *v_cache, const void *k_cur, const void *v_cur,
                          const kvi::DevRow *rows, int32_t n_tokens, int32_t row_bytes,
                          int64_t n_cells, int32_t *err, cudaStream_t st);
+// src: mapped pinned host memory (device-visible address); dst: device memory
+cudaError_t launch_upload(const void *src, void *dst, size_t bytes, cudaStream_t st);
 cudaError_t launch_apply_deltas(const kvi::Delta *d, int32_t n, int32_t n_words, int32_t *pos,
                                 uint32_t *epoch, uint64_t *bits, cudaStream_t st);
 
