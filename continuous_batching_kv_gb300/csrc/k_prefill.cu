@@ -6,29 +6,28 @@
 // not later) it is the same softmax(q K^T / sqrt(d) + mask) V as decode, but
 // now a dense contraction worth putting on the tensor cores.
 //
-// Design (sm_103a, one CTA of 352 threads per SM):
+// Design (sm_103a, one CTA of 608 threads per SM):
 //  * a block = up to 128 query vectors (rows sharing a stream and first
 //    sequence id, times the GQA group) = the 128 TMEM lanes of one MMA tile;
 //    a work item = one block, one KV head, a chunk of the block's list of
 //    visible 64-cell tiles, consumed two at a time (N = 128 cells);
-//  * warp 8 streams K tiles with TMA (128-byte swizzle) into a 2-slot ring,
+//  * warp 16 streams K tiles with TMA (128-byte swizzle) into a 3-slot ring,
 //    with each pair's list entries, flags and per-cell visibility fetched ahead
-//    into a metadata ring; warp 10 streams V tiles into a 3-slot ring; warp 9
-//    allocates TMEM and one thread issues
-//    tcgen05.mma: S = Q K^T (M 128, N 128, K 128) into one of two TMEM score
-//    buffers once the PV that read the P held there has completed, and
-//    O_h += P_h V_h for the two cell halves h, P_h read from TMEM (fp16, written
-//    over S) and V MN-major from shared memory; tcgen05.commit signals the
-//    mbarriers;
-//  * warps 0-7: thread (n, h) owns cells 64h .. 64h + 63 of query vector n
-//    (TMEM lane n) with its own running maximum, row sum and accumulator O_h;
-//    it reads its 64 columns of S with one tcgen05.ld as soon as they land,
-//    applies the mask per cell on tiles that are not fully visible, runs the
-//    online softmax in base 2 (a quarter of the exponentials on the FMA pipe),
-//    writes P (fp16, two cells per 32-bit column) over the S it read, and
-//    rescales O_h in TMEM only when its running maximum grew by more than 2^8
-//    (otherwise the stale maximum is kept; the final normalisation uses the
-//    same one); the two halves of a row combine their (m, l, O) once per item;
+//    into a metadata ring; warp 18 streams V tiles into a 3-slot ring; warp 17
+//    allocates TMEM and one of its threads issues tcgen05.mma in a fixed order
+//    (S_0, S_1, then PV_j and S_j+2 per pair, each after a blocking bounded
+//    wait): S = Q K^T (M 128, N 128, K 128; Q held in TMEM) into one of two
+//    TMEM score buffers, and O += P V with P read from TMEM (fp16, written over
+//    S) and V MN-major from shared memory; tcgen05.commit signals the mbarriers;
+//  * warps 0-15: thread (n, qd) owns cells 32qd .. 32qd + 31 of query vector n
+//    (TMEM lane n) and d = 32qd .. 32qd + 31 of O; it reads its 32 columns of S
+//    with one tcgen05.ld, applies the mask per cell on tiles that are not fully
+//    visible, exchanges the row maximum with the row's other three threads,
+//    runs the online softmax in base 2 (the exponent rounded to fp16, two
+//    exponentials per ex2.approx.f16x2), writes P (fp16, two cells per 32-bit
+//    column) at the start of the S columns it read, and rescales its part of O
+//    in TMEM only when the running maximum grew by more than 2^8 (otherwise the
+//    stale maximum is kept; the final normalisation uses the same one);
 //  * cells nobody in the block may see get their V rows zeroed in shared
 //    memory before the PV product (P is 0 there, but 0 * NaN would not be);
 //  * a block split over several CTAs leaves one partial (m, l, O) per piece,
@@ -128,25 +127,25 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// 2^x on the FMA pipe.  Range reduction: x = n + f with n = round(x) taken by
-// adding 1.5 * 2^23 (the integer lands in the low mantissa bits), f in
-// [-1/2, 1/2]; 2^f by a cubic 1 + f (c1 + f (c2 + f c3)) whose coefficients
-// were fitted here to minimise the maximum relative error on [-1/2, 1/2]
-// (about 1.0e-4, below the 4.9e-4 half-ulp of the fp16 P it feeds); 2^n is
-// added to the exponent field with one integer multiply-add.  x is clamped to
-// -127, where the result is exactly +0 (so is 2^-inf).
-__device__ __forceinline__ float ex2_poly(float x) {
-    constexpr float MAGIC = 12582912.0f;    // 1.5 * 2^23
-    constexpr float C1 = 6.932828051e-01f, C2 = 2.422090319e-01f, C3 = 5.500809860e-02f;
-    x = fmaxf(x, -127.0f);
-    const float t = x + MAGIC;
-    const float nf = t - MAGIC;
-    const float f = x - nf;
-    const float p = fmaf(f, fmaf(f, fmaf(f, C3, C2), C1), 1.0f);
-    return __uint_as_float(__float_as_uint(p) + (__float_as_uint(t) << 23));
+// {2^lo, 2^hi} as two fp16 in one 32-bit word (lo in the low half): the exponents
+// are rounded to fp16 first, then raised two at a time by the hardware's
+// approximate base-2 exponential (ex2.approx.f16x2; 2^-inf = +0).
+__device__ __forceinline__ uint32_t ex2_h2(float lo, float hi) {
+    uint32_t x, y;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(x) : "f"(hi), "f"(lo));
+    asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
 }
 
-// Packed fp32 pairs (one 64-bit register) for the two-wide FMA and add.
+// s0 += lo, s1 += hi for the two fp16 of p (exact products with 1, fp32 sums).
+__device__ __forceinline__ void sum_h2(uint32_t p, float &s0, float &s1) {
+    asm("{\n\t.reg .b16 a, b, one;\n\t"
+        "mov.b32 {a, b}, %2;\n\tmov.b16 one, 0x3C00;\n\t"
+        "fma.rn.f32.f16 %0, a, one, %0;\n\tfma.rn.f32.f16 %1, b, one, %1;\n\t}"
+        : "+f"(s0), "+f"(s1) : "r"(p));
+}
+
+// Packed fp32 pairs (one 64-bit register) for the two-wide FMA.
 __device__ __forceinline__ uint64_t pk2(float a, float b) {
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
@@ -158,11 +157,6 @@ __device__ __forceinline__ void upk2(uint64_t r, float &a, float &b) {
 __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
     uint64_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
 __device__ __forceinline__ float max3f(float a, float b, float c) {
@@ -606,29 +600,26 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 }
                 // ---- P = 2^(s*scale - m) as fp16 at the start of my S columns: my 32 cells
                 //      are 16 columns (two fp16 per column, lower cell in the low half);
-                //      one exponential in four on the FMA pipe ----
+                //      the exponent s*scale - m is rounded to fp16 and two of them are
+                //      raised at once (ex2.approx.f16x2), which yields P in the fp16 the PV
+                //      product reads; the row sum adds those same fp16 values in fp32 ----
                 {
                     // no maximum yet (nothing visible so far, or a lane past the block):
                     // subtract +inf so that every exponent is -inf and P is 0
                     const float nm = m_run != -INFINITY ? -m_run : -INFINITY;
                     const uint64_t sc2 = pk2(a.scale_log2, a.scale_log2), nm2 = pk2(nm, nm);
-                    uint64_t ls2[2] = {pk2(0.f, 0.f), pk2(0.f, 0.f)};
+                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
                     uint32_t pw[16];
 #pragma unroll
                     for (int c2 = 0; c2 < 16; ++c2) {
                         const int c = 2 * c2;
                         float x0, x1;
                         upk2(ffma2(pk2(__uint_as_float(sb[c]), __uint_as_float(sb[c + 1])), sc2, nm2), x0, x1);
-                        const float p0 = ex2_approx(x0);
-                        const float p1 = (c2 & 1) ? ex2_poly(x1) : ex2_approx(x1);
-                        ls2[c2 & 1] = fadd2(ls2[c2 & 1], pk2(p0, p1));
-                        __half2 hv = __floats2half2_rn(p0, p1);
-                        pw[c2] = *reinterpret_cast<uint32_t *>(&hv);
+                        const uint32_t p2 = ex2_h2(x0, x1);
+                        pw[c2] = p2;
+                        sum_h2(p2, ls[(c2 & 1) * 2], ls[(c2 & 1) * 2 + 1]);
                     }
-                    float la, lb, lc, ld;
-                    upk2(ls2[0], la, lb);
-                    upk2(ls2[1], lc, ld);
-                    l_run += (la + lb) + (lc + ld);
+                    l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                     tc::st16(s_addr, pw);
                 }
                 // ---- O *= alpha where the row's running maximum moved (rare), my 32
