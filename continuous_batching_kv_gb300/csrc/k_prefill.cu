@@ -483,7 +483,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         const uint32_t s_mine = tmem + lane_q + (uint32_t)(32 * qd);   // + 128 * score buffer
         const uint32_t o_mine = tmem + lane_q + COL_O + (uint32_t)(32 * qd);
         uint64_t *pbar = &x.pbar[warp & 3];
-        uint32_t n_s[2] = {0, 0};
+        uint32_t n_s0 = 0, n_s1 = 0;           // score-buffer phases (scalars: no local memory)
         uint32_t n_l = 0, n_p = 0;
         int32_t k = 0;                         // pair tiles consumed (stage ring position)
         bool ok = true;
@@ -538,9 +538,10 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 if (!ok) break;
                 const Meta &mt = x.meta[k % MSLOTS];
                 const bool full = mt.full != 0;
-                ok = __all_sync(0xffffffffu, wait_or_fail(&x.s_full[j & 1], n_s[j & 1] & 1u, fail));
+                const uint32_t ns = (j & 1) ? n_s1 : n_s0;
+                ok = __all_sync(0xffffffffu, wait_or_fail(&x.s_full[j & 1], ns & 1u, fail));
                 if (!ok) break;
-                ++n_s[j & 1];
+                if (j & 1) ++n_s1; else ++n_s0;
                 tc::fence_after();
                 // ---- my 32 columns of S -> registers (one TMEM read, warp collective);
                 //      masked -> -inf ----
