@@ -143,6 +143,29 @@ def test_retire_and_reuse_cells():
         p.close()
 
 
+def test_large_removal_grows_upload_buffers():
+    # 5000 cells of sequence 0, then its removal: more changed cells than the
+    # staging buffers hold (4096 deltas), so they are re-allocated (mapped pinned
+    # memory) before the next device call; a new prompt and a decode row follow
+    import continuous_batching_kv_gb300 as kv
+    cfg = {"id": 10, "name": "large-removal", "shape": dict(configs.QWEN, n_layer=1),
+           "params": dict(n_ctx=8192, n_batch=2048, n_ubatch=512, n_seq_max=2, n_stream=1),
+           "setup": [], "measured": []}
+    p = Pair(cfg)
+    try:
+        for c0 in range(0, 5000, 2048):
+            n = min(2048, 5000 - c0)
+            p.run_call({"pos": list(range(c0, c0 + n)), "seq": [[0]] * n, "content": [0] * n}, attend=False)
+        kv.kv_seq_rm(p.c, 0, 0, -1)
+        p.o.seq_rm(0, 0, -1)
+        st, _ = p.run_call({"pos": list(range(300)), "seq": [[1]] * 300, "content": [1] * 300}, rows_sample=sample_rows)
+        assert st
+        st, _ = p.run_call({"pos": [300], "seq": [[1]], "content": [1]})
+        assert st
+    finally:
+        p.close()
+
+
 def test_device_call_errors():
     import torch
     import continuous_batching_kv_gb300 as kv
