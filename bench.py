@@ -248,14 +248,12 @@ class OursArm:
                 lq, lk = n * self.H * self.d, n * self.Hk * self.d
                 per = lq + 2 * lk
                 buf = self._randn(self.L * per)
-                t = {"n": n, "dev": buf,
-                     "q": [buf[l * per:l * per + lq].view(n, self.H, self.d) for l in range(self.L)],
-                     "k": [buf[l * per + lq:l * per + lq + lk].view(n, self.Hk * self.d) for l in range(self.L)],
-                     "v": [buf[l * per + lq + lk:(l + 1) * per].view(n, self.Hk * self.d) for l in range(self.L)],
+                t = {"n": n, "dev": buf, "per": per, "lq": lq, "lk": lk,
                      "o": self.torch.empty((n, self.H, self.d), dtype=self.torch.float32, device=self.dev),
                      "pairs": int(row_visible_cells([call["pos"][r] for r in rows]).sum()),
                      "bytes": self._kv_bytes(call, rows, n),
                      "row_kv_bytes": len({call["seq"][r][0] for r in rows}) * 2 * self.Hk * self.d * 2}
+                t["q"], t["k"], t["v"] = self._views(t, buf)
                 ubs.append(t)
             kv.kv_split_free(s)
             # the batch is marshalled once (numpy arrays, ids as a flat list plus
@@ -276,20 +274,54 @@ class OursArm:
         kv_rows = sum(cells.values())
         return int(kv_rows * 2 * self.Hk * self.d * 2 + n * self.H * self.d * (2 + 4))
 
+    def _views(self, t, buf):
+        """Per layer Q [n, H, d], K and V [n, Hk*d] inside one ubatch input buffer."""
+        n, per, lq, lk = t["n"], t["per"], t["lq"], t["lk"]
+        return ([buf[l * per:l * per + lq].view(n, self.H, self.d) for l in range(self.L)],
+                [buf[l * per + lq:l * per + lq + lk].view(n, self.Hk * self.d) for l in range(self.L)],
+                [buf[l * per + lq + lk:(l + 1) * per].view(n, self.Hk * self.d) for l in range(self.L)])
+
     def input_bytes(self):
         return sum(t["dev"].numel() * 2 for _, ubs, _ in self.calls for t in ubs)
 
     def enable_host_inputs(self):
-        """End-to-end mode: a pinned host copy of every ubatch's input buffer, a
-        copy stream, and one event per ubatch."""
+        """End-to-end mode: a pinned host copy of every ubatch's input buffer and of
+        its output, two device input buffers per ubatch (a step computes from one
+        while the next step's inputs arrive in the other), a copy stream and events."""
         torch = self.torch
         for _, ubs, _ in self.calls:
             for t in ubs:
                 t["host"] = t["dev"].cpu().pin_memory()
-                t["in_ev"] = torch.cuda.Event()
+                dev2 = torch.empty_like(t["dev"])
+                t["sets"] = [(t["dev"], t["q"], t["k"], t["v"]), (dev2,) + self._views(t, dev2)]
+                t["in_ev"] = [torch.cuda.Event(), torch.cuda.Event()]
+                t["ohost"] = torch.empty(t["o"].shape, dtype=t["o"].dtype).pin_memory()
+                t["out_ev"] = torch.cuda.Event()
+                t["d2h_ev"] = torch.cuda.Event()
         self.copy_stream = torch.cuda.Stream(self.dev)
-        self.step_ev = torch.cuda.Event()
-        self.step_ev.record(self.stream)
+        self.set_ev = [torch.cuda.Event(), torch.cuda.Event()]
+        self.restart_host_steps()
+
+    def restart_host_steps(self):
+        """The next end-to-end step copies its own inputs (nothing prefetched)."""
+        self.e2e_n = 0
+        self.prefetched = False
+        for ev in self.set_ev:
+            ev.record(self.stream)
+        for _, ubs, _ in self.calls:
+            for t in ubs:
+                t["d2h_ev"].record(self.stream)
+
+    def _copy_inputs(self, set_i):
+        """Copy every ubatch's inputs into input buffer set set_i once the step that
+        last used that set has finished."""
+        torch = self.torch
+        self.copy_stream.wait_event(self.set_ev[set_i])
+        with torch.cuda.stream(self.copy_stream):
+            for _, ubs, _ in self.calls:
+                for t in ubs:
+                    t["sets"][set_i][0].copy_(t["host"], non_blocking=True)
+                    t["in_ev"][set_i].record(self.copy_stream)
 
     def reset(self):
         """Before a step: return the cache to its post-setup state, or, for the
@@ -321,46 +353,55 @@ class OursArm:
     def timed_calls_per_step(self):
         return sum(len(ubs) for _, ubs, _ in self.calls) * max(0, self.L - 1)
 
-    def step(self, timers=None, host=False):
+    def step(self, timers=None, host=False, prefetch=False):
         """One pass of the whole path.  timers: an EventPool that brackets the
         attention calls that launch no planning kernels (layers >= 1).
-        host: end-to-end mode -- every ubatch's inputs are copied from pinned host
-        memory on a copy stream (after the previous step's work, so the buffers
-        are free), the attention stream waits for each ubatch's copy, and each
-        ubatch's output is read back to the host."""
+        host: end-to-end mode -- every ubatch's inputs come from pinned host memory
+        over a copy stream, and every ubatch's output goes back to pinned host
+        memory over the same stream; the attention stream waits for each ubatch's
+        inputs.  prefetch: also copy the next step's inputs into the other input
+        buffers, so that they arrive while this step computes."""
         kv, torch = self.kv, self.torch
         self.reset()
         last = []
         off = max(0, self.step_no) if self.decode_loop else 0
+        cur = self.e2e_n & 1 if host else 0
         if host:
-            # the copies of this step overlap the compute of its earlier ubatches
-            self.copy_stream.wait_event(self.step_ev)
-            with torch.cuda.stream(self.copy_stream):
-                for _, ubs, _ in self.calls:
-                    for t in ubs:
-                        t["dev"].copy_(t["host"], non_blocking=True)
-                        t["in_ev"].record(self.copy_stream)
+            if not self.prefetched:
+                self._copy_inputs(cur)
+            self.prefetched = False
+            if prefetch:
+                self._copy_inputs(cur ^ 1)
+                self.prefetched = True
         for ci, (call, ubs, marsh) in enumerate(self.calls):
             s = kv.kv_split_ubatches(self.c, marsh[0] + off if off else marsh[0], marsh[1])
             assert kv.kv_prepare_cells(self.c, s) == 0
             for k, t in enumerate(ubs):
+                qs, ks, vs = t["q"], t["k"], t["v"]
                 if host:
-                    self.stream.wait_event(t["in_ev"])
+                    _, qs, ks, vs = t["sets"][cur]
+                    self.stream.wait_event(t["in_ev"][cur])
+                    self.stream.wait_event(t["d2h_ev"])   # last step's read of o is done
                 for layer in range(self.L):
-                    kv.kv_store(self.c, s, k, layer, t["k"][layer], t["v"][layer], self.stream)
+                    kv.kv_store(self.c, s, k, layer, ks[layer], vs[layer], self.stream)
                     if timers is not None and layer > 0:
                         e0, e1 = timers.take(t["pairs"] + off * t["n"], t["bytes"] + off * t["row_kv_bytes"])
                         e0.record(self.stream)
-                        kv.ubatch_attention(self.c, s, k, layer, t["q"][layer], t["o"], None, self.stream)
+                        kv.ubatch_attention(self.c, s, k, layer, qs[layer], t["o"], None, self.stream)
                         e1.record(self.stream)
                     else:
-                        kv.ubatch_attention(self.c, s, k, layer, t["q"][layer], t["o"], None, self.stream)
+                        kv.ubatch_attention(self.c, s, k, layer, qs[layer], t["o"], None, self.stream)
                 if host:
-                    with torch.cuda.stream(self.stream):
-                        last.append(t["o"].to("cpu", non_blocking=True))
+                    t["out_ev"].record(self.stream)
+                    self.copy_stream.wait_event(t["out_ev"])
+                    with torch.cuda.stream(self.copy_stream):
+                        t["ohost"].copy_(t["o"], non_blocking=True)
+                        t["d2h_ev"].record(self.copy_stream)
+                    last.append(t["ohost"])
             kv.kv_split_free(s)
         if host:
-            self.step_ev.record(self.stream)
+            self.set_ev[cur].record(self.stream)
+            self.e2e_n += 1
         return last
 
 
@@ -444,10 +485,14 @@ def run_ours(args, rank, world, device):
         arm.step(host=True)
         barrier()
         t0.record(arm.stream)
-        arm.step_ev.record(arm.stream)   # the first copies start inside the timed region
+        arm.restart_host_steps()   # the first timed step's copies start inside the timed region
         out = None
-        for _ in range(args.steps):
-            out = arm.step(host=True)
+        for i in range(args.steps):
+            # each step's inputs are copied inside the timed region: the first step's by
+            # itself, the others' by the step before (the last step prefetches nothing)
+            out = arm.step(host=True, prefetch=i + 1 < args.steps)
+        # the results are read back on the copy stream; the timed region ends after them
+        arm.stream.wait_stream(arm.copy_stream)
         t1.record(arm.stream)
         barrier()
         ms_e2e = t0.elapsed_time(t1)
