@@ -119,6 +119,9 @@ __device__ __forceinline__ int64_t slice_start(int64_t x, int64_t U, int64_t gx)
 // Start-up plus epilogue of one prefill work item, in units of one pair of
 // 64-cell tiles of work.
 constexpr int64_t PF_ITEM_COST = 5;
+// Extra cost of the piece that holds a block's last pair (its causal diagonal, with
+// the per-cell mask), in the same units.
+constexpr int64_t PF_DIAG_COST = 1;
 
 // Largest x with slice_start(x) <= q (U > 0).
 __device__ __forceinline__ int32_t slice_of(int64_t q, int64_t U, int64_t gx) {
@@ -142,11 +145,23 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
         if (pass == 1) {
             // Prefill: every item costs a start-up (Q load, first products) and an
             // epilogue on top of its pairs, so a column's cost is its pairs plus
-            // PF_ITEM_COST per item.  Columns are filled greedily in block order up to
+            // PF_ITEM_COST per item, plus PF_DIAG_COST for the piece holding a block's
+            // last pair.  Columns are filled greedily in block order up to
             // a budget T, a block spilling into the next column when the column is
             // full; T is the smallest budget with which the greedy fill needs at most
             // gx columns (each thread tries its own T; two rounds narrow the range).
-            const int64_t C = PF_ITEM_COST;
+            const int64_t C = PF_ITEM_COST, D = PF_DIAG_COST;
+            // how much of the rest of a block a column with `room` left takes: all of
+            // it when its diagonal fits too, else as much as fits short of the last pair
+            auto take_of = [&](int64_t rem, int64_t room, int64_t &cost) -> int64_t {
+                if (rem + D <= room) {
+                    cost = rem + D;
+                    return rem;
+                }
+                const int64_t t = min(rem - 1, room);
+                cost = t;
+                return t;
+            };
             if (tid == 0) {
                 int64_t P = 0;
                 int32_t nne = 0;
@@ -155,8 +170,8 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                     P += pr;
                     nne += pr > 0 ? 1 : 0;
                 }
-                tot = max(C + 1, (P + C * nne + gx - 1) / gx);   // lower bound on T
-                run_u = P + C * (nne + 1) + 1;                     // feasible with any gx >= 1
+                tot = max(C + D + 1, (P + (C + D) * nne + gx - 1) / gx);   // lower bound on T
+                run_u = P + (C + D) * (nne + 1) + 1;                       // feasible with any gx >= 1
             }
             __syncthreads();
             // columns the greedy fill needs with budget T (stops counting past gx)
@@ -166,15 +181,16 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                     const int64_t pairs = (p.counts[b] + 1) / 2;
                     int64_t done = 0;
                     while (done < pairs && x < gx) {
+                        int64_t cost = 0;
                         const int64_t room = T - acc - C;
-                        if (room < 1) {
+                        const int64_t take = room < 1 ? 0 : take_of(pairs - done, room, cost);
+                        if (take < 1) {
                             ++x;
                             acc = 0;
                             continue;
                         }
-                        const int64_t take = min(pairs - done, room);
                         done += take;
-                        acc += C + take;
+                        acc += C + cost;
                     }
                 }
                 return x + 1;
@@ -230,17 +246,22 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                     } else {
                         int64_t done = 0;
                         while (done < pairs) {
+                            int64_t cost = 0;
                             const int64_t room = T - acc - C;
-                            if (room < 1 && x < gx - 1) {   // this column is full
+                            int64_t take = room < 1 ? 0 : take_of(pairs - done, room, cost);
+                            if (take < 1 && x < gx - 1) {   // this column is full
                                 ++x;
                                 acc = 0;
                                 continue;
                             }
-                            const int64_t take = x < gx - 1 ? min(pairs - done, room) : pairs - done;
+                            if (x == gx - 1) {              // the last column takes the rest
+                                take = pairs - done;
+                                cost = take + D;
+                            }
                             emit(b, (int32_t)(2 * done), (int32_t)min((int64_t)cnt, 2 * (done + take)));
                             ++nseg;
                             done += take;
-                            acc += C + take;
+                            acc += C + cost;
                         }
                     }
                     p.blk_nitems[b] = nseg;
