@@ -286,6 +286,27 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                 }
                 p.pf_rows[e] = r;
             }
+            // and each column's first pair (TMA rows of its two tiles, fully visible?)
+            for (int32_t x = tid; x < (int32_t)gx; x += blockDim.x) {
+                const int32_t i = cta0[x];
+                int32_t f[4] = {-1, -1, 0, 0};
+                if (i < cta0[x + 1]) {
+                    const kvk::WorkItem w = p.work[item_base + i];
+                    if (w.t1 > w.t0) {
+                        const kvi::DevBlock b = u.blocks[w.block];
+                        const int32_t *list = p.tiles + (int64_t)w.block * p.tile_stride;
+                        const uint32_t *flg = p.flags + (int64_t)w.block * p.tile_stride;
+                        bool full = true;
+                        for (int h = 0; h < 2; ++h) {
+                            const int32_t t = w.t0 + h < w.t1 ? list[w.t0 + h] : -1;
+                            f[h] = t >= 0 ? b.stream * u.kv_size + t * TILE : -TILE;
+                            full = full && t >= 0 && (int32_t)(flg[t] & 0xffffu) == b.n_rows * TILE;
+                        }
+                        f[2] = full ? 1 : 0;
+                    }
+                }
+                for (int h = 0; h < 4; ++h) p.pf_first[4 * x + h] = f[h];
+            }
             __syncthreads();
             continue;
         }

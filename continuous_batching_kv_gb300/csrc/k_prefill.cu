@@ -262,6 +262,32 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         bool mhas[4] = {false, false, false, false}, many[4] = {false, false, false, false};
         int32_t mpos[4] = {0, 0, 0, 0};
         long long t_last = clock64();
+        // The first pair's K goes out as soon as the previous kernel has finished, from
+        // the planner's per-column record (one read, done before the wait); its
+        // metadata follows through the loop below, which skips that one copy.
+        bool first_out = false;
+        {
+            const int4 ff = *reinterpret_cast<const int4 *>(a.p.pf_first + 4 * blockIdx.x);
+            if (ff.x >= 0) {
+                if (lane < 8) {   // warm L2 with the pair's K and V (a prefetch returns nothing)
+                    const CUtensorMap *tm = lane < 4 ? &tm_k : &tm_v;
+                    const int32_t y = (lane >> 1) & 1 ? ff.y : ff.x;
+                    if (y >= 0) kvd::tma_prefetch_2d(tm, hk * 128 + 64 * (lane & 1), y);
+                }
+                kvd::pdl_wait();   // the K/V cache rows of this ubatch are written
+                if (lane == 0) {
+                    uint8_t *ks = smem + OFF_K;
+                    const int32_t xk = hk * 128;
+                    kvd::fence_proxy_async_smem();
+                    kvd::mbar_arrive_expect_tx(&x.k_full[0], TILEB);
+                    kvd::tma_load_2d(ks, &tm_k, xk, ff.x, &x.k_full[0]);
+                    kvd::tma_load_2d(ks + HALF, &tm_k, xk + 64, ff.x, &x.k_full[0]);
+                    kvd::tma_load_2d(ks + BOX, &tm_k, xk, ff.y, &x.k_full[0]);
+                    kvd::tma_load_2d(ks + HALF + BOX, &tm_k, xk + 64, ff.y, &x.k_full[0]);
+                }
+                first_out = true;
+            }
+        }
         while (true) {
             if (!warp_ok(fail)) break;
             bool prog = false;
@@ -334,7 +360,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     __syncwarp();
                     // the metadata goes out before the K copy is issued
                     kvd::mbar_arrive(&x.meta_full[kc % MSLOTS]);
-                    if (kc == 0) {
+                    if (kc == 0 && !first_out) {
                         // Warm L2 with the first pair's K and V while the previous kernel
                         // (normally the store of this ubatch's rows) finishes: a prefetch
                         // returns nothing, so racing that kernel's writes is harmless.
@@ -345,7 +371,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         }
                         kvd::pdl_wait();   // the K/V cache rows of this ubatch are written
                     }
-                    if (lane == 0) {
+                    if (lane == 0 && !(kc == 0 && first_out)) {
                         uint8_t *ks = smem + OFF_K + st * TILEB;
                         const int32_t xk = hk * 128;
                         const int32_t y0 = mt.ys[0], y1 = mt.ys[1];

@@ -55,6 +55,8 @@ struct Plan {
     int32_t *pf_rows;       // [gx_pf][128]: the ubatch row behind each query vector of each prefill
                             // CTA column's first item (-1: none), so that Q loads without the
                             // chain item -> block -> row permutation
+    int32_t *pf_first;      // [gx_pf][4]: each prefill CTA column's first pair: TMA rows of its two
+                            // tiles (-TILE: no second tile), 1 if fully visible; [0] < 0: none
     int32_t *err;
     int32_t tile_stride;
     int32_t cap_dec, cap_pf;
