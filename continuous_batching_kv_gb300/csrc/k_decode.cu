@@ -84,6 +84,7 @@ struct __align__(16) Aux {
     uint64_t full[S], empty[S];
     uint64_t cbar;                // consumer exchanges (all 256 consumer threads)
     int32_t fail;
+    int32_t last_piece;           // this CTA completed the last piece of the item's block
 };
 
 template <int NQ>
@@ -752,40 +753,64 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     int32_t prev = 0;
                     if (lane == 0) prev = atomicAdd(&a.p.counters[w.block * a.n_head_kv + hk], 1);
                     prev = __shfl_sync(0xffffffffu, prev, 0);
-                    if (prev == nitems - 1) {
-                        // the last piece of the block: merge all of its partials
-                        __threadfence();
-                        const int32_t it0 = a.p.blk_item0[w.block];
-                        const int64_t istride = (int64_t)a.n_head_kv * DEC_QMAX * PART_STRIDE;
-                        const float *pb = a.part + ((int64_t)it0 * a.n_head_kv + hk) * DEC_QMAX * PART_STRIDE;
-                        for (int32_t n = 0; n < nq; ++n) {
-                            const float *pn = pb + n * PART_STRIDE;
-                            float M = -INFINITY;
-                            for (int32_t q = 0; q < nitems; ++q) M = fmaxf(M, __ldcg(pn + q * istride));
-                            float L = 0.f;
-                            float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (M != -INFINITY) {
-                                for (int32_t q = 0; q < nitems; ++q) {
-                                    const float *pk = pn + q * istride;
-                                    const float mk = __ldcg(pk);
-                                    const float lk = __ldcg(pk + 1);
-                                    const float4 ov = __ldcg(reinterpret_cast<const float4 *>(pk + 4) + lane);
-                                    const float sc = mk == -INFINITY ? 0.f : ex2_approx(mk - M);
-                                    L = fmaf(lk, sc, L);
+                    if (lane == 0) x.last_piece = prev == nitems - 1 ? 1 : 0;
+                }
+            }
+            // A split block: the CTA that completed its last piece merges every piece's
+            // partial, all eight warps at once (query vectors n = warp, warp + 8):
+            //   O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
+            // Lanes read the pieces' (m, l) together (one warp-wide max and sum); each
+            // lane owns 4 of the 128 d of O, whose rows load several pieces at a time.
+            const int32_t nitems_b = a.p.blk_nitems[w.block];
+            if (nitems_b > 1) {
+                if (!(ok = cons_sync(&x.cbar, cph, fail))) break;
+                if (x.last_piece) {
+                    __threadfence();
+                    const int32_t it0 = a.p.blk_item0[w.block];
+                    const int64_t istride = (int64_t)a.n_head_kv * DEC_QMAX * PART_STRIDE;
+                    const float *pb = a.part + ((int64_t)it0 * a.n_head_kv + hk) * DEC_QMAX * PART_STRIDE;
+                    for (int32_t n = warp; n < nq; n += NW) {
+                        const float *pn = pb + n * PART_STRIDE;
+                        float M = -INFINITY;
+                        for (int32_t q0 = 0; q0 < nitems_b; q0 += 32) {
+                            const float mq = q0 + lane < nitems_b ? __ldcg(pn + (q0 + lane) * istride) : -INFINITY;
+                            M = fmaxf(M, mq);
+                        }
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                        float L = 0.f;
+                        float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (M != -INFINITY) {
+                            for (int32_t q0 = 0; q0 < nitems_b; q0 += 32) {
+                                const int32_t q = q0 + lane;
+                                float sq = 0.f;
+                                if (q < nitems_b) {
+                                    const float mq = __ldcg(pn + q * istride);
+                                    sq = mq == -INFINITY ? 0.f : ex2_approx(mq - M);
+                                    L = fmaf(__ldcg(pn + q * istride + 1), sq, L);
+                                }
+                                const int32_t nb = min(32, nitems_b - q0);
+#pragma unroll 4
+                                for (int32_t qq = 0; qq < nb; ++qq) {
+                                    const float sc = __shfl_sync(0xffffffffu, sq, qq);
+                                    const float4 ov =
+                                        __ldcg(reinterpret_cast<const float4 *>(pn + (q0 + qq) * istride + 4) + lane);
                                     o4.x = fmaf(ov.x, sc, o4.x);
                                     o4.y = fmaf(ov.y, sc, o4.y);
                                     o4.z = fmaf(ov.z, sc, o4.z);
                                     o4.w = fmaf(ov.w, sc, o4.w);
                                 }
                             }
-                            const float inv = L > 0.f ? 1.f / L : 0.f;
-                            const int32_t row = a.u.perm[b.row0 + n / G];
-                            const int32_t h = hk * G + (n % G);
-                            *reinterpret_cast<float4 *>(a.o + ((int64_t)row * a.n_head + h) * 128 + 4 * lane) =
-                                make_float4(o4.x * inv, o4.y * inv, o4.z * inv, o4.w * inv);
                         }
-                        if (lane == 0) a.p.counters[w.block * a.n_head_kv + hk] = 0;
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+                        const float inv = L > 0.f ? 1.f / L : 0.f;
+                        const int32_t row = a.u.perm[b.row0 + n / G];
+                        const int32_t h = hk * G + (n % G);
+                        *reinterpret_cast<float4 *>(a.o + ((int64_t)row * a.n_head + h) * 128 + 4 * lane) =
+                            make_float4(o4.x * inv, o4.y * inv, o4.z * inv, o4.w * inv);
                     }
+                    if (tid == 0) a.p.counters[w.block * a.n_head_kv + hk] = 0;   // for the next launch
                 }
             }
         }
