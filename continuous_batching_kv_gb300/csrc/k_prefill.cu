@@ -770,8 +770,9 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
 //   O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
 // Launched as a programmatic dependent of the attention kernel: the plan is
 // read first, the partials only after the attention grid has finished.  The
-// CTAs are small (128 threads, at most 64 registers each) so that one fits on
-// an SM beside an attention CTA and waits there, ready, for the grid to end.
+// CTAs are small (128 threads, at most 64 registers each); they take the SMs as
+// the attention CTAs retire (capping them at 48 registers, so that one would
+// wait beside each attention CTA, measured slower: two partials per round trip).
 constexpr int MERGE_SPLIT = 16;
 constexpr int MERGE_QMAX = 4;
 
