@@ -569,18 +569,35 @@ def oracle_sample(cfg, rows_per_ub):
     return t_split + t_store + t_attn, ntok / per_step, desc
 
 
-def cpu_baseline(cfg):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+def _oracle_run(cfg, threads):
+    """The oracle's bounded sample of the workload in a fresh process with `threads`
+    BLAS threads; returns (cpu seconds, tokens/s, description) or an error string."""
+    t = str(threads)
+    env = dict(os.environ, OMP_NUM_THREADS=t, OPENBLAS_NUM_THREADS=t, MKL_NUM_THREADS=t)
     code = ("import json,sys; sys.path.insert(0, %r); import bench; from workloads import configs; "
             "s, v, d = bench.oracle_sample(configs.config(%d), %d); print(json.dumps([s, v, d]))"
             % (ROOT, cfg["id"], 48 if cfg["id"] == 2 else 64))
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
-        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
-                "sample": "failed: " + r.stderr.strip().splitlines()[-1][:200] if r.stderr else "failed"}
-    secs, val, desc = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": round(val, 2), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
-            "cpu_seconds": round(secs, 2), "host_cores_available": os.cpu_count()}
+        return "failed: " + (r.stderr.strip().splitlines()[-1][:200] if r.stderr.strip() else "no output")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(cfg):
+    """The oracle as it stands on the host: one BLAS thread (the reported figure)
+    and, beside it, every host core."""
+    one = _oracle_run(cfg, 1)
+    if isinstance(one, str):
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": one}
+    secs, val, desc = one
+    out = {"value": round(val, 2), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
+           "cpu_seconds": round(secs, 2), "host_cores_available": os.cpu_count()}
+    ncpu = os.cpu_count() or 1
+    if ncpu > 1:
+        allc = _oracle_run(cfg, ncpu)
+        if not isinstance(allc, str):
+            out["all_cores"] = {"value": round(allc[1], 2), "cores": ncpu, "cpu_seconds": round(allc[0], 2)}
+    return out
 
 
 def run_reference(args, cfg):
