@@ -263,6 +263,7 @@ int device_init(kv_cache *c) {
     p.cap_pf = d->gx_pf + max_pf_blocks;
     const size_t fl = (size_t)d->max_blocks * p.tile_stride;
     if ((e = dev_alloc(d, &p.flags, fl)) != cudaSuccess || (e = dev_alloc(d, &p.tiles, fl)) != cudaSuccess ||
+        (e = dev_alloc(d, &p.cum, fl)) != cudaSuccess || (e = dev_alloc(d, &p.wcount, d->max_blocks)) != cudaSuccess ||
         (e = dev_alloc(d, &p.counts, d->max_blocks)) != cudaSuccess ||
         (e = dev_alloc(d, &p.work, (size_t)p.cap_dec + p.cap_pf)) != cudaSuccess ||
         (e = dev_alloc(d, &p.n_work, 2)) != cudaSuccess ||

@@ -74,35 +74,79 @@ __global__ void __launch_bounds__(TILE) k_plan_tiles(kvk::UbView u, kvk::Plan p)
     }
 }
 
-// One CTA per block: ordered list of the tiles with any visible pair.
+// One CTA per block: ordered list of the tiles with any visible pair, and the
+// decode cost of the list up to each entry, so that decode work is cut by cost, not
+// by tile count.  A fully visible tile costs 8 (its eight 8-cell groups); another
+// costs 2 plus the number of its 8-cell groups holding a visible pair (the decode
+// kernel loads exactly those groups, and the 2 stands for the per-tile work that
+// does not shrink with them: the flag read, the group queueing, the mask).
 __global__ void __launch_bounds__(256) k_plan_compact(kvk::UbView u, kvk::Plan p, int32_t n_tiles) {
-    __shared__ int32_t warp_sum[8];
-    __shared__ int32_t base;
+    __shared__ int32_t warp_sum[8], warp_cost[8];
+    __shared__ int32_t base, cbase;
     const int32_t b = blockIdx.x;
     const uint32_t *f = p.flags + (int64_t)b * p.tile_stride;
     int32_t *out = p.tiles + (int64_t)b * p.tile_stride;
-    if (threadIdx.x == 0) base = 0;
+    int32_t *cum = p.cum + (int64_t)b * p.tile_stride;
+    const int32_t full_cnt = u.blocks[b].n_rows * TILE;
+    if (threadIdx.x == 0) {
+        base = 0;
+        cbase = 0;
+    }
     __syncthreads();
     const int32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int32_t a = 0; a < n_tiles; a += blockDim.x) {
         const int32_t t = a + threadIdx.x;
-        const bool nz = t < n_tiles && f[t] != 0;
+        const uint32_t fl = t < n_tiles ? f[t] : 0u;
+        const bool nz = fl != 0;
+        const int32_t cost = !nz ? 0 : (int32_t)(fl & 0xffffu) == full_cnt ? 8 : 2 + __popc((fl >> 16) & 0xffu);
         const uint32_t bal = __ballot_sync(0xffffffffu, nz);
         const int32_t before = __popc(bal & ((1u << lane) - 1u));
+        int32_t incl = cost;   // inclusive warp scan of the costs
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
         if (lane == 0) warp_sum[warp] = __popc(bal);
+        if (lane == 31) warp_cost[warp] = incl;
         __syncthreads();
-        int32_t off = base;
-        for (int32_t w = 0; w < warp; ++w) off += warp_sum[w];
-        if (nz) out[off + before] = t;
+        int32_t off = base, coff = cbase;
+        for (int32_t w = 0; w < warp; ++w) {
+            off += warp_sum[w];
+            coff += warp_cost[w];
+        }
+        if (nz) {
+            out[off + before] = t;
+            cum[off + before] = coff + incl - cost;
+        }
         __syncthreads();
         if (threadIdx.x == 0) {
-            int32_t tot = 0;
-            for (int32_t w = 0; w < (int32_t)(blockDim.x >> 5); ++w) tot += warp_sum[w];
+            int32_t tot = 0, ctot = 0;
+            for (int32_t w = 0; w < (int32_t)(blockDim.x >> 5); ++w) {
+                tot += warp_sum[w];
+                ctot += warp_cost[w];
+            }
             base += tot;
+            cbase += ctot;
         }
         __syncthreads();
     }
-    if (threadIdx.x == 0) p.counts[b] = base;
+    if (threadIdx.x == 0) {
+        p.counts[b] = base;
+        p.wcount[b] = cbase;
+    }
+}
+
+// Decode: the first list entry whose cost-before is at least x (0 .. count).
+__device__ __forceinline__ int32_t tile_at_cost(const kvk::Plan &p, int32_t b, int64_t x) {
+    const int32_t *cum = p.cum + (int64_t)b * p.tile_stride;
+    int32_t lo = 0, hi = p.counts[b];
+    while (lo < hi) {
+        const int32_t mid = (lo + hi) >> 1;
+        if (cum[mid] < x) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
 }
 
 // One CTA: cut the tile lists into split-K work items, stream-K style.  Per
@@ -314,14 +358,14 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
         __syncthreads();
         for (int32_t b = lo + tid; b < hi; b += blockDim.x) {
             const int32_t c = p.counts[b];
-            atomicAdd((unsigned long long *)&tot, (unsigned long long)(pass ? (c + 1) / 2 : c));
+            atomicAdd((unsigned long long *)&tot, (unsigned long long)(pass ? (c + 1) / 2 : p.wcount[b]));
         }
         __syncthreads();
         const int64_t U = tot;
         for (int32_t a = lo; a < hi; a += blockDim.x) {
             const int32_t b = a + tid;
             int64_t ub = 0;
-            if (b < hi) ub = pass ? (p.counts[b] + 1) / 2 : p.counts[b];
+            if (b < hi) ub = pass ? (p.counts[b] + 1) / 2 : p.wcount[b];
             scan_u[tid] = ub;
             __syncthreads();
             for (int32_t d = 1; d < (int32_t)blockDim.x; d <<= 1) {
@@ -367,8 +411,10 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                     }
                     kvk::WorkItem w;
                     w.block = b;
-                    w.t0 = pass ? (int32_t)(2 * lo_u) : (int32_t)lo_u;
-                    w.t1 = pass ? (int32_t)min((int64_t)cnt, 2 * hi_u) : (int32_t)hi_u;
+                    // decode: cost offsets -> tile indices (equal offsets give equal
+                    // indices, so neighbouring items still meet exactly)
+                    w.t0 = pass ? (int32_t)(2 * lo_u) : tile_at_cost(p, b, lo_u);
+                    w.t1 = pass ? (int32_t)min((int64_t)cnt, 2 * hi_u) : tile_at_cost(p, b, hi_u);
                     w.cta = x;
                     const int32_t idx = ibase + k;
                     if (idx < cap) p.work[item_base + idx] = w;

@@ -45,6 +45,9 @@ struct Plan {
                             // pairs in the 64-cell tile, bits 16..23 which 8-cell groups
                             // hold a visible pair
     int32_t *tiles;         // [max_blocks][tile_stride] compacted tile lists
+    int32_t *cum;           // [max_blocks][tile_stride] decode cost of the listed tiles before each:
+                            // a fully visible tile 8, another its number of visible 8-cell groups
+    int32_t *wcount;        // [max_blocks] total decode cost of each block's list
     int32_t *counts;        // [max_blocks]
     WorkItem *work;         // decode items [0, cap_dec), prefill items [cap_dec, +cap_pf)
     int32_t *n_work;        // [2] decode / prefill item counts
