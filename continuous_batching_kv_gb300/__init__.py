@@ -72,7 +72,7 @@ class kv_ubatch_info(C.Structure):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError("libkvattn.so is not built; run "
-                          "`python -m continuous_batching_kv_gb300.build` (needs nvcc)")
+                          "`python continuous_batching_kv_gb300/build.py` (needs nvcc)")
     lib = C.CDLL(LIB_PATH)
     P = C.c_void_p
     sig = {

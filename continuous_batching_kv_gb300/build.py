@@ -5,7 +5,9 @@ into ``continuous_batching_kv_gb300/libkvattn.so`` with the static CUDA
 runtime, so the library loads on a machine without a GPU (its host-side
 calls work there; device calls return an error).
 
-    python -m continuous_batching_kv_gb300.build [--force] [--verbose]
+    python continuous_batching_kv_gb300/build.py [--force] [--verbose]
+
+(run as a script: importing the package first would look for the library).
 """
 
 import argparse

@@ -8,9 +8,11 @@
 //
 // Design (sm_103a), templated on NQ, the query vectors one block may hold
 // (1, 2, 4, 8 or 16; the ubatch's largest decode block picks the instance):
-//  * grid = (CTA columns, KV heads), two CTAs per SM; each CTA column owns an
-//    equal slice of the concatenated visible-tile lists of all decode blocks
-//    (stream-K), split at block boundaries into work items; a block is up to
+//  * grid = (CTA columns, KV heads), two CTAs per SM; the planner fills the CTA
+//    columns with consecutive pieces (work items) of the decode blocks' visible-
+//    tile lists, greedily by cost (tiles plus a fixed cost per item) up to the
+//    smallest budget that fits the grid, so a column takes a second block only
+//    where blocks are small next to the budget; a block is up to
 //    16 query vectors (rows sharing a first sequence id, times the GQA group),
 //    so every K/V byte read serves all of them;
 //  * warp 8 is the producer: K and V of one 64-cell tile per stage, by TMA
@@ -757,10 +759,13 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 }
             }
             // A split block: the CTA that completed its last piece merges every piece's
-            // partial, all eight warps at once (query vectors n = warp, warp + 8):
+            // partial with all eight warps:
             //   O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
-            // Lanes read the pieces' (m, l) together (one warp-wide max and sum); each
-            // lane owns 4 of the 128 d of O, whose rows load several pieces at a time.
+            // Each query vector gets wpn warps, each warp every wpn-th piece: its lanes
+            // read the pieces' (m, l) together and each lane owns 4 of the 128 d of O,
+            // the first O rows loaded alongside (m, l); a warp keeps a running maximum
+            // across rounds of 32 pieces.  The wpn warp states of a query vector then
+            // meet in the tree-merge scratch (room for 4 NQ states).
             const int32_t nitems_b = a.p.blk_nitems[w.block];
             if (nitems_b > 1) {
                 if (!(ok = cons_sync(&x.cbar, cph, fail))) break;
@@ -769,46 +774,105 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     const int32_t it0 = a.p.blk_item0[w.block];
                     const int64_t istride = (int64_t)a.n_head_kv * DEC_QMAX * PART_STRIDE;
                     const float *pb = a.part + ((int64_t)it0 * a.n_head_kv + hk) * DEC_QMAX * PART_STRIDE;
-                    for (int32_t n = warp; n < nq; n += NW) {
+                    const int32_t wpn = max(1, min(NW, 4 * NQ) / nq);   // warps per query vector
+                    const int32_t sub = warp % wpn;
+                    const int32_t myc = (nitems_b - sub + wpn - 1) / wpn;   // my pieces: sub + wpn j
+                    float *sm = &x.scr_m[0][0], *sl = &x.scr_l[0][0], *so = &x.scr_o[0][0][0];
+                    for (int32_t n = warp / wpn; n < nq; n += NW / wpn) {
                         const float *pn = pb + n * PART_STRIDE;
-                        float M = -INFINITY;
-                        for (int32_t q0 = 0; q0 < nitems_b; q0 += 32) {
-                            const float mq = q0 + lane < nitems_b ? __ldcg(pn + (q0 + lane) * istride) : -INFINITY;
-                            M = fmaxf(M, mq);
-                        }
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-                        float L = 0.f;
+                        auto orow = [&](int32_t j) -> float4 {
+                            return __ldcg(reinterpret_cast<const float4 *>(pn + (int64_t)(sub + wpn * j) * istride + 4) + lane);
+                        };
+                        float Mw = -INFINITY, Lw = 0.f;
                         float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (M != -INFINITY) {
-                            for (int32_t q0 = 0; q0 < nitems_b; q0 += 32) {
-                                const int32_t q = q0 + lane;
-                                float sq = 0.f;
-                                if (q < nitems_b) {
-                                    const float mq = __ldcg(pn + q * istride);
-                                    sq = mq == -INFINITY ? 0.f : ex2_approx(mq - M);
-                                    L = fmaf(__ldcg(pn + q * istride + 1), sq, L);
-                                }
-                                const int32_t nb = min(32, nitems_b - q0);
+                        for (int32_t j0 = 0; j0 < myc; j0 += 32) {
+                            const int32_t nb = min(32, myc - j0);
+                            float4 ov[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) ov[u] = u < nb ? orow(j0 + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            float mq = -INFINITY, lq = 0.f;
+                            if (lane < nb) {
+                                const float *pq = pn + (int64_t)(sub + wpn * (j0 + lane)) * istride;
+                                mq = __ldcg(pq);
+                                lq = __ldcg(pq + 1);
+                            }
+                            float Mc = mq;
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, o));
+                            const float Mn = fmaxf(Mw, Mc);
+                            const float rs = Mw == -INFINITY ? 0.f : ex2_approx(Mw - Mn);
+                            const float sq = mq == -INFINITY ? 0.f : ex2_approx(mq - Mn);
+                            float lsum = lq * sq;
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+                            Lw = Lw * rs + lsum;
+                            o4.x *= rs;
+                            o4.y *= rs;
+                            o4.z *= rs;
+                            o4.w *= rs;
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const float sc = __shfl_sync(0xffffffffu, sq, u);
+                                o4.x = fmaf(ov[u].x, sc, o4.x);
+                                o4.y = fmaf(ov[u].y, sc, o4.y);
+                                o4.z = fmaf(ov[u].z, sc, o4.z);
+                                o4.w = fmaf(ov[u].w, sc, o4.w);
+                            }
 #pragma unroll 4
-                                for (int32_t qq = 0; qq < nb; ++qq) {
-                                    const float sc = __shfl_sync(0xffffffffu, sq, qq);
-                                    const float4 ov =
-                                        __ldcg(reinterpret_cast<const float4 *>(pn + (q0 + qq) * istride + 4) + lane);
-                                    o4.x = fmaf(ov.x, sc, o4.x);
-                                    o4.y = fmaf(ov.y, sc, o4.y);
-                                    o4.z = fmaf(ov.z, sc, o4.z);
-                                    o4.w = fmaf(ov.w, sc, o4.w);
+                            for (int32_t qq = 4; qq < nb; ++qq) {
+                                const float sc = __shfl_sync(0xffffffffu, sq, qq);
+                                const float4 v = orow(j0 + qq);
+                                o4.x = fmaf(v.x, sc, o4.x);
+                                o4.y = fmaf(v.y, sc, o4.y);
+                                o4.z = fmaf(v.z, sc, o4.z);
+                                o4.w = fmaf(v.w, sc, o4.w);
+                            }
+                            Mw = Mn;
+                        }
+                        if (wpn == 1) {
+                            const float inv = Lw > 0.f ? 1.f / Lw : 0.f;
+                            const int32_t row = a.u.perm[b.row0 + n / G];
+                            const int32_t h = hk * G + (n % G);
+                            *reinterpret_cast<float4 *>(a.o + ((int64_t)row * a.n_head + h) * 128 + 4 * lane) =
+                                make_float4(o4.x * inv, o4.y * inv, o4.z * inv, o4.w * inv);
+                        } else {
+                            const int32_t slot = n * wpn + sub;   // < nq wpn <= 4 NQ
+                            if (lane == 0) {
+                                sm[slot] = Mw;
+                                sl[slot] = Lw;
+                            }
+                            *reinterpret_cast<float4 *>(so + slot * 128 + 4 * lane) = o4;
+                        }
+                    }
+                    if (wpn > 1) {
+                        if (!(ok = cons_sync(&x.cbar, cph, fail))) break;
+                        if (sub == 0 && warp / wpn < nq) {
+                            const int32_t n = warp / wpn;
+                            float M = -INFINITY;
+                            for (int32_t s2 = 0; s2 < wpn; ++s2) M = fmaxf(M, sm[n * wpn + s2]);
+                            float L = 0.f;
+                            float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (M != -INFINITY) {
+                                for (int32_t s2 = 0; s2 < wpn; ++s2) {
+                                    const int32_t slot = n * wpn + s2;
+                                    const float ms = sm[slot];
+                                    const float sc = ms == -INFINITY ? 0.f : ex2_approx(ms - M);
+                                    const float4 v = *reinterpret_cast<const float4 *>(so + slot * 128 + 4 * lane);
+                                    L = fmaf(sl[slot], sc, L);
+                                    o4.x = fmaf(v.x, sc, o4.x);
+                                    o4.y = fmaf(v.y, sc, o4.y);
+                                    o4.z = fmaf(v.z, sc, o4.z);
+                                    o4.w = fmaf(v.w, sc, o4.w);
                                 }
                             }
+                            const float inv = L > 0.f ? 1.f / L : 0.f;
+                            const int32_t row = a.u.perm[b.row0 + n / G];
+                            const int32_t h = hk * G + (n % G);
+                            *reinterpret_cast<float4 *>(a.o + ((int64_t)row * a.n_head + h) * 128 + 4 * lane) =
+                                make_float4(o4.x * inv, o4.y * inv, o4.z * inv, o4.w * inv);
                         }
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-                        const float inv = L > 0.f ? 1.f / L : 0.f;
-                        const int32_t row = a.u.perm[b.row0 + n / G];
-                        const int32_t h = hk * G + (n % G);
-                        *reinterpret_cast<float4 *>(a.o + ((int64_t)row * a.n_head + h) * 128 + 4 * lane) =
-                            make_float4(o4.x * inv, o4.y * inv, o4.z * inv, o4.w * inv);
+                        // the next item's tree merge reuses the scratch
+                        if (!(ok = cons_sync(&x.cbar, cph, fail))) break;
                     }
                     if (tid == 0) a.p.counters[w.block * a.n_head_kv + hk] = 0;   // for the next launch
                 }

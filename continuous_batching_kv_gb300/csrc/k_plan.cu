@@ -149,35 +149,68 @@ __device__ __forceinline__ int32_t tile_at_cost(const kvk::Plan &p, int32_t b, i
     return lo;
 }
 
-// One CTA: cut the tile lists into split-K work items, stream-K style.  Per
-// path (decode blocks first, then prefill blocks) the blocks' lists are laid
-// end to end (decode in tiles, prefill in pairs of tiles) and cut into gx
-// equal slices, one per CTA column of the attention grid; a slice is split at
-// block boundaries into items.  So every CTA gets the same amount of work, a
-// block's items are consecutive, and a block is covered by as few items as
-// the slices allow.  Only a block with an empty list gets an empty item (its
-// rows see nothing and get zeros); empty slices (more CTA columns than units)
-// get no item.
-__device__ __forceinline__ int64_t slice_start(int64_t x, int64_t U, int64_t gx) { return (x * U) / gx; }
+// One CTA: cut the tile lists into split-K work items.  Per path (decode blocks
+// first, then prefill blocks) the CTA columns of the attention grid are filled
+// greedily in block order: a column takes the rest of the current block if it
+// fits under a budget T, else as much of it as fits, and the block spills into
+// the next column.  Every item costs a start-up and an epilogue on top of its
+// work, so a column's cost is its work plus a fixed cost per item; T is the
+// smallest budget with which the fill needs at most gx columns.  So the columns
+// carry about the same time, a block's items are consecutive, and a column takes
+// a second block only where the blocks are small next to the budget.  A block
+// with an empty list gets one empty item (its rows see nothing and get zeros);
+// columns beyond the fill get no item.
 
-// Start-up plus epilogue of one prefill work item, in units of one pair of
-// 64-cell tiles of work.
+// Decode, in the units of the tile costs (a fully visible tile 8): start-up (the
+// first stage's latency, the Q load) plus epilogue (the merge of the eight warps'
+// states, the partial and its completion count) of one item.
+constexpr int64_t DEC_ITEM_COST = 16;
+// Decode: no piece smaller than one fully visible tile, unless it ends a block.
+constexpr int64_t DEC_MIN_TAKE = 8;
+// Decode block costs staged in shared memory for the budget search.
+constexpr int32_t DEC_STAGE = 2048;
+// Prefill, in units of one pair of 64-cell tiles: start-up plus epilogue of one item.
 constexpr int64_t PF_ITEM_COST = 5;
 // Extra cost of the piece that holds a block's last pair (its causal diagonal, with
 // the per-cell mask), in the same units.
 constexpr int64_t PF_DIAG_COST = 1;
 
-// Largest x with slice_start(x) <= q (U > 0).
-__device__ __forceinline__ int32_t slice_of(int64_t q, int64_t U, int64_t gx) {
-    return (int32_t)(((q + 1) * gx + U - 1) / U - 1);
+// The smallest budget T in [t_lo, t_hi] with columns(T) <= gx, given that t_hi is
+// feasible: every thread of the CTA tries its own candidate, in two rounds (the
+// second within the step of the first); t_lo and t_hi live in shared memory and
+// end with t_hi = the answer.  scan: blockDim.x ints of shared memory.
+template <class Cols>
+__device__ void smallest_budget(Cols columns, int64_t gx, long long &t_lo_s, long long &t_hi_s, int32_t *scan) {
+    const int32_t tid = threadIdx.x;
+    for (int32_t round = 0; round < 2; ++round) {
+        const int64_t t_lo = t_lo_s, t_hi = t_hi_s;
+        const int64_t step = max((int64_t)1, (t_hi - t_lo + blockDim.x) / (int64_t)blockDim.x);
+        const int64_t T = t_lo + (int64_t)tid * step;
+        const bool feas = T <= t_hi && columns(T) <= gx;
+        // the smallest feasible candidate (candidates increase with tid)
+        scan[tid] = feas ? tid : (int32_t)blockDim.x;
+        __syncthreads();
+        for (int32_t d = (int32_t)blockDim.x / 2; d > 0; d >>= 1) {
+            if (tid < d) scan[tid] = min(scan[tid], scan[tid + d]);
+            __syncthreads();
+        }
+        if (tid == 0) {
+            const int32_t w = scan[0];
+            if (w < (int32_t)blockDim.x) {
+                t_hi_s = t_lo + (int64_t)w * step;   // feasible
+                t_lo_s = w > 0 ? t_lo + (int64_t)(w - 1) * step + 1 : t_lo;
+            } else {
+                t_lo_s = t_lo + (int64_t)(blockDim.x - 1) * step + 1;
+            }
+        }
+        __syncthreads();
+    }
 }
 
 __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, int32_t gx_dec, int32_t gx_pf) {
-    __shared__ long long tot;
-    __shared__ long long run_u;
-    __shared__ int32_t run_i;
-    __shared__ long long scan_u[1024];
+    __shared__ long long t_lo_s, t_hi_s;
     __shared__ int32_t scan_i[1024];
+    __shared__ int32_t s_wc[DEC_STAGE];
     const int32_t tid = threadIdx.x;
     for (int32_t pass = 0; pass < 2; ++pass) {
         const int32_t lo = pass == 0 ? 0 : u.n_dec_blocks;
@@ -187,13 +220,8 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
         const int32_t cap = pass == 0 ? p.cap_dec : p.cap_pf;
         int32_t *cta0 = p.cta_item0 + (pass == 0 ? 0 : gx_dec + 1);
         if (pass == 1) {
-            // Prefill: every item costs a start-up (Q load, first products) and an
-            // epilogue on top of its pairs, so a column's cost is its pairs plus
-            // PF_ITEM_COST per item, plus PF_DIAG_COST for the piece holding a block's
-            // last pair.  Columns are filled greedily in block order up to
-            // a budget T, a block spilling into the next column when the column is
-            // full; T is the smallest budget with which the greedy fill needs at most
-            // gx columns (each thread tries its own T; two rounds narrow the range).
+            // Prefill: work in pairs of tiles, PF_ITEM_COST per item, plus PF_DIAG_COST
+            // for the piece holding a block's last pair.
             const int64_t C = PF_ITEM_COST, D = PF_DIAG_COST;
             // how much of the rest of a block a column with `room` left takes: all of
             // it when its diagonal fits too, else as much as fits short of the last pair
@@ -214,8 +242,8 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                     P += pr;
                     nne += pr > 0 ? 1 : 0;
                 }
-                tot = max(C + D + 1, (P + (C + D) * nne + gx - 1) / gx);   // lower bound on T
-                run_u = P + (C + D) * (nne + 1) + 1;                       // feasible with any gx >= 1
+                t_lo_s = max(C + D + 1, (P + (C + D) * nne + gx - 1) / gx);   // lower bound on T
+                t_hi_s = P + (C + D) * (nne + 1) + 1;                       // feasible with any gx >= 1
             }
             __syncthreads();
             // columns the greedy fill needs with budget T (stops counting past gx)
@@ -239,34 +267,9 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                 }
                 return x + 1;
             };
-            for (int32_t round = 0; round < 2; ++round) {
-                const int64_t t_lo = tot, t_hi = run_u;            // the answer lies in [t_lo, t_hi]
-                const int64_t step = max((int64_t)1, (t_hi - t_lo + blockDim.x) / (int64_t)blockDim.x);
-                __syncthreads();
-                if (tid == 0) run_i = 0;
-                __syncthreads();
-                const int64_t T = t_lo + (int64_t)tid * step;
-                const bool feas = T <= t_hi && columns(T) <= gx;
-                // the smallest feasible candidate (candidates increase with tid)
-                scan_i[tid] = feas ? tid : (int32_t)blockDim.x;
-                __syncthreads();
-                for (int32_t d = (int32_t)blockDim.x / 2; d > 0; d >>= 1) {
-                    if (tid < d) scan_i[tid] = min(scan_i[tid], scan_i[tid + d]);
-                    __syncthreads();
-                }
-                if (tid == 0) {
-                    const int32_t w = scan_i[0];
-                    if (w < (int32_t)blockDim.x) {
-                        run_u = t_lo + (int64_t)w * step;          // feasible
-                        tot = w > 0 ? t_lo + (int64_t)(w - 1) * step + 1 : t_lo;
-                    } else {
-                        tot = t_lo + (int64_t)(blockDim.x - 1) * step + 1;
-                    }
-                }
-                __syncthreads();
-            }
+            smallest_budget(columns, gx, t_lo_s, t_hi_s, scan_i);
             if (tid == 0) {
-                const int64_t T = run_u;
+                const int64_t T = t_hi_s;
                 int32_t x = 0, nitem = 0;
                 int64_t acc = 0;
                 auto emit = [&](int32_t b, int32_t t0, int32_t t1) {
@@ -354,81 +357,109 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
             __syncthreads();
             continue;
         }
-        if (tid == 0) { tot = 0; run_u = 0; run_i = 0; }
+        // Decode: work in the tile costs (the cumulative costs of k_plan_compact),
+        // DEC_ITEM_COST per item.  Items are cut in cost units and turned into tile
+        // ranges afterwards (equal offsets give equal tiles, so neighbouring items
+        // still meet exactly).
+        const int64_t C = DEC_ITEM_COST, MT = DEC_MIN_TAKE;
+        for (int32_t b = lo + tid; b < hi && b - lo < DEC_STAGE; b += blockDim.x) s_wc[b - lo] = p.wcount[b];
         __syncthreads();
-        for (int32_t b = lo + tid; b < hi; b += blockDim.x) {
-            const int32_t c = p.counts[b];
-            atomicAdd((unsigned long long *)&tot, (unsigned long long)(pass ? (c + 1) / 2 : p.wcount[b]));
+        auto wc = [&](int32_t b) -> int64_t { return b - lo < DEC_STAGE ? s_wc[b - lo] : p.wcount[b]; };
+        // how much of a block's remaining cost `rem` a column with `room` left takes
+        // (0: none, start a new column)
+        auto take_of = [&](int64_t rem, int64_t room) -> int64_t { return room >= min(rem, MT) ? min(rem, room) : 0; };
+        if (tid == 0) {
+            int64_t S = 0;
+            for (int32_t b = lo; b < hi; ++b) S += wc(b);
+            const int64_t nb = hi - lo;
+            t_lo_s = max(C + MT, (S + C * nb + gx - 1) / gx);   // lower bound on T
+            t_hi_s = max(C + MT, S + C * (nb + 1) + 1);         // one column takes everything
         }
         __syncthreads();
-        const int64_t U = tot;
-        for (int32_t a = lo; a < hi; a += blockDim.x) {
-            const int32_t b = a + tid;
-            int64_t ub = 0;
-            if (b < hi) ub = pass ? (p.counts[b] + 1) / 2 : p.wcount[b];
-            scan_u[tid] = ub;
-            __syncthreads();
-            for (int32_t d = 1; d < (int32_t)blockDim.x; d <<= 1) {
-                const long long v = tid >= d ? scan_u[tid - d] : 0;
-                __syncthreads();
-                scan_u[tid] += v;
-                __syncthreads();
-            }
-            const int64_t P = run_u + scan_u[tid] - ub;   // first unit of block b
-            int32_t first = 0, nseg = 0;
-            if (b < hi) {
-                if (ub == 0) {
-                    first = P < U ? slice_of(P, U, gx) : (int32_t)gx - 1;
-                    nseg = 1;
-                } else {
-                    // the slices overlapping [P, P + ub), skipping empty (zero-length) slices
-                    first = slice_of(P, U, gx);
-                    const int32_t last = slice_of(P + ub - 1, U, gx);
-                    for (int32_t x = first; x <= last; ++x)
-                        if (slice_start(x + 1, U, gx) > slice_start(x, U, gx)) ++nseg;
-                }
-            }
-            scan_i[tid] = nseg;
-            __syncthreads();
-            for (int32_t d = 1; d < (int32_t)blockDim.x; d <<= 1) {
-                const int32_t v = tid >= d ? scan_i[tid - d] : 0;
-                __syncthreads();
-                scan_i[tid] += v;
-                __syncthreads();
-            }
-            const int32_t ibase = run_i + scan_i[tid] - nseg;
-            if (b < hi) {
-                p.blk_item0[b] = item_base + ibase;
-                p.blk_nitems[b] = nseg;
-                const int32_t cnt = p.counts[b];
-                int32_t x = first;
-                for (int32_t k = 0; k < nseg; ++k, ++x) {
-                    int64_t lo_u = 0, hi_u = 0;
-                    if (ub > 0) {
-                        while (slice_start(x + 1, U, gx) == slice_start(x, U, gx)) ++x;
-                        lo_u = max(P, slice_start(x, U, gx)) - P;
-                        hi_u = min(P + ub, slice_start(x + 1, U, gx)) - P;
+        // columns the greedy fill needs with budget T (stops counting past gx)
+        auto columns = [&](int64_t T) -> int64_t {
+            int64_t x = 0, acc = 0;
+            for (int32_t b = lo; b < hi && x < gx; ++b) {
+                int64_t rem = wc(b);
+                if (rem == 0) {   // an empty item
+                    if (acc > 0 && acc + C > T) {
+                        ++x;
+                        acc = 0;
                     }
-                    kvk::WorkItem w;
-                    w.block = b;
-                    // decode: cost offsets -> tile indices (equal offsets give equal
-                    // indices, so neighbouring items still meet exactly)
-                    w.t0 = pass ? (int32_t)(2 * lo_u) : tile_at_cost(p, b, lo_u);
-                    w.t1 = pass ? (int32_t)min((int64_t)cnt, 2 * hi_u) : tile_at_cost(p, b, hi_u);
-                    w.cta = x;
-                    const int32_t idx = ibase + k;
-                    if (idx < cap) p.work[item_base + idx] = w;
-                    else kvd::report(p.err, kvd::DERR_BOUNDS);
+                    acc += C;
+                    continue;
+                }
+                while (rem > 0 && x < gx) {
+                    const int64_t take = take_of(rem, T - acc - C);
+                    if (take == 0) {
+                        ++x;
+                        acc = 0;
+                        continue;
+                    }
+                    rem -= take;
+                    acc += C + take;
                 }
             }
-            __syncthreads();
-            if (tid == blockDim.x - 1) { run_u += scan_u[tid]; run_i += scan_i[tid]; }
-            __syncthreads();
+            return x + 1;
+        };
+        smallest_budget(columns, gx, t_lo_s, t_hi_s, scan_i);
+        if (tid == 0) {
+            const int64_t T = t_hi_s;
+            int32_t x = 0, nitem = 0;
+            int64_t acc = 0;
+            auto emit = [&](int32_t b, int64_t c0, int64_t c1) {   // cost offsets, for now
+                kvk::WorkItem w;
+                w.block = b;
+                w.t0 = (int32_t)c0;
+                w.t1 = (int32_t)c1;
+                w.cta = x;
+                if (nitem < cap) p.work[item_base + nitem] = w;
+                else kvd::report(p.err, kvd::DERR_BOUNDS);
+                ++nitem;
+            };
+            for (int32_t b = lo; b < hi; ++b) {
+                int64_t rem = wc(b), off = 0;
+                p.blk_item0[b] = item_base + nitem;
+                int32_t nseg = 0;
+                if (rem == 0) {
+                    if (acc > 0 && acc + C > T && x < gx - 1) {
+                        ++x;
+                        acc = 0;
+                    }
+                    emit(b, 0, 0);
+                    acc += C;
+                    nseg = 1;
+                }
+                while (rem > 0) {
+                    int64_t take = take_of(rem, T - acc - C);
+                    if (take == 0 && x < gx - 1) {   // this column is full
+                        ++x;
+                        acc = 0;
+                        continue;
+                    }
+                    if (x == gx - 1) take = rem;     // the last column takes the rest
+                    emit(b, off, off + take);
+                    ++nseg;
+                    off += take;
+                    rem -= take;
+                    acc += C + take;
+                }
+                p.blk_nitems[b] = nseg;
+            }
+            p.n_work[0] = min(nitem, cap);
         }
-        const int32_t n_items = min(run_i, cap);
-        if (tid == 0) p.n_work[pass] = n_items;
+        __syncthreads();   // items written by thread 0 are visible below
+        const int32_t n_items = p.n_work[0];
+        for (int32_t i = tid; i < n_items; i += blockDim.x) {
+            kvk::WorkItem &w = p.work[item_base + i];
+            if (w.t1 > w.t0) {
+                const int32_t t0 = tile_at_cost(p, w.block, w.t0), t1 = tile_at_cost(p, w.block, w.t1);
+                w.t0 = t0;
+                w.t1 = t1;
+            }
+        }
         __syncthreads();   // items written by other threads are visible below
-        // cta0[x] = first item whose slice is >= x; cta0[gx] = n_items
+        // cta0[x] = first item of column >= x; cta0[gx] = n_items
         for (int32_t i = tid; i < n_items; i += blockDim.x) {
             const int32_t c = p.work[item_base + i].cta;
             const int32_t cp = i > 0 ? p.work[item_base + i - 1].cta : -1;

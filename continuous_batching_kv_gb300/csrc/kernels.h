@@ -46,7 +46,7 @@ struct Plan {
                             // hold a visible pair
     int32_t *tiles;         // [max_blocks][tile_stride] compacted tile lists
     int32_t *cum;           // [max_blocks][tile_stride] decode cost of the listed tiles before each:
-                            // a fully visible tile 8, another its number of visible 8-cell groups
+                            // a fully visible tile 8, another 2 + its number of visible 8-cell groups
     int32_t *wcount;        // [max_blocks] total decode cost of each block's list
     int32_t *counts;        // [max_blocks]
     WorkItem *work;         // decode items [0, cap_dec), prefill items [cap_dec, +cap_pf)

@@ -103,6 +103,25 @@ def test_ragged_kv_size_and_streams():
     assert len(stats) >= 5
 
 
+def test_non_causal_prefill_decode_and_prefix():
+    # causal = 0: a row sees every occupied cell of its sequence, later positions
+    # included, but not the cells that later ubatches of the same split fill
+    # (300 prompt tokens at n_ubatch 128: the first ubatch must not see the other
+    # two's cells); then a prompt shared by sequences 1 and 2, and decode rows
+    cfg = {"id": 14, "name": "non-causal", "shape": dict(configs.QWEN, n_layer=1),
+           "params": dict(n_ctx=1024, n_batch=512, n_ubatch=128, n_seq_max=3, n_stream=1,
+                          causal=False),
+           "setup": [],
+           "measured": [
+               {"pos": list(range(300)), "seq": [[0]] * 300, "content": [0] * 300},
+               {"pos": list(range(200)) + [300], "seq": [[1, 2]] * 200 + [[0]],
+                "content": [1] * 200 + [0]},
+               {"pos": [301, 200, 200], "seq": [[0], [1], [2]], "content": [0, 1, 2]},
+           ]}
+    stats, _ = _run(cfg, check_mask=True)
+    assert len(stats) >= 6
+
+
 def test_random_small_batches():
     rng = np.random.default_rng(5)
     calls = []
