@@ -256,7 +256,7 @@ int device_init(kv_cache *c) {
     d->max_blocks = c->n_ubatch;
     const int32_t max_pf_blocks = std::max<int32_t>(1, (c->n_ubatch * c->gqa + PF_MIN_QV - 1) / PF_MIN_QV);
     d->gx_dec = std::max<int32_t>(1, d->n_sm * kvk::decode_ctas_per_sm() / hkv);
-    d->gx_pf = std::max<int32_t>(1, d->n_sm / hkv);
+    d->gx_pf = std::min<int32_t>(kvk::PLAN_MAX_COLS, std::max<int32_t>(1, d->n_sm / hkv));
     kvk::Plan &p = d->plan;
     p.tile_stride = (c->kv_size + TILE - 1) / TILE;
     p.cap_dec = d->gx_dec + d->max_blocks;

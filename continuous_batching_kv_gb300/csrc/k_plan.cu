@@ -207,10 +207,23 @@ __device__ void smallest_budget(Cols columns, int64_t gx, long long &t_lo_s, lon
     }
 }
 
+// cta0[x] = the first item of column >= x, cta0[gx] = n_items (items in column
+// order; every thread of the CTA takes part).
+__device__ void fill_cta0(const kvk::WorkItem *work, int32_t n_items, int64_t gx, int32_t *cta0) {
+    for (int32_t i = threadIdx.x; i < n_items; i += blockDim.x) {
+        const int32_t c = work[i].cta;
+        const int32_t cp = i > 0 ? work[i - 1].cta : -1;
+        for (int32_t x = cp + 1; x <= c; ++x) cta0[x] = i;
+    }
+    const int32_t clast = n_items > 0 ? work[n_items - 1].cta : -1;
+    for (int32_t x = clast + 1 + (int32_t)threadIdx.x; x <= (int32_t)gx; x += blockDim.x) cta0[x] = n_items;
+}
+
 __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, int32_t gx_dec, int32_t gx_pf) {
     __shared__ long long t_lo_s, t_hi_s;
     __shared__ int32_t scan_i[1024];
     __shared__ int32_t s_wc[DEC_STAGE];
+    __shared__ int32_t s_r0[kvk::PLAN_MAX_COLS], s_nq[kvk::PLAN_MAX_COLS];
     const int32_t tid = threadIdx.x;
     for (int32_t pass = 0; pass < 2; ++pass) {
         const int32_t lo = pass == 0 ? 0 : u.n_dec_blocks;
@@ -219,10 +232,20 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
         const int32_t item_base = pass == 0 ? 0 : p.cap_dec;
         const int32_t cap = pass == 0 ? p.cap_dec : p.cap_pf;
         int32_t *cta0 = p.cta_item0 + (pass == 0 ? 0 : gx_dec + 1);
+        if (lo == hi) {   // no block on this path: its attention kernels are not launched
+            if (tid == 0) p.n_work[pass] = 0;
+            for (int32_t x = tid; x <= (int32_t)gx; x += blockDim.x) cta0[x] = 0;
+            __syncthreads();
+            continue;
+        }
         if (pass == 1) {
             // Prefill: work in pairs of tiles, PF_ITEM_COST per item, plus PF_DIAG_COST
             // for the piece holding a block's last pair.
             const int64_t C = PF_ITEM_COST, D = PF_DIAG_COST;
+            // the blocks' tile counts, staged for the budget search
+            for (int32_t b = lo + tid; b < hi && b - lo < DEC_STAGE; b += blockDim.x) s_wc[b - lo] = p.counts[b];
+            __syncthreads();
+            auto count_of = [&](int32_t b) -> int32_t { return b - lo < DEC_STAGE ? s_wc[b - lo] : p.counts[b]; };
             // how much of the rest of a block a column with `room` left takes: all of
             // it when its diagonal fits too, else as much as fits short of the last pair
             auto take_of = [&](int64_t rem, int64_t room, int64_t &cost) -> int64_t {
@@ -238,7 +261,7 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                 int64_t P = 0;
                 int32_t nne = 0;
                 for (int32_t b = lo; b < hi; ++b) {
-                    const int64_t pr = (p.counts[b] + 1) / 2;
+                    const int64_t pr = (count_of(b) + 1) / 2;
                     P += pr;
                     nne += pr > 0 ? 1 : 0;
                 }
@@ -250,7 +273,7 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
             auto columns = [&](int64_t T) -> int64_t {
                 int64_t x = 0, acc = 0;
                 for (int32_t b = lo; b < hi && x < gx; ++b) {
-                    const int64_t pairs = (p.counts[b] + 1) / 2;
+                    const int64_t pairs = (count_of(b) + 1) / 2;
                     int64_t done = 0;
                     while (done < pairs && x < gx) {
                         int64_t cost = 0;
@@ -283,7 +306,7 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                     ++nitem;
                 };
                 for (int32_t b = lo; b < hi; ++b) {
-                    const int32_t cnt = p.counts[b];
+                    const int32_t cnt = count_of(b);
                     const int64_t pairs = (cnt + 1) / 2;
                     p.blk_item0[b] = item_base + nitem;
                     int32_t nseg = 0;
@@ -313,34 +336,24 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                     }
                     p.blk_nitems[b] = nseg;
                 }
-                const int32_t n_items = min(nitem, cap);
-                p.n_work[1] = n_items;
-                int32_t i = 0;
-                for (int32_t xx = 0; xx <= (int32_t)gx; ++xx) {
-                    while (i < n_items && p.work[item_base + i].cta < xx) ++i;
-                    cta0[xx] = i;
-                }
+                p.n_work[1] = min(nitem, cap);
             }
-            __syncthreads();   // items and cta0 written by thread 0 are visible below
-            // the rows behind each column's first item, one entry per query vector
-            for (int32_t e = tid; e < (int32_t)gx * 128; e += blockDim.x) {
-                const int32_t x = e >> 7, qv = e & 127;
-                const int32_t i = cta0[x];
-                int32_t r = -1;
-                if (i < cta0[x + 1]) {
-                    const kvi::DevBlock b = u.blocks[p.work[item_base + i].block];
-                    if (qv < b.n_rows * p.gqa) r = u.perm[b.row0 + qv / p.gqa];
-                }
-                p.pf_rows[e] = r;
-            }
-            // and each column's first pair (TMA rows of its two tiles, fully visible?)
+            __syncthreads();   // items written by thread 0 are visible below
+            fill_cta0(p.work + item_base, p.n_work[1], gx, cta0);
+            __syncthreads();
+            // each column's first item: its first pair (TMA rows of its two tiles, fully
+            // visible?), and its block's first row and query-vector count, staged for the
+            // row table below
             for (int32_t x = tid; x < (int32_t)gx; x += blockDim.x) {
                 const int32_t i = cta0[x];
                 int32_t f[4] = {-1, -1, 0, 0};
+                int32_t r0 = 0, nq = 0;
                 if (i < cta0[x + 1]) {
                     const kvk::WorkItem w = p.work[item_base + i];
+                    const kvi::DevBlock b = u.blocks[w.block];
+                    r0 = b.row0;
+                    nq = b.n_rows * p.gqa;
                     if (w.t1 > w.t0) {
-                        const kvi::DevBlock b = u.blocks[w.block];
                         const int32_t *list = p.tiles + (int64_t)w.block * p.tile_stride;
                         const uint32_t *flg = p.flags + (int64_t)w.block * p.tile_stride;
                         bool full = true;
@@ -353,8 +366,15 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                     }
                 }
                 for (int h = 0; h < 4; ++h) p.pf_first[4 * x + h] = f[h];
+                s_r0[x] = r0;
+                s_nq[x] = nq;
             }
             __syncthreads();
+            // the rows behind each column's first item, one entry per query vector
+            for (int32_t e = tid; e < (int32_t)gx * 128; e += blockDim.x) {
+                const int32_t x = e >> 7, qv = e & 127;
+                p.pf_rows[e] = qv < s_nq[x] ? u.perm[s_r0[x] + qv / p.gqa] : -1;
+            }
             continue;
         }
         // Decode: work in the tile costs (the cumulative costs of k_plan_compact),
@@ -459,16 +479,7 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
             }
         }
         __syncthreads();   // items written by other threads are visible below
-        // cta0[x] = first item of column >= x; cta0[gx] = n_items
-        for (int32_t i = tid; i < n_items; i += blockDim.x) {
-            const int32_t c = p.work[item_base + i].cta;
-            const int32_t cp = i > 0 ? p.work[item_base + i - 1].cta : -1;
-            for (int32_t x = cp + 1; x <= c; ++x) cta0[x] = i;
-        }
-        if (tid == 0) {
-            const int32_t clast = n_items > 0 ? p.work[item_base + n_items - 1].cta : -1;
-            for (int32_t x = clast + 1; x <= (int32_t)gx; ++x) cta0[x] = n_items;
-        }
+        fill_cta0(p.work + item_base, n_items, gx, cta0);
         __syncthreads();
     }
 }

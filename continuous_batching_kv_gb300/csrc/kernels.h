@@ -12,6 +12,9 @@ namespace kvk {
 // One unit of attention work: tile-list entries [t0, t1) of one block, run
 // by CTA column `cta`.  A block's items are consecutive; an item's index
 // (within its path) names its split-K partial slot.
+// Most CTA columns a prefill grid may have (the planner stages one entry per column).
+constexpr int32_t PLAN_MAX_COLS = 1024;
+
 struct WorkItem {
     int32_t block;
     int32_t t0;
