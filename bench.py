@@ -19,8 +19,10 @@ on a bounded sample of the same workload; rank 0 only.
 """
 
 import argparse
+import datetime
 import json
 import os
+import select
 import statistics
 import subprocess
 import sys
@@ -74,7 +76,7 @@ def load_peaks():
 # from an ncu capture of the current kernel (profiles/k_decode_llama8b-decode-256seq-
 # lognormal.md; a launch at decode step 2, 3.519 GB algorithmic).  Cleared to nothing
 # whenever the kernel changes until it is captured again.
-DECODE_TRAFFIC = {5: 3555194000}
+DECODE_TRAFFIC = {5: 3556348000}
 
 DECODE_BOUND = {3: True, 5: True}
 
@@ -90,15 +92,20 @@ def row_visible_cells(pos):
 
 
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
+    """nvidia-smi sampling during the timed region.  The sampler starts before the
+    warm-up and the first sample is awaited there, so that nvidia-smi's own start-up
+    (which can hold up the device for a while) stays out of the timed region; only
+    samples stamped inside the timed window are kept."""
 
-    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+    Q = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu):
         self.proc = None
         self.gpu = gpu
+        self.first = ""
+        self.window = None
 
     def start(self):
         try:
@@ -107,34 +114,58 @@ class Clocks:
                  "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
+            return
+        ready, _, _ = select.select([self.proc.stdout], [], [], 10.0)
+        if ready:
+            self.first = self.proc.stdout.readline()
+
+    def mark(self, t0, t1):
+        """The timed window, as datetime.now() before and after it."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
             return None
+        if self.window is not None:   # let a sample land after a window shorter than the period
+            wait = 0.3 - (datetime.datetime.now() - self.window[1]).total_seconds()
+            if wait > 0:
+                time.sleep(wait)
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        rows = []
+        for line in (self.first + out).strip().splitlines():
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 7:
+            if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                sm, mx = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[3:7]):
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                ts = None   # unreadable stamp: the sample is kept unfiltered
+            rows.append((ts, sm, mx, parts[4:8]))
+        if self.window is not None and all(r[0] is not None for r in rows):
+            inside = [r for r in rows if self.window[0] <= r[0] <= self.window[1]]
+            # a window shorter than the sampling period: the two samples around it
+            before = [r for r in rows if r[0] < self.window[0]]
+            after = [r for r in rows if r[0] > self.window[1]]
+            rows = inside or before[-1:] + after[:1]
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[3]):
                 if v.lower() == "active":
                     reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median([r[1] for r in rows]), "sm_max_mhz": max(r[2] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
 
 
 class EventPool:
@@ -419,20 +450,22 @@ def run_ours(args, rank, world, device):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
+    clocks = Clocks(device if isinstance(device, int) else torch.cuda.current_device())
+    clocks.start()
     for _ in range(max(args.warmup, 3)):
         arm.step()
     barrier()
-    clocks = Clocks(device if isinstance(device, int) else torch.cuda.current_device())
     launches0 = kv.kv_launch_count(arm.c)
-    clocks.start()
     barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    w0 = datetime.datetime.now()
     t0.record(arm.stream)
     for _ in range(args.steps):
         arm.step()
     t1.record(arm.stream)
     barrier()
+    clocks.mark(w0, datetime.datetime.now())
     clk = clocks.stop()
     ms_total = t0.elapsed_time(t1)
     launches = kv.kv_launch_count(arm.c) - launches0
@@ -576,7 +609,7 @@ def _oracle_run(cfg, threads):
     env = dict(os.environ, OMP_NUM_THREADS=t, OPENBLAS_NUM_THREADS=t, MKL_NUM_THREADS=t)
     code = ("import json,sys; sys.path.insert(0, %r); import bench; from workloads import configs; "
             "s, v, d = bench.oracle_sample(configs.config(%d), %d); print(json.dumps([s, v, d]))"
-            % (ROOT, cfg["id"], 48 if cfg["id"] == 2 else 64))
+            % (ROOT, cfg["id"], 160 if cfg["id"] == 2 else 64))
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
         return "failed: " + (r.stderr.strip().splitlines()[-1][:200] if r.stderr.strip() else "no output")
