@@ -11,7 +11,7 @@ The functions keep the C names:
 
     kv_init, kv_free, kv_n_batch, kv_n_ubatch, kv_kv_size, kv_last_error,
     kv_split_ubatches, kv_split_count, kv_split_ubatch, kv_split_free,
-    kv_prepare_cells, kv_seq_rm, kv_seq_pos_max, kv_cells_read,
+    kv_prepare_cells, kv_seq_rm, kv_seq_cp, kv_seq_pos_max, kv_cells_read,
     kv_stream_n_kv, kv_store, ubatch_attention, ubatch_attention_static_scratch,
     kv_device_error, kv_device_bytes, kv_launch_count
 """
@@ -35,7 +35,7 @@ KV_STATIC_SCRATCH_BYTES = 24 << 20
 EXPORTS = [
     "kv_init", "kv_free", "kv_n_batch", "kv_n_ubatch", "kv_kv_size", "kv_last_error",
     "kv_split_ubatches", "kv_split_count", "kv_split_ubatch", "kv_split_free",
-    "kv_prepare_cells", "kv_seq_rm", "kv_seq_pos_max", "kv_cells_read", "kv_stream_n_kv",
+    "kv_prepare_cells", "kv_seq_rm", "kv_seq_cp", "kv_seq_pos_max", "kv_cells_read", "kv_stream_n_kv",
     "kv_store", "ubatch_attention", "ubatch_attention_static_scratch", "kv_device_error",
     "kv_device_bytes", "kv_launch_count",
 ]
@@ -88,6 +88,7 @@ def _load():
         "kv_split_free": (None, [P]),
         "kv_prepare_cells": (C.c_int, [P, P]),
         "kv_seq_rm": (C.c_int, [P, C.c_int32, C.c_int32, C.c_int32]),
+        "kv_seq_cp": (C.c_int, [P, C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
         "kv_seq_pos_max": (C.c_int32, [P, C.c_int32]),
         "kv_cells_read": (C.c_int, [P, C.c_int32, C.POINTER(C.c_int32), C.POINTER(C.c_uint64)]),
         "kv_stream_n_kv": (C.c_int32, [P, C.c_int32]),
@@ -297,6 +298,10 @@ def kv_prepare_cells(c, s):
 
 def kv_seq_rm(c, seq, p0=0, p1=-1):
     return _check(c, lib.kv_seq_rm(c, seq, p0, p1))
+
+
+def kv_seq_cp(c, src, dst, p0=0, p1=-1):
+    return _check(c, lib.kv_seq_cp(c, src, dst, p0, p1))
 
 
 def kv_seq_pos_max(c, seq):

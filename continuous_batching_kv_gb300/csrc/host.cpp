@@ -619,6 +619,32 @@ int kv_seq_rm(kv_cache *c, int32_t seq, int32_t p0, int32_t p1) {
     return KV_OK;
 }
 
+int kv_seq_cp(kv_cache *c, int32_t src, int32_t dst, int32_t p0, int32_t p1) {
+    if (!c) return KV_E_INVAL;
+    if (src < 0 || src >= c->prm.n_seq_max || dst < 0 || dst >= c->prm.n_seq_max)
+        return c->set_err(KV_E_SEQ_RANGE, "sequence id out of range");
+    const int32_t s = c->seq_to_stream[src];
+    if (c->seq_to_stream[dst] != s) return c->set_err(KV_E_CROSS_STREAM, "copy between streams");
+    if (src == dst) return KV_OK;
+    CellState &cs = c->cells;
+    const int32_t W = cs.n_words;
+    const int64_t hi = p1 < 0 ? INT64_MAX : (int64_t)p1;
+    const size_t base = (size_t)s * cs.kv_size;
+    bool changed = false;
+    for (int32_t j = 0; j < cs.used_max_p1[s]; ++j) {
+        const size_t g = base + j;
+        if (!cs.nseq[g] || cs.pos[g] < p0 || cs.pos[g] >= hi) continue;
+        uint64_t *w = &cs.bits[g * W];
+        if (!bit_has(w, src) || bit_has(w, dst)) continue;
+        w[dst >> 6] |= 1ull << (dst & 63);
+        cs.nseq[g] += 1;
+        changed = true;
+        if (c->has_device) push_delta(c, g);
+    }
+    if (changed) c->rm_gen++;   // splits prepared before see another cell state
+    return KV_OK;
+}
+
 int32_t kv_seq_pos_max(const kv_cache *c, int32_t seq) {
     if (!c || seq < 0 || seq >= c->prm.n_seq_max) return KV_E_SEQ_RANGE;
     return seq_pos_max(c, seq);

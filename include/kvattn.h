@@ -43,7 +43,7 @@ extern "C" {
 #define KV_E_SEQ_RANGE        (-3) /* a sequence id outside [0, n_seq_max) */
 #define KV_E_CROSS_STREAM     (-4) /* one slot's sequence ids map to different streams */
 #define KV_E_ORDER            (-5) /* device call out of order (attention before this layer stored ubatches 0..ub, or a split not prepared) */
-#define KV_E_STALE            (-6) /* the split was prepared before a later kv_seq_rm / kv_clear */
+#define KV_E_STALE            (-6) /* the split was prepared before a later kv_seq_rm / kv_seq_cp that changed a cell */
 #define KV_E_CUDA             (-7) /* a CUDA call failed; kv_last_error() has the text */
 #define KV_E_NOMEM            (-8) /* host or device allocation failed */
 #define KV_E_NO_DEVICE        (-9) /* device call on a host-only cache (k_layers == NULL in kv_init) */
@@ -228,6 +228,21 @@ int kv_prepare_cells(kv_cache *c, kv_split *s);
  * Errors: KV_E_SEQ_RANGE.
  */
 int kv_seq_rm(kv_cache *c, int32_t seq, int32_t p0, int32_t p1);
+
+/*
+ * kv_seq_cp -- let sequence `dst` share the cells of sequence `src` with
+ * p0 <= pos < p1 (p1 < 0: no upper bound): `dst` joins each such cell's
+ * sequence set, so both sequences' rows see the same K/V rows, no data moves.
+ * BATCH-ZH, Part E: a prompt shared by several sequences is one set of cells
+ * whose sequence set holds them all; this gives that state to a prefix stored
+ * for one sequence (the same cells as storing it with both ids).  Cells that
+ * already hold `dst` are left alone; src == dst does nothing.  Splits prepared
+ * before a call that changed a cell become stale (KV_E_STALE).
+ * Errors: KV_E_SEQ_RANGE (either id outside 0 .. n_seq_max - 1),
+ * KV_E_CROSS_STREAM (the two sequences live in different streams: sharing
+ * would need the K/V rows copied into the other stream's cache).
+ */
+int kv_seq_cp(kv_cache *c, int32_t src, int32_t dst, int32_t p0, int32_t p1);
 
 /* Largest position sequence `seq` holds in the cache, or -1. */
 int32_t kv_seq_pos_max(const kv_cache *c, int32_t seq);

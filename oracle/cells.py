@@ -145,6 +145,27 @@ class CellState:
                     self.fill(s, j, self.pos[s, j] if keep else -1, keep)
 
 
+    def seq_cp(self, src, dst, p0, p1):
+        """Let sequence dst share src's cells with p0 <= pos < p1; returns 0, or
+        "cross-stream" when the two sequences live in different streams.
+
+        BATCH-ZH, Part E: a prompt shared by several sequences is one set of
+        cells whose sequence set holds them all.  Reading (the pages give no copy
+        call): copying src to dst adds dst to the set of each cell of src in the
+        range, which is the state that storing those tokens with both ids gives.
+        Nothing else changes; p1 < 0 means no upper bound.
+        """
+        s = self.seq_to_stream[src]
+        if self.seq_to_stream[dst] != s:
+            return "cross-stream"
+        hi = np.iinfo(np.int64).max if p1 < 0 else p1
+        for j in range(self.kv_size):
+            if self.nseq[s, j] == 0 or not (p0 <= self.pos[s, j] < hi):
+                continue
+            if self.seq_has(s, j, src) and not self.seq_has(s, j, dst):
+                self.fill(s, j, self.pos[s, j], self.seqs_of(s, j) + [dst])
+        return 0
+
 def prepare(state, ubatches, pos_list, seq_lists, keep_snapshots=True):
     """Reserve a cell for every row of every ubatch, all or nothing.
 

@@ -95,3 +95,6 @@ class OracleKV:
 
     def seq_rm(self, q, p0, p1):
         return self.state.seq_rm(q, p0, p1)
+
+    def seq_cp(self, src, dst, p0, p1):
+        return self.state.seq_cp(src, dst, p0, p1)

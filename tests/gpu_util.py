@@ -54,6 +54,12 @@ class Pair:
     def close(self):
         self.kv.kv_free(self.c)
 
+    def seq_cp(self, src, dst, p0=0, p1=-1):
+        """Share src's cells with dst on both sides."""
+        self.kv.kv_seq_cp(self.c, src, dst, p0, p1)
+        if self.o is not None:
+            assert self.o.seq_cp(src, dst, p0, p1) == 0
+
     def qkv(self, layer, pos, content):
         from workloads import gen
         cid = self.cfg["id"]

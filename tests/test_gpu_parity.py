@@ -162,6 +162,27 @@ def test_retire_and_reuse_cells():
         p.close()
 
 
+def test_seq_cp_shares_a_prefix():
+    # a 100-token prompt of sequence 0, shared whole with sequence 2 and up to
+    # position 60 with sequence 1 (no K/V moves: the cells gain the ids); then a
+    # decode row each.  Sequence 2 continues sequence 0's content, so its row must
+    # give sequence 0's output: prefix-shared cells equal duplicated ones.
+    cfg = {"id": 15, "name": "seq-cp", "shape": dict(configs.QWEN, n_layer=1),
+           "params": dict(n_ctx=512, n_batch=256, n_ubatch=64, n_seq_max=4, n_stream=1),
+           "setup": [], "measured": []}
+    p = Pair(cfg)
+    try:
+        p.run_call({"pos": list(range(100)), "seq": [[0]] * 100, "content": [0] * 100})
+        p.seq_cp(0, 2)
+        p.seq_cp(0, 1, 0, 60)
+        st, outs = p.run_call({"pos": [100, 60, 100], "seq": [[0], [1], [2]], "content": [0, 1, 0]},
+                              check_mask=True)
+        assert len(st) == 1
+        np.testing.assert_allclose(outs[((2,), 100, 0)], outs[((0,), 100, 0)], rtol=0, atol=1e-5)
+    finally:
+        p.close()
+
+
 def test_large_removal_grows_upload_buffers():
     # 5000 cells of sequence 0, then its removal: more changed cells than the
     # staging buffers hold (4096 deltas), so they are re-allocated (mapped pinned

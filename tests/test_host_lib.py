@@ -128,6 +128,16 @@ def test_random_calls_match_oracle(mode, n_stream):
             assert kv.kv_seq_rm(c, q, p0, p1) == 0
             o.seq_rm(q, p0, p1)
             _compare_state(c, o)
+        if rng.random() < 0.3:
+            src, dst = rng.randrange(n_seq), rng.randrange(n_seq)
+            p0, p1 = rng.randint(0, 30), rng.choice([-1, rng.randint(0, 60)])
+            if o.seq_cp(src, dst, p0, p1) == "cross-stream":
+                with pytest.raises(kv.KvError) as ei:
+                    kv.kv_seq_cp(c, src, dst, p0, p1)
+                assert ei.value.code == kv.KV_E_CROSS_STREAM
+            else:
+                assert kv.kv_seq_cp(c, src, dst, p0, p1) == 0
+            _compare_state(c, o)
         for q in range(n_seq):
             assert kv.kv_seq_pos_max(c, q) == o.state.seq_pos_max(q)
 
@@ -150,6 +160,10 @@ def test_error_codes_match_oracle():
     with pytest.raises(kv.KvError) as ei:
         kv.kv_split_ubatches(c, [], [], n_tokens=0)
     assert ei.value.code == kv.KV_E_INVAL
+    for src, dst, code in ((0, 4, kv.KV_E_SEQ_RANGE), (-1, 0, kv.KV_E_SEQ_RANGE), (0, 2, kv.KV_E_CROSS_STREAM)):
+        with pytest.raises(kv.KvError) as ei:
+            kv.kv_seq_cp(c, src, dst, 0, -1)
+        assert ei.value.code == code
 
 
 def test_auto_fill_and_null_seq():

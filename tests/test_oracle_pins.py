@@ -231,6 +231,40 @@ def test_seq_rm_frees_cells_and_keeps_shared_prefix():
     assert sp.cells == [[0]]                  # freed cells are reused first-fit
 
 
+
+def test_seq_cp_equals_storing_with_every_id():
+    # BATCH-ZH, Part E: "Hello world" stored once for sequences {0, 1, 2}.  Storing
+    # it for sequence 0 and copying it to 1 and 2 must give the same cells, and
+    # each decode row then sees the page's three cells.
+    g = golden("prefix_sharing.json")
+    mk = lambda: OracleKV(n_ctx=16, n_batch=16, n_ubatch=16, n_seq_max=3, n_stream=1,
+                          n_layer=1, n_head=2, n_head_kv=1, head_dim=4, keep_kv=False)
+    shared, copied = mk(), mk()
+    assert shared.split(g["prefill"]["pos"], g["prefill"]["seq"], n_seq_id=[3, 3])[0] == 0
+    assert copied.split(g["prefill"]["pos"], [[0]] * len(g["prefill"]["pos"]))[0] == 0
+    assert copied.seq_cp(0, 1, 0, -1) == 0 and copied.seq_cp(0, 2, 0, -1) == 0
+    assert copied.state.same_as(shared.state)
+    code, sp = copied.split(g["decode"]["pos"], g["decode"]["seq"])
+    vis = (copied.mask(sp, 0) == M.F16_ZERO).sum(axis=1)
+    assert list(vis) == [g["cells_visible_per_decode_row"]] * 3
+
+
+def test_seq_cp_range_inverse_and_streams():
+    kv = OracleKV(n_ctx=32, n_batch=32, n_ubatch=32, n_seq_max=4, n_stream=2,
+                  n_layer=1, n_head=2, n_head_kv=1, head_dim=4, keep_kv=False,
+                  seq_to_stream=[0, 0, 1, 1])
+    kv.split(list(range(10)), [[0]] * 10)
+    before = kv.state.copy()
+    assert kv.seq_cp(0, 1, 3, 7) == 0
+    # only positions 3 .. 6 gain sequence 1
+    assert [j for j in range(10) if kv.state.seq_has(0, j, 1)] == [3, 4, 5, 6]
+    assert kv.state.seq_pos_max(1) == 6
+    assert kv.seq_cp(0, 1, 0, -1) == 0        # cells already holding 1 stay as they are
+    assert all(kv.state.seqs_of(0, j) == [0, 1] for j in range(10))
+    kv.seq_rm(1, 0, -1)                       # removing the copy restores the state
+    assert kv.state.same_as(before)
+    assert kv.seq_cp(0, 2, 0, -1) == "cross-stream" and kv.state.same_as(before)
+
 # ----------------------------------------------------------------------------
 # cache layout and the pages' measurements
 # ----------------------------------------------------------------------------
