@@ -15,6 +15,7 @@ import pytest
 
 from oracle import params as P, batch as B, cells as C, mask as M, attention as A
 from oracle import layout as L
+from oracle import sched as S
 from oracle.session import OracleKV
 from workloads import gen
 from tests.conftest import golden
@@ -311,6 +312,88 @@ def test_duty_cycle_pin():
         if "approx" in c:
             assert round(c["useful"] / c["executed"], 2) == c["approx"]
 
+
+
+def _drive(sched, check=None):
+    """Run the loop to the end, checking the budgets at every pass."""
+    def on_batch(retired, pos, seq):
+        assert len(pos) <= sched.token_budget
+        assert len(sched.running) <= sched.max_seqs and sched.free_cells >= 0
+        assert len(set(seq)) == len(sched.running)
+        if check is not None:
+            check(retired, pos, seq)
+    return S.run(sched, on_batch)
+
+
+def test_fixed_batch_duty_cycle_pin():
+    # ITER: the page's fixed batches, run through the scheduler loop in fixed mode
+    for c in golden("duty_cycle.json")["cases"]:
+        n = len(c["lengths"])
+        sch = S.Scheduler(kv_size=1 << 16, n_seq_max=n, max_seqs=n, token_budget=4096, fixed=True)
+        for N in c["lengths"]:
+            assert sch.submit(16, N) is not None
+        _drive(sch)
+        assert (sch.useful, sch.passes * sch.max_seqs) == (c["useful"], c["executed"])
+
+
+def test_continuous_equals_fixed_for_equal_lengths():
+    # equal output lengths leave nothing to refill: k full batches take k N passes
+    for fixed in (True, False):
+        sch = S.Scheduler(kv_size=4096, n_seq_max=8, max_seqs=4, token_budget=256, fixed=fixed)
+        for _ in range(12):
+            sch.submit(10, 7)
+        _drive(sch)
+        assert sch.passes == 3 * 7 and sch.duty_cycle() == 1.0
+
+
+def test_continuous_refills_slots():
+    # the page's eight lengths, eight requests each: the fixed batch stays at its
+    # 5568 / 16384 per group, the loop refills freed slots at once; useful
+    # positions are the same and equal the sum of the batch sizes
+    lengths = [64, 128, 256, 512, 512, 1024, 1024, 2048]
+    out = {}
+    for fixed in (True, False):
+        sch = S.Scheduler(kv_size=1 << 16, n_seq_max=8, max_seqs=8, token_budget=4096, fixed=fixed)
+        for _ in range(8):
+            for N in lengths:
+                sch.submit(32, N)
+        sizes = []
+        _drive(sch, lambda r, pos, seq: sizes.append(len(set(seq))) if pos else None)
+        assert sch.useful == 8 * sum(lengths) == sum(sizes)
+        out[fixed] = sch
+    assert out[True].passes == 8 * 2048 and out[True].duty_cycle() == 5568 / 16384
+    # neither budget binds here: while requests wait every pass runs eight
+    # sequences, and the drain after the last admission lasts at most one
+    # longest request
+    lo = -(-8 * sum(lengths) // 8)
+    assert lo <= out[False].passes <= lo + max(lengths)
+
+
+def test_scheduler_budgets_and_retirement():
+    # worked by hand: kv_size 100 cells, 40 positions per pass, four slots;
+    # A = (30 prompt, 10 new), B = (30, 10), C = (5, 3), D = (20, 2)
+    sch = S.Scheduler(kv_size=100, n_seq_max=4, max_seqs=4, token_budget=40, fixed=False)
+    assert sch.submit(41, 1) is None and sch.submit(60, 41) is None     # can never run
+    for L, N in [(30, 10), (30, 10), (5, 3), (20, 2)]:
+        assert sch.submit(L, N) is not None
+    expect = {
+        1: ([], [0] * 30, list(range(30))),                               # B: 30 + 30 > 40 positions
+        2: ([], [0] + [1] * 30 + [2] * 5, [30] + list(range(30)) + list(range(5))),   # D: 36 + 20 > 40
+        3: ([], [0, 1, 2], [31, 30, 5]),                                   # D: 22 cells > 12 free
+        4: ([], [0, 1, 2], [32, 31, 6]),
+        5: ([2], [0, 1], [33, 32]),                                        # C retired: 20 free < 22
+        11: ([0], [1] + [0] * 20, [38] + list(range(20))),                 # A retired: D takes id 0
+    }
+    n = 0
+    while True:
+        retired, pos, seq = sch.next_batch()
+        if not pos:
+            break
+        n += 1
+        if n in expect:
+            assert (retired, seq, pos) == expect[n], n
+        sch.advance()
+    assert n == 12 and sch.useful == 10 + 10 + 3 + 2 and not sch.waiting
 
 def test_f16_dump_pin():
     g = golden("f16_dump.json")
