@@ -13,7 +13,9 @@ The functions keep the C names:
     kv_split_ubatches, kv_split_count, kv_split_ubatch, kv_split_free,
     kv_prepare_cells, kv_seq_rm, kv_seq_cp, kv_seq_pos_max, kv_cells_read,
     kv_stream_n_kv, kv_store, ubatch_attention, ubatch_attention_static_scratch,
-    kv_device_error, kv_device_bytes, kv_launch_count
+    kv_device_error, kv_device_bytes, kv_launch_count,
+    kv_sched_init, kv_sched_free, kv_sched_submit, kv_sched_next, kv_sched_advance, kv_sched_stats
+    (and kv_split_sched_batch: kv_split_ubatches of a scheduler batch)
 """
 
 import ctypes as C
@@ -38,6 +40,8 @@ EXPORTS = [
     "kv_prepare_cells", "kv_seq_rm", "kv_seq_cp", "kv_seq_pos_max", "kv_cells_read", "kv_stream_n_kv",
     "kv_store", "ubatch_attention", "ubatch_attention_static_scratch", "kv_device_error",
     "kv_device_bytes", "kv_launch_count",
+    "kv_sched_init", "kv_sched_free", "kv_sched_submit", "kv_sched_next", "kv_sched_advance",
+    "kv_sched_stats",
 ]
 
 
@@ -69,6 +73,19 @@ class kv_ubatch_info(C.Structure):
                 ("streams", C.POINTER(C.c_int32)), ("cells", C.POINTER(C.c_int32))]
 
 
+class kv_sched_params(C.Structure):
+    _fields_ = [("max_seqs", C.c_int32), ("token_budget", C.c_int32), ("fixed", C.c_int32)]
+
+
+class kv_sched_batch(C.Structure):
+    _fields_ = [("batch", kv_batch), ("n_retired", C.c_int32), ("retired", C.POINTER(C.c_int32))]
+
+
+class kv_sched_info(C.Structure):
+    _fields_ = [("passes", C.c_int64), ("useful", C.c_int64), ("running", C.c_int32),
+                ("waiting", C.c_int32), ("free_cells", C.c_int32)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError("libkvattn.so is not built; run "
@@ -98,6 +115,12 @@ def _load():
         "kv_device_error": (C.c_int, [P]),
         "kv_device_bytes": (C.c_size_t, [P]),
         "kv_launch_count": (C.c_uint64, [P]),
+        "kv_sched_init": (C.c_int, [P, C.POINTER(kv_sched_params), C.POINTER(P)]),
+        "kv_sched_free": (None, [P]),
+        "kv_sched_submit": (C.c_int, [P, C.c_int32, C.c_int32]),
+        "kv_sched_next": (C.c_int, [P, C.POINTER(kv_sched_batch)]),
+        "kv_sched_advance": (C.c_int, [P]),
+        "kv_sched_stats": (C.c_int, [P, C.POINTER(kv_sched_info)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -262,6 +285,14 @@ def kv_split_ubatches(c, pos, seq_id=None, n_seq_id=None, mode=KV_SPLIT_AUTO, n_
     return Split(out.value, c)
 
 
+def kv_split_sched_batch(c, b, mode=KV_SPLIT_AUTO):
+    """kv_split_ubatches of a scheduler batch (a SchedBatch from kv_sched_next),
+    passed through as the C struct it is."""
+    out = C.c_void_p()
+    _check(c, lib.kv_split_ubatches(c, C.byref(b.raw.batch), mode, C.byref(out)))
+    return Split(out.value, c)
+
+
 def kv_split_count(s):
     return lib.kv_split_count(s)
 
@@ -351,3 +382,63 @@ def kv_device_bytes(c):
 
 def kv_launch_count(c):
     return lib.kv_launch_count(c)
+
+
+# ---- iteration-level batching (host) -----------------------------------------------
+
+class Sched:
+    """Handle returned by kv_sched_init (keeps its cache alive)."""
+
+    def __init__(self, ptr, cache):
+        self.ptr = ptr
+        self.cache = cache
+
+    @property
+    def _as_parameter_(self):
+        return self.ptr
+
+
+class SchedBatch:
+    """One pass's batch from kv_sched_next: n_tokens, pos and seq (copies),
+    retired ids; raw is the C struct (its arrays live until the next call)."""
+
+    def __init__(self, raw):
+        self.raw = raw
+        n = raw.batch.n_tokens
+        self.n_tokens = n
+        self.pos = np.ctypeslib.as_array(raw.batch.pos, (n,)).copy() if n else np.zeros(0, np.int32)
+        self.seq = np.array([raw.batch.seq_id[i][0] for i in range(n)], dtype=np.int32)
+        self.retired = [raw.retired[i] for i in range(raw.n_retired)]
+
+
+def kv_sched_init(c, max_seqs, token_budget, fixed=False):
+    p = kv_sched_params(max_seqs, token_budget, 1 if fixed else 0)
+    out = C.c_void_p()
+    _check(c, lib.kv_sched_init(c, C.byref(p), C.byref(out)))
+    return Sched(out.value, c)
+
+
+def kv_sched_free(s):
+    lib.kv_sched_free(s)
+    s.ptr = None
+
+
+def kv_sched_submit(s, prompt_len, max_new):
+    return _check(s.cache, lib.kv_sched_submit(s, prompt_len, max_new))
+
+
+def kv_sched_next(s):
+    raw = kv_sched_batch()
+    _check(s.cache, lib.kv_sched_next(s, C.byref(raw)))
+    return SchedBatch(raw)
+
+
+def kv_sched_advance(s):
+    return _check(s.cache, lib.kv_sched_advance(s))
+
+
+def kv_sched_stats(s):
+    st = kv_sched_info()
+    _check(s.cache, lib.kv_sched_stats(s, C.byref(st)))
+    return {"passes": st.passes, "useful": st.useful, "running": st.running,
+            "waiting": st.waiting, "free_cells": st.free_cells}

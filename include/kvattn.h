@@ -341,6 +341,62 @@ size_t kv_device_bytes(const kv_cache *c);
 /* Number of CUDA kernels this cache has launched so far (all entry points). */
 uint64_t kv_launch_count(const kv_cache *c);
 
+/* ------------------------------------------------------------------------
+ * Iteration-level (continuous) batching over one cache.  ITER, "The loop that
+ * replaces the batch": before every pass the scheduler retires the finished
+ * sequences (kv_seq_rm of all their cells), admits waiting requests first come,
+ * first served while both budgets allow, and assembles the batch -- a newly
+ * admitted sequence contributes its whole prompt (positions 0 .. L - 1), a
+ * running one a single token (position L + generated - 1).  "The budget that
+ * actually binds": the token budget counts positions per pass; the cache budget
+ * is the page's conservative one, prompt + max_new cells reserved at admission
+ * and released at retirement.  A request of N new tokens takes N passes.  A new
+ * sequence takes the smallest sequence id not running.  Host only: the caller
+ * runs each batch through kv_split_ubatches / kv_prepare_cells / kv_store /
+ * ubatch_attention, then calls kv_sched_advance.  The cache must be unified
+ * (n_stream 1) and used by this scheduler alone.
+ * ------------------------------------------------------------------------ */
+typedef struct kv_sched kv_sched;
+
+typedef struct kv_sched_params {
+    int32_t max_seqs;      /* sequences running at once: 1 .. n_seq_max */
+    int32_t token_budget;  /* positions per pass: >= max_seqs */
+    int32_t fixed;         /* 1: admit only into an empty batch (a classical fixed batch) */
+} kv_sched_params;
+
+typedef struct kv_sched_batch {
+    kv_batch batch;        /* this pass's tokens, one sequence id each: pass it to kv_split_ubatches */
+    int32_t n_retired;     /* sequences retired before this pass, and their ids */
+    const int32_t *retired;
+} kv_sched_batch;          /* arrays owned by the scheduler, valid until its next kv_sched_next */
+
+typedef struct kv_sched_info {
+    int64_t passes;        /* passes advanced */
+    int64_t useful;        /* tokens produced: the sequences of each advanced pass, summed */
+    int32_t running;       /* sequences admitted and not retired */
+    int32_t waiting;       /* requests not admitted yet */
+    int32_t free_cells;    /* cells no running sequence has reserved */
+} kv_sched_info;           /* duty cycle (ITER, "Two resources idled by a fixed batch"):
+                              useful / (passes * max_seqs) */
+
+/* Errors: KV_E_INVAL (bad parameters, n_stream != 1, max_seqs > n_seq_max). */
+int kv_sched_init(kv_cache *c, const kv_sched_params *p, kv_sched **out);
+void kv_sched_free(kv_sched *s);
+
+/* Queue a request of prompt_len prompt tokens and max_new new tokens; returns
+ * its id (0, 1, ...), or KV_E_INVAL when it could never run (a prompt longer
+ * than the token budget, prompt + max_new over the cache, a length < 1). */
+int kv_sched_submit(kv_sched *s, int32_t prompt_len, int32_t max_new);
+
+/* Retire, admit, assemble (see above).  out->batch.n_tokens == 0: nothing is
+ * left to run.  Errors: KV_E_ORDER (the previous batch was not advanced). */
+int kv_sched_next(kv_sched *s, kv_sched_batch *out);
+
+/* The pass of the last batch ran: each of its sequences has one more token. */
+int kv_sched_advance(kv_sched *s);
+
+int kv_sched_stats(const kv_sched *s, kv_sched_info *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -15,6 +15,7 @@ import continuous_batching_kv_gb300 as kv
 from oracle import batch as B, params as P
 from oracle.cells import NO_SLOT
 from oracle.session import OracleKV
+from oracle import sched as S
 from workloads import configs
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -233,3 +234,66 @@ def test_workload_worked_numbers():
     assert kv.kv_prepare_cells(c, s) == 0
     fill = [int((kv.kv_cells_read(c, st, 64)[0] >= 0).sum()) for st in range(4)]
     assert fill == [5136, 7686, 7905, 7905]
+
+
+@pytest.mark.parametrize("fixed", [False, True])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_scheduler_matches_oracle(fixed, seed):
+    # the native scheduler against the oracle's, pass by pass; every batch is
+    # split and placed in both caches and the cell states compared (retirement
+    # frees the cells the next admissions take)
+    rng = random.Random(100 * seed + fixed)
+    kv_size, budget = 300, 48
+    c, o = _pair(n_ctx=kv_size, n_batch=budget, n_ubatch=16, n_seq_max=6, n_stream=1)
+    sch = kv.kv_sched_init(c, max_seqs=4, token_budget=budget, fixed=fixed)
+    osch = S.Scheduler(kv_size=kv_size, n_seq_max=6, max_seqs=4, token_budget=budget, fixed=fixed)
+    for _ in range(40):
+        L, N = rng.randint(1, 60), rng.randint(1, 40)
+        rid = osch.submit(L, N)
+        if rid is None:
+            with pytest.raises(kv.KvError) as ei:
+                kv.kv_sched_submit(sch, L, N)
+            assert ei.value.code == kv.KV_E_INVAL
+        else:
+            assert kv.kv_sched_submit(sch, L, N) == rid
+    passes = 0
+    while True:
+        b = kv.kv_sched_next(sch)
+        retired, pos, seq = osch.next_batch()
+        for q in retired:
+            o.seq_rm(q, 0, -1)
+        assert b.retired == retired and list(b.pos) == pos and list(b.seq) == seq
+        if not pos:
+            break
+        s = kv.kv_split_sched_batch(c, b)
+        assert kv.kv_prepare_cells(c, s) == 0
+        code, _ = o.split(pos, [[q] for q in seq], keep_snapshots=False)
+        assert code == 0
+        _compare_state(c, o)
+        kv.kv_split_free(s)
+        kv.kv_sched_advance(sch)
+        osch.advance()
+        passes += 1
+    st = kv.kv_sched_stats(sch)
+    assert (st["passes"], st["useful"], st["running"], st["waiting"]) == (osch.passes, osch.useful, 0, 0)
+    assert st["free_cells"] == kv_size and passes == osch.passes
+    kv.kv_sched_free(sch)
+
+
+def test_scheduler_errors():
+    c = kv.kv_init(n_ctx=64, n_batch=16, n_ubatch=8, n_seq_max=4, n_stream=2)
+    with pytest.raises(kv.KvError) as ei:
+        kv.kv_sched_init(c, 2, 16)                  # needs a unified cache
+    assert ei.value.code == kv.KV_E_INVAL
+    c = kv.kv_init(n_ctx=64, n_batch=16, n_ubatch=8, n_seq_max=4)
+    for ms, tb in ((5, 16), (0, 16), (4, 3)):
+        with pytest.raises(kv.KvError):
+            kv.kv_sched_init(c, ms, tb)
+    sch = kv.kv_sched_init(c, 2, 16)
+    assert kv.kv_sched_submit(sch, 4, 2) == 0
+    b = kv.kv_sched_next(sch)
+    assert b.n_tokens == 4
+    with pytest.raises(kv.KvError) as ei:
+        kv.kv_sched_next(sch)                       # the batch was not advanced
+    assert ei.value.code == kv.KV_E_ORDER
+    kv.kv_sched_free(sch)
