@@ -55,6 +55,10 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
                     help="run fewer layers than the workload has (small cases for profiling only)")
+    ap.add_argument("--loop", action="store_true",
+                    help="iteration-level batching loop (native scheduler), fixed batch vs continuous")
+    ap.add_argument("--loop-copies", type=int, default=2,
+                    help="--loop: requests per output length (the page's eight lengths)")
     return ap.parse_args()
 
 
@@ -656,6 +660,94 @@ def run_reference(args, cfg):
             "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+LOOP_LENGTHS = [64, 128, 256, 512, 512, 1024, 1024, 2048]   # ITER: the fixed batch's eight output lengths
+
+
+def run_loop(args, device):
+    """The iteration-level batching loop through the native scheduler and the
+    attention path: requests with the page's eight output lengths (each
+    --loop-copies times, first come first served, 128-token prompts), eight
+    sequences at a time, 2048 positions per pass, Qwen3-0.6B attention shape over
+    28 layers.  Each pass: kv_sched_next, split + prepare, kv_store and
+    ubatch_attention per ubatch and layer, kv_sched_advance.  Run once as a fixed
+    batch (admission only into an empty batch) and once continuously; reports
+    tokens/s (new tokens over the loop's device time) and the duty cycle
+    (new tokens over passes x 8 slots: ITER, "Two resources idled by a fixed
+    batch")."""
+    import torch
+    import continuous_batching_kv_gb300 as kv
+    torch.cuda.set_device(device)
+    sh = configs.QWEN
+    H, Hk, d, L = sh["n_head"], sh["n_head_kv"], sh["head_dim"], sh["n_layer"]
+    max_seqs, budget, prompt = 8, 2048, 128
+    n_ctx = 24576                       # >= 8 reservations of prompt + 2048
+    gen = torch.Generator(device=device)
+    gen.manual_seed(7)
+    rnd = lambda *shape: torch.randn(*shape, generator=gen, device=device, dtype=torch.float32).half()
+    q = [rnd(budget, H, d) for _ in range(L)]
+    kk = [rnd(budget, Hk * d) for _ in range(L)]
+    vv = [rnd(budget, Hk * d) for _ in range(L)]
+    o = torch.empty(budget, H, d, device=device)
+    kc = [torch.zeros(n_ctx, Hk * d, dtype=torch.float16, device=device) for _ in range(L)]
+    vc = [torch.zeros_like(t) for t in kc]
+
+    def loop(fixed, requests):
+        c = kv.kv_init(n_ctx=n_ctx, n_batch=budget, n_ubatch=512, n_seq_max=max_seqs, n_layer=L,
+                       n_head=H, n_head_kv=Hk, head_dim=d, k_layers=kc, v_layers=vc)
+        sch = kv.kv_sched_init(c, max_seqs, budget, fixed)
+        for n_new in requests:
+            kv.kv_sched_submit(sch, prompt, n_new)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_host = time.perf_counter()
+        e0.record()
+        while True:
+            b = kv.kv_sched_next(sch)
+            if b.n_tokens == 0:
+                break
+            sp = kv.kv_split_sched_batch(c, b)
+            assert kv.kv_prepare_cells(c, sp) == 0
+            for k in range(kv.kv_split_count(sp)):
+                n = kv.kv_split_ubatch(sp, k)["n_tokens"]
+                for layer in range(L):
+                    kv.kv_store(c, sp, k, layer, kk[layer][:n], vv[layer][:n])
+                    kv.ubatch_attention(c, sp, k, layer, q[layer][:n], o[:n])
+            kv.kv_split_free(sp)
+            kv.kv_sched_advance(sch)
+        e1.record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t_host
+        st = kv.kv_sched_stats(sch)
+        assert kv.kv_device_error(c) == 0
+        launches = kv.kv_launch_count(c)
+        kv.kv_sched_free(sch)
+        kv.kv_free(c)
+        ms = e0.elapsed_time(e1)
+        return {"passes": st["passes"], "new_tokens": st["useful"],
+                "duty_cycle": round(st["useful"] / (st["passes"] * max_seqs), 4),
+                "ms": round(ms, 1), "host_wall_ms": round(1e3 * wall, 1),
+                "tokens_per_s": round(st["useful"] / (ms / 1e3), 1), "gpu_launches": launches}
+
+    loop(False, [64, 8, 8])             # warm-up (kernels loaded, clocks up)
+    requests = [n for _ in range(args.loop_copies) for n in LOOP_LENGTHS]
+    clocks = Clocks(device)
+    clocks.start()
+    w0 = datetime.datetime.now()
+    fixed = loop(True, requests)
+    cont = loop(False, requests)
+    clocks.mark(w0, datetime.datetime.now())
+    return {"metric": "iteration-loop new tokens/s", "value": cont["tokens_per_s"], "unit": "tokens/s",
+            "higher_is_better": True, "n_gpus": 1, "dtype": "f16 in, f32 accumulate",
+            "data": "synthetic N(0,1) fp16 Q/K/V (seeded); no weights",
+            "config": {"workload": "iteration-loop-qwen-%dx8req" % args.loop_copies,
+                       "output_lengths": LOOP_LENGTHS, "copies": args.loop_copies, "prompt_len": prompt,
+                       "max_seqs": max_seqs, "token_budget": budget, "n_layer": L, "n_head": H,
+                       "n_head_kv": Hk, "head_dim": d, "cache_budget": "prompt + max_new reserved at admission"},
+            "continuous": cont, "fixed": fixed,
+            "speedup_vs_fixed": round(cont["tokens_per_s"] / fixed["tokens_per_s"], 3),
+            "clocks": clocks.stop()}
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -665,6 +757,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, cfg)), flush=True)
+        return
+    if args.loop:
+        if rank == 0:
+            print(json.dumps(run_loop(args, local)), flush=True)
         return
     import torch
     if world > 1:
