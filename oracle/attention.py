@@ -55,7 +55,7 @@ def attend_row(q_row, k_cache, v_cache, s, vis, n_head, n_head_kv):
 
 
 def ubatch_attention(q, k_cache, v_cache, state, row_pos, row_seq0, row_stream,
-                     n_kv, causal, n_head, n_head_kv, rows=None):
+                     n_kv, causal, n_head, n_head_kv, rows=None, n_swa=0):
     """o[i, h, :] for the ubatch rows (all rows, or the listed subset).
 
     ``state`` must be the cell state this ubatch sees (after its own cells were
@@ -67,7 +67,7 @@ def ubatch_attention(q, k_cache, v_cache, state, row_pos, row_seq0, row_stream,
     d = q.shape[-1]
     out = np.zeros((len(rows), n_head, d), dtype=np.float64)
     for n, i in enumerate(rows):
-        vis = visible_row(state, row_stream[i], row_seq0[i], row_pos[i], n_kv, causal)
+        vis = visible_row(state, row_stream[i], row_seq0[i], row_pos[i], n_kv, causal, n_swa)
         out[n] = attend_row(q[i], k_cache, v_cache, row_stream[i], vis, n_head, n_head_kv)
     return out
 

@@ -38,7 +38,7 @@ class Split:
 class OracleKV:
     def __init__(self, n_ctx, n_batch=P.DEFAULT_N_BATCH, n_ubatch=P.DEFAULT_N_UBATCH,
                  n_seq_max=1, n_stream=1, n_layer=1, n_head=16, n_head_kv=8,
-                 head_dim=128, causal=True, seq_to_stream=None, keep_kv=True):
+                 head_dim=128, causal=True, seq_to_stream=None, keep_kv=True, n_swa=0):
         assert n_ctx % n_stream == 0
         self.n_batch, self.n_ubatch = P.clamp(n_ctx, n_batch, n_ubatch, causal)
         self.n_ctx, self.n_stream = n_ctx, n_stream
@@ -46,6 +46,7 @@ class OracleKV:
         self.n_seq_max = n_seq_max
         self.n_layer, self.n_head, self.n_head_kv, self.head_dim = n_layer, n_head, n_head_kv, head_dim
         self.causal = causal
+        self.n_swa = n_swa      # sliding window in positions (0: none)
         self.state = C.CellState(n_stream, self.kv_size, n_seq_max, seq_to_stream)
         self.k = self.v = None
         if keep_kv:
@@ -83,7 +84,7 @@ class OracleKV:
 
     def mask(self, sp, k):
         return M.kq_mask(sp.snapshots[k], sp.row_pos(k), sp.row_seq0(k),
-                         sp.streams[k], sp.n_kv[k], self.causal)
+                         sp.streams[k], sp.n_kv[k], self.causal, self.n_swa)
 
     def attention(self, sp, k, layer, q, rows=None, state=None):
         """q: [n_tokens of ubatch k, n_head, head_dim] fp16 -> float64 output."""
@@ -91,7 +92,7 @@ class OracleKV:
         return A.ubatch_attention(np.asarray(q), self.k[layer], self.v[layer], st,
                                   sp.row_pos(k), sp.row_seq0(k), sp.streams[k],
                                   sp.n_kv[k], self.causal, self.n_head, self.n_head_kv,
-                                  rows=rows)
+                                  rows=rows, n_swa=self.n_swa)
 
     def seq_rm(self, q, p0, p1):
         return self.state.seq_rm(q, p0, p1)

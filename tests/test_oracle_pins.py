@@ -455,9 +455,27 @@ def test_mask_vector_equals_pairwise_random():
         rq = rng.integers(0, n_seq, n).tolist()
         rs = rng.integers(0, 2, n).tolist()
         for causal in (True, False):
-            a = M.kq_mask(st, rp, rq, rs, 24, causal)
-            b = M.kq_mask_bruteforce(st, rp, rq, rs, 24, causal)
-            assert np.array_equal(a, b)
+            for n_swa in (0, 1, 3, 7):
+                a = M.kq_mask(st, rp, rq, rs, 24, causal, n_swa)
+                b = M.kq_mask_bruteforce(st, rp, rq, rs, 24, causal, n_swa)
+                assert np.array_equal(a, b)
+
+
+def test_sliding_window_closed_form():
+    # one sequence, 20 prompt cells, a window of w = 5 positions: causal row i
+    # sees cells max(0, i - 4) .. i, min(i + 1, 5) of them; without causality
+    # the window still drops cells more than 4 positions back, nothing ahead
+    w, T = 5, 20
+    for causal in (True, False):
+        kv = OracleKV(n_ctx=32, n_batch=32, n_ubatch=32, n_layer=1, n_head=2, n_head_kv=1,
+                      head_dim=4, keep_kv=False, causal=causal, n_swa=w)
+        code, sp = kv.split(list(range(T)), [[0]] * T)
+        m = kv.mask(sp, 0) == M.F16_ZERO
+        for i in range(T):
+            hi = i if causal else T - 1
+            assert set(np.flatnonzero(m[i])) == set(range(max(0, i - w + 1), hi + 1)), (causal, i)
+        if causal:
+            assert m.sum(axis=1).tolist() == [min(i + 1, w) for i in range(T)]
 
 
 # ----------------------------------------------------------------------------
@@ -510,6 +528,24 @@ def test_attention_chunked_with_explicit_mask_equals_sdpa():
     ref = _torch_sdpa(q[Ccache:], k, v, attn_mask=allowed)
     np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
 
+
+
+def test_attention_sliding_window_equals_banded_sdpa():
+    # a causal prompt under a window of 6 positions: the softmax over each row's
+    # last six keys, which SDPA gives with an explicit banded mask
+    d, H, Hk, T, w = 8, 4, 2, 23, 6
+    kv = OracleKV(n_ctx=32, n_batch=32, n_ubatch=32, n_layer=1, n_head=H, n_head_kv=Hk,
+                  head_dim=d, n_swa=w)
+    k = gen.uniform_f16(14, (T, Hk, d))
+    v = gen.uniform_f16(15, (T, Hk, d))
+    q = gen.uniform_f16(16, (T, H, d))
+    code, sp = kv.split(list(range(T)), [[0]] * T)
+    kv.store(sp, 0, 0, k.reshape(T, -1), v.reshape(T, -1))
+    out = kv.attention(sp, 0, 0, q)
+    band = np.zeros((T, T), dtype=bool)
+    for i in range(T):
+        band[i, max(0, i - w + 1):i + 1] = True
+    np.testing.assert_allclose(out, _torch_sdpa(q, k, v, attn_mask=band), rtol=1e-12, atol=1e-12)
 
 def test_attention_loops_equal_vectorised():
     rng = np.random.default_rng(11)
