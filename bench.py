@@ -22,6 +22,7 @@ import argparse
 import datetime
 import json
 import os
+import re
 import select
 import statistics
 import subprocess
@@ -55,6 +56,12 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
                     help="run fewer layers than the workload has (small cases for profiling only)")
+    ap.add_argument("--ubatch", type=int, default=None,
+                    help="override the workload's n_ubatch (the n_ubatch sweep)")
+    ap.add_argument("--streams", type=int, default=None,
+                    help="override n_stream (sequence q in stream q %% n_stream); with --kv-per-stream")
+    ap.add_argument("--kv-per-stream", type=int, default=None,
+                    help="with --streams: cells per stream (n_ctx = streams x this)")
     ap.add_argument("--loop", action="store_true",
                     help="iteration-level batching loop (native scheduler), fixed batch vs continuous")
     ap.add_argument("--loop-copies", type=int, default=2,
@@ -440,11 +447,28 @@ class OursArm:
         return last
 
 
+def apply_overrides(cfg, args):
+    """--ubatch / --streams: the same workload at another n_ubatch, or with one
+    cache stream per sequence group instead of the unified cache (KV-MEM,
+    "Unified versus non-unified"); the workload's name records the change."""
+    prm = cfg["params"]
+    if args.ubatch is not None:
+        prm["n_ubatch"] = args.ubatch
+        cfg["name"] = re.sub(r"-ub\d+", "", cfg["name"]) + "-ub%d" % args.ubatch
+    if args.streams is not None:
+        per = args.kv_per_stream or prm["n_ctx"] // args.streams
+        prm["n_stream"] = args.streams
+        prm["n_ctx"] = args.streams * per
+        prm.pop("seq_to_stream", None)
+        cfg["name"] += "-streams%dx%d" % (args.streams, per)
+    return cfg
+
+
 def run_ours(args, rank, world, device):
     import torch
     import continuous_batching_kv_gb300 as kv
     torch.cuda.set_device(device)
-    cfg = configs.config(args.config, n_layer=args.layers)
+    cfg = apply_overrides(configs.config(args.config, n_layer=args.layers), args)
     arm = OursArm(cfg, device)
     hbm, tflops, peak_src = load_peaks()
     dist = world > 1
@@ -753,7 +777,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    cfg = configs.config(args.config, n_layer=args.layers)
+    cfg = apply_overrides(configs.config(args.config, n_layer=args.layers), args)
+    if args.ubatch is not None or args.streams is not None:
+        args.no_cpu = True      # the oracle sample reads the stock workload
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, cfg)), flush=True)

@@ -55,7 +55,7 @@ class kv_params(C.Structure):
     _fields_ = [("n_ctx", C.c_int32), ("n_batch", C.c_int32), ("n_ubatch", C.c_int32),
                 ("n_seq_max", C.c_int32), ("n_stream", C.c_int32), ("n_layer", C.c_int32),
                 ("n_head", C.c_int32), ("n_head_kv", C.c_int32), ("head_dim", C.c_int32),
-                ("causal", C.c_int32), ("seq_to_stream", C.POINTER(C.c_int32)),
+                ("causal", C.c_int32), ("n_swa", C.c_int32), ("seq_to_stream", C.POINTER(C.c_int32)),
                 ("k_layers", C.POINTER(C.c_void_p)), ("v_layers", C.POINTER(C.c_void_p))]
 
 
@@ -184,7 +184,7 @@ class Split:
 
 def kv_init(n_ctx, n_batch=2048, n_ubatch=512, n_seq_max=1, n_stream=1, n_layer=1,
             n_head=16, n_head_kv=8, head_dim=128, causal=True, seq_to_stream=None,
-            k_layers=None, v_layers=None):
+            k_layers=None, v_layers=None, n_swa=0):
     """Create a cache.  k_layers / v_layers: lists of device tensors (or
     addresses), one per layer, each [n_stream * kv_size, n_head_kv * head_dim]
     fp16; None for a host-only cache."""
@@ -192,6 +192,7 @@ def kv_init(n_ctx, n_batch=2048, n_ubatch=512, n_seq_max=1, n_stream=1, n_layer=
     p.n_ctx, p.n_batch, p.n_ubatch = n_ctx, n_batch, n_ubatch
     p.n_seq_max, p.n_stream, p.n_layer = n_seq_max, n_stream, n_layer
     p.n_head, p.n_head_kv, p.head_dim, p.causal = n_head, n_head_kv, head_dim, int(bool(causal))
+    p.n_swa = n_swa
     keep = []
     if seq_to_stream is not None:
         arr = (C.c_int32 * len(seq_to_stream))(*seq_to_stream)

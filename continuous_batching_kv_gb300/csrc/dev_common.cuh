@@ -38,27 +38,13 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 
 // Everything a kernel needs to decide whether row i sees cell j.
 // "llama.cpp and the ubatch", "The mask is doing the work": the cell must be
-// occupied, hold the row's first sequence id, and (causal) not be later than
-// the row.  Cells reserved by later ubatches of the same batch carry a larger
-// epoch and are not visible yet ("Batch、Ubatch 与解码主循环", Part D).
-struct CellView {
-    const int32_t *pos;       // [n_cells]
-    const uint32_t *epoch;    // [n_cells]
-    const uint64_t *bits;     // [n_cells * n_words]
-    int32_t n_words;
-    uint32_t ub_epoch;
-    int32_t causal;
-};
-
-// Sequence-membership and epoch part of the rule (same for every row of a
-// block, since a block shares its first sequence id).
-__device__ __forceinline__ bool cell_has_seq(const CellView &cv, int64_t g, int32_t seq0) {
-    uint64_t w = cv.bits[g * cv.n_words + (seq0 >> 6)];
-    return ((w >> (seq0 & 63)) & 1ull) && cv.epoch[g] <= cv.ub_epoch;
-}
-
-__device__ __forceinline__ bool row_sees(const CellView &cv, int32_t cell_pos, int32_t row_pos) {
-    return !cv.causal || cell_pos <= row_pos;
+// occupied, hold the row's first sequence id, not come from a later ubatch of
+// the same batch (a larger epoch, "Batch、Ubatch 与解码主循环", Part D), and --
+// the position part, tested here -- not be later than the row under causal
+// attention nor n_swa or more positions behind it under a sliding window
+// (n_swa 0: none).
+__device__ __forceinline__ bool pos_visible(int32_t causal, int32_t n_swa, int32_t row_pos, int32_t cell_pos) {
+    return (!causal || cell_pos <= row_pos) && (n_swa <= 0 || (int64_t)row_pos - cell_pos < n_swa);
 }
 
 // ---- shared-memory addresses ---------------------------------------------

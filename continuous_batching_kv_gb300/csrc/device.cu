@@ -127,6 +127,7 @@ kvk::UbView make_view(const kv_cache *c, const kv_split *sp, int32_t ub) {
     v.n_words = c->n_words;
     v.ub_epoch = u.epoch;
     v.causal = c->prm.causal;
+    v.n_swa = c->prm.n_swa;
     v.kv_size = c->kv_size;
     v.n_kv = u.n_kv;
     v.n_tokens = u.n_tokens;

@@ -359,7 +359,7 @@ int kv_init(const kv_params *p, kv_cache **out) {
         p->n_seq_max > KV_MAX_SEQ || p->n_stream < 1 || p->n_stream > p->n_seq_max ||
         p->n_ctx % p->n_stream != 0 || p->n_layer < 1 || p->n_head < 1 || p->n_head_kv < 1 ||
         p->n_head % p->n_head_kv != 0 || p->n_head / p->n_head_kv > 8 ||
-        p->head_dim != KV_HEAD_DIM || (p->causal != 0 && p->causal != 1))
+        p->head_dim != KV_HEAD_DIM || (p->causal != 0 && p->causal != 1) || p->n_swa < 0)
         return KV_E_INVAL;
     if ((p->k_layers == nullptr) != (p->v_layers == nullptr)) return KV_E_INVAL;
     kv_cache *c = new (std::nothrow) kv_cache();

@@ -450,8 +450,8 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 }
                 const bool h0 = full || x.meta[st].has[c0], h1 = full || x.meta[st].has[c1];
                 const int32_t p0 = full ? 0 : x.meta[st].cpos[c0], p1 = full ? 0 : x.meta[st].cpos[c1];
-                const bool v0 = h0 && nl < nq && (full || !a.u.causal || p0 <= rp_l);
-                const bool v1 = h1 && nl < nq && (full || !a.u.causal || p1 <= rp_l);
+                const bool v0 = h0 && nl < nq && (full || kvd::pos_visible(a.u.causal, a.u.n_swa, rp_l, p0));
+                const bool v1 = h1 && nl < nq && (full || kvd::pos_visible(a.u.causal, a.u.n_swa, rp_l, p1));
                 const float s0 = v0 ? scv[0] * a.scale_log2 : -INFINITY;
                 const float s1 = v1 ? scv[1] * a.scale_log2 : -INFINITY;
                 // ---- online softmax of query nl over my warp's 8 cells ----
@@ -531,8 +531,8 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 // ---- online softmax over my warp's 8 cells (warp-uniform decisions) ----
 #pragma unroll
                 for (int n = 0; n < NQ; ++n) {
-                    const bool v0 = h0 && n < nq && (full || !a.u.causal || p0 <= rp[n]);
-                    const bool v1 = h1 && n < nq && (full || !a.u.causal || p1 <= rp[n]);
+                    const bool v0 = h0 && n < nq && (full || kvd::pos_visible(a.u.causal, a.u.n_swa, rp[n], p0));
+                    const bool v1 = h1 && n < nq && (full || kvd::pos_visible(a.u.causal, a.u.n_swa, rp[n], p1));
                     const float s0 = v0 ? sc[0][n] * a.scale_log2 : -INFINITY;
                     const float s1 = v1 ? sc[1][n] * a.scale_log2 : -INFINITY;
                     float t = fmaxf(s0, s1);
@@ -615,7 +615,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     float v = s[n];
                     v += __shfl_xor_sync(0xffffffffu, v, 1);
                     v += __shfl_xor_sync(0xffffffffu, v, 2);
-                    const bool vis = has && n < nq && (full || !a.u.causal || cpos <= x.rpos[n]);
+                    const bool vis = has && n < nq && (full || kvd::pos_visible(a.u.causal, a.u.n_swa, x.rpos[n], cpos));
                     s[n] = vis ? v * a.scale_log2 : -INFINITY;
                 }
                 // ---- online softmax over my warp's 8 cells (warp-uniform decisions) ----

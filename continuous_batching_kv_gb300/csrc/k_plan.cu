@@ -1,8 +1,9 @@
 // K2: the KQ-mask builder.
 //
 // "llama.cpp and the ubatch", "The mask is doing the work": row i sees cell j
-// iff the cell is occupied, holds seq_id[i][0], and (causal) pos_j <= pos_i;
-// everything else is -inf before the softmax.  The mask is built on the
+// iff the cell is occupied, holds seq_id[i][0], (causal) pos_j <= pos_i, and
+// (sliding window of n_swa positions) pos_i - pos_j < n_swa; everything else is
+// -inf before the softmax.  The mask is built on the
 // device from the cell mirror (position, sequence bitset, and the serial of
 // the ubatch that reserved the cell), once per ubatch, and reused by every
 // layer.  Two products:
@@ -24,13 +25,18 @@ using kvi::TILE;
 using kvi::SUB;
 
 // Rows of block b that see a cell at position cpos (sequence and epoch
-// already checked).
+// already checked).  The row positions that see it form one interval (from
+// cpos under causal attention, to cpos + n_swa - 1 under a window), so the
+// block's rows (positions pos_min .. pos_max) all see it when both ends do, and
+// none does when the interval misses that range.
 __device__ __forceinline__ int32_t rows_seeing(const kvk::UbView &u, const kvi::DevBlock &b,
                                                int32_t cpos) {
-    if (!u.causal || cpos <= b.pos_min) return b.n_rows;
-    if (cpos > b.pos_max) return 0;
+    if (kvd::pos_visible(u.causal, u.n_swa, b.pos_min, cpos) && kvd::pos_visible(u.causal, u.n_swa, b.pos_max, cpos))
+        return b.n_rows;
+    if ((u.causal && cpos > b.pos_max) || (u.n_swa > 0 && (int64_t)b.pos_min - cpos >= u.n_swa)) return 0;
     int32_t n = 0;
-    for (int32_t k = 0; k < b.n_rows; ++k) n += (cpos <= u.rows[u.perm[b.row0 + k]].pos) ? 1 : 0;
+    for (int32_t k = 0; k < b.n_rows; ++k)
+        n += kvd::pos_visible(u.causal, u.n_swa, u.rows[u.perm[b.row0 + k]].pos, cpos) ? 1 : 0;
     return n;
 }
 
@@ -495,7 +501,7 @@ __global__ void __launch_bounds__(256) k_mask(kvk::UbView u, uint16_t *mask) {
         const uint64_t w = u.cell_bits[g * u.n_words + (r.seq0 >> 6)];
         vis = (w >> (r.seq0 & 63)) & 1ull;
     }
-    if (vis && u.causal) vis = u.cell_pos[g] <= r.pos;
+    if (vis) vis = kvd::pos_visible(u.causal, u.n_swa, r.pos, u.cell_pos[g]);
     mask[(int64_t)i * u.n_kv + j] = vis ? (uint16_t)0x0000 : (uint16_t)0xFC00;
 }
 

@@ -332,7 +332,9 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                             }
                             mhas[r] = has;
                             mpos[r] = cp;
-                            many[r] = has && (!a.u.causal || cp <= kb.pos_max);
+                            // some row of the block (positions pos_min .. pos_max) may see it
+                            many[r] = has && (!a.u.causal || cp <= kb.pos_max) &&
+                                      (a.u.n_swa <= 0 || (int64_t)kb.pos_min - cp < a.u.n_swa);
                         }
                     }
                     have_k = true;
@@ -588,7 +590,13 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     for (int q = 0; q < 2; ++q) hb[q] = hs[q];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) cp[q] = cs[q];
+                    // positions this row sees: lo .. lim (up to its own under causal
+                    // attention, from rpos - n_swa + 1 under a sliding window; positions
+                    // are >= 0, so lo does not overflow and lo <= lim), tested as one
+                    // unsigned compare
                     const int32_t lim = a.u.causal ? rpos : INT32_MAX;
+                    const int32_t lo = a.u.n_swa > 0 ? rpos - a.u.n_swa + 1 : INT32_MIN;
+                    const uint32_t span = (uint32_t)lim - (uint32_t)lo;
                     uint32_t vm = 0;
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
@@ -596,7 +604,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         const int32_t c4[4] = {cp[q].x, cp[q].y, cp[q].z, cp[q].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const bool vis = ((hw >> (8 * e)) & 0xffu) != 0 && c4[e] <= lim;
+                            const bool vis = ((hw >> (8 * e)) & 0xffu) != 0 &&
+                                             (uint32_t)c4[e] - (uint32_t)lo <= span;
                             vm |= (uint32_t)vis << (4 * q + e);
                         }
                     }

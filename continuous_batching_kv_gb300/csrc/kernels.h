@@ -40,6 +40,7 @@ struct UbView {
     const kvi::DevBlock *blocks;  // [n_blocks]
     const int32_t *seq_blk_off;   // [n_seq_max + 1]
     const int32_t *seq_blk;       // [n_blocks]
+    int32_t n_swa;                // sliding window in positions (0: none)
 };
 
 // Attention plan buffers (library-owned device memory).

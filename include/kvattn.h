@@ -80,6 +80,9 @@ typedef struct kv_split kv_split;
  *   n_head_kv     KV heads
  *   head_dim      must be KV_HEAD_DIM
  *   causal        1 = causal attention (mask later positions), 0 = not
+ *   n_swa         sliding window in positions, 0 = none: a cell n_swa or more
+ *                 positions behind the row is masked (UBATCH, "The mask is
+ *                 doing the work": "outside the sliding window"); >= 0
  *   seq_to_stream NULL (sequence q lives in stream q % n_stream) or an array
  *                 of n_seq_max stream indices, copied by kv_init
  *   k_layers, v_layers
@@ -101,6 +104,7 @@ typedef struct kv_params {
     int32_t n_head_kv;
     int32_t head_dim;
     int32_t causal;
+    int32_t n_swa;
     const int32_t *seq_to_stream;
     void *const *k_layers;
     void *const *v_layers;

@@ -43,13 +43,14 @@ class Pair:
                             n_seq_max=prm["n_seq_max"], n_stream=prm["n_stream"], n_layer=self.L,
                             n_head=self.H, n_head_kv=self.Hk, head_dim=self.d,
                             causal=prm.get("causal", True), seq_to_stream=prm.get("seq_to_stream"),
-                            k_layers=self.kt, v_layers=self.vt)
+                            k_layers=self.kt, v_layers=self.vt, n_swa=prm.get("n_swa", 0))
         self.o = None
         if oracle:
             self.o = OracleKV(n_ctx=prm["n_ctx"], n_batch=prm["n_batch"], n_ubatch=prm["n_ubatch"],
                               n_seq_max=prm["n_seq_max"], n_stream=prm["n_stream"], n_layer=self.L,
                               n_head=self.H, n_head_kv=self.Hk, head_dim=self.d,
-                              causal=prm.get("causal", True), seq_to_stream=prm.get("seq_to_stream"))
+                              causal=prm.get("causal", True), seq_to_stream=prm.get("seq_to_stream"),
+                              n_swa=prm.get("n_swa", 0))
 
     def close(self):
         self.kv.kv_free(self.c)

@@ -122,6 +122,26 @@ def test_non_causal_prefill_decode_and_prefix():
     assert len(stats) >= 6
 
 
+@pytest.mark.parametrize("causal,n_swa", [(True, 100), (False, 100), (True, 1)])
+def test_sliding_window(causal, n_swa):
+    # a window of n_swa positions (a cell that far or further behind the row is
+    # masked): 300 prompt tokens in ubatches of 128 (the window cuts tiles, so
+    # both kernels take their per-cell paths), a mixed ubatch with a prompt
+    # shared by sequences 1 and 2, then decode rows; masks bit-exact
+    cfg = {"id": 16, "name": "swa", "shape": dict(configs.QWEN, n_layer=1),
+           "params": dict(n_ctx=1024, n_batch=512, n_ubatch=128, n_seq_max=3, n_stream=1,
+                          causal=causal, n_swa=n_swa),
+           "setup": [],
+           "measured": [
+               {"pos": list(range(300)), "seq": [[0]] * 300, "content": [0] * 300},
+               {"pos": list(range(150)) + [300], "seq": [[1, 2]] * 150 + [[0]],
+                "content": [1] * 150 + [0]},
+               {"pos": [301, 150, 150], "seq": [[0], [1], [2]], "content": [0, 1, 2]},
+           ]}
+    stats, _ = _run(cfg, check_mask=True)
+    assert len(stats) >= 6
+
+
 def test_random_small_batches():
     rng = np.random.default_rng(5)
     calls = []
