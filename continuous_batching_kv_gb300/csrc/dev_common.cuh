@@ -42,9 +42,27 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // the same batch (a larger epoch, "Batch、Ubatch 与解码主循环", Part D), and --
 // the position part, tested here -- not be later than the row under causal
 // attention nor n_swa or more positions behind it under a sliding window
-// (n_swa 0: none).
+// (n_swa 0: none).  Positions are >= 0, so row_pos - cell_pos cannot overflow.
 __device__ __forceinline__ bool pos_visible(int32_t causal, int32_t n_swa, int32_t row_pos, int32_t cell_pos) {
-    return (!causal || cell_pos <= row_pos) && (n_swa <= 0 || (int64_t)row_pos - cell_pos < n_swa);
+    return (!causal || cell_pos <= row_pos) && (n_swa <= 0 || row_pos - cell_pos < n_swa);
+}
+
+// The same test for hot loops: the positions a row sees form one interval
+// lo .. lim (lim = row_pos under causal attention, else INT32_MAX; lo = row_pos -
+// n_swa + 1 under a window, else INT32_MIN).  Positions are >= 0, so lo does not
+// overflow and lo <= lim; a cell position p is inside iff p - lo <= lim - lo in
+// unsigned arithmetic: one subtract and one compare per cell.
+struct PosRange {
+    int32_t lo;
+    uint32_t span;
+};
+__device__ __forceinline__ PosRange pos_range(int32_t causal, int32_t n_swa, int32_t row_pos) {
+    const int32_t lim = causal ? row_pos : INT32_MAX;
+    const int32_t lo = n_swa > 0 ? row_pos - n_swa + 1 : INT32_MIN;
+    return PosRange{lo, (uint32_t)lim - (uint32_t)lo};
+}
+__device__ __forceinline__ bool pos_in(const PosRange &r, int32_t cell_pos) {
+    return (uint32_t)cell_pos - (uint32_t)r.lo <= r.span;
 }
 
 // ---- shared-memory addresses ---------------------------------------------

@@ -590,13 +590,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     for (int q = 0; q < 2; ++q) hb[q] = hs[q];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) cp[q] = cs[q];
-                    // positions this row sees: lo .. lim (up to its own under causal
-                    // attention, from rpos - n_swa + 1 under a sliding window; positions
-                    // are >= 0, so lo does not overflow and lo <= lim), tested as one
-                    // unsigned compare
-                    const int32_t lim = a.u.causal ? rpos : INT32_MAX;
-                    const int32_t lo = a.u.n_swa > 0 ? rpos - a.u.n_swa + 1 : INT32_MIN;
-                    const uint32_t span = (uint32_t)lim - (uint32_t)lo;
+                    // the positions this row sees (causal order, sliding window)
+                    const kvd::PosRange rr = kvd::pos_range(a.u.causal, a.u.n_swa, rpos);
                     uint32_t vm = 0;
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
@@ -604,8 +599,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         const int32_t c4[4] = {cp[q].x, cp[q].y, cp[q].z, cp[q].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const bool vis = ((hw >> (8 * e)) & 0xffu) != 0 &&
-                                             (uint32_t)c4[e] - (uint32_t)lo <= span;
+                            const bool vis = ((hw >> (8 * e)) & 0xffu) != 0 && kvd::pos_in(rr, c4[e]);
                             vm |= (uint32_t)vis << (4 * q + e);
                         }
                     }
