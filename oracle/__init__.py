@@ -24,17 +24,22 @@ Modules
 params     context-parameter clamps (n_batch / n_ubatch)
 batch      batch validation and auto-fill, split_simple / split_equal /
            split_seq, the init_batch strategy choice, caller-side chunking
-cells      per-stream cell state, first-fit slot finder (prepare), n_kv
-mask       the KQ mask rule
+cells      per-stream cell state, first-fit slot finder (prepare), n_kv,
+           sequence removal and sharing (seq_rm / seq_cp)
+mask       the KQ mask rule (causal order, optional sliding window)
 attention  float64 masked-softmax GQA attention and the K/V scatter
 layout     cache sizes, strides, byte offsets, the fixed-batch duty cycle
 session    the whole path for one cache (split, prepare, store, attention)
+sched      the iteration-level batching loop (retire, admit, assemble)
 
 Parity status: every function is pinned by a ``-m "not gpu"`` test against a
 value the pages print, a closed form, a library routine, brute force or an
 invariant, except the exact tie-breaks of split_equal / split_seq and the
 first-fit slot policy, which the pages do not fix (they are pinned only by the
-written reading and by invariants; see each function's docstring).
+written reading and by invariants; see each function's docstring).  The
+sliding-window term and the scheduler's policy details are readings of
+passages that name them without defining them; they are pinned by closed forms,
+brute force, the page's duty cycles and a hand-worked trace.
 """
 
-from . import params, batch, cells, mask, attention, layout, session  # noqa: F401
+from . import params, batch, cells, mask, attention, layout, session, sched  # noqa: F401
