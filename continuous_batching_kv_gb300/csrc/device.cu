@@ -322,93 +322,97 @@ extern "C" {
 
 int kv_store(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer, const void *k_cur,
              const void *v_cur, void *stream) {
-    int rc = check_call(c, sp, ub, layer);
-    if (rc != KV_OK) return rc;
-    if (!k_cur || !v_cur || ((uintptr_t)k_cur & 15) || ((uintptr_t)v_cur & 15))
-        return c->set_err(KV_E_INVAL, "k_cur / v_cur must be 16-byte aligned device pointers");
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if ((rc = sync_device(c, sp, st)) != KV_OK) return rc;
-    const UbatchHost &u = sp->ub[ub];
-    DeviceState *d = c->dev;
-    const DevRow *rows = reinterpret_cast<const DevRow *>(d->d_tables + sp->off_rows[ub]);
-    cudaError_t e = kvk::launch_store(c->k_layers[layer], c->v_layers[layer], k_cur, v_cur, rows, u.n_tokens,
-                                      c->prm.n_head_kv * c->prm.head_dim * 2, (int64_t)c->prm.n_ctx, d->d_err, st);
-    if (e != cudaSuccess) return cuda_fail(c, e, "store launch");
-    c->launches += 1;
-    const_cast<kv_split *>(sp)->stored[layer][ub] = 1;
-    return KV_OK;
+    return guarded(c, [&]() -> int {
+        int rc = check_call(c, sp, ub, layer);
+        if (rc != KV_OK) return rc;
+        if (!k_cur || !v_cur || ((uintptr_t)k_cur & 15) || ((uintptr_t)v_cur & 15))
+            return c->set_err(KV_E_INVAL, "k_cur / v_cur must be 16-byte aligned device pointers");
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        if ((rc = sync_device(c, sp, st)) != KV_OK) return rc;
+        const UbatchHost &u = sp->ub[ub];
+        DeviceState *d = c->dev;
+        const DevRow *rows = reinterpret_cast<const DevRow *>(d->d_tables + sp->off_rows[ub]);
+        cudaError_t e = kvk::launch_store(c->k_layers[layer], c->v_layers[layer], k_cur, v_cur, rows, u.n_tokens,
+                                          c->prm.n_head_kv * c->prm.head_dim * 2, (int64_t)c->prm.n_ctx, d->d_err, st);
+        if (e != cudaSuccess) return cuda_fail(c, e, "store launch");
+        c->launches += 1;
+        const_cast<kv_split *>(sp)->stored[layer][ub] = 1;
+        return KV_OK;
+    });
 }
 
 int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer, const void *q, float *o,
                      void *mask_out, void *stream) {
-    int rc = check_call(c, sp, ub, layer);
-    if (rc != KV_OK) return rc;
-    if (!q || !o || ((uintptr_t)q & 15) || ((uintptr_t)o & 15))
-        return c->set_err(KV_E_INVAL, "q / o must be 16-byte aligned device pointers");
-    for (int32_t k = 0; k <= ub; ++k)
-        if (!sp->stored[layer][k]) return c->set_err(KV_E_ORDER, "attention before its K/V were stored");
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // Nothing of this call precedes the attention kernels when the device is in
-    // sync, the plan is cached and no mask is asked for: then the plan, tables
-    // and mirror were complete before the previous kernel began.
-    bool early_ok = !c->pending_reset && c->pending.empty() && c->dev_tables_split == sp->id && !mask_out;
-    if ((rc = sync_device(c, sp, st)) != KV_OK) return rc;
-    DeviceState *d = c->dev;
-    const UbatchHost &u = sp->ub[ub];
-    kvk::UbView v = make_view(c, sp, ub);
-    cudaError_t e;
-    if (d->plan_split != sp->id || d->plan_ub != ub) {
-        early_ok = false;
-        kvk::Plan p = d->plan;
-        if ((e = kvk::launch_plan(v, p, c->prm.n_stream, d->gx_dec, d->gx_pf, st)) != cudaSuccess)
-            return cuda_fail(c, e, "plan launch");
-        c->launches += 3;
-        d->plan_split = sp->id;
-        d->plan_ub = ub;
-    }
-    if (mask_out) {
-        if ((e = kvk::launch_mask(v, static_cast<uint16_t *>(mask_out), st)) != cudaSuccess)
-            return cuda_fail(c, e, "mask launch");
-        c->launches += 1;
-    }
-    const float scale_log2 = 1.4426950408889634f / sqrtf((float)c->prm.head_dim);
-    if (u.n_dec_blocks > 0) {
-        kvk::DecodeArgs a{};
-        a.u = v;
-        a.p = d->plan;
-        a.q = static_cast<const __half *>(q);
-        a.o = o;
-        a.part = d->d_part_dec;
-        a.n_head = c->prm.n_head;
-        a.n_head_kv = c->prm.n_head_kv;
-        a.gqa = c->gqa;
-        a.scale_log2 = scale_log2;
-        a.err = d->d_err;
-        a.nq_max = decode_nq_max(c, u);
-        a.early_ok = early_ok ? 1 : 0;
-        if ((e = kvk::launch_decode(&d->tm_dec[4 * (size_t)layer], a, d->gx_dec, st)) != cudaSuccess)
-            return cuda_fail(c, e, "decode launch");
-        c->launches += 1;
-    }
-    if (u.n_pf_blocks > 0) {
-        kvk::PrefillArgs a{};
-        a.u = v;
-        a.p = d->plan;
-        a.q = static_cast<const __half *>(q);
-        a.o = o;
-        a.part = d->d_part_pf;
-        a.gx_dec = d->gx_dec;
-        a.n_head = c->prm.n_head;
-        a.n_head_kv = c->prm.n_head_kv;
-        a.gqa = c->gqa;
-        a.scale_log2 = scale_log2;
-        a.err = d->d_err;
-        a.early_ok = early_ok ? 1 : 0;
-        if ((e = kvk::launch_prefill(&d->tm_k[layer], &d->tm_v[layer], a, d->gx_pf, st)) != cudaSuccess)
-            return cuda_fail(c, e, "prefill launch");
-        c->launches += 2;   // attention + split-K merge
-    }
-    return KV_OK;
+    return guarded(c, [&]() -> int {
+        int rc = check_call(c, sp, ub, layer);
+        if (rc != KV_OK) return rc;
+        if (!q || !o || ((uintptr_t)q & 15) || ((uintptr_t)o & 15))
+            return c->set_err(KV_E_INVAL, "q / o must be 16-byte aligned device pointers");
+        for (int32_t k = 0; k <= ub; ++k)
+            if (!sp->stored[layer][k]) return c->set_err(KV_E_ORDER, "attention before its K/V were stored");
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        // Nothing of this call precedes the attention kernels when the device is in
+        // sync, the plan is cached and no mask is asked for: then the plan, tables
+        // and mirror were complete before the previous kernel began.
+        bool early_ok = !c->pending_reset && c->pending.empty() && c->dev_tables_split == sp->id && !mask_out;
+        if ((rc = sync_device(c, sp, st)) != KV_OK) return rc;
+        DeviceState *d = c->dev;
+        const UbatchHost &u = sp->ub[ub];
+        kvk::UbView v = make_view(c, sp, ub);
+        cudaError_t e;
+        if (d->plan_split != sp->id || d->plan_ub != ub) {
+            early_ok = false;
+            kvk::Plan p = d->plan;
+            if ((e = kvk::launch_plan(v, p, c->prm.n_stream, d->gx_dec, d->gx_pf, st)) != cudaSuccess)
+                return cuda_fail(c, e, "plan launch");
+            c->launches += 3;
+            d->plan_split = sp->id;
+            d->plan_ub = ub;
+        }
+        if (mask_out) {
+            if ((e = kvk::launch_mask(v, static_cast<uint16_t *>(mask_out), st)) != cudaSuccess)
+                return cuda_fail(c, e, "mask launch");
+            c->launches += 1;
+        }
+        const float scale_log2 = 1.4426950408889634f / sqrtf((float)c->prm.head_dim);
+        if (u.n_dec_blocks > 0) {
+            kvk::DecodeArgs a{};
+            a.u = v;
+            a.p = d->plan;
+            a.q = static_cast<const __half *>(q);
+            a.o = o;
+            a.part = d->d_part_dec;
+            a.n_head = c->prm.n_head;
+            a.n_head_kv = c->prm.n_head_kv;
+            a.gqa = c->gqa;
+            a.scale_log2 = scale_log2;
+            a.err = d->d_err;
+            a.nq_max = decode_nq_max(c, u);
+            a.early_ok = early_ok ? 1 : 0;
+            if ((e = kvk::launch_decode(&d->tm_dec[4 * (size_t)layer], a, d->gx_dec, st)) != cudaSuccess)
+                return cuda_fail(c, e, "decode launch");
+            c->launches += 1;
+        }
+        if (u.n_pf_blocks > 0) {
+            kvk::PrefillArgs a{};
+            a.u = v;
+            a.p = d->plan;
+            a.q = static_cast<const __half *>(q);
+            a.o = o;
+            a.part = d->d_part_pf;
+            a.gx_dec = d->gx_dec;
+            a.n_head = c->prm.n_head;
+            a.n_head_kv = c->prm.n_head_kv;
+            a.gqa = c->gqa;
+            a.scale_log2 = scale_log2;
+            a.err = d->d_err;
+            a.early_ok = early_ok ? 1 : 0;
+            if ((e = kvk::launch_prefill(&d->tm_k[layer], &d->tm_v[layer], a, d->gx_pf, st)) != cudaSuccess)
+                return cuda_fail(c, e, "prefill launch");
+            c->launches += 2;   // attention + split-K merge
+        }
+        return KV_OK;
+    });
 }
 
 int kv_device_error(kv_cache *c) {
@@ -472,73 +476,75 @@ bool sync_would_allocate(const kv_cache *c, const kv_split *sp) {
 
 extern "C" int ubatch_attention_static_scratch(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
                                                const void *q, float *o, void *mask_out, void *stream) {
-    int rc = check_call(c, sp, ub, layer);
-    if (rc != KV_OK) return rc;
-    if (!q || !o || ((uintptr_t)q & 15) || ((uintptr_t)o & 15))
-        return c->set_err(KV_E_INVAL, "q / o must be 16-byte aligned device pointers");
-    for (int32_t k = 0; k <= ub; ++k)
-        if (!sp->stored[layer][k]) return c->set_err(KV_E_ORDER, "attention before its K/V were stored");
-    DeviceState *d = c->dev;
-    const UbatchHost &u = sp->ub[ub];
-    if (u.n_pf_blocks > 0)
-        return c->set_err(KV_E_INVAL, "static-scratch attention runs the decode path only; this ubatch has "
-                                      "prefill blocks (use ubatch_attention)");
-    const int32_t hkv = c->prm.n_head_kv;
-    const size_t cnt_bytes = ((size_t)u.n_dec_blocks * hkv * sizeof(int32_t) + 255) & ~(size_t)255;
-    const size_t part_bytes = ((size_t)d->gx_dec + u.n_dec_blocks) * hkv * DEC_PART_FLOATS * sizeof(float);
-    if (cnt_bytes + part_bytes > STATIC_SCRATCH_BYTES) {
-        char buf[200];
-        std::snprintf(buf, sizeof buf, "static-scratch attention needs %zu bytes of scratch for %d decode blocks, "
-                      "more than the %zu available", cnt_bytes + part_bytes, u.n_dec_blocks, STATIC_SCRATCH_BYTES);
-        return c->set_err(KV_E_INVAL, buf);
-    }
-    int cur = -1;
-    cudaError_t e = cudaGetDevice(&cur);
-    if (e != cudaSuccess) return cuda_fail(c, e, "cudaGetDevice");
-    if (cur != d->device || cur < 0 || cur >= MAX_DEVICES)
-        return c->set_err(KV_E_INVAL, "static-scratch attention: make the cache's device current");
-    if (sync_would_allocate(c, sp))
-        return c->set_err(KV_E_INVAL, "static-scratch attention: device tables need a larger upload buffer "
-                                      "(call kv_store for this split first)");
-    unsigned char *scratch = nullptr;
-    if ((e = static_scratch(cur, &scratch)) != cudaSuccess) return cuda_fail(c, e, "scratch address");
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    bool early_ok = !c->pending_reset && c->pending.empty() && c->dev_tables_split == sp->id && !mask_out;
-    if ((rc = sync_device(c, sp, st)) != KV_OK) return rc;
-    kvk::UbView v = make_view(c, sp, ub);
-    if (d->plan_split != sp->id || d->plan_ub != ub) {
-        early_ok = false;
-        if ((e = kvk::launch_plan(v, d->plan, c->prm.n_stream, d->gx_dec, d->gx_pf, st)) != cudaSuccess)
-            return cuda_fail(c, e, "plan launch");
-        c->launches += 3;
-        d->plan_split = sp->id;
-        d->plan_ub = ub;
-    }
-    if (mask_out) {
-        if ((e = kvk::launch_mask(v, static_cast<uint16_t *>(mask_out), st)) != cudaSuccess)
-            return cuda_fail(c, e, "mask launch");
+    return guarded(c, [&]() -> int {
+        int rc = check_call(c, sp, ub, layer);
+        if (rc != KV_OK) return rc;
+        if (!q || !o || ((uintptr_t)q & 15) || ((uintptr_t)o & 15))
+            return c->set_err(KV_E_INVAL, "q / o must be 16-byte aligned device pointers");
+        for (int32_t k = 0; k <= ub; ++k)
+            if (!sp->stored[layer][k]) return c->set_err(KV_E_ORDER, "attention before its K/V were stored");
+        DeviceState *d = c->dev;
+        const UbatchHost &u = sp->ub[ub];
+        if (u.n_pf_blocks > 0)
+            return c->set_err(KV_E_INVAL, "static-scratch attention runs the decode path only; this ubatch has "
+                                          "prefill blocks (use ubatch_attention)");
+        const int32_t hkv = c->prm.n_head_kv;
+        const size_t cnt_bytes = ((size_t)u.n_dec_blocks * hkv * sizeof(int32_t) + 255) & ~(size_t)255;
+        const size_t part_bytes = ((size_t)d->gx_dec + u.n_dec_blocks) * hkv * DEC_PART_FLOATS * sizeof(float);
+        if (cnt_bytes + part_bytes > STATIC_SCRATCH_BYTES) {
+            char buf[200];
+            std::snprintf(buf, sizeof buf, "static-scratch attention needs %zu bytes of scratch for %d decode blocks, "
+                          "more than the %zu available", cnt_bytes + part_bytes, u.n_dec_blocks, STATIC_SCRATCH_BYTES);
+            return c->set_err(KV_E_INVAL, buf);
+        }
+        int cur = -1;
+        cudaError_t e = cudaGetDevice(&cur);
+        if (e != cudaSuccess) return cuda_fail(c, e, "cudaGetDevice");
+        if (cur != d->device || cur < 0 || cur >= MAX_DEVICES)
+            return c->set_err(KV_E_INVAL, "static-scratch attention: make the cache's device current");
+        if (sync_would_allocate(c, sp))
+            return c->set_err(KV_E_INVAL, "static-scratch attention: device tables need a larger upload buffer "
+                                          "(call kv_store for this split first)");
+        unsigned char *scratch = nullptr;
+        if ((e = static_scratch(cur, &scratch)) != cudaSuccess) return cuda_fail(c, e, "scratch address");
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        bool early_ok = !c->pending_reset && c->pending.empty() && c->dev_tables_split == sp->id && !mask_out;
+        if ((rc = sync_device(c, sp, st)) != KV_OK) return rc;
+        kvk::UbView v = make_view(c, sp, ub);
+        if (d->plan_split != sp->id || d->plan_ub != ub) {
+            early_ok = false;
+            if ((e = kvk::launch_plan(v, d->plan, c->prm.n_stream, d->gx_dec, d->gx_pf, st)) != cudaSuccess)
+                return cuda_fail(c, e, "plan launch");
+            c->launches += 3;
+            d->plan_split = sp->id;
+            d->plan_ub = ub;
+        }
+        if (mask_out) {
+            if ((e = kvk::launch_mask(v, static_cast<uint16_t *>(mask_out), st)) != cudaSuccess)
+                return cuda_fail(c, e, "mask launch");
+            c->launches += 1;
+        }
+        if (u.n_dec_blocks == 0) return KV_OK;
+        int32_t *counters = reinterpret_cast<int32_t *>(scratch);
+        if ((e = cudaMemsetAsync(counters, 0, cnt_bytes, st)) != cudaSuccess) return cuda_fail(c, e, "counter clear");
+        kvk::DecodeArgs a{};
+        a.u = v;
+        a.p = d->plan;
+        a.p.counters = counters;
+        a.q = static_cast<const __half *>(q);
+        a.o = o;
+        a.part = reinterpret_cast<float *>(scratch + cnt_bytes);
+        a.n_head = c->prm.n_head;
+        a.n_head_kv = hkv;
+        a.gqa = c->gqa;
+        a.scale_log2 = 1.4426950408889634f / sqrtf((float)c->prm.head_dim);
+        a.err = d->d_err;
+        a.nq_max = decode_nq_max(c, u);
+        // the counters were just cleared by a copy engine, not a kernel: wait for it
+        a.early_ok = 0;
+        if ((e = kvk::launch_decode(&d->tm_dec[4 * (size_t)layer], a, d->gx_dec, st)) != cudaSuccess)
+            return cuda_fail(c, e, "decode launch");
         c->launches += 1;
-    }
-    if (u.n_dec_blocks == 0) return KV_OK;
-    int32_t *counters = reinterpret_cast<int32_t *>(scratch);
-    if ((e = cudaMemsetAsync(counters, 0, cnt_bytes, st)) != cudaSuccess) return cuda_fail(c, e, "counter clear");
-    kvk::DecodeArgs a{};
-    a.u = v;
-    a.p = d->plan;
-    a.p.counters = counters;
-    a.q = static_cast<const __half *>(q);
-    a.o = o;
-    a.part = reinterpret_cast<float *>(scratch + cnt_bytes);
-    a.n_head = c->prm.n_head;
-    a.n_head_kv = hkv;
-    a.gqa = c->gqa;
-    a.scale_log2 = 1.4426950408889634f / sqrtf((float)c->prm.head_dim);
-    a.err = d->d_err;
-    a.nq_max = decode_nq_max(c, u);
-    // the counters were just cleared by a copy engine, not a kernel: wait for it
-    a.early_ok = 0;
-    if ((e = kvk::launch_decode(&d->tm_dec[4 * (size_t)layer], a, d->gx_dec, st)) != cudaSuccess)
-        return cuda_fail(c, e, "decode launch");
-    c->launches += 1;
-    return KV_OK;
+        return KV_OK;
+    });
 }

@@ -352,63 +352,65 @@ void push_delta(kv_cache *c, size_t g) {
 extern "C" {
 
 int kv_init(const kv_params *p, kv_cache **out) {
-    if (!out) return KV_E_INVAL;
-    *out = nullptr;
-    if (!p) return KV_E_INVAL;
-    if (p->n_ctx < 1 || p->n_batch < 1 || p->n_ubatch < 0 || p->n_seq_max < 1 ||
-        p->n_seq_max > KV_MAX_SEQ || p->n_stream < 1 || p->n_stream > p->n_seq_max ||
-        p->n_ctx % p->n_stream != 0 || p->n_layer < 1 || p->n_head < 1 || p->n_head_kv < 1 ||
-        p->n_head % p->n_head_kv != 0 || p->n_head / p->n_head_kv > 8 ||
-        p->head_dim != KV_HEAD_DIM || (p->causal != 0 && p->causal != 1) || p->n_swa < 0)
-        return KV_E_INVAL;
-    if ((p->k_layers == nullptr) != (p->v_layers == nullptr)) return KV_E_INVAL;
-    kv_cache *c = new (std::nothrow) kv_cache();
-    if (!c) return KV_E_NOMEM;
-    c->prm = *p;
-    // UBATCH, "Three things called batch": the two clamps.
-    c->n_batch = p->causal ? std::min(p->n_ctx, p->n_batch) : p->n_batch;
-    int32_t req_ub = p->n_ubatch == 0 ? p->n_batch : p->n_ubatch;
-    c->n_ubatch = std::min(c->n_batch, req_ub);
-    c->kv_size = p->n_ctx / p->n_stream;
-    c->n_words = (p->n_seq_max + 63) / 64;
-    c->gqa = p->n_head / p->n_head_kv;
-    c->pf_min_qv = PF_MIN_QV;
-    c->seq_to_stream.resize(p->n_seq_max);
-    for (int32_t q = 0; q < p->n_seq_max; ++q) {
-        int32_t s = p->seq_to_stream ? p->seq_to_stream[q] : q % p->n_stream;
-        if (s < 0 || s >= p->n_stream) { delete c; return KV_E_INVAL; }
-        c->seq_to_stream[q] = s;
-    }
-    c->prm.seq_to_stream = nullptr;
-    c->prm.k_layers = c->prm.v_layers = nullptr;
-    cells_init(c->cells, p->n_stream, c->kv_size, c->n_words);
-    if (p->k_layers) {
-        c->pending_idx.assign((size_t)p->n_ctx, -1);
-        c->k_layers.assign(p->k_layers, p->k_layers + p->n_layer);
-        c->v_layers.assign(p->v_layers, p->v_layers + p->n_layer);
-        for (int32_t l = 0; l < p->n_layer; ++l) {
-            if (!c->k_layers[l] || !c->v_layers[l] ||
-                ((uintptr_t)c->k_layers[l] & 15) || ((uintptr_t)c->v_layers[l] & 15)) {
+    return guarded(nullptr, [&]() -> int {
+        if (!out) return KV_E_INVAL;
+        *out = nullptr;
+        if (!p) return KV_E_INVAL;
+        if (p->n_ctx < 1 || p->n_batch < 1 || p->n_ubatch < 0 || p->n_seq_max < 1 ||
+            p->n_seq_max > KV_MAX_SEQ || p->n_stream < 1 || p->n_stream > p->n_seq_max ||
+            p->n_ctx % p->n_stream != 0 || p->n_layer < 1 || p->n_head < 1 || p->n_head_kv < 1 ||
+            p->n_head % p->n_head_kv != 0 || p->n_head / p->n_head_kv > 8 ||
+            p->head_dim != KV_HEAD_DIM || (p->causal != 0 && p->causal != 1) || p->n_swa < 0)
+            return KV_E_INVAL;
+        if ((p->k_layers == nullptr) != (p->v_layers == nullptr)) return KV_E_INVAL;
+        kv_cache *c = new (std::nothrow) kv_cache();
+        if (!c) return KV_E_NOMEM;
+        c->prm = *p;
+        // UBATCH, "Three things called batch": the two clamps.
+        c->n_batch = p->causal ? std::min(p->n_ctx, p->n_batch) : p->n_batch;
+        int32_t req_ub = p->n_ubatch == 0 ? p->n_batch : p->n_ubatch;
+        c->n_ubatch = std::min(c->n_batch, req_ub);
+        c->kv_size = p->n_ctx / p->n_stream;
+        c->n_words = (p->n_seq_max + 63) / 64;
+        c->gqa = p->n_head / p->n_head_kv;
+        c->pf_min_qv = PF_MIN_QV;
+        c->seq_to_stream.resize(p->n_seq_max);
+        for (int32_t q = 0; q < p->n_seq_max; ++q) {
+            int32_t s = p->seq_to_stream ? p->seq_to_stream[q] : q % p->n_stream;
+            if (s < 0 || s >= p->n_stream) { delete c; return KV_E_INVAL; }
+            c->seq_to_stream[q] = s;
+        }
+        c->prm.seq_to_stream = nullptr;
+        c->prm.k_layers = c->prm.v_layers = nullptr;
+        cells_init(c->cells, p->n_stream, c->kv_size, c->n_words);
+        if (p->k_layers) {
+            c->pending_idx.assign((size_t)p->n_ctx, -1);
+            c->k_layers.assign(p->k_layers, p->k_layers + p->n_layer);
+            c->v_layers.assign(p->v_layers, p->v_layers + p->n_layer);
+            for (int32_t l = 0; l < p->n_layer; ++l) {
+                if (!c->k_layers[l] || !c->v_layers[l] ||
+                    ((uintptr_t)c->k_layers[l] & 15) || ((uintptr_t)c->v_layers[l] & 15)) {
+                    delete c;
+                    return KV_E_INVAL;
+                }
+            }
+            c->has_device = true;
+            int rc = device_init(c);
+            if (rc != KV_OK) {
+                if (log_on()) std::fprintf(stderr, "kvattn: device init failed: %s\n", c->err.c_str());
+                device_free(c);
                 delete c;
-                return KV_E_INVAL;
+                return rc;
             }
         }
-        c->has_device = true;
-        int rc = device_init(c);
-        if (rc != KV_OK) {
-            if (log_on()) std::fprintf(stderr, "kvattn: device init failed: %s\n", c->err.c_str());
-            device_free(c);
-            delete c;
-            return rc;
-        }
-    }
-    if (log_on())
-        std::fprintf(stderr, "kvattn: n_ctx %d n_stream %d kv_size %d n_batch %d n_ubatch %d "
-                     "layers %d heads %d/%d; K+V %.1f MiB\n", p->n_ctx, p->n_stream, c->kv_size,
-                     c->n_batch, c->n_ubatch, p->n_layer, p->n_head, p->n_head_kv,
-                     (double)p->n_ctx * p->n_head_kv * p->head_dim * 2 * 2 * p->n_layer / 1048576.0);
-    *out = c;
-    return KV_OK;
+        if (log_on())
+            std::fprintf(stderr, "kvattn: n_ctx %d n_stream %d kv_size %d n_batch %d n_ubatch %d "
+                         "layers %d heads %d/%d; K+V %.1f MiB\n", p->n_ctx, p->n_stream, c->kv_size,
+                         c->n_batch, c->n_ubatch, p->n_layer, p->n_head, p->n_head_kv,
+                         (double)p->n_ctx * p->n_head_kv * p->head_dim * 2 * 2 * p->n_layer / 1048576.0);
+        *out = c;
+        return KV_OK;
+    });
 }
 
 void kv_free(kv_cache *c) {
@@ -423,72 +425,74 @@ int32_t kv_kv_size(const kv_cache *c) { return c ? c->kv_size : KV_E_INVAL; }
 const char *kv_last_error(const kv_cache *c) { return c ? c->err.c_str() : "null cache"; }
 
 int kv_split_ubatches(kv_cache *c, const kv_batch *b, int32_t mode, kv_split **out) {
-    if (!c || !b || !out) return KV_E_INVAL;
-    *out = nullptr;
-    if (mode < KV_SPLIT_AUTO || mode > KV_SPLIT_SEQ) return c->set_err(KV_E_INVAL, "bad split mode");
-    const int32_t n = b->n_tokens;
-    if (n < 1) return c->set_err(KV_E_INVAL, "empty batch");
-    if (n > c->n_batch) return c->set_err(KV_E_BATCH_TOO_LARGE, "n_tokens > n_batch");
-    const int32_t nsm = c->prm.n_seq_max;
-    SplitIn in;
-    in.n = n;
-    in.ids.resize(n);
-    in.set.resize(n);
-    for (int32_t i = 0; i < n; ++i) {
-        std::vector<int32_t> &ids = in.ids[i];
-        if (!b->seq_id) {
-            ids.push_back(0);
-        } else if (!b->n_seq_id) {
-            if (!b->seq_id[i]) return c->set_err(KV_E_INVAL, "null seq_id row");
-            ids.push_back(b->seq_id[i][0]);
-        } else {
-            int32_t k = b->n_seq_id[i];
-            if (k < 1 || k > nsm) return c->set_err(KV_E_INVAL, "bad n_seq_id");
-            if (!b->seq_id[i]) return c->set_err(KV_E_INVAL, "null seq_id row");
-            ids.assign(b->seq_id[i], b->seq_id[i] + k);
-        }
-        for (int32_t q : ids)
-            if (q < 0 || q >= nsm) return c->set_err(KV_E_SEQ_RANGE, "sequence id out of range");
-        std::vector<int32_t> sorted = ids;
-        std::sort(sorted.begin(), sorted.end());
-        if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
-            return c->set_err(KV_E_INVAL, "repeated sequence id in one slot");
-        int32_t st = c->seq_to_stream[ids[0]];
-        for (int32_t q : ids)
-            if (c->seq_to_stream[q] != st)
-                return c->set_err(KV_E_CROSS_STREAM, "slot spans streams");
-        if (b->pos && b->pos[i] < 0) return c->set_err(KV_E_INVAL, "negative position");
-        in.set[i].ids = std::move(sorted);
-    }
-    in.pos.resize(n);
-    if (b->pos) {
-        for (int32_t i = 0; i < n; ++i) in.pos[i] = b->pos[i];
-    } else {
-        // BATCH-ZH, Part A: a NULL pos is filled by counting up per sequence.
-        std::map<int32_t, int32_t> last;   // sequence -> largest pos so far
+    return guarded(c, [&]() -> int {
+        if (!c || !b || !out) return KV_E_INVAL;
+        *out = nullptr;
+        if (mode < KV_SPLIT_AUTO || mode > KV_SPLIT_SEQ) return c->set_err(KV_E_INVAL, "bad split mode");
+        const int32_t n = b->n_tokens;
+        if (n < 1) return c->set_err(KV_E_INVAL, "empty batch");
+        if (n > c->n_batch) return c->set_err(KV_E_BATCH_TOO_LARGE, "n_tokens > n_batch");
+        const int32_t nsm = c->prm.n_seq_max;
+        SplitIn in;
+        in.n = n;
+        in.ids.resize(n);
+        in.set.resize(n);
         for (int32_t i = 0; i < n; ++i) {
-            int32_t q = in.ids[i][0];
-            auto it = last.find(q);
-            int32_t best = it != last.end() ? it->second : seq_pos_max(c, q);
-            in.pos[i] = best + 1;
-            for (int32_t x : in.ids[i]) {
-                auto jt = last.find(x);
-                int32_t prev = jt != last.end() ? jt->second : seq_pos_max(c, x);
-                last[x] = std::max(prev, in.pos[i]);
+            std::vector<int32_t> &ids = in.ids[i];
+            if (!b->seq_id) {
+                ids.push_back(0);
+            } else if (!b->n_seq_id) {
+                if (!b->seq_id[i]) return c->set_err(KV_E_INVAL, "null seq_id row");
+                ids.push_back(b->seq_id[i][0]);
+            } else {
+                int32_t k = b->n_seq_id[i];
+                if (k < 1 || k > nsm) return c->set_err(KV_E_INVAL, "bad n_seq_id");
+                if (!b->seq_id[i]) return c->set_err(KV_E_INVAL, "null seq_id row");
+                ids.assign(b->seq_id[i], b->seq_id[i] + k);
+            }
+            for (int32_t q : ids)
+                if (q < 0 || q >= nsm) return c->set_err(KV_E_SEQ_RANGE, "sequence id out of range");
+            std::vector<int32_t> sorted = ids;
+            std::sort(sorted.begin(), sorted.end());
+            if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
+                return c->set_err(KV_E_INVAL, "repeated sequence id in one slot");
+            int32_t st = c->seq_to_stream[ids[0]];
+            for (int32_t q : ids)
+                if (c->seq_to_stream[q] != st)
+                    return c->set_err(KV_E_CROSS_STREAM, "slot spans streams");
+            if (b->pos && b->pos[i] < 0) return c->set_err(KV_E_INVAL, "negative position");
+            in.set[i].ids = std::move(sorted);
+        }
+        in.pos.resize(n);
+        if (b->pos) {
+            for (int32_t i = 0; i < n; ++i) in.pos[i] = b->pos[i];
+        } else {
+            // BATCH-ZH, Part A: a NULL pos is filled by counting up per sequence.
+            std::map<int32_t, int32_t> last;   // sequence -> largest pos so far
+            for (int32_t i = 0; i < n; ++i) {
+                int32_t q = in.ids[i][0];
+                auto it = last.find(q);
+                int32_t best = it != last.end() ? it->second : seq_pos_max(c, q);
+                in.pos[i] = best + 1;
+                for (int32_t x : in.ids[i]) {
+                    auto jt = last.find(x);
+                    int32_t prev = jt != last.end() ? jt->second : seq_pos_max(c, x);
+                    last[x] = std::max(prev, in.pos[i]);
+                }
             }
         }
-    }
-    kv_split *sp = new (std::nothrow) kv_split();
-    if (!sp) return c->set_err(KV_E_NOMEM, "split alloc");
-    sp->id = c->next_split_id++;
-    sp->owner = c;
-    sp->n_tokens = n;
-    if (mode == KV_SPLIT_AUTO) mode = c->prm.n_stream == 1 ? KV_SPLIT_SIMPLE : KV_SPLIT_EQUAL;
-    if (mode == KV_SPLIT_SIMPLE) split_simple(sp, in, c->n_ubatch, c);
-    else if (mode == KV_SPLIT_EQUAL) split_equal(sp, in, c->n_ubatch, c);
-    else split_seq(sp, in, c->n_ubatch, c);
-    *out = sp;
-    return KV_OK;
+        kv_split *sp = new (std::nothrow) kv_split();
+        if (!sp) return c->set_err(KV_E_NOMEM, "split alloc");
+        sp->id = c->next_split_id++;
+        sp->owner = c;
+        sp->n_tokens = n;
+        if (mode == KV_SPLIT_AUTO) mode = c->prm.n_stream == 1 ? KV_SPLIT_SIMPLE : KV_SPLIT_EQUAL;
+        if (mode == KV_SPLIT_SIMPLE) split_simple(sp, in, c->n_ubatch, c);
+        else if (mode == KV_SPLIT_EQUAL) split_equal(sp, in, c->n_ubatch, c);
+        else split_seq(sp, in, c->n_ubatch, c);
+        *out = sp;
+        return KV_OK;
+    });
 }
 
 int32_t kv_split_count(const kv_split *s) { return s ? (int32_t)s->ub.size() : KV_E_INVAL; }
@@ -513,136 +517,142 @@ int kv_split_ubatch(const kv_split *s, int32_t k, kv_ubatch_info *out) {
 void kv_split_free(kv_split *s) { delete s; }
 
 int kv_prepare_cells(kv_cache *c, kv_split *sp) {
-    if (!c || !sp || sp->owner != c) return KV_E_INVAL;
-    if (sp->prepared) return c->set_err(KV_E_ORDER, "split already prepared");
-    CellState &cs = c->cells;
-    const int32_t W = cs.n_words;
-    // undo log: cells filled so far (all were empty before)
-    std::vector<size_t> filled;
-    std::vector<int32_t> saved_first_free = cs.first_free, saved_used = cs.used_max_p1;
-    uint32_t epoch = c->next_epoch;
-    bool ok = true;
-    for (UbatchHost &u : sp->ub) {
-        u.cells.assign(u.n_tokens, -1);
-        u.epoch = epoch++;
-        for (int32_t i = 0; i < u.n_tokens && ok; ++i) {
-            int32_t s = u.streams[i];
-            int32_t j = next_empty(cs, s, cs.first_free[s]);
-            if (j < 0) { ok = false; break; }
-            cs.first_free[s] = j + 1;
-            size_t g = (size_t)s * cs.kv_size + j;
-            cs.pos[g] = u.pos[i];
-            uint64_t *w = &cs.bits[g * W];
-            for (int32_t x = 0; x < W; ++x) w[x] = 0;
-            for (int32_t t = u.ids_off[i]; t < u.ids_off[i + 1]; ++t)
-                w[u.ids[t] >> 6] |= 1ull << (u.ids[t] & 63);
-            cs.nseq[g] = u.ids_off[i + 1] - u.ids_off[i];
-            cs.epoch[g] = u.epoch;
-            filled.push_back(g);
-            u.cells[i] = j;
-            cs.used_max_p1[s] = std::max(cs.used_max_p1[s], j + 1);
+    return guarded(c, [&]() -> int {
+        if (!c || !sp || sp->owner != c) return KV_E_INVAL;
+        if (sp->prepared) return c->set_err(KV_E_ORDER, "split already prepared");
+        CellState &cs = c->cells;
+        const int32_t W = cs.n_words;
+        // undo log: cells filled so far (all were empty before)
+        std::vector<size_t> filled;
+        std::vector<int32_t> saved_first_free = cs.first_free, saved_used = cs.used_max_p1;
+        uint32_t epoch = c->next_epoch;
+        bool ok = true;
+        for (UbatchHost &u : sp->ub) {
+            u.cells.assign(u.n_tokens, -1);
+            u.epoch = epoch++;
+            for (int32_t i = 0; i < u.n_tokens && ok; ++i) {
+                int32_t s = u.streams[i];
+                int32_t j = next_empty(cs, s, cs.first_free[s]);
+                if (j < 0) { ok = false; break; }
+                cs.first_free[s] = j + 1;
+                size_t g = (size_t)s * cs.kv_size + j;
+                cs.pos[g] = u.pos[i];
+                uint64_t *w = &cs.bits[g * W];
+                for (int32_t x = 0; x < W; ++x) w[x] = 0;
+                for (int32_t t = u.ids_off[i]; t < u.ids_off[i + 1]; ++t)
+                    w[u.ids[t] >> 6] |= 1ull << (u.ids[t] & 63);
+                cs.nseq[g] = u.ids_off[i + 1] - u.ids_off[i];
+                cs.epoch[g] = u.epoch;
+                filled.push_back(g);
+                u.cells[i] = j;
+                cs.used_max_p1[s] = std::max(cs.used_max_p1[s], j + 1);
+            }
+            if (!ok) break;
+            int32_t nkv = 0;
+            std::set<int32_t> touched(u.streams.begin(), u.streams.end());
+            for (int32_t s : touched) nkv = std::max(nkv, n_kv_of(cs, s));
+            u.n_kv = nkv;
         }
-        if (!ok) break;
-        int32_t nkv = 0;
-        std::set<int32_t> touched(u.streams.begin(), u.streams.end());
-        for (int32_t s : touched) nkv = std::max(nkv, n_kv_of(cs, s));
-        u.n_kv = nkv;
-    }
-    if (!ok) {
-        for (size_t g : filled) {
-            cs.pos[g] = -1;
-            cs.nseq[g] = 0;
-            cs.epoch[g] = 0;
-            for (int32_t x = 0; x < W; ++x) cs.bits[g * W + x] = 0;
+        if (!ok) {
+            for (size_t g : filled) {
+                cs.pos[g] = -1;
+                cs.nseq[g] = 0;
+                cs.epoch[g] = 0;
+                for (int32_t x = 0; x < W; ++x) cs.bits[g * W + x] = 0;
+            }
+            cs.first_free = saved_first_free;
+            cs.used_max_p1 = saved_used;
+            for (UbatchHost &u : sp->ub) { u.cells.clear(); u.n_kv = 0; }
+            return c->set_err(KV_NO_SLOT, "no free cell");
         }
-        cs.first_free = saved_first_free;
-        cs.used_max_p1 = saved_used;
-        for (UbatchHost &u : sp->ub) { u.cells.clear(); u.n_kv = 0; }
-        return c->set_err(KV_NO_SLOT, "no free cell");
-    }
-    c->next_epoch = epoch;
-    sp->prepared = true;
-    sp->rm_gen = c->rm_gen;
-    if (c->has_device) {
-        for (size_t g : filled) push_delta(c, g);
-        for (UbatchHost &u : sp->ub) build_blocks(u, c);
-        build_image(sp, c);
-        sp->stored.assign(c->prm.n_layer, std::vector<uint8_t>(sp->ub.size(), 0));
-    }
-    return KV_OK;
+        c->next_epoch = epoch;
+        sp->prepared = true;
+        sp->rm_gen = c->rm_gen;
+        if (c->has_device) {
+            for (size_t g : filled) push_delta(c, g);
+            for (UbatchHost &u : sp->ub) build_blocks(u, c);
+            build_image(sp, c);
+            sp->stored.assign(c->prm.n_layer, std::vector<uint8_t>(sp->ub.size(), 0));
+        }
+        return KV_OK;
+    });
 }
 
 int kv_seq_rm(kv_cache *c, int32_t seq, int32_t p0, int32_t p1) {
-    if (!c) return KV_E_INVAL;
-    if (seq >= c->prm.n_seq_max) return c->set_err(KV_E_SEQ_RANGE, "sequence id out of range");
-    CellState &cs = c->cells;
-    const int32_t W = cs.n_words;
-    const int64_t hi = p1 < 0 ? INT64_MAX : (int64_t)p1;
-    const bool all = seq < 0 && p0 <= 0 && p1 < 0;
-    bool changed = false;
-    for (int32_t s = 0; s < cs.n_stream; ++s) {
-        if (seq >= 0 && c->seq_to_stream[seq] != s) continue;
-        size_t base = (size_t)s * cs.kv_size;
-        for (int32_t j = 0; j < cs.used_max_p1[s]; ++j) {
-            size_t g = base + j;
-            if (!cs.nseq[g]) continue;
-            if (cs.pos[g] < p0 || cs.pos[g] >= hi) continue;
-            uint64_t *w = &cs.bits[g * W];
-            if (seq < 0) {
-                for (int32_t x = 0; x < W; ++x) w[x] = 0;
-                cs.nseq[g] = 0;
-            } else if (bit_has(w, seq)) {
-                w[seq >> 6] &= ~(1ull << (seq & 63));
-                cs.nseq[g] -= 1;
-            } else {
-                continue;
+    return guarded(c, [&]() -> int {
+        if (!c) return KV_E_INVAL;
+        if (seq >= c->prm.n_seq_max) return c->set_err(KV_E_SEQ_RANGE, "sequence id out of range");
+        CellState &cs = c->cells;
+        const int32_t W = cs.n_words;
+        const int64_t hi = p1 < 0 ? INT64_MAX : (int64_t)p1;
+        const bool all = seq < 0 && p0 <= 0 && p1 < 0;
+        bool changed = false;
+        for (int32_t s = 0; s < cs.n_stream; ++s) {
+            if (seq >= 0 && c->seq_to_stream[seq] != s) continue;
+            size_t base = (size_t)s * cs.kv_size;
+            for (int32_t j = 0; j < cs.used_max_p1[s]; ++j) {
+                size_t g = base + j;
+                if (!cs.nseq[g]) continue;
+                if (cs.pos[g] < p0 || cs.pos[g] >= hi) continue;
+                uint64_t *w = &cs.bits[g * W];
+                if (seq < 0) {
+                    for (int32_t x = 0; x < W; ++x) w[x] = 0;
+                    cs.nseq[g] = 0;
+                } else if (bit_has(w, seq)) {
+                    w[seq >> 6] &= ~(1ull << (seq & 63));
+                    cs.nseq[g] -= 1;
+                } else {
+                    continue;
+                }
+                if (cs.nseq[g] == 0) {
+                    cs.pos[g] = -1;
+                    cs.epoch[g] = 0;
+                    cs.first_free[s] = std::min(cs.first_free[s], j);
+                }
+                changed = true;
+                if (c->has_device && !all) push_delta(c, g);
             }
-            if (cs.nseq[g] == 0) {
-                cs.pos[g] = -1;
-                cs.epoch[g] = 0;
-                cs.first_free[s] = std::min(cs.first_free[s], j);
+            refresh_used_max(cs, s);
+        }
+        if (changed || all) {
+            c->rm_gen++;
+            if (c->has_device && all) {
+                // the whole mirror is cleared on the device instead of cell by cell
+                for (const Delta &d : c->pending) c->pending_idx[d.cell] = -1;
+                c->pending.clear();
+                c->pending_reset = true;
             }
-            changed = true;
-            if (c->has_device && !all) push_delta(c, g);
         }
-        refresh_used_max(cs, s);
-    }
-    if (changed || all) {
-        c->rm_gen++;
-        if (c->has_device && all) {
-            // the whole mirror is cleared on the device instead of cell by cell
-            for (const Delta &d : c->pending) c->pending_idx[d.cell] = -1;
-            c->pending.clear();
-            c->pending_reset = true;
-        }
-    }
-    return KV_OK;
+        return KV_OK;
+    });
 }
 
 int kv_seq_cp(kv_cache *c, int32_t src, int32_t dst, int32_t p0, int32_t p1) {
-    if (!c) return KV_E_INVAL;
-    if (src < 0 || src >= c->prm.n_seq_max || dst < 0 || dst >= c->prm.n_seq_max)
-        return c->set_err(KV_E_SEQ_RANGE, "sequence id out of range");
-    const int32_t s = c->seq_to_stream[src];
-    if (c->seq_to_stream[dst] != s) return c->set_err(KV_E_CROSS_STREAM, "copy between streams");
-    if (src == dst) return KV_OK;
-    CellState &cs = c->cells;
-    const int32_t W = cs.n_words;
-    const int64_t hi = p1 < 0 ? INT64_MAX : (int64_t)p1;
-    const size_t base = (size_t)s * cs.kv_size;
-    bool changed = false;
-    for (int32_t j = 0; j < cs.used_max_p1[s]; ++j) {
-        const size_t g = base + j;
-        if (!cs.nseq[g] || cs.pos[g] < p0 || cs.pos[g] >= hi) continue;
-        uint64_t *w = &cs.bits[g * W];
-        if (!bit_has(w, src) || bit_has(w, dst)) continue;
-        w[dst >> 6] |= 1ull << (dst & 63);
-        cs.nseq[g] += 1;
-        changed = true;
-        if (c->has_device) push_delta(c, g);
-    }
-    if (changed) c->rm_gen++;   // splits prepared before see another cell state
-    return KV_OK;
+    return guarded(c, [&]() -> int {
+        if (!c) return KV_E_INVAL;
+        if (src < 0 || src >= c->prm.n_seq_max || dst < 0 || dst >= c->prm.n_seq_max)
+            return c->set_err(KV_E_SEQ_RANGE, "sequence id out of range");
+        const int32_t s = c->seq_to_stream[src];
+        if (c->seq_to_stream[dst] != s) return c->set_err(KV_E_CROSS_STREAM, "copy between streams");
+        if (src == dst) return KV_OK;
+        CellState &cs = c->cells;
+        const int32_t W = cs.n_words;
+        const int64_t hi = p1 < 0 ? INT64_MAX : (int64_t)p1;
+        const size_t base = (size_t)s * cs.kv_size;
+        bool changed = false;
+        for (int32_t j = 0; j < cs.used_max_p1[s]; ++j) {
+            const size_t g = base + j;
+            if (!cs.nseq[g] || cs.pos[g] < p0 || cs.pos[g] >= hi) continue;
+            uint64_t *w = &cs.bits[g * W];
+            if (!bit_has(w, src) || bit_has(w, dst)) continue;
+            w[dst >> 6] |= 1ull << (dst & 63);
+            cs.nseq[g] += 1;
+            changed = true;
+            if (c->has_device) push_delta(c, g);
+        }
+        if (changed) c->rm_gen++;   // splits prepared before see another cell state
+        return KV_OK;
+    });
 }
 
 int32_t kv_seq_pos_max(const kv_cache *c, int32_t seq) {

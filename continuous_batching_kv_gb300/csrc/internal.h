@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cstddef>
+#include <new>
 #include <string>
 #include <vector>
 
@@ -124,6 +125,24 @@ struct kv_cache {
     std::string err;
     int set_err(int code, const std::string &msg) { err = msg; return code; }
 };
+
+
+// An entry point's body, run so that no C++ exception crosses the C boundary: a
+// failed host allocation (or any other exception) becomes KV_E_NOMEM.
+template <class F>
+int guarded(kv_cache *c, F &&body) noexcept {
+    try {
+        return body();
+    } catch (...) {
+        if (c) {
+            try {
+                c->err = "host allocation failed";
+            } catch (...) {
+            }
+        }
+        return KV_E_NOMEM;
+    }
+}
 
 // device.cu
 namespace kvi {
