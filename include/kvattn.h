@@ -23,7 +23,10 @@
  *     o, mask_out).  The library owns kv_cache and kv_split handles and the
  *     device memory it allocates in kv_init (cell-metadata mirror, per-ubatch
  *     row tables, attention plan and split-K scratch).
- *   - A kv_cache is not thread-safe; use one host thread per cache.
+ *   - A kv_cache is not thread-safe; use one host thread per cache (a kv_sched
+ *     belongs to its cache's thread too).
+ *   - A call that allocates host memory returns KV_E_NOMEM when that fails; no
+ *     C++ exception leaves the library.
  */
 #ifndef KVATTN_H
 #define KVATTN_H
