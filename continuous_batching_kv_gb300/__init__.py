@@ -187,7 +187,8 @@ def kv_init(n_ctx, n_batch=2048, n_ubatch=512, n_seq_max=1, n_stream=1, n_layer=
             k_layers=None, v_layers=None, n_swa=0):
     """Create a cache.  k_layers / v_layers: lists of device tensors (or
     addresses), one per layer, each [n_stream * kv_size, n_head_kv * head_dim]
-    fp16; None for a host-only cache."""
+    fp16; None for a host-only cache.  causal=False: bidirectional attention;
+    n_swa > 0: a sliding window of n_swa positions (see kv_params in kvattn.h)."""
     p = kv_params()
     p.n_ctx, p.n_batch, p.n_ubatch = n_ctx, n_batch, n_ubatch
     p.n_seq_max, p.n_stream, p.n_layer = n_seq_max, n_stream, n_layer

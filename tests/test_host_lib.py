@@ -297,3 +297,12 @@ def test_scheduler_errors():
         kv.kv_sched_next(sch)                       # the batch was not advanced
     assert ei.value.code == kv.KV_E_ORDER
     kv.kv_sched_free(sch)
+
+
+def test_init_rejects_a_negative_window():
+    with pytest.raises(kv.KvError) as ei:
+        kv.kv_init(n_ctx=64, n_swa=-1)
+    assert ei.value.code == kv.KV_E_INVAL
+    c = kv.kv_init(n_ctx=64, n_swa=16)          # a window is a host-side parameter only
+    s = kv.kv_split_ubatches(c, list(range(10)), [[0]] * 10)
+    assert kv.kv_prepare_cells(c, s) == 0
