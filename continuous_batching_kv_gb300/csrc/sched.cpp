@@ -49,6 +49,8 @@ int kv_sched_init(kv_cache *c, const kv_sched_params *p, kv_sched **out) {
         if (c->prm.n_stream != 1) return c->set_err(KV_E_INVAL, "the scheduler drives a unified cache");
         if (p->max_seqs < 1 || p->max_seqs > c->prm.n_seq_max || p->token_budget < p->max_seqs)
             return c->set_err(KV_E_INVAL, "scheduler: 1 <= max_seqs <= n_seq_max, token_budget >= max_seqs");
+        if (p->token_budget > c->n_batch)   // a pass's batch is one kv_split_ubatches call
+            return c->set_err(KV_E_INVAL, "scheduler: token_budget > n_batch");
         kv_sched *s = new kv_sched;
         s->c = c;
         s->p = *p;

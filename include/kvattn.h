@@ -367,7 +367,7 @@ typedef struct kv_sched kv_sched;
 
 typedef struct kv_sched_params {
     int32_t max_seqs;      /* sequences running at once: 1 .. n_seq_max */
-    int32_t token_budget;  /* positions per pass: >= max_seqs */
+    int32_t token_budget;  /* positions per pass: max_seqs .. n_batch (a pass is one batch) */
     int32_t fixed;         /* 1: admit only into an empty batch (a classical fixed batch) */
 } kv_sched_params;
 
@@ -386,7 +386,8 @@ typedef struct kv_sched_info {
 } kv_sched_info;           /* duty cycle (ITER, "Two resources idled by a fixed batch"):
                               useful / (passes * max_seqs) */
 
-/* Errors: KV_E_INVAL (bad parameters, n_stream != 1, max_seqs > n_seq_max). */
+/* Errors: KV_E_INVAL (bad parameters, n_stream != 1, max_seqs > n_seq_max,
+ * token_budget > n_batch). */
 int kv_sched_init(kv_cache *c, const kv_sched_params *p, kv_sched **out);
 void kv_sched_free(kv_sched *s);
 

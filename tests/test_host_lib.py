@@ -286,7 +286,7 @@ def test_scheduler_errors():
         kv.kv_sched_init(c, 2, 16)                  # needs a unified cache
     assert ei.value.code == kv.KV_E_INVAL
     c = kv.kv_init(n_ctx=64, n_batch=16, n_ubatch=8, n_seq_max=4)
-    for ms, tb in ((5, 16), (0, 16), (4, 3)):
+    for ms, tb in ((5, 16), (0, 16), (4, 3), (2, 17)):   # 17 > n_batch 16
         with pytest.raises(kv.KvError):
             kv.kv_sched_init(c, ms, tb)
     sch = kv.kv_sched_init(c, 2, 16)
