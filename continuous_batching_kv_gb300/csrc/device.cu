@@ -508,11 +508,9 @@ extern "C" int ubatch_attention_static_scratch(kv_cache *c, const kv_split *sp, 
         unsigned char *scratch = nullptr;
         if ((e = static_scratch(cur, &scratch)) != cudaSuccess) return cuda_fail(c, e, "scratch address");
         cudaStream_t st = static_cast<cudaStream_t>(stream);
-        bool early_ok = !c->pending_reset && c->pending.empty() && c->dev_tables_split == sp->id && !mask_out;
         if ((rc = sync_device(c, sp, st)) != KV_OK) return rc;
         kvk::UbView v = make_view(c, sp, ub);
         if (d->plan_split != sp->id || d->plan_ub != ub) {
-            early_ok = false;
             if ((e = kvk::launch_plan(v, d->plan, c->prm.n_stream, d->gx_dec, d->gx_pf, st)) != cudaSuccess)
                 return cuda_fail(c, e, "plan launch");
             c->launches += 3;
