@@ -11,7 +11,6 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
-#include <mutex>
 
 #include <cudaTypedefs.h>
 
@@ -46,6 +45,9 @@ struct DeviceState {
     float *d_part_dec = nullptr;
     float *d_part_pf = nullptr;
     int32_t *d_err = nullptr;
+    // device address of the library's fixed static-scratch array on this device
+    // (looked up at kv_init, which also makes the runtime load and back it)
+    unsigned char *static_scratch = nullptr;
     // one TMA descriptor per K / V tensor
     std::vector<CUtensorMap> tm_k, tm_v;
     std::vector<CUtensorMap> tm_dec;   // per layer: K, V with 64-row boxes, K, V with 8-row boxes
@@ -60,6 +62,15 @@ struct DeviceState {
 using namespace kvi;
 
 namespace {
+
+// Split-K scratch of ubatch_attention_static_scratch: one fixed array in this
+// file's device image.  Every process that loads the library holds it on each
+// device where a cache is created (kv_init looks up its address, which loads
+// this module there) until the process exits.  In host code the name is a
+// host-side stand-in; only the address from cudaGetSymbolAddress may be given
+// to a kernel.
+constexpr size_t STATIC_SCRATCH_BYTES = KV_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_static_scratch[STATIC_SCRATCH_BYTES];
 
 constexpr int32_t DEC_PART_FLOATS = DEC_QMAX * 132;
 constexpr int32_t PF_PART_FLOATS = PF_M * 132;
@@ -186,7 +197,7 @@ int sync_device(kv_cache *c, const kv_split *sp, cudaStream_t st) {
         c->launches += 1;
     }
     if (tbytes) {
-        if ((e = kvk::launch_upload(d->d_stage[sl] + dbytes, d->d_tables, tbytes, st)) != cudaSuccess)
+        if ((e = kvk::launch_upload(d->d_stage[sl] + dbytes, d->d_tables, tbytes, d->n_sm, st)) != cudaSuccess)
             return cuda_fail(c, e, "table upload");
         c->launches += 1;
         c->dev_tables_split = sp->id;
@@ -298,6 +309,19 @@ int device_init(kv_cache *c) {
         td[0] = d->tm_k[l];
         td[1] = d->tm_v[l];
     }
+    if ((e = kvk::load_store_kernels()) != cudaSuccess || (e = kvk::load_plan_kernels()) != cudaSuccess ||
+        (e = kvk::load_decode_kernels()) != cudaSuccess || (e = kvk::load_prefill_kernels()) != cudaSuccess)
+        return cuda_fail(c, e, "kernel load");
+    // The static-scratch array's address on this device (the current one).  With
+    // lazy module loading this lookup is what loads the module and backs the array,
+    // so it happens here, where memory is obtained anyway, and not during a call
+    // that promises to obtain none.
+    {
+        void *ps = nullptr;
+        if ((e = cudaGetSymbolAddress(&ps, g_static_scratch)) != cudaSuccess)
+            return cuda_fail(c, e, "static scratch address");
+        d->static_scratch = static_cast<unsigned char *>(ps);
+    }
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(c, e, "init sync");
     return KV_OK;
 }
@@ -333,7 +357,8 @@ int kv_store(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer, const v
         DeviceState *d = c->dev;
         const DevRow *rows = reinterpret_cast<const DevRow *>(d->d_tables + sp->off_rows[ub]);
         cudaError_t e = kvk::launch_store(c->k_layers[layer], c->v_layers[layer], k_cur, v_cur, rows, u.n_tokens,
-                                          c->prm.n_head_kv * c->prm.head_dim * 2, (int64_t)c->prm.n_ctx, d->d_err, st);
+                                          c->prm.n_head_kv * c->prm.head_dim * 2, (int64_t)c->prm.n_ctx, d->d_err,
+                                          d->n_sm, st);
         if (e != cudaSuccess) return cuda_fail(c, e, "store launch");
         c->launches += 1;
         const_cast<kv_split *>(sp)->stored[layer][ub] = 1;
@@ -441,28 +466,6 @@ uint64_t kv_launch_count(const kv_cache *c) { return c ? c->launches : 0; }
 
 namespace {
 
-constexpr size_t STATIC_SCRATCH_BYTES = KV_STATIC_SCRATCH_BYTES;
-constexpr int MAX_DEVICES = 64;
-
-static __device__ __align__(256) unsigned char g_static_scratch[STATIC_SCRATCH_BYTES];
-
-std::mutex g_scratch_mu;
-void *g_scratch_addr[MAX_DEVICES] = {};
-
-// The array's device address on `dev`, looked up once per device; `dev` must
-// be the current device.
-cudaError_t static_scratch(int dev, unsigned char **out) {
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
-    }
-    *out = static_cast<unsigned char *>(g_scratch_addr[dev]);
-    return cudaSuccess;
-}
-
 // True when sync_device would have to grow its delta or staging buffer.
 bool sync_would_allocate(const kv_cache *c, const kv_split *sp) {
     const DeviceState *d = c->dev;
@@ -500,13 +503,12 @@ extern "C" int ubatch_attention_static_scratch(kv_cache *c, const kv_split *sp, 
         int cur = -1;
         cudaError_t e = cudaGetDevice(&cur);
         if (e != cudaSuccess) return cuda_fail(c, e, "cudaGetDevice");
-        if (cur != d->device || cur < 0 || cur >= MAX_DEVICES)
+        if (cur != d->device)
             return c->set_err(KV_E_INVAL, "static-scratch attention: make the cache's device current");
         if (sync_would_allocate(c, sp))
             return c->set_err(KV_E_INVAL, "static-scratch attention: device tables need a larger upload buffer "
                                           "(call kv_store for this split first)");
-        unsigned char *scratch = nullptr;
-        if ((e = static_scratch(cur, &scratch)) != cudaSuccess) return cuda_fail(c, e, "scratch address");
+        unsigned char *scratch = d->static_scratch;   // looked up at kv_init
         cudaStream_t st = static_cast<cudaStream_t>(stream);
         if ((rc = sync_device(c, sp, st)) != KV_OK) return rc;
         kvk::UbView v = make_view(c, sp, ub);

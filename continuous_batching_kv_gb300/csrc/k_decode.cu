@@ -884,14 +884,14 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 }
 
 template <int NQ>
+cudaError_t load_nq() {
+    return cudaFuncSetAttribute(k_decode<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<NQ>());
+}
+
+// The shared-memory attribute was set for the current device by load_decode_kernels.
+template <int NQ>
 cudaError_t launch_nq(const CUtensorMap *tm, const kvk::DecodeArgs &a, int32_t grid_x, cudaStream_t st) {
-    static bool smem_set = false;
     constexpr size_t SMEM = smem_bytes<NQ>();
-    if (!smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_decode<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
-        if (e != cudaSuccess) return e;
-        smem_set = true;
-    }
     // a programmatic dependent of the kernel before it (normally the K/V store)
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -913,6 +913,14 @@ cudaError_t launch_nq(const CUtensorMap *tm, const kvk::DecodeArgs &a, int32_t g
 namespace kvk {
 
 int32_t decode_ctas_per_sm() { return 2; }
+
+cudaError_t load_decode_kernels() {
+    cudaError_t e;
+    if ((e = load_nq<1>()) != cudaSuccess || (e = load_nq<2>()) != cudaSuccess || (e = load_nq<4>()) != cudaSuccess ||
+        (e = load_nq<8>()) != cudaSuccess || (e = load_nq<16>()) != cudaSuccess)
+        return e;
+    return cudaSuccess;
+}
 
 cudaError_t launch_decode(const CUtensorMap *tm, const DecodeArgs &a, int32_t grid_x, cudaStream_t st) {
     if (a.nq_max <= 1) return launch_nq<1>(tm, a, grid_x, st);

@@ -524,6 +524,15 @@ cudaError_t launch_plan(const UbView &u, const Plan &p, int32_t n_stream, int32_
     return cudaGetLastError();
 }
 
+cudaError_t load_plan_kernels() {
+    cudaFuncAttributes fa;
+    cudaError_t e;
+    if ((e = cudaFuncGetAttributes(&fa, k_plan_tiles)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, k_plan_compact)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, k_plan_work)) != cudaSuccess) return e;
+    return cudaFuncGetAttributes(&fa, k_mask);
+}
+
 cudaError_t launch_mask(const UbView &u, uint16_t *mask, cudaStream_t st) {
     k_mask<<<dim3((u.n_kv + 255) / 256, u.n_tokens), 256, 0, st>>>(u, mask);
     return cudaGetLastError();

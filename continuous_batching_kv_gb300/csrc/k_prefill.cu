@@ -853,15 +853,16 @@ __global__ void __launch_bounds__(128, 8) k_merge_pf(const kvk::PrefillArgs a) {
 
 namespace kvk {
 
+cudaError_t load_prefill_kernels() {
+    cudaError_t e = cudaFuncSetAttribute(k_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    return cudaFuncGetAttributes(&fa, k_merge_pf);
+}
+
+// The shared-memory attribute was set for the current device by load_prefill_kernels.
 cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const PrefillArgs &a,
                            int32_t grid_x, cudaStream_t st) {
-    static bool smem_set = false;
-    if (!smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        smem_set = true;
-    }
     // Both kernels are programmatic dependents of the kernel before them: the
     // attention kernel sets up (and, with early_ok, reads its plan) while the K/V
     // store finishes; the merge reads the plan while the attention kernel runs.

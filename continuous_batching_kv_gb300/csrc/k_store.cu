@@ -78,11 +78,11 @@ namespace kvk {
 
 cudaError_t launch_store(void *k_cache, void *v_cache, const void *k_cur, const void *v_cur,
                          const kvi::DevRow *rows, int32_t n_tokens, int32_t row_bytes,
-                         int64_t n_cells, int32_t *err, cudaStream_t st) {
+                         int64_t n_cells, int32_t *err, int32_t n_sm, cudaStream_t st) {
     const int32_t cpr = row_bytes / 16;
     const int64_t total = (int64_t)n_tokens * cpr;
     int64_t blocks = (total + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks > (int64_t)n_sm * 16) blocks = (int64_t)n_sm * 16;
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -98,14 +98,22 @@ cudaError_t launch_store(void *k_cache, void *v_cache, const void *k_cur, const 
     return cudaGetLastError();
 }
 
-cudaError_t launch_upload(const void *src, void *dst, size_t bytes, cudaStream_t st) {
+cudaError_t launch_upload(const void *src, void *dst, size_t bytes, int32_t n_sm, cudaStream_t st) {
     const int64_t n16 = (int64_t)(bytes / 16);
     int64_t blocks = (n16 + 255) / 256;
     if (blocks < 1) blocks = 1;
-    if (blocks > 152 * 4) blocks = 152 * 4;
+    if (blocks > (int64_t)n_sm * 4) blocks = (int64_t)n_sm * 4;
     k_upload<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n16,
                                                 (int32_t)(bytes % 16));
     return cudaGetLastError();
+}
+
+cudaError_t load_store_kernels() {
+    cudaFuncAttributes fa;
+    cudaError_t e;
+    if ((e = cudaFuncGetAttributes(&fa, k_store)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, k_upload)) != cudaSuccess) return e;
+    return cudaFuncGetAttributes(&fa, k_apply_deltas);
 }
 
 cudaError_t launch_apply_deltas(const kvi::Delta *d, int32_t n, int32_t n_words, int32_t *pos,

@@ -73,11 +73,19 @@ struct Plan {
 // k_store.cu
 cudaError_t launch_store(void *k_cache, void *v_cache, const void *k_cur, const void *v_cur,
                          const kvi::DevRow *rows, int32_t n_tokens, int32_t row_bytes,
-                         int64_t n_cells, int32_t *err, cudaStream_t st);
+                         int64_t n_cells, int32_t *err, int32_t n_sm, cudaStream_t st);
 // src: mapped pinned host memory (device-visible address); dst: device memory
-cudaError_t launch_upload(const void *src, void *dst, size_t bytes, cudaStream_t st);
+cudaError_t launch_upload(const void *src, void *dst, size_t bytes, int32_t n_sm, cudaStream_t st);
 cudaError_t launch_apply_deltas(const kvi::Delta *d, int32_t n, int32_t n_words, int32_t *pos,
                                 uint32_t *epoch, uint64_t *bits, cudaStream_t st);
+
+// Per device, at cache creation (the device current): load every kernel's
+// module and set the attributes launches rely on, so that later calls obtain
+// no device memory for code or static data (modules load lazily otherwise).
+cudaError_t load_store_kernels();
+cudaError_t load_plan_kernels();
+cudaError_t load_decode_kernels();
+cudaError_t load_prefill_kernels();
 
 // k_plan.cu
 cudaError_t launch_plan(const UbView &u, const Plan &p, int32_t n_stream, int32_t gx_dec, int32_t gx_pf,

@@ -327,9 +327,12 @@ int ubatch_attention(kv_cache *c, const kv_split *s, int32_t ub, int32_t layer,
  * Every call on a device, for any cache, shares the one array: calls whose
  * device work overlaps in time (other streams, other threads) race on it and
  * give wrong results; order them on one stream.  Each call clears the
- * counters on its stream before its kernel.  The first call on each device,
- * made with that device current, looks up the array's device address once;
- * make that first call before any stream capture begins.
+ * counters on its stream before its kernel; the array otherwise keeps the
+ * last call's contents.  The array's device memory is taken when kv_init
+ * creates a device cache (kv_init looks up its address on the current
+ * device, which loads the library's device image there), so this call itself
+ * obtains none; the 24 MiB stay held on that device until the process exits
+ * and are not counted by kv_device_bytes.
  */
 #define KV_STATIC_SCRATCH_BYTES (24u << 20)
 int ubatch_attention_static_scratch(kv_cache *c, const kv_split *s, int32_t ub, int32_t layer,
@@ -342,7 +345,10 @@ int ubatch_attention_static_scratch(kv_cache *c, const kv_split *s, int32_t ub, 
  */
 int kv_device_error(kv_cache *c);
 
-/* Bytes of device memory the library allocated for this cache. */
+/* Bytes of device memory the library allocated for this cache (cell mirror,
+ * tables, plan, split-K scratch).  Not counted: the fixed
+ * KV_STATIC_SCRATCH_BYTES array of ubatch_attention_static_scratch, held once
+ * per device by the process from the first kv_init on that device. */
 size_t kv_device_bytes(const kv_cache *c);
 
 /* Number of CUDA kernels this cache has launched so far (all entry points). */

@@ -6,6 +6,11 @@ Collected last on purpose: it must pass alone and after every other test has
 used the device (the scratch array is shared by all calls on a device).
 """
 
+import os
+import subprocess
+import sys
+import textwrap
+
 import numpy as np
 import pytest
 
@@ -111,3 +116,48 @@ def test_static_scratch_rejects_prefill_and_oversize():
         kv.kv_split_free(s)
     finally:
         p.close()
+
+
+# Run in a fresh process: nothing of the library has touched the device before
+# kv_init, so a module load or an allocation made by the first static-scratch
+# call would show as a drop in the device's free memory.
+_FRESH = textwrap.dedent("""
+    import sys, torch
+    sys.path.insert(0, {root!r})
+    import continuous_batching_kv_gb300 as kv
+    from workloads import configs
+    from tests.gpu_util import Pair
+    from tests.test_zz_no_alloc import _prepared
+    cfg = configs.config(3, n_layer=1)
+    p = Pair(cfg, oracle=False)
+    for call in cfg["setup"]:
+        s, _ = _prepared(p, call)
+        kv.kv_split_free(s)
+    s, qs = _prepared(p, cfg["measured"][0])
+    q = qs[0][0]
+    o = torch.empty((q.shape[0], p.H, p.d), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    lib0 = kv.kv_device_bytes(p.c)
+    kv.ubatch_attention_static_scratch(p.c, s, 0, 0, q, o)
+    torch.cuda.synchronize()
+    assert kv.kv_device_error(p.c) == 0
+    free1 = torch.cuda.mem_get_info()[0]
+    lib1 = kv.kv_device_bytes(p.c)
+    kv.ubatch_attention_static_scratch(p.c, s, 0, 0, q, o)
+    torch.cuda.synchronize()
+    free2 = torch.cuda.mem_get_info()[0]
+    print("FREE", free0, free1, free2, "LIB", lib0, lib1)
+    assert free0 == free1 == free2, (free0, free1, free2)
+    assert lib0 == lib1, (lib0, lib1)
+    kv.kv_split_free(s)
+    p.close()
+""")
+
+
+def test_static_scratch_first_call_obtains_no_memory():
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FRESH.format(root=root)], cwd=root,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    assert "FREE" in r.stdout
