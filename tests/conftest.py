@@ -32,3 +32,18 @@ def golden(name):
 @pytest.fixture
 def gold():
     return golden
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Worst attention error per GPU test against the tolerance (max-abs 2e-3,
+    rel-L2 1e-2), so that the margin is on record in the run's output."""
+    try:
+        from tests.gpu_util import MARGINS
+    except Exception:
+        return
+    if not MARGINS:
+        return
+    tr = terminalreporter
+    tr.write_line("worst attention error per test (max-abs / rel-L2 / outputs compared):")
+    for name, (a, r, n) in sorted(MARGINS.items()):
+        tr.write_line("  %-58s %.2e  %.2e  %d" % (name[:58], a, r, n))

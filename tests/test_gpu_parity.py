@@ -21,7 +21,7 @@ def _cuda():
     import continuous_batching_kv_gb300  # noqa: F401  (fails loudly if the library is missing)
 
 
-def _run(cfg, rows_sample=None, check_mask=False, poison=False, layers=None):
+def _run(cfg, rows_sample=None, check_mask=False, poison=False, layers=None, check_store=False, defer=False):
     p = Pair(cfg, poison=poison)
     try:
         for call in cfg["setup"]:
@@ -30,28 +30,32 @@ def _run(cfg, rows_sample=None, check_mask=False, poison=False, layers=None):
         outs = {}
         for call in cfg["measured"]:
             st, o = p.run_call(call, attend=True, rows_sample=rows_sample, check_mask=check_mask,
-                               layers=layers)
+                               layers=layers, defer=defer)
             stats += st
             outs.update(o)
+        if check_store:
+            p.check_store()
         return stats, outs
     finally:
         p.close()
 
 
 def test_config1_prompt_then_decode_all_rows_and_masks():
-    stats, _ = _run(configs.config(1), check_mask=True)
+    stats, _ = _run(configs.config(1), check_mask=True, check_store=True)
     assert len(stats) == 5
 
 
 def test_config1_nan_poisoned_cache():
     # unused cells hold NaN: masked cells must contribute nothing at all
-    stats, outs = _run(configs.config(1), check_mask=True, poison=True)
+    stats, outs = _run(configs.config(1), check_mask=True, poison=True, check_store=True)
     assert all(np.isfinite(v).all() for v in outs.values())
 
 
-def test_config2_prefill_5000_sampled_rows():
+def test_config2_prefill_5000_all_rows():
+    # every row of all 10 ubatches at layer 1 (the plan built at layer 0 is reused,
+    # as in a model's later layers); the oracle's rows run in worker processes
     cfg = configs.config(2, n_layer=2)
-    stats, _ = _run(cfg, rows_sample=lambda n: sample_rows(n, 24), check_mask=True, layers=[1])
+    stats, _ = _run(cfg, check_mask=True, layers=[1], defer=True)
     assert len(stats) == 10
 
 
@@ -72,7 +76,7 @@ def test_config3_decode_unified_all_rows():
 
 def test_config4_mixed_prefix_streams_and_twins():
     cfg = configs.config(4, n_layer=1)
-    stats, outs = _run(cfg, rows_sample=lambda n: sample_rows(n, 40), check_mask=True)
+    stats, outs = _run(cfg, rows_sample=lambda n: sample_rows(n, 40), check_mask=True, check_store=True)
     assert len(stats) == 7
     # prefix cells shared by 16 sequences give the same output as duplicated copies
     for s in range(16):
@@ -81,9 +85,9 @@ def test_config4_mixed_prefix_streams_and_twins():
         check_close(a, b.astype(np.float64), "twin %d" % s)
 
 
-def test_config5_full_size_one_layer_sampled():
+def test_config5_full_size_one_layer_all_rows():
     cfg = configs.config(5, n_layer=1)
-    stats, _ = _run(cfg, rows_sample=lambda n: sample_rows(n, 32))
+    stats, _ = _run(cfg)
     assert len(stats) == 1
 
 
@@ -99,7 +103,7 @@ def test_ragged_kv_size_and_streams():
                 "seq": [[0]] * 67 + [[1, 3]] * 40, "content": [0] * 67 + [1] * 40},
                {"pos": [97, 30, 40, 40], "seq": [[0], [2], [1], [3]], "content": [0, 2, 1, 3]},
            ]}
-    stats, _ = _run(cfg, check_mask=True)
+    stats, _ = _run(cfg, check_mask=True, check_store=True)
     assert len(stats) >= 5
 
 
@@ -255,3 +259,54 @@ def test_device_call_errors():
     assert e.value.code == kv.KV_E_STALE
     assert kv.kv_device_error(c) == 0
     kv.kv_free(c)
+
+
+@pytest.mark.parametrize("fixed", [False, True])
+def test_batching_loop_through_scheduler(fixed):
+    # ITER, "The loop that replaces the batch": the native scheduler retires,
+    # admits and assembles each pass; every pass's batch goes through
+    # kv_split_ubatches -> kv_prepare_cells -> kv_store -> ubatch_attention on two
+    # layers, and the oracle scheduler + oracle cache are driven the same way.
+    # Prompts up to 70 tokens at n_ubatch 48 put both kernels on the path (a
+    # sequence's 24+ rows in one ubatch take the tensor-core path), mixed with
+    # decode rows; retirements free cells that later admissions take.
+    import random
+    import continuous_batching_kv_gb300 as kv
+    from oracle import sched as S
+    kv_size, budget, n_seq_max, max_seqs = 640, 96, 6, 4
+    cfg = {"id": 17, "name": "loop", "shape": dict(configs.QWEN, n_layer=2),
+           "params": dict(n_ctx=kv_size, n_batch=budget, n_ubatch=48, n_seq_max=n_seq_max, n_stream=1),
+           "setup": [], "measured": []}
+    p = Pair(cfg)
+    rng = random.Random(31 + fixed)
+    try:
+        sch = kv.kv_sched_init(p.c, max_seqs=max_seqs, token_budget=budget, fixed=fixed)
+        osch = S.Scheduler(kv_size=kv_size, n_seq_max=n_seq_max, max_seqs=max_seqs, token_budget=budget,
+                           fixed=fixed)
+        for _ in range(16):
+            L, N = rng.randint(1, 70), rng.randint(1, 12)
+            assert kv.kv_sched_submit(sch, L, N) == osch.submit(L, N)
+        passes = 0
+        while True:
+            b = kv.kv_sched_next(sch)
+            retired, pos, seq = osch.next_batch()
+            assert b.retired == retired and list(b.pos) == pos and list(b.seq) == seq
+            for q in retired:
+                p.o.seq_rm(q, 0, -1)
+            if not pos:
+                break
+            by_seq = {r.seq: r.rid for r in osch.running}
+            call = {"pos": pos, "seq": [[q] for q in seq], "content": [100 + by_seq[q] for q in seq]}
+            sp = kv.kv_split_sched_batch(p.c, b)
+            st, _ = p.run_call(call, check_mask=True, split=sp)
+            assert st
+            kv.kv_sched_advance(sch)
+            osch.advance()
+            passes += 1
+        info = kv.kv_sched_stats(sch)
+        assert (info["passes"], info["useful"]) == (osch.passes, osch.useful) and passes == osch.passes
+        assert passes >= 20
+        p.check_store()
+        kv.kv_sched_free(sch)
+    finally:
+        p.close()
