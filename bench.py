@@ -54,6 +54,11 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="default workload only: skip the decode legs (the 256- and 8-sequence decode "
+                         "workloads measured after it)")
+    ap.add_argument("--decode-steps", type=int, default=20,
+                    help="timed steps of each decode leg")
     ap.add_argument("--layers", type=int, default=None,
                     help="run fewer layers than the workload has (small cases for profiling only)")
     ap.add_argument("--ubatch", type=int, default=None,
@@ -238,6 +243,14 @@ class OursArm:
             self._setup()
             self._prepare_inputs()
 
+    def close(self):
+        """Free the library cache and this arm's device tensors."""
+        if self.c is not None:
+            self.torch.cuda.synchronize()
+            self.kv.kv_free(self.c)
+            self.c = None
+        self.kc = self.vc = self.calls = None
+
     def _randn(self, *shape):
         return self.torch.randn(*shape, generator=self.gen, device=self.dev, dtype=self.torch.float32).half()
 
@@ -407,6 +420,12 @@ class OursArm:
         self.reset()
         last = []
         off = max(0, self.step_no) if self.decode_loop else 0
+        # algorithmic work of this step's attention launches, all layers (counts only)
+        self.step_work = [0, 0]
+        for _, ubs, _ in self.calls:
+            for t in ubs:
+                self.step_work[0] += self.L * (t["pairs"] + off * t["n"])
+                self.step_work[1] += self.L * (t["bytes"] + off * t["row_kv_bytes"])
         cur = self.e2e_n & 1 if host else 0
         if host:
             if not self.prefetched:
@@ -489,8 +508,11 @@ def run_ours(args, rank, world, device):
     t1 = torch.cuda.Event(enable_timing=True)
     w0 = datetime.datetime.now()
     t0.record(arm.stream)
+    work = [0, 0]
     for _ in range(args.steps):
         arm.step()
+        work[0] += arm.step_work[0]
+        work[1] += arm.step_work[1]
     t1.record(arm.stream)
     barrier()
     clocks.mark(w0, datetime.datetime.now())
@@ -539,6 +561,19 @@ def run_ours(args, rank, world, device):
                  "timing": "CUDA events around each attention launch of layers >= 1, "
                            "on a second pass over the same steps",
                  "avg_launch_us": round(1e3 * sum(durs) / max(1, len(durs)), 2)})
+    # The same algorithmic work over the whole unbracketed timed region (split,
+    # reservation, stores, plans and attention of every step): a lower bound on
+    # the attention launches' own rate, free of the bracketing events' cost.
+    step_s = ms_total / 1e3
+    if roof["bound"] == "hbm":
+        st_ach = work[1] / step_s / 1e9
+    else:
+        st_ach = work[0] * 4 * arm.d * arm.H / step_s / 1e12
+    roof["step_level"] = {"achieved": round(st_ach, 2 if roof["bound"] == "tensor" else 1),
+                          "frac": round(st_ach / roof["peak"], 4), "unit": roof["unit"],
+                          "basis": "algorithmic %s of every attention launch of the timed steps / the "
+                                   "timed region (whole steps: host work, stores, plans included)"
+                                   % ("bytes" if roof["bound"] == "hbm" else "flops")}
 
     e2e = None
     if not args.no_e2e:
@@ -772,6 +807,29 @@ def run_loop(args, device):
             "clocks": clocks.stop()}
 
 
+def decode_legs(args, rank, world, device):
+    """The decode side of the metric, measured in the same run after the
+    default workload: the 256-sequence Llama-shape decode (lognormal
+    contexts, 32 layers) and the 8-sequence Qwen-shape decode, each through
+    run_ours with its own timed region, per-launch roofline, step-level
+    roofline and clock record (no end-to-end pass, no oracle)."""
+    import argparse as _ap
+    import torch
+    out = {}
+    for cid in (5, 3):
+        sub = _ap.Namespace(**vars(args))
+        sub.config, sub.no_e2e, sub.steps = cid, True, args.decode_steps
+        l, a = run_ours(sub, rank, world, device)
+        a.close()
+        del a
+        torch.cuda.empty_cache()
+        out[l["config"]["workload"]] = {
+            "metric": "decode KV-attention GB/s", "tokens_per_s": l["value"], "ms_per_step": l["ms_per_step"],
+            "steps": l["steps"], "warmup": l["warmup"], "config": l["config"], "roofline": l["roofline"],
+            "gpu_launches": l["gpu_launches"], "clocks": l["clocks"]}
+    return out
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -793,7 +851,12 @@ def main():
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
-    line, _ = run_ours(args, rank, world, local)
+    line, arm = run_ours(args, rank, world, local)
+    if args.config == 2 and not args.no_decode and args.layers is None and args.ubatch is None \
+            and args.streams is None:
+        arm.close()
+        del arm
+        line["decode"] = decode_legs(args, rank, world, local)
     if rank == 0:
         if not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline(cfg)
