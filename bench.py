@@ -556,7 +556,7 @@ def run_ours(args, rank, world, device):
         achieved = (sum(p for _, p, _ in res) * per_pair_flops) / secs / 1e12 if durs else 0.0
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tflops, "unit": "TFLOP/s",
                 "frac": round(achieved / tflops, 4), "traffic": None,
-                "kernel": "ubatch_attention (k_prefill + k_merge_pf)"}
+                "kernel": "ubatch_attention (k_prefill)"}
     roof.update({"peak_source": peak_src, "launches_timed": len(durs),
                  "timing": "CUDA events around each attention launch of layers >= 1, "
                            "on a second pass over the same steps",

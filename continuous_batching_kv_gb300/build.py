@@ -13,6 +13,7 @@ calls work there; device calls return an error).
 import argparse
 import concurrent.futures as cf
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -47,15 +48,40 @@ def headers():
     return hs
 
 
+# Kernels that split their registers between warpgroups (setmaxnreg): the split
+# in the source assumes this launch register count per thread, and an increase
+# beyond what the launch holds would wait forever, so the build refuses any
+# other count.
+REG_SPLIT = {"k_prefill.cu": ("k_prefill", 168)}
+
+
+def _check_regs(src, log):
+    name, want = REG_SPLIT[os.path.basename(src)]
+    lines = log.splitlines()
+    for i, line in enumerate(lines):
+        if "Compiling entry function" in line and name in line:
+            for nxt in lines[i + 1:i + 6]:
+                m = re.search(r"Used (\d+) registers", nxt)
+                if m:
+                    if int(m.group(1)) != want:
+                        raise RuntimeError("%s: ptxas allocated %s registers per thread, the register split "
+                                           "assumes %d" % (name, m.group(1), want))
+                    return
+    raise RuntimeError("%s: no ptxas register count found for %s" % (src, name))
+
+
 def _compile(src, verbose):
     obj = os.path.join(BUILD, os.path.basename(src) + ".o")
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
            "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
-    if src.endswith(".cu"):
-        cmd[1:1] = ["-Xptxas", "-v"] if verbose else []
+    check = os.path.basename(src) in REG_SPLIT
+    if src.endswith(".cu") and (verbose or check):
+        cmd[1:1] = ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, " ".join(cmd), r.stderr))
+    if check:
+        _check_regs(src, r.stderr)
     return obj, r.stderr
 
 

@@ -151,6 +151,43 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, int
         : "memory");
 }
 
+// Bulk copy of `bytes` contiguous bytes (a multiple of 16, both addresses
+// 16-byte aligned) from global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Bulk copy of `bytes` contiguous bytes (a multiple of 16, both addresses
+// 16-byte aligned) from shared to global memory, in this thread's current bulk
+// group; bulk_commit closes the group, bulk_wait_read<N> waits until at most N
+// of this thread's groups still read their shared source, bulk_wait_all until
+// every group of this thread has completed its writes.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(reinterpret_cast<uint64_t>(dst)), "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// 2-D tiled store of box (x, y) from shared memory, in this thread's current bulk
+// group.  x (innermost) must be a multiple of 4 for 32-bit data; x, y >= 0.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, int32_t x, int32_t y, const void *src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(src))
+                 : "memory");
+}
+
+// Order this thread's async-proxy global accesses with its generic ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a tile
 // written by TMA with 128-byte swizzling (rows of 128 bytes, 1024-byte atoms).
 __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk) {

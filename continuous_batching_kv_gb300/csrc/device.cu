@@ -43,7 +43,9 @@ struct DeviceState {
     int32_t max_blocks = 0;
     int32_t gx_dec = 1, gx_pf = 1;          // CTA columns of the decode / prefill grids
     float *d_part_dec = nullptr;
-    float *d_part_pf = nullptr;
+    float *d_part_pf = nullptr;      // prefill partials: O rows [rows][128], then (m, l) [rows][2]
+    int64_t pf_part_rows = 0;        // cap_pf * n_head_kv * PF_M
+    CUtensorMap tm_part{};           // the O rows as a 2-D fp32 matrix, 32 x 32 boxes, 128-byte swizzle
     int32_t *d_err = nullptr;
     // device address of the library's fixed static-scratch array on this device
     // (looked up at kv_init, which also makes the runtime load and back it)
@@ -283,7 +285,7 @@ int device_init(kv_cache *c) {
         (e = dev_alloc(d, &p.blk_nitems, d->max_blocks)) != cudaSuccess ||
         (e = dev_alloc(d, &p.counters, (size_t)d->max_blocks * hkv)) != cudaSuccess ||
         (e = dev_alloc(d, &p.cta_item0, (size_t)d->gx_dec + d->gx_pf + 2)) != cudaSuccess ||
-        (e = dev_alloc(d, &p.pf_rows, (size_t)d->gx_pf * 128)) != cudaSuccess ||
+        (e = dev_alloc(d, &p.pf_rows, (size_t)d->gx_pf * PF_M)) != cudaSuccess ||
         (e = dev_alloc(d, &p.pf_first, (size_t)d->gx_pf * 4)) != cudaSuccess ||
         (e = dev_alloc(d, &d->d_part_dec, (size_t)p.cap_dec * hkv * DEC_PART_FLOATS)) != cudaSuccess ||
         (e = dev_alloc(d, &d->d_part_pf, (size_t)p.cap_pf * hkv * PF_PART_FLOATS)) != cudaSuccess ||
@@ -291,6 +293,18 @@ int device_init(kv_cache *c) {
         return cuda_fail(c, e, "plan alloc");
     p.err = d->d_err;
     p.gqa = c->gqa;
+    d->pf_part_rows = (int64_t)p.cap_pf * hkv * PF_M;
+    {
+        auto enc = get_encode();
+        cuuint64_t dims[2] = {128, (cuuint64_t)d->pf_part_rows};
+        cuuint64_t strides[1] = {128 * sizeof(float)};
+        cuuint32_t box[2] = {32, 32};
+        cuuint32_t estr[2] = {1, 1};
+        if (!enc || enc(&d->tm_part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, d->d_part_pf, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return c->set_err(KV_E_CUDA, "cuTensorMapEncodeTiled failed (partials)");
+    }
     if ((e = cudaMemset(p.counters, 0, (size_t)d->max_blocks * hkv * sizeof(int32_t))) != cudaSuccess ||
         (e = cudaMemset(d->d_err, 0, sizeof(int32_t))) != cudaSuccess)
         return cuda_fail(c, e, "plan clear");
@@ -425,6 +439,7 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
             a.q = static_cast<const __half *>(q);
             a.o = o;
             a.part = d->d_part_pf;
+            a.part_ml = d->d_part_pf + d->pf_part_rows * 128;
             a.gx_dec = d->gx_dec;
             a.n_head = c->prm.n_head;
             a.n_head_kv = c->prm.n_head_kv;
@@ -432,9 +447,9 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
             a.scale_log2 = scale_log2;
             a.err = d->d_err;
             a.early_ok = early_ok ? 1 : 0;
-            if ((e = kvk::launch_prefill(&d->tm_k[layer], &d->tm_v[layer], a, d->gx_pf, st)) != cudaSuccess)
+            if ((e = kvk::launch_prefill(&d->tm_k[layer], &d->tm_v[layer], &d->tm_part, a, d->gx_pf, st)) != cudaSuccess)
                 return cuda_fail(c, e, "prefill launch");
-            c->launches += 2;   // attention + split-K merge
+            c->launches += 1;
         }
         return KV_OK;
     });
@@ -447,7 +462,13 @@ int kv_device_error(kv_cache *c) {
     int32_t v = 0;
     if ((e = cudaMemcpy(&v, c->dev->d_err, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
         return cuda_fail(c, e, "error word read");
-    if (v) cudaMemset(c->dev->d_err, 0, sizeof(int32_t));
+    if (v) {
+        // a kernel gave up part-way: clear the word, and the split-K completion
+        // counters it may have left counted, so that the next launch starts clean
+        cudaMemset(c->dev->d_err, 0, sizeof(int32_t));
+        cudaMemset(c->dev->plan.counters, 0, (size_t)c->dev->max_blocks * c->prm.n_head_kv * sizeof(int32_t));
+        cudaDeviceSynchronize();
+    }
     return v;
 }
 

@@ -17,9 +17,9 @@ enum : int32_t { PATH_DECODE = 0, PATH_PREFILL = 1 };
 
 // Rows of one group (same stream, same first sequence id) are cut into
 // blocks.  A decode block holds at most DEC_QMAX query vectors (rows x GQA
-// group size); a prefill block fills one 128-lane MMA tile.
+// group size); a prefill block fills two 128-lane MMA tiles.
 constexpr int DEC_QMAX = 16;
-constexpr int PF_M = 128;
+constexpr int PF_M = 256;
 // A group takes the prefill path when it has at least this many query vectors.
 constexpr int PF_MIN_QV = 64;
 // Cells per plan tile, and cells per TMA sub-box inside it.

@@ -175,8 +175,9 @@ constexpr int64_t DEC_ITEM_COST = 16;
 constexpr int64_t DEC_MIN_TAKE = 8;
 // Decode block costs staged in shared memory for the budget search.
 constexpr int32_t DEC_STAGE = 2048;
-// Prefill, in units of one pair of 64-cell tiles: start-up plus epilogue of one item.
-constexpr int64_t PF_ITEM_COST = 5;
+// Prefill, in units of one step (a pair of 64-cell tiles for both MMA tiles of a
+// block): start-up plus epilogue of one item.
+constexpr int64_t PF_ITEM_COST = 3;
 // Extra cost of the piece that holds a block's last pair (its causal diagonal, with
 // the per-cell mask), in the same units.
 constexpr int64_t PF_DIAG_COST = 1;
@@ -377,8 +378,8 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
             }
             __syncthreads();
             // the rows behind each column's first item, one entry per query vector
-            for (int32_t e = tid; e < (int32_t)gx * 128; e += blockDim.x) {
-                const int32_t x = e >> 7, qv = e & 127;
+            for (int32_t e = tid; e < (int32_t)gx * kvi::PF_M; e += blockDim.x) {
+                const int32_t x = e / kvi::PF_M, qv = e % kvi::PF_M;
                 p.pf_rows[e] = qv < s_nq[x] ? u.perm[s_r0[x] + qv / p.gqa] : -1;
             }
             continue;

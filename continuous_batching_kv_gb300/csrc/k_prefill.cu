@@ -6,33 +6,39 @@
 // not later) it is the same softmax(q K^T / sqrt(d) + mask) V as decode, but
 // now a dense contraction worth putting on the tensor cores.
 //
-// Design (sm_103a, one CTA of 608 threads per SM):
-//  * a block = up to 128 query vectors (rows sharing a stream and first
-//    sequence id, times the GQA group) = the 128 TMEM lanes of one MMA tile;
-//    a work item = one block, one KV head, a chunk of the block's list of
-//    visible 64-cell tiles, consumed two at a time (N = 128 cells);
-//  * warp 16 streams K tiles with TMA (128-byte swizzle) into a 3-slot ring,
-//    with each pair's list entries, flags and per-cell visibility fetched ahead
-//    into a metadata ring; warp 18 streams V tiles into a 3-slot ring; warp 17
-//    allocates TMEM and one of its threads issues tcgen05.mma in a fixed order
-//    (S_0, S_1, then PV_j and S_j+2 per pair, each after a blocking bounded
-//    wait): S = Q K^T (M 128, N 128, K 128; Q held in TMEM) into one of two
-//    TMEM score buffers, and O += P V with P read from TMEM (fp16, written over
-//    S) and V MN-major from shared memory; tcgen05.commit signals the mbarriers;
-//  * warps 0-15: thread (n, qd) owns cells 32qd .. 32qd + 31 of query vector n
-//    (TMEM lane n) and d = 32qd .. 32qd + 31 of O; it reads its 32 columns of S
-//    with one tcgen05.ld, applies the mask per cell on tiles that are not fully
-//    visible, exchanges the row maximum with the row's other three threads,
-//    runs the online softmax in base 2 (the exponent rounded to fp16, two
-//    exponentials per ex2.approx.f16x2), writes P (fp16, two cells per 32-bit
-//    column) at the start of the S columns it read, and rescales its part of O
-//    in TMEM only when the running maximum grew by more than 2^8 (otherwise the
-//    stale maximum is kept; the final normalisation uses the same one);
+// Design (sm_103a, one CTA of 384 threads per SM):
+//  * a block = up to 256 query vectors (rows sharing a stream and first
+//    sequence id, times the GQA group), held as two 128-lane MMA tiles A
+//    (query vectors 0..127) and B (128..255) that share every K/V tile; a work
+//    item = one block, one KV head, a chunk of the block's list of visible
+//    64-cell tiles, consumed two at a time (one step = 128 cells);
+//  * TMEM (512 columns): S_A, S_B (fp32 scores, 128 columns each; P is written
+//    over the first 64 as fp16 pairs), O_A, O_B (fp32, d = 0..127);
+//  * shared memory: Q_A, Q_B (written by the softmax threads, 128-byte
+//    swizzle), a 2-stage K ring and a 2-stage V ring of 128-cell tiles (TMA,
+//    128-byte swizzle), a ring of per-step metadata;
+//  * warp 8 streams K tiles and the steps' metadata (list entries, flags, the
+//    cells' positions and sequence membership), warp 10 streams V tiles, one
+//    thread of warp 9 issues the MMAs in the order
+//        S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
+//    so that the tensor core works on one tile while the other tile's softmax
+//    runs (S = Q K^T as SS-MMA M128 N128 K16 x 8; O += P V as TS-MMA with P
+//    read from TMEM);
+//  * warps 0-3 (tile A) and 4-7 (tile B): one thread per query vector (TMEM
+//    lane) holds the row's 128 scores of a step, applies the per-cell mask on
+//    steps that are not fully visible, takes the row maximum locally, runs the
+//    online softmax in base 2 (exponents rounded to fp16, two per
+//    ex2.approx.f16x2), writes P and rescales its O row only when the running
+//    maximum grew by more than 2^8 (otherwise the stale maximum is kept; the
+//    final normalisation uses the same one);
 //  * cells nobody in the block may see get their V rows zeroed in shared
 //    memory before the PV product (P is 0 there, but 0 * NaN would not be);
-//  * a block split over several CTAs leaves one partial (m, l, O) per piece,
-//    merged by a small second kernel launched as a programmatic dependent (it
-//    reads the plan while this kernel runs); every mbarrier wait is bounded.
+//  * a block split over several CTAs leaves one partial (m, l, O) per piece;
+//    the CTAs whose last item is a piece of that block wait (bounded) until
+//    every piece is counted and merge a share of its query vectors each, so no
+//    second kernel is needed.  (Only a column's last item waits, and a split
+//    block's other pieces are either the last item of an earlier column or the
+//    first of a later one, so every wait ends.)  Every wait is bounded.
 
 #include "dev_common.cuh"
 #include "kernels.h"
@@ -41,70 +47,78 @@
 namespace {
 
 using kvi::TILE;
+using kvi::PF_M;
 
-constexpr int NSM = 512;                 // softmax threads: four per TMEM lane
-constexpr int NT = NSM + 96;             // + K producer, MMA and V producer warps
-constexpr int W_K = NSM / 32;            // K producer warp
-constexpr int W_MMA = W_K + 1;           // TMEM allocation and MMA issue
-constexpr int W_V = W_K + 2;             // V producer warp
-constexpr int M = 128;
+constexpr int NT = 384;                  // 12 warps
+constexpr int W_K = 8;                   // K producer + metadata
+constexpr int W_MMA = 9;                 // TMEM allocation and MMA issue
+constexpr int W_V = 10;                  // V producer (warp 11 only takes part in set-up)
+constexpr int NSM = 256;                 // softmax threads (warps 0-7)
+constexpr int M = 128;                   // lanes of one MMA tile
+static_assert(PF_M == 2 * M, "a prefill block is two MMA tiles");
 constexpr int HALF = 128 * 128;          // [128 rows][64 fp16], 128-byte rows
-constexpr int TILEB = 2 * HALF;          // 32 KiB
+constexpr int TILEB = 2 * HALF;          // 32 KiB: 128 rows x 128 fp16
 constexpr int BOX = 64 * 128;            // one TMA box: 64 rows x 64 fp16
-constexpr int KSTAGES = 3;             // K ring: K of pair g + 3 loads once S of g has read K of g
-constexpr int VSTAGES = 3;             // V ring: V of pair g + 3 loads once PV of g is done
-constexpr int OFF_K = 0;
+constexpr int KSTAGES = 2;
+constexpr int VSTAGES = 2;
+constexpr int OFF_Q = 0;                 // Q_A, Q_B
+constexpr int OFF_K = 2 * TILEB;
 constexpr int OFF_V = OFF_K + KSTAGES * TILEB;
 constexpr int OFF_AUX = OFF_V + VSTAGES * TILEB;
-constexpr int PART_STRIDE = 132;
-constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128), S1 [128,256) (P written over S), O [256,384), Q [384,448)
-constexpr uint32_t COL_O = 256;          // O: fp32 accumulator, d = 0 .. 127
-constexpr uint32_t COL_Q = 384;          // Q: fp16, two d per column (the A operand of S = Q K^T)
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_S = 0;            // + 128 * tile
+constexpr uint32_t COL_O = 256;          // + 128 * tile
 constexpr float RESCALE_LOG2 = 8.0f;
-constexpr unsigned POLL_NS = 32;         // back-off of the polling producer / MMA loops
+// Register split (setmaxnreg, per warpgroup): the kernel is launched with
+// LAUNCH_REGS registers per thread (the build checks ptxas's count); the two
+// softmax warpgroups take SM_REGS each, the producer / MMA warpgroup gives back
+// down to PR_REGS.  The shares must not exceed what the launch holds, or the
+// increase would wait forever.
+constexpr int LAUNCH_REGS = 168;
+constexpr int SM_REGS = 224;
+constexpr int PR_REGS = 56;
+static_assert(LAUNCH_REGS * NT <= 65536, "launch registers");
+static_assert(2 * 128 * SM_REGS + 128 * PR_REGS <= LAUNCH_REGS * NT, "register split exceeds the launch's registers");
+static_assert(SM_REGS % 8 == 0 && PR_REGS % 8 == 0 && PR_REGS >= 24 && SM_REGS <= 256, "setmaxnreg counts");
+constexpr unsigned POLL_NS = 32;
 
 constexpr uint32_t IDESC_S = tc::idesc_f16(128, 128, 0, 0);
 constexpr uint32_t IDESC_PV = tc::idesc_f16(128, 128, 0, 1);
 
-// Metadata ring.  Pair g's slot is rewritten by the K load of pair g + MSLOTS,
-// which needs S of g + MSLOTS - KSTAGES to be done, which was issued only after
-// the PV of the pair before it in its score buffer (g + MSLOTS - KSTAGES - 2 or
-// later) was issued, i.e. after the softmax finished that pair: with MSLOTS >=
-// KSTAGES + 2 the softmax is done with pair g, and the V load of g (which reads
-// the slot) went out before that PV.
-constexpr int MSLOTS = 8;
+// Metadata ring.  The slot of step g is rewritten for step g + MSLOTS once the
+// K stage of step g + MSLOTS - KSTAGES is free, i.e. after S_A and S_B of that
+// step completed; those were issued after PV_A and PV_B of the step before,
+// which waited for both tiles' softmax of that step -- so both softmax groups
+// are past step g + MSLOTS - KSTAGES - 1 >= g + 1, and the V producer, which
+// issued V of that step, is past g too.
+constexpr int MSLOTS = 6;
 static_assert(MSLOTS >= KSTAGES + 2, "metadata ring too short for the K ring");
 
-struct __align__(16) Meta {     // per pair tile: what the producer learned about it (16-byte loads)
-    int32_t full;
+struct __align__(16) Meta {     // per step: what the K producer learned about its 128 cells
+    int32_t full;             // every row of the block sees every cell
     int32_t ys[2];            // TMA row coordinates of the two 64-cell halves
     int32_t pad;
     int32_t cpos[128];
-    uint8_t has[128];         // cell holds the block's sequence and is not from a later ubatch
-    uint8_t anyvis[128];      // ... and some row of the block may see it
+    uint32_t has[4];          // bit c: cell 32 r + c holds the block's sequence, not from a later ubatch
+    uint32_t anyvis[4];       // ... and some row of the block may see it
 };
 
 struct __align__(16) Aux {
     uint64_t k_full[KSTAGES], k_empty[KSTAGES], v_full[VSTAGES], v_empty[VSTAGES];
     uint64_t meta_full[MSLOTS];
-    uint64_t s_full[2], p_full[2], pv_done[2], q_full, spare;   // p_full, pv_done [g & 1]: pair g
-    uint64_t lbar;            // the halves' row-sum exchange at each item's end, all 256 threads
-    uint64_t pbar[4];         // per lane quarter: the four warps of a row exchange maxima per pair
+    uint64_t s_full[2], p_full[2], pv_done[2], q_full[2];   // [tile]
+    uint64_t wbar;            // the softmax threads meet (256 arrivals)
+    uint64_t gbar;            // a merge may start: every piece of the block is counted (1 arrival)
+    uint64_t mbar;            // the partials of one merge pass are in shared memory (bulk copies)
+    uint64_t spare;
     uint32_t tmem_base;
     int32_t fail;
-    int32_t flag;
-    int32_t pad;
+    int32_t mrg_lo, mrg_hi;   // this CTA's share of the merged block's query vectors
     Meta meta[MSLOTS];
-    float red[2][4][M];       // [pair parity][cell quarter][row]: partial row maxima
-    float lex[2][4][M];       // [item parity][cell quarter][row]: row sums
 };
 
 constexpr size_t SMEM_BYTES = OFF_AUX + sizeof(Aux);
-
-// Output staging at the CTA's last item, in the K ring: per softmax warp 32 rows
-// of 32 floats, padded so that the lanes' 16-byte writes fall in distinct banks.
-constexpr int STG_STRIDE = 36;
-static_assert((NSM / 32) * 32 * STG_STRIDE * 4 <= KSTAGES * TILEB, "output staging exceeds the K ring");
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, volatile int32_t *fail) {
     if (kvd::mbar_try_wait(bar, parity)) return true;
@@ -118,6 +132,10 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, vol
     }
     return true;
 }
+
+// True while no wait has given up, agreed by all 32 lanes of the warp (so a
+// failure never splits a warp in front of a warp-collective instruction).
+__device__ __forceinline__ bool warp_ok(volatile int32_t *fail) { return __all_sync(0xffffffffu, *fail == 0); }
 
 // 2^x with the hardware's approximate base-2 exponential (ex2.approx.ftz:
 // flushes subnormals, 2^-inf = +0).
@@ -165,12 +183,46 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return d;
 }
 
-// True while no wait has given up, agreed by all 32 lanes of the warp (so a
-// failure never splits a warp in front of a warp-collective instruction).
-__device__ __forceinline__ bool warp_ok(volatile int32_t *fail) { return __all_sync(0xffffffffu, *fail == 0); }
+// 1/x with the hardware's approximate reciprocal (rcp.approx.ftz: about 1 ulp).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ int32_t ld_acquire(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// S = Q K^T of one tile: 8 SS-MMAs (K = 16 each) over d = 0..127; a0 / b0 are the
+// descriptors of Q and of the K stage, advanced by the 32-byte K steps inside a
+// 128-byte swizzled row and by the second d half.  The bases go through an opaque
+// move first, so that the eight offset descriptors are formed next to their MMA
+// (one add each) instead of all being kept in registers across the issue loop;
+// forming a whole descriptor per MMA would cost the issuing thread more than the
+// tensor pipe takes for the MMA.
+__device__ __forceinline__ void issue_s8(uint32_t d, uint64_t a0, uint64_t b0) {
+    asm volatile("" : "+l"(a0), "+l"(b0));
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t off = (uint64_t)(((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
+        tc::mma_ss(d, a0 + off, b0 + off, IDESC_S, kk > 0 ? 1u : 0u);
+    }
+}
+
+// O += P V of one tile: 8 TS-MMAs (16 cells each); P of cells 16kk .. 16kk + 15 is
+// 8 TMEM columns at p + 8kk, V (MN-major) rows 16kk .. at b0 + 2 KiB kk.
+__device__ __forceinline__ void issue_pv8(uint32_t d, uint32_t p, uint64_t b0, uint32_t acc) {
+    asm volatile("" : "+l"(b0), "+r"(p));
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        tc::mma_ts(d, p + 8u * (uint32_t)kk, b0 + (uint64_t)((kk * 2048) >> 4), IDESC_PV, (acc | (uint32_t)kk) ? 1u : 0u);
+}
 
 struct ItemInfo {
-    int32_t block, t0, t1, pairs;
+    int32_t block, t0, t1, steps;
 };
 
 __device__ __forceinline__ ItemInfo item_info(const kvk::PrefillArgs &a, int32_t wi) {
@@ -179,27 +231,34 @@ __device__ __forceinline__ ItemInfo item_info(const kvk::PrefillArgs &a, int32_t
     r.block = w.block;
     r.t0 = w.t0;
     r.t1 = w.t1;
-    r.pairs = (w.t1 - w.t0 + 1) / 2;
+    r.steps = (w.t1 - w.t0 + 1) / 2;
     return r;
+}
+
+// Is prefill item wi the last item of its CTA column?  (A column's items are
+// consecutive.)
+__device__ __forceinline__ bool last_of_column(const kvk::PrefillArgs &a, int32_t wi, int32_t n_items) {
+    return wi + 1 >= n_items || a.p.work[a.p.cap_dec + wi + 1].cta != a.p.work[a.p.cap_dec + wi].cta;
 }
 
 __global__ void __launch_bounds__(NT, 1)
 k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-          const kvk::PrefillArgs a) {
+          const __grid_constant__ CUtensorMap tm_part, const kvk::PrefillArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     Aux &x = *reinterpret_cast<Aux *>(smem + OFF_AUX);
     volatile int32_t *fail = &x.fail;
     const int32_t tid = threadIdx.x;
     const int32_t warp = tid >> 5;
+    const int32_t lane = tid & 31;
     const int32_t hk = blockIdx.y;
     const int32_t G = a.gqa;
     const uint32_t sbase = kvd::smem_u32(smem);
 
     // Launched as a programmatic dependent: library state is read before waiting
     // for the previous kernel only when it was complete before that kernel began;
-    // Q, the K/V cache and the outputs are touched only after the wait.
+    // Q, the K/V cache, the outputs, the partials and the merge counters are
+    // touched only after the wait.
     if (!a.early_ok) kvd::pdl_wait();
-    if (tid == 0) kvd::pdl_trigger();   // the split-K merge may be scheduled
     const int32_t *c0 = a.p.cta_item0 + a.gx_dec + 1;
     const int32_t i0 = c0[blockIdx.x];
     const int32_t i1 = c0[blockIdx.x + 1];
@@ -210,6 +269,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     if (tid == 0) {
         kvd::prefetch_tmap(&tm_k);
         kvd::prefetch_tmap(&tm_v);
+        kvd::prefetch_tmap(&tm_part);
         for (int s = 0; s < KSTAGES; ++s) {
             kvd::mbar_init(&x.k_full[s], 1);
             kvd::mbar_init(&x.k_empty[s], 1);
@@ -219,16 +279,16 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             kvd::mbar_init(&x.v_empty[s], 1);
         }
         for (int s = 0; s < MSLOTS; ++s) kvd::mbar_init(&x.meta_full[s], 32);
-        kvd::mbar_init(&x.s_full[0], 1);
-        kvd::mbar_init(&x.s_full[1], 1);
-        kvd::mbar_init(&x.p_full[0], NSM);
-        kvd::mbar_init(&x.p_full[1], NSM);
-        kvd::mbar_init(&x.pv_done[0], 1);
-        kvd::mbar_init(&x.pv_done[1], 1);
-        kvd::mbar_init(&x.q_full, NSM);
+        for (int t = 0; t < 2; ++t) {
+            kvd::mbar_init(&x.s_full[t], 1);
+            kvd::mbar_init(&x.p_full[t], M);
+            kvd::mbar_init(&x.pv_done[t], 1);
+            kvd::mbar_init(&x.q_full[t], M);
+        }
+        kvd::mbar_init(&x.wbar, NSM);
+        kvd::mbar_init(&x.gbar, 1);
+        kvd::mbar_init(&x.mbar, 1);
         kvd::mbar_init(&x.spare, 1);
-        kvd::mbar_init(&x.lbar, NSM);
-        for (int q = 0; q < 4; ++q) kvd::mbar_init(&x.pbar[q], 128);
         x.fail = 0;
         kvd::fence_mbar_init();
     }
@@ -240,36 +300,34 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = x.tmem_base;
-
+    if (warp >= 8) {
+    // register split, one instruction per warpgroup: warps 8-11 give registers back
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PR_REGS));
     if (warp == W_K) {
         // ===================== K producer (whole warp) =====================
-        // K of pair g + KSTAGES loads as soon as S of pair g has read K of g.  Each
-        // pair's list entries, flags and per-cell visibility are fetched while the K
-        // slot is still busy and published through meta_full before the K copy is
-        // issued.  V has its own warp: these dependent global reads never hold up a
-        // V copy.
-        const int32_t lane = tid & 31;
-        // (no pass over the items first: the first K copy waits on as few dependent
-        // global reads as possible -- work item, tile list, flags)
+        // K of step g + KSTAGES loads as soon as S_A and S_B of step g have read K
+        // of g.  Each step's list entries, flags and per-cell visibility are
+        // fetched while the K slot is still busy and published through meta_full
+        // before the K copy is issued.
         int32_t kc = 0;
-        int32_t kwi = i0, kj = 0;              // K cursor: item and pair within it
+        int32_t kwi = i0, kj = 0;              // K cursor: item and step within it
         ItemInfo kit{};
-        int32_t kit_wi = -1;                   // the item kit describes
+        int32_t kit_wi = -1;
         kvi::DevBlock kb{};
         bool have_k = false;
         int32_t tt[2] = {-1, -1};
         bool full = false;
-        bool mhas[4] = {false, false, false, false}, many[4] = {false, false, false, false};
+        uint32_t mhas = 0, many = 0;           // bit r: cell lane + 32 r
         int32_t mpos[4] = {0, 0, 0, 0};
         long long t_last = clock64();
-        // The first pair's K goes out as soon as the previous kernel has finished, from
+        // The first step's K goes out as soon as the previous kernel has finished, from
         // the planner's per-column record (one read, done before the wait); its
         // metadata follows through the loop below, which skips that one copy.
         bool first_out = false;
         {
             const int4 ff = *reinterpret_cast<const int4 *>(a.p.pf_first + 4 * blockIdx.x);
             if (ff.x >= 0) {
-                if (lane < 8) {   // warm L2 with the pair's K and V (a prefetch returns nothing)
+                if (lane < 8) {   // warm L2 with the step's K and V (a prefetch returns nothing)
                     const CUtensorMap *tm = lane < 4 ? &tm_k : &tm_v;
                     const int32_t y = (lane >> 1) & 1 ? ff.y : ff.x;
                     if (y >= 0) kvd::tma_prefetch_2d(tm, hk * 128 + 64 * (lane & 1), y);
@@ -291,104 +349,106 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         while (true) {
             if (!warp_ok(fail)) break;
             bool prog = false;
-            {
-                if (!have_k) {
-                    // the next K load's global reads, done before its slot is free
-                    while (kwi < i1) {
-                        if (kit_wi != kwi) {
-                            kit = item_info(a, kwi);
-                            kit_wi = kwi;
-                        }
-                        if (kj < kit.pairs) break;
-                        ++kwi;
-                        kj = 0;
+            if (!have_k) {
+                // the next K load's global reads, done before its slot is free
+                while (kwi < i1) {
+                    if (kit_wi != kwi) {
+                        kit = item_info(a, kwi);
+                        kit_wi = kwi;
                     }
-                    if (kwi >= i1) break;      // every pair of every item is loaded
-                    kb = a.u.blocks[kit.block];
-                    const int32_t *list = a.p.tiles + (int64_t)kit.block * a.p.tile_stride;
-                    const uint32_t *flg = a.p.flags + (int64_t)kit.block * a.p.tile_stride;
-                    bool fullh[2];
-                    for (int h = 0; h < 2; ++h) {
-                        const int32_t e = kit.t0 + 2 * kj + h;
-                        tt[h] = e < kit.t1 ? list[e] : -1;
-                        fullh[h] = tt[h] >= 0 && (int32_t)(flg[tt[h]] & 0xffffu) == kb.n_rows * TILE;
-                    }
-                    full = fullh[0] && fullh[1];
-                    if (!full) {
+                    if (kj < kit.steps) break;
+                    ++kwi;
+                    kj = 0;
+                }
+                if (kwi >= i1) break;      // every step of every item is loaded
+                kb = a.u.blocks[kit.block];
+                const int32_t *list = a.p.tiles + (int64_t)kit.block * a.p.tile_stride;
+                const uint32_t *flg = a.p.flags + (int64_t)kit.block * a.p.tile_stride;
+                bool fullh[2];
+                for (int h = 0; h < 2; ++h) {
+                    const int32_t e = kit.t0 + 2 * kj + h;
+                    tt[h] = e < kit.t1 ? list[e] : -1;
+                    fullh[h] = tt[h] >= 0 && (int32_t)(flg[tt[h]] & 0xffffu) == kb.n_rows * TILE;
+                }
+                full = fullh[0] && fullh[1];
+                mhas = many = 0;
+                if (!full) {
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            const int32_t c = lane + 32 * r;
-                            const int32_t t = tt[c >> 6];
-                            bool has = false;
-                            int32_t cp = 0;
-                            if (t >= 0) {
-                                const int32_t jc = t * TILE + (c & 63);
-                                if (jc < a.u.n_kv) {
-                                    const int64_t g = (int64_t)kb.stream * a.u.kv_size + jc;
-                                    const uint64_t w = a.u.cell_bits[g * a.u.n_words + (kb.seq0 >> 6)];
-                                    has = ((w >> (kb.seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
-                                    cp = a.u.cell_pos[g];
-                                }
+                    for (int r = 0; r < 4; ++r) {
+                        const int32_t c = lane + 32 * r;
+                        const int32_t t = tt[c >> 6];
+                        bool has = false;
+                        int32_t cp = 0;
+                        if (t >= 0) {
+                            const int32_t jc = t * TILE + (c & 63);
+                            if (jc < a.u.n_kv) {
+                                const int64_t g = (int64_t)kb.stream * a.u.kv_size + jc;
+                                const uint64_t w = a.u.cell_bits[g * a.u.n_words + (kb.seq0 >> 6)];
+                                has = ((w >> (kb.seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
+                                cp = a.u.cell_pos[g];
                             }
-                            mhas[r] = has;
-                            mpos[r] = cp;
-                            // some row of the block (positions pos_min .. pos_max) may see it
-                            many[r] = has && (!a.u.causal || cp <= kb.pos_max) &&
-                                      (a.u.n_swa <= 0 || (int64_t)kb.pos_min - cp < a.u.n_swa);
                         }
+                        mpos[r] = cp;
+                        // some row of the block (positions pos_min .. pos_max) may see it
+                        const bool any = has && (!a.u.causal || cp <= kb.pos_max) &&
+                                         (a.u.n_swa <= 0 || (int64_t)kb.pos_min - cp < a.u.n_swa);
+                        mhas |= (has ? 1u : 0u) << r;
+                        many |= (any ? 1u : 0u) << r;
                     }
-                    have_k = true;
                 }
-                const int32_t st = kc % KSTAGES;
-                bool ready = kc < KSTAGES ||
-                             kvd::mbar_test_wait(&x.k_empty[st], (uint32_t)((kc / KSTAGES) - 1) & 1u);
-                ready = __shfl_sync(0xffffffffu, ready, 0);
-                if (ready) {
-                    Meta &mt = x.meta[kc % MSLOTS];
-                    if (lane == 0) {
-                        for (int h = 0; h < 2; ++h)   // a missing second tile: out of bounds, TMA writes zeros
-                            mt.ys[h] = tt[h] >= 0 ? kb.stream * a.u.kv_size + tt[h] * TILE : -TILE;
-                        mt.full = full ? 1 : 0;
-                    }
-                    if (!full) {
+                have_k = true;
+            }
+            const int32_t st = kc % KSTAGES;
+            bool ready = kc < KSTAGES ||
+                         kvd::mbar_test_wait(&x.k_empty[st], (uint32_t)((kc / KSTAGES) - 1) & 1u);
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            if (ready) {
+                Meta &mt = x.meta[kc % MSLOTS];
+                if (lane == 0) {
+                    for (int h = 0; h < 2; ++h)   // a missing second tile: out of bounds, TMA writes zeros
+                        mt.ys[h] = tt[h] >= 0 ? kb.stream * a.u.kv_size + tt[h] * TILE : -TILE;
+                    mt.full = full ? 1 : 0;
+                }
+                if (!full) {
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            const int32_t c = lane + 32 * r;
-                            mt.has[c] = mhas[r] ? 1 : 0;
-                            mt.cpos[c] = mpos[r];
-                            mt.anyvis[c] = many[r] ? 1 : 0;
+                    for (int r = 0; r < 4; ++r) {
+                        mt.cpos[lane + 32 * r] = mpos[r];
+                        const uint32_t hb = __ballot_sync(0xffffffffu, (mhas >> r) & 1u);
+                        const uint32_t ab = __ballot_sync(0xffffffffu, (many >> r) & 1u);
+                        if (lane == 0) {
+                            mt.has[r] = hb;
+                            mt.anyvis[r] = ab;
                         }
                     }
-                    __syncwarp();
-                    // the metadata goes out before the K copy is issued
-                    kvd::mbar_arrive(&x.meta_full[kc % MSLOTS]);
-                    if (kc == 0 && !first_out) {
-                        // Warm L2 with the first pair's K and V while the previous kernel
-                        // (normally the store of this ubatch's rows) finishes: a prefetch
-                        // returns nothing, so racing that kernel's writes is harmless.
-                        if (lane < 8) {
-                            const CUtensorMap *tm = lane < 4 ? &tm_k : &tm_v;
-                            const int32_t y = mt.ys[(lane >> 1) & 1];
-                            if (y >= 0) kvd::tma_prefetch_2d(tm, hk * 128 + 64 * (lane & 1), y);
-                        }
-                        kvd::pdl_wait();   // the K/V cache rows of this ubatch are written
-                    }
-                    if (lane == 0 && !(kc == 0 && first_out)) {
-                        uint8_t *ks = smem + OFF_K + st * TILEB;
-                        const int32_t xk = hk * 128;
-                        const int32_t y0 = mt.ys[0], y1 = mt.ys[1];
-                        kvd::fence_proxy_async_smem();
-                        kvd::mbar_arrive_expect_tx(&x.k_full[st], TILEB);
-                        kvd::tma_load_2d(ks, &tm_k, xk, y0, &x.k_full[st]);
-                        kvd::tma_load_2d(ks + HALF, &tm_k, xk + 64, y0, &x.k_full[st]);
-                        kvd::tma_load_2d(ks + BOX, &tm_k, xk, y1, &x.k_full[st]);
-                        kvd::tma_load_2d(ks + HALF + BOX, &tm_k, xk + 64, y1, &x.k_full[st]);
-                    }
-                    ++kc;
-                    ++kj;
-                    have_k = false;
-                    prog = true;
                 }
+                __syncwarp();
+                // the metadata goes out before the K copy is issued
+                kvd::mbar_arrive(&x.meta_full[kc % MSLOTS]);
+                if (kc == 0 && !first_out) {
+                    // Warm L2 with the first step's K and V while the previous kernel
+                    // (normally the store of this ubatch's rows) finishes.
+                    if (lane < 8) {
+                        const CUtensorMap *tm = lane < 4 ? &tm_k : &tm_v;
+                        const int32_t y = mt.ys[(lane >> 1) & 1];
+                        if (y >= 0) kvd::tma_prefetch_2d(tm, hk * 128 + 64 * (lane & 1), y);
+                    }
+                    kvd::pdl_wait();   // the K/V cache rows of this ubatch are written
+                }
+                if (lane == 0 && !(kc == 0 && first_out)) {
+                    uint8_t *ks = smem + OFF_K + st * TILEB;
+                    const int32_t xk = hk * 128;
+                    const int32_t y0 = mt.ys[0], y1 = mt.ys[1];
+                    kvd::fence_proxy_async_smem();
+                    kvd::mbar_arrive_expect_tx(&x.k_full[st], TILEB);
+                    kvd::tma_load_2d(ks, &tm_k, xk, y0, &x.k_full[st]);
+                    kvd::tma_load_2d(ks + HALF, &tm_k, xk + 64, y0, &x.k_full[st]);
+                    kvd::tma_load_2d(ks + BOX, &tm_k, xk, y1, &x.k_full[st]);
+                    kvd::tma_load_2d(ks + HALF + BOX, &tm_k, xk + 64, y1, &x.k_full[st]);
+                }
+                ++kc;
+                ++kj;
+                have_k = false;
+                prog = true;
             }
             if (prog) {
                 t_last = clock64();
@@ -406,11 +466,10 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         }
     } else if (warp == W_V) {
         // ===================== V producer (whole warp) =====================
-        // V of pair g + 3 loads as soon as PV of g is done; the tile coordinates come
-        // from the pair's metadata, published by the K producer before its K copy.
-        const int32_t lane = tid & 31;
+        // V of step g + VSTAGES loads as soon as PV_A and PV_B of g are done; the
+        // tile coordinates come from the step's metadata.
         int32_t total = 0;
-        for (int32_t wi = i0; wi < i1; ++wi) total += item_info(a, wi).pairs;
+        for (int32_t wi = i0; wi < i1; ++wi) total += item_info(a, wi).steps;
         int32_t vc = 0;
         for (; vc < total; ++vc) {
             const int32_t st = vc % VSTAGES;
@@ -421,7 +480,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             if (!ok) break;
             if (vc == 0) kvd::pdl_wait();   // the K/V cache rows of this ubatch are written
             if (lane == 0) {
-                const Meta &mt = x.meta[vc % MSLOTS];   // still intact (see MSLOTS)
+                const Meta &mt = x.meta[vc % MSLOTS];
                 uint8_t *vs = smem + OFF_V + st * TILEB;
                 const int32_t xk = hk * 128;
                 kvd::fence_proxy_async_smem();
@@ -439,318 +498,525 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         }
     } else if (warp == W_MMA) {
         // ===================== MMA issuer =====================
-        // The tensor core's work per item is a fixed sequence: S_0, S_1, then for
-        // each pair j: PV_j, S_j+2 (S_j+2 goes to the score buffer of pair j, whose P
-        // PV_j reads first: one thread's MMAs run in issue order).  Every step waits
-        // on its mbarrier with a blocking (suspending, bounded) wait, so the thread
-        // wakes as soon as a P or a K tile is ready.
-        if ((tid & 31) == 0) {
-            int32_t gidx = 0;                  // global pair-tile counter (stage rings)
-            uint32_t n_q = 0;
+        // Per item: S_A(0), S_B(0), then per step j: PV_A(j), S_A(j+1), PV_B(j),
+        // S_B(j+1).  S_t(j+1) overwrites the score buffer whose P the PV_t(j) just
+        // issued reads: one thread's MMAs run in issue order.  Tile B takes part
+        // only when the block has more than 128 query vectors.
+        if (lane == 0) {
+            int32_t g = 0;                     // steps issued (K / V / metadata rings)
+            uint32_t n_t[2] = {0, 0};          // steps per tile (s_full / p_full / pv_done phases)
+            uint32_t n_q[2] = {0, 0};          // items per tile (q_full phases)
             bool ok = true;
-            auto issue_s = [&](int32_t gi, int32_t buf) -> bool {
-                if (!wait_or_fail(&x.k_full[gi % KSTAGES], (uint32_t)(gi / KSTAGES) & 1u, fail)) return false;
-                tc::fence_after();
-                const uint32_t k_addr = sbase + OFF_K + (gi % KSTAGES) * TILEB;
-                const uint32_t d = tmem + (uint32_t)buf * 128u;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * HALF + (uint32_t)(kk & 3) * 32u;
-                    tc::mma_ts(d, tmem + COL_Q + 8u * (uint32_t)kk, tc::sdesc_sw128(k_addr + off, 16, 1024),
-                               IDESC_S, kk > 0 ? 1u : 0u);
-                }
-                tc::commit(&x.s_full[buf]);
-                tc::commit(&x.k_empty[gi % KSTAGES]);   // this K tile is consumed
-                return true;
-            };
+            // Shared-memory descriptors of every operand buffer, built once: the
+            // address field is (address >> 4) in the low 14 bits, and every buffer
+            // of this CTA lies below 256 KiB, so an offset inside a buffer is added
+            // to the descriptor directly.
+            const uint64_t dq = tc::sdesc_sw128(sbase + OFF_Q, 16, 1024);          // + t * TILEB
+            const uint64_t dk = tc::sdesc_sw128(sbase + OFF_K, 16, 1024);          // + stage * TILEB
+            const uint64_t dv = tc::sdesc_sw128(sbase + OFF_V, HALF, 1024);        // + stage * TILEB
             for (int32_t wi = i0; wi < i1 && ok; ++wi) {
                 const ItemInfo it = item_info(a, wi);
-                if (it.pairs == 0) continue;
-                if (!(ok = wait_or_fail(&x.q_full, n_q & 1u, fail))) break;
-                ++n_q;
-                tc::fence_after();
-                ok = issue_s(gidx, 0);
-                if (ok && it.pairs > 1) ok = issue_s(gidx + 1, 1);
-                for (int32_t j = 0; j < it.pairs && ok; ++j) {
-                    // P of pair gp is signalled on p_full[gp & 1]
-                    const int32_t gp = gidx + j;
-                    if (!(ok = wait_or_fail(&x.p_full[gp & 1], (uint32_t)(gp >> 1) & 1u, fail))) break;
-                    if (!(ok = wait_or_fail(&x.v_full[gp % VSTAGES], (uint32_t)(gp / VSTAGES) & 1u, fail))) break;
-                    tc::fence_after();
-                    const uint32_t v_addr = sbase + OFF_V + (gp % VSTAGES) * TILEB;
-                    const uint32_t p_tmem = tmem + 128u * (uint32_t)(j & 1);
-                    // O += P V over the 128 cells: P of cells 16kk .. 16kk + 15 is 8 TMEM
-                    // columns at 32 (kk / 2) + 8 (kk % 2) of the score buffer (each softmax
-                    // thread writes its 32 cells' P at the start of its own 32 S columns)
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        tc::mma_ts(tmem + COL_O, p_tmem + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1),
-                                   tc::sdesc_sw128(v_addr + (uint32_t)kk * 2048u, HALF, 1024), IDESC_PV,
-                                   (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc::commit(&x.pv_done[gp & 1]);
-                    tc::commit(&x.v_empty[gp % VSTAGES]);
-                    if (j + 2 < it.pairs) ok = issue_s(gidx + j + 2, j & 1);
+                if (it.steps == 0) continue;
+                const bool two = a.u.blocks[it.block].n_rows * G > M;
+                if (!(ok = wait_or_fail(&x.q_full[0], n_q[0] & 1u, fail))) break;
+                ++n_q[0];
+                if (two) {
+                    if (!(ok = wait_or_fail(&x.q_full[1], n_q[1] & 1u, fail))) break;
+                    ++n_q[1];
                 }
-                gidx += it.pairs;
+                if (!(ok = wait_or_fail(&x.k_full[g % KSTAGES], (uint32_t)(g / KSTAGES) & 1u, fail))) break;
+                tc::fence_after();
+                {
+                    const uint64_t kb0 = dk + (uint64_t)(((g % KSTAGES) * TILEB) >> 4);
+                    issue_s8(tmem + COL_S, dq, kb0);
+                    tc::commit(&x.s_full[0]);
+                    if (two) {
+                        issue_s8(tmem + COL_S + 128u, dq + (uint64_t)(TILEB >> 4), kb0);
+                        tc::commit(&x.s_full[1]);
+                    }
+                }
+                tc::commit(&x.k_empty[g % KSTAGES]);
+                for (int32_t j = 0; j < it.steps && ok; ++j) {
+                    const int32_t gs = g + j;
+                    const bool more = j + 1 < it.steps;
+                    if (!(ok = wait_or_fail(&x.p_full[0], (n_t[0] + (uint32_t)j) & 1u, fail))) break;
+                    if (!(ok = wait_or_fail(&x.v_full[gs % VSTAGES], (uint32_t)(gs / VSTAGES) & 1u, fail))) break;
+                    tc::fence_after();
+                    const uint64_t vb0 = dv + (uint64_t)(((gs % VSTAGES) * TILEB) >> 4);
+                    const uint64_t kb1 = dk + (uint64_t)((((gs + 1) % KSTAGES) * TILEB) >> 4);
+                    const uint32_t acc = j > 0 ? 1u : 0u;
+                    issue_pv8(tmem + COL_O, tmem + COL_S, vb0, acc);
+                    tc::commit(&x.pv_done[0]);
+                    if (more) {
+                        if (!(ok = wait_or_fail(&x.k_full[(gs + 1) % KSTAGES], (uint32_t)((gs + 1) / KSTAGES) & 1u,
+                                                fail)))
+                            break;
+                        tc::fence_after();
+                        issue_s8(tmem + COL_S, dq, kb1);
+                        tc::commit(&x.s_full[0]);
+                    }
+                    if (two) {
+                        if (!(ok = wait_or_fail(&x.p_full[1], (n_t[1] + (uint32_t)j) & 1u, fail))) break;
+                        tc::fence_after();
+                        issue_pv8(tmem + COL_O + 128u, tmem + COL_S + 128u, vb0, acc);
+                        tc::commit(&x.pv_done[1]);
+                        if (more) {
+                            issue_s8(tmem + COL_S + 128u, dq + (uint64_t)(TILEB >> 4), kb1);
+                            tc::commit(&x.s_full[1]);
+                        }
+                    }
+                    tc::commit(&x.v_empty[gs % VSTAGES]);
+                    if (more) tc::commit(&x.k_empty[(gs + 1) % KSTAGES]);
+                }
+                n_t[0] += (uint32_t)it.steps;
+                if (two) n_t[1] += (uint32_t)it.steps;
+                g += it.steps;
             }
             // all issued MMAs complete before TMEM is released
             tc::commit(&x.spare);
             (void)kvd::mbar_wait_bounded(&x.spare, 0);
         }
+    }
     } else {
-        // ============ softmax / correction / epilogue (warps 0-15, four threads per row) ============
-        // Warps w, w + 4, w + 8 and w + 12 share TMEM lane quarter w: thread (n, qd) owns
-        // cells 32qd .. 32qd + 31 of every pair tile of row n and d = 32qd .. 32qd + 31
-        // of O.  The four threads of a row exchange their maxima once per pair through
-        // an mbarrier of their four warps (arrive, then a bounded wait, never bar.sync:
-        // if a wait elsewhere gives up, the partners time out instead of hanging).
-        const int32_t n = tid & 127;           // TMEM lane = query vector
-        const int32_t qd = tid >> 7;           // cell quarter, and d quarter of O
+        // register split: the two softmax warpgroups take more registers
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SM_REGS));
+        // ============ softmax / epilogue / merge: warps 0-3 tile A, 4-7 tile B ============
+        // Thread n of tile t owns TMEM lane n: query vector 128 t + n of the block.
+        const int32_t t = warp >> 2;
+        const int32_t n = tid & 127;
+        const int32_t qv = M * t + n;
         const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t s_mine = tmem + lane_q + (uint32_t)(32 * qd);   // + 128 * score buffer
-        const uint32_t o_mine = tmem + lane_q + COL_O + (uint32_t)(32 * qd);
-        uint64_t *pbar = &x.pbar[warp & 3];
-        uint32_t n_s0 = 0, n_s1 = 0;           // score-buffer phases (scalars: no local memory)
-        uint32_t n_l = 0, n_p = 0;
-        int32_t k = 0;                         // pair tiles consumed (stage ring position)
+        const uint32_t s_mine = tmem + lane_q + COL_S + 128u * (uint32_t)t;
+        const uint32_t o_mine = tmem + lane_q + COL_O + 128u * (uint32_t)t;
+        uint8_t *q_sm = smem + OFF_Q + t * TILEB;
+        const int32_t n_all = a.p.n_work[1];
+        int32_t g = 0;                         // steps consumed (rings)
+        uint32_t n_s = 0;                      // steps of this tile (s_full / p_full / pv_done phases)
+        uint32_t n_w = 0;                      // wbar phases
         bool ok = true;
-        bool dep_done = false;                 // waited for the previous kernel of the stream
+        bool dep_done = false;
         for (int32_t wi = i0; wi < i1 && ok && warp_ok(fail); ++wi) {
             const ItemInfo it = item_info(a, wi);
-            const int32_t nitems = a.p.blk_nitems[it.block];   // used at the item's end
-            // the query vector behind my TMEM lane (an empty item has a block that sees
-            // no cell: zeros, or an empty partial), fetched here rather than from the
-            // producer so that Q starts loading as early as possible
-            int32_t row = -1, rpos = 0;
-            if (wi == i0) {
-                row = a.p.pf_rows[blockIdx.x * M + n];   // written by the planner
+            const kvi::DevBlock b = a.u.blocks[it.block];
+            const int32_t nq = b.n_rows * G;
+            const int32_t nitems = a.p.blk_nitems[it.block];
+            if (t == 0 || nq > M) {
+                // ---------------- this tile has query vectors in the block ----------------
+                int32_t row = -1, rpos = 0;
+                if (qv < nq) {
+                    row = wi == i0 ? a.p.pf_rows[blockIdx.x * PF_M + qv] : a.u.perm[b.row0 + qv / G];
+                    rpos = a.u.rows[row].pos;
+                }
+                const bool live = row >= 0;
+                const int32_t h = hk * G + (qv % G);
+                if (!dep_done) {   // before the first read of Q and the first write of an output
+                    if (live && it.steps > 0) {
+                        const __half *qp = a.q + ((int64_t)row * a.n_head + h) * 128;
+                        kvd::prefetch_l2(qp);
+                        kvd::prefetch_l2(qp + 64);
+                    }
+                    kvd::pdl_wait();
+                    dep_done = true;
+                }
+                float m_run = -INFINITY, l_run = 0.f;
+                if (it.steps > 0) {
+                    // ---- Q of the warp's 32 query vectors -> shared memory (the A operand
+                    //      of S = Q K^T), 128-byte swizzle.  Each load instruction covers
+                    //      two whole rows (16 lanes x 16 bytes each), so the reads are
+                    //      coalesced; lane j's row comes from the lane that owns it ----
+                    {
+                        const int32_t wrow = 32 * (warp & 3);
+                        uint4 v[16];
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const int32_t jr = 2 * k + (lane >> 4);      // row of the warp
+                            const int32_t rj = __shfl_sync(0xffffffffu, row, jr);
+                            const int32_t hj = hk * G + ((M * t + wrow + jr) % G);
+                            v[k] = rj >= 0 ? __ldg(reinterpret_cast<const uint4 *>(a.q + ((int64_t)rj * a.n_head + hj) * 128) +
+                                                   (lane & 15))
+                                           : make_uint4(0, 0, 0, 0);
+                        }
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const uint32_t rr = (uint32_t)(wrow + 2 * k + (lane >> 4));
+                            const uint32_t c = (uint32_t)(lane & 15);
+                            *reinterpret_cast<uint4 *>(q_sm + (c >> 3) * HALF + kvd::swz128(rr, c & 7u)) = v[k];
+                        }
+                        kvd::fence_proxy_async_smem();
+                        kvd::mbar_arrive(&x.q_full[t]);
+                    }
+                    for (int32_t j = 0; j < it.steps; ++j, ++g, ++n_s) {
+                        ok = __all_sync(0xffffffffu,
+                                        wait_or_fail(&x.meta_full[g % MSLOTS], (uint32_t)(g / MSLOTS) & 1u, fail));
+                        if (!ok) break;
+                        const Meta &mt = x.meta[g % MSLOTS];
+                        const bool full = mt.full != 0;
+                        // the cells this row sees (sequence, epoch, causal order, window), as
+                        // 128 bits, worked out while S is still being computed
+                        uint32_t vm[4] = {~0u, ~0u, ~0u, ~0u};
+                        if (!live) {
+                            vm[0] = vm[1] = vm[2] = vm[3] = 0u;
+                        } else if (!full) {
+                            const kvd::PosRange rr = kvd::pos_range(a.u.causal, a.u.n_swa, rpos);
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                const int4 *cs = reinterpret_cast<const int4 *>(&mt.cpos[32 * r]);
+                                uint32_t pb = 0;
+#pragma unroll
+                                for (int q4 = 0; q4 < 8; ++q4) {
+                                    const int4 cp = cs[q4];
+                                    pb |= (kvd::pos_in(rr, cp.x) ? 1u : 0u) << (4 * q4 + 0);
+                                    pb |= (kvd::pos_in(rr, cp.y) ? 1u : 0u) << (4 * q4 + 1);
+                                    pb |= (kvd::pos_in(rr, cp.z) ? 1u : 0u) << (4 * q4 + 2);
+                                    pb |= (kvd::pos_in(rr, cp.w) ? 1u : 0u) << (4 * q4 + 3);
+                                }
+                                vm[r] = pb & mt.has[r];
+                            }
+                        }
+                        ok = __all_sync(0xffffffffu, wait_or_fail(&x.s_full[t], n_s & 1u, fail));
+                        if (!ok) break;
+                        tc::fence_after();
+                        uint32_t sb[128];
+                        tc::ld128(s_mine, sb);
+                        if (!live || !full) {
+#pragma unroll
+                            for (int c = 0; c < 128; ++c)
+                                sb[c] = ((vm[c >> 5] >> (c & 31)) & 1u) ? sb[c] : __float_as_uint(-INFINITY);
+                        }
+                        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                        for (int c = 0; c < 128; c += 2)
+                            mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(sb[c]), __uint_as_float(sb[c + 1]));
+                        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+                        const float m_new = fmaxf(m_run, tmax);
+                        const bool grow = m_new > m_run + RESCALE_LOG2 || (m_run == -INFINITY && m_new != -INFINITY);
+                        float alpha = 1.f;
+                        if (grow) {
+                            alpha = ex2_approx(m_run - m_new);
+                            m_run = m_new;
+                            l_run *= alpha;
+                        }
+                        // ---- O *= alpha where the row's running maximum moved (rare): O is
+                        //      stable once PV of the previous step finished ----
+                        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                            ok = __all_sync(0xffffffffu, wait_or_fail(&x.pv_done[t], (n_s - 1) & 1u, fail));
+                            if (!ok) break;
+                            tc::fence_after();
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint32_t r[32];
+                                tc::ld32(o_mine + 32u * (uint32_t)q, r);
+#pragma unroll
+                                for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+                                tc::st32(o_mine + 32u * (uint32_t)q, r);
+                            }
+                        }
+                        // ---- P = 2^(s*scale - m) as fp16 pairs over the first 64 S columns
+                        //      (cell c in column c / 2); the row sum adds those same fp16
+                        //      values in fp32 ----
+                        {
+                            // no maximum yet (nothing visible so far, or a lane past the block):
+                            // subtract +inf so that every exponent is -inf and P is 0
+                            const float nm = m_run != -INFINITY ? -m_run : -INFINITY;
+                            const uint64_t sc2 = pk2(a.scale_log2, a.scale_log2), nm2 = pk2(nm, nm);
+                            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh) {
+                                uint32_t pw[32];
+#pragma unroll
+                                for (int c2 = 0; c2 < 32; ++c2) {
+                                    const int c = 64 * hh + 2 * c2;
+                                    float x0, x1;
+                                    upk2(ffma2(pk2(__uint_as_float(sb[c]), __uint_as_float(sb[c + 1])), sc2, nm2), x0,
+                                         x1);
+                                    const uint32_t p2 = ex2_h2(x0, x1);
+                                    pw[c2] = p2;
+                                    sum_h2(p2, ls[(c2 & 1) * 2], ls[(c2 & 1) * 2 + 1]);
+                                }
+                                tc::st32(s_mine + 32u * (uint32_t)hh, pw);
+                            }
+                            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                        }
+                        bool zeroed = false;
+                        if (t == 0 && !full) {
+                            // V rows of cells nobody in the block sees: zero (P is 0 there; V may
+                            // be garbage); thread n clears cell n's row in both d halves
+                            ok = __all_sync(0xffffffffu,
+                                            wait_or_fail(&x.v_full[g % VSTAGES], (uint32_t)(g / VSTAGES) & 1u, fail));
+                            if (!ok) break;
+                            if (!((mt.anyvis[n >> 5] >> (n & 31)) & 1u)) {
+                                uint8_t *vs = smem + OFF_V + (g % VSTAGES) * TILEB + n * 128;
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) {
+                                    *reinterpret_cast<uint4 *>(vs + c * 16) = make_uint4(0, 0, 0, 0);
+                                    *reinterpret_cast<uint4 *>(vs + HALF + c * 16) = make_uint4(0, 0, 0, 0);
+                                }
+                            }
+                            zeroed = true;
+                        }
+                        tc::wait_st();                     // P (and a rescaled O) are in TMEM
+                        if (zeroed) kvd::fence_proxy_async_smem();   // zeroed V rows are visible to the MMA
+                        tc::fence_before();
+                        kvd::mbar_arrive(&x.p_full[t]);
+                    }
+                    if (!ok) break;
+                    // ---- wait for the item's last PV ----
+                    ok = __all_sync(0xffffffffu, wait_or_fail(&x.pv_done[t], (n_s - 1) & 1u, fail));
+                    if (!ok) break;
+                    tc::fence_after();
+                }
+                // ---- epilogue: the normalised row, or this piece's partial.  Each
+                //      32-column quarter of the warp's 32 rows is staged in the warp's own
+                //      4 KiB of the tile's Q area (free: the item's last S has completed,
+                //      and the next item's Q is written by these same threads after this),
+                //      128-byte swizzled.  A partial's rows are consecutive: one TMA store
+                //      per quarter writes them (the tensor map undoes the swizzle); an
+                //      output row goes out 8 lanes per 128-byte segment ----
+                const bool split = nitems > 1;
+                float *dst = nullptr;
+                float sc = 1.f;
+                const int64_t prow = ((int64_t)wi * a.n_head_kv + hk) * PF_M;   // this item's first partial row
+                if (!split) {
+                    if (live) dst = a.o + ((int64_t)row * a.n_head + h) * 128;
+                    sc = l_run > 0.f ? 1.f / l_run : 0.f;
+                } else {
+                    *reinterpret_cast<float2 *>(a.part_ml + (prow + qv) * 2) = make_float2(m_run, l_run);
+                }
+                uint8_t *stg = q_sm + 4096 * (warp & 3);
+                // the O row in two TMEM reads of 64 columns (warp collective; an item
+                // without a step reads stale columns and replaces them with zeros)
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                uint32_t ob[64];
+                tc::ld64(o_mine + 64u * (uint32_t)hh, ob);
+                if (it.steps == 0) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) ob[c] = 0u;
+                }
+#pragma unroll
+                for (int qh = 0; qh < 2; ++qh) {
+                    const int q = 2 * hh + qh;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<float4 *>(stg + kvd::swz128((uint32_t)lane, (uint32_t)c)) =
+                            make_float4(__uint_as_float(ob[32 * qh + 4 * c]) * sc, __uint_as_float(ob[32 * qh + 4 * c + 1]) * sc,
+                                        __uint_as_float(ob[32 * qh + 4 * c + 2]) * sc,
+                                        __uint_as_float(ob[32 * qh + 4 * c + 3]) * sc);
+                    if (split) {
+                        kvd::fence_proxy_async_smem();   // the staged rows are visible to the TMA store
+                        __syncwarp();
+                        if (lane == 0) {
+                            kvd::tma_store_2d(&tm_part, 32 * q, (int32_t)(prow + M * t + 32 * (warp & 3)), stg);
+                            kvd::bulk_commit();
+                            kvd::bulk_wait_read<0>();   // the staging area is read: reusable
+                        }
+                        __syncwarp();
+                    } else {
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int32_t jr = 4 * k + (lane >> 3);         // row of the warp
+                            const uint32_t c = (uint32_t)(lane & 7);
+                            float *dj = reinterpret_cast<float *>(
+                                __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(dst), jr));
+                            if (dj)
+                                *reinterpret_cast<float4 *>(dj + 32 * q + 4 * c) =
+                                    *reinterpret_cast<const float4 *>(stg + kvd::swz128((uint32_t)jr, c));
+                        }
+                        __syncwarp();
+                    }
+                }
+                }
+                if (split && lane == 0) {
+                    // the partial's rows are written before the piece is counted
+                    kvd::bulk_wait_all();
+                    kvd::fence_proxy_async_global();
+                }
+                tc::fence_before();
             } else {
-                const kvi::DevBlock b = a.u.blocks[it.block];
-                if (n < b.n_rows * G) row = a.u.perm[b.row0 + n / G];
+                g += it.steps;                     // tile B has no query vector in this block
             }
-            if (row >= 0) rpos = a.u.rows[row].pos;
-            const bool live = row >= 0;
-            const int32_t h = hk * G + (n % G);
-            if (!dep_done) {   // before the first read of Q and the first write of an output
-                // warm L2 with my 64 bytes of Q while the previous kernel finishes (a
-                // prefetch returns nothing, so racing its writes is harmless)
-                if (live && it.pairs > 0) kvd::prefetch_l2(a.q + ((int64_t)row * a.n_head + h) * 128 + 32 * qd);
+            if (nitems == 1) continue;
+            // ---------------- a piece of a split block ----------------
+            // All 256 softmax threads meet once the piece's rows are written (every
+            // thread waits, so none can arrive for a later phase early); thread 0
+            // then counts the piece.  The CTAs whose last item is a piece of this
+            // block wait until all pieces are counted and merge a share each.
+            if (!dep_done) {
                 kvd::pdl_wait();
                 dep_done = true;
             }
-            float m_run = -INFINITY, l_run = 0.f;   // the row's running maximum, this quarter's row sum
-            if (it.pairs > 0) {
-            // ---- Q into TMEM (the A operand of S = Q K^T): row n, d quarter qd, fp16,
-            //      two values per 32-bit column ----
-            {
-                const uint4 *src =
-                    reinterpret_cast<const uint4 *>(a.q + ((int64_t)(live ? row : 0) * a.n_head + h) * 128 + 32 * qd);
-                uint32_t qw[16];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint4 v = live ? src[c] : make_uint4(0, 0, 0, 0);
-                    qw[4 * c + 0] = v.x;
-                    qw[4 * c + 1] = v.y;
-                    qw[4 * c + 2] = v.z;
-                    qw[4 * c + 3] = v.w;
+            kvd::fence_proxy_async_smem();   // the staging writes come before any later bulk copy into it
+            kvd::mbar_arrive(&x.wbar);
+            ok = __all_sync(0xffffffffu, wait_or_fail(&x.wbar, n_w & 1u, fail));
+            ++n_w;
+            if (!ok) break;
+            const bool mine = wi + 1 == i1;
+            int32_t *cnt = a.p.counters + (int64_t)it.block * a.n_head_kv + hk;
+            const int32_t it0 = a.p.blk_item0[it.block] - a.p.cap_dec;
+            // The merge participants are the block's pieces that are the last item of
+            // their column, in item order: warp 0 finds them with one ballot per 32
+            // pieces (np of them, `rank` of them before mine).
+            int32_t np = 0, rank = 0;
+            if (warp == 0 && mine) {
+                for (int32_t k0 = it0; k0 < it0 + nitems; k0 += 32) {
+                    const int32_t k = k0 + lane;
+                    const bool part = k < it0 + nitems && last_of_column(a, k, n_all);
+                    const uint32_t bal = __ballot_sync(0xffffffffu, part);
+                    np += __popc(bal);
+                    rank += __popc(bal & __ballot_sync(0xffffffffu, k < wi));
                 }
-                tc::st16(tmem + lane_q + COL_Q + 16u * (uint32_t)qd, qw);
-                tc::wait_st();
-                tc::fence_before();
-                kvd::mbar_arrive(&x.q_full);
             }
-            for (int32_t j = 0; j < it.pairs; ++j, ++k) {
-                const int32_t st = k % VSTAGES;
-                ok = __all_sync(0xffffffffu, wait_or_fail(&x.meta_full[k % MSLOTS], (uint32_t)(k / MSLOTS) & 1u, fail));
-                if (!ok) break;
-                const Meta &mt = x.meta[k % MSLOTS];
-                const bool full = mt.full != 0;
-                const uint32_t ns = (j & 1) ? n_s1 : n_s0;
-                ok = __all_sync(0xffffffffu, wait_or_fail(&x.s_full[j & 1], ns & 1u, fail));
-                if (!ok) break;
-                if (j & 1) ++n_s1; else ++n_s0;
-                tc::fence_after();
-                // ---- my 32 columns of S -> registers (one TMEM read, warp collective);
-                //      masked -> -inf ----
-                const uint32_t s_addr = s_mine + (uint32_t)(j & 1) * 128u;
-                uint32_t sb[32];
-                tc::ld32(s_addr, sb);
-                if (!live) {
+            if (tid == 0) {
+                // count the piece: every thread's writes of it came before the barrier
+                // above, so one release by this thread publishes them all
+                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(cnt) : "memory");
+                if (mine) {
+                    // wait (bounded) until every piece of the block is counted
+                    long long t0c = clock64();
+                    while (ld_acquire(cnt) < nitems) {
+                        if (*fail || clock64() - t0c > kvd::WAIT_LIMIT_CYCLES) {
+                            *fail = 1;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    x.mrg_lo = (int32_t)((int64_t)nq * rank / np);
+                    x.mrg_hi = (int32_t)((int64_t)nq * (rank + 1) / np);
+                    kvd::mbar_arrive(&x.gbar);
+                }
+            }
+            if (!mine) continue;
+            ok = __all_sync(0xffffffffu, wait_or_fail(&x.gbar, 0, fail));
+            if (!ok || !warp_ok(fail)) break;
+            // ---- merge query vectors mrg_lo .. mrg_hi - 1:
+            //      O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
+            //      Each piece's O rows of my share are one contiguous range: one bulk
+            //      copy per piece brings them into shared memory (the Q area and the K/V
+            //      rings, idle now), their (m, l) come by plain loads; warp w merges
+            //      query vectors v0 + 32k + 4w + r (r = 0..3) together, lane l owning
+            //      d = 4l .. 4l + 3, writes each merged row over the first piece's copy of
+            //      it and sends it out as one bulk copy ----
+            {
+                const int64_t istride = (int64_t)a.n_head_kv * PF_M;          // partial rows per item
+                const int64_t prow0 = ((int64_t)it0 * a.n_head_kv + hk) * PF_M;
+                const int32_t lo = x.mrg_lo, hi = x.mrg_hi;
+                constexpr uint32_t ROWB = 128 * 4;                          // bytes of one O row
+                constexpr uint32_t MCAP = OFF_AUX;                          // shared bytes free for the merge
+                const int32_t rp = min(PF_M, (int32_t)(MCAP / ((uint32_t)nitems * (ROWB + 8))));   // rows per pass
+                if (rp < 1) {
+                    if (tid == 0) kvd::report(a.err, kvd::DERR_BOUNDS);
+                    break;
+                }
+                uint32_t n_m = 0;                                          // mbar phases
+                bool stored = false;                                       // this lane issued bulk stores
+                for (int32_t v0 = lo; v0 < hi; v0 += rp, ++n_m) {
+                    const int32_t R = min(rp, hi - v0);
+                    const uint32_t qstride = (uint32_t)R * ROWB;
+                    float2 *mls = reinterpret_cast<float2 *>(smem + (uint32_t)nitems * qstride);   // [piece][row]
+                    if (tid == 0) {
+                        kvd::fence_proxy_async_global();
+                        kvd::mbar_arrive_expect_tx(&x.mbar, (uint32_t)nitems * qstride);
+                        for (int32_t q = 0; q < nitems; ++q)
+                            kvd::bulk_load(smem + (uint32_t)q * qstride, a.part + (prow0 + q * istride + v0) * 128, qstride,
+                                           &x.mbar);
+                    }
+                    for (int32_t e = tid; e < nitems * R; e += NSM) {
+                        const int32_t q = e / R, r = e - q * R;
+                        mls[e] = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + prow0 + q * istride + v0 + r);
+                    }
+                    // warp w's output rows, one load per lane (lane 8k + r: query vector
+                    // v0 + 64k + 8w + r), before they are needed
+                    int32_t orow = -1;
+                    {
+                        const int32_t vl = v0 + 64 * (lane >> 3) + 8 * warp + (lane & 7);
+                        if (vl < v0 + R) orow = a.u.perm[b.row0 + vl / G];
+                    }
+                    kvd::mbar_arrive(&x.wbar);                             // (m, l) are in shared memory
+                    ok = __all_sync(0xffffffffu, wait_or_fail(&x.wbar, n_w & 1u, fail));
+                    ++n_w;
+                    if (!ok) break;
+                    // pass 1, a thread per query vector: the pieces' weights 2^(m_q - M) / L
+                    // replace their m in shared memory
+                    for (int32_t r = tid; r < R; r += NSM) {
+                        float Mx = -INFINITY;
+                        for (int32_t q = 0; q < nitems; ++q) Mx = fmaxf(Mx, mls[q * R + r].x);
+                        float L = 0.f;
+                        for (int32_t q = 0; q < nitems; ++q) {
+                            const float2 ml = mls[q * R + r];
+                            const float w = (ml.x == -INFINITY || Mx == -INFINITY) ? 0.f : ex2_approx(ml.x - Mx);
+                            L = fmaf(ml.y, w, L);
+                            mls[q * R + r].x = w;
+                        }
+                        const float inv = L > 0.f ? rcp_approx(L) : 0.f;
+                        for (int32_t q = 0; q < nitems; ++q) mls[q * R + r].x *= inv;
+                    }
+                    kvd::mbar_arrive(&x.wbar);                             // the weights are in place
+                    ok = __all_sync(0xffffffffu, wait_or_fail(&x.wbar, n_w & 1u, fail));
+                    ++n_w;
+                    if (ok) ok = __all_sync(0xffffffffu, wait_or_fail(&x.mbar, n_m & 1u, fail));   // the O rows landed
+                    if (!ok) break;
+                    // pass 2, a warp per 8 query vectors at once, lane l owning d = 4l .. 4l + 3
+                    for (int32_t k = 0; 64 * k + 8 * warp < R; ++k) {
+                        const int32_t rb = 64 * k + 8 * warp;          // first row of the batch (pass-relative)
+                        const int32_t nr = min(8, R - rb);
+                        float4 acc[8];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) sb[c] = __float_as_uint(-INFINITY);
-                } else if (!full) {
-                    // which of my 32 cells this row sees (16-byte loads, all issued before
-                    // any test), applied as a 32-bit mask
-                    uint4 hb[2];
-                    int4 cp[8];
-                    const uint4 *hs = reinterpret_cast<const uint4 *>(&mt.has[32 * qd]);
-                    const int4 *cs = reinterpret_cast<const int4 *>(&mt.cpos[32 * qd]);
+                        for (int r = 0; r < 8; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int32_t q = 0; q < nitems; ++q) {
+                            float w[8];
+                            float4 ov[8];
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) hb[q] = hs[q];
+                            for (int r = 0; r < 8; ++r) {
+                                w[r] = r < nr ? mls[q * R + rb + r].x : 0.f;
+                                ov[r] = r < nr ? *reinterpret_cast<const float4 *>(smem + (uint32_t)q * qstride +
+                                                                                   (uint32_t)(rb + r) * ROWB + 16 * lane)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) cp[q] = cs[q];
-                    // the positions this row sees (causal order, sliding window)
-                    const kvd::PosRange rr = kvd::pos_range(a.u.causal, a.u.n_swa, rpos);
-                    uint32_t vm = 0;
+                            for (int r = 0; r < 8; ++r) {
+                                acc[r].x = fmaf(ov[r].x, w[r], acc[r].x);
+                                acc[r].y = fmaf(ov[r].y, w[r], acc[r].y);
+                                acc[r].z = fmaf(ov[r].z, w[r], acc[r].z);
+                                acc[r].w = fmaf(ov[r].w, w[r], acc[r].w);
+                            }
+                        }
+                        // the merged rows over the first piece's copies (only this warp
+                        // reads those rows), then one bulk copy per row
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const uint32_t hw = (&hb[q >> 2].x)[q & 3];   // has of cells 4q .. 4q + 3
-                        const int32_t c4[4] = {cp[q].x, cp[q].y, cp[q].z, cp[q].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const bool vis = ((hw >> (8 * e)) & 0xffu) != 0 && kvd::pos_in(rr, c4[e]);
-                            vm |= (uint32_t)vis << (4 * q + e);
+                        for (int r = 0; r < 8; ++r)
+                            if (r < nr) *reinterpret_cast<float4 *>(smem + (uint32_t)(rb + r) * ROWB + 16 * lane) = acc[r];
+                        kvd::fence_proxy_async_smem();
+                        __syncwarp();
+                        const int32_t mrow = __shfl_sync(0xffffffffu, orow, 8 * k + (lane & 7));
+                        if (lane < nr) {
+                            const int32_t v = v0 + rb + lane;
+                            kvd::bulk_store(a.o + ((int64_t)mrow * a.n_head + hk * G + (v % G)) * 128,
+                                            smem + (uint32_t)(rb + lane) * ROWB, ROWB);
+                            kvd::bulk_commit();
+                            stored = true;
                         }
                     }
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        sb[c] = ((vm >> c) & 1u) ? sb[c] : __float_as_uint(-INFINITY);
+                    // every read of this pass (mine and my bulk copies') is done before the
+                    // next pass's copies land
+                    if (stored) kvd::bulk_wait_read<0>();
+                    kvd::fence_proxy_async_smem();
+                    kvd::mbar_arrive(&x.wbar);
+                    ok = __all_sync(0xffffffffu, wait_or_fail(&x.wbar, n_w & 1u, fail));
+                    ++n_w;
+                    if (!ok) break;
                 }
-                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                for (int c = 0; c < 32; c += 2)
-                    mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(sb[c]), __uint_as_float(sb[c + 1]));
-                // ---- the row maximum over the four quarters (partners: the same lane of
-                //      warps w, w + 4, w + 8, w + 12) ----
-                x.red[j & 1][qd][n] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                kvd::mbar_arrive(pbar);
-                ok = __all_sync(0xffffffffu, wait_or_fail(pbar, n_p & 1u, fail));
-                ++n_p;
+                if (stored) kvd::bulk_wait_all();
                 if (!ok) break;
-                const float tmax = fmaxf(fmaxf(x.red[j & 1][0][n], x.red[j & 1][1][n]),
-                                         fmaxf(x.red[j & 1][2][n], x.red[j & 1][3][n])) * a.scale_log2;
-                const float m_new = fmaxf(m_run, tmax);
-                const bool grow = m_new > m_run + RESCALE_LOG2 || (m_run == -INFINITY && m_new != -INFINITY);
-                float alpha = 1.f;
-                if (grow) {
-                    alpha = ex2_approx(m_run - m_new);
-                    m_run = m_new;
-                    l_run *= alpha;
-                }
-                // ---- P = 2^(s*scale - m) as fp16 at the start of my S columns: my 32 cells
-                //      are 16 columns (two fp16 per column, lower cell in the low half);
-                //      the exponent s*scale - m is rounded to fp16 and two of them are
-                //      raised at once (ex2.approx.f16x2), which yields P in the fp16 the PV
-                //      product reads; the row sum adds those same fp16 values in fp32 ----
-                {
-                    // no maximum yet (nothing visible so far, or a lane past the block):
-                    // subtract +inf so that every exponent is -inf and P is 0
-                    const float nm = m_run != -INFINITY ? -m_run : -INFINITY;
-                    const uint64_t sc2 = pk2(a.scale_log2, a.scale_log2), nm2 = pk2(nm, nm);
-                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
-                    uint32_t pw[16];
-#pragma unroll
-                    for (int c2 = 0; c2 < 16; ++c2) {
-                        const int c = 2 * c2;
-                        float x0, x1;
-                        upk2(ffma2(pk2(__uint_as_float(sb[c]), __uint_as_float(sb[c + 1])), sc2, nm2), x0, x1);
-                        const uint32_t p2 = ex2_h2(x0, x1);
-                        pw[c2] = p2;
-                        sum_h2(p2, ls[(c2 & 1) * 2], ls[(c2 & 1) * 2 + 1]);
-                    }
-                    l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                    tc::st16(s_addr, pw);
-                }
-                // ---- O *= alpha where the row's running maximum moved (rare), my 32
-                //      columns; O is stable once PV of pair k - 1 finished ----
-                if (j > 0 && __any_sync(0xffffffffu, grow)) {
-                    ok = __all_sync(0xffffffffu,
-                                    wait_or_fail(&x.pv_done[(k - 1) & 1], (uint32_t)((k - 1) >> 1) & 1u, fail));
-                    if (!ok) break;
-                    tc::fence_after();
-                    uint32_t r[32];
-                    tc::ld32(o_mine, r);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-                    tc::st32(o_mine, r);
-                }
-                if (!full && qd < 2) {
-                    // V rows of cells nobody in the block sees: zero (P is 0 there; V may
-                    // be garbage); thread (n, qd < 2) clears d half qd of cell n
-                    ok = __all_sync(0xffffffffu, wait_or_fail(&x.v_full[st], (uint32_t)(k / VSTAGES) & 1u, fail));
-                    if (!ok) break;
-                    if (!mt.anyvis[n]) {
-                        uint8_t *vs = smem + OFF_V + st * TILEB + qd * HALF + n * 128;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(vs + c * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                }
-                tc::wait_st();                     // P (and a rescaled O) are in TMEM
-                kvd::fence_proxy_async_smem();     // zeroed V rows are visible to the MMA
-                tc::fence_before();
-                kvd::mbar_arrive(&x.p_full[k & 1]);
             }
-            if (!ok) break;
-            // ---- wait for the item's last PV (pair k - 1) ----
-            ok = __all_sync(0xffffffffu,
-                            wait_or_fail(&x.pv_done[(k - 1) & 1], (uint32_t)((k - 1) >> 1) & 1u, fail));
-            if (!ok) break;
-            tc::fence_after();
-            }   // it.pairs > 0
-            // ---- the row sum over the four quarters (double-buffered by item parity) ----
-            x.lex[n_l & 1][qd][n] = l_run;
-            kvd::mbar_arrive(&x.lbar);
-            ok = __all_sync(0xffffffffu, wait_or_fail(&x.lbar, n_l & 1u, fail));
-            if (!ok) break;
-            const float l_tot = (x.lex[n_l & 1][0][n] + x.lex[n_l & 1][1][n]) +
-                                (x.lex[n_l & 1][2][n] + x.lex[n_l & 1][3][n]);
-            ++n_l;
-            float *dst = nullptr;
-            float sc = 1.f;
-            if (nitems == 1) {
-                if (live) dst = a.o + ((int64_t)row * a.n_head + h) * 128 + 32 * qd;
-                sc = l_tot > 0.f ? 1.f / l_tot : 0.f;
-            } else {
-                // a split block: this item's partial (its slot is its index among the
-                // prefill items); k_merge_pf combines the partials after the kernel
-                float *pp = a.part + (((int64_t)wi * a.n_head_kv + hk) * M + n) * PART_STRIDE;
-                if (qd == 0) {
-                    pp[0] = m_run;
-                    pp[1] = l_tot;
-                }
-                dst = pp + 4 + 32 * qd;
+            // done reading the partials: count again; the arrival that completes the
+            // count (every piece once, every participant once more) resets it for the
+            // next launch
+            kvd::mbar_arrive(&x.wbar);
+            if (tid == 0 && wait_or_fail(&x.wbar, n_w & 1u, fail)) {
+                if (atomicAdd(cnt, 1) == nitems + np - 1) atomicExch(cnt, 0);
             }
-            uint32_t r[32];
-            if (it.pairs > 0) {                  // item-uniform: the TMEM read stays warp collective
-                tc::ld32(o_mine, r);
-            } else {
-#pragma unroll
-                for (int c = 0; c < 32; ++c) r[c] = 0u;
-            }
-            if (wi + 1 == i1) {
-                // The CTA's last item: the K ring is idle (every S has completed), so each
-                // warp stages its 32 rows there and writes them out row by row, 8 lanes
-                // per 128-byte row, instead of one row per lane.
-                float *stg = reinterpret_cast<float *>(smem + OFF_K) + warp * (32 * STG_STRIDE);
-#pragma unroll
-                for (int c = 0; c < 32; c += 4)
-                    *reinterpret_cast<float4 *>(stg + (tid & 31) * STG_STRIDE + c) =
-                        make_float4(__uint_as_float(r[c + 0]) * sc, __uint_as_float(r[c + 1]) * sc,
-                                    __uint_as_float(r[c + 2]) * sc, __uint_as_float(r[c + 3]) * sc);
-                __syncwarp();
-                const int32_t lane = tid & 31, part = lane & 7;
-#pragma unroll 4
-                for (int i = 0; i < 8; ++i) {
-                    const int32_t rr = 4 * i + (lane >> 3);   // the warp's row (its lane)
-                    float *d = reinterpret_cast<float *>(
-                        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(dst), rr));
-                    if (d)
-                        *reinterpret_cast<float4 *>(d + 4 * part) =
-                            *reinterpret_cast<const float4 *>(stg + rr * STG_STRIDE + 4 * part);
-                }
-            } else if (dst) {
-#pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    float4 v;
-                    v.x = __uint_as_float(r[c + 0]) * sc;
-                    v.y = __uint_as_float(r[c + 1]) * sc;
-                    v.z = __uint_as_float(r[c + 2]) * sc;
-                    v.w = __uint_as_float(r[c + 3]) * sc;
-                    *reinterpret_cast<float4 *>(dst + c) = v;
-                }
-            }
-            tc::fence_before();
+            ++n_w;
         }
     }
 
@@ -761,92 +1027,6 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         tc::fence_after();
         tc::dealloc(tmem, TMEM_COLS);
     }
-
-}
-
-
-// Split-K merge of the prefill path: sixteen 128-thread CTAs per (prefill block,
-// KV head), 8 query vectors each; blocks covered by a single item were written
-// directly and return at once.  Thread t takes query vector 8z + t / 16 and 8 of
-// its 128 values, and loads up to four partials at once, folding them into a
-// running (M, L, O):
-//   O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
-// Launched as a programmatic dependent of the attention kernel: the plan is
-// read first, the partials only after the attention grid has finished.  The
-// CTAs are small (128 threads, at most 64 registers each); they take the SMs as
-// the attention CTAs retire (capping them at 48 registers, so that one would
-// wait beside each attention CTA, measured slower: two partials per round trip).
-constexpr int MERGE_SPLIT = 16;
-constexpr int MERGE_QMAX = 4;
-
-__global__ void __launch_bounds__(128, 8) k_merge_pf(const kvk::PrefillArgs a) {
-    const int32_t b = a.u.n_dec_blocks + blockIdx.x;
-    const int32_t hk = blockIdx.y;
-    const int32_t nitems = a.p.blk_nitems[b];
-    if (nitems <= 1) {
-        kvd::pdl_trigger();
-        return;
-    }
-    const kvi::DevBlock blk = a.u.blocks[b];
-    const int32_t n = (int32_t)blockIdx.z * (M / MERGE_SPLIT) + (int32_t)(threadIdx.x >> 4);   // 8 per CTA
-    const int32_t d0 = (int32_t)(threadIdx.x & 15) * 8;
-    const int32_t G = a.gqa;
-    if (n >= blk.n_rows * G) return;
-    const int32_t row = a.u.perm[blk.row0 + n / G];
-    const int32_t h = hk * G + (n % G);
-    const int32_t first = a.p.blk_item0[b] - a.p.cap_dec;
-    const int64_t istride = (int64_t)a.n_head_kv * M * PART_STRIDE;
-    const float *pr = a.part + (((int64_t)first * a.n_head_kv + hk) * M + n) * PART_STRIDE;
-    kvd::pdl_wait();
-    kvd::pdl_trigger();   // the next kernel (a K/V store) may be scheduled
-    float mx = -INFINITY, L = 0.f;
-    float acc[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) acc[c] = 0.f;
-    for (int32_t q0 = 0; q0 < nitems; q0 += MERGE_QMAX) {
-        float mk[MERGE_QMAX], lk[MERGE_QMAX];
-        float4 v0[MERGE_QMAX], v1[MERGE_QMAX];
-#pragma unroll
-        for (int i = 0; i < MERGE_QMAX; ++i) {
-            mk[i] = -INFINITY;
-            lk[i] = 0.f;
-            v0[i] = v1[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (q0 + i < nitems) {
-                const float *pq = pr + (int64_t)(q0 + i) * istride;
-                mk[i] = __ldcg(pq);
-                lk[i] = __ldcg(pq + 1);
-                v0[i] = __ldcg(reinterpret_cast<const float4 *>(pq + 4 + d0));
-                v1[i] = __ldcg(reinterpret_cast<const float4 *>(pq + 4 + d0) + 1);
-            }
-        }
-        float mr = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < MERGE_QMAX; ++i) mr = fmaxf(mr, mk[i]);
-        const float mn = fmaxf(mx, mr);
-        if (mn == -INFINITY) continue;
-        const float al = mx == -INFINITY ? 0.f : ex2_approx(mx - mn);
-        L *= al;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) acc[c] *= al;
-#pragma unroll
-        for (int i = 0; i < MERGE_QMAX; ++i) {
-            const float sc = mk[i] == -INFINITY ? 0.f : ex2_approx(mk[i] - mn);
-            L = fmaf(lk[i], sc, L);
-            acc[0] = fmaf(v0[i].x, sc, acc[0]);
-            acc[1] = fmaf(v0[i].y, sc, acc[1]);
-            acc[2] = fmaf(v0[i].z, sc, acc[2]);
-            acc[3] = fmaf(v0[i].w, sc, acc[3]);
-            acc[4] = fmaf(v1[i].x, sc, acc[4]);
-            acc[5] = fmaf(v1[i].y, sc, acc[5]);
-            acc[6] = fmaf(v1[i].z, sc, acc[6]);
-            acc[7] = fmaf(v1[i].w, sc, acc[7]);
-        }
-        mx = mn;
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    float4 *dst = reinterpret_cast<float4 *>(a.o + ((int64_t)row * a.n_head + h) * 128 + d0);
-    dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-    dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
 }
 
 }  // namespace
@@ -854,18 +1034,14 @@ __global__ void __launch_bounds__(128, 8) k_merge_pf(const kvk::PrefillArgs a) {
 namespace kvk {
 
 cudaError_t load_prefill_kernels() {
-    cudaError_t e = cudaFuncSetAttribute(k_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    cudaFuncAttributes fa;
-    return cudaFuncGetAttributes(&fa, k_merge_pf);
+    return cudaFuncSetAttribute(k_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
 }
 
 // The shared-memory attribute was set for the current device by load_prefill_kernels.
-cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const PrefillArgs &a,
-                           int32_t grid_x, cudaStream_t st) {
-    // Both kernels are programmatic dependents of the kernel before them: the
-    // attention kernel sets up (and, with early_ok, reads its plan) while the K/V
-    // store finishes; the merge reads the plan while the attention kernel runs.
+cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const CUtensorMap *tm_part,
+                           const PrefillArgs &a, int32_t grid_x, cudaStream_t st) {
+    // A programmatic dependent of the kernel before it: the attention kernel sets
+    // up (and, with early_ok, reads its plan) while the K/V store finishes.
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -876,12 +1052,7 @@ cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, con
     cfg.stream = st;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_prefill, *tm_k, *tm_v, a);
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(a.u.n_blocks - a.u.n_dec_blocks, a.n_head_kv, MERGE_SPLIT);
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
-    e = cudaLaunchKernelEx(&cfg, k_merge_pf, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_prefill, *tm_k, *tm_v, *tm_part, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

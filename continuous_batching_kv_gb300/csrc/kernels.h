@@ -57,9 +57,9 @@ struct Plan {
     int32_t *n_work;        // [2] decode / prefill item counts
     int32_t *blk_item0;     // [max_blocks] first item of each block
     int32_t *blk_nitems;    // [max_blocks]
-    int32_t *counters;      // [max_blocks * n_head_kv] split-K completion counters
+    int32_t *counters;      // [max_blocks * n_head_kv] split-K completion counters (zero between launches)
     int32_t *cta_item0;     // decode [gx_dec + 1], then prefill [gx_pf + 1]: each CTA column's items
-    int32_t *pf_rows;       // [gx_pf][128]: the ubatch row behind each query vector of each prefill
+    int32_t *pf_rows;       // [gx_pf][PF_M]: the ubatch row behind each query vector of each prefill
                             // CTA column's first item (-1: none), so that Q loads without the
                             // chain item -> block -> row permutation
     int32_t *pf_first;      // [gx_pf][4]: each prefill CTA column's first pair: TMA rows of its two
@@ -115,7 +115,8 @@ struct PrefillArgs {
     Plan p;
     const __half *q;
     float *o;
-    float *part;            // [cap_pf][n_head_kv][128][2 + 128]
+    float *part;            // O rows of the partials: [cap_pf][n_head_kv][PF_M][128]
+    float *part_ml;         // their (m, l): [cap_pf][n_head_kv][PF_M][2]
     int32_t n_head, n_head_kv, gqa;
     int32_t gx_dec;         // decode grid columns (offset of the prefill cta_item0 table)
     float scale_log2;
@@ -124,7 +125,8 @@ struct PrefillArgs {
                             // previous kernel of the stream began, so they may be read before
                             // waiting for it (the kernel is launched as a programmatic dependent)
 };
-cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const PrefillArgs &a,
-                           int32_t grid_x, cudaStream_t st);
+// tm_part: the partials' O rows as a 2-D fp32 matrix (32 x 32 boxes, 128-byte swizzle)
+cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const CUtensorMap *tm_part,
+                           const PrefillArgs &a, int32_t grid_x, cudaStream_t st);
 
 }  // namespace kvk
