@@ -447,7 +447,27 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
             a.scale_log2 = scale_log2;
             a.err = d->d_err;
             a.early_ok = early_ok ? 1 : 0;
-            if ((e = kvk::launch_prefill(&d->tm_k[layer], &d->tm_v[layer], &d->tm_part, a, d->gx_pf, st)) != cudaSuccess)
+            // Q as a (d, head, token) tensor: a GQA group's query vectors of 128 / gqa
+            // consecutive rows are one (64, gqa, 128 / gqa) box per 64-value d half; used
+            // when every prefill block of the ubatch has consecutive rows
+            CUtensorMap tm_q{};
+            bool all_consecutive = true;
+            for (int32_t b = u.n_dec_blocks; b < (int32_t)u.blocks.size() && all_consecutive; ++b)
+                all_consecutive = u.blocks[b].tok0 >= 0;
+            if (128 % c->gqa == 0 && all_consecutive) {
+                auto enc = get_encode();
+                cuuint64_t dims[3] = {128, (cuuint64_t)c->prm.n_head, (cuuint64_t)u.n_tokens};
+                cuuint64_t strides[2] = {128 * 2, (cuuint64_t)c->prm.n_head * 128 * 2};
+                cuuint32_t box[3] = {64, (cuuint32_t)c->gqa, (cuuint32_t)(128 / c->gqa)};
+                cuuint32_t estr[3] = {1, 1, 1};
+                a.q_tma = enc && enc(&tm_q, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(q), dims, strides, box,
+                                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+                                  ? 1
+                                  : 0;
+            }
+            if ((e = kvk::launch_prefill(&d->tm_k[layer], &d->tm_v[layer], &d->tm_part, &tm_q, a, d->gx_pf, st)) !=
+                cudaSuccess)
                 return cuda_fail(c, e, "prefill launch");
             c->launches += 1;
         }

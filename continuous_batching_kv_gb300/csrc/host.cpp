@@ -255,6 +255,7 @@ void build_blocks(UbatchHost &u, const kv_cache *c) {
         for (size_t a = 0; a < g.size(); a += per) {
             std::vector<int32_t> rows(g.begin() + a, g.begin() + std::min(g.size(), a + per));
             DevBlock b{};
+            b.tok0 = -1;
             b.n_rows = (int32_t)rows.size();
             b.seq0 = q;
             b.stream = c->seq_to_stream[q];
@@ -280,6 +281,10 @@ void build_blocks(UbatchHost &u, const kv_cache *c) {
     for (size_t k = 0; k < pf.size(); ++k) {
         pf[k].row0 = (int32_t)u.perm.size();
         u.perm.insert(u.perm.end(), pf_rows[k].begin(), pf_rows[k].end());
+        bool consecutive = true;
+        for (size_t i = 1; i < pf_rows[k].size() && consecutive; ++i)
+            consecutive = pf_rows[k][i] == pf_rows[k][0] + (int32_t)i;
+        pf[k].tok0 = consecutive ? pf_rows[k][0] : -1;
         u.blocks.push_back(pf[k]);
     }
     // CSR: blocks of each sequence

@@ -43,7 +43,8 @@ struct DevBlock {
     int32_t path;    // PATH_DECODE / PATH_PREFILL
     int32_t pos_min;
     int32_t pos_max;
-    int32_t pad;
+    int32_t tok0;    // first ubatch row when the block's rows are consecutive ubatch rows in
+                     // order (perm[row0 + i] == tok0 + i), else -1
 };
 
 // Host-side per-ubatch tables (filled at split / prepare time).

@@ -52,7 +52,8 @@ using kvi::PF_M;
 constexpr int NT = 384;                  // 12 warps
 constexpr int W_K = 8;                   // K producer + metadata
 constexpr int W_MMA = 9;                 // TMEM allocation and MMA issue
-constexpr int W_V = 10;                  // V producer (warp 11 only takes part in set-up)
+constexpr int W_V = 10;                  // V producer
+constexpr int W_Q = 11;                  // Q producer (TMA), when the launch loads Q that way
 constexpr int NSM = 256;                 // softmax threads (warps 0-7)
 constexpr int M = 128;                   // lanes of one MMA tile
 static_assert(PF_M == 2 * M, "a prefill block is two MMA tiles");
@@ -107,6 +108,8 @@ struct __align__(16) Aux {
     uint64_t k_full[KSTAGES], k_empty[KSTAGES], v_full[VSTAGES], v_empty[VSTAGES];
     uint64_t meta_full[MSLOTS];
     uint64_t s_full[2], p_full[2], pv_done[2], q_full[2];   // [tile]
+    uint64_t qt_full[2];      // [tile] Q landed by TMA (1 arrival + bytes)
+    uint64_t q_free[2];       // [tile] the item's epilogue is done with the Q area (128 arrivals)
     uint64_t wbar;            // the softmax threads meet (256 arrivals)
     uint64_t gbar;            // a merge may start: every piece of the block is counted (1 arrival)
     uint64_t mbar;            // the partials of one merge pass are in shared memory (bulk copies)
@@ -243,7 +246,8 @@ __device__ __forceinline__ bool last_of_column(const kvk::PrefillArgs &a, int32_
 
 __global__ void __launch_bounds__(NT, 1)
 k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-          const __grid_constant__ CUtensorMap tm_part, const kvk::PrefillArgs a) {
+          const __grid_constant__ CUtensorMap tm_part, const __grid_constant__ CUtensorMap tm_q,
+          const kvk::PrefillArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     Aux &x = *reinterpret_cast<Aux *>(smem + OFF_AUX);
     volatile int32_t *fail = &x.fail;
@@ -284,6 +288,8 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             kvd::mbar_init(&x.p_full[t], M);
             kvd::mbar_init(&x.pv_done[t], 1);
             kvd::mbar_init(&x.q_full[t], M);
+            kvd::mbar_init(&x.qt_full[t], 1);
+            kvd::mbar_init(&x.q_free[t], M);
         }
         kvd::mbar_init(&x.wbar, NSM);
         kvd::mbar_init(&x.gbar, 1);
@@ -496,6 +502,42 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             for (int32_t q = vc > VSTAGES ? vc - VSTAGES : 0; q < vc; ++q)
                 (void)kvd::mbar_wait_bounded(&x.v_full[q % VSTAGES], (uint32_t)(q / VSTAGES) & 1u);
         }
+    } else if (warp == W_Q) {
+        // ===================== Q producer (launches with a.q_tma) =====================
+        // Per item with a step, per tile with query vectors: once the tile's previous
+        // such item is done with the Q area (its epilogue staged output there), Q
+        // arrives as two (64, gqa, 128 / gqa) boxes -- query vector n of the tile is
+        // row n of the 128-byte-swizzled tile, the A operand layout of S = Q K^T.
+        if (a.q_tma && lane == 0) {
+            uint32_t nt[2] = {0, 0};           // items loaded per tile
+            bool dep = false;
+            for (int32_t wi = i0; wi < i1; ++wi) {
+                const ItemInfo it = item_info(a, wi);
+                if (it.steps == 0) continue;
+                const kvi::DevBlock b = a.u.blocks[it.block];
+                bool ok = true;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (t == 1 && b.n_rows * G <= M) break;
+                    if (nt[t] > 0) ok = wait_or_fail(&x.q_free[t], (nt[t] - 1) & 1u, fail);
+                    if (!ok) break;
+                    if (!dep) {
+                        kvd::pdl_wait();   // Q comes from before the previous kernel of the stream
+                        dep = true;
+                    }
+                    uint8_t *qs = smem + OFF_Q + t * TILEB;
+                    const int32_t tok = b.tok0 + (M * t) / G;
+                    kvd::mbar_arrive_expect_tx(&x.qt_full[t], TILEB);
+                    kvd::tma_load_3d(qs, &tm_q, 0, hk * G, tok, &x.qt_full[t]);
+                    kvd::tma_load_3d(qs + HALF, &tm_q, 64, hk * G, tok, &x.qt_full[t]);
+                    ++nt[t];
+                }
+                if (!ok) break;
+            }
+            // loads already issued land before the CTA exits
+            if (*fail)
+                for (int t = 0; t < 2; ++t)
+                    if (nt[t] > 0) (void)kvd::mbar_wait_bounded(&x.qt_full[t], (nt[t] - 1) & 1u);
+        }
     } else if (warp == W_MMA) {
         // ===================== MMA issuer =====================
         // Per item: S_A(0), S_B(0), then per step j: PV_A(j), S_A(j+1), PV_B(j),
@@ -518,10 +560,13 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 const ItemInfo it = item_info(a, wi);
                 if (it.steps == 0) continue;
                 const bool two = a.u.blocks[it.block].n_rows * G > M;
-                if (!(ok = wait_or_fail(&x.q_full[0], n_q[0] & 1u, fail))) break;
+                // Q of each tile: by TMA (qt_full) or written by the softmax threads (q_full)
+                uint64_t *qb0 = a.q_tma ? &x.qt_full[0] : &x.q_full[0];
+                uint64_t *qb1 = a.q_tma ? &x.qt_full[1] : &x.q_full[1];
+                if (!(ok = wait_or_fail(qb0, n_q[0] & 1u, fail))) break;
                 ++n_q[0];
                 if (two) {
-                    if (!(ok = wait_or_fail(&x.q_full[1], n_q[1] & 1u, fail))) break;
+                    if (!(ok = wait_or_fail(qb1, n_q[1] & 1u, fail))) break;
                     ++n_q[1];
                 }
                 if (!(ok = wait_or_fail(&x.k_full[g % KSTAGES], (uint32_t)(g / KSTAGES) & 1u, fail))) break;
@@ -610,7 +655,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 const bool live = row >= 0;
                 const int32_t h = hk * G + (qv % G);
                 if (!dep_done) {   // before the first read of Q and the first write of an output
-                    if (live && it.steps > 0) {
+                    if (live && it.steps > 0 && !a.q_tma) {
                         const __half *qp = a.q + ((int64_t)row * a.n_head + h) * 128;
                         kvd::prefetch_l2(qp);
                         kvd::prefetch_l2(qp + 64);
@@ -624,7 +669,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     //      of S = Q K^T), 128-byte swizzle.  Each load instruction covers
                     //      two whole rows (16 lanes x 16 bytes each), so the reads are
                     //      coalesced; lane j's row comes from the lane that owns it ----
-                    {
+                    if (!a.q_tma) {   // (else the Q producer loads it)
                         const int32_t wrow = 32 * (warp & 3);
                         uint4 v[16];
 #pragma unroll
@@ -783,16 +828,12 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     *reinterpret_cast<float2 *>(a.part_ml + (prow + qv) * 2) = make_float2(m_run, l_run);
                 }
                 uint8_t *stg = q_sm + 4096 * (warp & 3);
-                // the O row in two TMEM reads of 64 columns (warp collective; an item
-                // without a step reads stale columns and replaces them with zeros)
+                if (it.steps > 0) {
+                // the O row in two TMEM reads of 64 columns (warp collective)
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
                 uint32_t ob[64];
                 tc::ld64(o_mine + 64u * (uint32_t)hh, ob);
-                if (it.steps == 0) {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) ob[c] = 0u;
-                }
 #pragma unroll
                 for (int qh = 0; qh < 2; ++qh) {
                     const int q = 2 * hh + qh;
@@ -831,6 +872,18 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     // the partial's rows are written before the piece is counted
                     kvd::bulk_wait_all();
                     kvd::fence_proxy_async_global();
+                }
+                if (a.q_tma) {
+                    // the Q area is free for the next item's Q (TMA writes after these
+                    // generic accesses)
+                    kvd::fence_proxy_async_smem();
+                    kvd::mbar_arrive(&x.q_free[t]);
+                }
+                } else if (dst) {
+                    // a block that sees nothing (a single item, no step): zeros, written
+                    // directly (the Q area may already hold the next item's Q)
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) *reinterpret_cast<float4 *>(dst + 4 * c) = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
                 tc::fence_before();
             } else {
@@ -1039,7 +1092,7 @@ cudaError_t load_prefill_kernels() {
 
 // The shared-memory attribute was set for the current device by load_prefill_kernels.
 cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const CUtensorMap *tm_part,
-                           const PrefillArgs &a, int32_t grid_x, cudaStream_t st) {
+                           const CUtensorMap *tm_q, const PrefillArgs &a, int32_t grid_x, cudaStream_t st) {
     // A programmatic dependent of the kernel before it: the attention kernel sets
     // up (and, with early_ok, reads its plan) while the K/V store finishes.
     cudaLaunchAttribute pdl[1];
@@ -1052,7 +1105,7 @@ cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, con
     cfg.stream = st;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_prefill, *tm_k, *tm_v, *tm_part, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_prefill, *tm_k, *tm_v, *tm_part, *tm_q, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

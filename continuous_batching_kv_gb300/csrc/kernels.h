@@ -119,14 +119,17 @@ struct PrefillArgs {
     float *part_ml;         // their (m, l): [cap_pf][n_head_kv][PF_M][2]
     int32_t n_head, n_head_kv, gqa;
     int32_t gx_dec;         // decode grid columns (offset of the prefill cta_item0 table)
+    int32_t q_tma;          // 1: Q of blocks with consecutive rows loads by TMA through tm_q
     float scale_log2;
     int32_t *err;
     int32_t early_ok;       // 1: the plan, tables and cell mirror were complete before the
                             // previous kernel of the stream began, so they may be read before
                             // waiting for it (the kernel is launched as a programmatic dependent)
 };
-// tm_part: the partials' O rows as a 2-D fp32 matrix (32 x 32 boxes, 128-byte swizzle)
+// tm_part: the partials' O rows as a 2-D fp32 matrix (32 x 32 boxes, 128-byte swizzle);
+// tm_q: q as a 3-D fp16 tensor (d, head, token) with (64, gqa, 128 / gqa) boxes, used when
+// a.q_tma is set
 cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const CUtensorMap *tm_part,
-                           const PrefillArgs &a, int32_t grid_x, cudaStream_t st);
+                           const CUtensorMap *tm_q, const PrefillArgs &a, int32_t grid_x, cudaStream_t st);
 
 }  // namespace kvk
