@@ -181,6 +181,9 @@ constexpr int64_t PF_ITEM_COST = 3;
 // Extra cost of the piece that holds a block's last pair (its causal diagonal, with
 // the per-cell mask), in the same units.
 constexpr int64_t PF_DIAG_COST = 1;
+// Extra cost of every piece of a block split over several columns: its partial is
+// written out and merged (the merge participants wait for the block's last piece).
+constexpr int64_t PF_SPLIT_COST = 3;
 
 // The smallest budget T in [t_lo, t_hi] with columns(T) <= gx, given that t_hi is
 // feasible: every thread of the CTA tries its own candidate, in two rounds (the
@@ -248,20 +251,24 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
         if (pass == 1) {
             // Prefill: work in pairs of tiles, PF_ITEM_COST per item, plus PF_DIAG_COST
             // for the piece holding a block's last pair.
-            const int64_t C = PF_ITEM_COST, D = PF_DIAG_COST;
+            const int64_t C = PF_ITEM_COST, D = PF_DIAG_COST, MS = PF_SPLIT_COST;
             // the blocks' tile counts, staged for the budget search
             for (int32_t b = lo + tid; b < hi && b - lo < DEC_STAGE; b += blockDim.x) s_wc[b - lo] = p.counts[b];
             __syncthreads();
             auto count_of = [&](int32_t b) -> int32_t { return b - lo < DEC_STAGE ? s_wc[b - lo] : p.counts[b]; };
             // how much of the rest of a block a column with `room` left takes: all of
-            // it when its diagonal fits too, else as much as fits short of the last pair
-            auto take_of = [&](int64_t rem, int64_t room, int64_t &cost) -> int64_t {
-                if (rem + D <= room) {
-                    cost = rem + D;
+            // it when its diagonal fits too (plus the merge cost when the block is
+            // already split), else as much as fits short of the last pair, which splits
+            // the block (0: nothing fits, start a new column)
+            auto take_of = [&](int64_t rem, int64_t room, bool split, int64_t &cost) -> int64_t {
+                const int64_t pen = split ? MS : 0;
+                if (rem + D + pen <= room) {
+                    cost = rem + D + pen;
                     return rem;
                 }
-                const int64_t t = min(rem - 1, room);
-                cost = t;
+                const int64_t t = min(rem - 1, room - MS);
+                if (t < 1) return 0;
+                cost = t + MS;
                 return t;
             };
             if (tid == 0) {
@@ -282,15 +289,17 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                 for (int32_t b = lo; b < hi && x < gx; ++b) {
                     const int64_t pairs = (count_of(b) + 1) / 2;
                     int64_t done = 0;
+                    bool split = false;
                     while (done < pairs && x < gx) {
                         int64_t cost = 0;
                         const int64_t room = T - acc - C;
-                        const int64_t take = room < 1 ? 0 : take_of(pairs - done, room, cost);
+                        const int64_t take = room < 1 ? 0 : take_of(pairs - done, room, split, cost);
                         if (take < 1) {
                             ++x;
                             acc = 0;
                             continue;
                         }
+                        if (take < pairs - done) split = true;
                         done += take;
                         acc += C + cost;
                     }
@@ -322,10 +331,11 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                         nseg = 1;
                     } else {
                         int64_t done = 0;
+                        bool split = false;
                         while (done < pairs) {
                             int64_t cost = 0;
                             const int64_t room = T - acc - C;
-                            int64_t take = room < 1 ? 0 : take_of(pairs - done, room, cost);
+                            int64_t take = room < 1 ? 0 : take_of(pairs - done, room, split, cost);
                             if (take < 1 && x < gx - 1) {   // this column is full
                                 ++x;
                                 acc = 0;
@@ -333,8 +343,9 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                             }
                             if (x == gx - 1) {              // the last column takes the rest
                                 take = pairs - done;
-                                cost = take + D;
+                                cost = take + D + (split ? MS : 0);
                             }
+                            if (take < pairs - done) split = true;
                             emit(b, (int32_t)(2 * done), (int32_t)min((int64_t)cnt, 2 * (done + take)));
                             ++nseg;
                             done += take;

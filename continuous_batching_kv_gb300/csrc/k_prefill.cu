@@ -263,6 +263,10 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     // Q, the K/V cache, the outputs, the partials and the merge counters are
     // touched only after the wait.
     if (!a.early_ok) kvd::pdl_wait();
+    // The next kernel of the stream (normally the next call's K/V store) may be
+    // scheduled now: it waits for this grid's completion before it touches memory,
+    // and meanwhile its launch and its own start-up overlap this kernel.
+    if (tid == 0) kvd::pdl_trigger();
     const int32_t *c0 = a.p.cta_item0 + a.gx_dec + 1;
     const int32_t i0 = c0[blockIdx.x];
     const int32_t i1 = c0[blockIdx.x + 1];
@@ -827,7 +831,6 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 } else {
                     *reinterpret_cast<float2 *>(a.part_ml + (prow + qv) * 2) = make_float2(m_run, l_run);
                 }
-                uint8_t *stg = q_sm + 4096 * (warp & 3);
                 if (it.steps > 0) {
                 // the O row in two TMEM reads of 64 columns (warp collective)
 #pragma unroll 1
@@ -837,6 +840,12 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
 #pragma unroll
                 for (int qh = 0; qh < 2; ++qh) {
                     const int q = 2 * hh + qh;
+                    // two staging buffers per warp (its rows in either d half of the tile's
+                    // Q area), used in turn: a partial's TMA store of one overlaps the
+                    // staging of the next
+                    uint8_t *stg = q_sm + qh * HALF + 4096 * (warp & 3);
+                    if (split && lane == 0 && q >= 2) kvd::bulk_wait_read<1>();   // the store from this buffer has read it
+                    __syncwarp();
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         *reinterpret_cast<float4 *>(stg + kvd::swz128((uint32_t)lane, (uint32_t)c)) =
@@ -849,7 +858,6 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         if (lane == 0) {
                             kvd::tma_store_2d(&tm_part, 32 * q, (int32_t)(prow + M * t + 32 * (warp & 3)), stg);
                             kvd::bulk_commit();
-                            kvd::bulk_wait_read<0>();   // the staging area is read: reusable
                         }
                         __syncwarp();
                     } else {
@@ -992,17 +1000,37 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     // pass 1, a thread per query vector: the pieces' weights 2^(m_q - M) / L
                     // replace their m in shared memory
                     for (int32_t r = tid; r < R; r += NSM) {
-                        float Mx = -INFINITY;
-                        for (int32_t q = 0; q < nitems; ++q) Mx = fmaxf(Mx, mls[q * R + r].x);
-                        float L = 0.f;
-                        for (int32_t q = 0; q < nitems; ++q) {
-                            const float2 ml = mls[q * R + r];
-                            const float w = (ml.x == -INFINITY || Mx == -INFINITY) ? 0.f : ex2_approx(ml.x - Mx);
-                            L = fmaf(ml.y, w, L);
-                            mls[q * R + r].x = w;
+                        if (nitems <= 8) {
+                            // every piece's (m, l) of the row in registers at once
+                            float2 ml[8];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) ml[q] = q < nitems ? mls[q * R + r] : make_float2(-INFINITY, 0.f);
+                            float Mx = -INFINITY;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) Mx = fmaxf(Mx, ml[q].x);
+                            float w[8], L = 0.f;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                w[q] = (ml[q].x == -INFINITY || Mx == -INFINITY) ? 0.f : ex2_approx(ml[q].x - Mx);
+                                L = fmaf(ml[q].y, w[q], L);
+                            }
+                            const float inv = L > 0.f ? rcp_approx(L) : 0.f;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                if (q < nitems) mls[q * R + r].x = w[q] * inv;
+                        } else {
+                            float Mx = -INFINITY;
+                            for (int32_t q = 0; q < nitems; ++q) Mx = fmaxf(Mx, mls[q * R + r].x);
+                            float L = 0.f;
+                            for (int32_t q = 0; q < nitems; ++q) {
+                                const float2 ml = mls[q * R + r];
+                                const float w = (ml.x == -INFINITY || Mx == -INFINITY) ? 0.f : ex2_approx(ml.x - Mx);
+                                L = fmaf(ml.y, w, L);
+                                mls[q * R + r].x = w;
+                            }
+                            const float inv = L > 0.f ? rcp_approx(L) : 0.f;
+                            for (int32_t q = 0; q < nitems; ++q) mls[q * R + r].x *= inv;
                         }
-                        const float inv = L > 0.f ? rcp_approx(L) : 0.f;
-                        for (int32_t q = 0; q < nitems; ++q) mls[q * R + r].x *= inv;
                     }
                     kvd::mbar_arrive(&x.wbar);                             // the weights are in place
                     ok = __all_sync(0xffffffffu, wait_or_fail(&x.wbar, n_w & 1u, fail));
