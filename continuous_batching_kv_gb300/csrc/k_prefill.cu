@@ -928,64 +928,79 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     rank += __popc(bal & __ballot_sync(0xffffffffu, k < wi));
                 }
             }
-            if (tid == 0) {
-                // count the piece: every thread's writes of it came before the barrier
-                // above, so one release by this thread publishes them all
-                asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(cnt) : "memory");
-                if (mine) {
-                    // wait (bounded) until every piece of the block is counted
-                    long long t0c = clock64();
-                    while (ld_acquire(cnt) < nitems) {
-                        if (*fail || clock64() - t0c > kvd::WAIT_LIMIT_CYCLES) {
-                            *fail = 1;
-                            break;
-                        }
-                        __nanosleep(64);
-                    }
-                    x.mrg_lo = (int32_t)((int64_t)nq * rank / np);
-                    x.mrg_hi = (int32_t)((int64_t)nq * (rank + 1) / np);
-                    kvd::mbar_arrive(&x.gbar);
+            // The merge of query vectors mrg_lo .. mrg_hi - 1:
+            //   O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
+            // Each piece's O rows of a share are one contiguous range, and so are their
+            // (m, l): two bulk copies per piece bring them into shared memory (the Q area
+            // and the K/V rings, idle now), in passes of rp query vectors.
+            const int64_t istride = (int64_t)a.n_head_kv * PF_M;           // partial rows per item
+            const int64_t prow0 = ((int64_t)it0 * a.n_head_kv + hk) * PF_M;
+            constexpr uint32_t ROWB = 128 * 4;                           // bytes of one O row
+            constexpr uint32_t MCAP = OFF_AUX;                           // shared bytes free for the merge
+            // rows per pass: a multiple of 8, with room for one more (m, l) per piece
+            const int32_t rp = min(PF_M, (int32_t)(((MCAP / (uint32_t)nitems - 8u) / (ROWB + 8u)) & ~7u));
+            auto issue_pass = [&](int32_t v0, int32_t R) {   // one thread: the copies of one pass
+                const int32_t R2 = (R + 1) & ~1;                         // (m, l) rows copied: an even count
+                const uint32_t qstride = (uint32_t)R * ROWB;
+                float2 *mls = reinterpret_cast<float2 *>(smem + (uint32_t)nitems * qstride);   // [piece][R2]
+                kvd::fence_proxy_async_global();
+                kvd::mbar_arrive_expect_tx(&x.mbar, (uint32_t)nitems * (qstride + 8u * (uint32_t)R2));
+                for (int32_t q = 0; q < nitems; ++q) {
+                    const int64_t r0 = prow0 + q * istride + v0;
+                    kvd::bulk_load(mls + q * R2, reinterpret_cast<const float2 *>(a.part_ml) + r0, 8u * (uint32_t)R2,
+                                   &x.mbar);
+                    kvd::bulk_load(smem + (uint32_t)q * qstride, a.part + r0 * 128, qstride, &x.mbar);
                 }
+            };
+            if (warp == 0) {
+                if (lane == 0) {
+                    // count the piece: every thread's writes of it came before the barrier
+                    // above, so one release by this thread publishes them all
+                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(cnt) : "memory");
+                    if (mine) {
+                        // wait (bounded) until every piece of the block is counted
+                        long long t0c = clock64();
+                        while (ld_acquire(cnt) < nitems) {
+                            if (*fail || clock64() - t0c > kvd::WAIT_LIMIT_CYCLES) {
+                                *fail = 1;
+                                break;
+                            }
+                            __nanosleep(64);
+                        }
+                        // shares start on a multiple of 8 query vectors (16-byte aligned
+                        // (m, l) copies)
+                        const int32_t lo = (int32_t)((int64_t)nq * rank / np) & ~7;
+                        const int32_t hi = rank + 1 == np ? nq : (int32_t)((int64_t)nq * (rank + 1) / np) & ~7;
+                        x.mrg_lo = lo;
+                        x.mrg_hi = hi;
+                        // the first pass's copies go out before the other warps are woken
+                        if (lo < hi && rp >= 8 && !*fail) issue_pass(lo, min(rp, hi - lo));
+                    }
+                }
+                // the rest of warp 0 waits here, not on the barrier below: lane 0 is
+                // the one that completes it
+                __syncwarp();
+                if (mine && lane == 0) kvd::mbar_arrive(&x.gbar);
             }
             if (!mine) continue;
-            ok = __all_sync(0xffffffffu, wait_or_fail(&x.gbar, 0, fail));
+            if (warp != 0) ok = __all_sync(0xffffffffu, wait_or_fail(&x.gbar, 0, fail));
             if (!ok || !warp_ok(fail)) break;
-            // ---- merge query vectors mrg_lo .. mrg_hi - 1:
-            //      O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q.
-            //      Each piece's O rows of my share are one contiguous range: one bulk
-            //      copy per piece brings them into shared memory (the Q area and the K/V
-            //      rings, idle now), their (m, l) come by plain loads; warp w merges
-            //      query vectors v0 + 32k + 4w + r (r = 0..3) together, lane l owning
-            //      d = 4l .. 4l + 3, writes each merged row over the first piece's copy of
-            //      it and sends it out as one bulk copy ----
+            if (rp < 8) {
+                if (tid == 0) kvd::report(a.err, kvd::DERR_BOUNDS);
+                break;
+            }
+            // ---- a pass: the weights from the (m, l) (a thread per query vector), then
+            //      the rows summed piece by piece as they land and stored, 512 contiguous
+            //      bytes each ----
             {
-                const int64_t istride = (int64_t)a.n_head_kv * PF_M;          // partial rows per item
-                const int64_t prow0 = ((int64_t)it0 * a.n_head_kv + hk) * PF_M;
                 const int32_t lo = x.mrg_lo, hi = x.mrg_hi;
-                constexpr uint32_t ROWB = 128 * 4;                          // bytes of one O row
-                constexpr uint32_t MCAP = OFF_AUX;                          // shared bytes free for the merge
-                const int32_t rp = min(PF_M, (int32_t)(MCAP / ((uint32_t)nitems * (ROWB + 8))));   // rows per pass
-                if (rp < 1) {
-                    if (tid == 0) kvd::report(a.err, kvd::DERR_BOUNDS);
-                    break;
-                }
                 uint32_t n_m = 0;                                          // mbar phases
-                bool stored = false;                                       // this lane issued bulk stores
                 for (int32_t v0 = lo; v0 < hi; v0 += rp, ++n_m) {
                     const int32_t R = min(rp, hi - v0);
+                    const int32_t R2 = (R + 1) & ~1;
                     const uint32_t qstride = (uint32_t)R * ROWB;
-                    float2 *mls = reinterpret_cast<float2 *>(smem + (uint32_t)nitems * qstride);   // [piece][row]
-                    if (tid == 0) {
-                        kvd::fence_proxy_async_global();
-                        kvd::mbar_arrive_expect_tx(&x.mbar, (uint32_t)nitems * qstride);
-                        for (int32_t q = 0; q < nitems; ++q)
-                            kvd::bulk_load(smem + (uint32_t)q * qstride, a.part + (prow0 + q * istride + v0) * 128, qstride,
-                                           &x.mbar);
-                    }
-                    for (int32_t e = tid; e < nitems * R; e += NSM) {
-                        const int32_t q = e / R, r = e - q * R;
-                        mls[e] = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + prow0 + q * istride + v0 + r);
-                    }
+                    float2 *mls = reinterpret_cast<float2 *>(smem + (uint32_t)nitems * qstride);
+                    if (v0 != lo && tid == 0) issue_pass(v0, R);
                     // warp w's output rows, one load per lane (lane 8k + r: query vector
                     // v0 + 64k + 8w + r), before they are needed
                     int32_t orow = -1;
@@ -993,18 +1008,15 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         const int32_t vl = v0 + 64 * (lane >> 3) + 8 * warp + (lane & 7);
                         if (vl < v0 + R) orow = a.u.perm[b.row0 + vl / G];
                     }
-                    kvd::mbar_arrive(&x.wbar);                             // (m, l) are in shared memory
-                    ok = __all_sync(0xffffffffu, wait_or_fail(&x.wbar, n_w & 1u, fail));
-                    ++n_w;
+                    ok = __all_sync(0xffffffffu, wait_or_fail(&x.mbar, n_m & 1u, fail));   // rows and (m, l) landed
                     if (!ok) break;
                     // pass 1, a thread per query vector: the pieces' weights 2^(m_q - M) / L
                     // replace their m in shared memory
                     for (int32_t r = tid; r < R; r += NSM) {
                         if (nitems <= 8) {
-                            // every piece's (m, l) of the row in registers at once
                             float2 ml[8];
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) ml[q] = q < nitems ? mls[q * R + r] : make_float2(-INFINITY, 0.f);
+                            for (int q = 0; q < 8; ++q) ml[q] = q < nitems ? mls[q * R2 + r] : make_float2(-INFINITY, 0.f);
                             float Mx = -INFINITY;
 #pragma unroll
                             for (int q = 0; q < 8; ++q) Mx = fmaxf(Mx, ml[q].x);
@@ -1017,28 +1029,28 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                             const float inv = L > 0.f ? rcp_approx(L) : 0.f;
 #pragma unroll
                             for (int q = 0; q < 8; ++q)
-                                if (q < nitems) mls[q * R + r].x = w[q] * inv;
+                                if (q < nitems) mls[q * R2 + r].x = w[q] * inv;
                         } else {
                             float Mx = -INFINITY;
-                            for (int32_t q = 0; q < nitems; ++q) Mx = fmaxf(Mx, mls[q * R + r].x);
+                            for (int32_t q = 0; q < nitems; ++q) Mx = fmaxf(Mx, mls[q * R2 + r].x);
                             float L = 0.f;
                             for (int32_t q = 0; q < nitems; ++q) {
-                                const float2 ml = mls[q * R + r];
+                                const float2 ml = mls[q * R2 + r];
                                 const float w = (ml.x == -INFINITY || Mx == -INFINITY) ? 0.f : ex2_approx(ml.x - Mx);
                                 L = fmaf(ml.y, w, L);
-                                mls[q * R + r].x = w;
+                                mls[q * R2 + r].x = w;
                             }
                             const float inv = L > 0.f ? rcp_approx(L) : 0.f;
-                            for (int32_t q = 0; q < nitems; ++q) mls[q * R + r].x *= inv;
+                            for (int32_t q = 0; q < nitems; ++q) mls[q * R2 + r].x *= inv;
                         }
                     }
                     kvd::mbar_arrive(&x.wbar);                             // the weights are in place
                     ok = __all_sync(0xffffffffu, wait_or_fail(&x.wbar, n_w & 1u, fail));
                     ++n_w;
-                    if (ok) ok = __all_sync(0xffffffffu, wait_or_fail(&x.mbar, n_m & 1u, fail));   // the O rows landed
                     if (!ok) break;
-                    // pass 2, a warp per 8 query vectors at once, lane l owning d = 4l .. 4l + 3
-                    for (int32_t k = 0; 64 * k + 8 * warp < R; ++k) {
+                    // pass 2, a warp per 8 query vectors at once (v0 + 64k + 8w + r), lane l
+                    // owning d = 4l .. 4l + 3
+                    for (int32_t k = 0; 64 * k + 8 * warp < R && ok; ++k) {
                         const int32_t rb = 64 * k + 8 * warp;          // first row of the batch (pass-relative)
                         const int32_t nr = min(8, R - rb);
                         float4 acc[8];
@@ -1049,7 +1061,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                             float4 ov[8];
 #pragma unroll
                             for (int r = 0; r < 8; ++r) {
-                                w[r] = r < nr ? mls[q * R + rb + r].x : 0.f;
+                                w[r] = r < nr ? mls[q * R2 + rb + r].x : 0.f;
                                 ov[r] = r < nr ? *reinterpret_cast<const float4 *>(smem + (uint32_t)q * qstride +
                                                                                    (uint32_t)(rb + r) * ROWB + 16 * lane)
                                                : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1062,32 +1074,27 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                                 acc[r].w = fmaf(ov[r].w, w[r], acc[r].w);
                             }
                         }
-                        // the merged rows over the first piece's copies (only this warp
-                        // reads those rows), then one bulk copy per row
+                        if (!ok) break;
 #pragma unroll
-                        for (int r = 0; r < 8; ++r)
-                            if (r < nr) *reinterpret_cast<float4 *>(smem + (uint32_t)(rb + r) * ROWB + 16 * lane) = acc[r];
-                        kvd::fence_proxy_async_smem();
-                        __syncwarp();
-                        const int32_t mrow = __shfl_sync(0xffffffffu, orow, 8 * k + (lane & 7));
-                        if (lane < nr) {
-                            const int32_t v = v0 + rb + lane;
-                            kvd::bulk_store(a.o + ((int64_t)mrow * a.n_head + hk * G + (v % G)) * 128,
-                                            smem + (uint32_t)(rb + lane) * ROWB, ROWB);
-                            kvd::bulk_commit();
-                            stored = true;
+                        for (int r = 0; r < 8; ++r) {
+                            const int32_t mrow = __shfl_sync(0xffffffffu, orow, 8 * k + r);
+                            if (r < nr) {
+                                const int32_t v = v0 + rb + r;
+                                *reinterpret_cast<float4 *>(a.o + ((int64_t)mrow * a.n_head + hk * G + (v % G)) * 128 +
+                                                            4 * lane) = acc[r];
+                            }
                         }
                     }
-                    // every read of this pass (mine and my bulk copies') is done before the
-                    // next pass's copies land
-                    if (stored) kvd::bulk_wait_read<0>();
-                    kvd::fence_proxy_async_smem();
-                    kvd::mbar_arrive(&x.wbar);
-                    ok = __all_sync(0xffffffffu, wait_or_fail(&x.wbar, n_w & 1u, fail));
-                    ++n_w;
                     if (!ok) break;
+                    if (v0 + rp < hi) {
+                        // every read of this pass is done before the next pass's copies land
+                        kvd::fence_proxy_async_smem();
+                        kvd::mbar_arrive(&x.wbar);
+                        ok = __all_sync(0xffffffffu, wait_or_fail(&x.wbar, n_w & 1u, fail));
+                        ++n_w;
+                        if (!ok) break;
+                    }
                 }
-                if (stored) kvd::bulk_wait_all();
                 if (!ok) break;
             }
             // done reading the partials: count again; the arrival that completes the
