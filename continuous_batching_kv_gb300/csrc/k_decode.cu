@@ -193,6 +193,12 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         bool dep_done = false;
         bool ok = true;
         uint32_t qh = 0, qt = 0;   // group queue head and tail (ring indices)
+        // warm L2 with the column's first four tiles (K and V, both d halves; a
+        // prefetch returns nothing) while the previous kernel may still be storing
+        if (lane < 16) {
+            const int32_t y = a.p.dec_first[4 * blockIdx.x + (lane >> 2)];
+            if (y >= 0) kvd::tma_prefetch_2d((lane & 2) ? &tm_v : &tm_k, hk * 128 + 64 * (lane & 1), y);
+        }
         // wait outcomes and the loop conditions are agreed by the whole warp, so a
         // failure never splits it in front of __syncwarp
         auto acquire = [&](int32_t st) -> bool {
@@ -691,9 +697,14 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
                 l[n] = v;
             }
+            // Three rounds, one exchange each: in round sd, warp sd + j writes slot
+            // (sd == 4 ? j : sd + j) and warp j merges it.  A slot is written again only
+            // by the warp that read it in the round before, so no second exchange is
+            // needed between rounds; one more after the last round keeps the next
+            // item's writers off slot 1 until warp 0 has read it.
             for (int sd = 4; sd >= 1 && ok; sd >>= 1) {
                 if (warp >= sd && warp < 2 * sd) {
-                    const int slot = warp - sd;
+                    const int slot = sd == 4 ? warp - sd : warp;
 #pragma unroll
                     for (int n = 0; n < NQ; ++n) {
                         if (lane == 0) {
@@ -706,10 +717,11 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 }
                 if (!(ok = cons_sync(&x.cbar, cph, fail))) break;
                 if (warp < sd) {
+                    const int slot = sd == 4 ? warp : sd + warp;
 #pragma unroll
                     for (int n = 0; n < NQ; ++n) {
-                        const float m2 = x.scr_m[warp][n], l2 = x.scr_l[warp][n];
-                        const float4 o2 = *reinterpret_cast<const float4 *>(&x.scr_o[warp][n][4 * lane]);
+                        const float m2 = x.scr_m[slot][n], l2 = x.scr_l[slot][n];
+                        const float4 o2 = *reinterpret_cast<const float4 *>(&x.scr_o[slot][n][4 * lane]);
                         const float mn = fmaxf(m[n], m2);
                         const float a1 = m[n] == -INFINITY ? 0.f : ex2_approx(m[n] - mn);
                         const float a2 = m2 == -INFINITY ? 0.f : ex2_approx(m2 - mn);
@@ -721,8 +733,8 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                         m[n] = mn;
                     }
                 }
-                ok = cons_sync(&x.cbar, cph, fail);
             }
+            if (ok) ok = cons_sync(&x.cbar, cph, fail);
             if (!ok) break;
             if (warp == 0) {
                 const int32_t nitems = a.p.blk_nitems[w.block];
@@ -750,10 +762,13 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                                 make_float4(acc[n][0], acc[n][1], acc[n][2], acc[n][3]);
                         }
                     }
-                    __threadfence();
+                    // the warp's partial writes come before lane 0's count, which
+                    // releases them (and, for the last piece, acquires the others')
                     __syncwarp();
                     int32_t prev = 0;
-                    if (lane == 0) prev = atomicAdd(&a.p.counters[w.block * a.n_head_kv + hk], 1);
+                    if (lane == 0)
+                        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                                     : "=r"(prev) : "l"(&a.p.counters[w.block * a.n_head_kv + hk]) : "memory");
                     prev = __shfl_sync(0xffffffffu, prev, 0);
                     if (lane == 0) x.last_piece = prev == nitems - 1 ? 1 : 0;
                 }
@@ -770,7 +785,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             if (nitems_b > 1) {
                 if (!(ok = cons_sync(&x.cbar, cph, fail))) break;
                 if (x.last_piece) {
-                    __threadfence();
+                    // (warp 0's acquiring count came before the exchange above)
                     const int32_t it0 = a.p.blk_item0[w.block];
                     const int64_t istride = (int64_t)a.n_head_kv * DEC_QMAX * PART_STRIDE;
                     const float *pb = a.part + ((int64_t)it0 * a.n_head_kv + hk) * DEC_QMAX * PART_STRIDE;

@@ -499,6 +499,19 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
         __syncthreads();   // items written by other threads are visible below
         fill_cta0(p.work + item_base, n_items, gx, cta0);
         __syncthreads();
+        // each column's first four listed tiles, as TMA rows
+        for (int32_t x = tid; x < (int32_t)gx; x += blockDim.x) {
+            int32_t f[4] = {-1, -1, -1, -1};
+            int32_t nf = 0;
+            for (int32_t i = cta0[x]; i < cta0[x + 1] && nf < 4; ++i) {
+                const kvk::WorkItem w = p.work[item_base + i];
+                const kvi::DevBlock b = u.blocks[w.block];
+                const int32_t *list = p.tiles + (int64_t)w.block * p.tile_stride;
+                for (int32_t t = w.t0; t < w.t1 && nf < 4; ++t) f[nf++] = b.stream * u.kv_size + list[t] * TILE;
+            }
+            for (int h = 0; h < 4; ++h) p.dec_first[4 * x + h] = f[h];
+        }
+        __syncthreads();
     }
 }
 

@@ -64,6 +64,8 @@ struct Plan {
                             // chain item -> block -> row permutation
     int32_t *pf_first;      // [gx_pf][4]: each prefill CTA column's first pair: TMA rows of its two
                             // tiles (-TILE: no second tile), 1 if fully visible; [0] < 0: none
+    int32_t *dec_first;     // [gx_dec][4]: the TMA rows of each decode CTA column's first four listed
+                            // tiles (-1: fewer), warmed into L2 before the kernel waits for the store
     int32_t *err;
     int32_t tile_stride;
     int32_t cap_dec, cap_pf;
