@@ -548,7 +548,11 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
         // S_B(j+1).  S_t(j+1) overwrites the score buffer whose P the PV_t(j) just
         // issued reads: one thread's MMAs run in issue order.  Tile B takes part
         // only when the block has more than 128 query vectors.
-        if (lane == 0) {
+        // The whole warp runs the loop (its waits agreed by all lanes); one elected
+        // lane -- the same one every time, the lowest, as the warp is converged --
+        // issues each group of MMAs and their commits, so that the operand
+        // descriptors stay warp-uniform values.
+        {
             int32_t g = 0;                     // steps issued (K / V / metadata rings)
             uint32_t n_t[2] = {0, 0};          // steps per tile (s_full / p_full / pv_done phases)
             uint32_t n_q[2] = {0, 0};          // items per tile (q_full phases)
@@ -560,6 +564,9 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             const uint64_t dq = tc::sdesc_sw128(sbase + OFF_Q, 16, 1024);          // + t * TILEB
             const uint64_t dk = tc::sdesc_sw128(sbase + OFF_K, 16, 1024);          // + stage * TILEB
             const uint64_t dv = tc::sdesc_sw128(sbase + OFF_V, HALF, 1024);        // + stage * TILEB
+            auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, wait_or_fail(bar, parity, fail));
+            };
             for (int32_t wi = i0; wi < i1 && ok; ++wi) {
                 const ItemInfo it = item_info(a, wi);
                 if (it.steps == 0) continue;
@@ -567,15 +574,15 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 // Q of each tile: by TMA (qt_full) or written by the softmax threads (q_full)
                 uint64_t *qb0 = a.q_tma ? &x.qt_full[0] : &x.q_full[0];
                 uint64_t *qb1 = a.q_tma ? &x.qt_full[1] : &x.q_full[1];
-                if (!(ok = wait_or_fail(qb0, n_q[0] & 1u, fail))) break;
+                if (!(ok = wait_all(qb0, n_q[0] & 1u))) break;
                 ++n_q[0];
                 if (two) {
-                    if (!(ok = wait_or_fail(qb1, n_q[1] & 1u, fail))) break;
+                    if (!(ok = wait_all(qb1, n_q[1] & 1u))) break;
                     ++n_q[1];
                 }
-                if (!(ok = wait_or_fail(&x.k_full[g % KSTAGES], (uint32_t)(g / KSTAGES) & 1u, fail))) break;
+                if (!(ok = wait_all(&x.k_full[g % KSTAGES], (uint32_t)(g / KSTAGES) & 1u))) break;
                 tc::fence_after();
-                {
+                if (kvd::elect_one()) {
                     const uint64_t kb0 = dk + (uint64_t)(((g % KSTAGES) * TILEB) >> 4);
                     issue_s8(tmem + COL_S, dq, kb0);
                     tc::commit(&x.s_full[0]);
@@ -583,47 +590,61 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                         issue_s8(tmem + COL_S + 128u, dq + (uint64_t)(TILEB >> 4), kb0);
                         tc::commit(&x.s_full[1]);
                     }
+                    tc::commit(&x.k_empty[g % KSTAGES]);
                 }
-                tc::commit(&x.k_empty[g % KSTAGES]);
+                __syncwarp();
                 for (int32_t j = 0; j < it.steps && ok; ++j) {
                     const int32_t gs = g + j;
                     const bool more = j + 1 < it.steps;
-                    if (!(ok = wait_or_fail(&x.p_full[0], (n_t[0] + (uint32_t)j) & 1u, fail))) break;
-                    if (!(ok = wait_or_fail(&x.v_full[gs % VSTAGES], (uint32_t)(gs / VSTAGES) & 1u, fail))) break;
+                    if (!(ok = wait_all(&x.p_full[0], (n_t[0] + (uint32_t)j) & 1u))) break;
+                    if (!(ok = wait_all(&x.v_full[gs % VSTAGES], (uint32_t)(gs / VSTAGES) & 1u))) break;
                     tc::fence_after();
                     const uint64_t vb0 = dv + (uint64_t)(((gs % VSTAGES) * TILEB) >> 4);
                     const uint64_t kb1 = dk + (uint64_t)((((gs + 1) % KSTAGES) * TILEB) >> 4);
                     const uint32_t acc = j > 0 ? 1u : 0u;
-                    issue_pv8(tmem + COL_O, tmem + COL_S, vb0, acc);
-                    tc::commit(&x.pv_done[0]);
+                    if (kvd::elect_one()) {
+                        issue_pv8(tmem + COL_O, tmem + COL_S, vb0, acc);
+                        tc::commit(&x.pv_done[0]);
+                    }
+                    __syncwarp();
                     if (more) {
-                        if (!(ok = wait_or_fail(&x.k_full[(gs + 1) % KSTAGES], (uint32_t)((gs + 1) / KSTAGES) & 1u,
-                                                fail)))
-                            break;
+                        if (!(ok = wait_all(&x.k_full[(gs + 1) % KSTAGES], (uint32_t)((gs + 1) / KSTAGES) & 1u))) break;
                         tc::fence_after();
-                        issue_s8(tmem + COL_S, dq, kb1);
-                        tc::commit(&x.s_full[0]);
+                        if (kvd::elect_one()) {
+                            issue_s8(tmem + COL_S, dq, kb1);
+                            tc::commit(&x.s_full[0]);
+                        }
+                        __syncwarp();
                     }
                     if (two) {
-                        if (!(ok = wait_or_fail(&x.p_full[1], (n_t[1] + (uint32_t)j) & 1u, fail))) break;
+                        if (!(ok = wait_all(&x.p_full[1], (n_t[1] + (uint32_t)j) & 1u))) break;
                         tc::fence_after();
-                        issue_pv8(tmem + COL_O + 128u, tmem + COL_S + 128u, vb0, acc);
-                        tc::commit(&x.pv_done[1]);
-                        if (more) {
-                            issue_s8(tmem + COL_S + 128u, dq + (uint64_t)(TILEB >> 4), kb1);
-                            tc::commit(&x.s_full[1]);
+                        if (kvd::elect_one()) {
+                            issue_pv8(tmem + COL_O + 128u, tmem + COL_S + 128u, vb0, acc);
+                            tc::commit(&x.pv_done[1]);
+                            if (more) {
+                                issue_s8(tmem + COL_S + 128u, dq + (uint64_t)(TILEB >> 4), kb1);
+                                tc::commit(&x.s_full[1]);
+                            }
                         }
+                        __syncwarp();
                     }
-                    tc::commit(&x.v_empty[gs % VSTAGES]);
-                    if (more) tc::commit(&x.k_empty[(gs + 1) % KSTAGES]);
+                    if (kvd::elect_one()) {
+                        tc::commit(&x.v_empty[gs % VSTAGES]);
+                        if (more) tc::commit(&x.k_empty[(gs + 1) % KSTAGES]);
+                    }
+                    __syncwarp();
                 }
                 n_t[0] += (uint32_t)it.steps;
                 if (two) n_t[1] += (uint32_t)it.steps;
                 g += it.steps;
             }
             // all issued MMAs complete before TMEM is released
-            tc::commit(&x.spare);
-            (void)kvd::mbar_wait_bounded(&x.spare, 0);
+            if (kvd::elect_one()) {
+                tc::commit(&x.spare);
+                (void)kvd::mbar_wait_bounded(&x.spare, 0);
+            }
+            __syncwarp();
         }
     }
     } else {
