@@ -90,9 +90,16 @@ def load_peaks():
 # workloads whose measured calls hold one decode row per sequence
 # DRAM bytes (read + write) of one k_decode launch of the 256-sequence workload,
 # from an ncu capture of the current kernel (profiles/k_decode_llama8b-decode-256seq-
-# lognormal.md; a launch at decode step 2, 3.519 GB algorithmic).  Cleared to nothing
+# lognormal.md; a launch at decode step 2, 3.521 GB algorithmic).  Cleared to nothing
 # whenever the kernel changes until it is captured again.
-DECODE_TRAFFIC = {5: 3552778000}
+DECODE_TRAFFIC = {5: 3557391872}
+# One k_prefill launch of the 5000-token prefill captured by ncu (profiles/k_prefill_
+# qwen-prefill-5000-b2048-ub512.md: ubatch 5, layer 5): its DRAM bytes (read + write)
+# and its algorithmic bytes.  The launches of a step differ in size, so the reported
+# traffic is this ratio times the timed launches' mean algorithmic bytes (DRAM traffic
+# grows with the K/V rows read; the O rows stay in L2 within a launch).  Cleared to
+# nothing whenever the kernel changes until it is captured again.
+PREFILL_TRAFFIC = {2: (14830848, 18874368)}
 
 DECODE_BOUND = {3: True, 5: True}
 
@@ -555,9 +562,13 @@ def run_ours(args, rank, world, device):
     else:
         per_pair_flops = 4 * arm.d * arm.H
         achieved = (sum(p for _, p, _ in res) * per_pair_flops) / secs / 1e12 if durs else 0.0
+        alg_bytes = sum(b for _, _, b in res) / max(1, len(durs))
+        tr = PREFILL_TRAFFIC.get(cfg["id"]) if args.ubatch is None and args.streams is None else None
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tflops, "unit": "TFLOP/s",
-                "frac": round(achieved / tflops, 4), "traffic": None,
-                "kernel": "ubatch_attention (k_prefill)"}
+                "frac": round(achieved / tflops, 4),
+                "traffic": int(alg_bytes * tr[0] / tr[1]) if tr else None,
+                "kernel": "ubatch_attention (k_prefill)",
+                "algorithmic_bytes_per_launch": int(alg_bytes)}
     roof.update({"peak_source": peak_src, "launches_timed": len(durs),
                  "timing": ("CUDA events around each attention launch of layers >= 1, " if arm.L > 1 else
                             "CUDA events around each attention launch (one layer: its plan kernels included), ")
