@@ -271,6 +271,13 @@ int device_init(kv_cache *c) {
     const int32_t max_pf_blocks = std::max<int32_t>(1, (c->n_ubatch * c->gqa + PF_MIN_QV - 1) / PF_MIN_QV);
     d->gx_dec = std::max<int32_t>(1, d->n_sm * kvk::decode_ctas_per_sm() / hkv);
     d->gx_pf = std::min<int32_t>(kvk::PLAN_MAX_COLS, std::max<int32_t>(1, d->n_sm / hkv));
+    // Prefill CTAs in clusters of PF_CLUSTER columns (a split block's pieces merge over
+    // distributed shared memory) when the grid has room for at least two clusters a row
+    d->plan.pf_cluster = 1;
+    if (d->gx_pf >= 2 * PF_CLUSTER) {
+        d->gx_pf -= d->gx_pf % PF_CLUSTER;
+        d->plan.pf_cluster = PF_CLUSTER;
+    }
     kvk::Plan &p = d->plan;
     p.tile_stride = (c->kv_size + TILE - 1) / TILE;
     p.cap_dec = d->gx_dec + d->max_blocks;
@@ -448,6 +455,7 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
             a.scale_log2 = scale_log2;
             a.err = d->d_err;
             a.early_ok = early_ok ? 1 : 0;
+            a.cluster = d->plan.pf_cluster;
             // Q as a (d, head, token) tensor: a GQA group's query vectors of 128 / gqa
             // consecutive rows are one (64, gqa, 128 / gqa) box per 64-value d half; used
             // when every prefill block of the ubatch has consecutive rows

@@ -22,6 +22,7 @@ constexpr int DEC_QMAX = 16;
 constexpr int PF_M = 256;
 // A group takes the prefill path when it has at least this many query vectors.
 constexpr int PF_MIN_QV = 64;
+constexpr int PF_CLUSTER = 4;             // prefill CTAs per thread-block cluster (see device.cu)
 // Cells per plan tile, and cells per TMA sub-box inside it.
 constexpr int TILE = 64;
 constexpr int SUB = 8;

@@ -184,6 +184,9 @@ constexpr int64_t PF_DIAG_COST = 1;
 // Extra cost of every piece of a block split over several columns: its partial is
 // written out and merged (the merge participants wait for the block's last piece).
 constexpr int64_t PF_SPLIT_COST = 3;
+// With clusters: extra cost of a piece of a block split over one cluster's columns (its
+// partial staged in shared memory and merged over distributed shared memory).
+constexpr int64_t PF_CLUSTER_MERGE_COST = 2;
 
 // The smallest budget T in [t_lo, t_hi] with columns(T) <= gx, given that t_hi is
 // feasible: every thread of the CTA tries its own candidate, in two rounds (the
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
     __shared__ int32_t scan_i[1024];
     __shared__ int32_t s_wc[DEC_STAGE];
     __shared__ int32_t s_r0[kvk::PLAN_MAX_COLS], s_nq[kvk::PLAN_MAX_COLS];
+    __shared__ long long s_load[kvk::PLAN_MAX_COLS];
     const int32_t tid = threadIdx.x;
     for (int32_t pass = 0; pass < 2; ++pass) {
         const int32_t lo = pass == 0 ? 0 : u.n_dec_blocks;
@@ -248,7 +252,100 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
             __syncthreads();
             continue;
         }
-        if (pass == 1) {
+        if (pass == 1 && p.pf_cluster > 1) {
+            // Prefill with clusters of C columns.  A block is either whole (one item)
+            // or split into C pieces of equal pair counts, one per column of one
+            // cluster, each the last item of its column (its partial stays in shared
+            // memory until the cluster merges it).  At most one split block per
+            // cluster: the blocks that gain from splitting, largest first; then the
+            // whole blocks, largest first, each into the least loaded column.
+            if (tid == 0) {
+                const int64_t C = p.pf_cluster, Ci = PF_ITEM_COST, D = PF_DIAG_COST, MC = PF_CLUSTER_MERGE_COST;
+                const int32_t ncl = (int32_t)(gx / C);
+                const int32_t nb = hi - lo;
+                auto pairs_of = [&](int32_t b) -> int64_t { return (p.counts[b] + 1) / 2; };
+                auto whole_cost = [&](int32_t b) -> int64_t { const int64_t pr = pairs_of(b); return Ci + pr + (pr > 0 ? D : 0); };
+                auto piece_cost = [&](int32_t b) -> int64_t { return Ci + (pairs_of(b) + C - 1) / C + D + MC; };
+                // scan_i[b - lo]: -2 unplaced, -1 split, else the block's column
+                for (int32_t k = 0; k < nb && k < 1024; ++k) scan_i[k] = -2;
+                for (int32_t x = 0; x < (int32_t)gx; ++x) {
+                    s_load[x] = 0;
+                    s_nq[x] = -1;                       // (for now) the cluster's split block
+                }
+                int32_t nsplit = 0;
+                while (nsplit < ncl) {
+                    int32_t best = -1;
+                    int64_t bw = 0;
+                    for (int32_t b = lo; b < hi && b - lo < 1024; ++b) {
+                        const int64_t w = whole_cost(b);
+                        if (scan_i[b - lo] == -2 && w > piece_cost(b) && w > bw) {
+                            best = b;
+                            bw = w;
+                        }
+                    }
+                    if (best < 0) break;
+                    scan_i[best - lo] = -1;
+                    s_nq[nsplit] = best;
+                    for (int32_t r = 0; r < (int32_t)C; ++r) s_load[nsplit * C + r] += piece_cost(best);
+                    ++nsplit;
+                }
+                while (true) {
+                    int32_t best = -1;
+                    int64_t bw = -1;
+                    for (int32_t b = lo; b < hi && b - lo < 1024; ++b) {
+                        const int64_t w = whole_cost(b);
+                        if (scan_i[b - lo] == -2 && w > bw) {
+                            best = b;
+                            bw = w;
+                        }
+                    }
+                    if (best < 0) break;
+                    int32_t xm = 0;
+                    for (int32_t x = 1; x < ncl * (int32_t)C; ++x)
+                        if (s_load[x] < s_load[xm]) xm = x;
+                    scan_i[best - lo] = xm;
+                    s_load[xm] += bw;
+                }
+                // items column by column: the column's whole blocks, then its piece
+                int32_t nitem = 0;
+                for (int32_t x = 0; x < (int32_t)gx; ++x) {
+                    for (int32_t b = lo; b < hi && b - lo < 1024; ++b) {
+                        if (scan_i[b - lo] != x) continue;
+                        kvk::WorkItem w;
+                        w.block = b;
+                        w.t0 = 0;
+                        w.t1 = p.counts[b];
+                        w.cta = x;
+                        p.blk_item0[b] = item_base + nitem;
+                        p.blk_nitems[b] = 1;
+                        if (nitem < cap) p.work[item_base + nitem] = w;
+                        else kvd::report(p.err, kvd::DERR_BOUNDS);
+                        ++nitem;
+                    }
+                    const int32_t cl = x / (int32_t)C, r = x % (int32_t)C;
+                    const int32_t sb = cl < ncl ? s_nq[cl] : -1;
+                    if (sb >= 0) {
+                        const int32_t cnt = p.counts[sb];
+                        const int64_t pr = pairs_of(sb);
+                        kvk::WorkItem w;
+                        w.block = sb;
+                        w.t0 = (int32_t)min((int64_t)cnt, 2 * (pr * r / C));
+                        w.t1 = (int32_t)min((int64_t)cnt, 2 * (pr * (r + 1) / C));
+                        w.cta = x;
+                        if (r == 0) {
+                            p.blk_item0[sb] = item_base + nitem;
+                            p.blk_nitems[sb] = (int32_t)C;
+                        }
+                        if (nitem < cap) p.work[item_base + nitem] = w;
+                        else kvd::report(p.err, kvd::DERR_BOUNDS);
+                        ++nitem;
+                    }
+                }
+                if (nb > 1024) kvd::report(p.err, kvd::DERR_BOUNDS);
+                p.n_work[1] = min(nitem, cap);
+            }
+            __syncthreads();   // items written by thread 0 are visible below
+        } else if (pass == 1) {
             // Prefill: work in pairs of tiles, PF_ITEM_COST per item, plus PF_DIAG_COST
             // for the piece holding a block's last pair.
             const int64_t C = PF_ITEM_COST, D = PF_DIAG_COST, MS = PF_SPLIT_COST;
@@ -357,6 +454,8 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                 p.n_work[1] = min(nitem, cap);
             }
             __syncthreads();   // items written by thread 0 are visible below
+        }
+        if (pass == 1) {
             fill_cta0(p.work + item_base, p.n_work[1], gx, cta0);
             __syncthreads();
             // each column's first item: its first pair (TMA rows of its two tiles, fully

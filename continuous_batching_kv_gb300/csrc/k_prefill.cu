@@ -118,6 +118,7 @@ struct __align__(16) Aux {
     int32_t fail;
     int32_t mrg_lo, mrg_hi;   // this CTA's share of the merged block's query vectors
     Meta meta[MSLOTS];
+    float2 mlx[PF_M];         // with clusters: this CTA's piece's (m, l) per query vector
 };
 
 constexpr size_t SMEM_BYTES = OFF_AUX + sizeof(Aux);
@@ -310,6 +311,10 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = x.tmem_base;
+    // With clusters: this CTA's last item is a piece of a block split over its cluster
+    // (its partial staged in shared memory), merged after the cluster's first barrier.
+    bool mrg_cl = false;
+    int32_t mrg_nq = 0, mrg_row0 = 0;
     if (warp >= 8) {
     // register split, one instruction per warpgroup: warps 8-11 give registers back
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PR_REGS));
@@ -647,6 +652,10 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             __syncwarp();
         }
     }
+    if (a.cluster > 1) {   // this warp's part in the cluster's two meetings (see the softmax warps' end)
+        kvd::cluster_sync();
+        kvd::cluster_sync();
+    }
     } else {
         // register split: the two softmax warpgroups take more registers
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SM_REGS));
@@ -670,6 +679,16 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             const kvi::DevBlock b = a.u.blocks[it.block];
             const int32_t nq = b.n_rows * G;
             const int32_t nitems = a.p.blk_nitems[it.block];
+            if (nitems > 1 && a.cluster > 1) {
+                // a split piece is its column's last item (the planner makes it so)
+                if (wi + 1 != i1) {
+                    if (tid == 0) kvd::report(a.err, kvd::DERR_BOUNDS);
+                    break;
+                }
+                mrg_cl = true;
+                mrg_nq = nq;
+                mrg_row0 = b.row0;
+            }
             if (t == 0 || nq > M) {
                 // ---------------- this tile has query vectors in the block ----------------
                 int32_t row = -1, rpos = 0;
@@ -843,6 +862,32 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 //      per quarter writes them (the tensor map undoes the swizzle); an
                 //      output row goes out 8 lanes per 128-byte segment ----
                 const bool split = nitems > 1;
+                if (split && a.cluster > 1) {
+                    // ---- a piece of a block split over the cluster: its (m, l) and its
+                    //      unnormalised O row stay in this CTA's shared memory, row qv at
+                    //      512 qv with the 16-byte chunks XOR-swizzled by qv (conflict-free
+                    //      for the writing warp and for a reading warp alike): tile A's
+                    //      rows over the Q area, tile B's over the K ring, both idle now ----
+                    x.mlx[qv] = make_float2(m_run, l_run);
+                    uint8_t *rowp = smem + (uint32_t)qv * 512u;
+                    const uint32_t sw = (uint32_t)(qv & 31);
+                    if (it.steps > 0) {
+#pragma unroll 1
+                        for (int hh = 0; hh < 2; ++hh) {
+                            uint32_t ob[64];
+                            tc::ld64(o_mine + 64u * (uint32_t)hh, ob);
+#pragma unroll
+                            for (int c = 0; c < 16; ++c)
+                                *reinterpret_cast<uint4 *>(rowp + 16u * ((uint32_t)(16 * hh + c) ^ sw)) =
+                                    make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) *reinterpret_cast<uint4 *>(rowp + 16u * c) = make_uint4(0, 0, 0, 0);
+                    }
+                    tc::fence_before();
+                    continue;
+                }
                 float *dst = nullptr;
                 float sc = 1.f;
                 const int64_t prow = ((int64_t)wi * a.n_head_kv + hk) * PF_M;   // this item's first partial row
@@ -918,7 +963,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             } else {
                 g += it.steps;                     // tile B has no query vector in this block
             }
-            if (nitems == 1) continue;
+            if (nitems == 1 || a.cluster > 1) continue;
             // ---------------- a piece of a split block ----------------
             // All 256 softmax threads meet once the piece's rows are written (every
             // thread waits, so none can arrive for a later phase early); thread 0
@@ -1127,15 +1172,67 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
             }
             ++n_w;
         }
+        if (a.cluster > 1) {
+            // Every thread of every CTA of the cluster reaches both barriers exactly once,
+            // after its bounded work: the first makes the staged pieces visible across the
+            // cluster, the second keeps each CTA's shared memory alive until the others
+            // have read it.
+            kvd::cluster_sync();
+            if (warp < 8 && mrg_cl && warp_ok(fail)) {
+                // ---- merge query vectors lo .. hi - 1 of the split block, this CTA's
+                //      share by its rank in the cluster:
+                //      O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q over the C pieces,
+                //      read from the pieces' shared memory; warp w takes vectors lo + w,
+                //      lo + w + 8, ..., lane l owning d = 4l .. 4l + 3 ----
+                constexpr int C = kvi::PF_CLUSTER;       // the launch's cluster size (checked at launch)
+                const uint32_t rank = kvd::cluster_ctarank();
+                const int32_t lo = (int32_t)((int64_t)mrg_nq * rank / C), hi = (int32_t)((int64_t)mrg_nq * (rank + 1) / C);
+                uint32_t ob_q[C], ml_q[C];
+#pragma unroll
+                for (int q = 0; q < C; ++q) {
+                    ob_q[q] = kvd::map_cluster(sbase, (uint32_t)q);
+                    ml_q[q] = kvd::map_cluster(kvd::smem_u32(&x.mlx[0]), (uint32_t)q);
+                }
+                for (int32_t v = lo + warp; v < hi; v += 8) {
+                    float2 ml[C];
+                    float Mx = -INFINITY;
+#pragma unroll
+                    for (int q = 0; q < C; ++q) {
+                        ml[q] = kvd::ld_cluster_f2(ml_q[q] + 8u * (uint32_t)v);
+                        Mx = fmaxf(Mx, ml[q].x);
+                    }
+                    const uint32_t off = (uint32_t)v * 512u + 16u * ((uint32_t)lane ^ (uint32_t)(v & 31));
+                    float4 o4[C];
+#pragma unroll
+                    for (int q = 0; q < C; ++q) o4[q] = kvd::ld_cluster_f4(ob_q[q] + off);
+                    float L = 0.f;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int q = 0; q < C; ++q) {
+                        const float w = (ml[q].x == -INFINITY || Mx == -INFINITY) ? 0.f : ex2_approx(ml[q].x - Mx);
+                        L = fmaf(ml[q].y, w, L);
+                        acc.x = fmaf(o4[q].x, w, acc.x);
+                        acc.y = fmaf(o4[q].y, w, acc.y);
+                        acc.z = fmaf(o4[q].z, w, acc.z);
+                        acc.w = fmaf(o4[q].w, w, acc.w);
+                    }
+                    const float inv = L > 0.f ? rcp_approx(L) : 0.f;
+                    const int32_t row = a.u.perm[mrg_row0 + v / G];
+                    *reinterpret_cast<float4 *>(a.o + ((int64_t)row * a.n_head + hk * G + (v % G)) * 128 + 4 * lane) =
+                        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                }
+            }
+            kvd::cluster_sync();
+        }
     }
 
     tc::fence_before();
     __syncthreads();
-    if (*fail && tid == 0) kvd::report(a.err, kvd::DERR_MMA_TIMEOUT);
     if (warp == W_MMA) {
         tc::fence_after();
         tc::dealloc(tmem, TMEM_COLS);
     }
+    if (*fail && tid == 0) kvd::report(a.err, kvd::DERR_MMA_TIMEOUT);
 }
 
 }  // namespace
@@ -1143,7 +1240,10 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
 namespace kvk {
 
 cudaError_t load_prefill_kernels() {
-    return cudaFuncSetAttribute(k_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(k_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    // clusters of up to 8 CTAs are portable; none larger is asked for
+    return cudaFuncSetAttribute(k_prefill, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
 }
 
 // The shared-memory attribute was set for the current device by load_prefill_kernels.
@@ -1151,16 +1251,23 @@ cudaError_t launch_prefill(const CUtensorMap *tm_k, const CUtensorMap *tm_v, con
                            const CUtensorMap *tm_q, const PrefillArgs &a, int32_t grid_x, cudaStream_t st) {
     // A programmatic dependent of the kernel before it: the attention kernel sets
     // up (and, with early_ok, reads its plan) while the K/V store finishes.
-    cudaLaunchAttribute pdl[1];
-    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    // With a.cluster > 1, also a thread-block cluster of that many columns (the grid's
+    // column count is a multiple of it).
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)(a.cluster > 1 ? a.cluster : 1);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    if (a.cluster != 1 && (a.cluster != kvi::PF_CLUSTER || grid_x % a.cluster != 0)) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_x, a.n_head_kv);
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = st;
-    cfg.attrs = pdl;
-    cfg.numAttrs = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.cluster > 1 ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, k_prefill, *tm_k, *tm_v, *tm_part, *tm_q, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

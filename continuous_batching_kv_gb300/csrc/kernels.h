@@ -69,6 +69,9 @@ struct Plan {
     int32_t *err;
     int32_t tile_stride;
     int32_t cap_dec, cap_pf;
+    int32_t pf_cluster;     // prefill CTAs per thread-block cluster along the columns (1: none);
+                            // > 1: a split block's pieces are the last items of one cluster's
+                            // columns and are merged through distributed shared memory
     int32_t gqa;            // query heads per KV head
 };
 
@@ -124,6 +127,7 @@ struct PrefillArgs {
     int32_t q_tma;          // 1: Q of blocks with consecutive rows loads by TMA through tm_q
     float scale_log2;
     int32_t *err;
+    int32_t cluster;        // Plan::pf_cluster of the launch (its cluster dimension along x)
     int32_t early_ok;       // 1: the plan, tables and cell mirror were complete before the
                             // previous kernel of the stream began, so they may be read before
                             // waiting for it (the kernel is launched as a programmatic dependent)
