@@ -126,6 +126,18 @@ def test_non_causal_prefill_decode_and_prefix():
     assert len(stats) >= 6
 
 
+def test_prefill_split_without_clusters_many_kv_heads():
+    # 32 KV heads leave a few prefill CTA columns per head (too few for clusters of
+    # four), so split blocks write partials to global memory and merge there
+    shape = dict(configs.QWEN, n_layer=1, n_head=32, n_head_kv=32)
+    cfg = {"id": 15, "name": "kv32", "shape": shape,
+           "params": dict(n_ctx=2048, n_batch=2048, n_ubatch=512, n_seq_max=1, n_stream=1),
+           "setup": [],
+           "measured": [{"pos": list(range(1200)), "seq": [[0]] * 1200, "content": [0] * 1200}]}
+    stats, _ = _run(cfg, rows_sample=lambda n: sample_rows(n, 48), check_mask=True)
+    assert len(stats) == 3
+
+
 @pytest.mark.parametrize("causal,n_swa", [(True, 100), (False, 100), (True, 1)])
 def test_sliding_window(causal, n_swa):
     # a window of n_swa positions (a cell that far or further behind the row is
