@@ -99,7 +99,7 @@ DECODE_TRAFFIC = {5: 3557391872}
 # traffic is this ratio times the timed launches' mean algorithmic bytes (DRAM traffic
 # grows with the K/V rows read; the O rows stay in L2 within a launch).  Cleared to
 # nothing whenever the kernel changes until it is captured again.
-PREFILL_TRAFFIC = {2: (14830848, 18874368)}
+PREFILL_TRAFFIC = {2: (14806016, 18874368)}
 
 DECODE_BOUND = {3: True, 5: True}
 
