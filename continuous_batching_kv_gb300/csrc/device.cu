@@ -334,6 +334,8 @@ int device_init(kv_cache *c) {
     if ((e = kvk::load_store_kernels()) != cudaSuccess || (e = kvk::load_plan_kernels()) != cudaSuccess ||
         (e = kvk::load_decode_kernels()) != cudaSuccess || (e = kvk::load_prefill_kernels()) != cudaSuccess)
         return cuda_fail(c, e, "kernel load");
+    // no cluster launch where no cluster of attention CTAs can be resident
+    if (d->plan.pf_cluster > 1 && kvk::prefill_max_active_clusters(d->plan.pf_cluster) < 1) d->plan.pf_cluster = 1;
     // The static-scratch array's address on this device (the current one).  With
     // lazy module loading this lookup is what loads the module and backs the array,
     // so it happens here, where memory is obtained anyway, and not during a call

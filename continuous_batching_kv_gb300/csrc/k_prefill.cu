@@ -1182,8 +1182,7 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 // ---- merge query vectors lo .. hi - 1 of the split block, this CTA's
                 //      share by its rank in the cluster:
                 //      O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q over the C pieces,
-                //      read from the pieces' shared memory; warp w takes vectors lo + w,
-                //      lo + w + 8, ..., lane l owning d = 4l .. 4l + 3 ----
+                //      read from the pieces' shared memory, lane l owning d = 4l .. 4l + 3 ----
                 constexpr int C = kvi::PF_CLUSTER;       // the launch's cluster size (checked at launch)
                 const uint32_t rank = kvd::cluster_ctarank();
                 const int32_t lo = (int32_t)((int64_t)mrg_nq * rank / C), hi = (int32_t)((int64_t)mrg_nq * (rank + 1) / C);
@@ -1193,33 +1192,48 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                     ob_q[q] = kvd::map_cluster(sbase, (uint32_t)q);
                     ml_q[q] = kvd::map_cluster(kvd::smem_u32(&x.mlx[0]), (uint32_t)q);
                 }
-                for (int32_t v = lo + warp; v < hi; v += 8) {
-                    float2 ml[C];
-                    float Mx = -INFINITY;
+                // Warp w takes vectors lo + 32k + 4w + r, r = 0..3, four at once: lane
+                // 4r + q reads piece q's (m, l) of vector r (one load each), the weights
+                // come from shuffles, and each lane then reads its d slice of the 16
+                // rows (4 vectors x 4 pieces) in one round of loads.
+                const int32_t rr = lane >> 2, qq = lane & 3;
+                for (int32_t v0 = lo + 4 * warp; v0 < hi; v0 += 32) {
+                    const int32_t vr = v0 + rr;
+                    float2 ml = make_float2(-INFINITY, 0.f);
+                    if (vr < hi) ml = kvd::ld_cluster_f2(ml_q[qq] + 8u * (uint32_t)vr);
+                    float4 o4[4][C];
 #pragma unroll
-                    for (int q = 0; q < C; ++q) {
-                        ml[q] = kvd::ld_cluster_f2(ml_q[q] + 8u * (uint32_t)v);
-                        Mx = fmaxf(Mx, ml[q].x);
+                    for (int r = 0; r < 4; ++r) {
+                        const int32_t v = min(v0 + r, hi - 1);
+                        const uint32_t off = (uint32_t)v * 512u + 16u * ((uint32_t)lane ^ (uint32_t)(v & 31));
+#pragma unroll
+                        for (int q = 0; q < C; ++q) o4[r][q] = kvd::ld_cluster_f4(ob_q[q] + off);
                     }
-                    const uint32_t off = (uint32_t)v * 512u + 16u * ((uint32_t)lane ^ (uint32_t)(v & 31));
-                    float4 o4[C];
+                    float Mx = fmaxf(ml.x, __shfl_xor_sync(0xffffffffu, ml.x, 1));
+                    Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, 2));
+                    const float w = (ml.x == -INFINITY || Mx == -INFINITY) ? 0.f : ex2_approx(ml.x - Mx);
+                    float L = ml.y * w;
+                    L += __shfl_xor_sync(0xffffffffu, L, 1);
+                    L += __shfl_xor_sync(0xffffffffu, L, 2);
+                    const float wn = L > 0.f ? w * rcp_approx(L) : 0.f;   // piece qq's weight for vector rr
 #pragma unroll
-                    for (int q = 0; q < C; ++q) o4[q] = kvd::ld_cluster_f4(ob_q[q] + off);
-                    float L = 0.f;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int r = 0; r < 4; ++r) {
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int q = 0; q < C; ++q) {
-                        const float w = (ml[q].x == -INFINITY || Mx == -INFINITY) ? 0.f : ex2_approx(ml[q].x - Mx);
-                        L = fmaf(ml[q].y, w, L);
-                        acc.x = fmaf(o4[q].x, w, acc.x);
-                        acc.y = fmaf(o4[q].y, w, acc.y);
-                        acc.z = fmaf(o4[q].z, w, acc.z);
-                        acc.w = fmaf(o4[q].w, w, acc.w);
+                        for (int q = 0; q < C; ++q) {
+                            const float wq = __shfl_sync(0xffffffffu, wn, 4 * r + q);
+                            acc.x = fmaf(o4[r][q].x, wq, acc.x);
+                            acc.y = fmaf(o4[r][q].y, wq, acc.y);
+                            acc.z = fmaf(o4[r][q].z, wq, acc.z);
+                            acc.w = fmaf(o4[r][q].w, wq, acc.w);
+                        }
+                        const int32_t v = v0 + r;
+                        if (v < hi) {
+                            const int32_t row = a.u.perm[mrg_row0 + v / G];
+                            *reinterpret_cast<float4 *>(a.o + ((int64_t)row * a.n_head + hk * G + (v % G)) * 128 + 4 * lane) =
+                                acc;
+                        }
                     }
-                    const float inv = L > 0.f ? rcp_approx(L) : 0.f;
-                    const int32_t row = a.u.perm[mrg_row0 + v / G];
-                    *reinterpret_cast<float4 *>(a.o + ((int64_t)row * a.n_head + hk * G + (v % G)) * 128 + 4 * lane) =
-                        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
                 }
             }
             kvd::cluster_sync();
@@ -1244,6 +1258,28 @@ cudaError_t load_prefill_kernels() {
     if (e != cudaSuccess) return e;
     // clusters of up to 8 CTAs are portable; none larger is asked for
     return cudaFuncSetAttribute(k_prefill, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+}
+
+// Clusters of `cluster` attention CTAs that can be resident at once on the current
+// device (0: the launch would fail, or the query did).
+int prefill_max_active_clusters(int cluster) {
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)cluster;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cluster, 1);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void *)k_prefill, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 // The shared-memory attribute was set for the current device by load_prefill_kernels.

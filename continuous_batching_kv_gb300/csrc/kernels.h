@@ -91,6 +91,7 @@ cudaError_t load_store_kernels();
 cudaError_t load_plan_kernels();
 cudaError_t load_decode_kernels();
 cudaError_t load_prefill_kernels();
+int prefill_max_active_clusters(int cluster);
 
 // k_plan.cu
 cudaError_t launch_plan(const UbView &u, const Plan &p, int32_t n_stream, int32_t gx_dec, int32_t gx_pf,
