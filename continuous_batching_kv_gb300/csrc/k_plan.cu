@@ -329,8 +329,11 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
                         const int64_t pr = pairs_of(sb);
                         kvk::WorkItem w;
                         w.block = sb;
-                        w.t0 = (int32_t)min((int64_t)cnt, 2 * (pr * r / C));
-                        w.t1 = (int32_t)min((int64_t)cnt, 2 * (pr * (r + 1) / C));
+                        // cut in cost, the last pair (the diagonal) costing 1 + D: the piece
+                        // holding it gets fewer pairs when the count does not divide evenly
+                        auto cut = [&](int64_t k) -> int64_t { return k >= C ? pr : min(pr, k * (pr + D) / C); };
+                        w.t0 = (int32_t)min((int64_t)cnt, 2 * cut(r));
+                        w.t1 = (int32_t)min((int64_t)cnt, 2 * cut(r + 1));
                         w.cta = x;
                         if (r == 0) {
                             p.blk_item0[sb] = item_base + nitem;
