@@ -266,6 +266,19 @@ void build_blocks(UbatchHost &u, const kv_cache *c) {
                 b.pos_min = std::min(b.pos_min, u.pos[i]);
                 b.pos_max = std::max(b.pos_max, u.pos[i]);
             }
+            // positions pos_min .. pos_max, each once: the rows that see a cell are then
+            // counted from the interval of positions that see it, with no pass over them
+            b.contig = 0;
+            if ((int64_t)b.pos_max - b.pos_min + 1 == (int64_t)rows.size()) {
+                std::vector<char> seen(rows.size(), 0);
+                bool ok = true;
+                for (int32_t i : rows) {
+                    char &f = seen[(size_t)(u.pos[i] - b.pos_min)];
+                    ok = ok && !f;
+                    f = 1;
+                }
+                b.contig = ok ? 1 : 0;
+            }
             (prefill ? pf : dec).push_back(b);
             (prefill ? pf_rows : dec_rows).push_back(rows);
         }

@@ -46,6 +46,7 @@ struct DevBlock {
     int32_t pos_max;
     int32_t tok0;    // first ubatch row when the block's rows are consecutive ubatch rows in
                      // order (perm[row0 + i] == tok0 + i), else -1
+    int32_t contig;  // 1: the rows' positions are pos_min .. pos_max, each once (in any order)
 };
 
 // Host-side per-ubatch tables (filled at split / prepare time).

@@ -34,6 +34,13 @@ __device__ __forceinline__ int32_t rows_seeing(const kvk::UbView &u, const kvi::
     if (kvd::pos_visible(u.causal, u.n_swa, b.pos_min, cpos) && kvd::pos_visible(u.causal, u.n_swa, b.pos_max, cpos))
         return b.n_rows;
     if ((u.causal && cpos > b.pos_max) || (u.n_swa > 0 && (int64_t)b.pos_min - cpos >= u.n_swa)) return 0;
+    if (b.contig) {
+        // the seeing positions cpos .. cpos + n_swa - 1 (each end open without causality
+        // or window) against the block's pos_min .. pos_max, each held by one row
+        const int64_t lo = u.causal ? max((int64_t)b.pos_min, (int64_t)cpos) : (int64_t)b.pos_min;
+        const int64_t hi = u.n_swa > 0 ? min((int64_t)b.pos_max, (int64_t)cpos + u.n_swa - 1) : (int64_t)b.pos_max;
+        return hi >= lo ? (int32_t)(hi - lo + 1) : 0;
+    }
     int32_t n = 0;
     for (int32_t k = 0; k < b.n_rows; ++k)
         n += kvd::pos_visible(u.causal, u.n_swa, u.rows[u.perm[b.row0 + k]].pos, cpos) ? 1 : 0;
