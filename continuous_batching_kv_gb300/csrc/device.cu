@@ -294,7 +294,7 @@ int device_init(kv_cache *c) {
         (e = dev_alloc(d, &p.cta_item0, (size_t)d->gx_dec + d->gx_pf + 2)) != cudaSuccess ||
         (e = dev_alloc(d, &p.pf_rows, (size_t)d->gx_pf * PF_M)) != cudaSuccess ||
         (e = dev_alloc(d, &p.pf_first, (size_t)d->gx_pf * 4)) != cudaSuccess ||
-        (e = dev_alloc(d, &p.dec_first, (size_t)d->gx_dec * 4)) != cudaSuccess ||
+        (e = dev_alloc(d, &p.dec_first, (size_t)d->gx_dec * kvk::DEC_FIRST)) != cudaSuccess ||
         (e = dev_alloc(d, &d->d_part_dec, (size_t)p.cap_dec * hkv * DEC_PART_FLOATS)) != cudaSuccess ||
         (e = dev_alloc(d, &d->d_part_pf, (size_t)p.cap_pf * hkv * PF_PART_FLOATS)) != cudaSuccess ||
         (e = dev_alloc(d, &d->d_err, 1)) != cudaSuccess)

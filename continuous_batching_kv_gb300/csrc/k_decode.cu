@@ -193,11 +193,16 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         bool dep_done = false;
         bool ok = true;
         uint32_t qh = 0, qt = 0;   // group queue head and tail (ring indices)
+        // the column's start record: the first window's entries without the chain
+        // item -> block -> list -> flags
+        const int4 *rp = reinterpret_cast<const int4 *>(a.p.dec_first + kvk::DEC_FIRST * blockIdx.x);
+        const int4 r_t = rp[0], r_fl = rp[1], r_w = rp[2], r_b = rp[3];
         // warm L2 with the column's first four tiles (K and V, both d halves; a
         // prefetch returns nothing) while the previous kernel may still be storing
         if (lane < 16) {
-            const int32_t y = a.p.dec_first[4 * blockIdx.x + (lane >> 2)];
-            if (y >= 0) kvd::tma_prefetch_2d((lane & 2) ? &tm_v : &tm_k, hk * 128 + 64 * (lane & 1), y);
+            const int32_t h = lane >> 2;
+            const int32_t t = h == 0 ? r_t.x : h == 1 ? r_t.y : h == 2 ? r_t.z : r_t.w;
+            if (t >= 0) kvd::tma_prefetch_2d((lane & 2) ? &tm_v : &tm_k, hk * 128 + 64 * (lane & 1), r_w.w + t * TILE);
         }
         // wait outcomes and the loop conditions are agreed by the whole warp, so a
         // failure never splits it in front of __syncwarp
@@ -212,21 +217,40 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             return true;
         };
         for (int32_t wi = i0; wi < i1 && ok; ++wi) {
-            const kvk::WorkItem w = a.p.work[wi];
-            const kvi::DevBlock b = a.u.blocks[w.block];
+            const bool first = wi == i0;
+            kvk::WorkItem w;
+            int32_t ybase, n_rows, seq0;
+            if (first) {   // from the start record
+                w.block = r_w.x;
+                w.t0 = r_w.y;
+                w.t1 = r_w.z;
+                ybase = r_w.w;
+                n_rows = r_b.x;
+                seq0 = r_b.y;
+            } else {
+                w = a.p.work[wi];
+                const kvi::DevBlock b = a.u.blocks[w.block];
+                ybase = b.stream * a.u.kv_size;
+                n_rows = b.n_rows;
+                seq0 = b.seq0;
+            }
             const int32_t *list = a.p.tiles + (int64_t)w.block * a.p.tile_stride;
             const uint32_t *flg = a.p.flags + (int64_t)w.block * a.p.tile_stride;
-            const int32_t ybase = b.stream * a.u.kv_size;
             const int32_t xk = hk * 128;
             for (int32_t base = w.t0; base < w.t1 && ok; base += WINDOW) {
                 const int32_t li = base + lane;
                 int32_t t = 0;
                 uint32_t fl = 0;
                 if (li < w.t1) {
-                    t = list[li];
-                    fl = flg[t];
+                    if (first && base == w.t0 && lane < 4) {
+                        t = lane == 0 ? r_t.x : lane == 1 ? r_t.y : lane == 2 ? r_t.z : r_t.w;
+                        fl = (uint32_t)(lane == 0 ? r_fl.x : lane == 1 ? r_fl.y : lane == 2 ? r_fl.z : r_fl.w);
+                    } else {
+                        t = list[li];
+                        fl = flg[t];
+                    }
                 }
-                const bool isfull = li < w.t1 && (int32_t)(fl & 0xffffu) == b.n_rows * TILE;
+                const bool isfull = li < w.t1 && (int32_t)(fl & 0xffffu) == n_rows * TILE;
                 uint32_t fm = __ballot_sync(0xffffffffu, isfull);
                 // queue the visible groups of my tile (flags bits 16..23), in list order
                 uint32_t gm = (li < w.t1 && !isfull) ? ((fl >> 16) & 0xffu) : 0u;
@@ -284,8 +308,8 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                             const int32_t j = x.gq[(qh + (uint32_t)(l >> 3)) & (GQ - 1)] + (l & 7);
                             if (j < a.u.n_kv) {
                                 const int64_t g = (int64_t)ybase + j;
-                                const uint64_t wb = a.u.cell_bits[g * a.u.n_words + (b.seq0 >> 6)];
-                                hs[r] = ((wb >> (b.seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
+                                const uint64_t wb = a.u.cell_bits[g * a.u.n_words + (seq0 >> 6)];
+                                hs[r] = ((wb >> (seq0 & 63)) & 1ull) && a.u.cell_epoch[g] <= a.u.ub_epoch;
                                 cp[r] = a.u.cell_pos[g];
                             }
                         }

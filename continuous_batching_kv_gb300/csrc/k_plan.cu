@@ -608,17 +608,30 @@ __global__ void __launch_bounds__(1024) k_plan_work(kvk::UbView u, kvk::Plan p, 
         __syncthreads();   // items written by other threads are visible below
         fill_cta0(p.work + item_base, n_items, gx, cta0);
         __syncthreads();
-        // each column's first four listed tiles, as TMA rows
+        // each column's start record (see Plan::dec_first)
         for (int32_t x = tid; x < (int32_t)gx; x += blockDim.x) {
-            int32_t f[4] = {-1, -1, -1, -1};
-            int32_t nf = 0;
-            for (int32_t i = cta0[x]; i < cta0[x + 1] && nf < 4; ++i) {
-                const kvk::WorkItem w = p.work[item_base + i];
+            int32_t f[kvk::DEC_FIRST];
+            for (int h = 0; h < kvk::DEC_FIRST; ++h) f[h] = -1;
+            if (cta0[x] < cta0[x + 1]) {
+                const kvk::WorkItem w = p.work[item_base + cta0[x]];
                 const kvi::DevBlock b = u.blocks[w.block];
                 const int32_t *list = p.tiles + (int64_t)w.block * p.tile_stride;
-                for (int32_t t = w.t0; t < w.t1 && nf < 4; ++t) f[nf++] = b.stream * u.kv_size + list[t] * TILE;
+                const uint32_t *flg = p.flags + (int64_t)w.block * p.tile_stride;
+                for (int h = 0; h < 4; ++h) {
+                    const int32_t e = w.t0 + h;
+                    if (e < w.t1) {
+                        f[h] = list[e];
+                        f[4 + h] = (int32_t)flg[f[h]];
+                    }
+                }
+                f[8] = w.block;
+                f[9] = w.t0;
+                f[10] = w.t1;
+                f[11] = b.stream * u.kv_size;
+                f[12] = b.n_rows;
+                f[13] = b.seq0;
             }
-            for (int h = 0; h < 4; ++h) p.dec_first[4 * x + h] = f[h];
+            for (int h = 0; h < kvk::DEC_FIRST; ++h) p.dec_first[kvk::DEC_FIRST * x + h] = f[h];
         }
         __syncthreads();
     }

@@ -44,6 +44,8 @@ struct UbView {
 };
 
 // Attention plan buffers (library-owned device memory).
+constexpr int32_t DEC_FIRST = 16;   // ints per decode start record (see Plan::dec_first)
+
 struct Plan {
     uint32_t *flags;        // [max_blocks][tile_stride]: bits 0..15 visible (row, cell)
                             // pairs in the 64-cell tile, bits 16..23 which 8-cell groups
@@ -64,8 +66,11 @@ struct Plan {
                             // chain item -> block -> row permutation
     int32_t *pf_first;      // [gx_pf][4]: each prefill CTA column's first pair: TMA rows of its two
                             // tiles (-TILE: no second tile), 1 if fully visible; [0] < 0: none
-    int32_t *dec_first;     // [gx_dec][4]: the TMA rows of each decode CTA column's first four listed
-                            // tiles (-1: fewer), warmed into L2 before the kernel waits for the store
+    int32_t *dec_first;     // [gx_dec][DEC_FIRST]: each decode CTA column's start record, so that
+                            // its first window needs no dependent load: the first item's first
+                            // four list entries (tile, -1 past the item) and their flags, its
+                            // block, t0, t1, the block's first cache row (stream * kv_size), row
+                            // count and first sequence id; block -1: no item
     int32_t *err;
     int32_t tile_stride;
     int32_t cap_dec, cap_pf;
