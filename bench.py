@@ -92,7 +92,7 @@ def load_peaks():
 # from an ncu capture of the current kernel (profiles/k_decode_llama8b-decode-256seq-
 # lognormal.md; a launch at decode step 2, 3.521 GB algorithmic).  Cleared to nothing
 # whenever the kernel changes until it is captured again.
-DECODE_TRAFFIC = {5: 3557391872}
+DECODE_TRAFFIC = {5: 3556978688}
 # One k_prefill launch of the 5000-token prefill captured by ncu (profiles/k_prefill_
 # qwen-prefill-5000-b2048-ub512.md: ubatch 5, layer 5): its DRAM bytes (read + write)
 # and its algorithmic bytes.  The launches of a step differ in size, so the reported
