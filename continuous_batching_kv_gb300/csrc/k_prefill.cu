@@ -601,8 +601,10 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                 for (int32_t j = 0; j < it.steps && ok; ++j) {
                     const int32_t gs = g + j;
                     const bool more = j + 1 < it.steps;
-                    if (!(ok = wait_all(&x.p_full[0], (n_t[0] + (uint32_t)j) & 1u))) break;
+                    // V of the step (loaded a step ahead) first, so that only tile A's P
+                    // stands between its softmax and PV_A
                     if (!(ok = wait_all(&x.v_full[gs % VSTAGES], (uint32_t)(gs / VSTAGES) & 1u))) break;
+                    if (!(ok = wait_all(&x.p_full[0], (n_t[0] + (uint32_t)j) & 1u))) break;
                     tc::fence_after();
                     const uint64_t vb0 = dv + (uint64_t)(((gs % VSTAGES) * TILEB) >> 4);
                     const uint64_t kb1 = dk + (uint64_t)((((gs + 1) % KSTAGES) * TILEB) >> 4);
@@ -772,11 +774,14 @@ k_prefill(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUte
                             for (int c = 0; c < 128; ++c)
                                 sb[c] = ((vm[c >> 5] >> (c & 31)) & 1u) ? sb[c] : __float_as_uint(-INFINITY);
                         }
-                        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                        float mx[8];
 #pragma unroll
-                        for (int c = 0; c < 128; c += 2)
-                            mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(sb[c]), __uint_as_float(sb[c + 1]));
-                        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+                        for (int u = 0; u < 8; ++u) mx[u] = max3f(-INFINITY, __uint_as_float(sb[2 * u]), __uint_as_float(sb[2 * u + 1]));
+#pragma unroll
+                        for (int c = 16; c < 128; c += 2)
+                            mx[(c >> 1) & 7] = max3f(mx[(c >> 1) & 7], __uint_as_float(sb[c]), __uint_as_float(sb[c + 1]));
+                        const float tmax = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+                                           a.scale_log2;
                         const float m_new = fmaxf(m_run, tmax);
                         const bool grow = m_new > m_run + RESCALE_LOG2 || (m_run == -INFINITY && m_new != -INFINITY);
                         float alpha = 1.f;
