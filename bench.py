@@ -99,7 +99,7 @@ DECODE_TRAFFIC = {5: 3556978688}
 # traffic is this ratio times the timed launches' mean algorithmic bytes (DRAM traffic
 # grows with the K/V rows read; the O rows stay in L2 within a launch).  Cleared to
 # nothing whenever the kernel changes until it is captured again.
-PREFILL_TRAFFIC = {2: (14806016, 18874368)}
+PREFILL_TRAFFIC = {2: (14806272, 18874368)}
 
 DECODE_BOUND = {3: True, 5: True}
 
