@@ -13,7 +13,7 @@ The functions keep the C names:
     kv_split_ubatches, kv_split_count, kv_split_ubatch, kv_split_free,
     kv_prepare_cells, kv_seq_rm, kv_seq_cp, kv_seq_pos_max, kv_cells_read,
     kv_stream_n_kv, kv_store, ubatch_attention, ubatch_attention_static_scratch,
-    kv_device_error, kv_device_bytes, kv_launch_count,
+    kv_device_error, kv_selftest_wait, kv_device_bytes, kv_launch_count,
     kv_sched_init, kv_sched_free, kv_sched_submit, kv_sched_next, kv_sched_advance, kv_sched_stats
     (and kv_split_sched_batch: kv_split_ubatches of a scheduler batch)
 """
@@ -33,13 +33,14 @@ KV_E_ORDER, KV_E_STALE, KV_E_CUDA, KV_E_NOMEM, KV_E_NO_DEVICE = -5, -6, -7, -8, 
 KV_SPLIT_AUTO, KV_SPLIT_SIMPLE, KV_SPLIT_EQUAL, KV_SPLIT_SEQ = 0, 1, 2, 3
 KV_MAX_SEQ, KV_HEAD_DIM = 256, 128
 KV_STATIC_SCRATCH_BYTES = 24 << 20
+KV_DERR_TMA_TIMEOUT, KV_DERR_MMA_TIMEOUT, KV_DERR_BOUNDS, KV_DERR_TMEM, KV_DERR_SELFTEST = 1, 2, 3, 4, 5
 
 EXPORTS = [
     "kv_init", "kv_free", "kv_n_batch", "kv_n_ubatch", "kv_kv_size", "kv_last_error",
     "kv_split_ubatches", "kv_split_count", "kv_split_ubatch", "kv_split_free",
     "kv_prepare_cells", "kv_seq_rm", "kv_seq_cp", "kv_seq_pos_max", "kv_cells_read", "kv_stream_n_kv",
     "kv_store", "ubatch_attention", "ubatch_attention_static_scratch", "kv_device_error",
-    "kv_device_bytes", "kv_launch_count",
+    "kv_selftest_wait", "kv_device_bytes", "kv_launch_count",
     "kv_sched_init", "kv_sched_free", "kv_sched_submit", "kv_sched_next", "kv_sched_advance",
     "kv_sched_stats",
 ]
@@ -113,6 +114,7 @@ def _load():
         "ubatch_attention": (C.c_int, [P, P, C.c_int32, C.c_int32, P, P, P, P]),
         "ubatch_attention_static_scratch": (C.c_int, [P, P, C.c_int32, C.c_int32, P, P, P, P]),
         "kv_device_error": (C.c_int, [P]),
+        "kv_selftest_wait": (C.c_int, [P, P]),
         "kv_device_bytes": (C.c_size_t, [P]),
         "kv_launch_count": (C.c_uint64, [P]),
         "kv_sched_init": (C.c_int, [P, C.POINTER(kv_sched_params), C.POINTER(P)]),
@@ -376,6 +378,12 @@ def ubatch_attention_static_scratch(c, s, ub, layer, q, o, mask_out=None, stream
 
 def kv_device_error(c):
     return _check(c, lib.kv_device_error(c))
+
+
+def kv_selftest_wait(c, stream=None):
+    """Launch one wait that nothing completes; it gives up after the kernels'
+    wait limit (~1 s) and sets the device error word to KV_DERR_SELFTEST."""
+    return _check(c, lib.kv_selftest_wait(c, _stream(stream)))
 
 
 def kv_device_bytes(c):

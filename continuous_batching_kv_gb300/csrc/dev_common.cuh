@@ -18,6 +18,7 @@ enum : int32_t {
     DERR_MMA_TIMEOUT = 2,     // an mbarrier wait for a tensor-core commit gave up
     DERR_BOUNDS = 3,          // an index check failed
     DERR_TMEM = 4,            // TMEM allocation returned an unusable address
+    DERR_SELFTEST = 5,        // the wait self-test's wait gave up (as it must)
 };
 
 // A bounded wait gives up after this many SM clock cycles (~1 s at 2 GHz).

@@ -503,6 +503,16 @@ int kv_device_error(kv_cache *c) {
     return v;
 }
 
+int kv_selftest_wait(kv_cache *c, void *stream) {
+    if (!c || !c->has_device) return KV_E_INVAL;
+    return guarded(c, [&]() -> int {
+        cudaError_t e = kvk::launch_wait_selftest(c->dev->d_err, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(c, e, "wait self-test launch");
+        c->launches += 1;
+        return KV_OK;
+    });
+}
+
 size_t kv_device_bytes(const kv_cache *c) { return (c && c->dev) ? c->dev->bytes : 0; }
 
 uint64_t kv_launch_count(const kv_cache *c) { return c ? c->launches : 0; }

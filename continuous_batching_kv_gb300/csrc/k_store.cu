@@ -72,9 +72,26 @@ __global__ void k_apply_deltas(const kvi::Delta *__restrict__ d, int32_t n, int3
     for (int32_t w = 0; w < n_words; ++w) bits[(int64_t)r.cell * n_words + w] = r.bits[w];
 }
 
+// The bounded-wait path, exercised: one thread waits on an mbarrier that nothing
+// arrives at, with the limit every wait of the attention kernels uses; when the
+// wait gives up (after ~1 s), the error word is set, as a kernel whose copy or
+// commit never came would set it, and the kernel returns normally.
+__global__ void k_wait_selftest(int32_t *err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    kvd::mbar_init(&bar, 1);
+    kvd::fence_mbar_init();
+    if (!kvd::mbar_wait_bounded(&bar, 0)) kvd::report(err, kvd::DERR_SELFTEST);
+}
+
 }  // namespace
 
 namespace kvk {
+
+cudaError_t launch_wait_selftest(int32_t *err, cudaStream_t st) {
+    k_wait_selftest<<<1, 32, 0, st>>>(err);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_store(void *k_cache, void *v_cache, const void *k_cur, const void *v_cur,
                          const kvi::DevRow *rows, int32_t n_tokens, int32_t row_bytes,

@@ -88,6 +88,8 @@ cudaError_t launch_store(void *k_cache, void *v_cache, const void *k_cur, const 
 cudaError_t launch_upload(const void *src, void *dst, size_t bytes, int32_t n_sm, cudaStream_t st);
 cudaError_t launch_apply_deltas(const kvi::Delta *d, int32_t n, int32_t n_words, int32_t *pos,
                                 uint32_t *epoch, uint64_t *bits, cudaStream_t st);
+// one wait that runs out (~1 s), reported to err as DERR_SELFTEST
+cudaError_t launch_wait_selftest(int32_t *err, cudaStream_t st);
 
 // Per device, at cache creation (the device current): load every kernel's
 // module and set the attributes launches rely on, so that later calls obtain

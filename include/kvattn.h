@@ -338,12 +338,33 @@ int ubatch_attention(kv_cache *c, const kv_split *s, int32_t ub, int32_t layer,
 int ubatch_attention_static_scratch(kv_cache *c, const kv_split *s, int32_t ub, int32_t layer,
                                     const void *q, float *o, void *mask_out, void *stream);
 
+/* Device error codes (the first one a kernel reported since the word was last read). */
+#define KV_DERR_TMA_TIMEOUT 1 /* a bounded wait for a TMA copy gave up */
+#define KV_DERR_MMA_TIMEOUT 2 /* a bounded wait for a tensor-core commit gave up */
+#define KV_DERR_BOUNDS      3 /* an index or layout check failed */
+#define KV_DERR_TMEM        4 /* tensor memory allocation returned an unusable address */
+#define KV_DERR_SELFTEST    5 /* kv_selftest_wait's wait gave up, as it must */
+
 /*
  * kv_device_error -- synchronise the cache's device work and return the
- * device error word: 0 if no kernel reported a fault, else a nonzero code
- * (a bounded wait gave up or an index check failed); clears it.
+ * device error word: 0 if no kernel reported a fault, else one of the
+ * KV_DERR_* codes (a bounded wait gave up or an index check failed); clears it.
  */
 int kv_device_error(kv_cache *c);
+
+/*
+ * kv_selftest_wait -- the failure path of the kernels' bounded waits, run on
+ * purpose: launches one thread on the cache's device (on `stream`, a
+ * cudaStream_t, NULL = the legacy default stream) that waits on a shared-memory
+ * barrier nothing completes, with the same limit as every wait of the attention
+ * kernels (2e9 SM cycles, about 1 s); when the wait gives up, the thread writes
+ * KV_DERR_SELFTEST to the device error word and returns.  No memory is touched
+ * but that word; the device stays usable.  Returns KV_OK once launched (the
+ * word reads nonzero from kv_device_error after the kernel ends), KV_E_INVAL
+ * for a host-only cache.  A fault-free stand-in for a copy or a commit that
+ * never arrives.
+ */
+int kv_selftest_wait(kv_cache *c, void *stream);
 
 /* Bytes of device memory the library allocated for this cache (cell mirror,
  * tables, plan, split-K scratch).  Not counted: the fixed

@@ -273,6 +273,35 @@ def test_device_call_errors():
     kv.kv_free(c)
 
 
+def test_bounded_wait_gives_up_reports_and_the_next_calls_are_clean():
+    # a wait that nothing completes runs to the kernels' limit, the error word says
+    # so (and is cleared by reading it), and later attention calls on the same cache
+    # still match the oracle
+    import time
+    import torch
+    import continuous_batching_kv_gb300 as kv
+    cfg = configs.config(1)
+    p = Pair(cfg)
+    try:
+        for call in cfg["setup"]:
+            p.run_call(call, attend=False)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        kv.kv_selftest_wait(p.c)
+        torch.cuda.synchronize()
+        waited = time.perf_counter() - t0
+        assert kv.kv_device_error(p.c) == kv.KV_DERR_SELFTEST
+        assert kv.kv_device_error(p.c) == 0
+        assert waited > 0.2, "the wait gave up after %.3f s, before its limit" % waited
+        stats = []
+        for call in cfg["measured"]:
+            st, _ = p.run_call(call, attend=True, check_mask=True)
+            stats += st
+        assert len(stats) == 5
+    finally:
+        p.close()
+
+
 @pytest.mark.parametrize("fixed", [False, True])
 def test_batching_loop_through_scheduler(fixed):
     # ITER, "The loop that replaces the batch": the native scheduler retires,
