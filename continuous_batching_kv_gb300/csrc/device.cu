@@ -53,8 +53,18 @@ struct DeviceState {
     // one TMA descriptor per K / V tensor
     std::vector<CUtensorMap> tm_k, tm_v;
     std::vector<CUtensorMap> tm_dec;   // per layer: K, V with 64-row boxes, K, V with 8-row boxes
-    uint64_t plan_split = 0;
-    int32_t plan_ub = -1;
+    // Two sets of plan arrays (plan, plan2).  While a split's ubatch runs its layers, the
+    // plan of its next ubatch is built into the other set on a side stream, ordered
+    // after everything the caller's stream had been given; the ubatch's first call then
+    // has its stream wait for that build instead of running the plan kernels itself.
+    kvk::Plan plan2{};
+    uint64_t pb_split[2] = {0, 0};      // (split, ubatch) each set holds; split 0: none
+    int32_t pb_ub[2] = {-1, -1};
+    bool pb_pending[2] = {false, false};   // built on the side stream, not yet waited for
+    cudaEvent_t pb_ready[2] = {nullptr, nullptr};
+    cudaEvent_t call_ev = nullptr;      // the caller's stream, when a look-ahead build starts
+    cudaStream_t side = nullptr;
+    int32_t pb_cur = 0;                 // the set the last attention call used
     size_t bytes = 0;
     std::vector<void *> allocs;
 };
@@ -160,6 +170,12 @@ int sync_device(kv_cache *c, const kv_split *sp, cudaStream_t st) {
     const bool need_tables = c->dev_tables_split != sp->id;
     if (!c->pending_reset && c->pending.empty() && !need_tables) return KV_OK;
     cudaError_t e;
+    // a look-ahead plan build reads the mirror and the tables: the uploads wait for it
+    for (int i = 0; i < 2; ++i) {
+        if (!d->pb_pending[i]) continue;
+        if ((e = cudaStreamWaitEvent(st, d->pb_ready[i], 0)) != cudaSuccess) return cuda_fail(c, e, "plan wait");
+        d->pb_pending[i] = false;
+    }
     const int sl = d->stage_slot;
     if (d->stage_pending[sl]) {   // this staging buffer is reused: wait for its last copy
         e = cudaEventSynchronize(d->stage_ev[sl]);
@@ -203,14 +219,85 @@ int sync_device(kv_cache *c, const kv_split *sp, cudaStream_t st) {
             return cuda_fail(c, e, "table upload");
         c->launches += 1;
         c->dev_tables_split = sp->id;
-        d->plan_split = 0;
-        d->plan_ub = -1;
+        for (int i = 0; i < 2; ++i) {
+            d->pb_split[i] = 0;
+            d->pb_ub[i] = -1;
+        }
     }
     if ((e = cudaEventRecord(d->stage_ev[sl], st)) != cudaSuccess) return cuda_fail(c, e, "stage record");
     d->stage_pending[sl] = true;
     d->stage_slot = sl ^ 1;
     for (const Delta &r : c->pending) c->pending_idx[r.cell] = -1;
     c->pending.clear();
+    return KV_OK;
+}
+
+kvk::Plan &plan_set(DeviceState *d, int i) { return i == 0 ? d->plan : d->plan2; }
+
+// The plan set holding (split, ubatch) for a call on stream st: one built ahead on the
+// side stream (st then waits for that build), one built before, or else one built now
+// on st into the set the last call used (the other may hold a look-ahead build).
+// fresh: the plan was not complete before this call's first kernel was issued.
+// Returns the set, or -1 with rc set.
+int plan_for(kv_cache *c, const kv_split *sp, int32_t ub, cudaStream_t st, bool &fresh, int &rc) {
+    DeviceState *d = c->dev;
+    fresh = false;
+    rc = KV_OK;
+    cudaError_t e;
+    for (int i = 0; i < 2; ++i) {
+        if (d->pb_split[i] != sp->id || d->pb_ub[i] != ub) continue;
+        if (d->pb_pending[i]) {
+            if ((e = cudaStreamWaitEvent(st, d->pb_ready[i], 0)) != cudaSuccess) {
+                rc = cuda_fail(c, e, "plan wait");
+                return -1;
+            }
+            d->pb_pending[i] = false;
+            fresh = true;
+        }
+        d->pb_cur = i;
+        return i;
+    }
+    int i = d->pb_cur;
+    if (d->pb_pending[i]) i ^= 1;   // the set a look-ahead build is writing is left alone
+    if ((e = kvk::launch_plan(make_view(c, sp, ub), plan_set(d, i), c->prm.n_stream, d->gx_dec, d->gx_pf, st)) !=
+        cudaSuccess) {
+        d->pb_split[i] = 0;
+        d->pb_ub[i] = -1;
+        rc = cuda_fail(c, e, "plan launch");
+        return -1;
+    }
+    c->launches += 3;
+    d->pb_split[i] = sp->id;
+    d->pb_ub[i] = ub;
+    d->pb_pending[i] = false;
+    d->pb_cur = i;
+    fresh = true;
+    return i;
+}
+
+// Build the plan of (split, ubatch) ahead on the side stream, into the set the current
+// call does not use, after everything already issued on st (which may still read that
+// set).  Not while st is being captured into a graph: the side stream's work would be
+// left outside the capture's joins.
+int plan_ahead(kv_cache *c, const kv_split *sp, int32_t ub, cudaStream_t st) {
+    DeviceState *d = c->dev;
+    const int i = d->pb_cur ^ 1;
+    if (d->pb_split[i] == sp->id && d->pb_ub[i] == ub) return KV_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return cuda_fail(c, e, "capture query");
+    if (cs != cudaStreamCaptureStatusNone) return KV_OK;
+    d->pb_split[i] = 0;   // holds nothing usable until the build is issued
+    d->pb_ub[i] = -1;
+    if ((e = cudaEventRecord(d->call_ev, st)) != cudaSuccess || (e = cudaStreamWaitEvent(d->side, d->call_ev, 0)) != cudaSuccess ||
+        (e = kvk::launch_plan(make_view(c, sp, ub), plan_set(d, i), c->prm.n_stream, d->gx_dec, d->gx_pf, d->side)) !=
+            cudaSuccess ||
+        (e = cudaEventRecord(d->pb_ready[i], d->side)) != cudaSuccess)
+        return cuda_fail(c, e, "look-ahead plan");
+    c->launches += 3;
+    d->pb_split[i] = sp->id;
+    d->pb_ub[i] = ub;
+    d->pb_pending[i] = true;
     return KV_OK;
 }
 
@@ -301,6 +388,27 @@ int device_init(kv_cache *c) {
         return cuda_fail(c, e, "plan alloc");
     p.err = d->d_err;
     p.gqa = c->gqa;
+    {
+        kvk::Plan &q = d->plan2;
+        q = p;   // shared: the split-K counters, the error word and the sizes
+        if ((e = dev_alloc(d, &q.flags, fl)) != cudaSuccess || (e = dev_alloc(d, &q.tiles, fl)) != cudaSuccess ||
+            (e = dev_alloc(d, &q.cum, fl)) != cudaSuccess || (e = dev_alloc(d, &q.wcount, d->max_blocks)) != cudaSuccess ||
+            (e = dev_alloc(d, &q.counts, d->max_blocks)) != cudaSuccess ||
+            (e = dev_alloc(d, &q.work, (size_t)q.cap_dec + q.cap_pf)) != cudaSuccess ||
+            (e = dev_alloc(d, &q.n_work, 2)) != cudaSuccess ||
+            (e = dev_alloc(d, &q.blk_item0, d->max_blocks)) != cudaSuccess ||
+            (e = dev_alloc(d, &q.blk_nitems, d->max_blocks)) != cudaSuccess ||
+            (e = dev_alloc(d, &q.cta_item0, (size_t)d->gx_dec + d->gx_pf + 2)) != cudaSuccess ||
+            (e = dev_alloc(d, &q.pf_rows, (size_t)d->gx_pf * PF_M)) != cudaSuccess ||
+            (e = dev_alloc(d, &q.pf_first, (size_t)d->gx_pf * 4)) != cudaSuccess ||
+            (e = dev_alloc(d, &q.dec_first, (size_t)d->gx_dec * kvk::DEC_FIRST)) != cudaSuccess)
+            return cuda_fail(c, e, "plan alloc");
+        if ((e = cudaStreamCreateWithFlags(&d->side, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&d->call_ev, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&d->pb_ready[0], cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&d->pb_ready[1], cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(c, e, "plan stream");
+    }
     d->pf_part_rows = (int64_t)p.cap_pf * hkv * PF_M;
     {
         auto enc = get_encode();
@@ -336,6 +444,7 @@ int device_init(kv_cache *c) {
         return cuda_fail(c, e, "kernel load");
     // no cluster launch where no cluster of attention CTAs can be resident
     if (d->plan.pf_cluster > 1 && kvk::prefill_max_active_clusters(d->plan.pf_cluster) < 1) d->plan.pf_cluster = 1;
+    d->plan2.pf_cluster = d->plan.pf_cluster;
     // The static-scratch array's address on this device (the current one).  With
     // lazy module loading this lookup is what loads the module and backs the array,
     // so it happens here, where memory is obtained anyway, and not during a call
@@ -355,7 +464,12 @@ void device_free(kv_cache *c) {
     if (!d) return;
     for (int sl = 0; sl < 2; ++sl)
         if (d->stage_pending[sl] && d->stage_ev[sl]) cudaEventSynchronize(d->stage_ev[sl]);
+    if (d->side) cudaStreamSynchronize(d->side);
     for (void *p : d->allocs) cudaFree(p);
+    for (int i = 0; i < 2; ++i)
+        if (d->pb_ready[i]) cudaEventDestroy(d->pb_ready[i]);
+    if (d->call_ev) cudaEventDestroy(d->call_ev);
+    if (d->side) cudaStreamDestroy(d->side);
     for (int sl = 0; sl < 2; ++sl) {
         if (d->h_stage[sl]) cudaFreeHost(d->h_stage[sl]);
         if (d->stage_ev[sl]) cudaEventDestroy(d->stage_ev[sl]);
@@ -409,15 +523,11 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
         const UbatchHost &u = sp->ub[ub];
         kvk::UbView v = make_view(c, sp, ub);
         cudaError_t e;
-        if (d->plan_split != sp->id || d->plan_ub != ub) {
-            early_ok = false;
-            kvk::Plan p = d->plan;
-            if ((e = kvk::launch_plan(v, p, c->prm.n_stream, d->gx_dec, d->gx_pf, st)) != cudaSuccess)
-                return cuda_fail(c, e, "plan launch");
-            c->launches += 3;
-            d->plan_split = sp->id;
-            d->plan_ub = ub;
-        }
+        bool fresh = false;
+        const int pi = plan_for(c, sp, ub, st, fresh, rc);
+        if (pi < 0) return rc;
+        if (fresh) early_ok = false;
+        const kvk::Plan &plan = plan_set(d, pi);
         if (mask_out) {
             if ((e = kvk::launch_mask(v, static_cast<uint16_t *>(mask_out), st)) != cudaSuccess)
                 return cuda_fail(c, e, "mask launch");
@@ -427,7 +537,7 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
         if (u.n_dec_blocks > 0) {
             kvk::DecodeArgs a{};
             a.u = v;
-            a.p = d->plan;
+            a.p = plan;
             a.q = static_cast<const __half *>(q);
             a.o = o;
             a.part = d->d_part_dec;
@@ -445,7 +555,7 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
         if (u.n_pf_blocks > 0) {
             kvk::PrefillArgs a{};
             a.u = v;
-            a.p = d->plan;
+            a.p = plan;
             a.q = static_cast<const __half *>(q);
             a.o = o;
             a.part = d->d_part_pf;
@@ -457,7 +567,7 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
             a.scale_log2 = scale_log2;
             a.err = d->d_err;
             a.early_ok = early_ok ? 1 : 0;
-            a.cluster = d->plan.pf_cluster;
+            a.cluster = plan.pf_cluster;
             // Q as a (d, head, token) tensor: a GQA group's query vectors of 128 / gqa
             // consecutive rows are one (64, gqa, 128 / gqa) box per 64-value d half; used
             // when every prefill block of the ubatch has consecutive rows
@@ -482,6 +592,8 @@ int ubatch_attention(kv_cache *c, const kv_split *sp, int32_t ub, int32_t layer,
                 return cuda_fail(c, e, "prefill launch");
             c->launches += 1;
         }
+        // the next ubatch of the split gets its plan while this one runs its layers
+        if (layer == 0 && ub + 1 < (int32_t)sp->ub.size()) return plan_ahead(c, sp, ub + 1, st);
         return KV_OK;
     });
 }
@@ -574,13 +686,9 @@ extern "C" int ubatch_attention_static_scratch(kv_cache *c, const kv_split *sp, 
         cudaStream_t st = static_cast<cudaStream_t>(stream);
         if ((rc = sync_device(c, sp, st)) != KV_OK) return rc;
         kvk::UbView v = make_view(c, sp, ub);
-        if (d->plan_split != sp->id || d->plan_ub != ub) {
-            if ((e = kvk::launch_plan(v, d->plan, c->prm.n_stream, d->gx_dec, d->gx_pf, st)) != cudaSuccess)
-                return cuda_fail(c, e, "plan launch");
-            c->launches += 3;
-            d->plan_split = sp->id;
-            d->plan_ub = ub;
-        }
+        bool fresh = false;
+        const int pi = plan_for(c, sp, ub, st, fresh, rc);
+        if (pi < 0) return rc;
         if (mask_out) {
             if ((e = kvk::launch_mask(v, static_cast<uint16_t *>(mask_out), st)) != cudaSuccess)
                 return cuda_fail(c, e, "mask launch");
@@ -591,7 +699,7 @@ extern "C" int ubatch_attention_static_scratch(kv_cache *c, const kv_split *sp, 
         if ((e = cudaMemsetAsync(counters, 0, cnt_bytes, st)) != cudaSuccess) return cuda_fail(c, e, "counter clear");
         kvk::DecodeArgs a{};
         a.u = v;
-        a.p = d->plan;
+        a.p = plan_set(d, pi);
         a.p.counters = counters;
         a.q = static_cast<const __half *>(q);
         a.o = o;

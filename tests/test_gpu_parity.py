@@ -273,6 +273,55 @@ def test_device_call_errors():
     kv.kv_free(c)
 
 
+def test_plans_built_ahead_unsynchronised_and_out_of_order():
+    # every ubatch's plan after the first is built ahead on the library's side stream
+    # while the previous ubatch runs; issue the calls back to back with no host
+    # synchronisation, then again in an order that leaves some look-ahead builds unused
+    # and misses others, and compare every output with the oracle
+    import torch
+    import continuous_batching_kv_gb300 as kv
+    cfg = configs.config(2, n_layer=2)
+    p = Pair(cfg)
+    try:
+        call = cfg["measured"][0]
+        s = kv.kv_split_ubatches(p.c, call["pos"], call["seq"])
+        assert kv.kv_prepare_cells(p.c, s) == 0
+        code, sp = p.o.split(call["pos"], call["seq"], keep_snapshots=True)
+        assert code == 0
+        nub = kv.kv_split_count(s)
+        assert nub >= 4
+        qs = {}
+        for k in range(nub):
+            u = kv.kv_split_ubatch(s, k)
+            rows = list(u["rows"])
+            pos = [call["pos"][r] for r in rows]
+            con = [call["content"][r] for r in rows]
+            for layer in range(p.L):
+                q, kk, vv = p.qkv(layer, pos, con)
+                kv.kv_store(p.c, s, k, layer, torch.from_numpy(kk).cuda(), torch.from_numpy(vv).cuda())
+                p.o.store(sp, k, layer, kk, vv)
+                qs[(k, layer)] = q.reshape(len(rows), p.H, p.d)
+        orders = [[(k, layer) for k in range(nub) for layer in range(p.L)],
+                  [(k, 0) for k in (1, 0, 3, 2)] + [(k, 1) for k in (0, 2, 1, 3)] + [(k, 0) for k in range(4, nub)]
+                  + [(k, 1) for k in range(4, nub)]]
+        # inputs and outputs on the device before the calls, so that nothing between
+        # them waits for the device
+        qd = {key: torch.from_numpy(q).cuda() for key, q in qs.items()}
+        for order in orders:
+            outs = {key: torch.empty(q.shape, dtype=torch.float32, device="cuda") for key, q in qs.items()}
+            torch.cuda.synchronize()
+            for k, layer in order:
+                kv.ubatch_attention(p.c, s, k, layer, qd[(k, layer)], outs[(k, layer)])
+            torch.cuda.synchronize()
+            assert kv.kv_device_error(p.c) == 0
+            for (k, layer), od in outs.items():
+                ref = p.o.attention(sp, k, layer, qs[(k, layer)])
+                check_close(od.cpu().numpy(), ref, "ubatch %d layer %d" % (k, layer))
+        kv.kv_split_free(s)
+    finally:
+        p.close()
+
+
 def test_bounded_wait_gives_up_reports_and_the_next_calls_are_clean():
     # a wait that nothing completes runs to the kernels' limit, the error word says
     # so (and is cleared by reading it), and later attention calls on the same cache
