@@ -19,6 +19,10 @@
  *   - Device pointers are plain CUDA device addresses on the current device;
  *     `stream` arguments are cudaStream_t values passed as void* (NULL = the
  *     legacy default stream).  All device work is asynchronous on `stream`.
+ *     A cache's device calls are ordered on one stream (the library keeps one
+ *     attention plan and its scratch per cache); besides, the library's own
+ *     side stream builds the next ubatch's plan ahead, ordered after the
+ *     caller's stream (see ubatch_attention).
  *   - The caller owns every buffer it passes in (K/V caches, q, k_cur, v_cur,
  *     o, mask_out).  The library owns kv_cache and kv_split handles and the
  *     device memory it allocates in kv_init (cell-metadata mirror, per-ubatch
@@ -297,6 +301,12 @@ int kv_store(kv_cache *c, const kv_split *s, int32_t ub, int32_t layer,
  *             0xFC00 (-inf) masked, column j = cell j of the row's stream
  * Requires kv_store(ub', layer) for every ub' <= ub of this split first
  * (KV_E_ORDER otherwise).  Errors: as kv_store.
+ * The call runs the plan kernels (the tile lists and the work split of the
+ * ubatch) unless the plan of (split, ub) is already on the device.  A layer-0
+ * call of ubatch ub also starts the plan of ubatch ub + 1 of the same split on
+ * a side stream of the cache, after everything issued on `stream` so far; the
+ * first call of ub + 1 then makes `stream` wait for it.  Not while `stream` is
+ * being captured into a CUDA graph.
  */
 int ubatch_attention(kv_cache *c, const kv_split *s, int32_t ub, int32_t layer,
                      const void *q, float *o, void *mask_out, void *stream);
