@@ -164,6 +164,16 @@ kvk::UbView make_view(const kv_cache *c, const kv_split *sp, int32_t ub) {
     return v;
 }
 
+// Order st after the look-ahead plan build into set i: a stream wait, or, while st is
+// being captured into a graph (which cannot wait for work outside it), a host wait.
+cudaError_t wait_build(DeviceState *d, int i, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return e;
+    if (cs != cudaStreamCaptureStatusNone) return cudaEventSynchronize(d->pb_ready[i]);
+    return cudaStreamWaitEvent(st, d->pb_ready[i], 0);
+}
+
 // Bring the device mirror and this split's tables up to date (stream-ordered).
 int sync_device(kv_cache *c, const kv_split *sp, cudaStream_t st) {
     DeviceState *d = c->dev;
@@ -173,7 +183,7 @@ int sync_device(kv_cache *c, const kv_split *sp, cudaStream_t st) {
     // a look-ahead plan build reads the mirror and the tables: the uploads wait for it
     for (int i = 0; i < 2; ++i) {
         if (!d->pb_pending[i]) continue;
-        if ((e = cudaStreamWaitEvent(st, d->pb_ready[i], 0)) != cudaSuccess) return cuda_fail(c, e, "plan wait");
+        if ((e = wait_build(d, i, st)) != cudaSuccess) return cuda_fail(c, e, "plan wait");
         d->pb_pending[i] = false;
     }
     const int sl = d->stage_slot;
@@ -247,7 +257,7 @@ int plan_for(kv_cache *c, const kv_split *sp, int32_t ub, cudaStream_t st, bool 
     for (int i = 0; i < 2; ++i) {
         if (d->pb_split[i] != sp->id || d->pb_ub[i] != ub) continue;
         if (d->pb_pending[i]) {
-            if ((e = cudaStreamWaitEvent(st, d->pb_ready[i], 0)) != cudaSuccess) {
+            if ((e = wait_build(d, i, st)) != cudaSuccess) {
                 rc = cuda_fail(c, e, "plan wait");
                 return -1;
             }
