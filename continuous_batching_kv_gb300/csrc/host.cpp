@@ -114,8 +114,18 @@ bool overlaps(const RowSet &a, const RowSet &b) {
 struct SplitIn {
     int32_t n;
     std::vector<int32_t> pos;
-    std::vector<std::vector<int32_t>> ids;   // first id first, as given
-    std::vector<RowSet> set;                 // sorted
+    std::vector<int32_t> ids;       // every row's ids, first id first, as given, row after row
+    std::vector<int32_t> ids_off;   // [n + 1]: row r's ids are ids[ids_off[r] .. ids_off[r + 1])
+    std::vector<RowSet> set;        // sorted, built only for the splits that compare sets
+    const int32_t *ids_of(int32_t r) const { return ids.data() + ids_off[r]; }
+    int32_t n_ids(int32_t r) const { return ids_off[r + 1] - ids_off[r]; }
+    void build_sets() {
+        set.resize(n);
+        for (int32_t r = 0; r < n; ++r) {
+            set[r].ids.assign(ids_of(r), ids_of(r) + n_ids(r));
+            std::sort(set[r].ids.begin(), set[r].ids.end());
+        }
+    }
 };
 
 void add_ubatch(kv_split *sp, const SplitIn &in, const std::vector<int32_t> &rows,
@@ -125,17 +135,23 @@ void add_ubatch(kv_split *sp, const SplitIn &in, const std::vector<int32_t> &row
     u.n_seq_tokens = n_seq_tokens;
     u.n_seqs = n_seqs;
     u.rows = rows;
-    std::set<int32_t> unq;
+    u.ids_off.reserve(rows.size() + 1);
+    u.pos.reserve(rows.size());
+    u.seq0.reserve(rows.size());
+    u.streams.reserve(rows.size());
     u.ids_off.push_back(0);
     for (int32_t r : rows) {
-        u.ids.insert(u.ids.end(), in.ids[r].begin(), in.ids[r].end());
+        const int32_t *ids = in.ids_of(r);
+        u.ids.insert(u.ids.end(), ids, ids + in.n_ids(r));
         u.ids_off.push_back((int32_t)u.ids.size());
         u.pos.push_back(in.pos[r]);
-        u.seq0.push_back(in.ids[r][0]);
-        u.streams.push_back(c->seq_to_stream[in.ids[r][0]]);
-        for (int32_t q : in.ids[r]) unq.insert(q);
+        u.seq0.push_back(ids[0]);
+        u.streams.push_back(c->seq_to_stream[ids[0]]);
     }
-    u.seq_unq.assign(unq.begin(), unq.end());
+    // the distinct ids, ascending
+    u.seq_unq = u.ids;
+    std::sort(u.seq_unq.begin(), u.seq_unq.end());
+    u.seq_unq.erase(std::unique(u.seq_unq.begin(), u.seq_unq.end()), u.seq_unq.end());
     sp->ub.push_back(std::move(u));
 }
 
@@ -453,33 +469,39 @@ int kv_split_ubatches(kv_cache *c, const kv_batch *b, int32_t mode, kv_split **o
         const int32_t nsm = c->prm.n_seq_max;
         SplitIn in;
         in.n = n;
-        in.ids.resize(n);
-        in.set.resize(n);
+        in.ids_off.resize((size_t)n + 1);
+        in.ids_off[0] = 0;
+        in.ids.reserve(n);
+        std::vector<int32_t> sorted;   // a row's ids, for the repeat check (rows of two or more)
         for (int32_t i = 0; i < n; ++i) {
-            std::vector<int32_t> &ids = in.ids[i];
+            const size_t at = in.ids.size();
             if (!b->seq_id) {
-                ids.push_back(0);
+                in.ids.push_back(0);
             } else if (!b->n_seq_id) {
                 if (!b->seq_id[i]) return c->set_err(KV_E_INVAL, "null seq_id row");
-                ids.push_back(b->seq_id[i][0]);
+                in.ids.push_back(b->seq_id[i][0]);
             } else {
                 int32_t k = b->n_seq_id[i];
                 if (k < 1 || k > nsm) return c->set_err(KV_E_INVAL, "bad n_seq_id");
                 if (!b->seq_id[i]) return c->set_err(KV_E_INVAL, "null seq_id row");
-                ids.assign(b->seq_id[i], b->seq_id[i] + k);
+                in.ids.insert(in.ids.end(), b->seq_id[i], b->seq_id[i] + k);
             }
-            for (int32_t q : ids)
-                if (q < 0 || q >= nsm) return c->set_err(KV_E_SEQ_RANGE, "sequence id out of range");
-            std::vector<int32_t> sorted = ids;
-            std::sort(sorted.begin(), sorted.end());
-            if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
-                return c->set_err(KV_E_INVAL, "repeated sequence id in one slot");
-            int32_t st = c->seq_to_stream[ids[0]];
-            for (int32_t q : ids)
-                if (c->seq_to_stream[q] != st)
+            const int32_t *ids = in.ids.data() + at;
+            const int32_t k = (int32_t)(in.ids.size() - at);
+            for (int32_t t = 0; t < k; ++t)
+                if (ids[t] < 0 || ids[t] >= nsm) return c->set_err(KV_E_SEQ_RANGE, "sequence id out of range");
+            if (k > 1) {
+                sorted.assign(ids, ids + k);
+                std::sort(sorted.begin(), sorted.end());
+                if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
+                    return c->set_err(KV_E_INVAL, "repeated sequence id in one slot");
+            }
+            const int32_t st = c->seq_to_stream[ids[0]];
+            for (int32_t t = 1; t < k; ++t)
+                if (c->seq_to_stream[ids[t]] != st)
                     return c->set_err(KV_E_CROSS_STREAM, "slot spans streams");
             if (b->pos && b->pos[i] < 0) return c->set_err(KV_E_INVAL, "negative position");
-            in.set[i].ids = std::move(sorted);
+            in.ids_off[i + 1] = (int32_t)in.ids.size();
         }
         in.pos.resize(n);
         if (b->pos) {
@@ -488,11 +510,12 @@ int kv_split_ubatches(kv_cache *c, const kv_batch *b, int32_t mode, kv_split **o
             // BATCH-ZH, Part A: a NULL pos is filled by counting up per sequence.
             std::map<int32_t, int32_t> last;   // sequence -> largest pos so far
             for (int32_t i = 0; i < n; ++i) {
-                int32_t q = in.ids[i][0];
+                int32_t q = in.ids_of(i)[0];
                 auto it = last.find(q);
                 int32_t best = it != last.end() ? it->second : seq_pos_max(c, q);
                 in.pos[i] = best + 1;
-                for (int32_t x : in.ids[i]) {
+                for (int32_t t = 0; t < in.n_ids(i); ++t) {
+                    const int32_t x = in.ids_of(i)[t];
                     auto jt = last.find(x);
                     int32_t prev = jt != last.end() ? jt->second : seq_pos_max(c, x);
                     last[x] = std::max(prev, in.pos[i]);
@@ -505,9 +528,13 @@ int kv_split_ubatches(kv_cache *c, const kv_batch *b, int32_t mode, kv_split **o
         sp->owner = c;
         sp->n_tokens = n;
         if (mode == KV_SPLIT_AUTO) mode = c->prm.n_stream == 1 ? KV_SPLIT_SIMPLE : KV_SPLIT_EQUAL;
-        if (mode == KV_SPLIT_SIMPLE) split_simple(sp, in, c->n_ubatch, c);
-        else if (mode == KV_SPLIT_EQUAL) split_equal(sp, in, c->n_ubatch, c);
-        else split_seq(sp, in, c->n_ubatch, c);
+        if (mode == KV_SPLIT_SIMPLE) {
+            split_simple(sp, in, c->n_ubatch, c);
+        } else {
+            in.build_sets();
+            if (mode == KV_SPLIT_EQUAL) split_equal(sp, in, c->n_ubatch, c);
+            else split_seq(sp, in, c->n_ubatch, c);
+        }
         *out = sp;
         return KV_OK;
     });
